@@ -1,0 +1,167 @@
+"""CPU oracle of the deterministic MoE layer (fp64) -- test infrastructure.
+
+Only the tests, the package smoke check and the benchmark's CPU-baseline leg may import
+this module. It loads `liboracle.so`, compiled from `oracle.c` with gcc, and wraps its
+functions for numpy arrays. It shares no code with the CUDA path.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SO = os.path.join(_HERE, "liboracle.so")
+_SRC = [os.path.join(_HERE, "oracle.c"), os.path.join(_HERE, "oracle.h")]
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so (plain C, OpenMP) if it is missing or older than its sources."""
+    stale = force or not os.path.exists(_SO) or any(
+        os.path.getmtime(s) > os.path.getmtime(_SO) for s in _SRC)
+    if stale:
+        tmp = _SO + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+                               "-o", tmp, _SRC[0], "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_SO)
+        i64, i32, p = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+        L.oracle_route.argtypes = [i64, i32, i32, p, p, p]
+        L.oracle_schedule.argtypes = [i64, i32, i64, p, p, p, p, p, p, i64, p]
+        L.oracle_schedule.restype = ctypes.c_int
+        L.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+        L.oracle_e4m3_encode.restype = ctypes.c_uint8
+        L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_decode.restype = ctypes.c_double
+        L.oracle_mxfp8_quantize.argtypes = [i64, i64, p, p, p]
+        L.oracle_mxfp8_dequantize.argtypes = [i64, i64, p, p, p]
+        L.oracle_forward.argtypes = [i64, i32, i32, i32, i32, p, p, p, p, p, i32, p]
+        L.oracle_backward.argtypes = [i64, i32, i32, i32, i32, p, p, p, p, p, p, p, p, p, p]
+        L.oracle_router_grad.argtypes = [i64, i32, i32, p, p, p, p]
+        _lib = L
+    return _lib
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _i32(a):
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (uint16) to float64."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+# ------------------------------------------------------------------------- steps
+
+def route(logits, K):
+    """Top-k routing: (idx int32 [T,K], w float64 [T,K])."""
+    lg = _f64(logits)
+    T, E = lg.shape
+    idx = np.empty((T, K), np.int32)
+    w = np.empty((T, K), np.float64)
+    lib().oracle_route(T, E, K, _p(lg), _p(idx), _p(w))
+    return idx, w
+
+
+def schedule(idx, E, MB, seg_cap=None):
+    """Stable expert schedule: dict of counts, offsets, perm, inv, segs [n,3]."""
+    f = _i32(idx).reshape(-1)
+    R = f.size
+    if seg_cap is None:
+        seg_cap = E + (R + MB - 1) // MB if R > 0 else 1
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    perm = np.empty(max(R, 1), np.int32)
+    inv = np.empty(max(R, 1), np.int32)
+    segs = np.empty((max(seg_cap, 1), 3), np.int32)
+    n = np.zeros(1, np.int32)
+    rc = lib().oracle_schedule(R, E, MB, _p(f), _p(counts), _p(offsets), _p(perm), _p(inv),
+                               _p(segs), seg_cap, _p(n))
+    if rc != 0:
+        raise ValueError("segment capacity exceeded")
+    return dict(counts=counts, offsets=offsets, perm=perm[:R], inv=inv[:R],
+                segs=segs[: int(n[0])].copy())
+
+
+def e4m3_encode(v: float) -> int:
+    return int(lib().oracle_e4m3_encode(float(v)))
+
+
+def e4m3_decode(code: int) -> float:
+    return float(lib().oracle_e4m3_decode(int(code)))
+
+
+def mxfp8_quantize(src):
+    """MXFP8 along the last axis: (q uint8 [rows,cols], scale uint8 [rows,cols/32])."""
+    s = _f64(src)
+    rows, cols = s.reshape(-1, s.shape[-1]).shape
+    assert cols % 32 == 0
+    q = np.empty((rows, cols), np.uint8)
+    sc = np.empty((rows, cols // 32), np.uint8)
+    lib().oracle_mxfp8_quantize(rows, cols, _p(s), _p(q), _p(sc))
+    return q.reshape(s.shape), sc.reshape(s.shape[:-1] + (cols // 32,))
+
+
+def mxfp8_dequantize(q, scale):
+    q = np.ascontiguousarray(q, np.uint8)
+    sc = np.ascontiguousarray(scale, np.uint8)
+    cols = q.shape[-1]
+    rows = q.size // cols
+    out = np.empty(q.shape, np.float64)
+    lib().oracle_mxfp8_dequantize(rows, cols, _p(q), _p(sc), _p(out))
+    return out
+
+
+def forward(x, idx, w, w13, w2, act_mxfp8=False):
+    """Layer forward in fp64: y [T,H]. All float inputs are widened to float64."""
+    x, w, w13, w2 = _f64(x), _f64(w), _f64(w13), _f64(w2)
+    idx = _i32(idx)
+    T, H = x.shape
+    E, I2, _ = w13.shape
+    K = idx.shape[1]
+    y = np.empty((T, H), np.float64)
+    lib().oracle_forward(T, H, I2 // 2, E, K, _p(x), _p(idx), _p(w), _p(w13), _p(w2),
+                         1 if act_mxfp8 else 0, _p(y))
+    return y
+
+
+def backward(x, idx, w, w13, w2, dy):
+    """Layer backward in fp64: (dx, dw13, dw2, dtopk)."""
+    x, w, w13, w2, dy = _f64(x), _f64(w), _f64(w13), _f64(w2), _f64(dy)
+    idx = _i32(idx)
+    T, H = x.shape
+    E, I2, _ = w13.shape
+    K = idx.shape[1]
+    dx = np.empty((T, H), np.float64)
+    dw13 = np.empty(w13.shape, np.float64)
+    dw2 = np.empty(w2.shape, np.float64)
+    dtopk = np.empty((T, K), np.float64)
+    lib().oracle_backward(T, H, I2 // 2, E, K, _p(x), _p(idx), _p(w), _p(w13), _p(w2), _p(dy),
+                          _p(dx), _p(dw13), _p(dw2), _p(dtopk))
+    return dx, dw13, dw2, dtopk
+
+
+def router_grad(idx, w, dtopk, E):
+    idx, w, dtopk = _i32(idx), _f64(w), _f64(dtopk)
+    T, K = idx.shape
+    dl = np.empty((T, E), np.float64)
+    lib().oracle_router_grad(T, E, K, _p(idx), _p(w), _p(dtopk), _p(dl))
+    return dl
+

@@ -1,0 +1,346 @@
+/*
+ * oracle.c -- plain fp64 CPU oracle of the deterministic MoE layer.
+ *
+ * TEST INFRASTRUCTURE ONLY (see oracle.h): loaded by the tests, the package smoke check and
+ * the benchmark's CPU-baseline leg; never by the CUDA path, with which it shares no code.
+ *
+ * Each function follows the plain definition of its step; the passages are cited in
+ * oracle.h. Parallelism is over independent tokens (or independent experts) only, so
+ * every sum keeps the order its definition states.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- routing */
+
+void oracle_route(int64_t T, int32_t E, int32_t K, const double *logits, int32_t *idx,
+                  double *w)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        const double *l = logits + t * (int64_t)E;
+        char *taken = (char *)calloc((size_t)E, 1);
+        /* selection in the order (logit descending, expert ascending): a strictly larger
+         * logit wins, so among equal logits the lower expert id stays chosen; the double
+         * comparison treats -0 and +0 as equal. */
+        for (int32_t k = 0; k < K; ++k) {
+            int32_t best = -1;
+            for (int32_t e = 0; e < E; ++e) {
+                if (taken[e])
+                    continue;
+                if (best < 0 || l[e] > l[best])
+                    best = e;
+            }
+            taken[best] = 1;
+            idx[t * K + k] = best;
+        }
+        free(taken);
+        /* softmax over the K chosen logits, shifted by the largest one */
+        const double m = l[idx[t * K]];
+        double den = 0.0;
+        for (int32_t k = 0; k < K; ++k)
+            den += exp(l[idx[t * K + k]] - m);
+        for (int32_t k = 0; k < K; ++k)
+            w[t * K + k] = exp(l[idx[t * K + k]] - m) / den;
+    }
+}
+
+/* ---------------------------------------------------------------- schedule */
+
+int oracle_schedule(int64_t R, int32_t E, int64_t MB, const int32_t *idx, int32_t *counts,
+                    int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *segs,
+                    int64_t seg_cap, int32_t *n_segs)
+{
+    for (int32_t e = 0; e < E; ++e)
+        counts[e] = 0;
+    for (int64_t f = 0; f < R; ++f)
+        counts[idx[f]] += 1;
+    offsets[0] = 0;
+    for (int32_t e = 0; e < E; ++e)
+        offsets[e + 1] = offsets[e] + counts[e];
+    /* stable counting sort: flat ids visited in ascending order */
+    int32_t *fill = (int32_t *)calloc((size_t)E, sizeof(int32_t));
+    for (int64_t f = 0; f < R; ++f) {
+        const int32_t e = idx[f];
+        const int32_t row = offsets[e] + fill[e];
+        fill[e] += 1;
+        perm[row] = (int32_t)f;
+        inv[f] = row;
+    }
+    free(fill);
+    /* expert ranges cut at minibatch boundaries */
+    int64_t n = 0;
+    for (int32_t e = 0; e < E; ++e) {
+        int64_t b = offsets[e];
+        const int64_t end = offsets[e + 1];
+        while (b < end) {
+            int64_t mb_end = (b / MB + 1) * MB;
+            int64_t se = end < mb_end ? end : mb_end;
+            if (n >= seg_cap) {
+                *n_segs = (int32_t)n;
+                return -1;
+            }
+            segs[3 * n + 0] = e;
+            segs[3 * n + 1] = (int32_t)b;
+            segs[3 * n + 2] = (int32_t)se;
+            ++n;
+            b = se;
+        }
+    }
+    *n_segs = (int32_t)n;
+    return 0;
+}
+
+/* ---------------------------------------------------------------- MXFP8 */
+
+uint8_t oracle_e4m3_encode(double v)
+{
+    const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    if (isnan(v))
+        return 0x7F;
+    double a = fabs(v);
+    if (a >= 448.0)
+        return sign | 0x7E; /* saturate to the largest finite magnitude */
+    if (a == 0.0)
+        return sign;
+    /* grid spacing in the binade [2^e, 2^(e+1)) is 2^(e-3); below 2^-6 (subnormals) it is
+     * 2^-9. Scaling a by the spacing is exact, nearbyint rounds ties to even, and an even
+     * grid index is an even mantissa. */
+    int ex;
+    frexp(a, &ex);
+    int e = ex - 1;
+    if (e < -6)
+        e = -6;
+    const double r = nearbyint(ldexp(a, 3 - e));
+    const double mag = ldexp(r, e - 3);
+    if (mag == 0.0)
+        return sign;
+    if (mag < ldexp(1.0, -6)) /* subnormal: mag = m * 2^-9, m = 1..7 */
+        return sign | (uint8_t)ldexp(mag, 9);
+    frexp(mag, &ex);
+    const int E = ex - 1; /* -6..8 */
+    const int mant = (int)ldexp(mag, 3 - E) - 8;
+    return sign | (uint8_t)(((E + 7) << 3) | mant);
+}
+
+double oracle_e4m3_decode(uint8_t code)
+{
+    const double s = (code & 0x80) ? -1.0 : 1.0;
+    const int ef = (code >> 3) & 0xF;
+    const int m = code & 0x7;
+    if (ef == 0xF && m == 0x7)
+        return NAN;
+    if (ef == 0)
+        return s * ldexp((double)m, -9);
+    return s * ldexp(8.0 + m, ef - 7 - 3);
+}
+
+void oracle_mxfp8_quantize(int64_t rows, int64_t cols, const double *src, uint8_t *q,
+                           uint8_t *scale)
+{
+    const int64_t nb = cols / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const double *v = src + r * cols + b * 32;
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i)
+                if (fabs(v[i]) > amax)
+                    amax = fabs(v[i]);
+            int sexp = -127;
+            if (amax > 0.0) {
+                int ex;
+                frexp(amax, &ex);
+                sexp = (ex - 1) - 8; /* floor(log2 amax) minus the E4M3 max exponent */
+                if (sexp < -127)
+                    sexp = -127;
+                if (sexp > 127)
+                    sexp = 127;
+            }
+            scale[r * nb + b] = (uint8_t)(sexp + 127);
+            for (int i = 0; i < 32; ++i)
+                q[r * cols + b * 32 + i] = oracle_e4m3_encode(ldexp(v[i], -sexp));
+        }
+    }
+}
+
+void oracle_mxfp8_dequantize(int64_t rows, int64_t cols, const uint8_t *q, const uint8_t *scale,
+                             double *out)
+{
+    const int64_t nb = cols / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c)
+            out[r * cols + c] = ldexp(oracle_e4m3_decode(q[r * cols + c]),
+                                      (int)scale[r * nb + c / 32] - 127);
+}
+
+static void qdq_row(int64_t n, double *v)
+{
+    uint8_t *q = (uint8_t *)malloc((size_t)n);
+    uint8_t *s = (uint8_t *)malloc((size_t)(n / 32));
+    oracle_mxfp8_quantize(1, n, v, q, s);
+    oracle_mxfp8_dequantize(1, n, q, s, v);
+    free(q);
+    free(s);
+}
+
+/* ---------------------------------------------------------------- forward */
+
+static double silu(double g) { return g / (1.0 + exp(-g)); }
+
+void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
+                    const int32_t *idx, const double *w, const double *w13, const double *w2,
+                    int32_t act_mxfp8, double *y)
+{
+    (void)E;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < T; ++t) {
+        double *xt = (double *)malloc(sizeof(double) * (size_t)H);
+        double *a = (double *)malloc(sizeof(double) * 2 * (size_t)I);
+        double *h = (double *)malloc(sizeof(double) * (size_t)I);
+        double *yt = y + t * (int64_t)H;
+        memcpy(xt, x + t * (int64_t)H, sizeof(double) * (size_t)H);
+        if (act_mxfp8)
+            qdq_row(H, xt);
+        for (int32_t c = 0; c < H; ++c)
+            yt[c] = 0.0;
+        for (int32_t k = 0; k < K; ++k) {
+            const int64_t e = idx[t * K + k];
+            const double *W13 = w13 + e * 2 * (int64_t)I * H;
+            const double *W2 = w2 + e * (int64_t)H * I;
+            for (int32_t j = 0; j < 2 * I; ++j) {
+                double acc = 0.0;
+                for (int32_t c = 0; c < H; ++c)
+                    acc += W13[(int64_t)j * H + c] * xt[c];
+                a[j] = acc;
+            }
+            for (int32_t i = 0; i < I; ++i)
+                h[i] = silu(a[i]) * a[I + i];
+            if (act_mxfp8)
+                qdq_row(I, h);
+            const double s = w[t * K + k];
+            for (int32_t c = 0; c < H; ++c) {
+                double o = 0.0;
+                for (int32_t i = 0; i < I; ++i)
+                    o += W2[(int64_t)c * I + i] * h[i];
+                yt[c] += s * o;
+            }
+        }
+        free(xt);
+        free(a);
+        free(h);
+    }
+}
+
+/* ---------------------------------------------------------------- backward */
+
+void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
+                     const int32_t *idx, const double *w, const double *w13, const double *w2,
+                     const double *dy, double *dx, double *dw13, double *dw2, double *dtopk)
+{
+    const int64_t R = T * K;
+    /* per routed row: da = dL/da [2I] and sh = w * h [I], kept for the weight gradients */
+    double *da_all = (double *)malloc(sizeof(double) * (size_t)(R * 2 * I));
+    double *sh_all = (double *)malloc(sizeof(double) * (size_t)(R * I));
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < T; ++t) {
+        const double *xt = x + t * (int64_t)H;
+        const double *dyt = dy + t * (int64_t)H;
+        double *dxt = dx + t * (int64_t)H;
+        double *a = (double *)malloc(sizeof(double) * 2 * (size_t)I);
+        double *g = (double *)malloc(sizeof(double) * (size_t)I);
+        for (int32_t c = 0; c < H; ++c)
+            dxt[c] = 0.0;
+        for (int32_t k = 0; k < K; ++k) {
+            const int64_t f = t * K + k;
+            const int64_t e = idx[f];
+            const double *W13 = w13 + e * 2 * (int64_t)I * H;
+            const double *W2 = w2 + e * (int64_t)H * I;
+            const double s = w[f];
+            double *da = da_all + f * 2 * I;
+            double *sh = sh_all + f * I;
+            for (int32_t j = 0; j < 2 * I; ++j) {
+                double acc = 0.0;
+                for (int32_t c = 0; c < H; ++c)
+                    acc += W13[(int64_t)j * H + c] * xt[c];
+                a[j] = acc;
+            }
+            /* g = W2^T dy */
+            for (int32_t i = 0; i < I; ++i) {
+                double acc = 0.0;
+                for (int32_t c = 0; c < H; ++c)
+                    acc += W2[(int64_t)c * I + i] * dyt[c];
+                g[i] = acc;
+            }
+            double dS = 0.0;
+            for (int32_t i = 0; i < I; ++i) {
+                const double ag = a[i], au = a[I + i];
+                const double sig = 1.0 / (1.0 + exp(-ag));
+                const double sl = ag * sig;
+                const double hi = sl * au;
+                dS += g[i] * hi;
+                const double dh = s * g[i];
+                /* silu'(g) = sig * (1 + g * (1 - sig)) */
+                da[i] = dh * au * sig * (1.0 + ag * (1.0 - sig));
+                da[I + i] = dh * sl;
+                sh[i] = s * hi;
+            }
+            dtopk[f] = dS;
+            /* dx += W13^T da */
+            for (int32_t c = 0; c < H; ++c) {
+                double acc = 0.0;
+                for (int32_t j = 0; j < 2 * I; ++j)
+                    acc += W13[(int64_t)j * H + c] * da[j];
+                dxt[c] += acc;
+            }
+        }
+        free(a);
+        free(g);
+    }
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t e = 0; e < E; ++e) {
+        double *DW13 = dw13 + (int64_t)e * 2 * I * H;
+        double *DW2 = dw2 + (int64_t)e * H * I;
+        memset(DW13, 0, sizeof(double) * (size_t)(2 * (int64_t)I * H));
+        memset(DW2, 0, sizeof(double) * (size_t)((int64_t)H * I));
+        for (int64_t f = 0; f < R; ++f) {
+            if (idx[f] != e)
+                continue;
+            const int64_t t = f / K;
+            const double *xt = x + t * (int64_t)H;
+            const double *dyt = dy + t * (int64_t)H;
+            const double *da = da_all + f * 2 * I;
+            const double *sh = sh_all + f * I;
+            for (int32_t j = 0; j < 2 * I; ++j)
+                for (int32_t c = 0; c < H; ++c)
+                    DW13[(int64_t)j * H + c] += da[j] * xt[c];
+            for (int32_t c = 0; c < H; ++c)
+                for (int32_t i = 0; i < I; ++i)
+                    DW2[(int64_t)c * I + i] += dyt[c] * sh[i];
+        }
+    }
+    free(da_all);
+    free(sh_all);
+}
+
+void oracle_router_grad(int64_t T, int32_t E, int32_t K, const int32_t *idx, const double *w,
+                        const double *dtopk, double *dlogits)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        double *dl = dlogits + t * (int64_t)E;
+        for (int32_t e = 0; e < E; ++e)
+            dl[e] = 0.0;
+        double sw = 0.0;
+        for (int32_t k = 0; k < K; ++k)
+            sw += w[t * K + k] * dtopk[t * K + k];
+        for (int32_t k = 0; k < K; ++k)
+            dl[idx[t * K + k]] = w[t * K + k] * (dtopk[t * K + k] - sw);
+    }
+}

@@ -1,0 +1,85 @@
+/*
+ * oracle.h -- plain, slow, fp64 CPU oracle of the deterministic MoE layer.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the tests, the package smoke check and the benchmark's
+ * CPU-baseline leg may load this library. It shares no code, header, table or helper with
+ * the CUDA path, and the CUDA path never calls it.
+ *
+ * Pages cited (by title and section):
+ *   [arex]     "Cursor 放出 MoK：NVL72 训练提速 2.37 倍" (arex-research.com)
+ *   [aigwx]    "Cursor 开源 MoK：面向 GB300 NVL72 的确定性 MoE 训练内核，性能提升 2.37 倍" (aigwx.org)
+ *   [alphalab] "Mixture-of-Kittens" analysis (alphalab.site)
+ *
+ * Every floating-point value is a double. Inputs stored as bf16/fp32 are widened exactly
+ * by the caller. No step is blocked, fused or reordered beyond its plain definition.
+ */
+#ifndef MOK_ORACLE_H
+#define MOK_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Top-k routing over router logits ([alphalab] section 四: top-k over Gaussian logits).
+ * For each token t the pairs (logit, e) are ordered by logit descending, then expert id
+ * ascending; the first K are taken in that order. w = softmax over the K chosen logits
+ * (routing function read from the workload description; the pages name none). */
+void oracle_route(int64_t T, int32_t E, int32_t K, const double *logits, int32_t *idx,
+                  double *w);
+
+/* Expert schedule ([arex] section "pull 代替 push": one schedule table serves dispatch,
+ * combine and their backward twins). Flat routed ids f = t*K + k are stably sorted by
+ * expert: perm[row] = f, inv[f] = row, counts[e], offsets[E+1] (exclusive scan).
+ * Segments are the non-empty intersections of each expert's row range with the minibatch
+ * row ranges [m*MB, (m+1)*MB), in increasing row order, as (expert, row_begin, row_end).
+ * Returns 0, or -1 when more than seg_cap segments would be written. */
+int oracle_schedule(int64_t R, int32_t E, int64_t MB, const int32_t *idx, int32_t *counts,
+                    int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *segs,
+                    int64_t seg_cap, int32_t *n_segs);
+
+/* OFP8 E4M3 (bias 7, no infinities, max finite 448): round to nearest, ties to even,
+ * saturating finite overflow to +-448, sign of zero kept. */
+uint8_t oracle_e4m3_encode(double v);
+double oracle_e4m3_decode(uint8_t code);
+
+/* MXFP8 block quantization along rows: 32-element blocks share an E8M0 scale
+ * 2^(floor(log2 amax) - 8), clamped to [2^-127, 2^127]; amax == 0 gives scale byte 0.
+ * cols must be a multiple of 32. q is [rows][cols], scale is [rows][cols/32]. */
+void oracle_mxfp8_quantize(int64_t rows, int64_t cols, const double *src, uint8_t *q,
+                           uint8_t *scale);
+void oracle_mxfp8_dequantize(int64_t rows, int64_t cols, const uint8_t *q, const uint8_t *scale,
+                             double *out);
+
+/* Forward of the layer, per token, with no schedule and no permutation:
+ *   a = W13[e] x  (gate rows 0..I-1, up rows I..2I-1), h = silu(a_g) * a_u,
+ *   o = W2[e] h,  y_t = sum over k ascending of w[t,k] * o_k.
+ * act_mxfp8 != 0 quantizes x along H and h along I to MXFP8 and back before use
+ * ([arex] section "pull 代替 push": activation quantization fused into dispatch and
+ * SwiGLU); the weights passed in are then already the dequantized MXFP8 weights.
+ * x [T][H], idx/w [T][K], w13 [E][2I][H], w2 [E][H][I], y [T][H]. */
+void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
+                    const int32_t *idx, const double *w, const double *w13, const double *w2,
+                    int32_t act_mxfp8, double *y);
+
+/* Backward of the BF16 layer by the chain rule, given dy [T][H]:
+ *   g = W2[e]^T dy_t, dS[t,k] = <g, h>, dh = w g,
+ *   da_g = dh * a_u * silu'(a_g), da_u = dh * silu(a_g),
+ *   dx_t = sum_k W13[e]^T da, dW13[e] = sum da x^T, dW2[e] = sum dy (w h)^T
+ * ([arex] section "pull 代替 push": router-weight gradient computed with the SwiGLU
+ * backward; [alphalab] section 一: expert gradient computation). Sums over routed rows run
+ * in ascending flat id. Outputs: dx [T][H], dw13 [E][2I][H], dw2 [E][H][I],
+ * dtopk [T][K] (= dS). */
+void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
+                     const int32_t *idx, const double *w, const double *w13, const double *w2,
+                     const double *dy, double *dx, double *dw13, double *dw2, double *dtopk);
+
+/* Router-logit gradient through the top-k softmax: for a chosen expert j = idx[t,k],
+ * dlogits[t,j] = w_k (dS_k - sum_m w_m dS_m); every other logit gets 0. */
+void oracle_router_grad(int64_t T, int32_t E, int32_t K, const int32_t *idx, const double *w,
+                        const double *dtopk, double *dlogits);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

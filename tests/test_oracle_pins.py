@@ -1,0 +1,334 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test ties one oracle function to something independent: a hand-worked example
+(tests/golden, with its derivation), a library routine (numpy stable sort, scipy softmax,
+torch's float8 conversion, numpy matmul for the dense special cases), brute force over a
+finite set, a closed form, an invariant, or central finite differences. A plausible
+mistake in the oracle (a dropped term, a wrong sign, a swapped gate/up half, a transposed
+weight, an unstable sort, a wrong rounding direction) fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(12345)
+
+
+def _silu(z):
+    return z / (1.0 + np.exp(-z))
+
+
+# ------------------------------------------------------------------ routing
+
+def test_route_matches_stable_lexsort_with_ties():
+    T, E, K = 64, 16, 5
+    # few distinct values -> many ties; include both zeros
+    vals = np.array([-1.5, -0.0, 0.0, 0.25, 0.25, 2.0])
+    logits = rng.choice(vals, size=(T, E))
+    idx, w = oracle.route(logits, K)
+    for t in range(T):
+        order = np.lexsort((np.arange(E), -logits[t]))  # by logit desc, then id asc
+        assert list(idx[t]) == list(order[:K])
+
+
+def test_route_weights_are_renormalised_full_softmax():
+    T, E, K = 50, 32, 6
+    logits = rng.standard_normal((T, E)) * 3
+    idx, w = oracle.route(logits, K)
+    p = scipy.special.softmax(logits, axis=1)
+    sel = np.take_along_axis(p, idx.astype(np.int64), axis=1)
+    np.testing.assert_allclose(w, sel / sel.sum(1, keepdims=True), rtol=1e-12, atol=0)
+    np.testing.assert_allclose(w.sum(1), 1.0, rtol=0, atol=1e-12)
+    assert np.all(np.diff(w, axis=1) <= 0)  # descending logits give descending weights
+
+
+def test_route_one_hot_and_k_equals_e():
+    E = 8
+    lg = np.zeros((E, E)) - 5.0
+    lg[np.arange(E), np.arange(E)] = 5.0
+    idx, w = oracle.route(lg, 1)
+    assert list(idx[:, 0]) == list(range(E)) and np.all(w == 1.0)
+    logits = rng.standard_normal((4, E))
+    idx, w = oracle.route(logits, E)
+    full = scipy.special.softmax(logits, axis=1)
+    np.testing.assert_allclose(np.take_along_axis(full, idx.astype(np.int64), 1), w,
+                               rtol=1e-12)
+
+
+# ------------------------------------------------------------------ schedule
+
+def test_schedule_hand_example():
+    g = json.load(open(os.path.join(GOLDEN, "schedule_hand.json")))
+    s = oracle.schedule(np.array(g["idx"]), g["E"], g["MB"])
+    for key in ("counts", "offsets", "perm", "inv"):
+        assert list(s[key]) == g[key], key
+    assert s["segs"].tolist() == g["segs"]
+
+
+@pytest.mark.parametrize("T,E,K,MB", [(200, 16, 4, 37), (64, 64, 8, 1000), (300, 5, 2, 1),
+                                      (1, 4, 1, 3), (0, 8, 2, 16)])
+def test_schedule_matches_stable_sort_and_run_lengths(T, E, K, MB):
+    idx = rng.integers(0, E, size=(T, K)).astype(np.int32)
+    if T > 3:
+        idx[: T // 3] = 0  # a hot expert and some empty ones
+    s = oracle.schedule(idx, E, MB)
+    f = idx.reshape(-1)
+    R = f.size
+    np.testing.assert_array_equal(s["perm"], np.argsort(f, kind="stable"))
+    np.testing.assert_array_equal(s["counts"], np.bincount(f, minlength=E))
+    assert s["counts"].sum() == R  # no routed row is dropped
+    if R:
+        np.testing.assert_array_equal(s["inv"][s["perm"]], np.arange(R))
+    # segments: maximal runs of rows sharing (expert, minibatch)
+    key_e = f[s["perm"]] if R else np.zeros(0, np.int64)
+    key_m = np.arange(R) // MB
+    runs = []
+    for r in range(R):
+        if r == 0 or key_e[r] != key_e[r - 1] or key_m[r] != key_m[r - 1]:
+            runs.append([int(key_e[r]), r, r + 1])
+        else:
+            runs[-1][2] = r + 1
+    assert s["segs"].tolist() == runs
+
+
+# ------------------------------------------------------------------ MXFP8
+
+def _torch_e4m3(v):
+    t = torch.tensor(np.asarray(v, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_decode_matches_torch_table():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ours = np.array([oracle.e4m3_decode(int(c)) for c in codes])
+    finite = ~np.isnan(ref)
+    np.testing.assert_array_equal(ours[finite], ref[finite])
+    assert np.all(np.isnan(ours[~finite]))
+
+
+@pytest.mark.parametrize("shift", [-9, 0, 6])
+def test_e4m3_encode_all_bf16_patterns(shift):
+    bits = np.arange(65536, dtype=np.uint32)
+    f = (bits << 16).view(np.float32)
+    f = f[np.isfinite(f)].astype(np.float64) * 2.0 ** shift
+    f = f[np.isfinite(f)]
+    ours = np.array([oracle.e4m3_encode(v) for v in f], dtype=np.uint8)
+    sat = np.abs(f) >= 448.0
+    # saturation by definition; torch's conversion does not saturate
+    assert np.all(ours[sat] & 0x7F == 0x7E)
+    assert np.all((ours[sat] >> 7) == np.signbit(f[sat]))
+    small = ~sat & (np.abs(f) < 3.0e38)
+    ref = _torch_e4m3(f[small])
+    np.testing.assert_array_equal(ours[small], ref)
+
+
+def test_e4m3_encode_bruteforce_nearest_even():
+    mags = np.array([oracle.e4m3_decode(c) for c in range(0x7F)])  # 0 .. 448
+    vals = np.concatenate([rng.uniform(0, 460, 3000), rng.uniform(0, 2.0 ** -5, 3000),
+                           (mags[:-1] + mags[1:]) / 2])  # exact midpoints
+    for v in vals:
+        d = np.abs(mags - v)
+        best = np.flatnonzero(d == d.min())
+        want = best[0] if len(best) == 1 else [b for b in best if b % 2 == 0][0]
+        if v >= 448:
+            want = 0x7E
+        assert oracle.e4m3_encode(v) == want, v
+        assert oracle.e4m3_encode(-v) == want | 0x80, v
+
+
+def test_mxfp8_hand_vectors():
+    g = json.load(open(os.path.join(GOLDEN, "mxfp8_hand.json")))
+    for case in g["cases"]:
+        blk = np.full(32, case["fill"])
+        first = np.array(case["block_first"], dtype=np.float64)
+        blk[: len(first)] = first
+        q, s = oracle.mxfp8_quantize(blk[None, :])
+        assert int(s[0, 0]) == case["scale_byte"], case["what"]
+        assert list(q[0, : len(first)]) == case["codes_first"], case["what"]
+
+
+def test_mxfp8_scale_rule_and_roundtrip_bound():
+    x = rng.standard_normal((40, 256)) * np.exp(rng.uniform(-20, 20, size=(40, 1)))
+    x[3, :32] = 0.0
+    q, s = oracle.mxfp8_quantize(x)
+    blocks = np.abs(x).reshape(40, 8, 32).max(-1)
+    m, e = np.frexp(blocks)  # blocks = m * 2**e, m in [0.5, 1)
+    want = np.where(blocks > 0, np.clip(e - 1 - 8, -127, 127) + 127, 0)
+    np.testing.assert_array_equal(s, want)
+    dq = oracle.mxfp8_dequantize(q, s)
+    # error per element: at most half a step of amax's binade (2^(e-4), e = floor(log2 amax)),
+    # or the clipping of the block's top values to 448 * 2^(e-8)
+    err = np.abs(dq - x).reshape(40, 8, 32).max(-1)
+    ef = e - 1
+    bound = np.maximum(np.ldexp(1.0, ef - 4), blocks - 448.0 * np.ldexp(1.0, ef - 8))
+    assert np.all(err <= np.where(blocks > 0, bound, 0.0))
+    # quantize-dequantize is idempotent
+    q2, s2 = oracle.mxfp8_quantize(dq)
+    np.testing.assert_array_equal(q2, q)
+    np.testing.assert_array_equal(s2, s)
+
+
+# ------------------------------------------------------------------ forward
+
+def _rand_layer(T, H, I, E, K, scale=0.3, seed=0):
+    r = np.random.default_rng(seed)
+    x = r.standard_normal((T, H))
+    logits = r.standard_normal((T, E))
+    w13 = r.standard_normal((E, 2 * I, H)) * scale
+    w2 = r.standard_normal((E, H, I)) * scale
+    return x, logits, w13, w2
+
+
+def test_forward_hand_example():
+    g = json.load(open(os.path.join(GOLDEN, "forward_hand.json")))
+    idx, w = oracle.route(np.array(g["logits"]), 2)
+    assert idx.tolist() == g["idx"]
+    np.testing.assert_allclose(w[0], g["w"], rtol=1e-15)
+    y = oracle.forward(np.array(g["x"]), idx, w, np.array(g["w13"]), np.array(g["w2"]))
+    np.testing.assert_allclose(y[0], g["y"], rtol=1e-14)
+    # closed form, recomputed from the definition of silu
+    h0, h1 = 2.0 / (1 + math.exp(-2.0)), 2.0 / (1 + math.exp(-1.0))
+    np.testing.assert_allclose(y[0], [0.75 * h1 + 0.5 * h0, -0.75 * h1], rtol=1e-14)
+
+
+def test_forward_single_expert_is_dense_swiglu_ffn():
+    T, H, I = 7, 24, 10
+    x, _, w13, w2 = _rand_layer(T, H, I, 1, 1)
+    idx = np.zeros((T, 1), np.int32)
+    w = np.ones((T, 1))
+    y = oracle.forward(x, idx, w, w13, w2)
+    a = x @ w13[0].T
+    ref = (_silu(a[:, :I]) * a[:, I:]) @ w2[0].T
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_forward_k_equals_e_is_dense_softmax_mixture():
+    T, H, I, E = 5, 16, 6, 4
+    x, logits, w13, w2 = _rand_layer(T, H, I, E, E)
+    idx, w = oracle.route(logits, E)
+    y = oracle.forward(x, idx, w, w13, w2)
+    p = scipy.special.softmax(logits, axis=1)
+    ref = np.zeros_like(y)
+    for e in range(E):
+        a = x @ w13[e].T
+        ref += p[:, e: e + 1] * ((_silu(a[:, :I]) * a[:, I:]) @ w2[e].T)
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_forward_equivariance_and_linearity():
+    T, H, I, E, K = 12, 16, 8, 6, 3
+    x, logits, w13, w2 = _rand_layer(T, H, I, E, K, seed=3)
+    idx, w = oracle.route(logits, K)
+    y = oracle.forward(x, idx, w, w13, w2)
+    # permuting tokens permutes outputs
+    p = rng.permutation(T)
+    idx_p, w_p = oracle.route(logits[p], K)
+    np.testing.assert_array_equal(oracle.forward(x[p], idx_p, w_p, w13, w2), y[p])
+    # relabelling experts (weights and logit columns together) leaves y unchanged
+    q = rng.permutation(E)
+    idx_q, w_q = oracle.route(logits[:, q], K)
+    np.testing.assert_allclose(oracle.forward(x, idx_q, w_q, w13[q], w2[q]), y, rtol=1e-13,
+                               atol=1e-15)
+    # y is linear in W2 and in the routing weights
+    np.testing.assert_allclose(oracle.forward(x, idx, w, w13, 2.0 * w2), 2.0 * y, rtol=1e-15)
+    np.testing.assert_allclose(oracle.forward(x, idx, 0.5 * w, w13, w2), 0.5 * y, rtol=1e-15)
+
+
+def test_forward_mxfp8_quantizes_x_and_h_at_the_right_places():
+    """With one expert, K=1 and W2 = identity (H = I = 32), y is exactly the dequantized
+    MXFP8 image of h computed from the dequantized MXFP8 image of x."""
+    T, H, I = 6, 32, 32
+    r = np.random.default_rng(5)
+    x = r.standard_normal((T, H))
+    w13 = r.standard_normal((1, 2 * I, H)) * 0.2
+    w2 = np.eye(H)[None]
+    idx = np.zeros((T, 1), np.int32)
+    w = np.ones((T, 1))
+    y = oracle.forward(x, idx, w, w13, w2, act_mxfp8=True)
+    xq = oracle.mxfp8_dequantize(*oracle.mxfp8_quantize(x))
+    a = xq @ w13[0].T
+    h = _silu(a[:, :I]) * a[:, I:]
+    hq = oracle.mxfp8_dequantize(*oracle.mxfp8_quantize(h))
+    np.testing.assert_allclose(y, hq, rtol=1e-12, atol=0)
+    assert not np.allclose(y, h, rtol=1e-6)  # quantization really happened
+
+
+# ------------------------------------------------------------------ backward
+
+def _loss(x, logits, w13, w2, dy, K):
+    idx, w = oracle.route(logits, K)
+    return float((oracle.forward(x, idx, w, w13, w2) * dy).sum())
+
+
+def _fd_check(f, arr, grad, n=40, eps=1e-6, seed=0):
+    r = np.random.default_rng(seed)
+    flat = arr.reshape(-1)
+    picks = r.choice(flat.size, size=min(n, flat.size), replace=False)
+    for i in picks:
+        old = flat[i]
+        flat[i] = old + eps
+        lp = f()
+        flat[i] = old - eps
+        lm = f()
+        flat[i] = old
+        fd = (lp - lm) / (2 * eps)
+        g = grad.reshape(-1)[i]
+        assert abs(fd - g) <= 1e-6 * max(1.0, abs(g)), (i, fd, g)
+
+
+def test_backward_hand_example():
+    g = json.load(open(os.path.join(GOLDEN, "forward_hand.json")))
+    x, w13, w2, dy = (np.array(g[k]) for k in ("x", "w13", "w2", "dy"))
+    idx, w = oracle.route(np.array(g["logits"]), 2)
+    dx, dw13, dw2, dtopk = oracle.backward(x, idx, w, w13, w2, dy)
+    np.testing.assert_allclose(dtopk[0], g["dtopk"], rtol=1e-14)
+    sig = lambda z: 1 / (1 + math.exp(-z))  # noqa: E731
+    dsilu = lambda z: sig(z) * (1 + z * (1 - sig(z)))  # noqa: E731
+    silu = lambda z: z * sig(z)  # noqa: E731
+    # expert 1 (w=3/4, g=1): da = (3/4 * 2 * silu'(1), 3/4 * silu(1)); W13[1] = identity
+    # expert 0 (w=1/4, g=2): da = (1/2 * silu'(2), 1/2 * silu(2)); W13[0] swaps the inputs
+    dx_ref = [0.75 * 2 * dsilu(1.0) + 0.5 * silu(2.0), 0.75 * silu(1.0) + 0.5 * dsilu(2.0)]
+    np.testing.assert_allclose(dx[0], dx_ref, rtol=1e-14)
+    h0, h1 = 2 / (1 + math.exp(-2.0)), 2 / (1 + math.exp(-1.0))
+    dl = oracle.router_grad(idx, w, dtopk, 2)
+    np.testing.assert_allclose(dl[0], [3 / 16 * (2 * h0 - h1), 3 / 16 * (h1 - 2 * h0)],
+                               rtol=1e-13)
+
+
+def test_backward_finite_differences():
+    T, H, I, E, K = 6, 16, 8, 4, 2
+    r = np.random.default_rng(7)
+    for _ in range(100):
+        logits = r.standard_normal((T, E))
+        s = -np.sort(-logits, axis=1)
+        if np.all(s[:, K - 1] - s[:, K] > 1e-2):
+            break
+    x = r.standard_normal((T, H))
+    w13 = r.standard_normal((E, 2 * I, H)) * 0.3
+    w2 = r.standard_normal((E, H, I)) * 0.3
+    dy = r.standard_normal((T, H))
+    idx, w = oracle.route(logits, K)
+    dx, dw13, dw2, dtopk = oracle.backward(x, idx, w, w13, w2, dy)
+    dlogits = oracle.router_grad(idx, w, dtopk, E)
+    f = lambda: _loss(x, logits, w13, w2, dy, K)  # noqa: E731
+    _fd_check(f, x, dx, seed=1)
+    _fd_check(f, w13, dw13, seed=2)
+    _fd_check(f, w2, dw2, seed=3)
+    _fd_check(f, logits, dlogits, seed=4)
+    # dS is the derivative with respect to the routing weights themselves
+    wv = w.copy()
+    g = lambda: float((oracle.forward(x, idx, wv, w13, w2) * dy).sum())  # noqa: E731
+    _fd_check(g, wv, dtopk, seed=5)
+    # unrouted experts get zero weight gradients
+    used = np.zeros(E, bool)
+    used[np.unique(idx)] = True
+    assert np.all(dw13[~used] == 0) and np.all(dw2[~used] == 0)

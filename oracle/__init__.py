@@ -43,8 +43,12 @@ def lib():
         L.oracle_e4m3_decode.restype = ctypes.c_double
         L.oracle_mxfp8_quantize.argtypes = [i64, i64, p, p, p]
         L.oracle_mxfp8_dequantize.argtypes = [i64, i64, p, p, p]
-        L.oracle_forward.argtypes = [i64, i32, i32, i32, i32, p, p, p, p, p, i32, p]
-        L.oracle_backward.argtypes = [i64, i32, i32, i32, i32, p, p, p, p, p, p, p, p, p, p]
+        L.oracle_mxfp8_quantize_bf16.argtypes = [i64, i64, p, p, p]
+        L.oracle_forward.argtypes = [i64, i32, i32, i32, i32, p, p, p, i32, p, p, p, p, i32, p]
+        L.oracle_backward.argtypes = [i64, i32, i32, i32, i32, p, p, p, i32, p, p, p, i32, p,
+                                      p, p, p]
+        L.oracle_round_bf16.argtypes = [ctypes.c_double]
+        L.oracle_round_bf16.restype = ctypes.c_double
         L.oracle_router_grad.argtypes = [i64, i32, i32, p, p, p, p]
         _lib = L
     return _lib
@@ -129,33 +133,75 @@ def mxfp8_dequantize(q, scale):
     return out
 
 
-def forward(x, idx, w, w13, w2, act_mxfp8=False):
-    """Layer forward in fp64: y [T,H]. All float inputs are widened to float64."""
-    x, w, w13, w2 = _f64(x), _f64(w), _f64(w13), _f64(w2)
+W_F64, W_BF16, W_MXFP8 = 0, 1, 2
+EXACT, BF16, MXFP8 = 0, 1, 2  # operand precision modes
+
+
+def round_bf16(v: float) -> float:
+    return float(lib().oracle_round_bf16(float(v)))
+
+
+def _weights(w):
+    """(kind, data, scale) of a weight tensor: float arrays are widened to float64, uint16
+    arrays are bf16 bit patterns, a (q, scale) pair of uint8 arrays is MXFP8."""
+    if isinstance(w, tuple):
+        q, s = np.ascontiguousarray(w[0], np.uint8), np.ascontiguousarray(w[1], np.uint8)
+        return W_MXFP8, q, s, q.shape
+    if w.dtype == np.uint16:
+        w = np.ascontiguousarray(w)
+        return W_BF16, w, None, w.shape
+    w = _f64(w)
+    return W_F64, w, None, w.shape
+
+
+def forward(x, idx, w, w13, w2, mode=EXACT):
+    """Layer forward in fp64: y [T,H], with the operand rounding of `mode` (EXACT, BF16 or
+    MXFP8). Weights as described in _weights (both of the same kind)."""
+    x, w = _f64(x), _f64(w)
     idx = _i32(idx)
+    k13, d13, s13, sh13 = _weights(w13)
+    k2, d2, s2, _ = _weights(w2)
+    assert k13 == k2
     T, H = x.shape
-    E, I2, _ = w13.shape
+    E, I2, _ = sh13
     K = idx.shape[1]
     y = np.empty((T, H), np.float64)
-    lib().oracle_forward(T, H, I2 // 2, E, K, _p(x), _p(idx), _p(w), _p(w13), _p(w2),
-                         1 if act_mxfp8 else 0, _p(y))
+    lib().oracle_forward(T, H, I2 // 2, E, K, _p(x), _p(idx), _p(w), k13, _p(d13),
+                         None if s13 is None else _p(s13), _p(d2),
+                         None if s2 is None else _p(s2), int(mode), _p(y))
     return y
 
 
-def backward(x, idx, w, w13, w2, dy):
-    """Layer backward in fp64: (dx, dw13, dw2, dtopk)."""
-    x, w, w13, w2, dy = _f64(x), _f64(w), _f64(w13), _f64(w2), _f64(dy)
+def backward(x, idx, w, w13, w2, dy, weight_grads=True, mode=EXACT):
+    """Layer backward in fp64: (dx, dw13, dw2, dtopk), with the operand rounding of `mode`
+    (EXACT or BF16); dw13/dw2 are None when weight_grads is False."""
+    x, w, dy = _f64(x), _f64(w), _f64(dy)
     idx = _i32(idx)
+    k13, d13, _, sh13 = _weights(w13)
+    k2, d2, _, sh2 = _weights(w2)
+    assert k13 == k2 and k13 != W_MXFP8
     T, H = x.shape
-    E, I2, _ = w13.shape
+    E, I2, _ = sh13
     K = idx.shape[1]
     dx = np.empty((T, H), np.float64)
-    dw13 = np.empty(w13.shape, np.float64)
-    dw2 = np.empty(w2.shape, np.float64)
+    dw13 = np.empty(sh13, np.float64) if weight_grads else None
+    dw2 = np.empty(sh2, np.float64) if weight_grads else None
     dtopk = np.empty((T, K), np.float64)
-    lib().oracle_backward(T, H, I2 // 2, E, K, _p(x), _p(idx), _p(w), _p(w13), _p(w2), _p(dy),
-                          _p(dx), _p(dw13), _p(dw2), _p(dtopk))
+    lib().oracle_backward(T, H, I2 // 2, E, K, _p(x), _p(idx), _p(w), k13, _p(d13), _p(d2),
+                          _p(dy), int(mode), _p(dx), None if dw13 is None else _p(dw13),
+                          None if dw2 is None else _p(dw2), _p(dtopk))
     return dx, dw13, dw2, dtopk
+
+
+def mxfp8_quantize_bf16(bits):
+    """MXFP8 of bf16 bit patterns along the last axis: (q, scale)."""
+    b = np.ascontiguousarray(bits, np.uint16)
+    cols = b.shape[-1]
+    rows = b.size // cols
+    q = np.empty(b.shape, np.uint8)
+    sc = np.empty(b.shape[:-1] + (cols // 32,), np.uint8)
+    lib().oracle_mxfp8_quantize_bf16(rows, cols, _p(b), _p(q), _p(sc))
+    return q, sc
 
 
 def router_grad(idx, w, dtopk, E):

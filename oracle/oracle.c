@@ -178,6 +178,54 @@ void oracle_mxfp8_dequantize(int64_t rows, int64_t cols, const uint8_t *q, const
                                       (int)scale[r * nb + c / 32] - 127);
 }
 
+void oracle_mxfp8_quantize_bf16(int64_t rows, int64_t cols, const uint16_t *src, uint8_t *q,
+                                uint8_t *scale)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        double v[32];
+        for (int64_t b = 0; b < cols / 32; ++b) {
+            for (int i = 0; i < 32; ++i) {
+                uint32_t u = (uint32_t)src[r * cols + b * 32 + i] << 16;
+                float f;
+                memcpy(&f, &u, 4);
+                v[i] = (double)f;
+            }
+            oracle_mxfp8_quantize(1, 32, v, q + r * cols + b * 32, scale + r * (cols / 32) + b);
+        }
+    }
+}
+
+/* element i of a weight tensor stored as `kind`, widened exactly to double */
+static double wget(int32_t kind, const void *data, const uint8_t *scale, int64_t row_len,
+                   int64_t i)
+{
+    if (kind == ORACLE_W_F64)
+        return ((const double *)data)[i];
+    if (kind == ORACLE_W_BF16) {
+        uint32_t u = (uint32_t)((const uint16_t *)data)[i] << 16;
+        float f;
+        memcpy(&f, &u, 4);
+        return (double)f;
+    }
+    const int64_t row = i / row_len, col = i % row_len;
+    return ldexp(oracle_e4m3_decode(((const uint8_t *)data)[i]),
+                 (int)scale[row * (row_len / 32) + col / 32] - 127);
+}
+
+double oracle_round_bf16(double v)
+{
+    if (v == 0.0 || isnan(v) || isinf(v))
+        return v;
+    /* 8 significant bits in the binade of v; below 2^-126 the spacing stays 2^-133 */
+    int ex;
+    frexp(fabs(v), &ex);
+    int e = ex - 1;
+    if (e < -126)
+        e = -126;
+    return ldexp(nearbyint(ldexp(v, 7 - e)), e - 7);
+}
+
 static void qdq_row(int64_t n, double *v)
 {
     uint8_t *q = (uint8_t *)malloc((size_t)n);
@@ -193,8 +241,9 @@ static void qdq_row(int64_t n, double *v)
 static double silu(double g) { return g / (1.0 + exp(-g)); }
 
 void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
-                    const int32_t *idx, const double *w, const double *w13, const double *w2,
-                    int32_t act_mxfp8, double *y)
+                    const int32_t *idx, const double *w, int32_t wkind, const void *w13,
+                    const uint8_t *w13_s, const void *w2, const uint8_t *w2_s, int32_t mode,
+                    double *y)
 {
     (void)E;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -204,29 +253,31 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
         double *h = (double *)malloc(sizeof(double) * (size_t)I);
         double *yt = y + t * (int64_t)H;
         memcpy(xt, x + t * (int64_t)H, sizeof(double) * (size_t)H);
-        if (act_mxfp8)
+        if (mode == ORACLE_MXFP8)
             qdq_row(H, xt);
         for (int32_t c = 0; c < H; ++c)
             yt[c] = 0.0;
         for (int32_t k = 0; k < K; ++k) {
             const int64_t e = idx[t * K + k];
-            const double *W13 = w13 + e * 2 * (int64_t)I * H;
-            const double *W2 = w2 + e * (int64_t)H * I;
+            const int64_t b13 = e * 2 * (int64_t)I * H, b2 = e * (int64_t)H * I;
             for (int32_t j = 0; j < 2 * I; ++j) {
                 double acc = 0.0;
                 for (int32_t c = 0; c < H; ++c)
-                    acc += W13[(int64_t)j * H + c] * xt[c];
+                    acc += wget(wkind, w13, w13_s, H, b13 + (int64_t)j * H + c) * xt[c];
                 a[j] = acc;
             }
             for (int32_t i = 0; i < I; ++i)
                 h[i] = silu(a[i]) * a[I + i];
-            if (act_mxfp8)
+            if (mode == ORACLE_MXFP8)
                 qdq_row(I, h);
+            else if (mode == ORACLE_BF16)
+                for (int32_t i = 0; i < I; ++i)
+                    h[i] = oracle_round_bf16(h[i]);
             const double s = w[t * K + k];
             for (int32_t c = 0; c < H; ++c) {
                 double o = 0.0;
                 for (int32_t i = 0; i < I; ++i)
-                    o += W2[(int64_t)c * I + i] * h[i];
+                    o += wget(wkind, w2, w2_s, I, b2 + (int64_t)c * I + i) * h[i];
                 yt[c] += s * o;
             }
         }
@@ -239,8 +290,9 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
 /* ---------------------------------------------------------------- backward */
 
 void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
-                     const int32_t *idx, const double *w, const double *w13, const double *w2,
-                     const double *dy, double *dx, double *dw13, double *dw2, double *dtopk)
+                     const int32_t *idx, const double *w, int32_t wkind, const void *w13,
+                     const void *w2, const double *dy, int32_t mode, double *dx, double *dw13,
+                     double *dw2, double *dtopk)
 {
     const int64_t R = T * K;
     /* per routed row: da = dL/da [2I] and sh = w * h [I], kept for the weight gradients */
@@ -259,22 +311,21 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
         for (int32_t k = 0; k < K; ++k) {
             const int64_t f = t * K + k;
             const int64_t e = idx[f];
-            const double *W13 = w13 + e * 2 * (int64_t)I * H;
-            const double *W2 = w2 + e * (int64_t)H * I;
+            const int64_t b13 = e * 2 * (int64_t)I * H, b2 = e * (int64_t)H * I;
             const double s = w[f];
             double *da = da_all + f * 2 * I;
             double *sh = sh_all + f * I;
             for (int32_t j = 0; j < 2 * I; ++j) {
                 double acc = 0.0;
                 for (int32_t c = 0; c < H; ++c)
-                    acc += W13[(int64_t)j * H + c] * xt[c];
+                    acc += wget(wkind, w13, NULL, H, b13 + (int64_t)j * H + c) * xt[c];
                 a[j] = acc;
             }
             /* g = W2^T dy */
             for (int32_t i = 0; i < I; ++i) {
                 double acc = 0.0;
                 for (int32_t c = 0; c < H; ++c)
-                    acc += W2[(int64_t)c * I + i] * dyt[c];
+                    acc += wget(wkind, w2, NULL, I, b2 + (int64_t)c * I + i) * dyt[c];
                 g[i] = acc;
             }
             double dS = 0.0;
@@ -290,12 +341,18 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
                 da[I + i] = dh * sl;
                 sh[i] = s * hi;
             }
+            if (mode == ORACLE_BF16) {
+                for (int32_t j = 0; j < 2 * I; ++j)
+                    da[j] = oracle_round_bf16(da[j]);
+                for (int32_t i = 0; i < I; ++i)
+                    sh[i] = oracle_round_bf16(sh[i]);
+            }
             dtopk[f] = dS;
             /* dx += W13^T da */
             for (int32_t c = 0; c < H; ++c) {
                 double acc = 0.0;
                 for (int32_t j = 0; j < 2 * I; ++j)
-                    acc += W13[(int64_t)j * H + c] * da[j];
+                    acc += wget(wkind, w13, NULL, H, b13 + (int64_t)j * H + c) * da[j];
                 dxt[c] += acc;
             }
         }
@@ -303,6 +360,11 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
         free(g);
     }
 
+    if (dw13 == NULL || dw2 == NULL) {
+        free(da_all);
+        free(sh_all);
+        return;
+    }
 #pragma omp parallel for schedule(dynamic, 1)
     for (int32_t e = 0; e < E; ++e) {
         double *DW13 = dw13 + (int64_t)e * 2 * I * H;

@@ -51,16 +51,37 @@ void oracle_mxfp8_quantize(int64_t rows, int64_t cols, const double *src, uint8_
 void oracle_mxfp8_dequantize(int64_t rows, int64_t cols, const uint8_t *q, const uint8_t *scale,
                              double *out);
 
+/* Weight storage read by the forward and backward. Every element is widened exactly to a
+ * double when it is read; nothing else differs between the kinds. */
+enum { ORACLE_W_F64 = 0, ORACLE_W_BF16 = 1, ORACLE_W_MXFP8 = 2 };
+
+/* MXFP8 quantization of bf16 bit patterns (same definition as oracle_mxfp8_quantize). */
+void oracle_mxfp8_quantize_bf16(int64_t rows, int64_t cols, const uint16_t *src, uint8_t *q,
+                                uint8_t *scale);
+
+/* bf16 rounding of a real value: nearest, ties to even, with bf16 subnormals. */
+double oracle_round_bf16(double v);
+
+/* Precision modes ([arex] section "pull 代替 push": the layer has a BF16 and an MXFP8
+ * mode; in MXFP8 mode activations are quantized where they enter the GEMMs, at dispatch
+ * and at SwiGLU). Read here as: the operands of every expert GEMM carry the mode's type.
+ *   ORACLE_EXACT: no rounding anywhere (the layer's real-valued definition);
+ *   ORACLE_BF16:  h is rounded to bf16 before the down GEMM (backward: dA and w*h are
+ *                 rounded to bf16 before the dgrad and weight-gradient GEMMs);
+ *   ORACLE_MXFP8: x is MXFP8-quantized along H before the gate/up GEMM and h along I
+ *                 before the down GEMM (forward only). */
+enum { ORACLE_EXACT = 0, ORACLE_BF16 = 1, ORACLE_MXFP8 = 2 };
+
 /* Forward of the layer, per token, with no schedule and no permutation:
  *   a = W13[e] x  (gate rows 0..I-1, up rows I..2I-1), h = silu(a_g) * a_u,
- *   o = W2[e] h,  y_t = sum over k ascending of w[t,k] * o_k.
- * act_mxfp8 != 0 quantizes x along H and h along I to MXFP8 and back before use
- * ([arex] section "pull 代替 push": activation quantization fused into dispatch and
- * SwiGLU); the weights passed in are then already the dequantized MXFP8 weights.
- * x [T][H], idx/w [T][K], w13 [E][2I][H], w2 [E][H][I], y [T][H]. */
+ *   o = W2[e] h,  y_t = sum over k ascending of w[t,k] * o_k,
+ * with the operand rounding of `mode` (ORACLE_*). Weights are stored as `wkind`
+ * (ORACLE_W_*); for ORACLE_W_MXFP8, w13_s and w2_s hold the E8M0 scales along each
+ * weight row. x [T][H], idx/w [T][K], w13 [E][2I][H], w2 [E][H][I], y [T][H]. */
 void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
-                    const int32_t *idx, const double *w, const double *w13, const double *w2,
-                    int32_t act_mxfp8, double *y);
+                    const int32_t *idx, const double *w, int32_t wkind, const void *w13,
+                    const uint8_t *w13_s, const void *w2, const uint8_t *w2_s, int32_t mode,
+                    double *y);
 
 /* Backward of the BF16 layer by the chain rule, given dy [T][H]:
  *   g = W2[e]^T dy_t, dS[t,k] = <g, h>, dh = w g,
@@ -68,11 +89,14 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
  *   dx_t = sum_k W13[e]^T da, dW13[e] = sum da x^T, dW2[e] = sum dy (w h)^T
  * ([arex] section "pull 代替 push": router-weight gradient computed with the SwiGLU
  * backward; [alphalab] section 一: expert gradient computation). Sums over routed rows run
- * in ascending flat id. Outputs: dx [T][H], dw13 [E][2I][H], dw2 [E][H][I],
- * dtopk [T][K] (= dS). */
+ * in ascending flat id. mode is ORACLE_EXACT or ORACLE_BF16 (dA and w*h rounded to bf16
+ * where they enter the dgrad and weight-gradient GEMMs). Weights are ORACLE_W_F64 or
+ * ORACLE_W_BF16. Outputs: dx [T][H], dw13 [E][2I][H], dw2 [E][H][I], dtopk [T][K] (= dS);
+ * dw13/dw2 may be NULL (skipped). */
 void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
-                     const int32_t *idx, const double *w, const double *w13, const double *w2,
-                     const double *dy, double *dx, double *dw13, double *dw2, double *dtopk);
+                     const int32_t *idx, const double *w, int32_t wkind, const void *w13,
+                     const void *w2, const double *dy, int32_t mode, double *dx, double *dw13,
+                     double *dw2, double *dtopk);
 
 /* Router-logit gradient through the top-k softmax: for a chosen expert j = idx[t,k],
  * dlogits[t,j] = w_k (dS_k - sum_m w_m dS_m); every other logit gets 0. */

@@ -243,6 +243,70 @@ def test_forward_equivariance_and_linearity():
     np.testing.assert_allclose(oracle.forward(x, idx, 0.5 * w, w13, w2), 0.5 * y, rtol=1e-15)
 
 
+def test_round_bf16_matches_single_rounding_of_fp32_values():
+    """For values exactly representable in fp32, rounding to bf16 is the library's fp32 ->
+    bf16 conversion (torch) and the workload generator's bit rounding."""
+    r = np.random.default_rng(8)
+    f = (r.standard_normal(20000) * np.exp(r.uniform(-90, 80, 20000))).astype(np.float32)
+    u = f.view(np.uint32)
+    ties = ((u & ~np.uint32(0xFFFF)) | np.uint32(0x8000)).view(np.float32)[:2000]  # halfway
+    f = np.concatenate([f, ties, np.array([1e-40, -3e-39, 0.0, -0.0], np.float32)])
+    ours = np.array([oracle.round_bf16(float(v)) for v in f])
+    lib_ref = torch.from_numpy(f).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(ours, lib_ref)
+    np.testing.assert_array_equal(np.signbit(ours), np.signbit(lib_ref))
+
+
+def test_forward_bf16_mode_rounds_h_before_the_down_gemm():
+    """With one expert, K=1 and W2 = identity (H = I), y is exactly bf16(h)."""
+    T, H, I = 6, 32, 32
+    r = np.random.default_rng(6)
+    x = r.standard_normal((T, H))
+    w13 = r.standard_normal((1, 2 * I, H)) * 0.2
+    w2 = np.eye(H)[None]
+    idx = np.zeros((T, 1), np.int32)
+    w = np.ones((T, 1))
+    y = oracle.forward(x, idx, w, w13, w2, mode=oracle.BF16)
+    a = x @ w13[0].T
+    h = _silu(a[:, :I]) * a[:, I:]
+    rb = np.array([oracle.round_bf16(v) for v in h.reshape(-1)]).reshape(h.shape)
+    # h here and inside the oracle may differ in the last bits; that can only change the
+    # rounding of values within a hair of a midpoint between bf16 neighbours
+    ulp = np.ldexp(1.0, np.frexp(np.abs(h))[1] - 8)
+    frac = np.abs(h) / ulp - np.floor(np.abs(h) / ulp)
+    near_mid = np.abs(frac - 0.5) < 1e-6
+    np.testing.assert_array_equal(y[~near_mid], rb[~near_mid])
+    assert np.all(np.abs(y - rb)[near_mid] <= ulp[near_mid])
+    assert not np.allclose(y, h, rtol=1e-6)
+    # exact mode does not round
+    np.testing.assert_allclose(oracle.forward(x, idx, w, w13, w2), h, rtol=1e-12, atol=1e-15)
+
+
+def test_backward_bf16_mode_rounds_da_and_sh():
+    """dtopk does not depend on the operand rounding; with W13 = [I; I] stacked identities
+    (H = I) and one row, dx is the sum of the rounded gate and up gradients."""
+    T, H, I = 4, 32, 32
+    r = np.random.default_rng(10)
+    x = r.standard_normal((T, H))
+    w13 = np.concatenate([np.eye(I), np.eye(I)])[None]  # a_g = a_u = x
+    w2 = r.standard_normal((1, H, I)) * 0.3
+    dy = r.standard_normal((T, H))
+    idx = np.zeros((T, 1), np.int32)
+    w = np.full((T, 1), 0.75)
+    dx0, _, _, dt0 = oracle.backward(x, idx, w, w13, w2, dy)
+    dx1, dw13, dw2, dt1 = oracle.backward(x, idx, w, w13, w2, dy, mode=oracle.BF16)
+    np.testing.assert_array_equal(dt0, dt1)
+    g = dy @ w2[0]
+    sig = 1 / (1 + np.exp(-x))
+    dag = 0.75 * g * x * sig * (1 + x * (1 - sig))
+    dau = 0.75 * g * x * sig
+    rb = np.vectorize(oracle.round_bf16)
+    np.testing.assert_allclose(dx1, rb(dag) + rb(dau), rtol=1e-12)
+    np.testing.assert_allclose(dx0, dag + dau, rtol=1e-12)
+    sh = rb(0.75 * x * sig * x)
+    np.testing.assert_allclose(dw2[0], dy.T @ sh, rtol=1e-12)
+
+
 def test_forward_mxfp8_quantizes_x_and_h_at_the_right_places():
     """With one expert, K=1 and W2 = identity (H = I = 32), y is exactly the dequantized
     MXFP8 image of h computed from the dequantized MXFP8 image of x."""
@@ -253,7 +317,7 @@ def test_forward_mxfp8_quantizes_x_and_h_at_the_right_places():
     w2 = np.eye(H)[None]
     idx = np.zeros((T, 1), np.int32)
     w = np.ones((T, 1))
-    y = oracle.forward(x, idx, w, w13, w2, act_mxfp8=True)
+    y = oracle.forward(x, idx, w, w13, w2, mode=oracle.MXFP8)
     xq = oracle.mxfp8_dequantize(*oracle.mxfp8_quantize(x))
     a = xq @ w13[0].T
     h = _silu(a[:, :I]) * a[:, I:]
@@ -332,3 +396,30 @@ def test_backward_finite_differences():
     used = np.zeros(E, bool)
     used[np.unique(idx)] = True
     assert np.all(dw13[~used] == 0) and np.all(dw2[~used] == 0)
+
+
+def test_weight_storage_kinds_agree_exactly():
+    """bf16 bit patterns and MXFP8 bytes are read as their exact values."""
+    from workloads.synth import f32_to_bf16_bits
+    T, H, I, E, K = 5, 64, 32, 3, 2
+    x, logits, w13, w2 = _rand_layer(T, H, I, E, K, seed=9)
+    b13 = f32_to_bf16_bits(w13.astype(np.float32))
+    b2 = f32_to_bf16_bits(w2.astype(np.float32))
+    idx, w = oracle.route(logits, K)
+    y_bits = oracle.forward(x, idx, w, b13, b2)
+    y_wide = oracle.forward(x, idx, w, oracle.bf16_to_f64(b13), oracle.bf16_to_f64(b2))
+    np.testing.assert_array_equal(y_bits, y_wide)
+    q13, s13 = oracle.mxfp8_quantize_bf16(b13)
+    q2, s2 = oracle.mxfp8_quantize_bf16(b2)
+    r13 = oracle.mxfp8_quantize(oracle.bf16_to_f64(b13))
+    np.testing.assert_array_equal(q13, r13[0])
+    np.testing.assert_array_equal(s13, r13[1])
+    y_q = oracle.forward(x, idx, w, (q13, s13), (q2, s2), mode=oracle.MXFP8)
+    y_d = oracle.forward(x, idx, w, oracle.mxfp8_dequantize(q13, s13),
+                         oracle.mxfp8_dequantize(q2, s2), mode=oracle.MXFP8)
+    np.testing.assert_array_equal(y_q, y_d)
+    dy = np.random.default_rng(1).standard_normal((T, H))
+    g_bits = oracle.backward(x, idx, w, b13, b2, dy)
+    g_wide = oracle.backward(x, idx, w, oracle.bf16_to_f64(b13), oracle.bf16_to_f64(b2), dy)
+    for a, b in zip(g_bits, g_wide):
+        np.testing.assert_array_equal(a, b)

@@ -1,0 +1,437 @@
+#!/usr/bin/env python
+"""Throughput of the deterministic MoE layer on GB300: prints one JSON line.
+
+A step is one pass of the whole hot path over one batch: top-k routing, schedule,
+forward (gather, gate/up GEMM + SwiGLU, down GEMM + scatter, weighted reduction) and
+backward (reverse-combine gather, G GEMM + SwiGLU backward + router-weight gradient,
+dgrad + reverse-dispatch + k-sum, weight gradients), on the 512-expert, H=4096, I=1024,
+top-10 shape with T=16384 tokens (BF16). Useful FLOPs per step: 6*R*H*I forward plus
+12*R*H*I backward, R = T*K.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mok|reference]
+
+Under torchrun (N > 1) every rank runs its own batch (weak scaling, no collective on the
+data path); timing is the max over ranks. `--impl reference` times the CPU oracle on a
+bounded sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import CONFIGS, synth  # noqa: E402
+
+METRIC = "MoE layer TFLOP/s fwd/bwd (BF16, MXFP8) on 1 GB300; % of tensor-core peak"
+UNIT = "TFLOP/s"
+WORKLOAD = "fwd_bf16"
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sust=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "mixture_experts_layer_deterministic_gb300", "csrc")
+    for fn in sorted(os.listdir(d)):
+        h.update(open(os.path.join(d, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            t = json.load(f)
+        if t.get("source_sha") != kernel_source_sha():
+            return None
+        return t["kernels"].get(kernel)
+    except Exception:
+        return None
+
+
+# algorithmic work per launch of each kernel kind, for a workload (R routed rows)
+def algorithmic(kind, c, n_launch_per_step):
+    R, H, I, T, K, E = c.R, c.H, c.I, c.T, c.K, c.E
+    tensor = {"gemm_up_swiglu": 4.0 * R * H * I, "gemm_down_push": 2.0 * R * H * I,
+              "gemm_g_swiglu_bwd": 2.0 * R * H * I, "gemm_dgrad_push": 4.0 * R * H * I,
+              "wgrad_w13": 4.0 * R * H * I, "wgrad_w2": 2.0 * R * H * I}
+    hbm = {"gather": 2.0 * R * H * 2, "combine": R * H * 4 + T * H * 4 + R * 4,
+           "dx_reduce": R * H * 4 + T * H * 4, "route_topk": T * E * 4 + T * K * 8,
+           "gather_bwd": 4.0 * R * H * 2}
+    if kind in tensor:
+        return "tensor", tensor[kind] / n_launch_per_step
+    if kind in hbm:
+        return "hbm", hbm[kind] / n_launch_per_step
+    return None, None
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_mok(args):
+    import torch
+    from mixture_experts_layer_deterministic_gb300 import binding as B
+    from mixture_experts_layer_deterministic_gb300.buffers import MoELayer, quantize_mxfp8
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    cfg = CONFIGS[WORKLOAD]
+    # weak scaling: each rank has its own tokens (seed shifted by rank), the same weights
+    cfg_r = cfg.with_(seed=cfg.seed + 1000 * rank) if rank else cfg
+    T, H, I, E, K = cfg.T, cfg.H, cfg.I, cfg.E, cfg.K
+    R = T * K
+
+    # pinned host inputs (the e2e leg copies these every step)
+    def pinned(shape, dtype):
+        return torch.empty(shape, dtype=dtype, pin_memory=True)
+
+    hx = pinned((T, H), torch.int16)
+    synth.make_x(cfg_r, out=hx.numpy().view(np.uint16))
+    hdy = pinned((T, H), torch.int16)
+    synth.make_dy(cfg_r, out=hdy.numpy().view(np.uint16))
+    hlg = torch.from_numpy(synth.make_logits(cfg_r)).pin_memory()
+    w13_host = synth.make_w13(cfg)
+    w2_host = synth.make_w2(cfg)
+    w13 = torch.from_numpy(w13_host.view(np.int16)).to(dev).view(torch.bfloat16)
+    w2 = torch.from_numpy(w2_host.view(np.int16)).to(dev).view(torch.bfloat16)
+    cpu_inputs = dict(w13=w13_host, w2=w2_host) if (rank == 0 and world == 1) else None
+    if cpu_inputs is None:
+        del w13_host, w2_host
+    x = hx.to(dev).view(torch.bfloat16)
+    dy = hdy.to(dev).view(torch.bfloat16)
+    lg = hlg.to(dev)
+
+    L = MoELayer(T, H, I, E, K, cfg.minibatch, cfg.ring_capacity, B.MOK_BF16, device=dev,
+                 backward=True)
+    y = torch.empty(T, H, dtype=torch.float32, device=dev)
+    pre = torch.empty(R, 2 * I, dtype=torch.float32, device=dev)
+    dx = torch.empty(T, H, dtype=torch.float32, device=dev)
+    dw13 = torch.empty(w13.shape, dtype=torch.float32, device=dev)
+    dw2 = torch.empty(w2.shape, dtype=torch.float32, device=dev)
+    dtk = torch.empty(R, dtype=torch.float32, device=dev)
+    dlg = torch.empty(T, E, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        L.route(lg, stream)
+        L.schedule(stream=stream)
+        L.forward(x, w13, w2, y, saved_preact=pre, stream=stream)
+
+    def bwd():
+        L.backward(x, pre, w13, w2, dy, dx, dw13, dw2, dtk, dlg, stream=stream)
+
+    def step():
+        fwd()
+        bwd()
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+
+    def timed(fn, n):
+        barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        barrier()
+        ms = a.elapsed_time(b) / n
+        if dist is not None:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    for _ in range(args.warmup):
+        step()
+    clocks = Clocks(local)
+    clocks.start()
+    ms = timed(step, args.steps)
+    clk = clocks.stop()
+    st, dstat = B.mok_read_device_status()
+    if st != B.MOK_OK or dstat != B.MOK_OK:
+        raise RuntimeError("device status %d/%d" % (st, dstat))
+
+    flops_step = cfg.fwd_flops() + cfg.bwd_flops()
+    value = world * flops_step / (ms * 1e-3) / 1e12
+
+    # per-kernel timing on the launching stream over a second timed region
+    B.check(B.mok_profile_enable(1))
+    timed(step, args.steps)
+    prof = B.mok_profile_read()
+    B.check(B.mok_profile_enable(0))
+    launches_per_step = sum(n for n, _ in prof.values()) / args.steps
+    kernels = {k: {"launches_per_step": n / args.steps, "avg_ms": t / n, "ms_per_step": t /
+                   args.steps, "share": t / max(1e-9, sum(v[1] for v in prof.values()))}
+               for k, (n, t) in prof.items()}
+    dom = max(prof, key=lambda k: prof[k][1])
+    pk = peaks()
+    n_l = prof[dom][0] / args.steps
+    bound, work = algorithmic(dom, cfg, n_l)
+    avg_s = prof[dom][1] / prof[dom][0] * 1e-3
+    if bound == "tensor":
+        achieved = work / avg_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_sust"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_sust"],
+                "peak_kind": "bf16 sustained, " + pk["src"]}
+    else:
+        achieved = work / avg_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                "frac": achieved / pk["hbm"], "peak_kind": "hbm copy, " + pk["src"]}
+    roof["kernel"] = dom
+    roof["traffic"] = ncu_traffic(dom)
+
+    # phases: forward alone, backward alone, MXFP8 forward
+    phases = {}
+    ms_f = timed(fwd, args.steps)
+    phases["fwd_bf16"] = {"ms": ms_f, "tflops": cfg.fwd_flops() / (ms_f * 1e-3) / 1e12}
+    ms_b = timed(bwd, args.steps)
+    phases["bwd_bf16"] = {"ms": ms_b, "tflops": cfg.bwd_flops() / (ms_b * 1e-3) / 1e12}
+    if not args.no_mxfp8:
+        q13, s13 = quantize_mxfp8(w13)
+        q2, s2 = quantize_mxfp8(w2)
+        Lm = MoELayer(T, H, I, E, K, cfg.minibatch, cfg.ring_capacity, B.MOK_MXFP8, device=dev)
+
+        def fwd_mx():
+            Lm.route(lg, stream)
+            Lm.schedule(stream=stream)
+            Lm.forward(x, q13, q2, y, s13, s2, stream=stream)
+
+        for _ in range(2):
+            fwd_mx()
+        ms_m = timed(fwd_mx, args.steps)
+        phases["fwd_mxfp8"] = {"ms": ms_m, "tflops": cfg.fwd_flops() / (ms_m * 1e-3) / 1e12}
+        del Lm, q13, s13, q2, s2
+
+    # e2e through the public API with host buffers: H2D of the step's inputs, D2H of y, dx
+    hy = pinned((T, H), torch.float32)
+    hdx = pinned((T, H), torch.float32)
+    xi, dyi = x.view(torch.int16), dy.view(torch.int16)
+
+    def e2e_step():
+        xi.copy_(hx, non_blocking=True)
+        lg.copy_(hlg, non_blocking=True)
+        dyi.copy_(hdy, non_blocking=True)
+        step()
+        hy.copy_(y, non_blocking=True)
+        hdx.copy_(dx, non_blocking=True)
+
+    e2e_step()
+    ms_e = timed(e2e_step, args.steps)
+    h2d = hx.numel() * 2 + hlg.numel() * 4 + hdy.numel() * 2
+    d2h = hy.numel() * 4 + hdx.numel() * 4
+
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Gaussian)",
+        "config": {"workload": "fwd+bwd BF16, 512 experts, H=4096, I=1024, top-10, T=16384",
+                   "T": T, "H": H, "I": I, "E": E, "K": K, "minibatch": cfg.minibatch,
+                   "ring_capacity": "all rows", "l2": "inputs larger than L2 (12.9 GB of "
+                   "expert weights read per step)", "parallelism": "replicas" if world > 1
+                   else "single GPU"},
+        "e2e": {"value": world * flops_step / (ms_e * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e},
+        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "roofline": roof,
+        "phases": phases,
+        "kernels": kernels,
+        "clocks": clk,
+        "peaks": pk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(cfg, cpu_inputs, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(cfg, host, n_tokens, n_experts):
+    """Times the oracle on a bounded sample: the forward of n_tokens tokens (with all their
+    K experts) and the backward of every routed row of n_experts experts. Returns
+    (useful FLOPs, seconds, description)."""
+    import oracle
+    lg = synth.make_logits(cfg)
+    idx, w = oracle.route(lg.astype(np.float64), cfg.K)
+    x = host.get("x")
+    if x is None:
+        x = synth.make_x(cfg)
+    toks = np.arange(n_tokens)
+    idx_s = idx[toks]
+    used = np.unique(idx_s)
+    remap = np.full(cfg.E, -1, np.int32)
+    remap[used] = np.arange(len(used), dtype=np.int32)
+    w13, w2 = host["w13"], host["w2"]
+    t0 = time.perf_counter()
+    oracle.forward(oracle.bf16_to_f64(x[toks]), remap[idx_s], w[toks], w13[used], w2[used],
+                   mode=oracle.BF16)
+    t_fwd = time.perf_counter() - t0
+    flops = 6.0 * n_tokens * cfg.K * cfg.H * cfg.I
+    dy = synth.make_dy(cfg)
+    t_bwd = 0.0
+    rows = 0
+    for e in range(n_experts):
+        t_e, k_e = np.nonzero(idx == e)
+        t0 = time.perf_counter()
+        oracle.backward(oracle.bf16_to_f64(x[t_e]), np.zeros((len(t_e), 1), np.int32),
+                        w[t_e, k_e][:, None], w13[e:e + 1], w2[e:e + 1],
+                        oracle.bf16_to_f64(dy[t_e]), mode=oracle.BF16)
+        t_bwd += time.perf_counter() - t0
+        rows += len(t_e)
+    flops += 12.0 * rows * cfg.H * cfg.I
+    desc = ("forward of %d tokens (%d routed rows) + backward of all %d routed rows of "
+            "experts 0..%d" % (n_tokens, n_tokens * cfg.K, rows, n_experts - 1))
+    return flops, t_fwd + t_bwd, desc
+
+
+def cores():
+    n = os.environ.get("OMP_NUM_THREADS")
+    return int(n) if n else (os.cpu_count() or 1)
+
+
+def cpu_baseline(cfg, host, budget_s=20.0):
+    flops, sec, desc = oracle_sample(cfg, host, 8, 1)   # calibration
+    rate = flops / sec
+    # size the sample to about budget_s seconds
+    n_tok = int(max(8, min(cfg.T, 8 * budget_s / 2 / max(sec, 1e-3))))
+    n_exp = int(max(1, min(cfg.E, budget_s / 2 / max(sec, 1e-3))))
+    flops, sec, desc = oracle_sample(cfg, host, n_tok, n_exp)
+    return {"value": flops / sec / 1e12, "unit": UNIT, "cores": cores(), "kind": "oracle",
+            "sample": desc, "seconds": sec, "calibration_tflops": rate / 1e12}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg = CONFIGS[WORKLOAD]
+    host = dict(w13=synth.make_w13(cfg), w2=synth.make_w2(cfg), x=synth.make_x(cfg))
+    n_tok, n_exp = args.ref_tokens, args.ref_experts
+    for _ in range(args.warmup):
+        oracle_sample(cfg, host, n_tok, n_exp)
+    tot_f, tot_s, desc = 0.0, 0.0, ""
+    for _ in range(args.steps):
+        f, s, desc = oracle_sample(cfg, host, n_tok, n_exp)
+        tot_f += f
+        tot_s += s
+    value = tot_f / tot_s / 1e12
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": tot_s / args.steps * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded Gaussian)", "impl": "reference",
+           "config": {"workload": "fwd+bwd BF16, 512 experts, H=4096, I=1024, top-10, "
+                                  "T=16384 (bounded sample per step)"},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "kind": "oracle",
+                            "sample": desc},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="mok", choices=["mok", "reference"])
+    ap.add_argument("--no-mxfp8", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--ref-tokens", type=int, default=16)
+    ap.add_argument("--ref-experts", type=int, default=1)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "mok":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_mok(args)
+
+
+if __name__ == "__main__":
+    main()

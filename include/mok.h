@@ -1,0 +1,218 @@
+/*
+ * mok.h -- C ABI of the deterministic MoE layer core for one GB300 (sm_103a).
+ *
+ * The layer: top-k routing over router logits, a deterministic expert schedule, a
+ * pull-style gather of token rows into expert order, an expert-grouped SwiGLU FFN
+ * (gate/up GEMM, SwiGLU, down GEMM), a push-style scatter of expert outputs back to
+ * (token, k) slots and a fixed-order router-weighted reduction; plus the matching
+ * backward pass. Every expert lives on this one GPU, so dispatch and combine are HBM
+ * gathers and scatters.
+ *
+ * Pages cited (by title and section):
+ *   [arex]     "Cursor 放出 MoK：NVL72 训练提速 2.37 倍" (arex-research.com)
+ *   [aigwx]    "Cursor 开源 MoK：面向 GB300 NVL72 的确定性 MoE 训练内核，性能提升 2.37 倍" (aigwx.org)
+ *   [alphalab] "Mixture-of-Kittens" analysis (alphalab.site)
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, 16-byte aligned,
+ *    row-major and densely packed. The library allocates no device memory: scratch
+ *    space comes from the caller's workspace (sized by mok_workspace_size).
+ *  - Work is enqueued on `stream` and returns without waiting for the GPU. Only
+ *    mok_read_device_status synchronises.
+ *  - Arguments are validated on the host before anything is enqueued; a non-OK status
+ *    means nothing was enqueued. Problems the GPU detects (an index out of range, a
+ *    bounded wait that ran out) are recorded in a device status word that
+ *    mok_read_device_status returns; the kernel that found them skips the bad access.
+ *  - Same inputs give bitwise-identical outputs, run to run: no floating-point sum
+ *    depends on thread or block scheduling ([alphalab] section 二: operator-level
+ *    run-to-run bitwise determinism through a fixed floating-point operation order).
+ *  - Only compute capability 10.3 is accepted ([alphalab] section 四: the functional API
+ *    rejects anything but SM103); other devices get MOK_ERR_UNSUPPORTED.
+ *
+ * Shapes: T tokens, H hidden, I expert intermediate, E experts, K experts per token,
+ * R = T*K routed rows. Limits: 1 <= K <= min(E, 32), E <= 1024, H and I multiples of 128,
+ * H <= 16384, I <= 8192, R < 2^31.
+ */
+#ifndef MOK_H
+#define MOK_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOK_ABI_VERSION 1u
+
+typedef enum mok_status {
+    MOK_OK = 0,
+    MOK_ERR_INVALID_ARG = 1,      /* shape, pointer, alignment or null-pointer error */
+    MOK_ERR_UNSUPPORTED = 2,      /* device is not compute capability 10.3 */
+    MOK_ERR_WORKSPACE = 3,        /* workspace missing or smaller than mok_workspace_size */
+    MOK_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
+    MOK_ERR_TIMEOUT = 5,          /* (device) a bounded wait inside a kernel ran out */
+    MOK_ERR_DEVICE_INVARIANT = 6, /* (device) an index or count was out of range */
+    MOK_ERR_ABI = 7               /* cfg->abi_version != MOK_ABI_VERSION */
+} mok_status;
+
+typedef enum mok_precision {
+    MOK_BF16 = 0, /* bf16 operands, fp32 accumulation */
+    MOK_MXFP8 = 1 /* E4M3 operands with an E8M0 scale per 32 elements along K */
+} mok_precision;
+
+typedef enum mok_workspace_kind {
+    MOK_WS_SCHEDULE = 0,
+    MOK_WS_FORWARD = 1,
+    MOK_WS_BACKWARD = 2
+} mok_workspace_kind;
+
+/* Layer configuration. minibatch and ring_capacity are two of the pages' tunables
+ * ([alphalab] section 四: forward/backward communication SMs, minibatch, macrobatch and
+ * schedule capacity; the communication-SM knobs have no meaning on one GPU). */
+typedef struct mok_config {
+    uint32_t abi_version; /* MOK_ABI_VERSION */
+    int32_t T, H, I, E, K;
+    /* Routed rows (of the expert-sorted stream) per minibatch, >= 1. The pages suggest a
+     * size that fills at least two SM waves per grouped GEMM ([arex] section "pull 代替
+     * push", point 3: about 2,368 tokens for one shape). */
+    int32_t minibatch;
+    /* Rows of the fixed-size dispatch ring ("macrobatch", [arex] section "pull 代替 push",
+     * point 2). 0, or any value >= R, means the ring holds every routed row and the
+     * forward runs as one pass. Otherwise the ring is floor(ring_capacity / minibatch)
+     * minibatch slots (at least one: ring_capacity >= minibatch is required), minibatch m
+     * uses slot m mod slots, and the forward runs one pass per minibatch. No routed row is
+     * ever dropped. */
+    int32_t ring_capacity;
+    int32_t prec; /* mok_precision of the forward; the backward is MOK_BF16 */
+} mok_config;
+
+/* The schedule table ([arex] section "pull 代替 push": one schedule serves dispatch,
+ * combine, reverse-combine and reverse-dispatch). All device arrays, caller-owned:
+ *   counts  [E]      routed rows per expert
+ *   offsets [E+1]    exclusive prefix sum of counts (offsets[E] = R)
+ *   perm    [R]      sorted row -> flat routed id f = t*K + k; rows are grouped by expert,
+ *                    and within an expert ordered by ascending f (a stable sort)
+ *   inv     [R]      flat id f -> sorted row (inverse of perm)
+ *   segs    [cap][3] (expert, row_begin, row_end): the non-empty intersections of each
+ *                    expert's rows with the minibatch ranges [m*MB, (m+1)*MB), in
+ *                    increasing row order; cap = mok_segment_capacity(cfg)
+ *   n_segs  [1]      number of valid segs entries */
+typedef struct mok_schedule {
+    int32_t *counts;
+    int32_t *offsets;
+    int32_t *perm;
+    int32_t *inv;
+    int32_t *segs;
+    int32_t *n_segs;
+} mok_schedule;
+
+/* ---- helpers (host only, no GPU work) ---------------------------------------------- */
+
+uint32_t mok_abi_version(void);
+const char *mok_status_string(mok_status s);
+
+/* Validates a configuration (shapes, limits, ABI version) without touching the GPU. */
+mok_status mok_check_config(const mok_config *cfg);
+
+/* Upper bound on the number of schedule segments: E + ceil(R / minibatch) - 1 (at least 1). */
+int64_t mok_segment_capacity(const mok_config *cfg);
+
+/* Bytes of device workspace that mok_build_schedule / mok_forward / mok_backward need
+ * (which = mok_workspace_kind). Returns 0 for an invalid configuration. The workspace
+ * must be 256-byte aligned; its contents on entry do not matter. */
+size_t mok_workspace_size(const mok_config *cfg, int which);
+
+/* ---- the hot path --------------------------------------------------------------- */
+
+/* Top-k routing ([alphalab] section 四: top-k over router logits).
+ * logits   [T][E] fp32.
+ * topk_idx [T][K] int32 out: the K largest logits of each token, ordered by logit
+ *          descending; equal logits (with -0 equal to +0) go to the lower expert id.
+ * topk_w   [T][K] fp32 out: softmax over the K chosen logits (fp32 arithmetic).
+ * Logits must be finite; NaN or infinite logits give unspecified (but in-range) ids. */
+mok_status mok_route_topk(const mok_config *cfg, const float *logits, int32_t *topk_idx,
+                          float *topk_w, cudaStream_t stream);
+
+/* Deterministic expert schedule from topk_idx [T][K] (values in [0, E); an id out of range
+ * is counted nowhere and raises MOK_ERR_DEVICE_INVARIANT in the device status). Fills
+ * every array of *sched. Bit-exact and run-to-run identical. */
+mok_status mok_build_schedule(const mok_config *cfg, const int32_t *topk_idx,
+                              const mok_schedule *sched, void *ws, size_t ws_bytes,
+                              cudaStream_t stream);
+
+/* Layer forward: gather -> gate/up GEMM + SwiGLU -> down GEMM -> scatter -> reduction
+ * ([alphalab] section 一: pull dispatch, expert FFN/SwiGLU, push combine; section 二: the
+ * final router-weighted reduction; section 三: that is the timed layer).
+ *   x       [T][H] bf16 token activations.
+ *   topk_w  [T][K] fp32 routing weights (from mok_route_topk).
+ *   BF16:  w13 [E][2I][H] bf16 (rows 0..I-1 gate, I..2I-1 up), w2 [E][H][I] bf16,
+ *          w13_scale = w2_scale = NULL. h = silu(gate)*up is rounded to bf16, the down
+ *          GEMM's operand type.
+ *   MXFP8: w13 [E][2I][H] E4M3 bytes with w13_scale [E][2I][H/32] E8M0 bytes, and
+ *          w2 [E][H][I] E4M3 with w2_scale [E][H][I/32] (as made by mok_quantize_mxfp8);
+ *          x is quantized to MXFP8 along H inside the gather and h along I inside the
+ *          gate/up GEMM's epilogue ([arex] section "pull 代替 push": weights pre-quantized,
+ *          activation quantization fused into dispatch, GEMM and SwiGLU).
+ *   y       [T][H] fp32 out: y[t] = sum over k = 0..K-1, in that order, of
+ *           topk_w[t,k] * o[t,k], fp32 throughout (o is the fp32 down-GEMM result).
+ *   saved_preact  NULL, or [R][2I] fp32 out: the gate/up GEMM result of sorted row r
+ *           (needed by mok_backward; BF16 only).
+ * GEMMs accumulate in fp32; values that are only stored (expert outputs, saved
+ * pre-activations) stay fp32. */
+mok_status mok_forward(const mok_config *cfg, const void *x, const mok_schedule *sched,
+                       const float *topk_w, const void *w13, const uint8_t *w13_scale,
+                       const void *w2, const uint8_t *w2_scale, void *y, void *saved_preact,
+                       void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Layer backward (BF16): reverse-combine gather of dy -> G = dy W2 with the SwiGLU
+ * backward and the router-weight gradient in its epilogue -> dgrad and reverse-dispatch
+ * scatter with a fixed-order k-sum -> weight gradients ([arex] section "pull 代替 push":
+ * pull reverse-combine, push reverse-dispatch, router-weight gradient fused into the
+ * SwiGLU backward; [alphalab] section 一: expert gradient computation).
+ *   x, topk_w, w13, w2 as in mok_forward (BF16), saved_preact [R][2I] fp32 from
+ *   mok_forward, dy [T][H] bf16 upstream gradient.
+ *   dx       [T][H] fp32 out (sum over k in order of the fp32 per-slot dgrad results).
+ *   dw13     [E][2I][H] fp32 out, dw2 [E][H][I] fp32 out (experts with no rows get 0).
+ *   d_topk_w [T][K] fp32 out: dL/dtopk_w.
+ *   d_logits NULL or [T][E] fp32 out: gradient through the top-k softmax (0 for logits
+ *            that were not chosen).
+ * The GEMM operands dA = dL/d(gate,up) and topk_w*h are rounded to bf16. */
+mok_status mok_backward(const mok_config *cfg, const void *x, const mok_schedule *sched,
+                        const float *topk_w, const void *saved_preact, const void *w13,
+                        const void *w2, const void *dy, void *dx, void *dw13, void *dw2,
+                        float *d_topk_w, float *d_logits, void *ws, size_t ws_bytes,
+                        cudaStream_t stream);
+
+/* MXFP8 quantization of a bf16 matrix along its rows ([arex] section "pull 代替 push":
+ * pre-quantized weights). src [rows][cols] bf16 -> q [rows][cols] E4M3, scale
+ * [rows][cols/32] E8M0: per 32-element block, scale = 2^(floor(log2 amax) - 8) clamped to
+ * [2^-127, 2^127] (byte 0 for an all-zero block); q = E4M3(value / scale), round to
+ * nearest even, saturating at +-448. cols must be a multiple of 32. */
+mok_status mok_quantize_mxfp8(const void *src_bf16, int64_t rows, int32_t cols, uint8_t *q,
+                              uint8_t *scale, cudaStream_t stream);
+
+/* ---- instrumentation ------------------------------------------------------------ */
+
+/* Per-kernel timing. While enabled (on != 0), each kernel (or fixed group of kernels) that
+ * the entry points launch is bracketed by a pair of CUDA events recorded on the caller's
+ * stream; enabling clears the record. Host-side only, off by default, not thread-safe. */
+mok_status mok_profile_enable(int on);
+
+/* Waits for the recorded events and reports, for up to `max` kernel kinds that launched at
+ * least once since mok_profile_enable(1): the kind's name (static storage), its number of
+ * kernel launches and the summed milliseconds of its event pairs. *n_kinds receives the
+ * number of such kinds (it may exceed max). */
+mok_status mok_profile_read(int32_t max, int32_t *n_kinds, const char **names,
+                            int64_t *launches, double *ms);
+
+/* Waits for the device, returns the first device-side error recorded since the last
+ * clear (MOK_OK if none) in *out, and returns MOK_ERR_CUDA if the wait itself failed. */
+mok_status mok_read_device_status(mok_status *out);
+mok_status mok_clear_device_status(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOK_H */

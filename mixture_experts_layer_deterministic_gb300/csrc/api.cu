@@ -1,0 +1,380 @@
+// api.cu -- the C ABI entry points (include/mok.h): argument validation, workspace layout
+// and the stream-ordered sequence of kernels for each call.
+#include <string.h>
+
+#include "common.cuh"
+#include "mok_internal.h"
+
+using namespace mok;
+
+// ---------------------------------------------------------------- device status word
+static __device__ int g_status;
+
+namespace {
+
+constexpr int MAX_DEV = 64;
+int g_cc_ok[MAX_DEV];        // 0 unknown, 1 ok, 2 unsupported
+int *g_status_ptr[MAX_DEV];  // device address of g_status, per device
+
+mok_status check_device(int **status) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) return MOK_ERR_CUDA;
+    if (g_cc_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return MOK_ERR_CUDA;
+        g_cc_ok[dev] = (major == 10 && minor == 3) ? 1 : 2;
+        if (g_cc_ok[dev] == 1) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return MOK_ERR_CUDA;
+            g_status_ptr[dev] = (int *)p;
+        }
+    }
+    if (g_cc_ok[dev] != 1) return MOK_ERR_UNSUPPORTED;
+    *status = g_status_ptr[dev];
+    return MOK_OK;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int64_t rows_R(const mok_config *c) { return (int64_t)c->T * c->K; }
+
+// ring geometry: n_slots == 0 means the ring holds every routed row
+void ring_geom(const mok_config *c, int32_t *n_slots, int64_t *ring_rows) {
+    const int64_t R = rows_R(c);
+    if (c->ring_capacity == 0 || (int64_t)c->ring_capacity >= R) {
+        *n_slots = 0;
+        *ring_rows = R;
+    } else {
+        *n_slots = c->ring_capacity / c->minibatch;
+        *ring_rows = (int64_t)(*n_slots) * c->minibatch;
+    }
+}
+
+// ---------------------------------------------------------------- workspace layouts
+struct Carver {
+    char *base;
+    size_t off = 0;
+    template <class T>
+    T *take(size_t bytes) {
+        off = (off + 255) & ~(size_t)255;
+        T *p = base ? (T *)(base + off) : nullptr;
+        off += bytes;
+        return p;
+    }
+};
+
+struct FwdWs {
+    int32_t *tiles;  // points past a 16-byte header holding the count
+    int64_t tiles_cap;
+    void *xring;
+    uint8_t *xring_s;
+    void *hring;
+    uint8_t *hring_s;
+    float *slots;
+};
+
+size_t carve_fwd(const mok_config *c, void *ws, FwdWs *o) {
+    Carver cv{(char *)ws};
+    const int64_t R = rows_R(c);
+    int32_t ns;
+    int64_t rr;
+    ring_geom(c, &ns, &rr);
+    const int64_t pass_rows = ns == 0 ? R : c->minibatch;
+    const bool mx = c->prec == MOK_MXFP8;
+    const int esz = mx ? 1 : 2;
+    FwdWs w;
+    // the smallest tile height in use bounds the tile count
+    w.tiles_cap = tile_list_cap(pass_rows, c->E, gemm_tile_rows());
+    int32_t *t = cv.take<int32_t>(16 + (size_t)w.tiles_cap * 16);
+    w.tiles = t ? t + 4 : nullptr;
+    w.xring = cv.take<void>((size_t)rr * c->H * esz);
+    w.xring_s = mx ? cv.take<uint8_t>((size_t)rr * (c->H / 32)) : nullptr;
+    w.hring = cv.take<void>((size_t)rr * c->I * esz);
+    w.hring_s = mx ? cv.take<uint8_t>((size_t)rr * (c->I / 32)) : nullptr;
+    w.slots = cv.take<float>((size_t)R * c->H * 4);
+    if (o) *o = w;
+    return cv.off;
+}
+
+struct BwdWs {
+    int32_t *poff;
+    int32_t *tiles;
+    int64_t tiles_cap;
+    int64_t rpad_cap;
+    uint16_t *dy_perm, *x_perm, *dA, *sh;
+    float *dx_slots;
+    float *dS_part;
+};
+
+size_t carve_bwd(const mok_config *c, void *ws, BwdWs *o) {
+    Carver cv{(char *)ws};
+    const int64_t R = rows_R(c);
+    BwdWs w;
+    w.rpad_cap = R + 15 * (int64_t)c->E;
+    w.poff = cv.take<int32_t>((size_t)(c->E + 1) * 4);
+    w.tiles_cap = tile_list_cap(R, c->E, gemm_tile_rows());
+    int32_t *t = cv.take<int32_t>(16 + (size_t)w.tiles_cap * 16);
+    w.tiles = t ? t + 4 : nullptr;
+    w.dy_perm = cv.take<uint16_t>((size_t)w.rpad_cap * c->H * 2);
+    w.x_perm = cv.take<uint16_t>((size_t)w.rpad_cap * c->H * 2);
+    w.dA = cv.take<uint16_t>((size_t)w.rpad_cap * 2 * c->I * 2);
+    w.sh = cv.take<uint16_t>((size_t)w.rpad_cap * c->I * 2);
+    w.dS_part = cv.take<float>((size_t)R * (c->I / 128) * 4);
+    w.dx_slots = cv.take<float>((size_t)R * c->H * 4);
+    if (o) *o = w;
+    return cv.off;
+}
+
+mok_status check_ws(void *ws, size_t ws_bytes, size_t need) {
+    if (need == 0) return MOK_OK;
+    if (ws == nullptr || ws_bytes < need) return MOK_ERR_WORKSPACE;
+    if (((uintptr_t)ws & 255u) != 0) return MOK_ERR_WORKSPACE;
+    return MOK_OK;
+}
+
+mok_status check_sched(const mok_config *c, const mok_schedule *s) {
+    if (s == nullptr) return MOK_ERR_INVALID_ARG;
+    const void *ps[] = {s->counts, s->offsets, s->perm, s->inv, s->segs, s->n_segs};
+    for (const void *p : ps)
+        if (p == nullptr) return MOK_ERR_INVALID_ARG;
+    (void)c;
+    return MOK_OK;
+}
+
+}  // namespace
+
+// a launch of `nk` kernels of one kind, bracketed by events while profiling is on
+#define MOK_LAUNCH(kind, nk, expr)                         \
+    do {                                                   \
+        prof_begin(kind, stream);                          \
+        cudaError_t _e = (expr);                           \
+        prof_end(kind, stream, nk);                        \
+        if (_e != cudaSuccess) return MOK_ERR_CUDA;        \
+    } while (0)
+
+extern "C" {
+
+uint32_t mok_abi_version(void) { return MOK_ABI_VERSION; }
+
+const char *mok_status_string(mok_status s) {
+    switch (s) {
+        case MOK_OK: return "ok";
+        case MOK_ERR_INVALID_ARG: return "invalid argument";
+        case MOK_ERR_UNSUPPORTED: return "unsupported device (compute capability 10.3 required)";
+        case MOK_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case MOK_ERR_CUDA: return "CUDA runtime error";
+        case MOK_ERR_TIMEOUT: return "device wait timed out";
+        case MOK_ERR_DEVICE_INVARIANT: return "device-side invariant violated";
+        case MOK_ERR_ABI: return "ABI version mismatch";
+    }
+    return "unknown status";
+}
+
+mok_status mok_check_config(const mok_config *c) {
+    if (c == nullptr) return MOK_ERR_INVALID_ARG;
+    if (c->abi_version != MOK_ABI_VERSION) return MOK_ERR_ABI;
+    if (c->T < 0 || c->E < 1 || c->E > 1024 || c->K < 1 || c->K > 32 || c->K > c->E)
+        return MOK_ERR_INVALID_ARG;
+    if (c->H < 128 || c->H > 16384 || c->H % 128 != 0) return MOK_ERR_INVALID_ARG;
+    if (c->I < 128 || c->I > 8192 || c->I % 128 != 0) return MOK_ERR_INVALID_ARG;
+    if (c->minibatch < 1) return MOK_ERR_INVALID_ARG;
+    if ((int64_t)c->T * c->K >= ((int64_t)1 << 31) - 16 * 1024) return MOK_ERR_INVALID_ARG;
+    if (c->ring_capacity < 0) return MOK_ERR_INVALID_ARG;
+    if (c->ring_capacity != 0 && (int64_t)c->ring_capacity < rows_R(c) &&
+        c->ring_capacity < c->minibatch)
+        return MOK_ERR_INVALID_ARG;
+    if (c->prec != MOK_BF16 && c->prec != MOK_MXFP8) return MOK_ERR_INVALID_ARG;
+    return MOK_OK;
+}
+
+int64_t mok_segment_capacity(const mok_config *c) {
+    if (mok_check_config(c) != MOK_OK) return 0;
+    const int64_t R = rows_R(c);
+    const int64_t cap = (int64_t)c->E + (R + c->minibatch - 1) / c->minibatch - 1;
+    return cap > 0 ? cap : 1;
+}
+
+size_t mok_workspace_size(const mok_config *c, int which) {
+    if (mok_check_config(c) != MOK_OK) return 0;
+    switch (which) {
+        case MOK_WS_SCHEDULE: return schedule_ws_bytes(rows_R(c), c->E);
+        case MOK_WS_FORWARD: return carve_fwd(c, nullptr, nullptr);
+        case MOK_WS_BACKWARD: return carve_bwd(c, nullptr, nullptr);
+    }
+    return 0;
+}
+
+mok_status mok_route_topk(const mok_config *c, const float *logits, int32_t *topk_idx,
+                          float *topk_w, cudaStream_t stream) {
+    mok_status st = mok_check_config(c);
+    if (st != MOK_OK) return st;
+    int *status;
+    if ((st = check_device(&status)) != MOK_OK) return st;
+    if (c->T == 0) return MOK_OK;
+    if (!logits || !topk_idx || !topk_w) return MOK_ERR_INVALID_ARG;
+    if (!aligned16(logits) || !aligned16(topk_idx) || !aligned16(topk_w))
+        return MOK_ERR_INVALID_ARG;
+    MOK_LAUNCH(KK_ROUTE, 1,
+               launch_route_topk(logits, c->T, c->E, c->K, topk_idx, topk_w, status, stream));
+    return MOK_OK;
+}
+
+mok_status mok_build_schedule(const mok_config *c, const int32_t *topk_idx,
+                              const mok_schedule *sch, void *ws, size_t ws_bytes,
+                              cudaStream_t stream) {
+    mok_status st = mok_check_config(c);
+    if (st != MOK_OK) return st;
+    int *status;
+    if ((st = check_device(&status)) != MOK_OK) return st;
+    if ((st = check_sched(c, sch)) != MOK_OK) return st;
+    const int64_t R = rows_R(c);
+    if (R > 0 && (topk_idx == nullptr || !aligned16(topk_idx))) return MOK_ERR_INVALID_ARG;
+    if ((st = check_ws(ws, ws_bytes, schedule_ws_bytes(R, c->E))) != MOK_OK) return st;
+    ScheduleWs w = schedule_ws_carve(ws, R, c->E);
+    MOK_LAUNCH(KK_SCHEDULE, R > 0 ? 4 : 1,
+               launch_build_schedule(topk_idx, R, c->E, c->minibatch, *sch, w, status, stream));
+    return MOK_OK;
+}
+
+mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *sch,
+                       const float *topk_w, const void *w13, const uint8_t *w13_scale,
+                       const void *w2, const uint8_t *w2_scale, void *y, void *saved_preact,
+                       void *ws, size_t ws_bytes, cudaStream_t stream) {
+    mok_status st = mok_check_config(c);
+    if (st != MOK_OK) return st;
+    int *status;
+    if ((st = check_device(&status)) != MOK_OK) return st;
+    if ((st = check_sched(c, sch)) != MOK_OK) return st;
+    const bool mx = c->prec == MOK_MXFP8;
+    if (!x || !topk_w || !w13 || !w2 || !y) return MOK_ERR_INVALID_ARG;
+    if (mx && (!w13_scale || !w2_scale || saved_preact)) return MOK_ERR_INVALID_ARG;
+    if (!mx && (w13_scale || w2_scale)) return MOK_ERR_INVALID_ARG;
+    const void *ps[] = {x, topk_w, w13, w2, y, w13_scale, w2_scale, saved_preact};
+    for (const void *p : ps)
+        if (p && !aligned16(p)) return MOK_ERR_INVALID_ARG;
+    const size_t need = carve_fwd(c, nullptr, nullptr);
+    if ((st = check_ws(ws, ws_bytes, need)) != MOK_OK) return st;
+    const int64_t R = rows_R(c);
+    if (R == 0) return MOK_OK;
+    FwdWs w;
+    carve_fwd(c, ws, &w);
+    int32_t n_slots;
+    int64_t ring_rows;
+    ring_geom(c, &n_slots, &ring_rows);
+    Ring ring{R, c->minibatch, n_slots};
+    const int64_t n_pass = n_slots == 0 ? 1 : (R + c->minibatch - 1) / c->minibatch;
+    for (int64_t m = 0; m < n_pass; ++m) {
+        const int64_t p0 = n_slots == 0 ? 0 : m * c->minibatch;
+        const int64_t p1 = n_slots == 0 ? R : (p0 + c->minibatch < R ? p0 + c->minibatch : R);
+        MOK_LAUNCH(KK_TILES, 1,
+                   launch_build_tiles(sch->offsets, c->E, p0, p1, gemm_tile_rows(), w.tiles,
+                                      w.tiles_cap, status, stream));
+        if (!mx)
+            MOK_LAUNCH(KK_GATHER, 1,
+                       launch_gather_bf16((const uint16_t *)x, sch->perm, c->K, c->H, p0, p1, R,
+                                          c->minibatch, n_slots, (uint16_t *)w.xring, stream));
+        else
+            MOK_LAUNCH(KK_GATHER, 1,
+                       launch_gather_mxfp8((const uint16_t *)x, sch->perm, c->K, c->H, p0, p1,
+                                           R, c->minibatch, n_slots, (uint8_t *)w.xring,
+                                           w.xring_s, stream));
+        GemmUpArgs ua{w.tiles, w.tiles_cap, w.xring, w.xring_s, w13, w13_scale, w.hring,
+                      w.hring_s, (float *)saved_preact, c->H, c->I, c->E, mx, ring, status};
+        MOK_LAUNCH(KK_GEMM_UP, 1, launch_gemm_up(ua, stream));
+        GemmDownArgs da{w.tiles, w.tiles_cap, w.hring, w.hring_s, w2, w2_scale, sch->perm,
+                        w.slots, c->H, c->I, c->E, mx, ring, status};
+        MOK_LAUNCH(KK_GEMM_DOWN, 1, launch_gemm_down(da, stream));
+    }
+    MOK_LAUNCH(KK_COMBINE, 1,
+               launch_combine(w.slots, topk_w, c->T, c->K, c->H, (float *)y, stream));
+    return MOK_OK;
+}
+
+mok_status mok_backward(const mok_config *c, const void *x, const mok_schedule *sch,
+                        const float *topk_w, const void *saved_preact, const void *w13,
+                        const void *w2, const void *dy, void *dx, void *dw13, void *dw2,
+                        float *d_topk_w, float *d_logits, void *ws, size_t ws_bytes,
+                        cudaStream_t stream) {
+    mok_status st = mok_check_config(c);
+    if (st != MOK_OK) return st;
+    int *status;
+    if ((st = check_device(&status)) != MOK_OK) return st;
+    if ((st = check_sched(c, sch)) != MOK_OK) return st;
+    if (c->prec != MOK_BF16) return MOK_ERR_INVALID_ARG;
+    if (!x || !topk_w || !saved_preact || !w13 || !w2 || !dy || !dx || !dw13 || !dw2 ||
+        !d_topk_w)
+        return MOK_ERR_INVALID_ARG;
+    const void *ps[] = {x, topk_w, saved_preact, w13, w2, dy, dx, dw13, dw2, d_topk_w, d_logits};
+    for (const void *p : ps)
+        if (p && !aligned16(p)) return MOK_ERR_INVALID_ARG;
+    const size_t need = carve_bwd(c, nullptr, nullptr);
+    if ((st = check_ws(ws, ws_bytes, need)) != MOK_OK) return st;
+    const int64_t R = rows_R(c);
+    BwdWs w;
+    carve_bwd(c, ws, &w);
+    const int E = c->E, H = c->H, I = c->I, K = c->K;
+    MOK_LAUNCH(KK_PAD, 1, launch_pad_offsets(sch->counts, E, w.poff, stream));
+    MOK_LAUNCH(KK_TILES, 1,
+               launch_build_tiles(sch->offsets, E, 0, R, gemm_tile_rows(), w.tiles, w.tiles_cap,
+                                  status, stream));
+    MOK_LAUNCH(KK_GATHER_BWD, 1,
+               launch_gather_bwd((const uint16_t *)dy, (const uint16_t *)x, sch->perm,
+                                 sch->offsets, w.poff, E, K, H, w.rpad_cap, w.dy_perm, w.x_perm,
+                                 stream));
+    GemmGArgs ga{w.tiles, w.tiles_cap, sch->offsets, w.poff, (const uint16_t *)w2, w.dy_perm,
+                 (const float *)saved_preact, sch->perm, topk_w, w.dA, w.sh, w.dS_part, H, I,
+                 status};
+    MOK_LAUNCH(KK_GEMM_G, 1, launch_gemm_g(ga, stream));
+    MOK_LAUNCH(KK_ROUTER_GRAD, 1,
+               launch_router_grad(w.dS_part, I / 128, sch->inv, sch->offsets, topk_w, c->T, K,
+                                  E, d_topk_w, d_logits, stream));
+    GemmDgradArgs dg{w.tiles, w.tiles_cap, sch->offsets, w.poff, (const uint16_t *)w13, w.dA,
+                     sch->perm, w.dx_slots, H, I, status};
+    MOK_LAUNCH(KK_GEMM_DGRAD, 1, launch_gemm_dgrad(dg, stream));
+    MOK_LAUNCH(KK_DX_REDUCE, 1,
+               launch_combine(w.dx_slots, nullptr, c->T, K, H, (float *)dx, stream));
+    GemmWgradArgs w1{sch->counts, w.poff, w.dA, w.x_perm, (float *)dw13, E, 2 * I, H, status};
+    MOK_LAUNCH(KK_WGRAD13, 1, launch_gemm_wgrad(w1, stream));
+    GemmWgradArgs w2a{sch->counts, w.poff, w.dy_perm, w.sh, (float *)dw2, E, H, I, status};
+    MOK_LAUNCH(KK_WGRAD2, 1, launch_gemm_wgrad(w2a, stream));
+    return MOK_OK;
+}
+
+mok_status mok_quantize_mxfp8(const void *src_bf16, int64_t rows, int32_t cols, uint8_t *q,
+                              uint8_t *scale, cudaStream_t stream) {
+    int *status;
+    mok_status st = check_device(&status);
+    if (st != MOK_OK) return st;
+    if (rows < 0 || cols <= 0 || cols % 32 != 0) return MOK_ERR_INVALID_ARG;
+    if (rows == 0) return MOK_OK;
+    if (!src_bf16 || !q || !scale) return MOK_ERR_INVALID_ARG;
+    if (!aligned16(src_bf16) || !aligned16(q)) return MOK_ERR_INVALID_ARG;
+    MOK_LAUNCH(KK_QUANTIZE, 1,
+               launch_quantize_mxfp8((const uint16_t *)src_bf16, rows, cols, q, scale, stream));
+    return MOK_OK;
+}
+
+mok_status mok_read_device_status(mok_status *out) {
+    if (out == nullptr) return MOK_ERR_INVALID_ARG;
+    int *status;
+    mok_status st = check_device(&status);
+    if (st != MOK_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MOK_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return MOK_ERR_CUDA;
+    *out = (mok_status)v;
+    return MOK_OK;
+}
+
+mok_status mok_clear_device_status(void) {
+    int *status;
+    mok_status st = check_device(&status);
+    if (st != MOK_OK) return st;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return MOK_ERR_CUDA;
+    return MOK_OK;
+}
+
+}  // extern "C"

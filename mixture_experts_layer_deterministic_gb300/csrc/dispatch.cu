@@ -1,0 +1,264 @@
+// dispatch.cu -- HBM-bound steps: pull dispatch, push-combine reduction, their backward
+// twins, MXFP8 quantization and the router gradient.
+//
+// [arex] "Cursor 放出 MoK：NVL72 训练提速 2.37 倍" (arex-research.com), section "pull 代替
+// push": the receiver pulls token rows into expert order (dispatch), results go back to
+// their source (combine), and the backward uses the same schedule in reverse; MXFP8
+// activation quantization is fused into dispatch. [alphalab] "Mixture-of-Kittens"
+// (alphalab.site), section 二: a final router-weighted reduction follows combine; section
+// 六: a fixed accumulation order makes results bitwise reproducible.
+#include "common.cuh"
+#include "mok_internal.h"
+
+namespace mok {
+namespace {
+
+constexpr int TPB = 256;
+
+inline unsigned grid_for(int64_t items, int per_block, int64_t cap = 152 * 32) {
+    int64_t b = (items + per_block - 1) / per_block;
+    if (b > cap) b = cap;
+    if (b < 1) b = 1;
+    return (unsigned)b;
+}
+
+// ---------------------------------------------------------------- BF16 gather
+// One warp per sorted row r in [p0, p1): ring[ring(r)] = x[perm[r] / K].
+__global__ void __launch_bounds__(TPB)
+    gather_bf16_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm, int K,
+                       int H, int64_t p0, int64_t p1, RingMap rm, uint16_t *__restrict__ ring) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * (TPB / 32);
+    const int nv = H / 8;  // 16-byte vectors per row
+    for (int64_t r = p0 + (int64_t)blockIdx.x * (TPB / 32) + (threadIdx.x >> 5); r < p1;
+         r += nw) {
+        const int64_t t = perm[r] / K;
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + t * H);
+        uint4 *dst = reinterpret_cast<uint4 *>(ring + rm(r) * H);
+#pragma unroll 4
+        for (int v = lane; v < nv; v += 32) dst[v] = ldg_nc_v4(src + v);
+    }
+}
+
+// ---------------------------------------------------------------- MXFP8 quantizer
+// One 32-element bf16 block -> 32 E4M3 bytes + one E8M0 byte.
+MOK_DEV void quant_block32(const uint16_t *__restrict__ src, uint8_t *__restrict__ q,
+                           uint8_t *__restrict__ sbyte) {
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = ldg_nc_v4(src + 8 * j);
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(v);
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+    const uint32_t sb = mx_scale_byte(amax);
+    const float inv = mx_inv_scale(sb);
+    uint32_t out[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t a = e4m3x2(bf16_lo(w[2 * j]) * inv, bf16_hi(w[2 * j]) * inv);
+        const uint32_t b = e4m3x2(bf16_lo(w[2 * j + 1]) * inv, bf16_hi(w[2 * j + 1]) * inv);
+        out[j] = a | (b << 16);
+    }
+    uint4 *qd = reinterpret_cast<uint4 *>(q);
+    qd[0] = make_uint4(out[0], out[1], out[2], out[3]);
+    qd[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    *sbyte = (uint8_t)sb;
+}
+
+// One thread per 32-element block of the rows [p0, p1) of the sorted stream.
+__global__ void __launch_bounds__(TPB)
+    gather_mxfp8_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm, int K,
+                        int H, int64_t p0, int64_t p1, RingMap rm, uint8_t *__restrict__ rq,
+                        uint8_t *__restrict__ rs) {
+    const int nb = H / 32;
+    const int64_t total = (p1 - p0) * nb;
+    const int64_t stride = (int64_t)gridDim.x * TPB;
+    for (int64_t i = (int64_t)blockIdx.x * TPB + threadIdx.x; i < total; i += stride) {
+        const int64_t r = p0 + i / nb;
+        const int b = (int)(i % nb);
+        const int64_t t = perm[r] / K;
+        const int64_t slot = rm(r);
+        quant_block32(x + t * H + b * 32, rq + slot * H + b * 32, rs + slot * nb + b);
+    }
+}
+
+__global__ void __launch_bounds__(TPB)
+    quantize_kernel(const uint16_t *__restrict__ src, int64_t rows, int cols,
+                    uint8_t *__restrict__ q, uint8_t *__restrict__ sc) {
+    const int nb = cols / 32;
+    const int64_t total = rows * nb;
+    const int64_t stride = (int64_t)gridDim.x * TPB;
+    for (int64_t i = (int64_t)blockIdx.x * TPB + threadIdx.x; i < total; i += stride) {
+        const int64_t r = i / nb;
+        const int b = (int)(i % nb);
+        quant_block32(src + r * cols + b * 32, q + r * cols + b * 32, sc + r * nb + b);
+    }
+}
+
+// ---------------------------------------------------------------- combine
+// y[t][c..c+3] = sum over k = 0..K-1 of w[t,k] * slots[t*K+k][c..c+3] in fp32, k ascending
+// (fmaf from zero); w == nullptr sums with weight one.
+__global__ void __launch_bounds__(TPB)
+    combine_kernel(const float *__restrict__ slots, const float *__restrict__ w, int64_t T,
+                   int K, int H, float *__restrict__ y) {
+    const int nv = H / 4;
+    const int64_t total = T * nv;
+    const int64_t stride = (int64_t)gridDim.x * TPB;
+    for (int64_t i = (int64_t)blockIdx.x * TPB + threadIdx.x; i < total; i += stride) {
+        const int64_t t = i / nv;
+        const int v = (int)(i % nv);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < K; ++k) {
+            const int64_t f = t * K + k;
+            const uint4 o = ldg_nc_v4(slots + f * H + v * 4);
+            const float s = (w != nullptr) ? __ldg(w + f) : 1.0f;
+            acc.x = fmaf(s, __uint_as_float(o.x), acc.x);
+            acc.y = fmaf(s, __uint_as_float(o.y), acc.y);
+            acc.z = fmaf(s, __uint_as_float(o.z), acc.z);
+            acc.w = fmaf(s, __uint_as_float(o.w), acc.w);
+        }
+        *reinterpret_cast<float4 *>(y + t * H + v * 4) = acc;
+    }
+}
+
+// ---------------------------------------------------------------- backward gather
+// Padded row space: expert e owns rows [poff[e], poff[e+1]) with its counts[e] real rows
+// first and zero rows after. One warp per padded row p < rpad_cap:
+//   dy_perm[p] = dy[t], x_perm[p] = x[t] for t = perm[offsets[e] + p - poff[e]] / K.
+__global__ void __launch_bounds__(TPB)
+    gather_bwd_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict__ x,
+                      const int32_t *__restrict__ perm, const int32_t *__restrict__ offsets,
+                      const int32_t *__restrict__ poff, int E, int K, int H, int64_t rpad_cap,
+                      uint16_t *__restrict__ dyp, uint16_t *__restrict__ xp) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * (TPB / 32);
+    const int nv = H / 8;
+    const int64_t rpad = poff[E];
+    const int64_t pend = rpad < rpad_cap ? rpad : rpad_cap;
+    for (int64_t p = (int64_t)blockIdx.x * (TPB / 32) + (threadIdx.x >> 5); p < pend; p += nw) {
+        // expert of padded row p: last e with poff[e] <= p (binary search)
+        int lo = 0, hi = E - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (poff[mid] <= p) lo = mid; else hi = mid - 1;
+        }
+        const int e = lo;
+        const int64_t local = p - poff[e];
+        const int64_t n_e = offsets[e + 1] - offsets[e];
+        uint4 *d0 = reinterpret_cast<uint4 *>(dyp + p * H);
+        uint4 *d1 = reinterpret_cast<uint4 *>(xp + p * H);
+        if (local < n_e) {
+            const int64_t t = perm[offsets[e] + local] / K;
+            const uint4 *s0 = reinterpret_cast<const uint4 *>(dy + t * H);
+            const uint4 *s1 = reinterpret_cast<const uint4 *>(x + t * H);
+#pragma unroll 4
+            for (int v = lane; v < nv; v += 32) {
+                d0[v] = ldg_nc_v4(s0 + v);
+                d1[v] = ldg_nc_v4(s1 + v);
+            }
+        } else {
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            for (int v = lane; v < nv; v += 32) {
+                d0[v] = z;
+                d1[v] = z;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- router gradient
+// One warp per token. dS of routed id f is the fixed-order sum of its per-feature-block
+// partials; d_topk = dS; d_logits through the top-k softmax (zero for unchosen logits).
+__global__ void __launch_bounds__(TPB)
+    router_grad_kernel(const float *__restrict__ part, int n_parts, const int32_t *__restrict__ inv,
+                       const int32_t *__restrict__ offsets, const float *__restrict__ w,
+                       int64_t T, int K, int E, float *__restrict__ d_topk,
+                       float *__restrict__ d_logits) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * (TPB / 32);
+    for (int64_t t = (int64_t)blockIdx.x * (TPB / 32) + (threadIdx.x >> 5); t < T; t += nw) {
+        float dS = 0.f, wk = 0.f;
+        int ek = 0;
+        if (lane < K) {
+            const int64_t f = t * K + lane;
+            const int64_t r = inv[f];
+            for (int j = 0; j < n_parts; ++j) dS += part[r * n_parts + j];
+            d_topk[f] = dS;
+            wk = w[f];
+            // expert of sorted row r: last e with offsets[e] <= r
+            int lo = 0, hi = E - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (offsets[mid] <= r) lo = mid; else hi = mid - 1;
+            }
+            ek = lo;
+        }
+        if (d_logits == nullptr) continue;
+        float sw = 0.f;
+        for (int k = 0; k < K; ++k) sw += __shfl_sync(0xFFFFFFFFu, wk * dS, k);
+        float *dl = d_logits + t * E;
+        for (int e = lane; e < E; e += 32) dl[e] = 0.f;
+        __syncwarp();
+        if (lane < K) dl[ek] = wk * (dS - sw);
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gather_bf16(const uint16_t *x, const int32_t *perm, int K, int H, int64_t p0,
+                               int64_t p1, int64_t R, int MB, int n_slots, uint16_t *ring,
+                               cudaStream_t s) {
+    if (p1 <= p0) return cudaSuccess;
+    RingMap rm{R, MB, n_slots};
+    gather_bf16_kernel<<<grid_for(p1 - p0, TPB / 32, 152 * 16), TPB, 0, s>>>(x, perm, K, H, p0,
+                                                                             p1, rm, ring);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_mxfp8(const uint16_t *x, const int32_t *perm, int K, int H, int64_t p0,
+                                int64_t p1, int64_t R, int MB, int n_slots, uint8_t *ring_q,
+                                uint8_t *ring_s, cudaStream_t s) {
+    if (p1 <= p0) return cudaSuccess;
+    RingMap rm{R, MB, n_slots};
+    gather_mxfp8_kernel<<<grid_for((p1 - p0) * (H / 32), TPB, 152 * 16), TPB, 0, s>>>(
+        x, perm, K, H, p0, p1, rm, ring_q, ring_s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_mxfp8(const uint16_t *src, int64_t rows, int cols, uint8_t *q,
+                                  uint8_t *scale, cudaStream_t s) {
+    if (rows == 0) return cudaSuccess;
+    quantize_kernel<<<grid_for(rows * (cols / 32), TPB, 152 * 16), TPB, 0, s>>>(src, rows, cols,
+                                                                                q, scale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float *slots, const float *w, int64_t T, int K, int H,
+                           float *y, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    combine_kernel<<<grid_for(T * (H / 4), TPB, 152 * 16), TPB, 0, s>>>(slots, w, T, K, H, y);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_bwd(const uint16_t *dy, const uint16_t *x, const int32_t *perm,
+                              const int32_t *offsets, const int32_t *poff, int E, int K, int H,
+                              int64_t rpad_cap, uint16_t *dy_perm, uint16_t *x_perm,
+                              cudaStream_t s) {
+    if (rpad_cap == 0) return cudaSuccess;
+    gather_bwd_kernel<<<grid_for(rpad_cap, TPB / 32, 152 * 16), TPB, 0, s>>>(
+        dy, x, perm, offsets, poff, E, K, H, rpad_cap, dy_perm, x_perm);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_grad(const float *dS_part, int n_parts, const int32_t *inv,
+                               const int32_t *offsets, const float *w, int64_t T, int K, int E,
+                               float *d_topk, float *d_logits, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    router_grad_kernel<<<grid_for(T, TPB / 32, 152 * 16), TPB, 0, s>>>(
+        dS_part, n_parts, inv, offsets, w, T, K, E, d_topk, d_logits);
+    return cudaGetLastError();
+}
+
+}  // namespace mok

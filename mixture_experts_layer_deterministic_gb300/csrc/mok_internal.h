@@ -1,0 +1,171 @@
+// mok_internal.h -- host-side launchers shared between the entry points and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mok.h"
+
+namespace mok {
+
+// ---------------------------------------------------------------- instrumentation
+enum KernelKind {
+    KK_ROUTE = 0, KK_SCHEDULE, KK_TILES, KK_GATHER, KK_GEMM_UP, KK_GEMM_DOWN, KK_COMBINE,
+    KK_QUANTIZE, KK_PAD, KK_GATHER_BWD, KK_GEMM_G, KK_ROUTER_GRAD, KK_GEMM_DGRAD,
+    KK_DX_REDUCE, KK_WGRAD13, KK_WGRAD2, KK_COUNT
+};
+// while profiling is on: brackets the launches between begin and end with events
+void prof_begin(int kind, cudaStream_t s);
+void prof_end(int kind, cudaStream_t s, int n_kernels);
+bool prof_on();
+
+// ---------------------------------------------------------------- routing / schedule
+cudaError_t launch_route_topk(const float *logits, int64_t T, int E, int K, int32_t *idx,
+                              float *w, int *status, cudaStream_t s);
+
+struct ScheduleWs {
+    int32_t *hist;   // [n_chunks][E] per-chunk expert counts, then per-chunk bases
+    int64_t n_chunks;
+};
+size_t schedule_ws_bytes(int64_t R, int E);
+ScheduleWs schedule_ws_carve(void *ws, int64_t R, int E);
+cudaError_t launch_build_schedule(const int32_t *idx, int64_t R, int E, int MB,
+                                  const mok_schedule &sch, const ScheduleWs &ws, int *status,
+                                  cudaStream_t s);
+
+// ---------------------------------------------------------------- tile lists
+// A tile is (expert, row_begin, row_end) over sorted rows; lists are built on the device
+// from the schedule's offsets for a row window [p0, p1), cutting each expert's rows into
+// chunks of at most `chunk` rows. Layout: int32 [cap][4], count at list[-4].
+int64_t tile_list_cap(int64_t rows, int E, int chunk);
+cudaError_t launch_build_tiles(const int32_t *offsets, int E, int64_t p0, int64_t p1, int chunk,
+                               int32_t *list, int64_t cap, int *status, cudaStream_t s);
+
+// ---------------------------------------------------------------- dispatch / combine
+cudaError_t launch_gather_bf16(const uint16_t *x, const int32_t *perm, int K, int H, int64_t p0,
+                               int64_t p1, int64_t R, int MB, int n_slots, uint16_t *ring,
+                               cudaStream_t s);
+cudaError_t launch_gather_mxfp8(const uint16_t *x, const int32_t *perm, int K, int H, int64_t p0,
+                                int64_t p1, int64_t R, int MB, int n_slots, uint8_t *ring_q,
+                                uint8_t *ring_s, cudaStream_t s);
+cudaError_t launch_quantize_mxfp8(const uint16_t *src, int64_t rows, int cols, uint8_t *q,
+                                  uint8_t *scale, cudaStream_t s);
+// y[t] = sum_k w[t,k] * slots[t*K+k] in fp32 (w == nullptr: plain sum), k ascending
+cudaError_t launch_combine(const float *slots, const float *w, int64_t T, int K, int H,
+                           float *y, cudaStream_t s);
+
+// backward: padded row offsets (each expert's rows rounded up to 16) and gathers
+cudaError_t launch_pad_offsets(const int32_t *counts, int E, int32_t *poff, cudaStream_t s);
+cudaError_t launch_gather_bwd(const uint16_t *dy, const uint16_t *x, const int32_t *perm,
+                              const int32_t *offsets, const int32_t *poff, int E, int K, int H,
+                              int64_t rpad_cap, uint16_t *dy_perm, uint16_t *x_perm,
+                              cudaStream_t s);
+cudaError_t launch_router_grad(const float *dS_part, int n_parts, const int32_t *inv,
+                               const int32_t *offsets, const float *w, int64_t T, int K, int E,
+                               float *d_topk, float *d_logits, cudaStream_t s);
+
+// ---------------------------------------------------------------- grouped GEMMs
+// Ring map parameters (see RingMap in common.cuh).
+struct Ring {
+    int64_t R;
+    int32_t MB;
+    int32_t n_slots;
+};
+
+// Forward gate/up GEMM with the SwiGLU epilogue, per tile (e, r0, r1):
+//   a[r][j] = sum_c W13[e][j][c] * xring[ring(r)][c]   (j < 2I)
+//   h[ring(r)][i] = silu(a[r][i]) * a[r][I+i]          (bf16, or MXFP8 along I)
+//   preact[r][j] = a[r][j] (fp32) when preact != nullptr
+struct GemmUpArgs {
+    const int32_t *tiles;
+    int64_t tiles_cap;
+    const void *xring;
+    const uint8_t *xring_s;
+    const void *w13;
+    const uint8_t *w13_s;
+    void *hring;
+    uint8_t *hring_s;
+    float *preact;
+    int H, I, E;
+    bool mxfp8;
+    Ring ring;
+    int *status;
+};
+cudaError_t launch_gemm_up(const GemmUpArgs &a, cudaStream_t s);
+
+// Forward down GEMM with the push scatter, per tile (e, r0, r1):
+//   slots[perm[r]][c] = sum_i W2[e][c][i] * hring[ring(r)][i]   (fp32)
+struct GemmDownArgs {
+    const int32_t *tiles;
+    int64_t tiles_cap;
+    const void *hring;
+    const uint8_t *hring_s;
+    const void *w2;
+    const uint8_t *w2_s;
+    const int32_t *perm;
+    float *slots;
+    int H, I, E;
+    bool mxfp8;
+    Ring ring;
+    int *status;
+};
+cudaError_t launch_gemm_down(const GemmDownArgs &a, cudaStream_t s);
+
+int gemm_tile_rows();
+
+// Backward G GEMM with the SwiGLU backward and router-weight gradient epilogue, per tile
+// (e, r0, r1) over sorted rows; p(r) = poff[e] + r - offsets[e] is the padded row:
+//   g[r][i] = sum_c W2[e][c][i] * dy_perm[p(r)][c]
+//   dS_part[r][i / 128] = sum over the 128-feature block of g * h   (fixed order)
+//   dA[p(r)][i] = w g a_u silu'(a_g), dA[p(r)][I+i] = w g silu(a_g), sh[p(r)][i] = w h
+// Pad rows of the tile (up to the next multiple of 16) get zeros in dA and sh.
+struct GemmGArgs {
+    const int32_t *tiles;
+    int64_t tiles_cap;
+    const int32_t *offsets;
+    const int32_t *poff;
+    const uint16_t *w2;
+    const uint16_t *dy_perm;
+    const float *preact;
+    const int32_t *perm;
+    const float *topk_w;
+    uint16_t *dA;
+    uint16_t *sh;
+    float *dS_part;
+    int H, I;
+    int *status;
+};
+cudaError_t launch_gemm_g(const GemmGArgs &a, cudaStream_t s);
+
+// Backward dgrad GEMM with the reverse-dispatch scatter, per tile (e, r0, r1):
+//   dx_slots[perm[r]][c] = sum_j W13[e][j][c] * dA[p(r)][j]   (fp32)
+struct GemmDgradArgs {
+    const int32_t *tiles;
+    int64_t tiles_cap;
+    const int32_t *offsets;
+    const int32_t *poff;
+    const uint16_t *w13;
+    const uint16_t *dA;
+    const int32_t *perm;
+    float *dx_slots;
+    int H, I;
+    int *status;
+};
+cudaError_t launch_gemm_dgrad(const GemmDgradArgs &a, cudaStream_t s);
+
+// Weight gradient, per expert e: out[e][m][n] = sum over padded rows p of e of
+//   A[p][m] * B[p][n] (fp32) with A [rows][M] and B [rows][N] row-major; experts with no rows
+// get zeros. dW13: A = dA (M = 2I), B = x_perm (N = H). dW2: A = dy_perm (M = H), B = sh
+// (N = I).
+struct GemmWgradArgs {
+    const int32_t *counts;
+    const int32_t *poff;
+    const uint16_t *A;
+    const uint16_t *B;
+    float *out;
+    int E, M, N;
+    int *status;
+};
+cudaError_t launch_gemm_wgrad(const GemmWgradArgs &a, cudaStream_t s);
+
+}  // namespace mok

@@ -1,0 +1,98 @@
+"""The C ABI without a GPU: the library loads, exports every entry point include/mok.h
+declares, and validates configurations on the host."""
+import os
+import re
+
+import pytest
+
+from mixture_experts_layer_deterministic_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(B.LIB_PATH):
+        import mixture_experts_layer_deterministic_gb300 as pkg
+        pkg.build()
+    return B.lib()
+
+
+def declared_entry_points():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(mok_\w+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_entry_points()
+    assert "mok_forward" in names and "mok_backward" in names
+    for n in sorted(names):
+        assert hasattr(lib, n), "missing export " + n
+    assert names <= set(B.EXPORTED)
+
+
+def test_abi_version_and_strings(lib):
+    assert B.mok_abi_version() == B.MOK_ABI_VERSION
+    for s in range(8):
+        assert B.status_string(s)
+    assert B.status_string(0) == "ok"
+
+
+def cfg(**kw):
+    base = dict(T=256, H=256, I=128, E=8, K=2, minibatch=64, ring_capacity=0, prec=B.MOK_BF16)
+    base.update(kw)
+    return B.make_config(**base)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(), B.MOK_OK),
+    (dict(T=0), B.MOK_OK),
+    (dict(K=9), B.MOK_ERR_INVALID_ARG),          # K > E
+    (dict(K=0), B.MOK_ERR_INVALID_ARG),
+    (dict(E=2000, K=2), B.MOK_ERR_INVALID_ARG),   # E > 1024
+    (dict(E=64, K=33), B.MOK_ERR_INVALID_ARG),    # K > 32
+    (dict(H=200), B.MOK_ERR_INVALID_ARG),         # H % 128
+    (dict(I=64), B.MOK_ERR_INVALID_ARG),          # I < 128
+    (dict(minibatch=0), B.MOK_ERR_INVALID_ARG),
+    (dict(ring_capacity=32), B.MOK_ERR_INVALID_ARG),  # smaller than a minibatch
+    (dict(ring_capacity=100), B.MOK_OK),              # one minibatch slot
+    (dict(ring_capacity=10000), B.MOK_OK),            # >= R: holds every row
+    (dict(prec=5), B.MOK_ERR_INVALID_ARG),
+    (dict(T=1 << 28, K=8, E=8), B.MOK_ERR_INVALID_ARG),  # R >= 2^31
+    (dict(abi_version=99), B.MOK_ERR_ABI),
+])
+def test_check_config(lib, kw, want):
+    assert B.mok_check_config(cfg(**kw)) == want
+
+
+def test_workspace_sizes(lib):
+    c = cfg()
+    for which in (B.MOK_WS_SCHEDULE, B.MOK_WS_FORWARD, B.MOK_WS_BACKWARD):
+        assert B.mok_workspace_size(c, which) > 0
+    assert B.mok_workspace_size(cfg(K=9), B.MOK_WS_FORWARD) == 0
+    # a smaller ring needs a smaller forward workspace
+    big = B.mok_workspace_size(cfg(T=4096), B.MOK_WS_FORWARD)
+    small = B.mok_workspace_size(cfg(T=4096, ring_capacity=128), B.MOK_WS_FORWARD)
+    assert small < big
+    # MXFP8 rings hold one byte per element
+    assert B.mok_workspace_size(cfg(prec=B.MOK_MXFP8), B.MOK_WS_FORWARD) < \
+        B.mok_workspace_size(c, B.MOK_WS_FORWARD)
+
+
+def test_segment_capacity(lib):
+    # E + ceil(R / MB) - 1
+    assert B.mok_segment_capacity(cfg()) == 8 + (512 + 63) // 64 - 1
+    assert B.mok_segment_capacity(cfg(T=0)) == 7
+
+
+def test_device_calls_fail_cleanly_without_gpu(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = B.lib().mok_route_topk(B.ctypes.byref(cfg()), None, None, None, None)
+    assert st in (B.MOK_ERR_CUDA, B.MOK_ERR_UNSUPPORTED)

@@ -142,6 +142,29 @@ mok_status mok_build_schedule(const mok_config *cfg, const int32_t *topk_idx,
                               const mok_schedule *sched, void *ws, size_t ws_bytes,
                               cudaStream_t stream);
 
+/* The schedule builder for callers that cannot allocate device memory. The pages have no
+ * counterpart to this entry point; it is a deployment convenience of this library.
+ * mok_build_schedule needs a workspace from the caller. Some callers cannot allocate one:
+ * code running under a device-memory budget that another component owns (a framework or
+ * server that hands out all GPU memory from its own pool and forbids raw cudaMalloc), or a
+ * time-critical loop that cannot pay cudaMalloc's latency and implicit synchronisation.
+ * This variant computes exactly what mok_build_schedule computes (same kernels, same
+ * outputs, bit for bit) but keeps its scratch in a fixed array inside the library: a
+ * file-scope __device__ array of MOK_NOALLOC_SCHEDULE_SCRATCH_BYTES bytes that every GPU
+ * loading the library holds until the process exits. It calls no cudaMalloc or cudaFree.
+ *   - The first call on a device, with that device current, looks up the array's device
+ *     address (cudaGetSymbolAddress) and caches it; make that first call before any stream
+ *     capture.
+ *   - Configurations whose schedule workspace, mok_workspace_size(cfg, MOK_WS_SCHEDULE),
+ *     exceeds MOK_NOALLOC_SCHEDULE_SCRATCH_BYTES are rejected with MOK_ERR_WORKSPACE before
+ *     anything is enqueued (with E = 512 that is more than 2,097,152 routed rows).
+ *   - Every call shares the one array and leaves its contents behind; nothing in it needs
+ *     to start at zero. Calls whose work overlaps on the GPU (other streams, other host
+ *     threads) race on the array and give undefined results: order them on one stream. */
+#define MOK_NOALLOC_SCHEDULE_SCRATCH_BYTES (4u << 20)
+mok_status mok_build_schedule_noalloc(const mok_config *cfg, const int32_t *topk_idx,
+                                      const mok_schedule *sched, cudaStream_t stream);
+
 /* Layer forward: gather -> gate/up GEMM + SwiGLU -> down GEMM -> scatter -> reduction
  * ([alphalab] section 一: pull dispatch, expert FFN/SwiGLU, push combine; section 二: the
  * final router-weighted reduction; section 三: that is the timed layer).

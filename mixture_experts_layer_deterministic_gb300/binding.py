@@ -38,7 +38,11 @@ EXPORTED = [
     "mok_workspace_size", "mok_route_topk", "mok_build_schedule", "mok_forward",
     "mok_backward", "mok_quantize_mxfp8", "mok_read_device_status",
     "mok_clear_device_status", "mok_profile_enable", "mok_profile_read",
+    "mok_build_schedule_noalloc",
 ]
+
+# bytes of the fixed scratch array behind mok_build_schedule_noalloc
+MOK_NOALLOC_SCHEDULE_SCRATCH_BYTES = 4 << 20
 
 
 class MokConfig(ctypes.Structure):
@@ -83,6 +87,7 @@ def lib():
             "mok_workspace_size": ([cfgp, ctypes.c_int], sz),
             "mok_route_topk": ([cfgp, p, p, p, p], ctypes.c_int),
             "mok_build_schedule": ([cfgp, p, schp, p, sz, p], ctypes.c_int),
+            "mok_build_schedule_noalloc": ([cfgp, p, schp, p], ctypes.c_int),
             "mok_forward": ([cfgp, p, schp, p, p, p, p, p, p, p, p, sz, p], ctypes.c_int),
             "mok_backward": ([cfgp, p, schp, p, p, p, p, p, p, p, p, p, p, p, sz, p],
                              ctypes.c_int),
@@ -166,6 +171,12 @@ def mok_route_topk(cfg, logits, topk_idx, topk_w, stream=None) -> int:
 def mok_build_schedule(cfg, topk_idx, sched, ws, ws_bytes, stream=None) -> int:
     return lib().mok_build_schedule(ctypes.byref(cfg), _ptr(topk_idx), ctypes.byref(sched),
                                     _ptr(ws), int(ws_bytes), _stream(stream))
+
+
+def mok_build_schedule_noalloc(cfg, topk_idx, sched, stream=None) -> int:
+    """mok_build_schedule for callers that cannot allocate a workspace (see include/mok.h)."""
+    return lib().mok_build_schedule_noalloc(ctypes.byref(cfg), _ptr(topk_idx),
+                                            ctypes.byref(sched), _stream(stream))
 
 
 def mok_forward(cfg, x, sched, topk_w, w13, w13_scale, w2, w2_scale, y, saved_preact, ws,

@@ -145,6 +145,10 @@ mok_status check_sched(const mok_config *c, const mok_schedule *s) {
 
 }  // namespace
 
+namespace mok {
+mok_status current_device_status_word(int **status) { return check_device(status); }
+}  // namespace mok
+
 // a launch of `nk` kernels of one kind, bracketed by events while profiling is on
 #define MOK_LAUNCH(kind, nk, expr)                         \
     do {                                                   \

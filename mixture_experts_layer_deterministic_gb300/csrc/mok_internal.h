@@ -19,6 +19,9 @@ void prof_begin(int kind, cudaStream_t s);
 void prof_end(int kind, cudaStream_t s, int n_kernels);
 bool prof_on();
 
+// the entry points' device check (compute capability 10.3) and the device's status word
+mok_status current_device_status_word(int **status);
+
 // ---------------------------------------------------------------- routing / schedule
 cudaError_t launch_route_topk(const float *logits, int64_t T, int E, int K, int32_t *idx,
                               float *w, int *status, cudaStream_t s);

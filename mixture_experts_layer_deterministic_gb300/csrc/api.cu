@@ -272,9 +272,11 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
     for (int64_t m = 0; m < n_pass; ++m) {
         const int64_t p0 = n_slots == 0 ? 0 : m * c->minibatch;
         const int64_t p1 = n_slots == 0 ? R : (p0 + c->minibatch < R ? p0 + c->minibatch : R);
+        const int chunk = mx ? gemm_tile_rows() : gemm_tc_tile_rows();
+        const int64_t cap = tile_list_cap(p1 - p0, c->E, chunk);
         MOK_LAUNCH(KK_TILES, 1,
-                   launch_build_tiles(sch->offsets, c->E, p0, p1, gemm_tile_rows(), w.tiles,
-                                      w.tiles_cap, status, stream));
+                   launch_build_tiles(sch->offsets, c->E, p0, p1, chunk, w.tiles, cap, status,
+                                      stream));
         if (!mx)
             MOK_LAUNCH(KK_GATHER, 1,
                        launch_gather_bf16((const uint16_t *)x, sch->perm, c->K, c->H, p0, p1, R,
@@ -284,12 +286,17 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
                        launch_gather_mxfp8((const uint16_t *)x, sch->perm, c->K, c->H, p0, p1,
                                            R, c->minibatch, n_slots, (uint8_t *)w.xring,
                                            w.xring_s, stream));
-        GemmUpArgs ua{w.tiles, w.tiles_cap, w.xring, w.xring_s, w13, w13_scale, w.hring,
+        GemmUpArgs ua{w.tiles, cap, w.xring, w.xring_s, w13, w13_scale, w.hring,
                       w.hring_s, (float *)saved_preact, c->H, c->I, c->E, mx, ring, status};
-        MOK_LAUNCH(KK_GEMM_UP, 1, launch_gemm_up(ua, stream));
-        GemmDownArgs da{w.tiles, w.tiles_cap, w.hring, w.hring_s, w2, w2_scale, sch->perm,
+        GemmDownArgs da{w.tiles, cap, w.hring, w.hring_s, w2, w2_scale, sch->perm,
                         w.slots, c->H, c->I, c->E, mx, ring, status};
-        MOK_LAUNCH(KK_GEMM_DOWN, 1, launch_gemm_down(da, stream));
+        if (mx) {
+            MOK_LAUNCH(KK_GEMM_UP, 1, launch_gemm_up(ua, stream));
+            MOK_LAUNCH(KK_GEMM_DOWN, 1, launch_gemm_down(da, stream));
+        } else {
+            MOK_LAUNCH(KK_GEMM_UP, 1, launch_gemm_up_tc(ua, ring_rows, stream));
+            MOK_LAUNCH(KK_GEMM_DOWN, 1, launch_gemm_down_tc(da, ring_rows, stream));
+        }
     }
     MOK_LAUNCH(KK_COMBINE, 1,
                launch_combine(w.slots, topk_w, c->T, c->K, c->H, (float *)y, stream));

@@ -114,6 +114,12 @@ struct GemmDownArgs {
 };
 cudaError_t launch_gemm_down(const GemmDownArgs &a, cudaStream_t s);
 
+// tensor-core versions (BF16): tiles cut at gemm_tc_tile_rows() rows; ring_rows = rows of
+// the ring buffers the TMA maps cover
+int gemm_tc_tile_rows();
+cudaError_t launch_gemm_up_tc(const GemmUpArgs &a, int64_t ring_rows, cudaStream_t s);
+cudaError_t launch_gemm_down_tc(const GemmDownArgs &a, int64_t ring_rows, cudaStream_t s);
+
 int gemm_tile_rows();
 
 // Backward G GEMM with the SwiGLU backward and router-weight gradient epilogue, per tile

@@ -44,9 +44,11 @@ def lib():
         L.oracle_mxfp8_quantize.argtypes = [i64, i64, p, p, p]
         L.oracle_mxfp8_dequantize.argtypes = [i64, i64, p, p, p]
         L.oracle_mxfp8_quantize_bf16.argtypes = [i64, i64, p, p, p]
-        L.oracle_forward.argtypes = [i64, i32, i32, i32, i32, p, p, p, i32, p, p, p, p, i32, p]
+        L.oracle_forward.argtypes = [i64, i32, i32, i32, i32, p, p, p, i32, p, p, p, p, i32, p, p]
         L.oracle_backward.argtypes = [i64, i32, i32, i32, i32, p, p, p, i32, p, p, p, i32, p,
-                                      p, p, p]
+                                      p, p, p, p, p, p]
+        L.oracle_bf16_slack.argtypes = [ctypes.c_double]
+        L.oracle_bf16_slack.restype = ctypes.c_double
         L.oracle_round_bf16.argtypes = [ctypes.c_double]
         L.oracle_round_bf16.restype = ctypes.c_double
         L.oracle_router_grad.argtypes = [i64, i32, i32, p, p, p, p]
@@ -154,9 +156,15 @@ def _weights(w):
     return W_F64, w, None, w.shape
 
 
-def forward(x, idx, w, w13, w2, mode=EXACT):
+def bf16_slack(v: float) -> float:
+    return float(lib().oracle_bf16_slack(float(v)))
+
+
+def forward(x, idx, w, w13, w2, mode=EXACT, with_slack=False):
     """Layer forward in fp64: y [T,H], with the operand rounding of `mode` (EXACT, BF16 or
-    MXFP8). Weights as described in _weights (both of the same kind)."""
+    MXFP8). Weights as described in _weights (both of the same kind). With with_slack,
+    returns (y, slack): the per-element bound on how far a correct result may lie from y
+    because of rounding decisions taken on values within fp32 error of a midpoint."""
     x, w = _f64(x), _f64(w)
     idx = _i32(idx)
     k13, d13, s13, sh13 = _weights(w13)
@@ -166,15 +174,18 @@ def forward(x, idx, w, w13, w2, mode=EXACT):
     E, I2, _ = sh13
     K = idx.shape[1]
     y = np.empty((T, H), np.float64)
+    sl = np.empty((T, H), np.float64) if with_slack else None
     lib().oracle_forward(T, H, I2 // 2, E, K, _p(x), _p(idx), _p(w), k13, _p(d13),
                          None if s13 is None else _p(s13), _p(d2),
-                         None if s2 is None else _p(s2), int(mode), _p(y))
-    return y
+                         None if s2 is None else _p(s2), int(mode), _p(y),
+                         None if sl is None else _p(sl))
+    return (y, sl) if with_slack else y
 
 
-def backward(x, idx, w, w13, w2, dy, weight_grads=True, mode=EXACT):
+def backward(x, idx, w, w13, w2, dy, weight_grads=True, mode=EXACT, with_slack=False):
     """Layer backward in fp64: (dx, dw13, dw2, dtopk), with the operand rounding of `mode`
-    (EXACT or BF16); dw13/dw2 are None when weight_grads is False."""
+    (EXACT or BF16); dw13/dw2 are None when weight_grads is False. With with_slack, also
+    the slacks of dx, dw13, dw2 (see forward)."""
     x, w, dy = _f64(x), _f64(w), _f64(dy)
     idx = _i32(idx)
     k13, d13, _, sh13 = _weights(w13)
@@ -187,9 +198,20 @@ def backward(x, idx, w, w13, w2, dy, weight_grads=True, mode=EXACT):
     dw13 = np.empty(sh13, np.float64) if weight_grads else None
     dw2 = np.empty(sh2, np.float64) if weight_grads else None
     dtopk = np.empty((T, K), np.float64)
+    sdx = np.empty((T, H), np.float64) if with_slack else None
+    sdw13 = np.empty(sh13, np.float64) if (with_slack and weight_grads) else None
+    sdw2 = np.empty(sh2, np.float64) if (with_slack and weight_grads) else None
+    n = lambda a: None if a is None else _p(a)  # noqa: E731
     lib().oracle_backward(T, H, I2 // 2, E, K, _p(x), _p(idx), _p(w), k13, _p(d13), _p(d2),
-                          _p(dy), int(mode), _p(dx), None if dw13 is None else _p(dw13),
-                          None if dw2 is None else _p(dw2), _p(dtopk))
+                          _p(dy), int(mode), _p(dx), n(dw13), n(dw2), _p(dtopk), n(sdx),
+                          n(sdw13), n(sdw2))
+    if with_slack:
+        if sdx is not None and mode == EXACT:
+            sdx[:] = 0.0
+            if sdw13 is not None:
+                sdw13[:] = 0.0
+                sdw2[:] = 0.0
+        return dx, dw13, dw2, dtopk, sdx, sdw13, sdw2
     return dx, dw13, dw2, dtopk
 
 

@@ -236,6 +236,92 @@ static void qdq_row(int64_t n, double *v)
     free(s);
 }
 
+/* ---------------------------------------------------------------- rounding slack
+ * A rounding decision taken on a value that the GPU computes in fp32 (with a relative
+ * error of a few fp32 ulps) and the oracle in fp64 can fall on either side of a rounding
+ * midpoint when the exact value is that close to it; both outcomes are then correct
+ * results of the definition. The slack of a decision is the distance between its two
+ * possible results when the exact value lies within ORACLE_SLACK_REL of a midpoint (or, for
+ * an MXFP8 block, of a scale-exponent boundary), and 0 otherwise. */
+
+double oracle_bf16_slack(double v)
+{
+    if (v == 0.0 || !isfinite(v))
+        return 0.0;
+    int ex;
+    frexp(fabs(v), &ex);
+    int e = ex - 1;
+    if (e < -126)
+        e = -126;
+    const double ulp = ldexp(1.0, e - 7);
+    const double q = fabs(v) / ulp;
+    const double dist = fabs((q - floor(q)) - 0.5) * ulp;
+    return dist <= ORACLE_SLACK_REL * fabs(v) ? ulp : 0.0;
+}
+
+/* slack of the E4M3 code of a scaled value u (saturation at 448 is one-sided: none) */
+static double e4m3_slack(double u)
+{
+    const double a = fabs(u);
+    if (a == 0.0 || a >= 448.0)
+        return 0.0;
+    int ex;
+    frexp(a, &ex);
+    int e = ex - 1;
+    if (e < -6)
+        e = -6;
+    const double sp = ldexp(1.0, e - 3);
+    const double q = a / sp;
+    const double dist = fabs((q - floor(q)) - 0.5) * sp;
+    return dist <= ORACLE_SLACK_REL * a ? sp : 0.0;
+}
+
+/* MXFP8 quantize-dequantize of one row along its 32-element blocks, with each element's
+ * slack: the code decision's slack, and when the block's amax is that close to a power of
+ * two (the shared exponent could go either way) the difference to the other exponent's
+ * result as well. */
+static void qdq_row_slack(int64_t n, double *v, double *slack)
+{
+    double alt[32];
+    for (int64_t b = 0; b < n / 32; ++b) {
+        double *blk = v + b * 32, *sl = slack + b * 32;
+        double amax = 0.0;
+        for (int i = 0; i < 32; ++i)
+            if (fabs(blk[i]) > amax)
+                amax = fabs(blk[i]);
+        int ex = 0;
+        if (amax > 0.0)
+            frexp(amax, &ex);
+        const int sexp = amax > 0.0 ? (ex - 1) - 8 : -127;
+        /* the nearer power of two decides which other exponent is possible */
+        const double p_lo = ldexp(1.0, ex - 1), p_hi = ldexp(1.0, ex);
+        int other = 0;
+        if (amax > 0.0 && sexp > -127 && amax - p_lo <= ORACLE_SLACK_REL * amax)
+            other = -1;
+        else if (amax > 0.0 && p_hi - amax <= ORACLE_SLACK_REL * amax)
+            other = +1;
+        for (int i = 0; i < 32; ++i)
+            sl[i] = ldexp(e4m3_slack(ldexp(blk[i], -(sexp < -127 ? -127 : sexp))),
+                          sexp < -127 ? -127 : sexp);
+        if (other != 0) {
+            int s2 = sexp + other;
+            if (s2 < -127)
+                s2 = -127;
+            for (int i = 0; i < 32; ++i)
+                alt[i] = ldexp(oracle_e4m3_decode(oracle_e4m3_encode(ldexp(blk[i], -s2))), s2);
+        }
+        uint8_t q[32], sc;
+        oracle_mxfp8_quantize(1, 32, blk, q, &sc);
+        oracle_mxfp8_dequantize(1, 32, q, &sc, blk);
+        if (other != 0)
+            for (int i = 0; i < 32; ++i) {
+                const double d = fabs(alt[i] - blk[i]);
+                if (d > sl[i])
+                    sl[i] = d;
+            }
+    }
+}
+
 /* ---------------------------------------------------------------- forward */
 
 static double silu(double g) { return g / (1.0 + exp(-g)); }
@@ -243,7 +329,7 @@ static double silu(double g) { return g / (1.0 + exp(-g)); }
 void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
                     const int32_t *idx, const double *w, int32_t wkind, const void *w13,
                     const uint8_t *w13_s, const void *w2, const uint8_t *w2_s, int32_t mode,
-                    double *y)
+                    double *y, double *slack)
 {
     (void)E;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -251,12 +337,17 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
         double *xt = (double *)malloc(sizeof(double) * (size_t)H);
         double *a = (double *)malloc(sizeof(double) * 2 * (size_t)I);
         double *h = (double *)malloc(sizeof(double) * (size_t)I);
+        double *hs = (double *)calloc((size_t)I, sizeof(double));
         double *yt = y + t * (int64_t)H;
+        double *st = slack ? slack + t * (int64_t)H : NULL;
         memcpy(xt, x + t * (int64_t)H, sizeof(double) * (size_t)H);
         if (mode == ORACLE_MXFP8)
             qdq_row(H, xt);
         for (int32_t c = 0; c < H; ++c)
             yt[c] = 0.0;
+        if (st)
+            for (int32_t c = 0; c < H; ++c)
+                st[c] = 0.0;
         for (int32_t k = 0; k < K; ++k) {
             const int64_t e = idx[t * K + k];
             const int64_t b13 = e * 2 * (int64_t)I * H, b2 = e * (int64_t)H * I;
@@ -268,11 +359,14 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
             }
             for (int32_t i = 0; i < I; ++i)
                 h[i] = silu(a[i]) * a[I + i];
-            if (mode == ORACLE_MXFP8)
-                qdq_row(I, h);
-            else if (mode == ORACLE_BF16)
-                for (int32_t i = 0; i < I; ++i)
+            if (mode == ORACLE_MXFP8) {
+                qdq_row_slack(I, h, hs);
+            } else if (mode == ORACLE_BF16) {
+                for (int32_t i = 0; i < I; ++i) {
+                    hs[i] = oracle_bf16_slack(h[i]);
                     h[i] = oracle_round_bf16(h[i]);
+                }
+            }
             const double s = w[t * K + k];
             for (int32_t c = 0; c < H; ++c) {
                 double o = 0.0;
@@ -280,10 +374,20 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
                     o += wget(wkind, w2, w2_s, I, b2 + (int64_t)c * I + i) * h[i];
                 yt[c] += s * o;
             }
+            /* slack of y: the h decisions that could go either way, through |W2| */
+            if (st && mode != ORACLE_EXACT)
+                for (int32_t i = 0; i < I; ++i) {
+                    if (hs[i] == 0.0)
+                        continue;
+                    for (int32_t c = 0; c < H; ++c)
+                        st[c] += fabs(s * wget(wkind, w2, w2_s, I, b2 + (int64_t)c * I + i)) *
+                                 hs[i];
+                }
         }
         free(xt);
         free(a);
         free(h);
+        free(hs);
     }
 }
 
@@ -292,12 +396,18 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
 void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
                      const int32_t *idx, const double *w, int32_t wkind, const void *w13,
                      const void *w2, const double *dy, int32_t mode, double *dx, double *dw13,
-                     double *dw2, double *dtopk)
+                     double *dw2, double *dtopk, double *sdx, double *sdw13, double *sdw2)
 {
     const int64_t R = T * K;
-    /* per routed row: da = dL/da [2I] and sh = w * h [I], kept for the weight gradients */
+    const int want_slack = (sdx != NULL) && mode == ORACLE_BF16;
+    /* per routed row: da = dL/da [2I] and sh = w * h [I], kept for the weight gradients,
+     * and the slack of their bf16 decisions */
     double *da_all = (double *)malloc(sizeof(double) * (size_t)(R * 2 * I));
     double *sh_all = (double *)malloc(sizeof(double) * (size_t)(R * I));
+    double *das_all = want_slack ? (double *)calloc((size_t)(R * 2 * I), sizeof(double)) : NULL;
+    double *shs_all = want_slack ? (double *)calloc((size_t)(R * I), sizeof(double)) : NULL;
+    if (sdx != NULL)
+        memset(sdx, 0, sizeof(double) * (size_t)(T * (int64_t)H));
 
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t t = 0; t < T; ++t) {
@@ -342,10 +452,16 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
                 sh[i] = s * hi;
             }
             if (mode == ORACLE_BF16) {
-                for (int32_t j = 0; j < 2 * I; ++j)
+                for (int32_t j = 0; j < 2 * I; ++j) {
+                    if (want_slack)
+                        das_all[f * 2 * I + j] = oracle_bf16_slack(da[j]);
                     da[j] = oracle_round_bf16(da[j]);
-                for (int32_t i = 0; i < I; ++i)
+                }
+                for (int32_t i = 0; i < I; ++i) {
+                    if (want_slack)
+                        shs_all[f * I + i] = oracle_bf16_slack(sh[i]);
                     sh[i] = oracle_round_bf16(sh[i]);
+                }
             }
             dtopk[f] = dS;
             /* dx += W13^T da */
@@ -355,6 +471,15 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
                     acc += wget(wkind, w13, NULL, H, b13 + (int64_t)j * H + c) * da[j];
                 dxt[c] += acc;
             }
+            if (want_slack)
+                for (int32_t j = 0; j < 2 * I; ++j) {
+                    const double sj = das_all[f * 2 * I + j];
+                    if (sj == 0.0)
+                        continue;
+                    for (int32_t c = 0; c < H; ++c)
+                        sdx[t * (int64_t)H + c] +=
+                            fabs(wget(wkind, w13, NULL, H, b13 + (int64_t)j * H + c)) * sj;
+                }
         }
         free(a);
         free(g);
@@ -363,6 +488,8 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
     if (dw13 == NULL || dw2 == NULL) {
         free(da_all);
         free(sh_all);
+        free(das_all);
+        free(shs_all);
         return;
     }
 #pragma omp parallel for schedule(dynamic, 1)
@@ -371,6 +498,12 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
         double *DW2 = dw2 + (int64_t)e * H * I;
         memset(DW13, 0, sizeof(double) * (size_t)(2 * (int64_t)I * H));
         memset(DW2, 0, sizeof(double) * (size_t)((int64_t)H * I));
+        double *S13 = sdw13 ? sdw13 + (int64_t)e * 2 * I * H : NULL;
+        double *S2 = sdw2 ? sdw2 + (int64_t)e * H * I : NULL;
+        if (S13)
+            memset(S13, 0, sizeof(double) * (size_t)(2 * (int64_t)I * H));
+        if (S2)
+            memset(S2, 0, sizeof(double) * (size_t)((int64_t)H * I));
         for (int64_t f = 0; f < R; ++f) {
             if (idx[f] != e)
                 continue;
@@ -385,10 +518,26 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
             for (int32_t c = 0; c < H; ++c)
                 for (int32_t i = 0; i < I; ++i)
                     DW2[(int64_t)c * I + i] += dyt[c] * sh[i];
+            if (want_slack && S13 && S2) {
+                for (int32_t j = 0; j < 2 * I; ++j) {
+                    const double sj = das_all[f * 2 * I + j];
+                    if (sj != 0.0)
+                        for (int32_t c = 0; c < H; ++c)
+                            S13[(int64_t)j * H + c] += sj * fabs(xt[c]);
+                }
+                for (int32_t i = 0; i < I; ++i) {
+                    const double si = shs_all[f * I + i];
+                    if (si != 0.0)
+                        for (int32_t c = 0; c < H; ++c)
+                            S2[(int64_t)c * I + i] += fabs(dyt[c]) * si;
+                }
+            }
         }
     }
     free(da_all);
     free(sh_all);
+    free(das_all);
+    free(shs_all);
 }
 
 void oracle_router_grad(int64_t T, int32_t E, int32_t K, const int32_t *idx, const double *w,

@@ -62,6 +62,17 @@ void oracle_mxfp8_quantize_bf16(int64_t rows, int64_t cols, const uint16_t *src,
 /* bf16 rounding of a real value: nearest, ties to even, with bf16 subnormals. */
 double oracle_round_bf16(double v);
 
+/* Rounding slack. A kernel computes the value it rounds (h, dA, w*h) in fp32, with a
+ * relative error of a few fp32 ulps; when the exact value lies that close to a rounding
+ * midpoint, the kernel may round to the other neighbour, and both results are correct.
+ * The slack of a decision is the distance between its two possible results when the
+ * exact value lies within ORACLE_SLACK_REL of a midpoint (for MXFP8, also when the block's
+ * amax lies that close to a power of two), else 0. The forward and backward propagate
+ * these slacks linearly (through |weights|, |x|, |dy|) to bounds on how far a correct
+ * result may lie from the oracle's; parity tests subtract them before comparing. */
+#define ORACLE_SLACK_REL 3.814697265625e-06 /* 2^-18 */
+double oracle_bf16_slack(double v);
+
 /* Precision modes ([arex] section "pull 代替 push": the layer has a BF16 and an MXFP8
  * mode; in MXFP8 mode activations are quantized where they enter the GEMMs, at dispatch
  * and at SwiGLU). Read here as: the operands of every expert GEMM carry the mode's type.
@@ -81,7 +92,7 @@ enum { ORACLE_EXACT = 0, ORACLE_BF16 = 1, ORACLE_MXFP8 = 2 };
 void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
                     const int32_t *idx, const double *w, int32_t wkind, const void *w13,
                     const uint8_t *w13_s, const void *w2, const uint8_t *w2_s, int32_t mode,
-                    double *y);
+                    double *y, double *slack /* nullable [T][H] */);
 
 /* Backward of the BF16 layer by the chain rule, given dy [T][H]:
  *   g = W2[e]^T dy_t, dS[t,k] = <g, h>, dh = w g,
@@ -96,7 +107,8 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
 void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
                      const int32_t *idx, const double *w, int32_t wkind, const void *w13,
                      const void *w2, const double *dy, int32_t mode, double *dx, double *dw13,
-                     double *dw2, double *dtopk);
+                     double *dw2, double *dtopk, double *sdx /* nullable slacks */,
+                     double *sdw13, double *sdw2);
 
 /* Router-logit gradient through the top-k softmax: for a chosen expert j = idx[t,k],
  * dlogits[t,j] = w_k (dS_k - sum_m w_m dS_m); every other logit gets 0. */

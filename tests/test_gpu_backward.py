@@ -65,14 +65,15 @@ def same_bits(a, b):
 
 
 def check_all(g, idx, w, x, w13, w2, dy, E):
-    dx_o, dw13_o, dw2_o, dtk_o = oracle.backward(oracle.bf16_to_f64(x), idx, w, w13, w2,
-                                                 oracle.bf16_to_f64(dy), mode=oracle.BF16)
+    dx_o, dw13_o, dw2_o, dtk_o, sdx, sdw13, sdw2 = oracle.backward(
+        oracle.bf16_to_f64(x), idx, w, w13, w2, oracle.bf16_to_f64(dy), mode=oracle.BF16,
+        with_slack=True)
     dl_o = oracle.router_grad(idx, w, dtk_o, E)
-    for name, got, want in (("dx", g["dx"], dx_o), ("dw13", g["dw13"], dw13_o),
-                            ("dw2", g["dw2"], dw2_o), ("d_topk_w", g["dtk"], dtk_o),
-                            ("d_logits", g["dlg"], dl_o)):
-        err = rel_err(host(got).reshape(want.shape), want)
-        assert err <= TOL_BF16, (name, err)
+    for name, got, want, sl in (("dx", g["dx"], dx_o, sdx), ("dw13", g["dw13"], dw13_o, sdw13),
+                                ("dw2", g["dw2"], dw2_o, sdw2), ("d_topk_w", g["dtk"], dtk_o, None),
+                                ("d_logits", g["dlg"], dl_o, None)):
+        err = rel_err(host(got).reshape(want.shape), want, sl)
+        assert err <= TOL_BF16, (name, err, rel_err(host(got).reshape(want.shape), want))
 
 
 def test_tiny_config():
@@ -115,12 +116,12 @@ def test_full_size_bwd():
     remap[used] = np.arange(len(used), dtype=np.int32)
     xs = oracle.bf16_to_f64(d["x"][toks])
     dys = oracle.bf16_to_f64(d["dy"][toks])
-    dx_o, _, _, dtk_o = oracle.backward(xs, remap[idx_s], w[toks], d["w13"][used],
-                                        d["w2"][used], dys, weight_grads=False,
-                                        mode=oracle.BF16)
+    dx_o, _, _, dtk_o, sdx, _, _ = oracle.backward(xs, remap[idx_s], w[toks], d["w13"][used],
+                                                   d["w2"][used], dys, weight_grads=False,
+                                                   mode=oracle.BF16, with_slack=True)
     import torch
     tk = torch.from_numpy(toks).cuda()
-    assert rel_err(host(g["dx"][tk]), dx_o) <= TOL_BF16
+    assert rel_err(host(g["dx"][tk]), dx_o, sdx) <= TOL_BF16
     assert rel_err(host(g["dtk"][tk]), dtk_o) <= TOL_BF16
     dl_o = oracle.router_grad(idx_s, w[toks], dtk_o, cfg.E)
     assert rel_err(host(g["dlg"][tk]), dl_o) <= TOL_BF16
@@ -132,9 +133,11 @@ def test_full_size_bwd():
         t_e, k_e = np.nonzero(idx == e)
         order = np.argsort(t_e * cfg.K + k_e, kind="stable")
         t_e, k_e = t_e[order], k_e[order]
-        _, dw13_o, dw2_o, _ = oracle.backward(
+        _, dw13_o, dw2_o, _, _, s13, s2 = oracle.backward(
             oracle.bf16_to_f64(d["x"][t_e]), np.zeros((len(t_e), 1), np.int32),
             w[t_e, k_e][:, None], d["w13"][e:e + 1], d["w2"][e:e + 1],
-            oracle.bf16_to_f64(d["dy"][t_e]), mode=oracle.BF16)
-        assert rel_err(host(g["dw13"][e]).reshape(-1), dw13_o.reshape(-1)) <= TOL_BF16, e
-        assert rel_err(host(g["dw2"][e]).reshape(-1), dw2_o.reshape(-1)) <= TOL_BF16, e
+            oracle.bf16_to_f64(d["dy"][t_e]), mode=oracle.BF16, with_slack=True)
+        g13 = host(g["dw13"][e]).reshape(-1)
+        g2 = host(g["dw2"][e]).reshape(-1)
+        assert rel_err(g13, dw13_o.reshape(-1), s13) <= TOL_BF16, (e, rel_err(g13, dw13_o.reshape(-1)))
+        assert rel_err(g2, dw2_o.reshape(-1), s2) <= TOL_BF16, (e, rel_err(g2, dw2_o.reshape(-1)))

@@ -56,8 +56,9 @@ def oracle_y(x, idx, w, w13, w2, mx):
         q13, s13 = oracle.mxfp8_quantize_bf16(w13)
         q2, s2 = oracle.mxfp8_quantize_bf16(w2)
         return oracle.forward(oracle.bf16_to_f64(x), idx, w, (q13, s13), (q2, s2),
-                              mode=oracle.MXFP8)
-    return oracle.forward(oracle.bf16_to_f64(x), idx, w, w13, w2, mode=oracle.BF16)
+                              mode=oracle.MXFP8, with_slack=True)
+    return oracle.forward(oracle.bf16_to_f64(x), idx, w, w13, w2, mode=oracle.BF16,
+                          with_slack=True)
 
 
 @pytest.mark.parametrize("prec", [B.MOK_BF16, B.MOK_MXFP8])
@@ -67,8 +68,8 @@ def test_tiny_config(prec):
     g = gpu_forward((cfg.T, cfg.H, cfg.I, cfg.E, cfg.K), d["x"], d["logits"], d["w13"],
                     d["w2"], prec, cfg.minibatch, cfg.ring_capacity, reps=3)
     mx = prec == B.MOK_MXFP8
-    y_o = oracle_y(d["x"], g["idx"], g["w"], d["w13"], d["w2"], mx)
-    err = rel_err(g["y"][0], y_o)
+    y_o, sl = oracle_y(d["x"], g["idx"], g["w"], d["w13"], d["w2"], mx)
+    err = rel_err(g["y"][0], y_o, sl)
     assert err <= (TOL_MXFP8 if mx else TOL_BF16), err
     for y in g["y"][1:]:
         np.testing.assert_array_equal(y, g["y"][0])  # bitwise run to run
@@ -87,8 +88,8 @@ def test_ragged_multi_pass_rings(prec):
     for g in outs[1:]:
         np.testing.assert_array_equal(g["y"][0], outs[0]["y"][0])
     mx = prec == B.MOK_MXFP8
-    y_o = oracle_y(x, outs[0]["idx"], outs[0]["w"], w13, w2, mx)
-    err = rel_err(outs[0]["y"][0], y_o)
+    y_o, sl = oracle_y(x, outs[0]["idx"], outs[0]["w"], w13, w2, mx)
+    err = rel_err(outs[0]["y"][0], y_o, sl)
     assert err <= (TOL_MXFP8 if mx else TOL_BF16), err
 
 
@@ -97,8 +98,8 @@ def test_ragged_multi_pass_rings(prec):
 def test_edge_shapes(dims):
     x, lg, w13, w2 = small_case(*dims, seed=sum(dims))
     g = gpu_forward(dims, x, lg, w13, w2, B.MOK_BF16, 37, 0)
-    y_o = oracle_y(x, g["idx"], g["w"], w13, w2, False)
-    assert rel_err(g["y"][0], y_o) <= TOL_BF16
+    y_o, sl = oracle_y(x, g["idx"], g["w"], w13, w2, False)
+    assert rel_err(g["y"][0], y_o, sl) <= TOL_BF16
 
 
 def test_empty_batch():
@@ -147,9 +148,9 @@ def full_case(name, n_tokens=256):
         wo = ((q13, s13), (q2, s2))
     else:
         wo = (d["w13"], d["w2"])
-    y_o = oracle_forward_tokens(toks, d["x"], g["idx"], g["w"], wo[0], wo[1],
-                                mode=oracle.MXFP8 if mx else oracle.BF16)
-    err = rel_err(g["y"][0][toks], y_o)
+    y_o, sl = oracle_forward_tokens(toks, d["x"], g["idx"], g["w"], wo[0], wo[1],
+                                    mode=oracle.MXFP8 if mx else oracle.BF16)
+    err = rel_err(g["y"][0][toks], y_o, sl)
     assert err <= (TOL_MXFP8 if mx else TOL_BF16), err
     return g
 

@@ -423,3 +423,51 @@ def test_weight_storage_kinds_agree_exactly():
     g_wide = oracle.backward(x, idx, w, oracle.bf16_to_f64(b13), oracle.bf16_to_f64(b2), dy)
     for a, b in zip(g_bits, g_wide):
         np.testing.assert_array_equal(a, b)
+
+
+def test_bf16_slack_marks_exactly_the_decisions_a_small_error_can_flip():
+    r = np.random.default_rng(21)
+    f = (r.standard_normal(3000) * np.exp(r.uniform(-30, 30, 3000))).astype(np.float32)
+    u = f.view(np.uint32) & ~np.uint32(0xFFFF)
+    lo = u.view(np.float32).astype(np.float64)
+    hi = (u + np.uint32(0x10000)).view(np.float32).astype(np.float64)
+    mid = (lo + hi) / 2  # exact midpoints between bf16 neighbours
+    rel = 2.0 ** -18
+    for m, a, b in zip(mid[:500], lo[:500], hi[:500]):
+        for v in (m, m * (1 + rel / 4), m * (1 - rel / 4)):
+            # the two fp32-sized perturbations of v round to different neighbours
+            down = torch.tensor(v * (1 - rel / 2)).float().to(torch.bfloat16).double().item()
+            up = torch.tensor(v * (1 + rel / 2)).float().to(torch.bfloat16).double().item()
+            assert oracle.bf16_slack(v) == abs(b - a) >= abs(up - down)
+        assert oracle.bf16_slack(m * (1 + 2.0 ** -12)) == 0.0
+    for v in lo[:500]:  # representable values are far from every midpoint
+        assert oracle.bf16_slack(v) == 0.0
+
+
+def test_forward_slack_in_the_identity_structure():
+    """With one expert, K=1, weight 1 and W2 = identity, y = bf16(h) and the slack of y_c is
+    the slack of the single decision h_c."""
+    T, H, I = 64, 32, 32
+    r = np.random.default_rng(22)
+    x = r.standard_normal((T, H))
+    w13 = r.standard_normal((1, 2 * I, H)) * 0.2
+    idx = np.zeros((T, 1), np.int32)
+    y, sl = oracle.forward(x, idx, np.ones((T, 1)), w13, np.eye(H)[None], mode=oracle.BF16,
+                           with_slack=True)
+    a = x @ w13[0].T
+    h = _silu(a[:, :I]) * a[:, I:]
+    want = np.array([oracle.bf16_slack(v) for v in h.reshape(-1)]).reshape(h.shape)
+    np.testing.assert_array_equal(sl, want)
+    _, sl0 = oracle.forward(x, idx, np.ones((T, 1)), w13, np.eye(H)[None], with_slack=True)
+    assert np.all(sl0 == 0.0)  # exact mode rounds nothing
+
+
+def test_backward_slack_zero_in_exact_mode_and_bounds_flipped_operands():
+    T, H, I, E, K = 16, 32, 32, 2, 2
+    x, logits, w13, w2 = _rand_layer(T, H, I, E, K, seed=23)
+    dy = np.random.default_rng(24).standard_normal((T, H))
+    idx, w = oracle.route(logits, K)
+    out0 = oracle.backward(x, idx, w, w13, w2, dy, with_slack=True)
+    assert all(np.all(s == 0) for s in out0[4:])
+    out = oracle.backward(x, idx, w, w13, w2, dy, mode=oracle.BF16, with_slack=True)
+    assert all(np.all(s >= 0) for s in out[4:])

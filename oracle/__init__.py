@@ -47,7 +47,7 @@ def lib():
         L.oracle_forward.argtypes = [i64, i32, i32, i32, i32, p, p, p, i32, p, p, p, p, i32, p, p]
         L.oracle_backward.argtypes = [i64, i32, i32, i32, i32, p, p, p, i32, p, p, p, i32, p,
                                       p, p, p, p, p, p]
-        L.oracle_bf16_slack.argtypes = [ctypes.c_double]
+        L.oracle_bf16_slack.argtypes = [ctypes.c_double, ctypes.c_double]
         L.oracle_bf16_slack.restype = ctypes.c_double
         L.oracle_round_bf16.argtypes = [ctypes.c_double]
         L.oracle_round_bf16.restype = ctypes.c_double
@@ -156,8 +156,9 @@ def _weights(w):
     return W_F64, w, None, w.shape
 
 
-def bf16_slack(v: float) -> float:
-    return float(lib().oracle_bf16_slack(float(v)))
+def bf16_slack(v: float, err: float = 0.0) -> float:
+    """Slack of rounding v to bf16 when the value is only known to within err."""
+    return float(lib().oracle_bf16_slack(float(v), float(err)))
 
 
 def forward(x, idx, w, w13, w2, mode=EXACT, with_slack=False):

@@ -244,7 +244,7 @@ static void qdq_row(int64_t n, double *v)
  * possible results when the exact value lies within ORACLE_SLACK_REL of a midpoint (or, for
  * an MXFP8 block, of a scale-exponent boundary), and 0 otherwise. */
 
-double oracle_bf16_slack(double v)
+double oracle_bf16_slack(double v, double err)
 {
     if (v == 0.0 || !isfinite(v))
         return 0.0;
@@ -256,11 +256,12 @@ double oracle_bf16_slack(double v)
     const double ulp = ldexp(1.0, e - 7);
     const double q = fabs(v) / ulp;
     const double dist = fabs((q - floor(q)) - 0.5) * ulp;
-    return dist <= ORACLE_SLACK_REL * fabs(v) ? ulp : 0.0;
+    return dist <= err + ORACLE_SLACK_REL * fabs(v) ? ulp : 0.0;
 }
 
-/* slack of the E4M3 code of a scaled value u (saturation at 448 is one-sided: none) */
-static double e4m3_slack(double u)
+/* slack of the E4M3 code of a scaled value u known to within err_u (saturation at 448 is
+ * one-sided: none) */
+static double e4m3_slack(double u, double err_u)
 {
     const double a = fabs(u);
     if (a == 0.0 || a >= 448.0)
@@ -273,22 +274,26 @@ static double e4m3_slack(double u)
     const double sp = ldexp(1.0, e - 3);
     const double q = a / sp;
     const double dist = fabs((q - floor(q)) - 0.5) * sp;
-    return dist <= ORACLE_SLACK_REL * a ? sp : 0.0;
+    return dist <= err_u + ORACLE_SLACK_REL * a ? sp : 0.0;
 }
 
 /* MXFP8 quantize-dequantize of one row along its 32-element blocks, with each element's
  * slack: the code decision's slack, and when the block's amax is that close to a power of
  * two (the shared exponent could go either way) the difference to the other exponent's
  * result as well. */
-static void qdq_row_slack(int64_t n, double *v, double *slack)
+static void qdq_row_slack(int64_t n, double *v, const double *err, double *slack)
 {
     double alt[32];
     for (int64_t b = 0; b < n / 32; ++b) {
         double *blk = v + b * 32, *sl = slack + b * 32;
-        double amax = 0.0;
-        for (int i = 0; i < 32; ++i)
+        const double *eb = err + b * 32;
+        double amax = 0.0, emax = 0.0;
+        for (int i = 0; i < 32; ++i) {
             if (fabs(blk[i]) > amax)
                 amax = fabs(blk[i]);
+            if (eb[i] > emax)
+                emax = eb[i];
+        }
         int ex = 0;
         if (amax > 0.0)
             frexp(amax, &ex);
@@ -296,13 +301,14 @@ static void qdq_row_slack(int64_t n, double *v, double *slack)
         /* the nearer power of two decides which other exponent is possible */
         const double p_lo = ldexp(1.0, ex - 1), p_hi = ldexp(1.0, ex);
         int other = 0;
-        if (amax > 0.0 && sexp > -127 && amax - p_lo <= ORACLE_SLACK_REL * amax)
+        const double tol = emax + ORACLE_SLACK_REL * amax;
+        if (amax > 0.0 && sexp > -127 && amax - p_lo <= tol)
             other = -1;
-        else if (amax > 0.0 && p_hi - amax <= ORACLE_SLACK_REL * amax)
+        else if (amax > 0.0 && p_hi - amax <= tol)
             other = +1;
+        const int sx = sexp < -127 ? -127 : sexp;
         for (int i = 0; i < 32; ++i)
-            sl[i] = ldexp(e4m3_slack(ldexp(blk[i], -(sexp < -127 ? -127 : sexp))),
-                          sexp < -127 ? -127 : sexp);
+            sl[i] = ldexp(e4m3_slack(ldexp(blk[i], -sx), ldexp(eb[i], -sx)), sx);
         if (other != 0) {
             int s2 = sexp + other;
             if (s2 < -127)
@@ -325,6 +331,16 @@ static void qdq_row_slack(int64_t n, double *v, double *slack)
 /* ---------------------------------------------------------------- forward */
 
 static double silu(double g) { return g / (1.0 + exp(-g)); }
+static double dsilu(double g)
+{
+    const double sg = 1.0 / (1.0 + exp(-g));
+    return sg * (1.0 + g * (1.0 - sg));
+}
+static double d2silu(double g)
+{
+    const double sg = 1.0 / (1.0 + exp(-g));
+    return sg * (1.0 - sg) * (2.0 + g * (1.0 - 2.0 * sg));
+}
 
 void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
                     const int32_t *idx, const double *w, int32_t wkind, const void *w13,
@@ -338,6 +354,8 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
         double *a = (double *)malloc(sizeof(double) * 2 * (size_t)I);
         double *h = (double *)malloc(sizeof(double) * (size_t)I);
         double *hs = (double *)calloc((size_t)I, sizeof(double));
+        double *aa = (double *)malloc(sizeof(double) * 2 * (size_t)I); /* sum |W13||x| */
+        double *he = (double *)malloc(sizeof(double) * (size_t)I);     /* error bound of h */
         double *yt = y + t * (int64_t)H;
         double *st = slack ? slack + t * (int64_t)H : NULL;
         memcpy(xt, x + t * (int64_t)H, sizeof(double) * (size_t)H);
@@ -352,18 +370,26 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
             const int64_t e = idx[t * K + k];
             const int64_t b13 = e * 2 * (int64_t)I * H, b2 = e * (int64_t)H * I;
             for (int32_t j = 0; j < 2 * I; ++j) {
-                double acc = 0.0;
-                for (int32_t c = 0; c < H; ++c)
-                    acc += wget(wkind, w13, w13_s, H, b13 + (int64_t)j * H + c) * xt[c];
+                double acc = 0.0, mag = 0.0;
+                for (int32_t c = 0; c < H; ++c) {
+                    const double wv = wget(wkind, w13, w13_s, H, b13 + (int64_t)j * H + c);
+                    acc += wv * xt[c];
+                    mag += fabs(wv * xt[c]);
+                }
                 a[j] = acc;
+                aa[j] = mag;
             }
-            for (int32_t i = 0; i < I; ++i)
+            for (int32_t i = 0; i < I; ++i) {
                 h[i] = silu(a[i]) * a[I + i];
+                /* how far a kernel's fp32 h can be from this one */
+                he[i] = fabs(dsilu(a[i]) * a[I + i]) * ORACLE_DOT_REL * aa[i] +
+                        fabs(silu(a[i])) * ORACLE_DOT_REL * aa[I + i];
+            }
             if (mode == ORACLE_MXFP8) {
-                qdq_row_slack(I, h, hs);
+                qdq_row_slack(I, h, he, hs);
             } else if (mode == ORACLE_BF16) {
                 for (int32_t i = 0; i < I; ++i) {
-                    hs[i] = oracle_bf16_slack(h[i]);
+                    hs[i] = oracle_bf16_slack(h[i], he[i]);
                     h[i] = oracle_round_bf16(h[i]);
                 }
             }
@@ -388,6 +414,8 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
         free(a);
         free(h);
         free(hs);
+        free(aa);
+        free(he);
     }
 }
 
@@ -416,6 +444,8 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
         double *dxt = dx + t * (int64_t)H;
         double *a = (double *)malloc(sizeof(double) * 2 * (size_t)I);
         double *g = (double *)malloc(sizeof(double) * (size_t)I);
+        double *aa = (double *)malloc(sizeof(double) * 2 * (size_t)I); /* sum |W13||x| */
+        double *gg = (double *)malloc(sizeof(double) * (size_t)I);     /* sum |W2||dy| */
         for (int32_t c = 0; c < H; ++c)
             dxt[c] = 0.0;
         for (int32_t k = 0; k < K; ++k) {
@@ -426,17 +456,25 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
             double *da = da_all + f * 2 * I;
             double *sh = sh_all + f * I;
             for (int32_t j = 0; j < 2 * I; ++j) {
-                double acc = 0.0;
-                for (int32_t c = 0; c < H; ++c)
-                    acc += wget(wkind, w13, NULL, H, b13 + (int64_t)j * H + c) * xt[c];
+                double acc = 0.0, mag = 0.0;
+                for (int32_t c = 0; c < H; ++c) {
+                    const double wv = wget(wkind, w13, NULL, H, b13 + (int64_t)j * H + c);
+                    acc += wv * xt[c];
+                    mag += fabs(wv * xt[c]);
+                }
                 a[j] = acc;
+                aa[j] = mag;
             }
             /* g = W2^T dy */
             for (int32_t i = 0; i < I; ++i) {
-                double acc = 0.0;
-                for (int32_t c = 0; c < H; ++c)
-                    acc += wget(wkind, w2, NULL, I, b2 + (int64_t)c * I + i) * dyt[c];
+                double acc = 0.0, mag = 0.0;
+                for (int32_t c = 0; c < H; ++c) {
+                    const double wv = wget(wkind, w2, NULL, I, b2 + (int64_t)c * I + i);
+                    acc += wv * dyt[c];
+                    mag += fabs(wv * dyt[c]);
+                }
                 g[i] = acc;
+                gg[i] = mag;
             }
             double dS = 0.0;
             for (int32_t i = 0; i < I; ++i) {
@@ -452,16 +490,27 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
                 sh[i] = s * hi;
             }
             if (mode == ORACLE_BF16) {
-                for (int32_t j = 0; j < 2 * I; ++j) {
-                    if (want_slack)
-                        das_all[f * 2 * I + j] = oracle_bf16_slack(da[j]);
+                if (want_slack)
+                    for (int32_t i = 0; i < I; ++i) {
+                        /* how far a kernel's fp32 values can be from these: first-order
+                         * propagation of the dot products' error bounds */
+                        const double ag = a[i], au = a[I + i], gi = g[i];
+                        const double eag = ORACLE_DOT_REL * aa[i];
+                        const double eau = ORACLE_DOT_REL * aa[I + i];
+                        const double eg = ORACLE_DOT_REL * gg[i];
+                        const double sl = silu(ag), d1 = dsilu(ag), d2 = d2silu(ag);
+                        const double e_dag = fabs(s) * (fabs(au * d1) * eg + fabs(gi * d1) * eau +
+                                                         fabs(gi * au * d2) * eag);
+                        const double e_dau = fabs(s) * (fabs(sl) * eg + fabs(gi * d1) * eag);
+                        const double e_sh = fabs(s) * (fabs(d1 * au) * eag + fabs(sl) * eau);
+                        das_all[f * 2 * I + i] = oracle_bf16_slack(da[i], e_dag);
+                        das_all[f * 2 * I + I + i] = oracle_bf16_slack(da[I + i], e_dau);
+                        shs_all[f * I + i] = oracle_bf16_slack(sh[i], e_sh);
+                    }
+                for (int32_t j = 0; j < 2 * I; ++j)
                     da[j] = oracle_round_bf16(da[j]);
-                }
-                for (int32_t i = 0; i < I; ++i) {
-                    if (want_slack)
-                        shs_all[f * I + i] = oracle_bf16_slack(sh[i]);
+                for (int32_t i = 0; i < I; ++i)
                     sh[i] = oracle_round_bf16(sh[i]);
-                }
             }
             dtopk[f] = dS;
             /* dx += W13^T da */
@@ -483,6 +532,8 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
         }
         free(a);
         free(g);
+        free(aa);
+        free(gg);
     }
 
     if (dw13 == NULL || dw2 == NULL) {

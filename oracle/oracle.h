@@ -62,16 +62,19 @@ void oracle_mxfp8_quantize_bf16(int64_t rows, int64_t cols, const uint16_t *src,
 /* bf16 rounding of a real value: nearest, ties to even, with bf16 subnormals. */
 double oracle_round_bf16(double v);
 
-/* Rounding slack. A kernel computes the value it rounds (h, dA, w*h) in fp32, with a
- * relative error of a few fp32 ulps; when the exact value lies that close to a rounding
- * midpoint, the kernel may round to the other neighbour, and both results are correct.
- * The slack of a decision is the distance between its two possible results when the
- * exact value lies within ORACLE_SLACK_REL of a midpoint (for MXFP8, also when the block's
- * amax lies that close to a power of two), else 0. The forward and backward propagate
- * these slacks linearly (through |weights|, |x|, |dy|) to bounds on how far a correct
- * result may lie from the oracle's; parity tests subtract them before comparing. */
-#define ORACLE_SLACK_REL 3.814697265625e-06 /* 2^-18 */
-double oracle_bf16_slack(double v);
+/* Rounding slack. A kernel computes the value it rounds (h, dA, w*h) in fp32 from fp32 dot
+ * products, so its value may differ from the exact one by about ORACLE_DOT_REL times the
+ * sum of the dot products' absolute terms (propagated through the SwiGLU formulas), plus
+ * ORACLE_SLACK_REL of the value for the elementwise operations. When the exact value lies
+ * within that bound of a rounding midpoint, the kernel may round to the other neighbour
+ * and both results are correct. The slack of such a decision is the distance between its
+ * two possible results (for MXFP8 also when the block's amax lies that close to a power of
+ * two, which decides the shared exponent); otherwise it is 0. The forward and backward
+ * propagate these slacks linearly (through |weights|, |x|, |dy|) to bounds on how far a
+ * correct result may lie from the oracle's; parity tests subtract them before comparing. */
+#define ORACLE_SLACK_REL 9.5367431640625e-07 /* 2^-20 */
+#define ORACLE_DOT_REL 2.384185791015625e-07 /* 2^-22 */
+double oracle_bf16_slack(double v, double err);
 
 /* Precision modes ([arex] section "pull 代替 push": the layer has a BF16 and an MXFP8
  * mode; in MXFP8 mode activations are quantized where they enter the GEMMs, at dispatch

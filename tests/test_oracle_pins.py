@@ -432,16 +432,19 @@ def test_bf16_slack_marks_exactly_the_decisions_a_small_error_can_flip():
     lo = u.view(np.float32).astype(np.float64)
     hi = (u + np.uint32(0x10000)).view(np.float32).astype(np.float64)
     mid = (lo + hi) / 2  # exact midpoints between bf16 neighbours
-    rel = 2.0 ** -18
     for m, a, b in zip(mid[:500], lo[:500], hi[:500]):
-        for v in (m, m * (1 + rel / 4), m * (1 - rel / 4)):
-            # the two fp32-sized perturbations of v round to different neighbours
-            down = torch.tensor(v * (1 - rel / 2)).float().to(torch.bfloat16).double().item()
-            up = torch.tensor(v * (1 + rel / 2)).float().to(torch.bfloat16).double().item()
-            assert oracle.bf16_slack(v) == abs(b - a) >= abs(up - down)
-        assert oracle.bf16_slack(m * (1 + 2.0 ** -12)) == 0.0
+        err = abs(m) * 2.0 ** -16  # a value known to within err
+        for v in (m, m + err / 2, m - err / 2):
+            # values within err of v on either side round to different neighbours
+            down = torch.tensor(v - err * 0.9).float().to(torch.bfloat16).double().item()
+            up = torch.tensor(v + err * 0.9).float().to(torch.bfloat16).double().item()
+            assert oracle.bf16_slack(v, err) == abs(b - a) >= abs(up - down)
+        # with no error beyond the elementwise margin, points a bit off the midpoint are
+        # unambiguous
+        assert oracle.bf16_slack(m * (1 + 2.0 ** -12), 0.0) == 0.0
+        assert oracle.bf16_slack(m, 0.0) == abs(b - a)
     for v in lo[:500]:  # representable values are far from every midpoint
-        assert oracle.bf16_slack(v) == 0.0
+        assert oracle.bf16_slack(v, abs(v) * 2.0 ** -16) == 0.0
 
 
 def test_forward_slack_in_the_identity_structure():
@@ -456,8 +459,13 @@ def test_forward_slack_in_the_identity_structure():
                            with_slack=True)
     a = x @ w13[0].T
     h = _silu(a[:, :I]) * a[:, I:]
-    want = np.array([oracle.bf16_slack(v) for v in h.reshape(-1)]).reshape(h.shape)
-    np.testing.assert_array_equal(sl, want)
+    # the h error bound: dot-product bounds through the partial derivatives of silu(g)*u
+    mag = np.abs(x) @ np.abs(w13[0]).T * 2.0 ** -22
+    sig = 1 / (1 + np.exp(-a[:, :I]))
+    dsl = sig * (1 + a[:, :I] * (1 - sig))
+    err = np.abs(dsl * a[:, I:]) * mag[:, :I] + np.abs(_silu(a[:, :I])) * mag[:, I:]
+    want = np.array([oracle.bf16_slack(v, e) for v, e in zip(h.reshape(-1), err.reshape(-1))])
+    np.testing.assert_allclose(sl, want.reshape(h.shape), rtol=0, atol=0)
     _, sl0 = oracle.forward(x, idx, np.ones((T, 1)), w13, np.eye(H)[None], with_slack=True)
     assert np.all(sl0 == 0.0)  # exact mode rounds nothing
 

@@ -153,7 +153,7 @@ def run_mok(args):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local)
-    cfg = CONFIGS[WORKLOAD]
+    cfg = CONFIGS[args.workload]
     # weak scaling: each rank has its own tokens (seed shifted by rank), the same weights
     cfg_r = cfg.with_(seed=cfg.seed + 1000 * rank) if rank else cfg
     T, H, I, E, K = cfg.T, cfg.H, cfg.I, cfg.E, cfg.K
@@ -250,7 +250,9 @@ def run_mok(args):
     n_l = prof[dom][0] / args.steps
     bound, work = algorithmic(dom, cfg, n_l)
     avg_s = prof[dom][1] / prof[dom][0] * 1e-3
-    if bound == "tensor":
+    if bound is None:
+        roof = {"bound": None, "achieved": None, "peak": None, "unit": None, "frac": None}
+    elif bound == "tensor":
         achieved = work / avg_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_sust"],
                 "unit": "TFLOP/s", "frac": achieved / pk["bf16_sust"],
@@ -306,10 +308,12 @@ def run_mok(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Gaussian)",
-        "config": {"workload": "fwd+bwd BF16, 512 experts, H=4096, I=1024, top-10, T=16384",
+        "config": {"workload": "fwd+bwd BF16, %d experts, H=%d, I=%d, top-%d, T=%d" % (
+                       E, H, I, K, T),
                    "T": T, "H": H, "I": I, "E": E, "K": K, "minibatch": cfg.minibatch,
-                   "ring_capacity": "all rows", "l2": "inputs larger than L2 (12.9 GB of "
-                   "expert weights read per step)", "parallelism": "replicas" if world > 1
+                   "ring_capacity": "all rows", "l2": "inputs larger than L2 (%.1f GB of "
+                   "expert weights read per step)" % (3.0 * E * H * I * 2 / 1e9),
+                   "parallelism": "replicas" if world > 1
                    else "single GPU"},
         "e2e": {"value": world * flops_step / (ms_e * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e},
@@ -389,7 +393,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    cfg = CONFIGS[WORKLOAD]
+    cfg = CONFIGS[args.workload]
     host = dict(w13=synth.make_w13(cfg), w2=synth.make_w2(cfg), x=synth.make_x(cfg))
     n_tok, n_exp = args.ref_tokens, args.ref_experts
     for _ in range(args.warmup):
@@ -419,6 +423,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="mok", choices=["mok", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(CONFIGS))
     ap.add_argument("--no-mxfp8", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)

@@ -73,6 +73,8 @@ struct FwdWs {
     void *hring;
     uint8_t *hring_s;
     float *slots;
+    uint8_t *sf_w13, *sf_w2;  // MXFP8 weight scales as tensor-core atoms
+    uint8_t *sf_x, *sf_h;     // MXFP8 token-tile scales as atoms (per pass)
 };
 
 size_t carve_fwd(const mok_config *c, void *ws, FwdWs *o) {
@@ -85,8 +87,7 @@ size_t carve_fwd(const mok_config *c, void *ws, FwdWs *o) {
     const bool mx = c->prec == MOK_MXFP8;
     const int esz = mx ? 1 : 2;
     FwdWs w;
-    // the smallest tile height in use bounds the tile count
-    w.tiles_cap = tile_list_cap(pass_rows, c->E, gemm_tile_rows());
+    w.tiles_cap = tile_list_cap(pass_rows, c->E, gemm_tc_tile_rows(mx));
     int32_t *t = cv.take<int32_t>(16 + (size_t)w.tiles_cap * 16);
     w.tiles = t ? t + 4 : nullptr;
     w.xring = cv.take<void>((size_t)rr * c->H * esz);
@@ -94,6 +95,13 @@ size_t carve_fwd(const mok_config *c, void *ws, FwdWs *o) {
     w.hring = cv.take<void>((size_t)rr * c->I * esz);
     w.hring_s = mx ? cv.take<uint8_t>((size_t)rr * (c->I / 32)) : nullptr;
     w.slots = cv.take<float>((size_t)R * c->H * 4);
+    w.sf_w13 = w.sf_w2 = w.sf_x = w.sf_h = nullptr;
+    if (mx) {
+        w.sf_w13 = cv.take<uint8_t>((size_t)c->E * 2 * c->I * (c->H / 32));
+        w.sf_w2 = cv.take<uint8_t>((size_t)c->E * c->H * (c->I / 32));
+        w.sf_x = cv.take<uint8_t>((size_t)w.tiles_cap * (c->H / 128) * 1024);
+        w.sf_h = cv.take<uint8_t>((size_t)w.tiles_cap * (c->I / 128) * 1024);
+    }
     if (o) *o = w;
     return cv.off;
 }
@@ -114,18 +122,20 @@ size_t carve_bwd(const mok_config *c, void *ws, BwdWs *o) {
     BwdWs w;
     w.rpad_cap = R + 15 * (int64_t)c->E;
     w.poff = cv.take<int32_t>((size_t)(c->E + 1) * 4);
-    w.tiles_cap = tile_list_cap(R, c->E, gemm_tile_rows());
+    w.tiles_cap = tile_list_cap(R, c->E, gemm_tc_tile_rows(false));
     int32_t *t = cv.take<int32_t>(16 + (size_t)w.tiles_cap * 16);
     w.tiles = t ? t + 4 : nullptr;
     w.dy_perm = cv.take<uint16_t>((size_t)w.rpad_cap * c->H * 2);
     w.x_perm = cv.take<uint16_t>((size_t)w.rpad_cap * c->H * 2);
     w.dA = cv.take<uint16_t>((size_t)w.rpad_cap * 2 * c->I * 2);
     w.sh = cv.take<uint16_t>((size_t)w.rpad_cap * c->I * 2);
-    w.dS_part = cv.take<float>((size_t)R * (c->I / 128) * 4);
+    w.dS_part = cv.take<float>((size_t)R * gemm_tc_dS_parts(c->I) * 4);
     w.dx_slots = cv.take<float>((size_t)R * c->H * 4);
     if (o) *o = w;
     return cv.off;
 }
+
+cudaError_t first_error(cudaError_t a, cudaError_t b) { return a != cudaSuccess ? a : b; }
 
 mok_status check_ws(void *ws, size_t ws_bytes, size_t need) {
     if (need == 0) return MOK_OK;
@@ -269,10 +279,18 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
     ring_geom(c, &n_slots, &ring_rows);
     Ring ring{R, c->minibatch, n_slots};
     const int64_t n_pass = n_slots == 0 ? 1 : (R + c->minibatch - 1) / c->minibatch;
+    if (mx) {
+        // the weights' scales in the tensor cores' atom layout, once per call
+        MOK_LAUNCH(KK_SCALE_ATOMS, 2,
+                   first_error(launch_scale_atoms_rows(w13_scale, (int64_t)c->E * 2 * c->I,
+                                                       c->H, w.sf_w13, stream),
+                               launch_scale_atoms_rows(w2_scale, (int64_t)c->E * c->H, c->I,
+                                                       w.sf_w2, stream)));
+    }
     for (int64_t m = 0; m < n_pass; ++m) {
         const int64_t p0 = n_slots == 0 ? 0 : m * c->minibatch;
         const int64_t p1 = n_slots == 0 ? R : (p0 + c->minibatch < R ? p0 + c->minibatch : R);
-        const int chunk = mx ? gemm_tile_rows() : gemm_tc_tile_rows();
+        const int chunk = gemm_tc_tile_rows(mx);
         const int64_t cap = tile_list_cap(p1 - p0, c->E, chunk);
         MOK_LAUNCH(KK_TILES, 1,
                    launch_build_tiles(sch->offsets, c->E, p0, p1, chunk, w.tiles, cap, status,
@@ -291,8 +309,16 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
         GemmDownArgs da{w.tiles, cap, w.hring, w.hring_s, w2, w2_scale, sch->perm,
                         w.slots, c->H, c->I, c->E, mx, ring, status};
         if (mx) {
-            MOK_LAUNCH(KK_GEMM_UP, 1, launch_gemm_up(ua, stream));
-            MOK_LAUNCH(KK_GEMM_DOWN, 1, launch_gemm_down(da, stream));
+            MOK_LAUNCH(KK_SCALE_ATOMS, 1,
+                       launch_scale_atoms_tiles(w.tiles, cap, w.xring_s, R, c->minibatch, n_slots,
+                                                c->H, w.sf_x, stream));
+            MOK_LAUNCH(KK_GEMM_UP, 1,
+                       launch_gemm_up_tc_mx(ua, ring_rows, w.sf_w13, w.sf_x, stream));
+            MOK_LAUNCH(KK_SCALE_ATOMS, 1,
+                       launch_scale_atoms_tiles(w.tiles, cap, w.hring_s, R, c->minibatch, n_slots,
+                                                c->I, w.sf_h, stream));
+            MOK_LAUNCH(KK_GEMM_DOWN, 1,
+                       launch_gemm_down_tc_mx(da, ring_rows, w.sf_w2, w.sf_h, stream));
         } else {
             MOK_LAUNCH(KK_GEMM_UP, 1, launch_gemm_up_tc(ua, ring_rows, stream));
             MOK_LAUNCH(KK_GEMM_DOWN, 1, launch_gemm_down_tc(da, ring_rows, stream));
@@ -328,8 +354,8 @@ mok_status mok_backward(const mok_config *c, const void *x, const mok_schedule *
     const int E = c->E, H = c->H, I = c->I, K = c->K;
     MOK_LAUNCH(KK_PAD, 1, launch_pad_offsets(sch->counts, E, w.poff, stream));
     MOK_LAUNCH(KK_TILES, 1,
-               launch_build_tiles(sch->offsets, E, 0, R, gemm_tile_rows(), w.tiles, w.tiles_cap,
-                                  status, stream));
+               launch_build_tiles(sch->offsets, E, 0, R, gemm_tc_tile_rows(false), w.tiles,
+                                  w.tiles_cap, status, stream));
     MOK_LAUNCH(KK_GATHER_BWD, 1,
                launch_gather_bwd((const uint16_t *)dy, (const uint16_t *)x, sch->perm,
                                  sch->offsets, w.poff, E, K, H, w.rpad_cap, w.dy_perm, w.x_perm,
@@ -337,19 +363,23 @@ mok_status mok_backward(const mok_config *c, const void *x, const mok_schedule *
     GemmGArgs ga{w.tiles, w.tiles_cap, sch->offsets, w.poff, (const uint16_t *)w2, w.dy_perm,
                  (const float *)saved_preact, sch->perm, topk_w, w.dA, w.sh, w.dS_part, H, I,
                  status};
-    MOK_LAUNCH(KK_GEMM_G, 1, launch_gemm_g(ga, stream));
+    MOK_LAUNCH(KK_GEMM_G, 1, launch_gemm_g_tc(ga, E, w.rpad_cap, stream));
     MOK_LAUNCH(KK_ROUTER_GRAD, 1,
-               launch_router_grad(w.dS_part, I / 128, sch->inv, sch->offsets, topk_w, c->T, K,
-                                  E, d_topk_w, d_logits, stream));
+               launch_router_grad(w.dS_part, gemm_tc_dS_parts(I), sch->inv, sch->offsets,
+                                  topk_w, c->T, K, E, d_topk_w, d_logits, stream));
     GemmDgradArgs dg{w.tiles, w.tiles_cap, sch->offsets, w.poff, (const uint16_t *)w13, w.dA,
                      sch->perm, w.dx_slots, H, I, status};
-    MOK_LAUNCH(KK_GEMM_DGRAD, 1, launch_gemm_dgrad(dg, stream));
+    MOK_LAUNCH(KK_GEMM_DGRAD, 1, launch_gemm_dgrad_tc(dg, E, w.rpad_cap, stream));
     MOK_LAUNCH(KK_DX_REDUCE, 1,
                launch_combine(w.dx_slots, nullptr, c->T, K, H, (float *)dx, stream));
-    GemmWgradArgs w1{sch->counts, w.poff, w.dA, w.x_perm, (float *)dw13, E, 2 * I, H, status};
-    MOK_LAUNCH(KK_WGRAD13, 1, launch_gemm_wgrad(w1, stream));
-    GemmWgradArgs w2a{sch->counts, w.poff, w.dy_perm, w.sh, (float *)dw2, E, H, I, status};
-    MOK_LAUNCH(KK_WGRAD2, 1, launch_gemm_wgrad(w2a, stream));
+    // dW13[e] is [2I][H]: rows j (N) x contiguous c (M)
+    MOK_LAUNCH(KK_WGRAD13, 1,
+               launch_wgrad_tc(sch->counts, w.poff, w.x_perm, w.dA, (float *)dw13, E, H, 2 * I,
+                               w.rpad_cap, status, stream));
+    // dW2[e] is [H][I]: rows c (N) x contiguous i (M)
+    MOK_LAUNCH(KK_WGRAD2, 1,
+               launch_wgrad_tc(sch->counts, w.poff, w.sh, w.dy_perm, (float *)dw2, E, I, H,
+                               w.rpad_cap, status, stream));
     return MOK_OK;
 }
 

@@ -205,6 +205,49 @@ __global__ void __launch_bounds__(TPB)
     }
 }
 
+// ---------------------------------------------------------------- MXFP8 scale atoms
+// The tensor cores read an operand's E8M0 scales as atoms of 128 rows x 4 K-blocks (512
+// bytes: 32 rows of 16 bytes, row i holding the 4 scales of rows i, i+32, i+64, i+96).
+// Weights: plain [rows][K/32] -> atom (row/128, kg) at ((row/128) * K/128 + kg) * 512.
+__global__ void __launch_bounds__(TPB)
+    scale_atoms_rows_kernel(const uint8_t *__restrict__ src, int64_t rows, int K,
+                            uint8_t *__restrict__ dst) {
+    const int kgn = K / 128;
+    const int64_t total = rows * kgn;
+    const int64_t stride = (int64_t)gridDim.x * TPB;
+    for (int64_t i = (int64_t)blockIdx.x * TPB + threadIdx.x; i < total; i += stride) {
+        const int64_t row = i / kgn;
+        const int kg = (int)(i % kgn);
+        const uint32_t v = *reinterpret_cast<const uint32_t *>(src + row * (K / 32) + 4 * kg);
+        uint8_t *o = dst + ((row / 128) * kgn + kg) * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4;
+        *reinterpret_cast<uint32_t *>(o) = v;
+    }
+}
+
+// Token tiles: the rows n < 256 of tile t = (e, r0, r1) (rows past the tile get byte 0) ->
+// two atoms per 128-wide K block at (t * K/128 + kg) * 1024 + (n / 128) * 512.
+__global__ void __launch_bounds__(TPB)
+    scale_atoms_tiles_kernel(const int32_t *__restrict__ tiles, int64_t cap,
+                             const uint8_t *__restrict__ src, RingMap rm, int K,
+                             uint8_t *__restrict__ dst) {
+    const int kgn = K / 128;
+    const int64_t nt = tiles[-4] < cap ? tiles[-4] : cap;
+    const int64_t total = nt * 256 * kgn;
+    const int64_t stride = (int64_t)gridDim.x * TPB;
+    for (int64_t i = (int64_t)blockIdx.x * TPB + threadIdx.x; i < total; i += stride) {
+        const int kg = (int)(i % kgn);
+        const int n = (int)((i / kgn) % 256);
+        const int64_t t = i / ((int64_t)kgn * 256);
+        const int64_t r0 = tiles[4 * t + 1], r1 = tiles[4 * t + 2];
+        uint32_t v = 0;
+        if (n < r1 - r0)
+            v = *reinterpret_cast<const uint32_t *>(src + rm(r0 + n) * (K / 32) + 4 * kg);
+        uint8_t *o = dst + (t * kgn + kg) * 1024 + (n / 128) * 512 + (n % 32) * 16 +
+                     ((n % 128) / 32) * 4;
+        *reinterpret_cast<uint32_t *>(o) = v;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_gather_bf16(const uint16_t *x, const int32_t *perm, int K, int H, int64_t p0,
@@ -258,6 +301,28 @@ cudaError_t launch_router_grad(const float *dS_part, int n_parts, const int32_t 
     if (T == 0) return cudaSuccess;
     router_grad_kernel<<<grid_for(T, TPB / 32, 152 * 16), TPB, 0, s>>>(
         dS_part, n_parts, inv, offsets, w, T, K, E, d_topk, d_logits);
+    return cudaGetLastError();
+}
+
+}  // namespace mok
+
+namespace mok {
+
+cudaError_t launch_scale_atoms_rows(const uint8_t *src, int64_t rows, int K, uint8_t *dst,
+                                    cudaStream_t s) {
+    if (rows == 0) return cudaSuccess;
+    scale_atoms_rows_kernel<<<grid_for(rows * (K / 128), TPB, 152 * 16), TPB, 0, s>>>(src, rows,
+                                                                                     K, dst);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scale_atoms_tiles(const int32_t *tiles, int64_t cap, const uint8_t *src,
+                                     int64_t R, int MB, int n_slots, int K, uint8_t *dst,
+                                     cudaStream_t s) {
+    if (cap == 0) return cudaSuccess;
+    RingMap rm{R, MB, n_slots};
+    scale_atoms_tiles_kernel<<<grid_for(cap * 256 * (K / 128), TPB, 152 * 16), TPB, 0, s>>>(
+        tiles, cap, src, rm, K, dst);
     return cudaGetLastError();
 }
 

@@ -1,20 +1,28 @@
-// gemm_tc.cu -- expert-grouped GEMMs of the forward on the 5th-generation tensor cores.
+// gemm_tc.cu -- the expert-grouped GEMMs of the layer on the 5th-generation tensor cores.
 //
 // [alphalab] "Mixture-of-Kittens" (alphalab.site), section 一: routed experts run a SwiGLU
-// FFN (gate/up GEMM, SwiGLU, down GEMM); section 五: warp specialization and PTX.
+// FFN (gate/up GEMM, SwiGLU, down GEMM) and the backward computes expert gradients between
+// reverse-combine and reverse-dispatch; section 五: warp specialization and PTX.
 // [arex] "Cursor 放出 MoK" (arex-research.com), section "pull 代替 push": expert-grouped
-// GEMMs fed by a pull dispatch, results pushed back to their (token, k) slots.
+// GEMMs fed by pull dispatch, results pushed back to their (token, k) slots, and the
+// router-weight gradient computed inside the SwiGLU backward.
 //
-// One persistent kernel per GEMM, 192 threads per CTA, one CTA per SM:
-//   warp 0     TMA producer: weight tiles A0, A1 (128 rows each) and the token tile B
-//              (up to 256 rows) of each 64-wide K block into a 3-stage ring
-//   warp 1     TMEM owner and MMA issuer: D0 += A0 B^T, D1 += A1 B^T (M=128, N<=256, K=16
-//              per instruction), fp32 accumulators at TMEM columns 0 and 256
-//   warps 2-5  epilogue: TMEM -> registers -> fused SwiGLU / scatter -> global memory
-// Work unit = (token tile, weight block). Swapping the GEMM so that the weights are M and
-// the expert's routed rows are N keeps the ragged dimension at a 16-row granularity.
-// Every output element is one fixed-order fp32 dot product, so results do not depend on
-// which CTA computes a unit.
+// One persistent kernel template, 192 threads per CTA, one CTA per SM:
+//   warp 0     TMA producer: two 128-row A tiles and one B tile (up to 256 rows) per
+//              64-wide K block into a 3-stage shared-memory ring
+//   warp 1     TMEM owner and MMA issuer: D0 += A0 B^T, D1 += A1 B^T (M=128, N<=256,
+//              K=16 per instruction), fp32 accumulators at TMEM columns 0 and 256
+//   warps 2-5  epilogue: TMEM -> registers -> fused epilogue -> global memory
+// A problem policy supplies the work-unit decomposition, the operand majors and the
+// epilogue:
+//   FwdUp     A = W13 (K-major), B = x ring (K-major)      -> SwiGLU, h (bf16 / MXFP8)
+//   FwdDown   A = W2 (K-major),  B = h ring (K-major)      -> fp32 push scatter to slots
+//   BwdG      A = W2^T (MN-major), B = dy_perm (K-major)   -> SwiGLU backward, dA, w*h, dS
+//   BwdDgrad  A = W13^T (MN-major), B = dA (K-major)       -> fp32 reverse-dispatch scatter
+//   Wgrad     A, B MN-major over an expert's padded rows   -> fp32 dW
+// Every GEMM puts the weight (or output-contiguous) dimension on M and the routed rows on
+// N or K, so ragged experts cost at most 15 padding rows. Every output element is one
+// fixed-order fp32 dot product, independent of which CTA computes its unit.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -24,42 +32,22 @@
 namespace mok {
 namespace {
 
-constexpr int BK = 64;            // K elements per stage (128 bytes of bf16)
+constexpr int BK = 64;            // bf16 K elements per stage (128 bytes per row)
+constexpr int BK_MX = 128;        // E4M3 K elements per stage (128 bytes per row)
 constexpr int STAGES = 3;
-constexpr int TILE_ROWS = 256;    // max token rows per unit (N)
-constexpr int BOX_ROWS = 32;      // token rows per TMA box
-constexpr int A_BYTES = 128 * BK * 2;
-constexpr int B_BYTES = TILE_ROWS * BK * 2;
-constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
+constexpr int TILE_ROWS = 256;    // max N per unit (bf16)
+constexpr int TILE_ROWS_MX = 240; // max N per unit (MXFP8: TMEM also holds the scales)
+constexpr int KBOX_ROWS = 32;     // rows per TMA box of a K-major B operand
+constexpr int A_BYTES = 128 * 128;                // 128 rows x 128 bytes
+constexpr int B_BYTES = TILE_ROWS * 128;          // 256 rows x 128 bytes
+constexpr int SF_BYTES = 2048;    // MXFP8 scale atoms per stage: A0, A1 (512 B), B (1 KB)
 constexpr int NTHREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-
-struct PairArgs {
-    const int32_t *tiles;   // (e, r0, r1, _) list, count at tiles[-4]
-    int64_t tiles_cap;
-    int n_mblocks;          // weight blocks per tile
-    int k_blocks;           // K / BK
-    int a_rows_per_expert;  // rows of A per expert in the 2D A map
-    int a_off1;             // row offset of A1 relative to A0 inside the expert
-    int a_mb_stride;        // row step per weight block
-    Ring ring;
-    int *status;
-};
-
-struct EpiUpArgs {
-    void *hring;
-    uint8_t *hring_s;
-    float *preact;
-    int I;
-    bool mxfp8;
-};
-
-struct EpiDownArgs {
-    const int32_t *perm;
-    float *slots;
-    int H;
-};
+constexpr uint32_t SF_COL = 480;  // MXFP8: TMEM columns of the stage's scale atoms
+template <bool MX>
+__host__ __device__ constexpr int stage_bytes() { return 2 * A_BYTES + B_BYTES + (MX ? SF_BYTES : 0); }
+template <bool MX>
+__host__ __device__ constexpr int smem_bytes() { return STAGES * stage_bytes<MX>() + 1024 /*align*/ + 512; }
 
 struct Smem {
     uint64_t full[STAGES];
@@ -68,6 +56,17 @@ struct Smem {
     uint64_t tmem_empty;
     uint32_t tmem_base;
     int abort;
+};
+
+// One work unit as the producer and the MMA issuer see it.
+struct Geom {
+    int32_t ax0, ay0, ax1, ay1;  // first box of A0 and A1 (x innermost)
+    int32_t bx, by;              // first box of B
+    int n_mma;                   // N of each MMA (multiple of 16, <= 256)
+    int nbox;                    // B boxes per stage
+    int k_steps;                 // K steps of one MMA (16 bf16 or 32 E4M3 elements); 0 leaves
+                                 // the accumulators unwritten
+    int64_t sfa0, sfa1, sfb;     // MXFP8: byte offsets of the first stage's scale atoms
 };
 
 MOK_DEV float silu_f(float g) { return g / (1.0f + expf(-g)); }
@@ -90,18 +89,380 @@ MOK_DEV bool wait_or_abort(uint64_t *bar, uint32_t parity, int *status, volatile
     return true;
 }
 
-template <int KIND>  // 0: gate/up + SwiGLU, 1: down + push scatter
+// ---------------------------------------------------------------- problem policies
+
+// tile-based problems: units = tiles x weight blocks, tile = (e, r0, r1)
+struct TileUnits {
+    const int32_t *tiles;
+    int64_t cap;
+    int n_mblocks;
+    MOK_DEV int64_t count() const {
+        const int64_t n = tiles[-4] < cap ? tiles[-4] : cap;
+        return n * n_mblocks;
+    }
+    MOK_DEV void get(int64_t u, int *e, int64_t *r0, int64_t *r1, int *mb) const {
+        const int64_t t = u / n_mblocks;
+        *mb = (int)(u % n_mblocks);
+        *e = tiles[4 * t + 0];
+        *r0 = tiles[4 * t + 1];
+        *r1 = tiles[4 * t + 2];
+    }
+};
+
+// MXFP8 scale atoms: 128 rows x 4 blocks of 32 K elements as 32 rows of 16 bytes, row i
+// holding rows i, i+32, i+64, i+96 (4 bytes each, one per block). Weights: atom
+// (row/128, k/128) at ((row/128) * K/128 + k/128) * 512; token tiles: two atoms (rows
+// 0-127, 128-255 of the tile) per 128-wide K block at (tile * K/128 + k/128) * 1024.
+template <bool MXv>
+struct FwdUpT {
+    static constexpr bool A_MN = false, B_MN = false, MX = MXv;
+    TileUnits tu;
+    int H, I;
+    Ring ring;
+    void *hring;
+    uint8_t *hring_s;
+    float *preact;
+    bool mxfp8;
+    int *status;
+    const uint8_t *sf_a, *sf_b;
+
+    MOK_DEV int64_t n_units() const { return tu.count(); }
+    MOK_DEV Geom geom(int64_t u) const {
+        int e, mb;
+        int64_t r0, r1;
+        tu.get(u, &e, &r0, &r1, &mb);
+        const RingMap rm{ring.R, ring.MB, ring.n_slots};
+        Geom g;
+        g.ax0 = 0;
+        g.ay0 = e * 2 * I + mb * 128;
+        g.ax1 = 0;
+        g.ay1 = g.ay0 + I;
+        g.bx = 0;
+        g.by = (int32_t)rm(r0);
+        g.n_mma = (int)((r1 - r0 + 15) & ~15);
+        g.nbox = (int)((r1 - r0 + KBOX_ROWS - 1) / KBOX_ROWS);
+        g.k_steps = MX ? H / 32 : H / 16;
+        const int64_t kg = H / 128;
+        g.sfa0 = (int64_t)(g.ay0 / 128) * kg * 512;
+        g.sfa1 = (int64_t)(g.ay1 / 128) * kg * 512;
+        g.sfb = (u / tu.n_mblocks) * kg * 1024;
+        return g;
+    }
+    template <class LD>
+    MOK_DEV void epilogue(int64_t u, const LD &ld, Smem *, int q, int lane) const {
+        int e, mb;
+        int64_t r0, r1;
+        tu.get(u, &e, &r0, &r1, &mb);
+        const int nr = (int)(r1 - r0);
+        const int n_mma = (nr + 15) & ~15;
+        const RingMap rm{ring.R, ring.MB, ring.n_slots};
+        const int i = mb * 128 + q * 32 + lane;  // gate feature; its up feature is I + i
+        for (int n0 = 0; n0 < n_mma; n0 += 16) {
+            float d0[16], d1[16];
+            ld(n0, d0, d1);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int n = n0 + j;
+                const bool live = n < nr;
+                const int64_t r = r0 + n;
+                const float h = silu_f(d0[j]) * d1[j];
+                if (live && preact != nullptr) {
+                    preact[r * 2 * I + i] = d0[j];
+                    preact[r * 2 * I + I + i] = d1[j];
+                }
+                if (!mxfp8) {
+                    if (live) ((uint16_t *)hring)[rm(r) * I + i] = f32_to_bf16(h);
+                } else {
+                    // the warp's 32 lanes hold one 32-feature MXFP8 block of row r
+                    float amax = fabsf(h);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                    const uint32_t sb = mx_scale_byte(amax);
+                    const uint32_t code = e4m3x2(h * mx_inv_scale(sb), 0.f) & 0xFFu;
+                    if (live) {
+                        const int64_t slot = rm(r);
+                        ((uint8_t *)hring)[slot * I + i] = (uint8_t)code;
+                        if (lane == 0) hring_s[slot * (I / 32) + i / 32] = (uint8_t)sb;
+                    }
+                }
+            }
+        }
+    }
+};
+
+template <bool MXv>
+struct FwdDownT {
+    static constexpr bool A_MN = false, B_MN = false, MX = MXv;
+    TileUnits tu;
+    int H, I;
+    Ring ring;
+    const int32_t *perm;
+    float *slots;
+    int *status;
+    const uint8_t *sf_a, *sf_b;
+
+    MOK_DEV int64_t n_units() const { return tu.count(); }
+    MOK_DEV Geom geom(int64_t u) const {
+        int e, mb;
+        int64_t r0, r1;
+        tu.get(u, &e, &r0, &r1, &mb);
+        const RingMap rm{ring.R, ring.MB, ring.n_slots};
+        Geom g;
+        g.ax0 = 0;
+        g.ay0 = e * H + mb * 256;
+        g.ax1 = 0;
+        g.ay1 = g.ay0 + 128;
+        g.bx = 0;
+        g.by = (int32_t)rm(r0);
+        g.n_mma = (int)((r1 - r0 + 15) & ~15);
+        g.nbox = (int)((r1 - r0 + KBOX_ROWS - 1) / KBOX_ROWS);
+        g.k_steps = MX ? I / 32 : I / 16;
+        const int64_t kg = I / 128;
+        g.sfa0 = (int64_t)(g.ay0 / 128) * kg * 512;
+        // when H is not a multiple of 256 the last block's A1 lies past this expert (its
+        // results are discarded); keep its scale reads inside the expert
+        g.sfa1 = mb * 256 + 128 < H ? (int64_t)(g.ay1 / 128) * kg * 512 : g.sfa0;
+        g.sfb = (u / tu.n_mblocks) * kg * 1024;
+        return g;
+    }
+    template <class LD>
+    MOK_DEV void epilogue(int64_t u, const LD &ld, Smem *, int q, int lane) const {
+        int e, mb;
+        int64_t r0, r1;
+        tu.get(u, &e, &r0, &r1, &mb);
+        const int nr = (int)(r1 - r0);
+        const int n_mma = (nr + 15) & ~15;
+        const int c = mb * 256 + q * 32 + lane;
+        for (int n0 = 0; n0 < n_mma; n0 += 16) {
+            float d0[16], d1[16];
+            ld(n0, d0, d1);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int n = n0 + j;
+                if (n < nr) {
+                    const int64_t f = perm[r0 + n];
+                    slots[f * H + c] = d0[j];
+                    if (c + 128 < H) slots[f * H + c + 128] = d1[j];
+                }
+            }
+        }
+    }
+};
+
+// backward G GEMM: g[r][i] = sum_c W2[e][c][i] dy_perm[p(r)][c]; A0/A1 = features
+// [mb*256, +128) and [mb*256+128, +128) of W2^T (MN-major: W2 rows are c).
+struct BwdG {
+    static constexpr bool A_MN = true, B_MN = false, MX = false;
+    static constexpr const uint8_t *sf_a = nullptr, *sf_b = nullptr;
+    TileUnits tu;
+    int H, I;
+    const int32_t *offsets, *poff, *perm;
+    const float *preact, *topk_w;
+    uint16_t *dA, *sh;
+    float *dS_part;
+    int n_parts;
+    int *status;
+
+    MOK_DEV int64_t n_units() const { return tu.count(); }
+    MOK_DEV Geom geom(int64_t u) const {
+        int e, mb;
+        int64_t r0, r1;
+        tu.get(u, &e, &r0, &r1, &mb);
+        Geom g;
+        g.ax0 = mb * 256;
+        g.ay0 = e * H;
+        g.ax1 = g.ax0 + 128;
+        g.ay1 = e * H;
+        g.bx = 0;
+        g.by = (int32_t)(poff[e] + (r0 - offsets[e]));
+        g.n_mma = (int)((r1 - r0 + 15) & ~15);
+        g.nbox = (int)((r1 - r0 + KBOX_ROWS - 1) / KBOX_ROWS);
+        g.k_steps = H / 16;
+        return g;
+    }
+    template <class LD>
+    MOK_DEV void epilogue(int64_t u, const LD &ld, Smem *, int q, int lane) const {
+        int e, mb;
+        int64_t r0, r1;
+        tu.get(u, &e, &r0, &r1, &mb);
+        const int nr = (int)(r1 - r0);
+        const int n_mma = (nr + 15) & ~15;
+        const int64_t pb = poff[e] + (r0 - offsets[e]);
+        const bool last = r1 == offsets[e + 1];
+        const int i0 = mb * 256 + q * 32 + lane;
+        for (int n0 = 0; n0 < n_mma; n0 += 16) {
+            float d[2][16];
+            ld(n0, d[0], d[1]);
+            float part[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int n = n0 + j;
+                const int64_t p = pb + n;
+                float gh_sum = 0.f;
+#pragma unroll
+                for (int a = 0; a < 2; ++a) {
+                    const int i = i0 + a * 128;
+                    if (i >= I) continue;
+                    if (n < nr) {
+                        const int64_t r = r0 + n;
+                        const float ag = preact[r * 2 * I + i];
+                        const float au = preact[r * 2 * I + I + i];
+                        const float s = topk_w[perm[r]];
+                        const float g = d[a][j];
+                        const float sig = 1.0f / (1.0f + expf(-ag));
+                        const float sl = ag * sig;
+                        const float h = sl * au;
+                        const float dh = s * g;
+                        dA[p * 2 * I + i] = f32_to_bf16(dh * au * sig * (1.0f + ag * (1.0f - sig)));
+                        dA[p * 2 * I + I + i] = f32_to_bf16(dh * sl);
+                        sh[p * I + i] = f32_to_bf16(s * h);
+                        gh_sum += g * h;
+                    } else if (last) {  // zero pad rows up to the next multiple of 16
+                        dA[p * 2 * I + i] = 0;
+                        dA[p * 2 * I + I + i] = 0;
+                        sh[p * I + i] = 0;
+                    }
+                }
+                // fixed-order sum over the warp's 32 lanes
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) gh_sum += __shfl_xor_sync(0xFFFFFFFFu, gh_sum, o);
+                part[j] = gh_sum;
+            }
+            // one partial per (row, weight block, warp); the router-gradient kernel adds
+            // them in index order
+            if (lane < 16 && n0 + lane < nr) {
+                float v = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (j == lane) v = part[j];
+                dS_part[(r0 + n0 + lane) * n_parts + mb * 4 + q] = v;
+            }
+        }
+    }
+};
+
+// backward dgrad: dx_slots[perm[r]][c] = sum_j W13[e][j][c] dA[p(r)][j]; A = W13^T
+// (MN-major: W13 rows are j).
+struct BwdDgrad {
+    static constexpr bool A_MN = true, B_MN = false, MX = false;
+    static constexpr const uint8_t *sf_a = nullptr, *sf_b = nullptr;
+    TileUnits tu;
+    int H, I;
+    const int32_t *offsets, *poff, *perm;
+    float *dx_slots;
+    int *status;
+
+    MOK_DEV int64_t n_units() const { return tu.count(); }
+    MOK_DEV Geom geom(int64_t u) const {
+        int e, mb;
+        int64_t r0, r1;
+        tu.get(u, &e, &r0, &r1, &mb);
+        Geom g;
+        g.ax0 = mb * 256;
+        g.ay0 = e * 2 * I;
+        g.ax1 = g.ax0 + 128;
+        g.ay1 = e * 2 * I;
+        g.bx = 0;
+        g.by = (int32_t)(poff[e] + (r0 - offsets[e]));
+        g.n_mma = (int)((r1 - r0 + 15) & ~15);
+        g.nbox = (int)((r1 - r0 + KBOX_ROWS - 1) / KBOX_ROWS);
+        g.k_steps = 2 * I / 16;
+        return g;
+    }
+    template <class LD>
+    MOK_DEV void epilogue(int64_t u, const LD &ld, Smem *, int q, int lane) const {
+        int e, mb;
+        int64_t r0, r1;
+        tu.get(u, &e, &r0, &r1, &mb);
+        const int nr = (int)(r1 - r0);
+        const int n_mma = (nr + 15) & ~15;
+        const int c = mb * 256 + q * 32 + lane;
+        for (int n0 = 0; n0 < n_mma; n0 += 16) {
+            float d0[16], d1[16];
+            ld(n0, d0, d1);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int n = n0 + j;
+                if (n < nr) {
+                    const int64_t f = perm[r0 + n];
+                    dx_slots[f * H + c] = d0[j];
+                    if (c + 128 < H) dx_slots[f * H + c + 128] = d1[j];
+                }
+            }
+        }
+    }
+};
+
+// weight gradient of one expert: out[e][n][m] = sum over its padded rows p of
+// A[p][m] * B[p][n]; A, B row-major [rows][M] / [rows][N] (both MN-major operands).
+struct Wgrad {
+    static constexpr bool A_MN = true, B_MN = true, MX = false;
+    static constexpr const uint8_t *sf_a = nullptr, *sf_b = nullptr;
+    const int32_t *counts, *poff;
+    float *out;
+    int E, M, N;     // out is [E][N][M]
+    int nmb, nnb;    // ceil(M/256), ceil(N/256)
+    int *status;
+
+    MOK_DEV int64_t n_units() const { return (int64_t)E * nmb * nnb; }
+    MOK_DEV void get(int64_t u, int *e, int *mb, int *nb) const {
+        *e = (int)(u / ((int64_t)nmb * nnb));
+        const int rest = (int)(u % ((int64_t)nmb * nnb));
+        *nb = rest / nmb;
+        *mb = rest % nmb;
+    }
+    MOK_DEV Geom geom(int64_t u) const {
+        int e, mb, nb;
+        get(u, &e, &mb, &nb);
+        Geom g;
+        g.ax0 = mb * 256;
+        g.ay0 = poff[e];
+        g.ax1 = g.ax0 + 128;
+        g.ay1 = poff[e];
+        g.bx = nb * 256;
+        g.by = poff[e];
+        const int nn = N - nb * 256 < 256 ? N - nb * 256 : 256;
+        g.n_mma = nn;
+        g.nbox = nn / 64;
+        g.k_steps = ((counts[e] + 15) & ~15) / 16;
+        return g;
+    }
+    template <class LD>
+    MOK_DEV void epilogue(int64_t u, const LD &ld, Smem *, int q, int lane) const {
+        int e, mb, nb;
+        get(u, &e, &mb, &nb);
+        const int nn = N - nb * 256 < 256 ? N - nb * 256 : 256;
+        const bool any = counts[e] > 0;
+        const int m = mb * 256 + q * 32 + lane;
+        float *o = out + (int64_t)e * N * M;
+        for (int n0 = 0; n0 < nn; n0 += 16) {
+            float d0[16], d1[16];
+            ld(n0, d0, d1);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int64_t row = (int64_t)(nb * 256 + n0 + j) * M;
+                o[row + m] = any ? d0[j] : 0.f;
+                if (m + 128 < M) o[row + m + 128] = any ? d1[j] : 0.f;
+            }
+        }
+    }
+};
+
+// ---------------------------------------------------------------- the kernel
+template <class P>
 __global__ void __launch_bounds__(NTHREADS, 1)
-    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, PairArgs p, EpiUpArgs up,
-                     EpiDownArgs down) {
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB, const P p) {
+    constexpr bool MX = P::MX;
+    constexpr int SB = stage_bytes<MX>();
+    constexpr int BKE = MX ? BK_MX : BK;             // K elements per stage
+    constexpr uint32_t ACC1 = MX ? TILE_ROWS_MX : 256; // TMEM column of the second accumulator
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    Smem *sm = (Smem *)(base + STAGES * STAGE_BYTES);
+    Smem *sm = (Smem *)(base + STAGES * SB);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    const int64_t n_tiles = p.tiles[-4] < p.tiles_cap ? p.tiles[-4] : p.tiles_cap;
-    const int64_t n_units = n_tiles * p.n_mblocks;
+    const int64_t n_units = p.n_units();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -124,6 +485,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc::tc_fence_after();
     const uint32_t tmem = sm->tmem_base;
     volatile int *abort = &sm->abort;
+    constexpr int A_HALF = A_BYTES / 2;                        // one 64-wide MN-major box
+    constexpr int B_BOX = P::B_MN ? 64 * 128 : KBOX_ROWS * 128;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -132,25 +495,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             uint32_t ph = 0;
             int64_t issued = 0;
             for (int64_t u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
-                const int64_t t = u / p.n_mblocks;
-                const int mb = (int)(u % p.n_mblocks);
-                const int e = p.tiles[4 * t + 0];
-                const int64_t r0 = p.tiles[4 * t + 1], r1 = p.tiles[4 * t + 2];
-                const int nbox = (int)((r1 - r0 + BOX_ROWS - 1) / BOX_ROWS);
-                const RingMap rm{p.ring.R, p.ring.MB, p.ring.n_slots};
-                const int32_t brow = (int32_t)rm(r0);
-                const int32_t arow0 = e * p.a_rows_per_expert + mb * p.a_mb_stride;
-                const int32_t arow1 = arow0 + p.a_off1;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                const Geom g = p.geom(u);
+                const int kblocks = (g.k_steps + 3) / 4;
+                for (int kb = 0; kb < kblocks; ++kb) {
                     if (!wait_or_abort(&sm->empty[s], ph ^ 1u, p.status, abort)) break;
-                    uint8_t *st = base + s * STAGE_BYTES;
-                    tc::mbar_arrive_expect_tx(&sm->full[s],
-                                              2 * A_BYTES + nbox * BOX_ROWS * BK * 2);
-                    tc::tma_load_2d(st, &tmA, &sm->full[s], kb * BK, arow0);
-                    tc::tma_load_2d(st + A_BYTES, &tmA, &sm->full[s], kb * BK, arow1);
-                    for (int j = 0; j < nbox; ++j)
-                        tc::tma_load_2d(st + 2 * A_BYTES + j * BOX_ROWS * BK * 2, &tmB,
-                                        &sm->full[s], kb * BK, brow + j * BOX_ROWS);
+                    uint8_t *st = base + s * SB;
+                    uint64_t *fb = &sm->full[s];
+                    tc::mbar_arrive_expect_tx(fb, 2 * A_BYTES + g.nbox * B_BOX +
+                                                      (MX ? SF_BYTES : 0));
+                    const int k0 = kb * BKE;
+                    if (MX) {
+                        uint8_t *sf = st + 2 * A_BYTES + B_BYTES;
+                        tc::bulk_load(sf, p.sf_a + g.sfa0 + kb * 512, 512, fb);
+                        tc::bulk_load(sf + 512, p.sf_a + g.sfa1 + kb * 512, 512, fb);
+                        tc::bulk_load(sf + 1024, p.sf_b + g.sfb + kb * 1024, 1024, fb);
+                    }
+                    if (P::A_MN) {
+                        tc::tma_load_2d(st, &tmA, fb, g.ax0, g.ay0 + k0);
+                        tc::tma_load_2d(st + A_HALF, &tmA, fb, g.ax0 + 64, g.ay0 + k0);
+                        tc::tma_load_2d(st + A_BYTES, &tmA, fb, g.ax1, g.ay1 + k0);
+                        tc::tma_load_2d(st + A_BYTES + A_HALF, &tmA, fb, g.ax1 + 64, g.ay1 + k0);
+                    } else {
+                        tc::tma_load_2d(st, &tmA, fb, g.ax0 + k0, g.ay0);
+                        tc::tma_load_2d(st + A_BYTES, &tmA, fb, g.ax1 + k0, g.ay1);
+                    }
+                    uint8_t *bt = st + 2 * A_BYTES;
+                    for (int j = 0; j < g.nbox; ++j) {
+                        if (P::B_MN)
+                            tc::tma_load_2d(bt + j * B_BOX, &tmB, fb, g.bx + 64 * j, g.by + k0);
+                        else
+                            tc::tma_load_2d(bt + j * B_BOX, &tmB, fb, g.bx + k0,
+                                            g.by + KBOX_ROWS * j);
+                    }
                     ++issued;
                     if (++s == STAGES) {
                         s = 0;
@@ -176,30 +552,54 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             int s = 0;
             uint32_t ph = 0, acc_ph = 0;
             for (int64_t u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
-                const int64_t t = u / p.n_mblocks;
-                const int64_t r0 = p.tiles[4 * t + 1], r1 = p.tiles[4 * t + 2];
-                const int n_mma = (int)((r1 - r0 + 15) & ~15);
-                const uint32_t idesc = tc::idesc_bf16(128, n_mma, false, false);
+                const Geom g = p.geom(u);
+                const uint32_t idesc = tc::idesc_bf16(128, g.n_mma, P::A_MN, P::B_MN);
+                const uint32_t idesc_mx = tc::idesc_mxf8(128, g.n_mma, 0);
                 if (!wait_or_abort(&sm->tmem_empty, acc_ph ^ 1u, p.status, abort)) break;
                 tc::tc_fence_after();
+                const int kblocks = (g.k_steps + 3) / 4;
                 bool ok = true;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb = 0; kb < kblocks; ++kb) {
                     if (!wait_or_abort(&sm->full[s], ph, p.status, abort)) {
                         ok = false;
                         break;
                     }
                     tc::tc_fence_after();
-                    const uint32_t a0 = tc::smem_u32(base + s * STAGE_BYTES);
+                    const uint32_t a0 = tc::smem_u32(base + s * SB);
                     const uint32_t a1 = a0 + A_BYTES;
                     const uint32_t b = a0 + 2 * A_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t da0 = tc::sdesc_sw128(a0 + kk * 32, 16, 1024);
-                        const uint64_t da1 = tc::sdesc_sw128(a1 + kk * 32, 16, 1024);
-                        const uint64_t db = tc::sdesc_sw128(b + kk * 32, 16, 1024);
+                    const int steps = g.k_steps - kb * 4 < 4 ? g.k_steps - kb * 4 : 4;
+                    if (MX) {
+                        // this stage's scale atoms into TMEM: A0, A1, B rows 0-127, 128-255
+                        const uint32_t sf = b + B_BYTES;
+                        tc::tmem_cp_32x128b_x4(tmem + SF_COL + 0, tc::sdesc_plain_rows16(sf));
+                        tc::tmem_cp_32x128b_x4(tmem + SF_COL + 4, tc::sdesc_plain_rows16(sf + 512));
+                        tc::tmem_cp_32x128b_x4(tmem + SF_COL + 8, tc::sdesc_plain_rows16(sf + 1024));
+                        tc::tmem_cp_32x128b_x4(tmem + SF_COL + 12, tc::sdesc_plain_rows16(sf + 1536));
+                    }
+                    for (int kk = 0; kk < steps; ++kk) {
+                        // K-major: 16 elements = 32 bytes along the swizzled row;
+                        // MN-major: 16 K rows = 2 groups of eight 128-byte rows
+                        const uint32_t ao = P::A_MN ? kk * 2048 : kk * 32;
+                        const uint32_t bo = P::B_MN ? kk * 2048 : kk * 32;
+                        const uint32_t albo = P::A_MN ? A_HALF : 16;
+                        const uint32_t blbo = P::B_MN ? B_BOX : 16;
+                        const uint64_t da0 = tc::sdesc_sw128(a0 + ao, albo, 1024);
+                        const uint64_t da1 = tc::sdesc_sw128(a1 + ao, albo, 1024);
+                        const uint64_t db = tc::sdesc_sw128(b + bo, blbo, 1024);
                         const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-                        tc::mma_f16(tmem + 0, da0, db, idesc, acc);
-                        tc::mma_f16(tmem + 256, da1, db, idesc, acc);
+                        if (MX) {
+                            // byte kk of each 32-bit scale word is this K=32 block's scale
+                            const uint32_t id = idesc_mx | ((uint32_t)kk << 4) |
+                                                ((uint32_t)kk << 29);
+                            tc::mma_mxf8(tmem + 0, da0, db, id, tmem + SF_COL + 0,
+                                         tmem + SF_COL + 8, acc);
+                            tc::mma_mxf8(tmem + ACC1, da1, db, id, tmem + SF_COL + 4,
+                                         tmem + SF_COL + 8, acc);
+                        } else {
+                            tc::mma_f16(tmem + 0, da0, db, idesc, acc);
+                            tc::mma_f16(tmem + ACC1, da1, db, idesc, acc);
+                        }
                     }
                     tc::mma_commit(&sm->empty[s]);  // frees the stage once these MMAs finish
                     if (++s == STAGES) {
@@ -216,68 +616,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
-        const int fl = q * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         uint32_t acc_ph = 0;
+        auto ld = [&](int n0, float (&d0)[16], float (&d1)[16]) {
+            tc::tmem_ld16(tmem + lane_base + 0 + n0, d0);
+            tc::tmem_ld16(tmem + lane_base + ACC1 + n0, d1);
+            tc::tmem_ld_wait();
+        };
         for (int64_t u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
-            const int64_t t = u / p.n_mblocks;
-            const int mb = (int)(u % p.n_mblocks);
-            const int64_t r0 = p.tiles[4 * t + 1], r1 = p.tiles[4 * t + 2];
-            const int nr = (int)(r1 - r0);
-            const int n_mma = (nr + 15) & ~15;
             if (!wait_or_abort(&sm->tmem_full, acc_ph, p.status, abort)) break;
             tc::tc_fence_after();
-            const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-            const RingMap rm{p.ring.R, p.ring.MB, p.ring.n_slots};
-            for (int n0 = 0; n0 < n_mma; n0 += 16) {
-                float d0[16], d1[16];
-                tc::tmem_ld16(tmem + lane_base + 0 + n0, d0);
-                tc::tmem_ld16(tmem + lane_base + 256 + n0, d1);
-                tc::tmem_ld_wait();
-                if (KIND == 0) {
-                    const int I = up.I;
-                    const int i = mb * 128 + fl;  // gate feature; up feature is I + i
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int n = n0 + j;
-                        const bool live = n < nr;
-                        const int64_t r = r0 + n;
-                        const float h = silu_f(d0[j]) * d1[j];
-                        if (live && up.preact != nullptr) {
-                            up.preact[r * 2 * I + i] = d0[j];
-                            up.preact[r * 2 * I + I + i] = d1[j];
-                        }
-                        if (!up.mxfp8) {
-                            if (live)
-                                ((uint16_t *)up.hring)[rm(r) * I + i] = f32_to_bf16(h);
-                        } else {
-                            // the warp's 32 lanes hold one 32-feature MXFP8 block of row r
-                            float amax = fabsf(h);
-#pragma unroll
-                            for (int o = 16; o > 0; o >>= 1)
-                                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-                            const uint32_t sb = mx_scale_byte(amax);
-                            const uint32_t code = e4m3x2(h * mx_inv_scale(sb), 0.f) & 0xFFu;
-                            if (live) {
-                                const int64_t slot = rm(r);
-                                ((uint8_t *)up.hring)[slot * I + i] = (uint8_t)code;
-                                if (lane == 0) up.hring_s[slot * (I / 32) + i / 32] = (uint8_t)sb;
-                            }
-                        }
-                    }
-                } else {
-                    const int H = down.H;
-                    const int c = mb * 256 + fl;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int n = n0 + j;
-                        if (n < nr) {
-                            const int64_t f = down.perm[r0 + n];
-                            down.slots[f * H + c] = d0[j];
-                            if (c + 128 < H) down.slots[f * H + c + 128] = d1[j];
-                        }
-                    }
-                }
-            }
+            p.epilogue(u, ld, sm, q, lane);
             tc::tc_fence_before();
             tc::mbar_arrive(&sm->tmem_empty);
             acc_ph ^= 1u;
@@ -295,7 +644,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 int g_num_sms = 0;
-bool g_attr_set[2] = {false, false};
 
 cudaError_t init_host() {
     if (g_encode == nullptr) {
@@ -316,7 +664,8 @@ cudaError_t init_host() {
     return cudaSuccess;
 }
 
-// row-major bf16 matrix [rows][cols] -> 2D map with 64 x box_rows boxes, 128-byte swizzle
+// row-major bf16 matrix [rows][cols] -> 2D map of 64-column x box_rows boxes with
+// 128-byte swizzle
 cudaError_t make_map_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols,
                           int box_rows) {
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -330,52 +679,129 @@ cudaError_t make_map_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int KIND>
-cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const PairArgs &p,
-                        const EpiUpArgs &up, const EpiDownArgs &dn, cudaStream_t s) {
-    if (!g_attr_set[KIND]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<KIND>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SMEM_BYTES);
+// row-major byte matrix [rows][cols] (E4M3) -> 2D map of 128-byte x box_rows boxes with
+// 128-byte swizzle
+cudaError_t make_map_u8(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols,
+                        int box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols};
+    cuuint32_t box[2] = {(cuuint32_t)BK_MX, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <class P>
+cudaError_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const P &p, int64_t units_cap,
+                   cudaStream_t s) {
+    constexpr int SMEM = smem_bytes<P::MX>();
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<P>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
-        g_attr_set[KIND] = true;
+        attr = true;
     }
-    const int64_t units = p.tiles_cap * p.n_mblocks;
-    const int grid = (int)(units < g_num_sms ? units : g_num_sms);
+    const int grid = (int)(units_cap < g_num_sms ? units_cap : g_num_sms);
     if (grid < 1) return cudaSuccess;
-    gemm_pair_kernel<KIND><<<grid, NTHREADS, SMEM_BYTES, s>>>(ma, mb, p, up, dn);
+    tc_gemm_kernel<P><<<grid, NTHREADS, SMEM, s>>>(ma, mb, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-int gemm_tc_tile_rows() { return TILE_ROWS; }
+int gemm_tc_tile_rows(bool mxfp8) { return mxfp8 ? TILE_ROWS_MX : TILE_ROWS; }
 
 cudaError_t launch_gemm_up_tc(const GemmUpArgs &a, int64_t ring_rows, cudaStream_t s) {
     cudaError_t e = init_host();
     if (e != cudaSuccess) return e;
-    // A: W13 viewed as [E*2I][H]; B: the ring [ring_rows][H]
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb;  // A: W13 as [E*2I][H]; B: the x ring [ring_rows][H]
     if ((e = make_map_bf16(&ma, a.w13, (int64_t)a.E * 2 * a.I, a.H, 128)) != cudaSuccess) return e;
-    if ((e = make_map_bf16(&mb, a.xring, ring_rows, a.H, BOX_ROWS)) != cudaSuccess) return e;
-    PairArgs p{a.tiles, a.tiles_cap, a.I / 128, a.H / BK, 2 * a.I, a.I, 128, a.ring, a.status};
-    EpiUpArgs up{a.hring, a.hring_s, a.preact, a.I, a.mxfp8};
-    EpiDownArgs dn{nullptr, nullptr, 0};
-    return launch_pair<0>(ma, mb, p, up, dn, s);
+    if ((e = make_map_bf16(&mb, a.xring, ring_rows, a.H, KBOX_ROWS)) != cudaSuccess) return e;
+    FwdUpT<false> p{TileUnits{a.tiles, a.tiles_cap, a.I / 128}, a.H, a.I, a.ring, a.hring,
+                    a.hring_s, a.preact, false, a.status, nullptr, nullptr};
+    return launch(ma, mb, p, a.tiles_cap * (a.I / 128), s);
 }
 
 cudaError_t launch_gemm_down_tc(const GemmDownArgs &a, int64_t ring_rows, cudaStream_t s) {
     cudaError_t e = init_host();
     if (e != cudaSuccess) return e;
-    // A: W2 viewed as [E*H][I]; B: the h ring [ring_rows][I]
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb;  // A: W2 as [E*H][I]; B: the h ring [ring_rows][I]
     if ((e = make_map_bf16(&ma, a.w2, (int64_t)a.E * a.H, a.I, 128)) != cudaSuccess) return e;
-    if ((e = make_map_bf16(&mb, a.hring, ring_rows, a.I, BOX_ROWS)) != cudaSuccess) return e;
-    PairArgs p{a.tiles, a.tiles_cap, (a.H + 255) / 256, a.I / BK, a.H, 128, 256, a.ring,
-               a.status};
-    EpiUpArgs up{nullptr, nullptr, nullptr, 0, false};
-    EpiDownArgs dn{a.perm, a.slots, a.H};
-    return launch_pair<1>(ma, mb, p, up, dn, s);
+    if ((e = make_map_bf16(&mb, a.hring, ring_rows, a.I, KBOX_ROWS)) != cudaSuccess) return e;
+    const int nmb = (a.H + 255) / 256;
+    FwdDownT<false> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.ring, a.perm, a.slots,
+                      a.status, nullptr, nullptr};
+    return launch(ma, mb, p, a.tiles_cap * nmb, s);
+}
+
+cudaError_t launch_gemm_up_tc_mx(const GemmUpArgs &a, int64_t ring_rows, const uint8_t *sf_w,
+                                 const uint8_t *sf_x, cudaStream_t s) {
+    cudaError_t e = init_host();
+    if (e != cudaSuccess) return e;
+    CUtensorMap ma, mb;  // A: W13 E4M3 [E*2I][H]; B: the quantized x ring [ring_rows][H]
+    if ((e = make_map_u8(&ma, a.w13, (int64_t)a.E * 2 * a.I, a.H, 128)) != cudaSuccess) return e;
+    if ((e = make_map_u8(&mb, a.xring, ring_rows, a.H, KBOX_ROWS)) != cudaSuccess) return e;
+    FwdUpT<true> p{TileUnits{a.tiles, a.tiles_cap, a.I / 128}, a.H, a.I, a.ring, a.hring,
+                   a.hring_s, nullptr, true, a.status, sf_w, sf_x};
+    return launch(ma, mb, p, a.tiles_cap * (a.I / 128), s);
+}
+
+cudaError_t launch_gemm_down_tc_mx(const GemmDownArgs &a, int64_t ring_rows, const uint8_t *sf_w,
+                                   const uint8_t *sf_h, cudaStream_t s) {
+    cudaError_t e = init_host();
+    if (e != cudaSuccess) return e;
+    CUtensorMap ma, mb;  // A: W2 E4M3 [E*H][I]; B: the quantized h ring [ring_rows][I]
+    if ((e = make_map_u8(&ma, a.w2, (int64_t)a.E * a.H, a.I, 128)) != cudaSuccess) return e;
+    if ((e = make_map_u8(&mb, a.hring, ring_rows, a.I, KBOX_ROWS)) != cudaSuccess) return e;
+    const int nmb = (a.H + 255) / 256;
+    FwdDownT<true> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.ring, a.perm, a.slots,
+                     a.status, sf_w, sf_h};
+    return launch(ma, mb, p, a.tiles_cap * nmb, s);
+}
+
+cudaError_t launch_gemm_g_tc(const GemmGArgs &a, int E, int64_t rpad_cap, cudaStream_t s) {
+    cudaError_t e = init_host();
+    if (e != cudaSuccess) return e;
+    CUtensorMap ma, mb;  // A: W2 as [E*H][I] read MN-major; B: dy_perm [rpad][H]
+    if ((e = make_map_bf16(&ma, a.w2, (int64_t)E * a.H, a.I, 64)) != cudaSuccess) return e;
+    if ((e = make_map_bf16(&mb, a.dy_perm, rpad_cap, a.H, KBOX_ROWS)) != cudaSuccess) return e;
+    const int nmb = (a.I + 255) / 256;
+    BwdG p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff, a.perm, a.preact,
+           a.topk_w, a.dA, a.sh, a.dS_part, 4 * nmb, a.status};
+    return launch(ma, mb, p, a.tiles_cap * nmb, s);
+}
+
+int gemm_tc_dS_parts(int I) { return 4 * ((I + 255) / 256); }
+
+cudaError_t launch_gemm_dgrad_tc(const GemmDgradArgs &a, int E, int64_t rpad_cap,
+                                 cudaStream_t s) {
+    cudaError_t e = init_host();
+    if (e != cudaSuccess) return e;
+    CUtensorMap ma, mb;  // A: W13 as [E*2I][H] read MN-major; B: dA [rpad][2I]
+    if ((e = make_map_bf16(&ma, a.w13, (int64_t)E * 2 * a.I, a.H, 64)) != cudaSuccess) return e;
+    if ((e = make_map_bf16(&mb, a.dA, rpad_cap, 2 * a.I, KBOX_ROWS)) != cudaSuccess) return e;
+    const int nmb = (a.H + 255) / 256;
+    BwdDgrad p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff, a.perm,
+               a.dx_slots, a.status};
+    return launch(ma, mb, p, a.tiles_cap * nmb, s);
+}
+
+// out [E][N][M] = per expert sum over padded rows of A[p][m] B[p][n]
+cudaError_t launch_wgrad_tc(const int32_t *counts, const int32_t *poff, const uint16_t *A,
+                            const uint16_t *Bm, float *out, int E, int M, int N,
+                            int64_t rpad_cap, int *status, cudaStream_t s) {
+    cudaError_t e = init_host();
+    if (e != cudaSuccess) return e;
+    CUtensorMap ma, mb;
+    if ((e = make_map_bf16(&ma, A, rpad_cap, M, 64)) != cudaSuccess) return e;
+    if ((e = make_map_bf16(&mb, Bm, rpad_cap, N, 64)) != cudaSuccess) return e;
+    const int nmb = (M + 255) / 256, nnb = (N + 255) / 256;
+    Wgrad p{counts, poff, out, E, M, N, nmb, nnb, status};
+    return launch(ma, mb, p, (int64_t)E * nmb * nnb, s);
 }
 
 }  // namespace mok

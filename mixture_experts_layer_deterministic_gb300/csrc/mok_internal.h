@@ -12,7 +12,7 @@ namespace mok {
 enum KernelKind {
     KK_ROUTE = 0, KK_SCHEDULE, KK_TILES, KK_GATHER, KK_GEMM_UP, KK_GEMM_DOWN, KK_COMBINE,
     KK_QUANTIZE, KK_PAD, KK_GATHER_BWD, KK_GEMM_G, KK_ROUTER_GRAD, KK_GEMM_DGRAD,
-    KK_DX_REDUCE, KK_WGRAD13, KK_WGRAD2, KK_COUNT
+    KK_DX_REDUCE, KK_WGRAD13, KK_WGRAD2, KK_SCALE_ATOMS, KK_COUNT
 };
 // while profiling is on: brackets the launches between begin and end with events
 void prof_begin(int kind, cudaStream_t s);
@@ -94,7 +94,6 @@ struct GemmUpArgs {
     Ring ring;
     int *status;
 };
-cudaError_t launch_gemm_up(const GemmUpArgs &a, cudaStream_t s);
 
 // Forward down GEMM with the push scatter, per tile (e, r0, r1):
 //   slots[perm[r]][c] = sum_i W2[e][c][i] * hring[ring(r)][i]   (fp32)
@@ -112,20 +111,30 @@ struct GemmDownArgs {
     Ring ring;
     int *status;
 };
-cudaError_t launch_gemm_down(const GemmDownArgs &a, cudaStream_t s);
-
-// tensor-core versions (BF16): tiles cut at gemm_tc_tile_rows() rows; ring_rows = rows of
-// the ring buffers the TMA maps cover
-int gemm_tc_tile_rows();
+// The GEMMs run on the tensor cores (gemm_tc.cu). Tiles are cut at gemm_tc_tile_rows()
+// rows; ring_rows / rpad_cap are the rows of the buffers the TMA maps cover.
+int gemm_tc_tile_rows(bool mxfp8);
+int gemm_tc_dS_parts(int I);
 cudaError_t launch_gemm_up_tc(const GemmUpArgs &a, int64_t ring_rows, cudaStream_t s);
 cudaError_t launch_gemm_down_tc(const GemmDownArgs &a, int64_t ring_rows, cudaStream_t s);
-
-int gemm_tile_rows();
+// MXFP8: E4M3 operands with scale atoms (see launch_scale_atoms_*): sf_w for the weights,
+// sf_x / sf_h for the token tiles
+cudaError_t launch_gemm_up_tc_mx(const GemmUpArgs &a, int64_t ring_rows, const uint8_t *sf_w,
+                                 const uint8_t *sf_x, cudaStream_t s);
+cudaError_t launch_gemm_down_tc_mx(const GemmDownArgs &a, int64_t ring_rows, const uint8_t *sf_w,
+                                   const uint8_t *sf_h, cudaStream_t s);
+// MXFP8 scales, plain [rows][K/32] -> the tensor cores' 128-row x 4-block atoms: per 128
+// weight rows, or per token tile of the list (two atoms per tile)
+cudaError_t launch_scale_atoms_rows(const uint8_t *src, int64_t rows, int K, uint8_t *dst,
+                                    cudaStream_t s);
+cudaError_t launch_scale_atoms_tiles(const int32_t *tiles, int64_t cap, const uint8_t *src,
+                                     int64_t R, int MB, int n_slots, int K, uint8_t *dst,
+                                     cudaStream_t s);
 
 // Backward G GEMM with the SwiGLU backward and router-weight gradient epilogue, per tile
 // (e, r0, r1) over sorted rows; p(r) = poff[e] + r - offsets[e] is the padded row:
 //   g[r][i] = sum_c W2[e][c][i] * dy_perm[p(r)][c]
-//   dS_part[r][i / 128] = sum over the 128-feature block of g * h   (fixed order)
+//   dS_part[r][part] = fixed-order partial sums of g * h over feature blocks
 //   dA[p(r)][i] = w g a_u silu'(a_g), dA[p(r)][I+i] = w g silu(a_g), sh[p(r)][i] = w h
 // Pad rows of the tile (up to the next multiple of 16) get zeros in dA and sh.
 struct GemmGArgs {
@@ -144,7 +153,6 @@ struct GemmGArgs {
     int H, I;
     int *status;
 };
-cudaError_t launch_gemm_g(const GemmGArgs &a, cudaStream_t s);
 
 // Backward dgrad GEMM with the reverse-dispatch scatter, per tile (e, r0, r1):
 //   dx_slots[perm[r]][c] = sum_j W13[e][j][c] * dA[p(r)][j]   (fp32)
@@ -160,21 +168,12 @@ struct GemmDgradArgs {
     int H, I;
     int *status;
 };
-cudaError_t launch_gemm_dgrad(const GemmDgradArgs &a, cudaStream_t s);
-
-// Weight gradient, per expert e: out[e][m][n] = sum over padded rows p of e of
-//   A[p][m] * B[p][n] (fp32) with A [rows][M] and B [rows][N] row-major; experts with no rows
-// get zeros. dW13: A = dA (M = 2I), B = x_perm (N = H). dW2: A = dy_perm (M = H), B = sh
-// (N = I).
-struct GemmWgradArgs {
-    const int32_t *counts;
-    const int32_t *poff;
-    const uint16_t *A;
-    const uint16_t *B;
-    float *out;
-    int E, M, N;
-    int *status;
-};
-cudaError_t launch_gemm_wgrad(const GemmWgradArgs &a, cudaStream_t s);
+cudaError_t launch_gemm_g_tc(const GemmGArgs &a, int E, int64_t rpad_cap, cudaStream_t s);
+cudaError_t launch_gemm_dgrad_tc(const GemmDgradArgs &a, int E, int64_t rpad_cap,
+                                 cudaStream_t s);
+// out [E][N][M] = per expert e, sum over its padded rows p of A[p][m] * B[p][n]
+cudaError_t launch_wgrad_tc(const int32_t *counts, const int32_t *poff, const uint16_t *A,
+                            const uint16_t *B, float *out, int E, int M, int N,
+                            int64_t rpad_cap, int *status, cudaStream_t s);
 
 }  // namespace mok

@@ -168,21 +168,30 @@ __global__ void __launch_bounds__(SCHED_WARPS * 32)
 }
 
 // ---------------------------------------------------------------- tile lists
-// One block: for each expert, the part of its rows inside [p0, p1), cut into chunks of at
-// most `chunk` rows, written in expert order. count at list[-4].
+// One block: for each expert, the part of its rows inside [p0, p1), cut into tiles of at
+// most `chunk` rows (balanced heights, multiples of 16 but for the last), written in
+// expert order. count at list[-4].
 __global__ void __launch_bounds__(MAX_E)
     build_tiles(const int32_t *__restrict__ offsets, int E, int64_t p0, int64_t p1, int chunk,
                 int32_t *__restrict__ list, int64_t cap, int *status) {
     __shared__ int32_t sc[MAX_E];
     const int e = threadIdx.x;
-    int64_t b = 0, end = 0;
+    int64_t b = 0, end = 0, size = chunk;
     int32_t n = 0;
     if (e < E) {
         b = offsets[e];
         end = offsets[e + 1];
         if (b < p0) b = p0;
         if (end > p1) end = p1;
-        if (end > b) n = (int32_t)((end - b + chunk - 1) / chunk);
+        if (end > b) {
+            // balanced cut: as many tiles as chunk-sized tiles would need, of equal height
+            // rounded up to 16 rows (the last one may be shorter)
+            const int64_t len = end - b;
+            const int64_t n0 = (len + chunk - 1) / chunk;
+            size = (((len + n0 - 1) / n0) + 15) & ~(int64_t)15;
+            if (size > chunk) size = chunk;
+            n = (int32_t)((len + size - 1) / size);
+        }
     }
     sc[e] = n;
     __syncthreads();
@@ -198,8 +207,8 @@ __global__ void __launch_bounds__(MAX_E)
         if (sc[e] > cap) raise_status(status, MOK_ERR_DEVICE_INVARIANT);
     }
     for (int32_t q = 0; q < n; ++q, ++s) {
-        const int64_t r0 = b + (int64_t)q * chunk;
-        const int64_t r1 = (r0 + chunk < end) ? r0 + chunk : end;
+        const int64_t r0 = b + (int64_t)q * size;
+        const int64_t r1 = (r0 + size < end) ? r0 + size : end;
         if (s < cap) {
             list[4 * s + 0] = e;
             list[4 * s + 1] = (int32_t)r0;

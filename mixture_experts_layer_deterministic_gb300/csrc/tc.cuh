@@ -74,6 +74,15 @@ MOK_DEV void tma_load_2d(void *smem_dst, const CUtensorMap *m, uint64_t *bar, in
         : "memory");
 }
 
+// 1D bulk copy global -> shared (16-byte aligned, size a multiple of 16), counted on `bar`
+MOK_DEV void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(smem_dst)),
+        "l"((uint64_t)gsrc), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 // TMEM allocation by one full warp; the base address is written to shared memory.
 MOK_DEV void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
@@ -102,6 +111,25 @@ MOK_DEV void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t i
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= (A * scale_A)[smem] * (B * scale_B)[smem]^T for E4M3 operands with one E8M0
+// scale per 32 K-elements taken from TMEM (kind::mxf8f6f4, K = 32 per instruction).
+MOK_DEV void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                      uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %6, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+        "[%5], p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Copies a 32-row x 16-byte block of shared memory into TMEM: row i goes to lane i of each
+// of the four 32-lane quadrants, 4 consecutive 32-bit columns.
+MOK_DEV void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 operation issued so far by this thread is done.
 MOK_DEV void mma_commit(uint64_t *bar) {
     asm volatile(
@@ -139,6 +167,30 @@ MOK_DEV uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;
     d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Shared-memory descriptor of a non-swizzled block of 8-row x 16-byte core matrices
+// stacked along the rows every 128 bytes (the source of tcgen05.cp 32x128b).
+MOK_DEV uint64_t sdesc_plain_rows16(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((128u >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with block scaling: E4M3 A and B (format 0),
+// fp32 D (bit 4), K-major operands, B scale-factor id (bits 4-5), N >> 3 (17-22), scale
+// type UE8M0 (bit 23), M >> 4 (24-28), A scale-factor id (29-30). The ids select the byte
+// of the 32-bit TMEM scale word that holds this instruction's 32-element block.
+MOK_DEV uint32_t idesc_mxf8(int M, int N, uint32_t sf_id) {
+    uint32_t d = 0;
+    d |= (sf_id & 3u) << 4;
+    d |= (uint32_t)(N >> 3) << 17;
+    d |= 1u << 23;
+    d |= (uint32_t)(M >> 4) << 24;
+    d |= (sf_id & 3u) << 29;
     return d;
 }
 

@@ -54,6 +54,10 @@ CONFIGS = {
                         prec="bf16", passes="fwd"),
     "fwd_bf16": LayerConfig(name="fwd_bf16", T=16384, seed=0, prec="bf16", passes="fwd", **_BIG),
     "fwd_mxfp8": LayerConfig(name="fwd_mxfp8", T=16384, seed=1, prec="mxfp8", passes="fwd", **_BIG),
+    # profiling case: same routed rows per expert (320) as fwd_bf16 with a quarter of the
+    # experts, so a full counter capture holds a few GB on the device
+    "fwd_bf16_e128": LayerConfig(name="fwd_bf16_e128", T=4096, seed=0, prec="bf16",
+                                 passes="fwd", **{**_BIG, "E": 128}),
     "bwd_bf16": LayerConfig(name="bwd_bf16", T=8192, seed=2, prec="bf16", passes="bwd", **_BIG),
     "imbalanced_bf16": LayerConfig(name="imbalanced_bf16", T=65536, seed=3, prec="bf16",
                                    passes="fwd", **{**_BIG, "zipf_bias": True,

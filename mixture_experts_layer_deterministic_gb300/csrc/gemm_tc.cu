@@ -46,8 +46,14 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL = 480;  // MXFP8: TMEM columns of the stage's scale atoms
 template <bool MX>
 __host__ __device__ constexpr int stage_bytes() { return 2 * A_BYTES + B_BYTES + (MX ? SF_BYTES : 0); }
-template <bool MX>
-__host__ __device__ constexpr int smem_bytes() { return STAGES * stage_bytes<MX>() + 1024 /*align*/ + 512; }
+
+
+// per epilogue warp: one value per token column of the unit (a routing weight or a slot
+// index) and a transpose buffer for fixed-order reductions over the warp's 32 lanes
+struct EpiScratch {
+    float col[TILE_ROWS];
+    float red[16][33];
+};
 
 struct Smem {
     uint64_t full[STAGES];
@@ -56,7 +62,13 @@ struct Smem {
     uint64_t tmem_empty;
     uint32_t tmem_base;
     int abort;
+    EpiScratch epi[4];
 };
+
+template <bool MX>
+__host__ __device__ constexpr int smem_bytes() {
+    return STAGES * stage_bytes<MX>() + 1024 /*align*/ + (int)sizeof(Smem);
+}
 
 // One work unit as the producer and the MMA issuer see it.
 struct Geom {
@@ -227,13 +239,16 @@ struct FwdDownT {
         return g;
     }
     template <class LD>
-    MOK_DEV void epilogue(int64_t u, const LD &ld, Smem *, int q, int lane) const {
+    MOK_DEV void epilogue(int64_t u, const LD &ld, Smem *sm, int q, int lane) const {
         int e, mb;
         int64_t r0, r1;
         tu.get(u, &e, &r0, &r1, &mb);
         const int nr = (int)(r1 - r0);
         const int n_mma = (nr + 15) & ~15;
         const int c = mb * 256 + q * 32 + lane;
+        int *fcol = reinterpret_cast<int *>(sm->epi[q].col);  // slot of each column
+        for (int n = lane; n < nr; n += 32) fcol[n] = perm[r0 + n];
+        __syncwarp();
         for (int n0 = 0; n0 < n_mma; n0 += 16) {
             float d0[16], d1[16];
             ld(n0, d0, d1);
@@ -241,12 +256,13 @@ struct FwdDownT {
             for (int j = 0; j < 16; ++j) {
                 const int n = n0 + j;
                 if (n < nr) {
-                    const int64_t f = perm[r0 + n];
+                    const int64_t f = fcol[n];
                     slots[f * H + c] = d0[j];
                     if (c + 128 < H) slots[f * H + c + 128] = d1[j];
                 }
             }
         }
+        __syncwarp();
     }
 };
 
@@ -282,7 +298,7 @@ struct BwdG {
         return g;
     }
     template <class LD>
-    MOK_DEV void epilogue(int64_t u, const LD &ld, Smem *, int q, int lane) const {
+    MOK_DEV void epilogue(int64_t u, const LD &ld, Smem *sm, int q, int lane) const {
         int e, mb;
         int64_t r0, r1;
         tu.get(u, &e, &r0, &r1, &mb);
@@ -291,10 +307,25 @@ struct BwdG {
         const int64_t pb = poff[e] + (r0 - offsets[e]);
         const bool last = r1 == offsets[e + 1];
         const int i0 = mb * 256 + q * 32 + lane;
+        EpiScratch &es = sm->epi[q];
+        // the routing weight of every column of the unit, loaded once
+        for (int n = lane; n < nr; n += 32) es.col[n] = topk_w[perm[r0 + n]];
+        __syncwarp();
         for (int n0 = 0; n0 < n_mma; n0 += 16) {
             float d[2][16];
             ld(n0, d[0], d[1]);
-            float part[16];
+            // issue every pre-activation load of the chunk before using any
+            float ag[2][16], au[2][16];
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int i = i0 + a * 128;
+                    const int64_t r = r0 + n0 + j;
+                    const bool ok = (n0 + j < nr) && i < I;
+                    ag[a][j] = ok ? preact[r * 2 * I + i] : 0.f;
+                    au[a][j] = ok ? preact[r * 2 * I + I + i] : 0.f;
+                }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int n = n0 + j;
@@ -305,16 +336,14 @@ struct BwdG {
                     const int i = i0 + a * 128;
                     if (i >= I) continue;
                     if (n < nr) {
-                        const int64_t r = r0 + n;
-                        const float ag = preact[r * 2 * I + i];
-                        const float au = preact[r * 2 * I + I + i];
-                        const float s = topk_w[perm[r]];
+                        const float s = es.col[n];
                         const float g = d[a][j];
-                        const float sig = 1.0f / (1.0f + expf(-ag));
-                        const float sl = ag * sig;
-                        const float h = sl * au;
+                        const float sig = 1.0f / (1.0f + expf(-ag[a][j]));
+                        const float sl = ag[a][j] * sig;
+                        const float h = sl * au[a][j];
                         const float dh = s * g;
-                        dA[p * 2 * I + i] = f32_to_bf16(dh * au * sig * (1.0f + ag * (1.0f - sig)));
+                        dA[p * 2 * I + i] =
+                            f32_to_bf16(dh * au[a][j] * sig * (1.0f + ag[a][j] * (1.0f - sig)));
                         dA[p * 2 * I + I + i] = f32_to_bf16(dh * sl);
                         sh[p * I + i] = f32_to_bf16(s * h);
                         gh_sum += g * h;
@@ -324,20 +353,17 @@ struct BwdG {
                         sh[p * I + i] = 0;
                     }
                 }
-                // fixed-order sum over the warp's 32 lanes
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) gh_sum += __shfl_xor_sync(0xFFFFFFFFu, gh_sum, o);
-                part[j] = gh_sum;
+                es.red[j][lane] = gh_sum;
             }
-            // one partial per (row, weight block, warp); the router-gradient kernel adds
-            // them in index order
+            __syncwarp();
+            // one partial per (row, weight block, warp): lanes summed in lane order; the
+            // router-gradient kernel adds the partials in index order
             if (lane < 16 && n0 + lane < nr) {
                 float v = 0.f;
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (j == lane) v = part[j];
+                for (int l = 0; l < 32; ++l) v += es.red[lane][l];
                 dS_part[(r0 + n0 + lane) * n_parts + mb * 4 + q] = v;
             }
+            __syncwarp();
         }
     }
 };
@@ -371,13 +397,16 @@ struct BwdDgrad {
         return g;
     }
     template <class LD>
-    MOK_DEV void epilogue(int64_t u, const LD &ld, Smem *, int q, int lane) const {
+    MOK_DEV void epilogue(int64_t u, const LD &ld, Smem *sm, int q, int lane) const {
         int e, mb;
         int64_t r0, r1;
         tu.get(u, &e, &r0, &r1, &mb);
         const int nr = (int)(r1 - r0);
         const int n_mma = (nr + 15) & ~15;
         const int c = mb * 256 + q * 32 + lane;
+        int *fcol = reinterpret_cast<int *>(sm->epi[q].col);  // slot of each column
+        for (int n = lane; n < nr; n += 32) fcol[n] = perm[r0 + n];
+        __syncwarp();
         for (int n0 = 0; n0 < n_mma; n0 += 16) {
             float d0[16], d1[16];
             ld(n0, d0, d1);
@@ -385,12 +414,13 @@ struct BwdDgrad {
             for (int j = 0; j < 16; ++j) {
                 const int n = n0 + j;
                 if (n < nr) {
-                    const int64_t f = perm[r0 + n];
+                    const int64_t f = fcol[n];
                     dx_slots[f * H + c] = d0[j];
                     if (c + 128 < H) dx_slots[f * H + c + 128] = d1[j];
                 }
             }
         }
+        __syncwarp();
     }
 };
 

@@ -99,8 +99,8 @@ size_t carve_fwd(const mok_config *c, void *ws, FwdWs *o) {
     if (mx) {
         w.sf_w13 = cv.take<uint8_t>((size_t)c->E * 2 * c->I * (c->H / 32));
         w.sf_w2 = cv.take<uint8_t>((size_t)c->E * c->H * (c->I / 32));
-        w.sf_x = cv.take<uint8_t>((size_t)w.tiles_cap * (c->H / 128) * 1024);
-        w.sf_h = cv.take<uint8_t>((size_t)w.tiles_cap * (c->I / 128) * 1024);
+        w.sf_x = cv.take<uint8_t>((size_t)w.tiles_cap * (c->H / 128) * 512);
+        w.sf_h = cv.take<uint8_t>((size_t)w.tiles_cap * (c->I / 128) * 512);
     }
     if (o) *o = w;
     return cv.off;

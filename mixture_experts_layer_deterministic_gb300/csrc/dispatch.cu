@@ -224,26 +224,25 @@ __global__ void __launch_bounds__(TPB)
     }
 }
 
-// Token tiles: the rows n < 256 of tile t = (e, r0, r1) (rows past the tile get byte 0) ->
-// two atoms per 128-wide K block at (t * K/128 + kg) * 1024 + (n / 128) * 512.
+// Token tiles: the rows n < 128 of tile t = (e, r0, r1) (rows past the tile get byte 0) ->
+// one atom per 128-wide K block at (t * K/128 + kg) * 512.
 __global__ void __launch_bounds__(TPB)
     scale_atoms_tiles_kernel(const int32_t *__restrict__ tiles, int64_t cap,
                              const uint8_t *__restrict__ src, RingMap rm, int K,
                              uint8_t *__restrict__ dst) {
     const int kgn = K / 128;
     const int64_t nt = tiles[-4] < cap ? tiles[-4] : cap;
-    const int64_t total = nt * 256 * kgn;
+    const int64_t total = nt * 128 * kgn;
     const int64_t stride = (int64_t)gridDim.x * TPB;
     for (int64_t i = (int64_t)blockIdx.x * TPB + threadIdx.x; i < total; i += stride) {
         const int kg = (int)(i % kgn);
-        const int n = (int)((i / kgn) % 256);
-        const int64_t t = i / ((int64_t)kgn * 256);
+        const int n = (int)((i / kgn) % 128);
+        const int64_t t = i / ((int64_t)kgn * 128);
         const int64_t r0 = tiles[4 * t + 1], r1 = tiles[4 * t + 2];
         uint32_t v = 0;
         if (n < r1 - r0)
             v = *reinterpret_cast<const uint32_t *>(src + rm(r0 + n) * (K / 32) + 4 * kg);
-        uint8_t *o = dst + (t * kgn + kg) * 1024 + (n / 128) * 512 + (n % 32) * 16 +
-                     ((n % 128) / 32) * 4;
+        uint8_t *o = dst + (t * kgn + kg) * 512 + (n % 32) * 16 + (n / 32) * 4;
         *reinterpret_cast<uint32_t *>(o) = v;
     }
 }
@@ -321,7 +320,7 @@ cudaError_t launch_scale_atoms_tiles(const int32_t *tiles, int64_t cap, const ui
                                      cudaStream_t s) {
     if (cap == 0) return cudaSuccess;
     RingMap rm{R, MB, n_slots};
-    scale_atoms_tiles_kernel<<<grid_for(cap * 256 * (K / 128), TPB, 152 * 16), TPB, 0, s>>>(
+    scale_atoms_tiles_kernel<<<grid_for(cap * 128 * (K / 128), TPB, 152 * 16), TPB, 0, s>>>(
         tiles, cap, src, rm, K, dst);
     return cudaGetLastError();
 }

@@ -8,11 +8,13 @@
 // router-weight gradient computed inside the SwiGLU backward.
 //
 // One persistent kernel template, 192 threads per CTA, one CTA per SM:
-//   warp 0     TMA producer: two 128-row A tiles and one B tile (up to 256 rows) per
-//              64-wide K block into a 3-stage shared-memory ring
-//   warp 1     TMEM owner and MMA issuer: D0 += A0 B^T, D1 += A1 B^T (M=128, N<=256,
-//              K=16 per instruction), fp32 accumulators at TMEM columns 0 and 256
+//   warp 0     TMA producer: two 128-row A tiles and one B tile (up to 128 rows) per
+//              64-wide K block into a 4-stage shared-memory ring
+//   warp 1     TMEM owner and MMA issuer: D0 += A0 B^T, D1 += A1 B^T (M=128, N<=128,
+//              K=16 per instruction) into one of two fp32 accumulator sets in TMEM
 //   warps 2-5  epilogue: TMEM -> registers -> fused epilogue -> global memory
+// The two accumulator sets alternate between consecutive units of a CTA, so the epilogue
+// of one unit runs while the tensor cores compute the next.
 // A problem policy supplies the work-unit decomposition, the operand majors and the
 // epilogue:
 //   FwdUp     A = W13 (K-major), B = x ring (K-major)      -> SwiGLU, h (bf16 / MXFP8)
@@ -34,16 +36,21 @@ namespace {
 
 constexpr int BK = 64;            // bf16 K elements per stage (128 bytes per row)
 constexpr int BK_MX = 128;        // E4M3 K elements per stage (128 bytes per row)
-constexpr int STAGES = 3;
-constexpr int TILE_ROWS = 256;    // max N per unit (bf16)
-constexpr int TILE_ROWS_MX = 240; // max N per unit (MXFP8: TMEM also holds the scales)
+constexpr int STAGES = 4;
+constexpr int TILE_ROWS = 128;    // max N per unit (bf16)
+constexpr int TILE_ROWS_MX = 112; // max N per unit (MXFP8: TMEM also holds the scales)
 constexpr int KBOX_ROWS = 32;     // rows per TMA box of a K-major B operand
 constexpr int A_BYTES = 128 * 128;                // 128 rows x 128 bytes
-constexpr int B_BYTES = TILE_ROWS * 128;          // 256 rows x 128 bytes
-constexpr int SF_BYTES = 2048;    // MXFP8 scale atoms per stage: A0, A1 (512 B), B (1 KB)
+constexpr int B_BYTES = TILE_ROWS * 128;          // 128 rows x 128 bytes
+constexpr int SF_BYTES = 2048;    // MXFP8 scale atoms per stage: A0, A1, B (512 B each), pad
 constexpr int NTHREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL = 480;  // MXFP8: TMEM columns of the stage's scale atoms
+// TMEM column of accumulator a (0: A0, 1: A1) of accumulator set b
+template <bool MX>
+__host__ __device__ constexpr uint32_t acc_col(int b, int a) {
+    return (uint32_t)((2 * b + a) * (MX ? TILE_ROWS_MX : TILE_ROWS));
+}
 template <bool MX>
 __host__ __device__ constexpr int stage_bytes() { return 2 * A_BYTES + B_BYTES + (MX ? SF_BYTES : 0); }
 
@@ -58,8 +65,8 @@ struct EpiScratch {
 struct Smem {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
-    uint64_t tmem_full;
-    uint64_t tmem_empty;
+    uint64_t tmem_full[2];   // accumulator set b holds a finished unit
+    uint64_t tmem_empty[2];  // the epilogue has drained accumulator set b
     uint32_t tmem_base;
     int abort;
     EpiScratch epi[4];
@@ -123,8 +130,8 @@ struct TileUnits {
 
 // MXFP8 scale atoms: 128 rows x 4 blocks of 32 K elements as 32 rows of 16 bytes, row i
 // holding rows i, i+32, i+64, i+96 (4 bytes each, one per block). Weights: atom
-// (row/128, k/128) at ((row/128) * K/128 + k/128) * 512; token tiles: two atoms (rows
-// 0-127, 128-255 of the tile) per 128-wide K block at (tile * K/128 + k/128) * 1024.
+// (row/128, k/128) at ((row/128) * K/128 + k/128) * 512; token tiles: one atom per
+// 128-wide K block at (tile * K/128 + k/128) * 512.
 template <bool MXv>
 struct FwdUpT {
     static constexpr bool A_MN = false, B_MN = false, MX = MXv;
@@ -157,7 +164,7 @@ struct FwdUpT {
         const int64_t kg = H / 128;
         g.sfa0 = (int64_t)(g.ay0 / 128) * kg * 512;
         g.sfa1 = (int64_t)(g.ay1 / 128) * kg * 512;
-        g.sfb = (u / tu.n_mblocks) * kg * 1024;
+        g.sfb = (u / tu.n_mblocks) * kg * 512;
         return g;
     }
     template <class LD>
@@ -235,7 +242,7 @@ struct FwdDownT {
         // when H is not a multiple of 256 the last block's A1 lies past this expert (its
         // results are discarded); keep its scale reads inside the expert
         g.sfa1 = mb * 256 + 128 < H ? (int64_t)(g.ay1 / 128) * kg * 512 : g.sfa0;
-        g.sfb = (u / tu.n_mblocks) * kg * 1024;
+        g.sfb = (u / tu.n_mblocks) * kg * 512;
         return g;
     }
     template <class LD>
@@ -432,7 +439,7 @@ struct Wgrad {
     const int32_t *counts, *poff;
     float *out;
     int E, M, N;     // out is [E][N][M]
-    int nmb, nnb;    // ceil(M/256), ceil(N/256)
+    int nmb, nnb;    // ceil(M/256), ceil(N/128)
     int *status;
 
     MOK_DEV int64_t n_units() const { return (int64_t)E * nmb * nnb; }
@@ -450,9 +457,9 @@ struct Wgrad {
         g.ay0 = poff[e];
         g.ax1 = g.ax0 + 128;
         g.ay1 = poff[e];
-        g.bx = nb * 256;
+        g.bx = nb * TILE_ROWS;
         g.by = poff[e];
-        const int nn = N - nb * 256 < 256 ? N - nb * 256 : 256;
+        const int nn = N - nb * TILE_ROWS < TILE_ROWS ? N - nb * TILE_ROWS : TILE_ROWS;
         g.n_mma = nn;
         g.nbox = nn / 64;
         g.k_steps = ((counts[e] + 15) & ~15) / 16;
@@ -462,7 +469,7 @@ struct Wgrad {
     MOK_DEV void epilogue(int64_t u, const LD &ld, Smem *, int q, int lane) const {
         int e, mb, nb;
         get(u, &e, &mb, &nb);
-        const int nn = N - nb * 256 < 256 ? N - nb * 256 : 256;
+        const int nn = N - nb * TILE_ROWS < TILE_ROWS ? N - nb * TILE_ROWS : TILE_ROWS;
         const bool any = counts[e] > 0;
         const int m = mb * 256 + q * 32 + lane;
         float *o = out + (int64_t)e * N * M;
@@ -471,7 +478,7 @@ struct Wgrad {
             ld(n0, d0, d1);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const int64_t row = (int64_t)(nb * 256 + n0 + j) * M;
+                const int64_t row = (int64_t)(nb * TILE_ROWS + n0 + j) * M;
                 o[row + m] = any ? d0[j] : 0.f;
                 if (m + 128 < M) o[row + m + 128] = any ? d1[j] : 0.f;
             }
@@ -487,7 +494,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     constexpr bool MX = P::MX;
     constexpr int SB = stage_bytes<MX>();
     constexpr int BKE = MX ? BK_MX : BK;             // K elements per stage
-    constexpr uint32_t ACC1 = MX ? TILE_ROWS_MX : 256; // TMEM column of the second accumulator
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     Smem *sm = (Smem *)(base + STAGES * SB);
@@ -499,8 +505,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::mbar_init(&sm->full[s], 1);
             tc::mbar_init(&sm->empty[s], 1);
         }
-        tc::mbar_init(&sm->tmem_full, 1);
-        tc::mbar_init(&sm->tmem_empty, 128);
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&sm->tmem_full[b], 1);
+            tc::mbar_init(&sm->tmem_empty[b], 128);
+        }
         sm->abort = 0;
         tc::fence_mbar_init();
         tc::prefetch_tmap(&tmA);
@@ -532,13 +540,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     uint8_t *st = base + s * SB;
                     uint64_t *fb = &sm->full[s];
                     tc::mbar_arrive_expect_tx(fb, 2 * A_BYTES + g.nbox * B_BOX +
-                                                      (MX ? SF_BYTES : 0));
+                                                      (MX ? 1536 : 0));
                     const int k0 = kb * BKE;
                     if (MX) {
                         uint8_t *sf = st + 2 * A_BYTES + B_BYTES;
                         tc::bulk_load(sf, p.sf_a + g.sfa0 + kb * 512, 512, fb);
                         tc::bulk_load(sf + 512, p.sf_a + g.sfa1 + kb * 512, 512, fb);
-                        tc::bulk_load(sf + 1024, p.sf_b + g.sfb + kb * 1024, 1024, fb);
+                        tc::bulk_load(sf + 1024, p.sf_b + g.sfb + kb * 512, 512, fb);
                     }
                     if (P::A_MN) {
                         tc::tma_load_2d(st, &tmA, fb, g.ax0, g.ay0 + k0);
@@ -580,13 +588,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ------------------------------------------------------------ MMA issuer
         if (tc::elect_one()) {
             int s = 0;
-            uint32_t ph = 0, acc_ph = 0;
-            for (int64_t u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
+            uint32_t ph = 0;
+            int64_t i = 0;  // units of this CTA so far; unit i uses accumulator set i % 2
+            for (int64_t u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++i) {
                 const Geom g = p.geom(u);
                 const uint32_t idesc = tc::idesc_bf16(128, g.n_mma, P::A_MN, P::B_MN);
                 const uint32_t idesc_mx = tc::idesc_mxf8(128, g.n_mma, 0);
-                if (!wait_or_abort(&sm->tmem_empty, acc_ph ^ 1u, p.status, abort)) break;
+                const int ab = (int)(i & 1);
+                const uint32_t use = (uint32_t)((i >> 1) & 1);
+                if (!wait_or_abort(&sm->tmem_empty[ab], use ^ 1u, p.status, abort)) break;
                 tc::tc_fence_after();
+                const uint32_t d0 = tmem + acc_col<MX>(ab, 0), d1 = tmem + acc_col<MX>(ab, 1);
                 const int kblocks = (g.k_steps + 3) / 4;
                 bool ok = true;
                 for (int kb = 0; kb < kblocks; ++kb) {
@@ -600,12 +612,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const uint32_t b = a0 + 2 * A_BYTES;
                     const int steps = g.k_steps - kb * 4 < 4 ? g.k_steps - kb * 4 : 4;
                     if (MX) {
-                        // this stage's scale atoms into TMEM: A0, A1, B rows 0-127, 128-255
+                        // this stage's scale atoms into TMEM: A0, A1, B
                         const uint32_t sf = b + B_BYTES;
                         tc::tmem_cp_32x128b_x4(tmem + SF_COL + 0, tc::sdesc_plain_rows16(sf));
                         tc::tmem_cp_32x128b_x4(tmem + SF_COL + 4, tc::sdesc_plain_rows16(sf + 512));
                         tc::tmem_cp_32x128b_x4(tmem + SF_COL + 8, tc::sdesc_plain_rows16(sf + 1024));
-                        tc::tmem_cp_32x128b_x4(tmem + SF_COL + 12, tc::sdesc_plain_rows16(sf + 1536));
                     }
                     for (int kk = 0; kk < steps; ++kk) {
                         // K-major: 16 elements = 32 bytes along the swizzled row;
@@ -622,13 +633,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             // byte kk of each 32-bit scale word is this K=32 block's scale
                             const uint32_t id = idesc_mx | ((uint32_t)kk << 4) |
                                                 ((uint32_t)kk << 29);
-                            tc::mma_mxf8(tmem + 0, da0, db, id, tmem + SF_COL + 0,
-                                         tmem + SF_COL + 8, acc);
-                            tc::mma_mxf8(tmem + ACC1, da1, db, id, tmem + SF_COL + 4,
-                                         tmem + SF_COL + 8, acc);
+                            tc::mma_mxf8(d0, da0, db, id, tmem + SF_COL + 0, tmem + SF_COL + 8,
+                                         acc);
+                            tc::mma_mxf8(d1, da1, db, id, tmem + SF_COL + 4, tmem + SF_COL + 8,
+                                         acc);
                         } else {
-                            tc::mma_f16(tmem + 0, da0, db, idesc, acc);
-                            tc::mma_f16(tmem + ACC1, da1, db, idesc, acc);
+                            tc::mma_f16(d0, da0, db, idesc, acc);
+                            tc::mma_f16(d1, da1, db, idesc, acc);
                         }
                     }
                     tc::mma_commit(&sm->empty[s]);  // frees the stage once these MMAs finish
@@ -638,8 +649,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                 }
                 if (!ok) break;
-                tc::mma_commit(&sm->tmem_full);
-                acc_ph ^= 1u;
+                tc::mma_commit(&sm->tmem_full[ab]);
+            }
+            // on an abort, do not free TMEM under MMAs still in flight: the last commit
+            // completes once every earlier MMA of this thread has (bounded wait)
+            if (i > 0) {
+                const int lb = (int)((i - 1) & 1);
+                const uint32_t lu = (uint32_t)(((i - 1) >> 1) & 1);
+                const uint64_t t0 = tc::globaltimer();
+                while (!tc::mbar_try_wait(&sm->tmem_full[lb], lu) &&
+                       tc::globaltimer() - t0 < 100000000ull) {
+                }
             }
         }
         __syncwarp();
@@ -647,19 +667,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        uint32_t acc_ph = 0;
+        uint32_t c0 = 0, c1 = 0;  // accumulator columns of the current unit
         auto ld = [&](int n0, float (&d0)[16], float (&d1)[16]) {
-            tc::tmem_ld16(tmem + lane_base + 0 + n0, d0);
-            tc::tmem_ld16(tmem + lane_base + ACC1 + n0, d1);
+            tc::tmem_ld16(tmem + lane_base + c0 + n0, d0);
+            tc::tmem_ld16(tmem + lane_base + c1 + n0, d1);
             tc::tmem_ld_wait();
         };
-        for (int64_t u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
-            if (!wait_or_abort(&sm->tmem_full, acc_ph, p.status, abort)) break;
+        int64_t i = 0;
+        for (int64_t u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++i) {
+            const int ab = (int)(i & 1);
+            if (!wait_or_abort(&sm->tmem_full[ab], (uint32_t)((i >> 1) & 1), p.status, abort))
+                break;
             tc::tc_fence_after();
+            c0 = acc_col<MX>(ab, 0);
+            c1 = acc_col<MX>(ab, 1);
             p.epilogue(u, ld, sm, q, lane);
             tc::tc_fence_before();
-            tc::mbar_arrive(&sm->tmem_empty);
-            acc_ph ^= 1u;
+            tc::mbar_arrive(&sm->tmem_empty[ab]);
         }
     }
 
@@ -829,7 +853,7 @@ cudaError_t launch_wgrad_tc(const int32_t *counts, const int32_t *poff, const ui
     CUtensorMap ma, mb;
     if ((e = make_map_bf16(&ma, A, rpad_cap, M, 64)) != cudaSuccess) return e;
     if ((e = make_map_bf16(&mb, Bm, rpad_cap, N, 64)) != cudaSuccess) return e;
-    const int nmb = (M + 255) / 256, nnb = (N + 255) / 256;
+    const int nmb = (M + 255) / 256, nnb = (N + TILE_ROWS - 1) / TILE_ROWS;
     Wgrad p{counts, poff, out, E, M, N, nmb, nnb, status};
     return launch(ma, mb, p, (int64_t)E * nmb * nnb, s);
 }

@@ -124,7 +124,7 @@ cudaError_t launch_gemm_up_tc_mx(const GemmUpArgs &a, int64_t ring_rows, const u
 cudaError_t launch_gemm_down_tc_mx(const GemmDownArgs &a, int64_t ring_rows, const uint8_t *sf_w,
                                    const uint8_t *sf_h, cudaStream_t s);
 // MXFP8 scales, plain [rows][K/32] -> the tensor cores' 128-row x 4-block atoms: per 128
-// weight rows, or per token tile of the list (two atoms per tile)
+// weight rows, or per token tile of the list (one atom per tile and K block)
 cudaError_t launch_scale_atoms_rows(const uint8_t *src, int64_t rows, int K, uint8_t *dst,
                                     cudaStream_t s);
 cudaError_t launch_scale_atoms_tiles(const int32_t *tiles, int64_t cap, const uint8_t *src,

@@ -121,20 +121,49 @@ def ncu_traffic(kernel):
         return None
 
 
-# algorithmic work per launch of each kernel kind, for a workload (R routed rows)
-def algorithmic(kind, c, n_launch_per_step):
+# algorithmic work of each kernel kind per step (BF16 training step, pre-activations
+# saved): tensor FLOPs and the HBM bytes the kernel cannot avoid moving (each operand read
+# once, each result written once)
+def algorithmic_step(kind, c):
     R, H, I, T, K, E = c.R, c.H, c.I, c.T, c.K, c.E
-    tensor = {"gemm_up_swiglu": 4.0 * R * H * I, "gemm_down_push": 2.0 * R * H * I,
-              "gemm_g_swiglu_bwd": 2.0 * R * H * I, "gemm_dgrad_push": 4.0 * R * H * I,
-              "wgrad_w13": 4.0 * R * H * I, "wgrad_w2": 2.0 * R * H * I}
-    hbm = {"gather": 2.0 * R * H * 2, "combine": R * H * 4 + T * H * 4 + R * 4,
+    w13, w2 = 2.0 * E * 2 * I * H, 2.0 * E * H * I        # bf16 weights
+    xr, hr, dyr = 2.0 * R * H, 2.0 * R * I, 2.0 * R * H    # bf16 routed rows
+    pre, slots = 4.0 * R * 2 * I, 4.0 * R * H              # fp32 pre-activations, slots
+    flops = {"gemm_up_swiglu": 4.0 * R * H * I, "gemm_down_push": 2.0 * R * H * I,
+             "gemm_g_swiglu_bwd": 2.0 * R * H * I, "gemm_dgrad_push": 4.0 * R * H * I,
+             "wgrad_w13": 4.0 * R * H * I, "wgrad_w2": 2.0 * R * H * I}
+    hbm = {"gemm_up_swiglu": w13 + xr + hr + pre,
+           "gemm_down_push": w2 + hr + slots,
+           "gemm_g_swiglu_bwd": w2 + dyr + pre + 2 * hr + hr,
+           "gemm_dgrad_push": w13 + 2 * hr + slots,
+           "wgrad_w13": xr + 2 * hr + 2 * w13,
+           "wgrad_w2": hr + dyr + 2 * w2,
+           "gather": 2.0 * T * H + xr, "combine": R * H * 4 + T * H * 4 + R * 4,
            "dx_reduce": R * H * 4 + T * H * 4, "route_topk": T * E * 4 + T * K * 8,
-           "gather_bwd": 4.0 * R * H * 2}
-    if kind in tensor:
-        return "tensor", tensor[kind] / n_launch_per_step
-    if kind in hbm:
-        return "hbm", hbm[kind] / n_launch_per_step
-    return None, None
+           "gather_bwd": 2 * (2.0 * T * H) + xr + dyr}
+    return flops.get(kind), hbm.get(kind)
+
+
+def roofline_of(kind, c, launches_per_step, avg_ms, pk):
+    """The bound (tensor or hbm) that sets the kernel's floor and the achieved fraction of
+    it, from algorithmic work per launch and the measured average launch duration."""
+    flops, nbytes = algorithmic_step(kind, c)
+    if nbytes is None:
+        return {"bound": None, "achieved": None, "peak": None, "unit": None, "frac": None}
+    flops = (flops or 0.0) / launches_per_step
+    nbytes = nbytes / launches_per_step
+    s = avg_ms * 1e-3
+    t_tensor = flops / (pk["bf16_sust"] * 1e12)
+    t_hbm = nbytes / (pk["hbm"] * 1e9)
+    if t_tensor >= t_hbm:
+        a = flops / s / 1e12
+        return {"bound": "tensor", "achieved": a, "peak": pk["bf16_sust"], "unit": "TFLOP/s",
+                "frac": a / pk["bf16_sust"], "peak_kind": "bf16 sustained, " + pk["src"],
+                "algorithmic_per_launch": flops}
+    a = nbytes / s / 1e9
+    return {"bound": "hbm", "achieved": a, "peak": pk["hbm"], "unit": "GB/s",
+            "frac": a / pk["hbm"], "peak_kind": "hbm copy, " + pk["src"],
+            "algorithmic_per_launch": nbytes}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -247,20 +276,11 @@ def run_mok(args):
                for k, (n, t) in prof.items()}
     dom = max(prof, key=lambda k: prof[k][1])
     pk = peaks()
-    n_l = prof[dom][0] / args.steps
-    bound, work = algorithmic(dom, cfg, n_l)
-    avg_s = prof[dom][1] / prof[dom][0] * 1e-3
-    if bound is None:
-        roof = {"bound": None, "achieved": None, "peak": None, "unit": None, "frac": None}
-    elif bound == "tensor":
-        achieved = work / avg_s / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_sust"],
-                "unit": "TFLOP/s", "frac": achieved / pk["bf16_sust"],
-                "peak_kind": "bf16 sustained, " + pk["src"]}
-    else:
-        achieved = work / avg_s / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
-                "frac": achieved / pk["hbm"], "peak_kind": "hbm copy, " + pk["src"]}
+    for k, v in kernels.items():
+        r = roofline_of(k, cfg, v["launches_per_step"], v["avg_ms"], pk)
+        if r["bound"] is not None:
+            v["bound"], v["frac"] = r["bound"], r["frac"]
+    roof = roofline_of(dom, cfg, kernels[dom]["launches_per_step"], kernels[dom]["avg_ms"], pk)
     roof["kernel"] = dom
     roof["traffic"] = ncu_traffic(dom)
 

@@ -8,8 +8,9 @@
 // router-weight gradient computed inside the SwiGLU backward.
 //
 // One persistent kernel template, 192 threads per CTA, one CTA per SM:
-//   warp 0     TMA producer: two 128-row A tiles and one B tile (up to 128 rows) per
-//              64-wide K block into a 4-stage shared-memory ring
+//   warp 0     TMA producer: two 128-row A tiles and one 128-row B tile per 64-wide K
+//              block into a 4-stage shared-memory ring, in as few boxes as the operand
+//              layout allows (each box costs the copy engine a fixed overhead)
 //   warp 1     TMEM owner and MMA issuer: D0 += A0 B^T, D1 += A1 B^T (M=128, N<=128,
 //              K=16 per instruction) into one of two fp32 accumulator sets in TMEM
 //   warps 2-5  epilogue: TMEM -> registers -> fused epilogue -> global memory
@@ -39,7 +40,8 @@ constexpr int BK_MX = 128;        // E4M3 K elements per stage (128 bytes per ro
 constexpr int STAGES = 4;
 constexpr int TILE_ROWS = 128;    // max N per unit (bf16)
 constexpr int TILE_ROWS_MX = 112; // max N per unit (MXFP8: TMEM also holds the scales)
-constexpr int KBOX_ROWS = 32;     // rows per TMA box of a K-major B operand
+constexpr int KBOX_ROWS = 128;    // rows of the TMA box of a K-major B operand: a tile's rows
+                                  // and whatever follows them (unused) or zero fill past the end
 constexpr int A_BYTES = 128 * 128;                // 128 rows x 128 bytes
 constexpr int B_BYTES = TILE_ROWS * 128;          // 128 rows x 128 bytes
 constexpr int SF_BYTES = 2048;    // MXFP8 scale atoms per stage: A0, A1, B (512 B each), pad
@@ -77,12 +79,19 @@ __host__ __device__ constexpr int smem_bytes() {
     return STAGES * stage_bytes<MX>() + 1024 /*align*/ + (int)sizeof(Smem);
 }
 
+// How the producer fetches A0 and A1 (128 rows each) for one stage:
+enum AMode {
+    A_ROWS256 = 0,  // K-major, A1 directly below A0: one 256-row box at (k, ay0)
+    A_PAIR5D = 1,   // K-major W13 gate/up blocks: one 5D box at (k, 0, ay0 = block, 0, ay1 = e)
+    A_MN4 = 2,      // MN-major: four 64x64 boxes at (ax0, ay0 + k), (ax0 + 64, ..), (ax1, ..)
+};
+
 // One work unit as the producer and the MMA issuer see it.
 struct Geom {
-    int32_t ax0, ay0, ax1, ay1;  // first box of A0 and A1 (x innermost)
+    int32_t ax0, ay0, ax1, ay1;  // A0 and A1 coordinates (x innermost), per the policy's AMode
     int32_t bx, by;              // first box of B
     int n_mma;                   // N of each MMA (multiple of 16, <= 256)
-    int nbox;                    // B boxes per stage
+    int nbox;                    // B boxes per stage (MN-major B only)
     int k_steps;                 // K steps of one MMA (16 bf16 or 32 E4M3 elements); 0 leaves
                                  // the accumulators unwritten
     int64_t sfa0, sfa1, sfb;     // MXFP8: byte offsets of the first stage's scale atoms
@@ -135,6 +144,7 @@ struct TileUnits {
 template <bool MXv>
 struct FwdUpT {
     static constexpr bool A_MN = false, B_MN = false, MX = MXv;
+    static constexpr int A_MODE = A_PAIR5D;
     TileUnits tu;
     int H, I;
     Ring ring;
@@ -153,17 +163,18 @@ struct FwdUpT {
         const RingMap rm{ring.R, ring.MB, ring.n_slots};
         Geom g;
         g.ax0 = 0;
-        g.ay0 = e * 2 * I + mb * 128;
+        g.ay0 = mb;
         g.ax1 = 0;
-        g.ay1 = g.ay0 + I;
+        g.ay1 = e;
         g.bx = 0;
         g.by = (int32_t)rm(r0);
         g.n_mma = (int)((r1 - r0 + 15) & ~15);
-        g.nbox = (int)((r1 - r0 + KBOX_ROWS - 1) / KBOX_ROWS);
+        g.nbox = 1;
         g.k_steps = MX ? H / 32 : H / 16;
         const int64_t kg = H / 128;
-        g.sfa0 = (int64_t)(g.ay0 / 128) * kg * 512;
-        g.sfa1 = (int64_t)(g.ay1 / 128) * kg * 512;
+        const int64_t gate_row = (int64_t)e * 2 * I + mb * 128;
+        g.sfa0 = (gate_row / 128) * kg * 512;
+        g.sfa1 = ((gate_row + I) / 128) * kg * 512;
         g.sfb = (u / tu.n_mblocks) * kg * 512;
         return g;
     }
@@ -213,6 +224,7 @@ struct FwdUpT {
 template <bool MXv>
 struct FwdDownT {
     static constexpr bool A_MN = false, B_MN = false, MX = MXv;
+    static constexpr int A_MODE = A_ROWS256;
     TileUnits tu;
     int H, I;
     Ring ring;
@@ -235,7 +247,7 @@ struct FwdDownT {
         g.bx = 0;
         g.by = (int32_t)rm(r0);
         g.n_mma = (int)((r1 - r0 + 15) & ~15);
-        g.nbox = (int)((r1 - r0 + KBOX_ROWS - 1) / KBOX_ROWS);
+        g.nbox = 1;
         g.k_steps = MX ? I / 32 : I / 16;
         const int64_t kg = I / 128;
         g.sfa0 = (int64_t)(g.ay0 / 128) * kg * 512;
@@ -277,6 +289,7 @@ struct FwdDownT {
 // [mb*256, +128) and [mb*256+128, +128) of W2^T (MN-major: W2 rows are c).
 struct BwdG {
     static constexpr bool A_MN = true, B_MN = false, MX = false;
+    static constexpr int A_MODE = A_MN4;
     static constexpr const uint8_t *sf_a = nullptr, *sf_b = nullptr;
     TileUnits tu;
     int H, I;
@@ -300,7 +313,7 @@ struct BwdG {
         g.bx = 0;
         g.by = (int32_t)(poff[e] + (r0 - offsets[e]));
         g.n_mma = (int)((r1 - r0 + 15) & ~15);
-        g.nbox = (int)((r1 - r0 + KBOX_ROWS - 1) / KBOX_ROWS);
+        g.nbox = 1;
         g.k_steps = H / 16;
         return g;
     }
@@ -379,6 +392,7 @@ struct BwdG {
 // (MN-major: W13 rows are j).
 struct BwdDgrad {
     static constexpr bool A_MN = true, B_MN = false, MX = false;
+    static constexpr int A_MODE = A_MN4;
     static constexpr const uint8_t *sf_a = nullptr, *sf_b = nullptr;
     TileUnits tu;
     int H, I;
@@ -399,7 +413,7 @@ struct BwdDgrad {
         g.bx = 0;
         g.by = (int32_t)(poff[e] + (r0 - offsets[e]));
         g.n_mma = (int)((r1 - r0 + 15) & ~15);
-        g.nbox = (int)((r1 - r0 + KBOX_ROWS - 1) / KBOX_ROWS);
+        g.nbox = 1;
         g.k_steps = 2 * I / 16;
         return g;
     }
@@ -435,6 +449,7 @@ struct BwdDgrad {
 // A[p][m] * B[p][n]; A, B row-major [rows][M] / [rows][N] (both MN-major operands).
 struct Wgrad {
     static constexpr bool A_MN = true, B_MN = true, MX = false;
+    static constexpr int A_MODE = A_MN4;
     static constexpr const uint8_t *sf_a = nullptr, *sf_b = nullptr;
     const int32_t *counts, *poff;
     float *out;
@@ -539,7 +554,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     if (!wait_or_abort(&sm->empty[s], ph ^ 1u, p.status, abort)) break;
                     uint8_t *st = base + s * SB;
                     uint64_t *fb = &sm->full[s];
-                    tc::mbar_arrive_expect_tx(fb, 2 * A_BYTES + g.nbox * B_BOX +
+                    tc::mbar_arrive_expect_tx(fb, 2 * A_BYTES +
+                                                      (P::B_MN ? g.nbox * B_BOX : B_BYTES) +
                                                       (MX ? 1536 : 0));
                     const int k0 = kb * BKE;
                     if (MX) {
@@ -548,22 +564,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         tc::bulk_load(sf + 512, p.sf_a + g.sfa1 + kb * 512, 512, fb);
                         tc::bulk_load(sf + 1024, p.sf_b + g.sfb + kb * 512, 512, fb);
                     }
-                    if (P::A_MN) {
+                    if (P::A_MODE == A_MN4) {
                         tc::tma_load_2d(st, &tmA, fb, g.ax0, g.ay0 + k0);
                         tc::tma_load_2d(st + A_HALF, &tmA, fb, g.ax0 + 64, g.ay0 + k0);
                         tc::tma_load_2d(st + A_BYTES, &tmA, fb, g.ax1, g.ay1 + k0);
                         tc::tma_load_2d(st + A_BYTES + A_HALF, &tmA, fb, g.ax1 + 64, g.ay1 + k0);
+                    } else if (P::A_MODE == A_PAIR5D) {
+                        tc::tma_load_5d(st, &tmA, fb, k0, 0, g.ay0, 0, g.ay1);
                     } else {
-                        tc::tma_load_2d(st, &tmA, fb, g.ax0 + k0, g.ay0);
-                        tc::tma_load_2d(st + A_BYTES, &tmA, fb, g.ax1 + k0, g.ay1);
+                        tc::tma_load_2d(st, &tmA, fb, k0, g.ay0);
                     }
                     uint8_t *bt = st + 2 * A_BYTES;
-                    for (int j = 0; j < g.nbox; ++j) {
-                        if (P::B_MN)
+                    if (P::B_MN) {
+                        for (int j = 0; j < g.nbox; ++j)
                             tc::tma_load_2d(bt + j * B_BOX, &tmB, fb, g.bx + 64 * j, g.by + k0);
-                        else
-                            tc::tma_load_2d(bt + j * B_BOX, &tmB, fb, g.bx + k0,
-                                            g.by + KBOX_ROWS * j);
+                    } else {
+                        tc::tma_load_2d(bt, &tmB, fb, k0, g.by);
                     }
                     ++issued;
                     if (++s == STAGES) {
@@ -748,6 +764,24 @@ cudaError_t make_map_u8(CUtensorMap *m, const void *ptr, int64_t rows, int64_t c
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// W13 [E][2I][H] (bf16, or E4M3 bytes when mx) viewed as 5D [E][2][I/128][128][H] (gate
+// rows, then up rows): one box of {one 128-byte K block, 128 rows, 1 block, 2 halves, 1
+// expert} puts the gate block and its up block one after the other in shared memory.
+cudaError_t make_map_w13_pairs(CUtensorMap *m, const void *ptr, int64_t E, int64_t I,
+                               int64_t H, bool mx) {
+    const int64_t es = mx ? 1 : 2;
+    cuuint64_t dims[5] = {(cuuint64_t)H, 128, (cuuint64_t)(I / 128), 2, (cuuint64_t)E};
+    cuuint64_t strides[4] = {(cuuint64_t)(H * es), (cuuint64_t)(128 * H * es),
+                             (cuuint64_t)(I * H * es), (cuuint64_t)(2 * I * H * es)};
+    cuuint32_t box[5] = {(cuuint32_t)(mx ? BK_MX : BK), 128, 1, 2, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(m, mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          5, const_cast<void *>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <class P>
 cudaError_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const P &p, int64_t units_cap,
                    cudaStream_t s) {
@@ -772,8 +806,8 @@ int gemm_tc_tile_rows(bool mxfp8) { return mxfp8 ? TILE_ROWS_MX : TILE_ROWS; }
 cudaError_t launch_gemm_up_tc(const GemmUpArgs &a, int64_t ring_rows, cudaStream_t s) {
     cudaError_t e = init_host();
     if (e != cudaSuccess) return e;
-    CUtensorMap ma, mb;  // A: W13 as [E*2I][H]; B: the x ring [ring_rows][H]
-    if ((e = make_map_bf16(&ma, a.w13, (int64_t)a.E * 2 * a.I, a.H, 128)) != cudaSuccess) return e;
+    CUtensorMap ma, mb;  // A: W13 gate/up block pairs; B: the x ring [ring_rows][H]
+    if ((e = make_map_w13_pairs(&ma, a.w13, a.E, a.I, a.H, false)) != cudaSuccess) return e;
     if ((e = make_map_bf16(&mb, a.xring, ring_rows, a.H, KBOX_ROWS)) != cudaSuccess) return e;
     FwdUpT<false> p{TileUnits{a.tiles, a.tiles_cap, a.I / 128}, a.H, a.I, a.ring, a.hring,
                     a.hring_s, a.preact, false, a.status, nullptr, nullptr};
@@ -783,8 +817,8 @@ cudaError_t launch_gemm_up_tc(const GemmUpArgs &a, int64_t ring_rows, cudaStream
 cudaError_t launch_gemm_down_tc(const GemmDownArgs &a, int64_t ring_rows, cudaStream_t s) {
     cudaError_t e = init_host();
     if (e != cudaSuccess) return e;
-    CUtensorMap ma, mb;  // A: W2 as [E*H][I]; B: the h ring [ring_rows][I]
-    if ((e = make_map_bf16(&ma, a.w2, (int64_t)a.E * a.H, a.I, 128)) != cudaSuccess) return e;
+    CUtensorMap ma, mb;  // A: W2 as [E*H][I], 256-row boxes; B: the h ring [ring_rows][I]
+    if ((e = make_map_bf16(&ma, a.w2, (int64_t)a.E * a.H, a.I, 256)) != cudaSuccess) return e;
     if ((e = make_map_bf16(&mb, a.hring, ring_rows, a.I, KBOX_ROWS)) != cudaSuccess) return e;
     const int nmb = (a.H + 255) / 256;
     FwdDownT<false> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.ring, a.perm, a.slots,
@@ -796,8 +830,8 @@ cudaError_t launch_gemm_up_tc_mx(const GemmUpArgs &a, int64_t ring_rows, const u
                                  const uint8_t *sf_x, cudaStream_t s) {
     cudaError_t e = init_host();
     if (e != cudaSuccess) return e;
-    CUtensorMap ma, mb;  // A: W13 E4M3 [E*2I][H]; B: the quantized x ring [ring_rows][H]
-    if ((e = make_map_u8(&ma, a.w13, (int64_t)a.E * 2 * a.I, a.H, 128)) != cudaSuccess) return e;
+    CUtensorMap ma, mb;  // A: W13 E4M3 gate/up block pairs; B: the quantized x ring
+    if ((e = make_map_w13_pairs(&ma, a.w13, a.E, a.I, a.H, true)) != cudaSuccess) return e;
     if ((e = make_map_u8(&mb, a.xring, ring_rows, a.H, KBOX_ROWS)) != cudaSuccess) return e;
     FwdUpT<true> p{TileUnits{a.tiles, a.tiles_cap, a.I / 128}, a.H, a.I, a.ring, a.hring,
                    a.hring_s, nullptr, true, a.status, sf_w, sf_x};
@@ -808,8 +842,8 @@ cudaError_t launch_gemm_down_tc_mx(const GemmDownArgs &a, int64_t ring_rows, con
                                    const uint8_t *sf_h, cudaStream_t s) {
     cudaError_t e = init_host();
     if (e != cudaSuccess) return e;
-    CUtensorMap ma, mb;  // A: W2 E4M3 [E*H][I]; B: the quantized h ring [ring_rows][I]
-    if ((e = make_map_u8(&ma, a.w2, (int64_t)a.E * a.H, a.I, 128)) != cudaSuccess) return e;
+    CUtensorMap ma, mb;  // A: W2 E4M3 [E*H][I], 256-row boxes; B: the quantized h ring
+    if ((e = make_map_u8(&ma, a.w2, (int64_t)a.E * a.H, a.I, 256)) != cudaSuccess) return e;
     if ((e = make_map_u8(&mb, a.hring, ring_rows, a.I, KBOX_ROWS)) != cudaSuccess) return e;
     const int nmb = (a.H + 255) / 256;
     FwdDownT<true> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.ring, a.perm, a.slots,

@@ -73,6 +73,15 @@ MOK_DEV void tma_load_2d(void *smem_dst, const CUtensorMap *m, uint64_t *bar, in
         "l"((uint64_t)m), "r"(smem_u32(bar)), "r"(x), "r"(y)
         : "memory");
 }
+// 5D tile load (coordinates innermost first), completion counted on `bar`
+MOK_DEV void tma_load_5d(void *smem_dst, const CUtensorMap *m, uint64_t *bar, int32_t c0,
+                         int32_t c1, int32_t c2, int32_t c3, int32_t c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"((uint64_t)m), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+        : "memory");
+}
 
 // 1D bulk copy global -> shared (16-byte aligned, size a multiple of 16), counted on `bar`
 MOK_DEV void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar) {

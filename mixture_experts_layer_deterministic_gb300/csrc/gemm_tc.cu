@@ -7,13 +7,14 @@
 // GEMMs fed by pull dispatch, results pushed back to their (token, k) slots, and the
 // router-weight gradient computed inside the SwiGLU backward.
 //
-// One persistent kernel template, 192 threads per CTA, one CTA per SM:
+// One persistent kernel template, 320 threads per CTA, one CTA per SM:
 //   warp 0     TMA producer: two 128-row A tiles and one 128-row B tile per 64-wide K
 //              block into a 4-stage shared-memory ring, in as few boxes as the operand
 //              layout allows (each box costs the copy engine a fixed overhead)
 //   warp 1     TMEM owner and MMA issuer: D0 += A0 B^T, D1 += A1 B^T (M=128, N<=128,
 //              K=16 per instruction) into one of two fp32 accumulator sets in TMEM
-//   warps 2-5  epilogue: TMEM -> registers -> fused epilogue -> global memory
+//   warps 2-9  epilogue: TMEM -> registers -> fused epilogue -> global memory; two warps
+//              per TMEM lane quadrant, taking alternate 16-column chunks of a unit
 // The two accumulator sets alternate between consecutive units of a CTA, so the epilogue
 // of one unit runs while the tensor cores compute the next.
 // A problem policy supplies the work-unit decomposition, the operand majors and the
@@ -45,7 +46,8 @@ constexpr int KBOX_ROWS = 128;    // rows of the TMA box of a K-major B operand:
 constexpr int A_BYTES = 128 * 128;                // 128 rows x 128 bytes
 constexpr int B_BYTES = TILE_ROWS * 128;          // 128 rows x 128 bytes
 constexpr int SF_BYTES = 2048;    // MXFP8 scale atoms per stage: A0, A1, B (512 B each), pad
-constexpr int NTHREADS = 192;
+constexpr int EPI_WARPS = 8;
+constexpr int NTHREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL = 480;  // MXFP8: TMEM columns of the stage's scale atoms
 // TMEM column of accumulator a (0: A0, 1: A1) of accumulator set b
@@ -71,7 +73,7 @@ struct Smem {
     uint64_t tmem_empty[2];  // the epilogue has drained accumulator set b
     uint32_t tmem_base;
     int abort;
-    EpiScratch epi[4];
+    EpiScratch epi[EPI_WARPS];
 };
 
 template <bool MX>
@@ -179,7 +181,8 @@ struct FwdUpT {
         return g;
     }
     template <class LD>
-    MOK_DEV void epilogue(int64_t u, const LD &ld, Smem *, int q, int lane) const {
+    MOK_DEV void epilogue(int64_t u, const LD &ld, EpiScratch &, int q, int half,
+                          int lane) const {
         int e, mb;
         int64_t r0, r1;
         tu.get(u, &e, &r0, &r1, &mb);
@@ -187,7 +190,7 @@ struct FwdUpT {
         const int n_mma = (nr + 15) & ~15;
         const RingMap rm{ring.R, ring.MB, ring.n_slots};
         const int i = mb * 128 + q * 32 + lane;  // gate feature; its up feature is I + i
-        for (int n0 = 0; n0 < n_mma; n0 += 16) {
+        for (int n0 = 16 * half; n0 < n_mma; n0 += 32) {
             float d0[16], d1[16];
             ld(n0, d0, d1);
 #pragma unroll
@@ -258,17 +261,18 @@ struct FwdDownT {
         return g;
     }
     template <class LD>
-    MOK_DEV void epilogue(int64_t u, const LD &ld, Smem *sm, int q, int lane) const {
+    MOK_DEV void epilogue(int64_t u, const LD &ld, EpiScratch &es, int q, int half,
+                          int lane) const {
         int e, mb;
         int64_t r0, r1;
         tu.get(u, &e, &r0, &r1, &mb);
         const int nr = (int)(r1 - r0);
         const int n_mma = (nr + 15) & ~15;
         const int c = mb * 256 + q * 32 + lane;
-        int *fcol = reinterpret_cast<int *>(sm->epi[q].col);  // slot of each column
+        int *fcol = reinterpret_cast<int *>(es.col);  // slot of each column
         for (int n = lane; n < nr; n += 32) fcol[n] = perm[r0 + n];
         __syncwarp();
-        for (int n0 = 0; n0 < n_mma; n0 += 16) {
+        for (int n0 = 16 * half; n0 < n_mma; n0 += 32) {
             float d0[16], d1[16];
             ld(n0, d0, d1);
 #pragma unroll
@@ -318,7 +322,8 @@ struct BwdG {
         return g;
     }
     template <class LD>
-    MOK_DEV void epilogue(int64_t u, const LD &ld, Smem *sm, int q, int lane) const {
+    MOK_DEV void epilogue(int64_t u, const LD &ld, EpiScratch &es, int q, int half,
+                          int lane) const {
         int e, mb;
         int64_t r0, r1;
         tu.get(u, &e, &r0, &r1, &mb);
@@ -327,11 +332,10 @@ struct BwdG {
         const int64_t pb = poff[e] + (r0 - offsets[e]);
         const bool last = r1 == offsets[e + 1];
         const int i0 = mb * 256 + q * 32 + lane;
-        EpiScratch &es = sm->epi[q];
         // the routing weight of every column of the unit, loaded once
         for (int n = lane; n < nr; n += 32) es.col[n] = topk_w[perm[r0 + n]];
         __syncwarp();
-        for (int n0 = 0; n0 < n_mma; n0 += 16) {
+        for (int n0 = 16 * half; n0 < n_mma; n0 += 32) {
             float d[2][16];
             ld(n0, d[0], d[1]);
             // issue every pre-activation load of the chunk before using any
@@ -418,17 +422,18 @@ struct BwdDgrad {
         return g;
     }
     template <class LD>
-    MOK_DEV void epilogue(int64_t u, const LD &ld, Smem *sm, int q, int lane) const {
+    MOK_DEV void epilogue(int64_t u, const LD &ld, EpiScratch &es, int q, int half,
+                          int lane) const {
         int e, mb;
         int64_t r0, r1;
         tu.get(u, &e, &r0, &r1, &mb);
         const int nr = (int)(r1 - r0);
         const int n_mma = (nr + 15) & ~15;
         const int c = mb * 256 + q * 32 + lane;
-        int *fcol = reinterpret_cast<int *>(sm->epi[q].col);  // slot of each column
+        int *fcol = reinterpret_cast<int *>(es.col);  // slot of each column
         for (int n = lane; n < nr; n += 32) fcol[n] = perm[r0 + n];
         __syncwarp();
-        for (int n0 = 0; n0 < n_mma; n0 += 16) {
+        for (int n0 = 16 * half; n0 < n_mma; n0 += 32) {
             float d0[16], d1[16];
             ld(n0, d0, d1);
 #pragma unroll
@@ -481,14 +486,15 @@ struct Wgrad {
         return g;
     }
     template <class LD>
-    MOK_DEV void epilogue(int64_t u, const LD &ld, Smem *, int q, int lane) const {
+    MOK_DEV void epilogue(int64_t u, const LD &ld, EpiScratch &, int q, int half,
+                          int lane) const {
         int e, mb, nb;
         get(u, &e, &mb, &nb);
         const int nn = N - nb * TILE_ROWS < TILE_ROWS ? N - nb * TILE_ROWS : TILE_ROWS;
         const bool any = counts[e] > 0;
         const int m = mb * 256 + q * 32 + lane;
         float *o = out + (int64_t)e * N * M;
-        for (int n0 = 0; n0 < nn; n0 += 16) {
+        for (int n0 = 16 * half; n0 < nn; n0 += 32) {
             float d0[16], d1[16];
             ld(n0, d0, d1);
 #pragma unroll
@@ -522,7 +528,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&sm->tmem_full[b], 1);
-            tc::mbar_init(&sm->tmem_empty[b], 128);
+            tc::mbar_init(&sm->tmem_empty[b], 32 * EPI_WARPS);
         }
         sm->abort = 0;
         tc::fence_mbar_init();
@@ -682,6 +688,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        const int half = (warp - 2) >> 2;  // which alternate 16-column chunks it takes
+        EpiScratch &es = sm->epi[warp - 2];
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         uint32_t c0 = 0, c1 = 0;  // accumulator columns of the current unit
         auto ld = [&](int n0, float (&d0)[16], float (&d1)[16]) {
@@ -697,7 +705,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::tc_fence_after();
             c0 = acc_col<MX>(ab, 0);
             c1 = acc_col<MX>(ab, 1);
-            p.epilogue(u, ld, sm, q, lane);
+            p.epilogue(u, ld, es, q, half, lane);
             tc::tc_fence_before();
             tc::mbar_arrive(&sm->tmem_empty[ab]);
         }

@@ -108,13 +108,13 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel):
+def ncu_traffic(kernel, workload):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+    on the current kernel sources and applies to `workload` (else None)."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
             t = json.load(f)
-        if t.get("source_sha") != kernel_source_sha():
+        if t.get("source_sha") != kernel_source_sha() or t.get("scaled_to") != workload:
             return None
         return t["kernels"].get(kernel)
     except Exception:
@@ -282,7 +282,7 @@ def run_mok(args):
             v["bound"], v["frac"] = r["bound"], r["frac"]
     roof = roofline_of(dom, cfg, kernels[dom]["launches_per_step"], kernels[dom]["avg_ms"], pk)
     roof["kernel"] = dom
-    roof["traffic"] = ncu_traffic(dom)
+    roof["traffic"] = ncu_traffic(dom, args.workload)
 
     # phases: forward alone, backward alone, MXFP8 forward
     phases = {}

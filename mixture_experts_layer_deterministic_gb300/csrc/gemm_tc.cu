@@ -17,6 +17,14 @@
 //              per TMEM lane quadrant, taking alternate 16-column chunks of a unit
 // The two accumulator sets alternate between consecutive units of a CTA, so the epilogue
 // of one unit runs while the tensor cores compute the next.
+//
+// Scheduling: one CTA is launched per work unit, but a running CTA does not exit after its
+// unit. Near the end of each unit its producer thread asks Cluster Launch Control to cancel
+// the launch of a CTA that has not started yet and takes over that CTA's unit, so about one
+// CTA per SM runs and units go, in launch order, to whichever CTA frees up first. (The G
+// GEMM instead strides statically over its units with one CTA per SM; see BwdG.) The producer passes each unit index to
+// the MMA thread and the epilogue warps through a small shared-memory queue. CTAs whose
+// index is past the device-side unit count return at once.
 // A problem policy supplies the work-unit decomposition, the operand majors and the
 // epilogue:
 //   FwdUp     A = W13 (K-major), B = x ring (K-major)      -> SwiGLU, h (bf16 / MXFP8)
@@ -47,6 +55,7 @@ constexpr int A_BYTES = 128 * 128;                // 128 rows x 128 bytes
 constexpr int B_BYTES = TILE_ROWS * 128;          // 128 rows x 128 bytes
 constexpr int SF_BYTES = 2048;    // MXFP8 scale atoms per stage: A0, A1, B (512 B each), pad
 constexpr int EPI_WARPS = 8;
+constexpr int QD = 8;             // depth of the shared-memory queue of unit indices
 constexpr int NTHREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL = 480;  // MXFP8: TMEM columns of the stage's scale atoms
@@ -67,8 +76,13 @@ struct EpiScratch {
 };
 
 struct Smem {
+    uint4 clc_resp;          // Cluster Launch Control response (16-byte aligned)
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
+    uint64_t qfull[QD];      // unit queue: the producer published slot j
+    uint64_t qempty[QD];     // the MMA thread and every epilogue warp read slot j
+    uint64_t clc_bar;        // a cancel response has landed
+    int32_t q[QD];           // unit indices, -1 = no more work
     uint64_t tmem_full[2];   // accumulator set b holds a finished unit
     uint64_t tmem_empty[2];  // the epilogue has drained accumulator set b
     uint32_t tmem_base;
@@ -147,6 +161,7 @@ template <bool MXv>
 struct FwdUpT {
     static constexpr bool A_MN = false, B_MN = false, MX = MXv;
     static constexpr int A_MODE = A_PAIR5D;
+    static constexpr bool CLC = true;
     TileUnits tu;
     int H, I;
     Ring ring;
@@ -228,6 +243,7 @@ template <bool MXv>
 struct FwdDownT {
     static constexpr bool A_MN = false, B_MN = false, MX = MXv;
     static constexpr int A_MODE = A_ROWS256;
+    static constexpr bool CLC = true;
     TileUnits tu;
     int H, I;
     Ring ring;
@@ -294,6 +310,11 @@ struct FwdDownT {
 struct BwdG {
     static constexpr bool A_MN = true, B_MN = false, MX = false;
     static constexpr int A_MODE = A_MN4;
+    // static striding: the four units of a token tile (one per 256-feature block) then run
+    // in lockstep on neighbouring CTAs, so their epilogues read the pre-activation rows
+    // together; under Cluster Launch Control they drift apart and this epilogue-bound
+    // kernel measured 16% slower
+    static constexpr bool CLC = false;
     static constexpr const uint8_t *sf_a = nullptr, *sf_b = nullptr;
     TileUnits tu;
     int H, I;
@@ -397,6 +418,7 @@ struct BwdG {
 struct BwdDgrad {
     static constexpr bool A_MN = true, B_MN = false, MX = false;
     static constexpr int A_MODE = A_MN4;
+    static constexpr bool CLC = true;
     static constexpr const uint8_t *sf_a = nullptr, *sf_b = nullptr;
     TileUnits tu;
     int H, I;
@@ -455,6 +477,7 @@ struct BwdDgrad {
 struct Wgrad {
     static constexpr bool A_MN = true, B_MN = true, MX = false;
     static constexpr int A_MODE = A_MN4;
+    static constexpr bool CLC = true;
     static constexpr const uint8_t *sf_a = nullptr, *sf_b = nullptr;
     const int32_t *counts, *poff;
     float *out;
@@ -520,6 +543,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     Smem *sm = (Smem *)(base + STAGES * SB);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t n_units = p.n_units();
+    if ((int64_t)blockIdx.x >= n_units) return;  // uniform across the CTA
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -530,6 +554,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::mbar_init(&sm->tmem_full[b], 1);
             tc::mbar_init(&sm->tmem_empty[b], 32 * EPI_WARPS);
         }
+        for (int j = 0; j < QD; ++j) {
+            tc::mbar_init(&sm->qfull[j], 1);
+            tc::mbar_init(&sm->qempty[j], 1 + EPI_WARPS);
+        }
+        tc::mbar_init(&sm->clc_bar, 1);
         sm->abort = 0;
         tc::fence_mbar_init();
         tc::prefetch_tmap(&tmA);
@@ -551,13 +580,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ------------------------------------------------------------ TMA producer
         if (tc::elect_one()) {
             int s = 0;
-            uint32_t ph = 0;
-            int64_t issued = 0;
-            for (int64_t u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
+            uint32_t ph = 0, clc_ph = 0;
+            int64_t issued = 0, j = 0;
+            bool clc_live = true, clc_pending = false;
+            int64_t u = blockIdx.x;
+            for (;;) {
+                // publish the unit (or the end marker) to the MMA thread and the epilogue
+                const int slot = (int)(j % QD);
+                if (!wait_or_abort(&sm->qempty[slot], (uint32_t)(((j / QD) & 1) ^ 1), p.status,
+                                   abort))
+                    break;
+                *(volatile int32_t *)&sm->q[slot] = (int32_t)u;
+                tc::mbar_arrive(&sm->qfull[slot]);
+                ++j;
+                if (u < 0) break;
                 const Geom g = p.geom(u);
                 const int kblocks = (g.k_steps + 3) / 4;
+                // ask for the next unit while the last two stages of this one are issued:
+                // asking later keeps units that share operand tiles (consecutive indices)
+                // starting together on whichever CTAs free up, so L2 serves their re-reads
+                const int ask_at = kblocks > 2 ? kblocks - 2 : 0;
+                bool ok = true;
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!wait_or_abort(&sm->empty[s], ph ^ 1u, p.status, abort)) break;
+                    if (P::CLC && kb == ask_at && clc_live) {
+                        tc::mbar_arrive_expect_tx(&sm->clc_bar, 16);
+                        tc::clc_try_cancel(&sm->clc_resp, &sm->clc_bar);
+                        clc_pending = true;
+                    }
+                    if (!wait_or_abort(&sm->empty[s], ph ^ 1u, p.status, abort)) {
+                        ok = false;
+                        break;
+                    }
                     uint8_t *st = base + s * SB;
                     uint64_t *fb = &sm->full[s];
                     tc::mbar_arrive_expect_tx(fb, 2 * A_BYTES +
@@ -593,6 +646,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         ph ^= 1u;
                     }
                 }
+                if (!ok) break;
+                int64_t next = -1;
+                if (!P::CLC) {
+                    next = u + (int64_t)gridDim.x < n_units ? u + (int64_t)gridDim.x : -1;
+                } else if (clc_pending) {
+                    if (!wait_or_abort(&sm->clc_bar, clc_ph, p.status, abort)) break;
+                    clc_ph ^= 1u;
+                    clc_pending = false;
+                    uint32_t x;
+                    // after a failed or out-of-range answer no further request is made
+                    if (tc::clc_query(&sm->clc_resp, &x) && (int64_t)x < n_units)
+                        next = x;
+                    else
+                        clc_live = false;
+                }
+                u = next;
+            }
+            // do not leave while a cancel response may still be landing
+            if (clc_pending) {
+                const uint64_t t0 = tc::globaltimer();
+                while (!tc::mbar_try_wait(&sm->clc_bar, clc_ph) &&
+                       tc::globaltimer() - t0 < 100000000ull) {
+                }
             }
             // do not leave while copies this CTA issued may still be landing
             for (int q = 0; q < STAGES && q < issued; ++q) {
@@ -612,7 +688,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             int s = 0;
             uint32_t ph = 0;
             int64_t i = 0;  // units of this CTA so far; unit i uses accumulator set i % 2
-            for (int64_t u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++i) {
+            for (;; ++i) {
+                const int slot = (int)(i % QD);
+                if (!wait_or_abort(&sm->qfull[slot], (uint32_t)((i / QD) & 1), p.status, abort))
+                    break;
+                const int64_t u = *(volatile int32_t *)&sm->q[slot];
+                tc::mbar_arrive(&sm->qempty[slot]);
+                if (u < 0) break;
                 const Geom g = p.geom(u);
                 const uint32_t idesc = tc::idesc_bf16(128, g.n_mma, P::A_MN, P::B_MN);
                 const uint32_t idesc_mx = tc::idesc_mxf8(128, g.n_mma, 0);
@@ -697,8 +779,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::tmem_ld16(tmem + lane_base + c1 + n0, d1);
             tc::tmem_ld_wait();
         };
-        int64_t i = 0;
-        for (int64_t u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++i) {
+        for (int64_t i = 0;; ++i) {
+            const int slot = (int)(i % QD);
+            if (!wait_or_abort(&sm->qfull[slot], (uint32_t)((i / QD) & 1), p.status, abort))
+                break;
+            const int64_t u = *(volatile int32_t *)&sm->q[slot];
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&sm->qempty[slot]);
+            if (u < 0) break;
             const int ab = (int)(i & 1);
             if (!wait_or_abort(&sm->tmem_full[ab], (uint32_t)((i >> 1) & 1), p.status, abort))
                 break;
@@ -801,8 +889,11 @@ cudaError_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const P &p, int
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    const int grid = (int)(units_cap < g_num_sms ? units_cap : g_num_sms);
-    if (grid < 1) return cudaSuccess;
+    // Cluster Launch Control: one CTA per unit, running CTAs take over the units of CTAs
+    // not yet launched; static striding: one CTA per SM
+    if (units_cap < 1) return cudaSuccess;
+    if (units_cap > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    const int grid = P::CLC || units_cap < g_num_sms ? (int)units_cap : g_num_sms;
     tc_gemm_kernel<P><<<grid, NTHREADS, SMEM, s>>>(ma, mb, p);
     return cudaGetLastError();
 }

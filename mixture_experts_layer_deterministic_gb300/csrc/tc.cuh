@@ -92,6 +92,33 @@ MOK_DEV void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_
         : "memory");
 }
 
+// ---------------------------------------------------------------- Cluster Launch Control
+// Ask the hardware to cancel the launch of a CTA (a cluster of one) that has not started;
+// a 16-byte response lands in shared memory and completes 16 transaction bytes on `bar`.
+MOK_DEV void clc_try_cancel(void *resp16, uint64_t *bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128"
+        " [%0], [%1];" ::"r"(smem_u32(resp16)),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+// Decode a response: true and the cancelled CTA's x index if a launch was cancelled, false
+// when no CTA was left to cancel.
+MOK_DEV bool clc_query(const void *resp16, uint32_t *ctaid_x) {
+    uint32_t ok, x = 0, y, z;
+    asm volatile(
+        "{\n.reg .pred p;\n.reg .b128 r;\nld.shared.b128 r, [%4];\n"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid.v4.b32.b128 {%1, %2, %3, _}, r;\n"
+        "}\n"
+        : "=r"(ok), "+r"(x), "=r"(y), "=r"(z)
+        : "r"(smem_u32(resp16))
+        : "memory");
+    *ctaid_x = x;
+    return ok != 0;
+}
+
 // ---------------------------------------------------------------- tcgen05
 // TMEM allocation by one full warp; the base address is written to shared memory.
 MOK_DEV void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {

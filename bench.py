@@ -166,6 +166,25 @@ def roofline_of(kind, c, launches_per_step, avg_ms, pk):
             "algorithmic_per_launch": nbytes}
 
 
+# ----------------------------------------------------------------------------- ranks
+
+def max_over_ranks(ms, dist=None, device="cpu"):
+    """The slowest rank's time: every rank runs the same number of steps on its own
+    batch, so the job is done when the last rank is."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([float(ms)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(world, flops_per_rank_step, ms_max):
+    """Whole-job TFLOP/s: the useful FLOPs of every rank's step over the slowest rank's
+    step time (weak scaling: each rank has its own tokens)."""
+    return world * flops_per_rank_step / (ms_max * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 def run_mok(args):
@@ -245,12 +264,7 @@ def run_mok(args):
             fn()
         b.record(stream)
         barrier()
-        ms = a.elapsed_time(b) / n
-        if dist is not None:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(a.elapsed_time(b) / n, dist, dev)
 
     for _ in range(args.warmup):
         step()
@@ -263,7 +277,7 @@ def run_mok(args):
         raise RuntimeError("device status %d/%d" % (st, dstat))
 
     flops_step = cfg.fwd_flops() + cfg.bwd_flops()
-    value = world * flops_step / (ms * 1e-3) / 1e12
+    value = whole_job_value(world, flops_step, ms)
 
     # per-kernel timing on the launching stream over a second timed region
     B.check(B.mok_profile_enable(1))
@@ -335,7 +349,7 @@ def run_mok(args):
                    "expert weights read per step)" % (3.0 * E * H * I * 2 / 1e9),
                    "parallelism": "replicas" if world > 1
                    else "single GPU"},
-        "e2e": {"value": world * flops_step / (ms_e * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": whole_job_value(world, flops_step, ms_e), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e},
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "roofline": roof,
@@ -437,7 +451,7 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
-def main():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
@@ -449,9 +463,14 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--ref-experts", type=int, default=1)
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "mok":
         args.warmup = 3
+    return args
+
+
+def main():
+    args = parse_args()
     if args.impl == "reference":
         run_reference(args)
     else:

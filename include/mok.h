@@ -65,7 +65,8 @@ typedef enum mok_precision {
 typedef enum mok_workspace_kind {
     MOK_WS_SCHEDULE = 0,
     MOK_WS_FORWARD = 1,
-    MOK_WS_BACKWARD = 2
+    MOK_WS_BACKWARD = 2,
+    MOK_WS_BACKWARD_RECOMPUTE = 3  /* backward without saved pre-activations */
 } mok_workspace_kind;
 
 /* Layer configuration. minibatch and ring_capacity are two of the pages' tunables
@@ -194,8 +195,13 @@ mok_status mok_forward(const mok_config *cfg, const void *x, const mok_schedule 
  * scatter with a fixed-order k-sum -> weight gradients ([arex] section "pull 代替 push":
  * pull reverse-combine, push reverse-dispatch, router-weight gradient fused into the
  * SwiGLU backward; [alphalab] section 一: expert gradient computation).
- *   x, topk_w, w13, w2 as in mok_forward (BF16), saved_preact [R][2I] fp32 from
- *   mok_forward, dy [T][H] bf16 upstream gradient.
+ *   x, topk_w, w13, w2 as in mok_forward (BF16), dy [T][H] bf16 upstream gradient.
+ *   saved_preact  [R][2I] fp32 from mok_forward, or NULL: the backward then recomputes
+ *            the gate/up GEMM from x and W13 ([alphalab] section 一, the backward's
+ *            recompute of forward activations), with the same tiles and accumulation order
+ *            as the forward, so the results are those of the saved-A path. The workspace
+ *            must then be of size mok_workspace_size(cfg, MOK_WS_BACKWARD_RECOMPUTE),
+ *            which adds an [R][2I] fp32 buffer for the recomputed pre-activations.
  *   dx       [T][H] fp32 out (sum over k in order of the fp32 per-slot dgrad results).
  *   dw13     [E][2I][H] fp32 out, dw2 [E][H][I] fp32 out (experts with no rows get 0).
  *   d_topk_w [T][K] fp32 out: dL/dtopk_w.

@@ -32,6 +32,7 @@ MOK_MXFP8 = 1
 MOK_WS_SCHEDULE = 0
 MOK_WS_FORWARD = 1
 MOK_WS_BACKWARD = 2
+MOK_WS_BACKWARD_RECOMPUTE = 3
 
 EXPORTED = [
     "mok_abi_version", "mok_status_string", "mok_check_config", "mok_segment_capacity",

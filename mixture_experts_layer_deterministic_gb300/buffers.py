@@ -74,11 +74,18 @@ class MoELayer:
 
     def backward(self, x, saved_preact, w13, w2, dy, dx, dw13, dw2, d_topk_w, d_logits=None,
                  topk_w=None, stream=None):
-        if self.ws_b is None:
-            self.ws_b, self.ws_b_n = workspace(self.cfg, B.MOK_WS_BACKWARD, self.device)
+        if saved_preact is None:  # recompute the pre-activations: larger workspace
+            if getattr(self, "ws_r", None) is None:
+                self.ws_r, self.ws_r_n = workspace(self.cfg, B.MOK_WS_BACKWARD_RECOMPUTE,
+                                                   self.device)
+            ws, ws_n = self.ws_r, self.ws_r_n
+        else:
+            if self.ws_b is None:
+                self.ws_b, self.ws_b_n = workspace(self.cfg, B.MOK_WS_BACKWARD, self.device)
+            ws, ws_n = self.ws_b, self.ws_b_n
         B.check(B.mok_backward(self.cfg, x, self.sched.struct, self.w if topk_w is None else
                                topk_w, saved_preact, w13, w2, dy, dx, dw13, dw2, d_topk_w,
-                               d_logits, self.ws_b, self.ws_b_n, stream), "backward")
+                               d_logits, ws, ws_n, stream), "backward")
         return dx
 
 

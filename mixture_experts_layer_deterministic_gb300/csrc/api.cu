@@ -114,9 +114,10 @@ struct BwdWs {
     uint16_t *dy_perm, *x_perm, *dA, *sh;
     float *dx_slots;
     float *dS_part;
+    float *preact;  // recomputed pre-activations [R][2I] (recompute workspace only)
 };
 
-size_t carve_bwd(const mok_config *c, void *ws, BwdWs *o) {
+size_t carve_bwd(const mok_config *c, void *ws, BwdWs *o, bool recompute = false) {
     Carver cv{(char *)ws};
     const int64_t R = rows_R(c);
     BwdWs w;
@@ -131,6 +132,7 @@ size_t carve_bwd(const mok_config *c, void *ws, BwdWs *o) {
     w.sh = cv.take<uint16_t>((size_t)w.rpad_cap * c->I * 2);
     w.dS_part = cv.take<float>((size_t)R * gemm_tc_dS_parts(c->I) * 4);
     w.dx_slots = cv.take<float>((size_t)R * c->H * 4);
+    w.preact = recompute ? cv.take<float>((size_t)R * 2 * c->I * 4) : nullptr;
     if (o) *o = w;
     return cv.off;
 }
@@ -215,6 +217,7 @@ size_t mok_workspace_size(const mok_config *c, int which) {
     switch (which) {
         case MOK_WS_SCHEDULE: return schedule_ws_bytes(rows_R(c), c->E);
         case MOK_WS_FORWARD: return carve_fwd(c, nullptr, nullptr);
+        case MOK_WS_BACKWARD_RECOMPUTE: return carve_bwd(c, nullptr, nullptr, true);
         case MOK_WS_BACKWARD: return carve_bwd(c, nullptr, nullptr);
     }
     return 0;
@@ -340,17 +343,17 @@ mok_status mok_backward(const mok_config *c, const void *x, const mok_schedule *
     if ((st = check_device(&status)) != MOK_OK) return st;
     if ((st = check_sched(c, sch)) != MOK_OK) return st;
     if (c->prec != MOK_BF16) return MOK_ERR_INVALID_ARG;
-    if (!x || !topk_w || !saved_preact || !w13 || !w2 || !dy || !dx || !dw13 || !dw2 ||
-        !d_topk_w)
+    if (!x || !topk_w || !w13 || !w2 || !dy || !dx || !dw13 || !dw2 || !d_topk_w)
         return MOK_ERR_INVALID_ARG;
+    const bool recompute = saved_preact == nullptr;
     const void *ps[] = {x, topk_w, saved_preact, w13, w2, dy, dx, dw13, dw2, d_topk_w, d_logits};
     for (const void *p : ps)
         if (p && !aligned16(p)) return MOK_ERR_INVALID_ARG;
-    const size_t need = carve_bwd(c, nullptr, nullptr);
+    const size_t need = carve_bwd(c, nullptr, nullptr, recompute);
     if ((st = check_ws(ws, ws_bytes, need)) != MOK_OK) return st;
     const int64_t R = rows_R(c);
     BwdWs w;
-    carve_bwd(c, ws, &w);
+    carve_bwd(c, ws, &w, recompute);
     const int E = c->E, H = c->H, I = c->I, K = c->K;
     MOK_LAUNCH(KK_PAD, 1, launch_pad_offsets(sch->counts, E, w.poff, stream));
     MOK_LAUNCH(KK_TILES, 1,
@@ -360,9 +363,14 @@ mok_status mok_backward(const mok_config *c, const void *x, const mok_schedule *
                launch_gather_bwd((const uint16_t *)dy, (const uint16_t *)x, sch->perm,
                                  sch->offsets, w.poff, E, K, H, w.rpad_cap, w.dy_perm, w.x_perm,
                                  stream));
+    if (recompute)
+        MOK_LAUNCH(KK_GEMM_UP, 1,
+                   launch_gemm_up_recompute_tc(w.tiles, w.tiles_cap, w.x_perm, w.rpad_cap, w13,
+                                               sch->offsets, w.poff, w.preact, H, I, E, status,
+                                               stream));
+    const float *pre = recompute ? w.preact : (const float *)saved_preact;
     GemmGArgs ga{w.tiles, w.tiles_cap, sch->offsets, w.poff, (const uint16_t *)w2, w.dy_perm,
-                 (const float *)saved_preact, sch->perm, topk_w, w.dA, w.sh, w.dS_part, H, I,
-                 status};
+                 pre, sch->perm, topk_w, w.dA, w.sh, w.dS_part, H, I, status};
     MOK_LAUNCH(KK_GEMM_G, 1, launch_gemm_g_tc(ga, E, w.rpad_cap, stream));
     MOK_LAUNCH(KK_ROUTER_GRAD, 1,
                launch_router_grad(w.dS_part, gemm_tc_dS_parts(I), sch->inv, sch->offsets,

@@ -171,6 +171,8 @@ struct FwdUpT {
     bool mxfp8;
     int *status;
     const uint8_t *sf_a, *sf_b;
+    // backward recompute: B rows in the padded expert layout, no h output (else nullptr)
+    const int32_t *offsets_b, *poff_b;
 
     MOK_DEV int64_t n_units() const { return tu.count(); }
     MOK_DEV Geom geom(int64_t u) const {
@@ -184,7 +186,7 @@ struct FwdUpT {
         g.ax1 = 0;
         g.ay1 = e;
         g.bx = 0;
-        g.by = (int32_t)rm(r0);
+        g.by = poff_b != nullptr ? (int32_t)(poff_b[e] + (r0 - offsets_b[e])) : (int32_t)rm(r0);
         g.n_mma = (int)((r1 - r0 + 15) & ~15);
         g.nbox = 1;
         g.k_steps = MX ? H / 32 : H / 16;
@@ -218,6 +220,7 @@ struct FwdUpT {
                     preact[r * 2 * I + i] = d0[j];
                     preact[r * 2 * I + I + i] = d1[j];
                 }
+                if (hring == nullptr) continue;
                 if (!mxfp8) {
                     if (live) ((uint16_t *)hring)[rm(r) * I + i] = f32_to_bf16(h);
                 } else {
@@ -909,8 +912,23 @@ cudaError_t launch_gemm_up_tc(const GemmUpArgs &a, int64_t ring_rows, cudaStream
     if ((e = make_map_w13_pairs(&ma, a.w13, a.E, a.I, a.H, false)) != cudaSuccess) return e;
     if ((e = make_map_bf16(&mb, a.xring, ring_rows, a.H, KBOX_ROWS)) != cudaSuccess) return e;
     FwdUpT<false> p{TileUnits{a.tiles, a.tiles_cap, a.I / 128}, a.H, a.I, a.ring, a.hring,
-                    a.hring_s, a.preact, false, a.status, nullptr, nullptr};
+                    a.hring_s, a.preact, false, a.status, nullptr, nullptr, nullptr, nullptr};
     return launch(ma, mb, p, a.tiles_cap * (a.I / 128), s);
+}
+
+cudaError_t launch_gemm_up_recompute_tc(const int32_t *tiles, int64_t tiles_cap,
+                                        const uint16_t *x_perm, int64_t rpad_cap,
+                                        const void *w13, const int32_t *offsets,
+                                        const int32_t *poff, float *preact, int H, int I,
+                                        int E, int *status, cudaStream_t s) {
+    cudaError_t e = init_host();
+    if (e != cudaSuccess) return e;
+    CUtensorMap ma, mb;  // A: W13 gate/up block pairs; B: x in the padded layout [rpad][H]
+    if ((e = make_map_w13_pairs(&ma, w13, E, I, H, false)) != cudaSuccess) return e;
+    if ((e = make_map_bf16(&mb, x_perm, rpad_cap, H, KBOX_ROWS)) != cudaSuccess) return e;
+    FwdUpT<false> p{TileUnits{tiles, tiles_cap, I / 128}, H, I, Ring{1, 1, 0}, nullptr,
+                    nullptr, preact, false, status, nullptr, nullptr, offsets, poff};
+    return launch(ma, mb, p, tiles_cap * (I / 128), s);
 }
 
 cudaError_t launch_gemm_down_tc(const GemmDownArgs &a, int64_t ring_rows, cudaStream_t s) {
@@ -933,7 +951,7 @@ cudaError_t launch_gemm_up_tc_mx(const GemmUpArgs &a, int64_t ring_rows, const u
     if ((e = make_map_w13_pairs(&ma, a.w13, a.E, a.I, a.H, true)) != cudaSuccess) return e;
     if ((e = make_map_u8(&mb, a.xring, ring_rows, a.H, KBOX_ROWS)) != cudaSuccess) return e;
     FwdUpT<true> p{TileUnits{a.tiles, a.tiles_cap, a.I / 128}, a.H, a.I, a.ring, a.hring,
-                   a.hring_s, nullptr, true, a.status, sf_w, sf_x};
+                   a.hring_s, nullptr, true, a.status, sf_w, sf_x, nullptr, nullptr};
     return launch(ma, mb, p, a.tiles_cap * (a.I / 128), s);
 }
 

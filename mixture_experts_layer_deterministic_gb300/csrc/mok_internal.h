@@ -116,6 +116,14 @@ struct GemmDownArgs {
 int gemm_tc_tile_rows(bool mxfp8);
 int gemm_tc_dS_parts(int I);
 cudaError_t launch_gemm_up_tc(const GemmUpArgs &a, int64_t ring_rows, cudaStream_t s);
+// The gate/up GEMM again, for a backward without saved pre-activations: B is the gathered
+// x in the padded expert layout (row poff[e] + r - offsets[e] holds sorted row r), and only
+// the fp32 pre-activations of each sorted row are written.
+cudaError_t launch_gemm_up_recompute_tc(const int32_t *tiles, int64_t tiles_cap,
+                                        const uint16_t *x_perm, int64_t rpad_cap,
+                                        const void *w13, const int32_t *offsets,
+                                        const int32_t *poff, float *preact, int H, int I,
+                                        int E, int *status, cudaStream_t s);
 cudaError_t launch_gemm_down_tc(const GemmDownArgs &a, int64_t ring_rows, cudaStream_t s);
 // MXFP8: E4M3 operands with scale atoms (see launch_scale_atoms_*): sf_w for the weights,
 // sf_x / sf_h for the token tiles

@@ -74,6 +74,12 @@ def test_workspace_sizes(lib):
     c = cfg()
     for which in (B.MOK_WS_SCHEDULE, B.MOK_WS_FORWARD, B.MOK_WS_BACKWARD):
         assert B.mok_workspace_size(c, which) > 0
+    # the recompute backward adds the [R][2I] fp32 pre-activations (plus alignment)
+    extra = (B.mok_workspace_size(c, B.MOK_WS_BACKWARD_RECOMPUTE) -
+             B.mok_workspace_size(c, B.MOK_WS_BACKWARD))
+    R, I = c.T * c.K, c.I
+    assert R * 2 * I * 4 <= extra < R * 2 * I * 4 + 256
+    assert B.mok_workspace_size(c, 99) == 0
     assert B.mok_workspace_size(cfg(K=9), B.MOK_WS_FORWARD) == 0
     # a smaller ring needs a smaller forward workspace
     big = B.mok_workspace_size(cfg(T=4096), B.MOK_WS_FORWARD)

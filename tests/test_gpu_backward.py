@@ -13,7 +13,7 @@ from workloads.synth import f32_to_bf16_bits
 pytestmark = pytest.mark.gpu
 
 
-def gpu_backward(dims, x, logits, w13, w2, dy, MB, reps=1):
+def gpu_backward(dims, x, logits, w13, w2, dy, MB, reps=1, recompute=False):
     import torch
     T, H, I, E, K = dims
     L = MoELayer(T, H, I, E, K, MB, 0, B.MOK_BF16, backward=True)
@@ -31,7 +31,7 @@ def gpu_backward(dims, x, logits, w13, w2, dy, MB, reps=1):
         dw2 = torch.empty(w2d.shape, dtype=torch.float32, device="cuda")
         dtk = torch.empty(max(R, 1), dtype=torch.float32, device="cuda")
         dlg = torch.empty(max(T, 1), E, dtype=torch.float32, device="cuda")
-        L.backward(xd, pre, w13d, w2d, dyd, dx, dw13, dw2, dtk, dlg)
+        L.backward(xd, None if recompute else pre, w13d, w2d, dyd, dx, dw13, dw2, dtk, dlg)
         outs.append((dx, dw13, dw2, dtk, dlg))
     torch.cuda.synchronize()
     st, dev = B.mok_read_device_status()
@@ -99,6 +99,20 @@ def test_ragged_and_empty_experts(dims, skew):
     check_all(res[0], idx, w, x, w13, w2, dy, dims[3])
 
 
+@pytest.mark.parametrize("dims,MB", [((256, 256, 128, 8, 2), 64),
+                                     ((600, 256, 256, 16, 4), 100),
+                                     ((333, 384, 128, 24, 3), 2368)])
+def test_recompute_matches_saved_preact(dims, MB):
+    """Without saved pre-activations the backward recomputes the gate/up GEMM with the
+    forward's tiles and K order, so every output equals the saved-A path bit for bit (the
+    forward here runs in several ring passes when MB < R)."""
+    x, lg, w13, w2, dy = small_case(*dims, seed=11)
+    a, _, _ = gpu_backward(dims, x, lg, w13, w2, dy, MB)
+    b, _, _ = gpu_backward(dims, x, lg, w13, w2, dy, MB, recompute=True)
+    for k in a[0]:
+        assert same_bits(a[0][k], b[0][k]), k
+
+
 def test_full_size_bwd():
     cfg = CONFIGS["bwd_bf16"]
     d = inputs(cfg)
@@ -108,6 +122,10 @@ def test_full_size_bwd():
     g = res[0]
     for k in g:
         assert same_bits(g[k], res[1][k]), k
+    rc, _, _ = gpu_backward(dims, d["x"], d["logits"], d["w13"], d["w2"], d["dy"],
+                            cfg.minibatch, recompute=True)
+    for k in g:
+        assert same_bits(g[k], rc[0][k]), ("recompute", k)
     # token-local outputs on sampled tokens
     toks = sample_tokens(cfg.T, 128, seed=cfg.seed)
     idx_s = idx[toks]

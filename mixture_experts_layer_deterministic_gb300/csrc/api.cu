@@ -298,10 +298,20 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
         MOK_LAUNCH(KK_TILES, 1,
                    launch_build_tiles(sch->offsets, c->E, p0, p1, chunk, w.tiles, cap, status,
                                       stream));
-        if (!mx)
+        // a ring that holds every row is filled token by token (each x row read once);
+        // a smaller ring pass by pass in sorted-row order
+        if (!mx && n_slots == 0)
+            MOK_LAUNCH(KK_GATHER, 1,
+                       launch_gather_tok_bf16((const uint16_t *)x, sch->inv, c->T, c->K, c->H,
+                                              (uint16_t *)w.xring, stream));
+        else if (!mx)
             MOK_LAUNCH(KK_GATHER, 1,
                        launch_gather_bf16((const uint16_t *)x, sch->perm, c->K, c->H, p0, p1, R,
                                           c->minibatch, n_slots, (uint16_t *)w.xring, stream));
+        else if (n_slots == 0)
+            MOK_LAUNCH(KK_GATHER, 1,
+                       launch_gather_tok_mxfp8((const uint16_t *)x, sch->inv, c->T, c->K, c->H,
+                                               (uint8_t *)w.xring, w.xring_s, stream));
         else
             MOK_LAUNCH(KK_GATHER, 1,
                        launch_gather_mxfp8((const uint16_t *)x, sch->perm, c->K, c->H, p0, p1,
@@ -360,9 +370,9 @@ mok_status mok_backward(const mok_config *c, const void *x, const mok_schedule *
                launch_build_tiles(sch->offsets, E, 0, R, gemm_tc_tile_rows(false), w.tiles,
                                   w.tiles_cap, status, stream));
     MOK_LAUNCH(KK_GATHER_BWD, 1,
-               launch_gather_bwd((const uint16_t *)dy, (const uint16_t *)x, sch->perm,
-                                 sch->offsets, w.poff, E, K, H, w.rpad_cap, w.dy_perm, w.x_perm,
-                                 stream));
+               launch_gather_bwd((const uint16_t *)dy, (const uint16_t *)x, sch->inv,
+                                 sch->counts, sch->offsets, w.poff, E, c->T, K, H, w.dy_perm,
+                                 w.x_perm, stream));
     if (recompute)
         MOK_LAUNCH(KK_GEMM_UP, 1,
                    launch_gemm_up_recompute_tc(w.tiles, w.tiles_cap, w.x_perm, w.rpad_cap, w13,

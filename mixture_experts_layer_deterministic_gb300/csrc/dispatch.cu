@@ -40,8 +40,60 @@ __global__ void __launch_bounds__(TPB)
     }
 }
 
+// Token-major form, when the ring holds every row (slot r = r): one warp per token t reads
+// x[t] once and writes it to the ring rows inv[t*K + k] of its K routed copies. Reading
+// each token row once keeps the gather at the bytes it must write, where the sorted-order
+// form re-reads every row K times from scattered positions.
+__global__ void __launch_bounds__(TPB)
+    gather_tok_bf16_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ inv,
+                           int64_t T, int K, int H, uint16_t *__restrict__ ring) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * (TPB / 32);
+    const int nv = H / 8;
+    for (int64_t t = (int64_t)blockIdx.x * (TPB / 32) + (threadIdx.x >> 5); t < T; t += nw) {
+        const int32_t rk = lane < K ? inv[t * K + lane] : 0;  // K <= 32
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + t * H);
+        for (int v0 = 0; v0 < nv; v0 += 32 * 16) {
+            uint4 b[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int v = v0 + j * 32 + lane;
+                if (v < nv) b[j] = ldg_nc_v4(src + v);
+            }
+            for (int k = 0; k < K; ++k) {
+                const int64_t r = __shfl_sync(0xFFFFFFFFu, rk, k);
+                uint4 *dst = reinterpret_cast<uint4 *>(ring + r * H);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int v = v0 + j * 32 + lane;
+                    if (v < nv) dst[v] = b[j];
+                }
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- MXFP8 quantizer
-// One 32-element bf16 block -> 32 E4M3 bytes + one E8M0 byte.
+// One 32-element bf16 block -> 32 E4M3 bytes (out[8]) and its E8M0 byte.
+MOK_DEV uint32_t quant_block32_regs(const uint16_t *__restrict__ src, uint32_t (&out)[8]) {
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = ldg_nc_v4(src + 8 * j);
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(v);
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+    const uint32_t sb = mx_scale_byte(amax);
+    const float inv = mx_inv_scale(sb);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t a = e4m3x2(bf16_lo(w[2 * j]) * inv, bf16_hi(w[2 * j]) * inv);
+        const uint32_t b = e4m3x2(bf16_lo(w[2 * j + 1]) * inv, bf16_hi(w[2 * j + 1]) * inv);
+        out[j] = a | (b << 16);
+    }
+    return sb;
+}
+
 MOK_DEV void quant_block32(const uint16_t *__restrict__ src, uint8_t *__restrict__ q,
                            uint8_t *__restrict__ sbyte) {
     uint4 v[4];
@@ -80,6 +132,30 @@ __global__ void __launch_bounds__(TPB)
         const int64_t t = perm[r] / K;
         const int64_t slot = rm(r);
         quant_block32(x + t * H + b * 32, rq + slot * H + b * 32, rs + slot * nb + b);
+    }
+}
+
+// Token-major form (ring holds every row): one thread per 32-element block of token t,
+// quantized once and written to the ring rows of its K routed copies.
+__global__ void __launch_bounds__(TPB)
+    gather_tok_mxfp8_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ inv,
+                            int64_t T, int K, int H, uint8_t *__restrict__ rq,
+                            uint8_t *__restrict__ rs) {
+    const int nb = H / 32;
+    const int64_t total = T * nb;
+    const int64_t stride = (int64_t)gridDim.x * TPB;
+    for (int64_t i = (int64_t)blockIdx.x * TPB + threadIdx.x; i < total; i += stride) {
+        const int64_t t = i / nb;
+        const int b = (int)(i % nb);
+        uint32_t out[8];
+        const uint32_t sb = quant_block32_regs(x + t * H + b * 32, out);
+        for (int k = 0; k < K; ++k) {
+            const int64_t r = __ldg(inv + t * K + k);
+            uint4 *qd = reinterpret_cast<uint4 *>(rq + r * H + b * 32);
+            qd[0] = make_uint4(out[0], out[1], out[2], out[3]);
+            qd[1] = make_uint4(out[4], out[5], out[6], out[7]);
+            rs[r * nb + b] = (uint8_t)sb;
+        }
     }
 }
 
@@ -124,45 +200,72 @@ __global__ void __launch_bounds__(TPB)
 
 // ---------------------------------------------------------------- backward gather
 // Padded row space: expert e owns rows [poff[e], poff[e+1]) with its counts[e] real rows
-// first and zero rows after. One warp per padded row p < rpad_cap:
-//   dy_perm[p] = dy[t], x_perm[p] = x[t] for t = perm[offsets[e] + p - poff[e]] / K.
+// first and zero rows after; sorted row r of expert e sits at poff[e] + r - offsets[e].
+// One warp per token t reads dy[t] and x[t] once and writes them to the padded rows of its
+// K routed copies (the row of copy k found from inv[t*K + k] by binary search over the
+// expert offsets: the last e with offsets[e] <= r, which skips empty experts).
 __global__ void __launch_bounds__(TPB)
     gather_bwd_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict__ x,
-                      const int32_t *__restrict__ perm, const int32_t *__restrict__ offsets,
-                      const int32_t *__restrict__ poff, int E, int K, int H, int64_t rpad_cap,
+                      const int32_t *__restrict__ inv, const int32_t *__restrict__ offsets,
+                      const int32_t *__restrict__ poff, int E, int64_t T, int K, int H,
                       uint16_t *__restrict__ dyp, uint16_t *__restrict__ xp) {
     const int lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * (TPB / 32);
     const int nv = H / 8;
-    const int64_t rpad = poff[E];
-    const int64_t pend = rpad < rpad_cap ? rpad : rpad_cap;
-    for (int64_t p = (int64_t)blockIdx.x * (TPB / 32) + (threadIdx.x >> 5); p < pend; p += nw) {
-        // expert of padded row p: last e with poff[e] <= p (binary search)
-        int lo = 0, hi = E - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (poff[mid] <= p) lo = mid; else hi = mid - 1;
+    for (int64_t t = (int64_t)blockIdx.x * (TPB / 32) + (threadIdx.x >> 5); t < T; t += nw) {
+        int64_t pk = 0;
+        if (lane < K) {
+            const int32_t r = inv[t * K + lane];
+            int lo = 0, hi = E - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (offsets[mid] <= r) lo = mid; else hi = mid - 1;
+            }
+            pk = poff[lo] + (int64_t)(r - offsets[lo]);
         }
-        const int e = lo;
-        const int64_t local = p - poff[e];
-        const int64_t n_e = offsets[e + 1] - offsets[e];
+        for (int which = 0; which < 2; ++which) {
+            const uint4 *src = reinterpret_cast<const uint4 *>((which ? x : dy) + t * H);
+            uint16_t *dbase = which ? xp : dyp;
+            for (int v0 = 0; v0 < nv; v0 += 32 * 16) {
+                uint4 b[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int v = v0 + j * 32 + lane;
+                    if (v < nv) b[j] = ldg_nc_v4(src + v);
+                }
+                for (int k = 0; k < K; ++k) {
+                    const int64_t p = __shfl_sync(0xFFFFFFFFu, pk, k);
+                    uint4 *dst = reinterpret_cast<uint4 *>(dbase + p * H);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int v = v0 + j * 32 + lane;
+                        if (v < nv) dst[v] = b[j];
+                    }
+                }
+            }
+        }
+    }
+}
+
+// The pad rows of every expert (at most 15) are zero in both padded arrays: one warp per
+// (expert, pad row).
+__global__ void __launch_bounds__(TPB)
+    zero_pad_rows_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__ poff,
+                         int E, int H, uint16_t *__restrict__ dyp, uint16_t *__restrict__ xp) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * (TPB / 32);
+    const int nv = H / 8;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int64_t w = (int64_t)blockIdx.x * (TPB / 32) + (threadIdx.x >> 5); w < (int64_t)E * 16;
+         w += nw) {
+        const int e = (int)(w / 16), j = (int)(w % 16);
+        const int64_t p = poff[e] + counts[e] + j;
+        if (p >= poff[e + 1]) continue;
         uint4 *d0 = reinterpret_cast<uint4 *>(dyp + p * H);
         uint4 *d1 = reinterpret_cast<uint4 *>(xp + p * H);
-        if (local < n_e) {
-            const int64_t t = perm[offsets[e] + local] / K;
-            const uint4 *s0 = reinterpret_cast<const uint4 *>(dy + t * H);
-            const uint4 *s1 = reinterpret_cast<const uint4 *>(x + t * H);
-#pragma unroll 4
-            for (int v = lane; v < nv; v += 32) {
-                d0[v] = ldg_nc_v4(s0 + v);
-                d1[v] = ldg_nc_v4(s1 + v);
-            }
-        } else {
-            const uint4 z = make_uint4(0, 0, 0, 0);
-            for (int v = lane; v < nv; v += 32) {
-                d0[v] = z;
-                d1[v] = z;
-            }
+        for (int v = lane; v < nv; v += 32) {
+            d0[v] = z;
+            d1[v] = z;
         }
     }
 }
@@ -259,6 +362,22 @@ cudaError_t launch_gather_bf16(const uint16_t *x, const int32_t *perm, int K, in
     return cudaGetLastError();
 }
 
+cudaError_t launch_gather_tok_bf16(const uint16_t *x, const int32_t *inv, int64_t T, int K,
+                                   int H, uint16_t *ring, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    gather_tok_bf16_kernel<<<grid_for(T, TPB / 32, 152 * 16), TPB, 0, s>>>(x, inv, T, K, H,
+                                                                           ring);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_tok_mxfp8(const uint16_t *x, const int32_t *inv, int64_t T, int K,
+                                    int H, uint8_t *ring_q, uint8_t *ring_s, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    gather_tok_mxfp8_kernel<<<grid_for(T * (H / 32), TPB, 152 * 16), TPB, 0, s>>>(
+        x, inv, T, K, H, ring_q, ring_s);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gather_mxfp8(const uint16_t *x, const int32_t *perm, int K, int H, int64_t p0,
                                 int64_t p1, int64_t R, int MB, int n_slots, uint8_t *ring_q,
                                 uint8_t *ring_s, cudaStream_t s) {
@@ -284,13 +403,16 @@ cudaError_t launch_combine(const float *slots, const float *w, int64_t T, int K,
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather_bwd(const uint16_t *dy, const uint16_t *x, const int32_t *perm,
-                              const int32_t *offsets, const int32_t *poff, int E, int K, int H,
-                              int64_t rpad_cap, uint16_t *dy_perm, uint16_t *x_perm,
-                              cudaStream_t s) {
-    if (rpad_cap == 0) return cudaSuccess;
-    gather_bwd_kernel<<<grid_for(rpad_cap, TPB / 32, 152 * 16), TPB, 0, s>>>(
-        dy, x, perm, offsets, poff, E, K, H, rpad_cap, dy_perm, x_perm);
+cudaError_t launch_gather_bwd(const uint16_t *dy, const uint16_t *x, const int32_t *inv,
+                              const int32_t *counts, const int32_t *offsets,
+                              const int32_t *poff, int E, int64_t T, int K, int H,
+                              uint16_t *dy_perm, uint16_t *x_perm, cudaStream_t s) {
+    if (E == 0) return cudaSuccess;
+    if (T > 0)
+        gather_bwd_kernel<<<grid_for(T, TPB / 32, 152 * 16), TPB, 0, s>>>(
+            dy, x, inv, offsets, poff, E, T, K, H, dy_perm, x_perm);
+    zero_pad_rows_kernel<<<grid_for((int64_t)E * 16, TPB / 32, 152 * 16), TPB, 0, s>>>(
+        counts, poff, E, H, dy_perm, x_perm);
     return cudaGetLastError();
 }
 

@@ -48,6 +48,11 @@ cudaError_t launch_build_tiles(const int32_t *offsets, int E, int64_t p0, int64_
 cudaError_t launch_gather_bf16(const uint16_t *x, const int32_t *perm, int K, int H, int64_t p0,
                                int64_t p1, int64_t R, int MB, int n_slots, uint16_t *ring,
                                cudaStream_t s);
+// token-major gathers, for a ring that holds every row: ring[inv[t*K + k]] = x[t]
+cudaError_t launch_gather_tok_bf16(const uint16_t *x, const int32_t *inv, int64_t T, int K,
+                                   int H, uint16_t *ring, cudaStream_t s);
+cudaError_t launch_gather_tok_mxfp8(const uint16_t *x, const int32_t *inv, int64_t T, int K,
+                                    int H, uint8_t *ring_q, uint8_t *ring_s, cudaStream_t s);
 cudaError_t launch_gather_mxfp8(const uint16_t *x, const int32_t *perm, int K, int H, int64_t p0,
                                 int64_t p1, int64_t R, int MB, int n_slots, uint8_t *ring_q,
                                 uint8_t *ring_s, cudaStream_t s);
@@ -59,10 +64,10 @@ cudaError_t launch_combine(const float *slots, const float *w, int64_t T, int K,
 
 // backward: padded row offsets (each expert's rows rounded up to 16) and gathers
 cudaError_t launch_pad_offsets(const int32_t *counts, int E, int32_t *poff, cudaStream_t s);
-cudaError_t launch_gather_bwd(const uint16_t *dy, const uint16_t *x, const int32_t *perm,
-                              const int32_t *offsets, const int32_t *poff, int E, int K, int H,
-                              int64_t rpad_cap, uint16_t *dy_perm, uint16_t *x_perm,
-                              cudaStream_t s);
+cudaError_t launch_gather_bwd(const uint16_t *dy, const uint16_t *x, const int32_t *inv,
+                              const int32_t *counts, const int32_t *offsets,
+                              const int32_t *poff, int E, int64_t T, int K, int H,
+                              uint16_t *dy_perm, uint16_t *x_perm, cudaStream_t s);
 cudaError_t launch_router_grad(const float *dS_part, int n_parts, const int32_t *inv,
                                const int32_t *offsets, const float *w, int64_t T, int K, int E,
                                float *d_topk, float *d_logits, cudaStream_t s);

@@ -105,14 +105,14 @@ MOK_DEV void clc_try_cancel(void *resp16, uint64_t *bar) {
 // Decode a response: true and the cancelled CTA's x index if a launch was cancelled, false
 // when no CTA was left to cancel.
 MOK_DEV bool clc_query(const void *resp16, uint32_t *ctaid_x) {
-    uint32_t ok, x = 0, y, z;
+    uint32_t ok, x = 0;
     asm volatile(
-        "{\n.reg .pred p;\n.reg .b128 r;\nld.shared.b128 r, [%4];\n"
+        "{\n.reg .pred p;\n.reg .b128 r;\nld.shared.b128 r, [%2];\n"
         "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n"
         "selp.u32 %0, 1, 0, p;\n"
-        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid.v4.b32.b128 {%1, %2, %3, _}, r;\n"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid.v4.b32.b128 {%1, _, _, _}, r;\n"
         "}\n"
-        : "=r"(ok), "+r"(x), "=r"(y), "=r"(z)
+        : "=r"(ok), "+r"(x)
         : "r"(smem_u32(resp16))
         : "memory");
     *ctaid_x = x;

@@ -313,6 +313,19 @@ def run_mok(args):
     ms_r = timed(bwd_rc, args.steps)
     phases["bwd_bf16_recompute"] = {"ms": ms_r,
                                     "tflops": cfg.bwd_flops() / (ms_r * 1e-3) / 1e12}
+
+    # the shared expert's forward (every token, weight one), added into y
+    from mixture_experts_layer_deterministic_gb300.buffers import SharedExpert
+    S = SharedExpert(L)
+    w13s = (torch.randn(2 * I, H, device=dev) * cfg.w_std).to(torch.bfloat16)
+    w2s = (torch.randn(H, I, device=dev) * cfg.w_std).to(torch.bfloat16)
+
+    def fwd_shared():
+        S.forward(x, w13s, w2s, y, stream=stream)
+    fwd_shared()
+    ms_s = timed(fwd_shared, args.steps)
+    phases["fwd_shared_bf16"] = {"ms": ms_s, "tflops": 6.0 * T * H * I / (ms_s * 1e-3) / 1e12}
+    del S, w13s, w2s
     if not args.no_mxfp8:
         q13, s13 = quantize_mxfp8(w13)
         q2, s2 = quantize_mxfp8(w2)

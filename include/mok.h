@@ -66,7 +66,8 @@ typedef enum mok_workspace_kind {
     MOK_WS_SCHEDULE = 0,
     MOK_WS_FORWARD = 1,
     MOK_WS_BACKWARD = 2,
-    MOK_WS_BACKWARD_RECOMPUTE = 3  /* backward without saved pre-activations */
+    MOK_WS_BACKWARD_RECOMPUTE = 3, /* backward without saved pre-activations */
+    MOK_WS_SHARED = 4              /* shared-expert forward */
 } mok_workspace_kind;
 
 /* Layer configuration. minibatch and ring_capacity are two of the pages' tunables
@@ -213,6 +214,23 @@ mok_status mok_backward(const mok_config *cfg, const void *x, const mok_schedule
                         const void *w2, const void *dy, void *dx, void *dw13, void *dw2,
                         float *d_topk_w, float *d_logits, void *ws, size_t ws_bytes,
                         cudaStream_t stream);
+
+/* Shared expert, forward ([alphalab] "Mixture-of-Kittens" (alphalab.site), section 一: the
+ * forward runs the FFN/SwiGLU of the shared and of the routed experts). Every token passes
+ * through one more SwiGLU expert, with weight one and no routing, and its output is added
+ * to y after the routed combine:
+ *   y[t] += W2s (silu(W13s[0:I] x_t) * W13s[I:2I] x_t)      (fp32 add, one writer per element)
+ * The shared expert has the routed experts' shape (H, I of cfg) and the mode's operand
+ * rounding (h to bf16 before the down GEMM).
+ *   x              [T][H] bf16, as for mok_forward.
+ *   w13_s          [2I][H] bf16 (gate rows, then up rows); w2_s [H][I] bf16.
+ *   y              [T][H] fp32, in and out (typically mok_forward's result).
+ *   saved_preact_s NULL, or [T][2I] fp32 out: the shared expert's gate/up GEMM result.
+ *   ws             at least mok_workspace_size(cfg, MOK_WS_SHARED) bytes.
+ * BF16 only (cfg->prec == MOK_BF16, else MOK_ERR_UNSUPPORTED). Asynchronous on `stream`. */
+mok_status mok_shared_expert_forward(const mok_config *cfg, const void *x, const void *w13_s,
+                                     const void *w2_s, void *y, void *saved_preact_s, void *ws,
+                                     size_t ws_bytes, cudaStream_t stream);
 
 /* MXFP8 quantization of a bf16 matrix along its rows ([arex] section "pull 代替 push":
  * pre-quantized weights). src [rows][cols] bf16 -> q [rows][cols] E4M3, scale

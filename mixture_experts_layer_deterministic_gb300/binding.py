@@ -33,13 +33,14 @@ MOK_WS_SCHEDULE = 0
 MOK_WS_FORWARD = 1
 MOK_WS_BACKWARD = 2
 MOK_WS_BACKWARD_RECOMPUTE = 3
+MOK_WS_SHARED = 4
 
 EXPORTED = [
     "mok_abi_version", "mok_status_string", "mok_check_config", "mok_segment_capacity",
     "mok_workspace_size", "mok_route_topk", "mok_build_schedule", "mok_forward",
     "mok_backward", "mok_quantize_mxfp8", "mok_read_device_status",
     "mok_clear_device_status", "mok_profile_enable", "mok_profile_read",
-    "mok_build_schedule_noalloc",
+    "mok_build_schedule_noalloc", "mok_shared_expert_forward",
 ]
 
 # bytes of the fixed scratch array behind mok_build_schedule_noalloc
@@ -92,6 +93,7 @@ def lib():
             "mok_forward": ([cfgp, p, schp, p, p, p, p, p, p, p, p, sz, p], ctypes.c_int),
             "mok_backward": ([cfgp, p, schp, p, p, p, p, p, p, p, p, p, p, p, sz, p],
                              ctypes.c_int),
+            "mok_shared_expert_forward": ([cfgp, p, p, p, p, p, p, sz, p], ctypes.c_int),
             "mok_quantize_mxfp8": ([p, i64, i32, p, p, p], ctypes.c_int),
             "mok_read_device_status": ([ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
             "mok_clear_device_status": ([], ctypes.c_int),
@@ -193,6 +195,13 @@ def mok_backward(cfg, x, sched, topk_w, saved_preact, w13, w2, dy, dx, dw13, dw2
                               _ptr(saved_preact), _ptr(w13), _ptr(w2), _ptr(dy), _ptr(dx),
                               _ptr(dw13), _ptr(dw2), _ptr(d_topk_w), _ptr(d_logits), _ptr(ws),
                               int(ws_bytes), _stream(stream))
+
+
+def mok_shared_expert_forward(cfg, x, w13_s, w2_s, y, saved_preact_s, ws, ws_bytes,
+                              stream=None) -> int:
+    return lib().mok_shared_expert_forward(ctypes.byref(cfg), _ptr(x), _ptr(w13_s), _ptr(w2_s),
+                                           _ptr(y), _ptr(saved_preact_s), _ptr(ws),
+                                           int(ws_bytes), _stream(stream))
 
 
 def mok_quantize_mxfp8(src, rows, cols, q, scale, stream=None) -> int:

@@ -89,6 +89,20 @@ class MoELayer:
         return dx
 
 
+class SharedExpert:
+    """The shared expert of a layer configuration (same H, I as the routed experts)."""
+
+    def __init__(self, layer):
+        self.cfg = layer.cfg
+        self.ws, self.ws_n = workspace(self.cfg, B.MOK_WS_SHARED, layer.device)
+
+    def forward(self, x, w13_s, w2_s, y, saved_preact=None, stream=None):
+        """y += the shared expert's output for every token (after the routed forward)."""
+        B.check(B.mok_shared_expert_forward(self.cfg, x, w13_s, w2_s, y, saved_preact,
+                                            self.ws, self.ws_n, stream), "shared forward")
+        return y
+
+
 def quantize_mxfp8(src, stream=None):
     """MXFP8 along the last axis of a bf16 tensor: (q uint8, scale uint8)."""
     cols = src.shape[-1]

@@ -137,6 +137,26 @@ size_t carve_bwd(const mok_config *c, void *ws, BwdWs *o, bool recompute = false
     return cv.off;
 }
 
+// shared-expert forward: the expert's offsets, its tile list and h [T][I] bf16
+struct SharedWs {
+    int32_t *offsets;
+    int32_t *tiles;
+    int64_t tiles_cap;
+    uint16_t *h;
+};
+
+size_t carve_shared(const mok_config *c, void *ws, SharedWs *o) {
+    Carver cv{(char *)ws};
+    SharedWs w;
+    w.offsets = cv.take<int32_t>(2 * 4);
+    w.tiles_cap = tile_list_cap(c->T, 1, gemm_tc_tile_rows(false));
+    int32_t *t = cv.take<int32_t>(16 + (size_t)w.tiles_cap * 16);
+    w.tiles = t ? t + 4 : nullptr;
+    w.h = cv.take<uint16_t>((size_t)c->T * c->I * 2);
+    if (o) *o = w;
+    return cv.off;
+}
+
 cudaError_t first_error(cudaError_t a, cudaError_t b) { return a != cudaSuccess ? a : b; }
 
 mok_status check_ws(void *ws, size_t ws_bytes, size_t need) {
@@ -218,6 +238,7 @@ size_t mok_workspace_size(const mok_config *c, int which) {
         case MOK_WS_SCHEDULE: return schedule_ws_bytes(rows_R(c), c->E);
         case MOK_WS_FORWARD: return carve_fwd(c, nullptr, nullptr);
         case MOK_WS_BACKWARD_RECOMPUTE: return carve_bwd(c, nullptr, nullptr, true);
+        case MOK_WS_SHARED: return carve_shared(c, nullptr, nullptr);
         case MOK_WS_BACKWARD: return carve_bwd(c, nullptr, nullptr);
     }
     return 0;
@@ -320,7 +341,7 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
         GemmUpArgs ua{w.tiles, cap, w.xring, w.xring_s, w13, w13_scale, w.hring,
                       w.hring_s, (float *)saved_preact, c->H, c->I, c->E, mx, ring, status};
         GemmDownArgs da{w.tiles, cap, w.hring, w.hring_s, w2, w2_scale, sch->perm,
-                        w.slots, c->H, c->I, c->E, mx, ring, status};
+                        w.slots, c->H, c->I, c->E, mx, ring, status, false};
         if (mx) {
             MOK_LAUNCH(KK_SCALE_ATOMS, 1,
                        launch_scale_atoms_tiles(w.tiles, cap, w.xring_s, R, c->minibatch, n_slots,
@@ -398,6 +419,38 @@ mok_status mok_backward(const mok_config *c, const void *x, const mok_schedule *
     MOK_LAUNCH(KK_WGRAD2, 1,
                launch_wgrad_tc(sch->counts, w.poff, w.sh, w.dy_perm, (float *)dw2, E, I, H,
                                w.rpad_cap, status, stream));
+    return MOK_OK;
+}
+
+mok_status mok_shared_expert_forward(const mok_config *c, const void *x, const void *w13_s,
+                                     const void *w2_s, void *y, void *saved_preact_s, void *ws,
+                                     size_t ws_bytes, cudaStream_t stream) {
+    mok_status st = mok_check_config(c);
+    if (st != MOK_OK) return st;
+    int *status;
+    if ((st = check_device(&status)) != MOK_OK) return st;
+    if (c->prec != MOK_BF16) return MOK_ERR_UNSUPPORTED;
+    if (!x || !w13_s || !w2_s || !y) return MOK_ERR_INVALID_ARG;
+    const void *ps[] = {x, w13_s, w2_s, y, saved_preact_s};
+    for (const void *p : ps)
+        if (p && !aligned16(p)) return MOK_ERR_INVALID_ARG;
+    const size_t need = carve_shared(c, nullptr, nullptr);
+    if ((st = check_ws(ws, ws_bytes, need)) != MOK_OK) return st;
+    if (c->T == 0) return MOK_OK;
+    SharedWs w;
+    carve_shared(c, ws, &w);
+    // one expert owning every token, in token order: x itself is the ring (slot t = t)
+    const Ring ring{c->T, c->minibatch, 0};
+    MOK_LAUNCH(KK_TILES, 2,
+               first_error(launch_single_expert_offsets(w.offsets, c->T, stream),
+                           launch_build_tiles(w.offsets, 1, 0, c->T, gemm_tc_tile_rows(false),
+                                              w.tiles, w.tiles_cap, status, stream)));
+    GemmUpArgs ua{w.tiles, w.tiles_cap, x, nullptr, w13_s, nullptr, w.h, nullptr,
+                  (float *)saved_preact_s, c->H, c->I, 1, false, ring, status};
+    MOK_LAUNCH(KK_SHARED_UP, 1, launch_gemm_up_tc(ua, c->T, stream));
+    GemmDownArgs da{w.tiles, w.tiles_cap, w.h, nullptr, w2_s, nullptr, nullptr, (float *)y,
+                    c->H, c->I, 1, false, ring, status, true};
+    MOK_LAUNCH(KK_SHARED_DOWN, 1, launch_gemm_down_tc(da, c->T, stream));
     return MOK_OK;
 }
 

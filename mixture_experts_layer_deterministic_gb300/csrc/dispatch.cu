@@ -362,6 +362,16 @@ cudaError_t launch_gather_bf16(const uint16_t *x, const int32_t *perm, int K, in
     return cudaGetLastError();
 }
 
+__global__ void single_expert_offsets_kernel(int32_t *off, int64_t rows) {
+    off[0] = 0;
+    off[1] = (int32_t)rows;
+}
+
+cudaError_t launch_single_expert_offsets(int32_t *off, int64_t rows, cudaStream_t s) {
+    single_expert_offsets_kernel<<<1, 1, 0, s>>>(off, rows);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gather_tok_bf16(const uint16_t *x, const int32_t *inv, int64_t T, int K,
                                    int H, uint16_t *ring, cudaStream_t s) {
     if (T == 0) return cudaSuccess;

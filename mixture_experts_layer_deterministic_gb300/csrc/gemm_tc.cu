@@ -250,10 +250,11 @@ struct FwdDownT {
     TileUnits tu;
     int H, I;
     Ring ring;
-    const int32_t *perm;
+    const int32_t *perm;  // output row of each sorted row (nullptr: the row itself)
     float *slots;
     int *status;
     const uint8_t *sf_a, *sf_b;
+    bool accumulate;      // add into the output (the shared expert adds into y)
 
     MOK_DEV int64_t n_units() const { return tu.count(); }
     MOK_DEV Geom geom(int64_t u) const {
@@ -289,7 +290,8 @@ struct FwdDownT {
         const int n_mma = (nr + 15) & ~15;
         const int c = mb * 256 + q * 32 + lane;
         int *fcol = reinterpret_cast<int *>(es.col);  // slot of each column
-        for (int n = lane; n < nr; n += 32) fcol[n] = perm[r0 + n];
+        for (int n = lane; n < nr; n += 32)
+            fcol[n] = perm != nullptr ? perm[r0 + n] : (int)(r0 + n);
         __syncwarp();
         for (int n0 = 16 * half; n0 < n_mma; n0 += 32) {
             float d0[16], d1[16];
@@ -298,9 +300,14 @@ struct FwdDownT {
             for (int j = 0; j < 16; ++j) {
                 const int n = n0 + j;
                 if (n < nr) {
-                    const int64_t f = fcol[n];
-                    slots[f * H + c] = d0[j];
-                    if (c + 128 < H) slots[f * H + c + 128] = d1[j];
+                    float *o = slots + (int64_t)fcol[n] * H + c;
+                    if (accumulate) {
+                        o[0] += d0[j];
+                        if (c + 128 < H) o[128] += d1[j];
+                    } else {
+                        o[0] = d0[j];
+                        if (c + 128 < H) o[128] = d1[j];
+                    }
                 }
             }
         }
@@ -939,7 +946,7 @@ cudaError_t launch_gemm_down_tc(const GemmDownArgs &a, int64_t ring_rows, cudaSt
     if ((e = make_map_bf16(&mb, a.hring, ring_rows, a.I, KBOX_ROWS)) != cudaSuccess) return e;
     const int nmb = (a.H + 255) / 256;
     FwdDownT<false> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.ring, a.perm, a.slots,
-                      a.status, nullptr, nullptr};
+                      a.status, nullptr, nullptr, a.accumulate};
     return launch(ma, mb, p, a.tiles_cap * nmb, s);
 }
 
@@ -964,7 +971,7 @@ cudaError_t launch_gemm_down_tc_mx(const GemmDownArgs &a, int64_t ring_rows, con
     if ((e = make_map_u8(&mb, a.hring, ring_rows, a.I, KBOX_ROWS)) != cudaSuccess) return e;
     const int nmb = (a.H + 255) / 256;
     FwdDownT<true> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.ring, a.perm, a.slots,
-                     a.status, sf_w, sf_h};
+                     a.status, sf_w, sf_h, a.accumulate};
     return launch(ma, mb, p, a.tiles_cap * nmb, s);
 }
 

@@ -12,7 +12,8 @@ namespace mok {
 enum KernelKind {
     KK_ROUTE = 0, KK_SCHEDULE, KK_TILES, KK_GATHER, KK_GEMM_UP, KK_GEMM_DOWN, KK_COMBINE,
     KK_QUANTIZE, KK_PAD, KK_GATHER_BWD, KK_GEMM_G, KK_ROUTER_GRAD, KK_GEMM_DGRAD,
-    KK_DX_REDUCE, KK_WGRAD13, KK_WGRAD2, KK_SCALE_ATOMS, KK_COUNT
+    KK_DX_REDUCE, KK_WGRAD13, KK_WGRAD2, KK_SCALE_ATOMS, KK_SHARED_UP, KK_SHARED_DOWN,
+    KK_COUNT
 };
 // while profiling is on: brackets the launches between begin and end with events
 void prof_begin(int kind, cudaStream_t s);
@@ -48,6 +49,8 @@ cudaError_t launch_build_tiles(const int32_t *offsets, int E, int64_t p0, int64_
 cudaError_t launch_gather_bf16(const uint16_t *x, const int32_t *perm, int K, int H, int64_t p0,
                                int64_t p1, int64_t R, int MB, int n_slots, uint16_t *ring,
                                cudaStream_t s);
+// offsets of a single expert owning rows [0, rows): off[0] = 0, off[1] = rows
+cudaError_t launch_single_expert_offsets(int32_t *off, int64_t rows, cudaStream_t s);
 // token-major gathers, for a ring that holds every row: ring[inv[t*K + k]] = x[t]
 cudaError_t launch_gather_tok_bf16(const uint16_t *x, const int32_t *inv, int64_t T, int K,
                                    int H, uint16_t *ring, cudaStream_t s);
@@ -109,12 +112,13 @@ struct GemmDownArgs {
     const uint8_t *hring_s;
     const void *w2;
     const uint8_t *w2_s;
-    const int32_t *perm;
+    const int32_t *perm;  // slot of each sorted row; nullptr: row r -> output row r
     float *slots;
     int H, I, E;
     bool mxfp8;
     Ring ring;
     int *status;
+    bool accumulate;      // add into the output rows instead of storing
 };
 // The GEMMs run on the tensor cores (gemm_tc.cu). Tiles are cut at gemm_tc_tile_rows()
 // rows; ring_rows / rpad_cap are the rows of the buffers the TMA maps cover.

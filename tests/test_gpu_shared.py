@@ -1,0 +1,133 @@
+"""GPU parity of the shared-expert forward against the oracle: every token also passes
+through one SwiGLU expert with weight one, added to the routed output. The oracle of the
+shared expert is its own layer forward with one expert and top-1 routing at weight one
+(the E=1, K=1 case, pinned on the CPU as a plain SwiGLU FFN)."""
+import numpy as np
+import pytest
+
+import oracle
+from harness import TOL_BF16, inputs, rel_err, sample_tokens, to_dev
+from mixture_experts_layer_deterministic_gb300 import binding as B
+from mixture_experts_layer_deterministic_gb300.buffers import MoELayer, SharedExpert
+from workloads import CONFIGS
+from workloads.synth import f32_to_bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def shared_weights(H, I, seed, scale):
+    r = np.random.default_rng(seed)
+    w13s = f32_to_bf16_bits((r.standard_normal((2 * I, H)) * scale).astype(np.float32))
+    w2s = f32_to_bf16_bits((r.standard_normal((H, I)) * scale).astype(np.float32))
+    return w13s, w2s
+
+
+def gpu_routed_plus_shared(dims, x, logits, w13, w2, w13s, w2s, MB=2368, reps=1):
+    import torch
+    T, H, I, E, K = dims
+    L = MoELayer(T, H, I, E, K, MB, 0, B.MOK_BF16)
+    S = SharedExpert(L)
+    xd, w13d, w2d, w13sd, w2sd = to_dev(x), to_dev(w13), to_dev(w2), to_dev(w13s), to_dev(w2s)
+    L.route(to_dev(logits))
+    L.schedule()
+    pre_s = torch.empty(max(T, 1), 2 * I, dtype=torch.float32, device="cuda")
+    outs = []
+    for _ in range(reps):
+        y = torch.empty(max(T, 1), H, dtype=torch.float32, device="cuda")
+        L.forward(xd, w13d, w2d, y)
+        y_routed = y[:T].clone()
+        S.forward(xd, w13sd, w2sd, y, saved_preact=pre_s)
+        outs.append((y_routed.cpu().numpy(), y[:T].cpu().numpy()))
+    torch.cuda.synchronize()
+    st, dev = B.mok_read_device_status()
+    assert st == B.MOK_OK and dev == B.MOK_OK
+    R = T * K
+    idx = L.idx[:R].view(T, K).cpu().numpy()
+    w = L.w[:R].view(T, K).cpu().numpy().astype(np.float64)
+    return outs, idx, w, pre_s[:T].cpu().numpy()
+
+
+def oracle_shared(x_bits, w13s, w2s):
+    T = x_bits.shape[0]
+    return oracle.forward(oracle.bf16_to_f64(x_bits), np.zeros((T, 1), np.int32),
+                          np.ones((T, 1)), w13s[None], w2s[None], mode=oracle.BF16,
+                          with_slack=True)
+
+
+def check(outs, idx, w, pre_s, x, w13, w2, w13s, w2s, toks=None):
+    y_routed, y_total = outs[0]
+    if toks is not None:
+        idx_s = idx[toks]
+        used = np.unique(idx_s)
+        remap = np.full(w13.shape[0], -1, np.int32)
+        remap[used] = np.arange(len(used), dtype=np.int32)
+        yr, sr = oracle.forward(oracle.bf16_to_f64(x[toks]), remap[idx_s], w[toks], w13[used],
+                                w2[used], mode=oracle.BF16, with_slack=True)
+        ys, ss = oracle_shared(x[toks], w13s, w2s)
+        y_routed, y_total, pre_s, xs = y_routed[toks], y_total[toks], pre_s[toks], x[toks]
+    else:
+        yr, sr = oracle.forward(oracle.bf16_to_f64(x), idx, w, w13, w2, mode=oracle.BF16,
+                                with_slack=True)
+        ys, ss = oracle_shared(x, w13s, w2s)
+        xs = x
+    # the routed part is untouched and the total is the routed plus the shared output
+    assert rel_err(y_routed, yr, sr) <= TOL_BF16
+    assert rel_err(y_total, yr + ys, sr + ss) <= TOL_BF16
+    # the shared output alone, as the GPU's fp32 difference
+    assert rel_err(y_total - y_routed, ys, ss) <= TOL_BF16
+    # saved pre-activations: fp32 dot products of the bf16 operands, whose products are
+    # exact in fp32; n-term fp32 summation stays within n * 2^-24 * sum|terms| of the exact
+    # sum (the recursive-summation bound), elementwise
+    xf, wf = oracle.bf16_to_f64(xs), oracle.bf16_to_f64(w13s)
+    a = xf @ wf.T
+    bound = xf.shape[1] * 2.0 ** -24 * (np.abs(xf) @ np.abs(wf).T)
+    assert np.all(np.abs(pre_s - a) <= bound)
+
+
+def test_tiny_config():
+    cfg = CONFIGS["tiny"]
+    d = inputs(cfg)
+    w13s, w2s = shared_weights(cfg.H, cfg.I, 5, 0.05)
+    dims = (cfg.T, cfg.H, cfg.I, cfg.E, cfg.K)
+    outs, idx, w, pre_s = gpu_routed_plus_shared(dims, d["x"], d["logits"], d["w13"], d["w2"],
+                                                 w13s, w2s, cfg.minibatch, reps=2)
+    check(outs, idx, w, pre_s, d["x"], d["w13"], d["w2"], w13s, w2s)
+    np.testing.assert_array_equal(outs[0][1], outs[1][1])  # bitwise run to run
+
+
+@pytest.mark.parametrize("dims", [(300, 256, 128, 8, 2), (1, 128, 128, 4, 1),
+                                  (517, 384, 256, 16, 4)])
+def test_ragged_token_counts(dims):
+    T, H, I, E, K = dims
+    r = np.random.default_rng(T)
+    x = f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
+    lg = r.standard_normal((T, E)).astype(np.float32)
+    w13 = f32_to_bf16_bits((r.standard_normal((E, 2 * I, H)) * 0.05).astype(np.float32))
+    w2 = f32_to_bf16_bits((r.standard_normal((E, H, I)) * 0.05).astype(np.float32))
+    w13s, w2s = shared_weights(H, I, T + 1, 0.05)
+    outs, idx, w, pre_s = gpu_routed_plus_shared(dims, x, lg, w13, w2, w13s, w2s, 100)
+    check(outs, idx, w, pre_s, x, w13, w2, w13s, w2s)
+
+
+def test_full_size_sampled_tokens():
+    cfg = CONFIGS["fwd_bf16"]
+    d = inputs(cfg)
+    w13s, w2s = shared_weights(cfg.H, cfg.I, 9, cfg.w_std)
+    dims = (cfg.T, cfg.H, cfg.I, cfg.E, cfg.K)
+    outs, idx, w, pre_s = gpu_routed_plus_shared(dims, d["x"], d["logits"], d["w13"], d["w2"],
+                                                 w13s, w2s, cfg.minibatch)
+    check(outs, idx, w, pre_s, d["x"], d["w13"], d["w2"], w13s, w2s,
+          toks=sample_tokens(cfg.T, 128, seed=3))
+
+
+def test_mxfp8_config_is_unsupported():
+    import torch
+    L = MoELayer(64, 128, 128, 4, 2, 64, 0, B.MOK_MXFP8)
+    ws = torch.empty(max(1, B.mok_workspace_size(L.cfg, B.MOK_WS_SHARED)), dtype=torch.uint8,
+                     device="cuda")
+    x = torch.zeros(64, 128, dtype=torch.bfloat16, device="cuda")
+    w13s = torch.zeros(256, 128, dtype=torch.bfloat16, device="cuda")
+    w2s = torch.zeros(128, 128, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(64, 128, dtype=torch.float32, device="cuda")
+    st = B.mok_shared_expert_forward(L.cfg, x, w13s, w2s, y, None, ws, ws.numel())
+    assert st == B.MOK_ERR_UNSUPPORTED

@@ -293,21 +293,34 @@ struct FwdDownT {
         for (int n = lane; n < nr; n += 32)
             fcol[n] = perm != nullptr ? perm[r0 + n] : (int)(r0 + n);
         __syncwarp();
+        const bool has1 = c + 128 < H;
         for (int n0 = 16 * half; n0 < n_mma; n0 += 32) {
             float d0[16], d1[16];
             ld(n0, d0, d1);
+            if (accumulate) {
+                // every load of the chunk before any store: a store to one row may alias
+                // the next row's load, which would otherwise serialise the round trips
+                float a0[16], a1[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const bool ok = n0 + j < nr;
+                    const float *o = slots + (int64_t)fcol[ok ? n0 + j : 0] * H + c;
+                    a0[j] = ok ? o[0] : 0.f;
+                    a1[j] = ok && has1 ? o[128] : 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    d0[j] += a0[j];
+                    d1[j] += a1[j];
+                }
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int n = n0 + j;
                 if (n < nr) {
                     float *o = slots + (int64_t)fcol[n] * H + c;
-                    if (accumulate) {
-                        o[0] += d0[j];
-                        if (c + 128 < H) o[128] += d1[j];
-                    } else {
-                        o[0] = d0[j];
-                        if (c + 128 < H) o[128] = d1[j];
-                    }
+                    o[0] = d0[j];
+                    if (has1) o[128] = d1[j];
                 }
             }
         }

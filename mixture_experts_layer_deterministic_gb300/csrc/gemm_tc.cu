@@ -557,7 +557,7 @@ struct Wgrad {
 template <class P>
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB, const P p) {
+                   const __grid_constant__ CUtensorMap tmB, const P p, const int use_clc) {
     constexpr bool MX = P::MX;
     constexpr int SB = stage_bytes<MX>();
     constexpr int BKE = MX ? BK_MX : BK;             // K elements per stage
@@ -566,6 +566,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     Smem *sm = (Smem *)(base + STAGES * SB);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t n_units = p.n_units();
+    const bool clc = P::CLC && use_clc != 0;  // else static striding, one CTA per SM
     if ((int64_t)blockIdx.x >= n_units) return;  // uniform across the CTA
 
     if (threadIdx.x == 0) {
@@ -625,7 +626,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int ask_at = kblocks > 2 ? kblocks - 2 : 0;
                 bool ok = true;
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    if (P::CLC && kb == ask_at && clc_live) {
+                    if (clc && kb == ask_at && clc_live) {
                         tc::mbar_arrive_expect_tx(&sm->clc_bar, 16);
                         tc::clc_try_cancel(&sm->clc_resp, &sm->clc_bar);
                         clc_pending = true;
@@ -671,7 +672,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 if (!ok) break;
                 int64_t next = -1;
-                if (!P::CLC) {
+                if (!clc) {
                     next = u + (int64_t)gridDim.x < n_units ? u + (int64_t)gridDim.x : -1;
                 } else if (clc_pending) {
                     if (!wait_or_abort(&sm->clc_bar, clc_ph, p.status, abort)) break;
@@ -901,9 +902,14 @@ cudaError_t make_map_w13_pairs(CUtensorMap *m, const void *ptr, int64_t E, int64
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// units_cap: the host-side bound on the units (the grid under Cluster Launch Control);
+// units_min: a lower bound on the units there will be. CTAs past the device-side count
+// return at once, but each still costs a launch; when the bound is loose (more than twice
+// the minimum, e.g. a ring pass that touches few experts) the launch strides statically
+// over one CTA per SM instead.
 template <class P>
 cudaError_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const P &p, int64_t units_cap,
-                   cudaStream_t s) {
+                   int64_t units_min, cudaStream_t s) {
     constexpr int SMEM = smem_bytes<P::MX>();
     static bool attr = false;
     if (!attr) {
@@ -916,8 +922,9 @@ cudaError_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const P &p, int
     // not yet launched; static striding: one CTA per SM
     if (units_cap < 1) return cudaSuccess;
     if (units_cap > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    const int grid = P::CLC || units_cap < g_num_sms ? (int)units_cap : g_num_sms;
-    tc_gemm_kernel<P><<<grid, NTHREADS, SMEM, s>>>(ma, mb, p);
+    const bool clc = P::CLC && units_cap <= 2 * units_min;
+    const int grid = clc || units_cap < g_num_sms ? (int)units_cap : g_num_sms;
+    tc_gemm_kernel<P><<<grid, NTHREADS, SMEM, s>>>(ma, mb, p, clc ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -933,7 +940,8 @@ cudaError_t launch_gemm_up_tc(const GemmUpArgs &a, int64_t ring_rows, cudaStream
     if ((e = make_map_bf16(&mb, a.xring, ring_rows, a.H, KBOX_ROWS)) != cudaSuccess) return e;
     FwdUpT<false> p{TileUnits{a.tiles, a.tiles_cap, a.I / 128}, a.H, a.I, a.ring, a.hring,
                     a.hring_s, a.preact, false, a.status, nullptr, nullptr, nullptr, nullptr};
-    return launch(ma, mb, p, a.tiles_cap * (a.I / 128), s);
+    return launch(ma, mb, p, a.tiles_cap * (a.I / 128),
+                  (ring_rows + TILE_ROWS - 1) / TILE_ROWS * (a.I / 128), s);
 }
 
 cudaError_t launch_gemm_up_recompute_tc(const int32_t *tiles, int64_t tiles_cap,
@@ -948,7 +956,9 @@ cudaError_t launch_gemm_up_recompute_tc(const int32_t *tiles, int64_t tiles_cap,
     if ((e = make_map_bf16(&mb, x_perm, rpad_cap, H, KBOX_ROWS)) != cudaSuccess) return e;
     FwdUpT<false> p{TileUnits{tiles, tiles_cap, I / 128}, H, I, Ring{1, 1, 0}, nullptr,
                     nullptr, preact, false, status, nullptr, nullptr, offsets, poff};
-    return launch(ma, mb, p, tiles_cap * (I / 128), s);
+    // the padded rows overestimate the real ones by at most 15 per expert
+    return launch(ma, mb, p, tiles_cap * (I / 128),
+                  (rpad_cap + TILE_ROWS - 1) / TILE_ROWS * (I / 128), s);
 }
 
 cudaError_t launch_gemm_down_tc(const GemmDownArgs &a, int64_t ring_rows, cudaStream_t s) {
@@ -960,7 +970,7 @@ cudaError_t launch_gemm_down_tc(const GemmDownArgs &a, int64_t ring_rows, cudaSt
     const int nmb = (a.H + 255) / 256;
     FwdDownT<false> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.ring, a.perm, a.slots,
                       a.status, nullptr, nullptr, a.accumulate};
-    return launch(ma, mb, p, a.tiles_cap * nmb, s);
+    return launch(ma, mb, p, a.tiles_cap * nmb, (ring_rows + TILE_ROWS - 1) / TILE_ROWS * nmb, s);
 }
 
 cudaError_t launch_gemm_up_tc_mx(const GemmUpArgs &a, int64_t ring_rows, const uint8_t *sf_w,
@@ -972,7 +982,8 @@ cudaError_t launch_gemm_up_tc_mx(const GemmUpArgs &a, int64_t ring_rows, const u
     if ((e = make_map_u8(&mb, a.xring, ring_rows, a.H, KBOX_ROWS)) != cudaSuccess) return e;
     FwdUpT<true> p{TileUnits{a.tiles, a.tiles_cap, a.I / 128}, a.H, a.I, a.ring, a.hring,
                    a.hring_s, nullptr, true, a.status, sf_w, sf_x, nullptr, nullptr};
-    return launch(ma, mb, p, a.tiles_cap * (a.I / 128), s);
+    return launch(ma, mb, p, a.tiles_cap * (a.I / 128),
+                  (ring_rows + TILE_ROWS_MX - 1) / TILE_ROWS_MX * (a.I / 128), s);
 }
 
 cudaError_t launch_gemm_down_tc_mx(const GemmDownArgs &a, int64_t ring_rows, const uint8_t *sf_w,
@@ -985,7 +996,8 @@ cudaError_t launch_gemm_down_tc_mx(const GemmDownArgs &a, int64_t ring_rows, con
     const int nmb = (a.H + 255) / 256;
     FwdDownT<true> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.ring, a.perm, a.slots,
                      a.status, sf_w, sf_h, a.accumulate};
-    return launch(ma, mb, p, a.tiles_cap * nmb, s);
+    return launch(ma, mb, p, a.tiles_cap * nmb,
+                  (ring_rows + TILE_ROWS_MX - 1) / TILE_ROWS_MX * nmb, s);
 }
 
 cudaError_t launch_gemm_g_tc(const GemmGArgs &a, int E, int64_t rpad_cap, cudaStream_t s) {
@@ -997,7 +1009,7 @@ cudaError_t launch_gemm_g_tc(const GemmGArgs &a, int E, int64_t rpad_cap, cudaSt
     const int nmb = (a.I + 255) / 256;
     BwdG p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff, a.perm, a.preact,
            a.topk_w, a.dA, a.sh, a.dS_part, 4 * nmb, a.status};
-    return launch(ma, mb, p, a.tiles_cap * nmb, s);
+    return launch(ma, mb, p, a.tiles_cap * nmb, a.tiles_cap * nmb, s);  // static striding
 }
 
 int gemm_tc_dS_parts(int I) { return 4 * ((I + 255) / 256); }
@@ -1012,7 +1024,7 @@ cudaError_t launch_gemm_dgrad_tc(const GemmDgradArgs &a, int E, int64_t rpad_cap
     const int nmb = (a.H + 255) / 256;
     BwdDgrad p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff, a.perm,
                a.dx_slots, a.status};
-    return launch(ma, mb, p, a.tiles_cap * nmb, s);
+    return launch(ma, mb, p, a.tiles_cap * nmb, (rpad_cap + TILE_ROWS - 1) / TILE_ROWS * nmb, s);
 }
 
 // out [E][N][M] = per expert sum over padded rows of A[p][m] B[p][n]
@@ -1026,7 +1038,7 @@ cudaError_t launch_wgrad_tc(const int32_t *counts, const int32_t *poff, const ui
     if ((e = make_map_bf16(&mb, Bm, rpad_cap, N, 64)) != cudaSuccess) return e;
     const int nmb = (M + 255) / 256, nnb = (N + TILE_ROWS - 1) / TILE_ROWS;
     Wgrad p{counts, poff, out, E, M, N, nmb, nnb, status};
-    return launch(ma, mb, p, (int64_t)E * nmb * nnb, s);
+    return launch(ma, mb, p, (int64_t)E * nmb * nnb, (int64_t)E * nmb * nnb, s);  // exact
 }
 
 }  // namespace mok

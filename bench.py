@@ -185,6 +185,60 @@ def whole_job_value(world, flops_per_rank_step, ms_max):
     return world * flops_per_rank_step / (ms_max * 1e-3) / 1e12
 
 
+def imbalanced_phases(args, torch, B, MoELayer, quantize_mxfp8, dev, w13, w2, barrier,
+                      with_mx=True):
+    out = {}
+    stream = torch.cuda.Stream(dev)  # a captured stream must not be the legacy default one
+
+    def timed(fn, n):
+        barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        barrier()
+        return a.elapsed_time(b) / n
+    for name in ("imbalanced_bf16",) + (("imbalanced_mxfp8",) if with_mx else ()):
+        c = CONFIGS[name]
+        mx = c.prec == "mxfp8"
+        Li = MoELayer(c.T, c.H, c.I, c.E, c.K, c.minibatch, c.ring_capacity,
+                      B.MOK_MXFP8 if mx else B.MOK_BF16, device=dev)
+        xi = torch.from_numpy(synth.make_x(c).view(np.int16)).to(dev).view(torch.bfloat16)
+        lgi = torch.from_numpy(synth.make_logits(c)).to(dev)
+        if mx:
+            (a13, s13), (a2, s2) = quantize_mxfp8(w13), quantize_mxfp8(w2)
+        else:
+            a13, s13, a2, s2 = w13, None, w2, None
+        yi = torch.empty(c.T, c.H, dtype=torch.float32, device=dev)
+
+        def fwd_i():
+            Li.route(lgi, stream)
+            Li.schedule(stream=stream)
+            Li.forward(xi, a13, a2, yi, s13, s2, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                fwd_i()
+        ms_e = timed(fwd_i, args.steps)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fwd_i()
+
+        def replay():
+            with torch.cuda.stream(stream):
+                g.replay()
+        replay()
+        ms_g = timed(replay, args.steps)
+        out["fwd_" + name] = {"ms": ms_e, "tflops": c.fwd_flops() / (ms_e * 1e-3) / 1e12,
+                              "ms_graph": ms_g,
+                              "tflops_graph": c.fwd_flops() / (ms_g * 1e-3) / 1e12,
+                              "tokens": c.T, "ring_rows": c.ring_capacity}
+        del g, Li, xi, lgi, yi, a13, a2, s13, s2
+        torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 def run_mok(args):
@@ -326,6 +380,12 @@ def run_mok(args):
     ms_s = timed(fwd_shared, args.steps)
     phases["fwd_shared_bf16"] = {"ms": ms_s, "tflops": 6.0 * T * H * I / (ms_s * 1e-3) / 1e12}
     del S, w13s, w2s
+
+    # the imbalanced workload's forward (Zipf-skewed routing, 65536 tokens, a ring of 2960
+    # rows, so many passes): eager, and replayed from a captured CUDA graph
+    if not args.no_imbalanced:
+        phases.update(imbalanced_phases(args, torch, B, MoELayer, quantize_mxfp8, dev, w13, w2,
+                                        barrier, with_mx=not args.no_mxfp8))
     if not args.no_mxfp8:
         q13, s13 = quantize_mxfp8(w13)
         q2, s2 = quantize_mxfp8(w2)
@@ -527,6 +587,7 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(CONFIGS))
     ap.add_argument("--no-mxfp8", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-imbalanced", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--ref-experts", type=int, default=1)

@@ -1,0 +1,63 @@
+"""The layer's calls are stream-ordered with no host synchronisation and no allocation,
+so a training step captures into a CUDA graph; its replay must reproduce the eager
+results bit for bit (single-pass and multi-pass rings)."""
+import numpy as np
+import pytest
+
+from harness import to_dev
+from mixture_experts_layer_deterministic_gb300 import binding as B
+from mixture_experts_layer_deterministic_gb300.buffers import MoELayer, SharedExpert
+from workloads.synth import f32_to_bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("dims,MB,ring", [((256, 256, 128, 8, 2), 64, 0),
+                                          ((600, 256, 256, 16, 4), 256, 512)])
+def test_captured_step_replays_eager_results(dims, MB, ring):
+    import torch
+    T, H, I, E, K = dims
+    r = np.random.default_rng(T)
+    x = to_dev(f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32)))
+    lg = to_dev(r.standard_normal((T, E)).astype(np.float32))
+    w13 = to_dev(f32_to_bf16_bits((r.standard_normal((E, 2 * I, H)) * 0.05).astype(np.float32)))
+    w2 = to_dev(f32_to_bf16_bits((r.standard_normal((E, H, I)) * 0.05).astype(np.float32)))
+    w13s = to_dev(f32_to_bf16_bits((r.standard_normal((2 * I, H)) * 0.05).astype(np.float32)))
+    w2s = to_dev(f32_to_bf16_bits((r.standard_normal((H, I)) * 0.05).astype(np.float32)))
+    dy = to_dev(f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32)))
+    L = MoELayer(T, H, I, E, K, MB, ring, B.MOK_BF16, backward=True)
+    S = SharedExpert(L)
+    R = T * K
+    f32 = dict(dtype=torch.float32, device="cuda")
+    pre = torch.empty(R, 2 * I, **f32)
+    y, dx = torch.empty(T, H, **f32), torch.empty(T, H, **f32)
+    dw13, dw2 = torch.empty(E, 2 * I, H, **f32), torch.empty(E, H, I, **f32)
+    dtk, dlg = torch.empty(R, **f32), torch.empty(T, E, **f32)
+    s = torch.cuda.Stream()
+
+    def step():
+        L.route(lg, s)
+        L.schedule(stream=s)
+        L.forward(x, w13, w2, y, saved_preact=pre, stream=s)
+        S.forward(x, w13s, w2s, y, stream=s)
+        L.backward(x, pre, w13, w2, dy, dx, dw13, dw2, dtk, dlg, stream=s)
+
+    outs = (y, dx, dw13, dw2, dtk, dlg, pre)
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in outs]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    for t in outs:
+        t.fill_(float("nan"))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        g.replay()
+        g.replay()
+    torch.cuda.synchronize()
+    st, dev = B.mok_read_device_status()
+    assert st == B.MOK_OK and dev == B.MOK_OK
+    for a, b in zip(outs, eager):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))

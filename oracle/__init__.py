@@ -45,8 +45,8 @@ def lib():
         L.oracle_mxfp8_dequantize.argtypes = [i64, i64, p, p, p]
         L.oracle_mxfp8_quantize_bf16.argtypes = [i64, i64, p, p, p]
         L.oracle_forward.argtypes = [i64, i32, i32, i32, i32, p, p, p, i32, p, p, p, p, i32, p, p]
-        L.oracle_backward.argtypes = [i64, i32, i32, i32, i32, p, p, p, i32, p, p, p, i32, p,
-                                      p, p, p, p, p, p]
+        L.oracle_backward.argtypes = [i64, i32, i32, i32, i32, p, p, p, i32, p, p, p, p, i32,
+                                      p, p, p, p, p, p, p, p, p]
         L.oracle_bf16_slack.argtypes = [ctypes.c_double, ctypes.c_double]
         L.oracle_bf16_slack.restype = ctypes.c_double
         L.oracle_round_bf16.argtypes = [ctypes.c_double]
@@ -185,13 +185,25 @@ def forward(x, idx, w, w13, w2, mode=EXACT, with_slack=False):
 
 def backward(x, idx, w, w13, w2, dy, weight_grads=True, mode=EXACT, with_slack=False):
     """Layer backward in fp64: (dx, dw13, dw2, dtopk), with the operand rounding of `mode`
-    (EXACT or BF16); dw13/dw2 are None when weight_grads is False. With with_slack, also
-    the slacks of dx, dw13, dw2 (see forward)."""
+    (EXACT, BF16 or MXFP8); dw13/dw2 are None when weight_grads is False. With with_slack,
+    also the slacks of dx, dw13, dw2 (see forward).
+
+    In MXFP8 mode w13 and w2 are the bf16 weights (uint16 bit patterns). A is recomputed
+    with the forward's operands (x and W13 quantized along H); G uses dy and W2 quantized
+    along H; dgrad uses dA and W13 quantized along 2I; the weight gradients use bf16 dA
+    and w*h."""
     x, w, dy = _f64(x), _f64(w), _f64(dy)
     idx = _i32(idx)
-    k13, d13, _, sh13 = _weights(w13)
+    w13d = w2g = None
+    s13 = None
+    if mode == MXFP8:
+        assert w13.dtype == np.uint16 and w2.dtype == np.uint16
+        w13d = mxfp8_qdq_axis_bf16(w13, axis=1)   # W13 [E][2I][H] along 2I
+        w2g = mxfp8_qdq_axis_bf16(w2, axis=1)     # W2 [E][H][I] along H
+        w13 = mxfp8_quantize_bf16(w13)            # the forward's W13, along H
+    k13, d13, s13, sh13 = _weights(w13)
     k2, d2, _, sh2 = _weights(w2)
-    assert k13 == k2 and k13 != W_MXFP8
+    assert k2 != W_MXFP8 and (k13 != W_MXFP8 or mode == MXFP8)
     T, H = x.shape
     E, I2, _ = sh13
     K = idx.shape[1]
@@ -203,9 +215,9 @@ def backward(x, idx, w, w13, w2, dy, weight_grads=True, mode=EXACT, with_slack=F
     sdw13 = np.empty(sh13, np.float64) if (with_slack and weight_grads) else None
     sdw2 = np.empty(sh2, np.float64) if (with_slack and weight_grads) else None
     n = lambda a: None if a is None else _p(a)  # noqa: E731
-    lib().oracle_backward(T, H, I2 // 2, E, K, _p(x), _p(idx), _p(w), k13, _p(d13), _p(d2),
-                          _p(dy), int(mode), _p(dx), n(dw13), n(dw2), _p(dtopk), n(sdx),
-                          n(sdw13), n(sdw2))
+    lib().oracle_backward(T, H, I2 // 2, E, K, _p(x), _p(idx), _p(w), k13, _p(d13), n(s13),
+                          _p(d2), _p(dy), int(mode), n(w13d), n(w2g), _p(dx), n(dw13),
+                          n(dw2), _p(dtopk), n(sdx), n(sdw13), n(sdw2))
     if with_slack:
         if sdx is not None and mode == EXACT:
             sdx[:] = 0.0
@@ -214,6 +226,14 @@ def backward(x, idx, w, w13, w2, dy, weight_grads=True, mode=EXACT, with_slack=F
                 sdw2[:] = 0.0
         return dx, dw13, dw2, dtopk, sdx, sdw13, sdw2
     return dx, dw13, dw2, dtopk
+
+
+def mxfp8_qdq_axis_bf16(bits, axis):
+    """MXFP8 quantize-dequantize of bf16 bit patterns in 32-element blocks along `axis`
+    (the oracle's row quantizer applied to that axis moved last): float64, same shape."""
+    b = np.moveaxis(np.asarray(bits, np.uint16), axis, -1)
+    q, sc = mxfp8_quantize_bf16(np.ascontiguousarray(b))
+    return np.ascontiguousarray(np.moveaxis(mxfp8_dequantize(q, sc), -1, axis))
 
 
 def mxfp8_quantize_bf16(bits):

@@ -423,11 +423,13 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
 
 void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
                      const int32_t *idx, const double *w, int32_t wkind, const void *w13,
-                     const void *w2, const double *dy, int32_t mode, double *dx, double *dw13,
+                     const uint8_t *w13_s, const void *w2, const double *dy, int32_t mode,
+                     const double *w13d, const double *w2g, double *dx, double *dw13,
                      double *dw2, double *dtopk, double *sdx, double *sdw13, double *sdw2)
 {
     const int64_t R = T * K;
-    const int want_slack = (sdx != NULL) && mode == ORACLE_BF16;
+    const int mx = mode == ORACLE_MXFP8;
+    const int want_slack = (sdx != NULL) && mode != ORACLE_EXACT;
     /* per routed row: da = dL/da [2I] and sh = w * h [I], kept for the weight gradients,
      * and the slack of their bf16 decisions */
     double *da_all = (double *)malloc(sizeof(double) * (size_t)(R * 2 * I));
@@ -446,6 +448,20 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
         double *g = (double *)malloc(sizeof(double) * (size_t)I);
         double *aa = (double *)malloc(sizeof(double) * 2 * (size_t)I); /* sum |W13||x| */
         double *gg = (double *)malloc(sizeof(double) * (size_t)I);     /* sum |W2||dy| */
+        /* MXFP8: the forward's quantized x (operand of the recomputed A), dy quantized along
+         * H (operand of G), and dA quantized along 2I with its slack (operand of dgrad) */
+        double *xq = mx ? (double *)malloc(sizeof(double) * (size_t)H) : NULL;
+        double *dyq = mx ? (double *)malloc(sizeof(double) * (size_t)H) : NULL;
+        double *daq = mx ? (double *)malloc(sizeof(double) * 2 * (size_t)I) : NULL;
+        double *dae = mx ? (double *)malloc(sizeof(double) * 2 * (size_t)I) : NULL;
+        double *daqs = mx ? (double *)malloc(sizeof(double) * 2 * (size_t)I) : NULL;
+        if (mx) {
+            memcpy(xq, xt, sizeof(double) * (size_t)H);
+            qdq_row(H, xq);
+            memcpy(dyq, dyt, sizeof(double) * (size_t)H);
+            qdq_row(H, dyq);
+        }
+        const double *xa = mx ? xq : xt, *dyg = mx ? dyq : dyt;
         for (int32_t c = 0; c < H; ++c)
             dxt[c] = 0.0;
         for (int32_t k = 0; k < K; ++k) {
@@ -458,9 +474,9 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
             for (int32_t j = 0; j < 2 * I; ++j) {
                 double acc = 0.0, mag = 0.0;
                 for (int32_t c = 0; c < H; ++c) {
-                    const double wv = wget(wkind, w13, NULL, H, b13 + (int64_t)j * H + c);
-                    acc += wv * xt[c];
-                    mag += fabs(wv * xt[c]);
+                    const double wv = wget(wkind, w13, w13_s, H, b13 + (int64_t)j * H + c);
+                    acc += wv * xa[c];
+                    mag += fabs(wv * xa[c]);
                 }
                 a[j] = acc;
                 aa[j] = mag;
@@ -469,9 +485,10 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
             for (int32_t i = 0; i < I; ++i) {
                 double acc = 0.0, mag = 0.0;
                 for (int32_t c = 0; c < H; ++c) {
-                    const double wv = wget(wkind, w2, NULL, I, b2 + (int64_t)c * I + i);
-                    acc += wv * dyt[c];
-                    mag += fabs(wv * dyt[c]);
+                    const double wv = mx ? w2g[b2 + (int64_t)c * I + i]
+                                         : wget(wkind, w2, NULL, I, b2 + (int64_t)c * I + i);
+                    acc += wv * dyg[c];
+                    mag += fabs(wv * dyg[c]);
                 }
                 g[i] = acc;
                 gg[i] = mag;
@@ -489,8 +506,8 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
                 da[I + i] = dh * sl;
                 sh[i] = s * hi;
             }
-            if (mode == ORACLE_BF16) {
-                if (want_slack)
+            if (mode != ORACLE_EXACT) {
+                if (want_slack || mx)
                     for (int32_t i = 0; i < I; ++i) {
                         /* how far a kernel's fp32 values can be from these: first-order
                          * propagation of the dot products' error bounds */
@@ -503,37 +520,57 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
                                                          fabs(gi * au * d2) * eag);
                         const double e_dau = fabs(s) * (fabs(sl) * eg + fabs(gi * d1) * eag);
                         const double e_sh = fabs(s) * (fabs(d1 * au) * eag + fabs(sl) * eau);
-                        das_all[f * 2 * I + i] = oracle_bf16_slack(da[i], e_dag);
-                        das_all[f * 2 * I + I + i] = oracle_bf16_slack(da[I + i], e_dau);
-                        shs_all[f * I + i] = oracle_bf16_slack(sh[i], e_sh);
+                        if (mx) {
+                            dae[i] = e_dag;
+                            dae[I + i] = e_dau;
+                        }
+                        if (want_slack) {
+                            das_all[f * 2 * I + i] = oracle_bf16_slack(da[i], e_dag);
+                            das_all[f * 2 * I + I + i] = oracle_bf16_slack(da[I + i], e_dau);
+                            shs_all[f * I + i] = oracle_bf16_slack(sh[i], e_sh);
+                        }
                     }
+                if (mx) { /* dgrad operand: dA quantized in 32-blocks along 2I */
+                    memcpy(daq, da, sizeof(double) * 2 * (size_t)I);
+                    qdq_row_slack(2 * (int64_t)I, daq, dae, daqs);
+                }
                 for (int32_t j = 0; j < 2 * I; ++j)
                     da[j] = oracle_round_bf16(da[j]);
                 for (int32_t i = 0; i < I; ++i)
                     sh[i] = oracle_round_bf16(sh[i]);
             }
             dtopk[f] = dS;
-            /* dx += W13^T da */
+            /* dx += W13^T da (MXFP8: W13 quantized along 2I times dA quantized along 2I) */
+            const double *dad = mx ? daq : da;
             for (int32_t c = 0; c < H; ++c) {
                 double acc = 0.0;
-                for (int32_t j = 0; j < 2 * I; ++j)
-                    acc += wget(wkind, w13, NULL, H, b13 + (int64_t)j * H + c) * da[j];
+                for (int32_t j = 0; j < 2 * I; ++j) {
+                    const int64_t o = b13 + (int64_t)j * H + c;
+                    acc += (mx ? w13d[o] : wget(wkind, w13, w13_s, H, o)) * dad[j];
+                }
                 dxt[c] += acc;
             }
             if (want_slack)
                 for (int32_t j = 0; j < 2 * I; ++j) {
-                    const double sj = das_all[f * 2 * I + j];
+                    const double sj = mx ? daqs[j] : das_all[f * 2 * I + j];
                     if (sj == 0.0)
                         continue;
-                    for (int32_t c = 0; c < H; ++c)
+                    for (int32_t c = 0; c < H; ++c) {
+                        const int64_t o = b13 + (int64_t)j * H + c;
                         sdx[t * (int64_t)H + c] +=
-                            fabs(wget(wkind, w13, NULL, H, b13 + (int64_t)j * H + c)) * sj;
+                            fabs(mx ? w13d[o] : wget(wkind, w13, w13_s, H, o)) * sj;
+                    }
                 }
         }
         free(a);
         free(g);
         free(aa);
         free(gg);
+        free(xq);
+        free(dyq);
+        free(daq);
+        free(dae);
+        free(daqs);
     }
 
     if (dw13 == NULL || dw2 == NULL) {

@@ -103,15 +103,22 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
  *   dx_t = sum_k W13[e]^T da, dW13[e] = sum da x^T, dW2[e] = sum dy (w h)^T
  * ([arex] section "pull 代替 push": router-weight gradient computed with the SwiGLU
  * backward; [alphalab] section 一: expert gradient computation). Sums over routed rows run
- * in ascending flat id. mode is ORACLE_EXACT or ORACLE_BF16 (dA and w*h rounded to bf16
- * where they enter the dgrad and weight-gradient GEMMs). Weights are ORACLE_W_F64 or
- * ORACLE_W_BF16. Outputs: dx [T][H], dw13 [E][2I][H], dw2 [E][H][I], dtopk [T][K] (= dS);
- * dw13/dw2 may be NULL (skipped). */
+ * in ascending flat id. mode is ORACLE_EXACT, ORACLE_BF16 (dA and w*h rounded to bf16
+ * where they enter the dgrad and weight-gradient GEMMs) or ORACLE_MXFP8 ([arex] section
+ * "pull 代替 push": MXFP8 activations and pre-quantized weights): A is recomputed from the
+ * forward's quantized operands (x quantized along H, W13 given as ORACLE_W_MXFP8 with
+ * w13_s), G = W2g^T Q(dy) with dy quantized along H and W2g = W2 quantized along H
+ * (w2g [E][H][I], dequantized), dx = W13d^T Q(dA) with dA quantized in 32-blocks along 2I
+ * and W13d = W13 quantized along 2I (w13d [E][2I][H], dequantized); the weight gradients
+ * take dA and w*h rounded to bf16 as in ORACLE_BF16. Weights are ORACLE_W_F64 or
+ * ORACLE_W_BF16 (ORACLE_W_MXFP8 for w13 in MXFP8 mode; w13d, w2g are NULL otherwise).
+ * Outputs: dx [T][H], dw13 [E][2I][H], dw2 [E][H][I], dtopk [T][K] (= dS); dw13/dw2 may be
+ * NULL (skipped). */
 void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
                      const int32_t *idx, const double *w, int32_t wkind, const void *w13,
-                     const void *w2, const double *dy, int32_t mode, double *dx, double *dw13,
-                     double *dw2, double *dtopk, double *sdx /* nullable slacks */,
-                     double *sdw13, double *sdw2);
+                     const uint8_t *w13_s, const void *w2, const double *dy, int32_t mode,
+                     const double *w13d, const double *w2g, double *dx, double *dw13,
+                     double *dw2, double *dtopk, double *sdx, double *sdw13, double *sdw2);
 
 /* Router-logit gradient through the top-k softmax: for a chosen expert j = idx[t,k],
  * dlogits[t,j] = w_k (dS_k - sum_m w_m dS_m); every other logit gets 0. */

@@ -479,3 +479,79 @@ def test_backward_slack_zero_in_exact_mode_and_bounds_flipped_operands():
     assert all(np.all(s == 0) for s in out0[4:])
     out = oracle.backward(x, idx, w, w13, w2, dy, mode=oracle.BF16, with_slack=True)
     assert all(np.all(s >= 0) for s in out[4:])
+
+
+# ---------------------------------------------------------------- MXFP8 backward
+from workloads.synth import f32_to_bf16_bits  # noqa: E402  (seeded input helper only)
+# [arex] "Cursor 放出 MoK", section "pull 代替 push": MXFP8 with pre-quantized weights and
+# activations quantized where they enter a GEMM. The backward's G GEMM contracts over H
+# (dy and W2 quantized along H), dgrad over 2I (dA and W13 quantized along 2I).
+
+def test_mxfp8_axis_quantization_is_per_column_quantization():
+    r = np.random.default_rng(41)
+    w = f32_to_bf16_bits((r.standard_normal((2, 64, 96)) * 0.1).astype(np.float32))
+    got = oracle.mxfp8_qdq_axis_bf16(w, axis=1)
+    for e in range(2):
+        for col in range(96):
+            q, s = oracle.mxfp8_quantize_bf16(w[e, :, col][None, :].copy())
+            np.testing.assert_array_equal(got[e, :, col], oracle.mxfp8_dequantize(q, s)[0])
+
+
+def _exact_case():
+    """Every MXFP8 quantization in the backward is exact and so is every bf16 rounding.
+    K = 1 (weight 1); x[t] and dy[t] are one-hot (+-1 at column c_t, d_t); the weights
+    take values in {0, +-1, +-2}, with W13's gate rows zero in the columns c_t, so
+    a_g = 0 (silu(0) = 0, silu'(0) = 1/2), a_u and G = W2^T dy are single weight entries,
+    and dA_g = G a_u / 2 lies in {0, +-1/2, +-1, +-2}, while dx = W13_g^T dA_g is not
+    zero."""
+    T, H, I, E = 3, 64, 32, 2
+    r = np.random.default_rng(43)
+    pick = lambda *s: r.choice([-2.0, -1.0, 0.0, 1.0, 2.0], size=s).astype(np.float64)  # noqa
+    c = np.array([5, 17, 40]); d = np.array([3, 33, 60])
+    sign = np.array([1.0, -1.0, 1.0])
+    x = np.zeros((T, H)); x[np.arange(T), c] = sign
+    dy = np.zeros((T, H)); dy[np.arange(T), d] = -sign
+    w13 = np.concatenate([pick(E, I, H), pick(E, I, H)], axis=1)
+    w13[:, :I, c] = 0.0  # a_g = 0 for every token
+    w2 = pick(E, H, I)
+    idx = np.array([[0], [1], [1]], np.int32)
+    w = np.ones((T, 1))
+    b = lambda a: f32_to_bf16_bits(a.astype(np.float32))  # noqa: E731
+    return b(x), idx, w, b(w13), b(w2), b(dy)
+
+
+def test_mxfp8_backward_equals_exact_when_every_quantization_is_exact():
+    x, idx, w, w13, w2, dy = _exact_case()
+    xf, dyf = oracle.bf16_to_f64(x), oracle.bf16_to_f64(dy)
+    ref = oracle.backward(xf, idx, w, w13, w2, dyf, mode=oracle.EXACT)
+    assert np.abs(ref[0]).max() > 0 and np.abs(ref[1]).max() > 0  # dx, dW13 not trivial
+    for mode in (oracle.BF16, oracle.MXFP8):
+        got = oracle.backward(xf, idx, w, w13, w2, dyf, mode=mode)
+        for a, b in zip(got, ref):
+            np.testing.assert_array_equal(a, b)
+
+
+def test_mxfp8_backward_g_uses_the_quantized_operands():
+    """dS = <G, h> with G = W2q^T Q(dy) and h from A = W13q Q(x): equal to the BF16-mode
+    backward run on those operands already quantized (W13 along H, W2 along H, x and dy
+    along H), where nothing else touches dS."""
+    r = np.random.default_rng(47)
+    T, H, I, E, K = 5, 64, 32, 3, 2
+    x = f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
+    dy = f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
+    w13 = f32_to_bf16_bits((r.standard_normal((E, 2 * I, H)) * 0.2).astype(np.float32))
+    w2 = f32_to_bf16_bits((r.standard_normal((E, H, I)) * 0.2).astype(np.float32))
+    idx, w = oracle.route(r.standard_normal((T, E)).astype(np.float32), K)
+    _, _, _, dtk = oracle.backward(oracle.bf16_to_f64(x), idx, w, w13, w2,
+                                   oracle.bf16_to_f64(dy), mode=oracle.MXFP8)
+    # references built without the along-axis helper: the row quantizer on rows that run
+    # along H (x, dy, W13 rows), and on an explicit transpose for W2 (its H axis is not last)
+    rowq = lambda b: oracle.mxfp8_dequantize(*oracle.mxfp8_quantize_bf16(b))  # noqa: E731
+    xq, dyq, w13q = rowq(x), rowq(dy), rowq(w13)
+    w2q = rowq(np.ascontiguousarray(w2.transpose(0, 2, 1))).transpose(0, 2, 1)
+    _, _, _, dtk_ref = oracle.backward(xq, idx, w, w13q, w2q, dyq, mode=oracle.BF16)
+    np.testing.assert_array_equal(dtk, dtk_ref)
+    # and differs from the unquantized BF16 backward (the quantization is not skipped)
+    _, _, _, dtk_b = oracle.backward(oracle.bf16_to_f64(x), idx, w, w13, w2,
+                                     oracle.bf16_to_f64(dy), mode=oracle.BF16)
+    assert not np.array_equal(dtk, dtk_b)

@@ -400,7 +400,24 @@ def run_mok(args):
             fwd_mx()
         ms_m = timed(fwd_mx, args.steps)
         phases["fwd_mxfp8"] = {"ms": ms_m, "tflops": cfg.fwd_flops() / (ms_m * 1e-3) / 1e12}
-        del Lm, q13, s13, q2, s2
+
+        # MXFP8 backward (G and dgrad in MXFP8 on weights pre-quantized along their
+        # contraction axes, untimed like the forward's; weight gradients BF16), after an
+        # MXFP8 forward that saved its pre-activations
+        from mixture_experts_layer_deterministic_gb300.buffers import (
+            backward_mxfp8, quantize_mxfp8_transposed)
+        w13t, w2t = quantize_mxfp8_transposed(w13), quantize_mxfp8_transposed(w2)
+        Lm.route(lg, stream)
+        Lm.schedule(stream=stream)
+        Lm.forward(x, q13, q2, y, s13, s2, saved_preact=pre, stream=stream)
+
+        def bwd_mx():
+            backward_mxfp8(Lm, x, pre, w13t, w2t, dy, dx, dw13, dw2, dtk, dlg, stream=stream)
+        for _ in range(2):
+            bwd_mx()
+        ms_mb = timed(bwd_mx, args.steps)
+        phases["bwd_mxfp8"] = {"ms": ms_mb, "tflops": cfg.bwd_flops() / (ms_mb * 1e-3) / 1e12}
+        del Lm, q13, s13, q2, s2, w13t, w2t
 
     # e2e through the public API with host buffers: every step copies its inputs (x, logits,
     # dy) from pinned host memory and reads its results (y, dx) back. As a training loop

@@ -183,7 +183,7 @@ mok_status mok_build_schedule_noalloc(const mok_config *cfg, const int32_t *topk
  *   y       [T][H] fp32 out: y[t] = sum over k = 0..K-1, in that order, of
  *           topk_w[t,k] * o[t,k], fp32 throughout (o is the fp32 down-GEMM result).
  *   saved_preact  NULL, or [R][2I] fp32 out: the gate/up GEMM result of sorted row r
- *           (needed by mok_backward; BF16 only).
+ *           (needed by mok_backward, or by mok_backward_mxfp8 after an MXFP8 forward).
  * GEMMs accumulate in fp32; values that are only stored (expert outputs, saved
  * pre-activations) stay fp32. */
 mok_status mok_forward(const mok_config *cfg, const void *x, const mok_schedule *sched,
@@ -215,6 +215,24 @@ mok_status mok_backward(const mok_config *cfg, const void *x, const mok_schedule
                         float *d_topk_w, float *d_logits, void *ws, size_t ws_bytes,
                         cudaStream_t stream);
 
+/* Layer backward, MXFP8 ([arex] section "pull 代替 push": pre-quantized weights, MXFP8
+ * activations): as mok_backward, with cfg->prec == MOK_MXFP8, after an MXFP8 mok_forward
+ * that saved its pre-activations (required here). The G GEMM contracts over H with dy and
+ * W2 quantized along H; the dgrad GEMM over 2I with dA and W13 quantized along 2I (dA is
+ * quantized in the G GEMM's epilogue). The weight-gradient GEMMs stay BF16 (dA and w*h
+ * rounded to bf16): their time is the fp32 dW writes, which MXFP8 would not shorten.
+ *   w13t_q [E][H][2I] E4M3, w13t_s [E][H][2I/32]: W13 quantized along 2I, transposed;
+ *   w2t_q  [E][I][H] E4M3,  w2t_s  [E][I][H/32]:  W2 quantized along H, transposed (both as
+ *          made by mok_quantize_mxfp8_transposed from the bf16 weights).
+ *   Other arguments and outputs as for mok_backward; the workspace is
+ *   mok_workspace_size(cfg, MOK_WS_BACKWARD) for this (MXFP8) configuration. */
+mok_status mok_backward_mxfp8(const mok_config *cfg, const void *x, const mok_schedule *sched,
+                              const float *topk_w, const void *saved_preact,
+                              const uint8_t *w13t_q, const uint8_t *w13t_s,
+                              const uint8_t *w2t_q, const uint8_t *w2t_s, const void *dy,
+                              void *dx, void *dw13, void *dw2, float *d_topk_w,
+                              float *d_logits, void *ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Shared expert, forward ([alphalab] "Mixture-of-Kittens" (alphalab.site), section 一: the
  * forward runs the FFN/SwiGLU of the shared and of the routed experts). Every token passes
  * through one more SwiGLU expert, with weight one and no routing, and its output is added
@@ -239,6 +257,17 @@ mok_status mok_shared_expert_forward(const mok_config *cfg, const void *x, const
  * nearest even, saturating at +-448. cols must be a multiple of 32. */
 mok_status mok_quantize_mxfp8(const void *src_bf16, int64_t rows, int32_t cols, uint8_t *q,
                               uint8_t *scale, cudaStream_t stream);
+
+/* MXFP8 quantization of a batch of bf16 matrices along their ROWS, stored transposed: the
+ * pre-quantized weights of the MXFP8 backward ([arex] section "pull 代替 push"), whose G
+ * and dgrad GEMMs contract over W2's H and W13's 2I. src [batch][rows][cols] bf16 ->
+ * q [batch][cols][rows] E4M3, scale [batch][cols][rows/32] E8M0, each 32-element block of
+ * a column (rows 32j..32j+31) quantized by the rule of mok_quantize_mxfp8. For the
+ * backward: W2 [E][H][I] -> W2t [E][I][H]; W13 [E][2I][H] -> W13t [E][H][2I]. rows must be
+ * a multiple of 32. */
+mok_status mok_quantize_mxfp8_transposed(const void *src_bf16, int64_t batch, int32_t rows,
+                                         int32_t cols, uint8_t *q, uint8_t *scale,
+                                         cudaStream_t stream);
 
 /* ---- instrumentation ------------------------------------------------------------ */
 

@@ -41,6 +41,7 @@ EXPORTED = [
     "mok_backward", "mok_quantize_mxfp8", "mok_read_device_status",
     "mok_clear_device_status", "mok_profile_enable", "mok_profile_read",
     "mok_build_schedule_noalloc", "mok_shared_expert_forward",
+    "mok_quantize_mxfp8_transposed", "mok_backward_mxfp8",
 ]
 
 # bytes of the fixed scratch array behind mok_build_schedule_noalloc
@@ -94,7 +95,10 @@ def lib():
             "mok_backward": ([cfgp, p, schp, p, p, p, p, p, p, p, p, p, p, p, sz, p],
                              ctypes.c_int),
             "mok_shared_expert_forward": ([cfgp, p, p, p, p, p, p, sz, p], ctypes.c_int),
+            "mok_backward_mxfp8": ([cfgp, p, schp, p, p, p, p, p, p, p, p, p, p, p, p, p, sz,
+                                    p], ctypes.c_int),
             "mok_quantize_mxfp8": ([p, i64, i32, p, p, p], ctypes.c_int),
+            "mok_quantize_mxfp8_transposed": ([p, i64, i32, i32, p, p, p], ctypes.c_int),
             "mok_read_device_status": ([ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
             "mok_clear_device_status": ([], ctypes.c_int),
             "mok_profile_enable": ([ctypes.c_int], ctypes.c_int),
@@ -204,9 +208,23 @@ def mok_shared_expert_forward(cfg, x, w13_s, w2_s, y, saved_preact_s, ws, ws_byt
                                            int(ws_bytes), _stream(stream))
 
 
+def mok_backward_mxfp8(cfg, x, sched, topk_w, saved_preact, w13t_q, w13t_s, w2t_q, w2t_s, dy,
+                       dx, dw13, dw2, d_topk_w, d_logits, ws, ws_bytes, stream=None) -> int:
+    return lib().mok_backward_mxfp8(ctypes.byref(cfg), _ptr(x), ctypes.byref(sched),
+                                    _ptr(topk_w), _ptr(saved_preact), _ptr(w13t_q),
+                                    _ptr(w13t_s), _ptr(w2t_q), _ptr(w2t_s), _ptr(dy), _ptr(dx),
+                                    _ptr(dw13), _ptr(dw2), _ptr(d_topk_w), _ptr(d_logits),
+                                    _ptr(ws), int(ws_bytes), _stream(stream))
+
+
 def mok_quantize_mxfp8(src, rows, cols, q, scale, stream=None) -> int:
     return lib().mok_quantize_mxfp8(_ptr(src), int(rows), int(cols), _ptr(q), _ptr(scale),
                                     _stream(stream))
+
+
+def mok_quantize_mxfp8_transposed(src, batch, rows, cols, q, scale, stream=None) -> int:
+    return lib().mok_quantize_mxfp8_transposed(_ptr(src), int(batch), int(rows), int(cols),
+                                               _ptr(q), _ptr(scale), _stream(stream))
 
 
 def mok_read_device_status():

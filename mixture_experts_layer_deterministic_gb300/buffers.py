@@ -89,6 +89,19 @@ class MoELayer:
         return dx
 
 
+def backward_mxfp8(layer, x, saved_preact, w13t, w2t, dy, dx, dw13, dw2, d_topk_w,
+                   d_logits=None, topk_w=None, stream=None):
+    """MXFP8 backward of a layer built with prec=MOK_MXFP8 (backward=True); w13t, w2t are
+    (q, scale) pairs from quantize_mxfp8_transposed of the bf16 W13 and W2."""
+    if layer.ws_b is None:
+        layer.ws_b, layer.ws_b_n = workspace(layer.cfg, B.MOK_WS_BACKWARD, layer.device)
+    B.check(B.mok_backward_mxfp8(layer.cfg, x, layer.sched.struct,
+                                 layer.w if topk_w is None else topk_w, saved_preact, w13t[0],
+                                 w13t[1], w2t[0], w2t[1], dy, dx, dw13, dw2, d_topk_w, d_logits,
+                                 layer.ws_b, layer.ws_b_n, stream), "backward mxfp8")
+    return dx
+
+
 class SharedExpert:
     """The shared expert of a layer configuration (same H, I as the routed experts)."""
 
@@ -101,6 +114,16 @@ class SharedExpert:
         B.check(B.mok_shared_expert_forward(self.cfg, x, w13_s, w2_s, y, saved_preact,
                                             self.ws, self.ws_n, stream), "shared forward")
         return y
+
+
+def quantize_mxfp8_transposed(src, stream=None):
+    """MXFP8 of a [batch][rows][cols] bf16 tensor along rows, stored as [batch][cols][rows]
+    (q) and [batch][cols][rows/32] (scale): the MXFP8 backward's pre-quantized weights."""
+    b, r, c = src.shape
+    q = torch.empty((b, c, r), dtype=torch.uint8, device=src.device)
+    s = torch.empty((b, c, r // 32), dtype=torch.uint8, device=src.device)
+    B.check(B.mok_quantize_mxfp8_transposed(src, b, r, c, q, s, stream), "quantize_transposed")
+    return q, s
 
 
 def quantize_mxfp8(src, stream=None):

@@ -115,15 +115,20 @@ struct BwdWs {
     float *dx_slots;
     float *dS_part;
     float *preact;  // recomputed pre-activations [R][2I] (recompute workspace only)
+    // MXFP8: padded row of every flat id; dy and dA quantized along H / 2I; scale atoms of
+    // the transposed weights and of the dy and dA tiles
+    int32_t *prow;
+    uint8_t *dy_q, *dy_s, *dA_q, *dA_s, *sf_w2t, *sf_w13t, *sf_dy, *sf_dA;
 };
 
 size_t carve_bwd(const mok_config *c, void *ws, BwdWs *o, bool recompute = false) {
     Carver cv{(char *)ws};
     const int64_t R = rows_R(c);
+    const bool mx = c->prec == MOK_MXFP8;
     BwdWs w;
     w.rpad_cap = R + 15 * (int64_t)c->E;
     w.poff = cv.take<int32_t>((size_t)(c->E + 1) * 4);
-    w.tiles_cap = tile_list_cap(R, c->E, gemm_tc_tile_rows(false));
+    w.tiles_cap = tile_list_cap(R, c->E, gemm_tc_tile_rows(mx));
     int32_t *t = cv.take<int32_t>(16 + (size_t)w.tiles_cap * 16);
     w.tiles = t ? t + 4 : nullptr;
     w.dy_perm = cv.take<uint16_t>((size_t)w.rpad_cap * c->H * 2);
@@ -133,6 +138,20 @@ size_t carve_bwd(const mok_config *c, void *ws, BwdWs *o, bool recompute = false
     w.dS_part = cv.take<float>((size_t)R * gemm_tc_dS_parts(c->I) * 4);
     w.dx_slots = cv.take<float>((size_t)R * c->H * 4);
     w.preact = recompute ? cv.take<float>((size_t)R * 2 * c->I * 4) : nullptr;
+    w.prow = nullptr;
+    w.dy_q = w.dy_s = w.dA_q = w.dA_s = w.sf_w2t = w.sf_w13t = w.sf_dy = w.sf_dA = nullptr;
+    if (mx) {
+        const int64_t H = c->H, I2 = 2 * (int64_t)c->I, E = c->E;
+        w.prow = cv.take<int32_t>((size_t)R * 4);
+        w.dy_q = cv.take<uint8_t>((size_t)(w.rpad_cap * H));
+        w.dy_s = cv.take<uint8_t>((size_t)(w.rpad_cap * (H / 32)));
+        w.dA_q = cv.take<uint8_t>((size_t)(w.rpad_cap * I2));
+        w.dA_s = cv.take<uint8_t>((size_t)(w.rpad_cap * (I2 / 32)));
+        w.sf_w2t = cv.take<uint8_t>((size_t)(E * c->I * H / 32));
+        w.sf_w13t = cv.take<uint8_t>((size_t)(E * H * I2 / 32));
+        w.sf_dy = cv.take<uint8_t>((size_t)(w.tiles_cap * (H / 128) * 512));
+        w.sf_dA = cv.take<uint8_t>((size_t)(w.tiles_cap * (I2 / 128) * 512));
+    }
     if (o) *o = w;
     return cv.off;
 }
@@ -287,7 +306,7 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
     if ((st = check_sched(c, sch)) != MOK_OK) return st;
     const bool mx = c->prec == MOK_MXFP8;
     if (!x || !topk_w || !w13 || !w2 || !y) return MOK_ERR_INVALID_ARG;
-    if (mx && (!w13_scale || !w2_scale || saved_preact)) return MOK_ERR_INVALID_ARG;
+    if (mx && (!w13_scale || !w2_scale)) return MOK_ERR_INVALID_ARG;
     if (!mx && (w13_scale || w2_scale)) return MOK_ERR_INVALID_ARG;
     const void *ps[] = {x, topk_w, w13, w2, y, w13_scale, w2_scale, saved_preact};
     for (const void *p : ps)
@@ -363,21 +382,33 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
     return MOK_OK;
 }
 
-mok_status mok_backward(const mok_config *c, const void *x, const mok_schedule *sch,
-                        const float *topk_w, const void *saved_preact, const void *w13,
-                        const void *w2, const void *dy, void *dx, void *dw13, void *dw2,
-                        float *d_topk_w, float *d_logits, void *ws, size_t ws_bytes,
-                        cudaStream_t stream) {
+}  // extern "C"
+
+namespace mok {
+// the transposed, MXFP8-quantized weights of the MXFP8 backward
+struct MxBwdWeights {
+    const uint8_t *w13t_q, *w13t_s, *w2t_q, *w2t_s;
+};
+
+mok_status backward_impl(const mok_config *c, const void *x, const mok_schedule *sch,
+                         const float *topk_w, const void *saved_preact, const void *w13,
+                         const void *w2, const MxBwdWeights *mxw, const void *dy, void *dx,
+                         void *dw13, void *dw2, float *d_topk_w, float *d_logits, void *ws,
+                         size_t ws_bytes, cudaStream_t stream) {
     mok_status st = mok_check_config(c);
     if (st != MOK_OK) return st;
     int *status;
     if ((st = check_device(&status)) != MOK_OK) return st;
     if ((st = check_sched(c, sch)) != MOK_OK) return st;
-    if (c->prec != MOK_BF16) return MOK_ERR_INVALID_ARG;
-    if (!x || !topk_w || !w13 || !w2 || !dy || !dx || !dw13 || !dw2 || !d_topk_w)
+    const bool mx = mxw != nullptr;
+    if (c->prec != (mx ? MOK_MXFP8 : MOK_BF16)) return MOK_ERR_INVALID_ARG;
+    if (!x || !topk_w || !dy || !dx || !dw13 || !dw2 || !d_topk_w) return MOK_ERR_INVALID_ARG;
+    if (!mx && (!w13 || !w2)) return MOK_ERR_INVALID_ARG;
+    if (mx && (!saved_preact || !mxw->w13t_q || !mxw->w13t_s || !mxw->w2t_q || !mxw->w2t_s))
         return MOK_ERR_INVALID_ARG;
     const bool recompute = saved_preact == nullptr;
-    const void *ps[] = {x, topk_w, saved_preact, w13, w2, dy, dx, dw13, dw2, d_topk_w, d_logits};
+    const void *ps[] = {x, topk_w, saved_preact, w13, w2, dy, dx, dw13, dw2, d_topk_w, d_logits,
+                        mx ? mxw->w13t_q : nullptr, mx ? mxw->w2t_q : nullptr};
     for (const void *p : ps)
         if (p && !aligned16(p)) return MOK_ERR_INVALID_ARG;
     const size_t need = carve_bwd(c, nullptr, nullptr, recompute);
@@ -388,26 +419,54 @@ mok_status mok_backward(const mok_config *c, const void *x, const mok_schedule *
     const int E = c->E, H = c->H, I = c->I, K = c->K;
     MOK_LAUNCH(KK_PAD, 1, launch_pad_offsets(sch->counts, E, w.poff, stream));
     MOK_LAUNCH(KK_TILES, 1,
-               launch_build_tiles(sch->offsets, E, 0, R, gemm_tc_tile_rows(false), w.tiles,
+               launch_build_tiles(sch->offsets, E, 0, R, gemm_tc_tile_rows(mx), w.tiles,
                                   w.tiles_cap, status, stream));
     MOK_LAUNCH(KK_GATHER_BWD, 1,
                launch_gather_bwd((const uint16_t *)dy, (const uint16_t *)x, sch->inv,
                                  sch->counts, sch->offsets, w.poff, E, c->T, K, H, w.dy_perm,
-                                 w.x_perm, stream));
+                                 w.x_perm, w.prow, w.dy_q, w.dy_s, stream));
     if (recompute)
         MOK_LAUNCH(KK_GEMM_UP, 1,
                    launch_gemm_up_recompute_tc(w.tiles, w.tiles_cap, w.x_perm, w.rpad_cap, w13,
                                                sch->offsets, w.poff, w.preact, H, I, E, status,
                                                stream));
+    if (mx)  // the tensor cores' scale atoms of W2t, W13t and of the dy tiles
+        MOK_LAUNCH(KK_SCALE_ATOMS, 3,
+                   first_error(first_error(launch_scale_atoms_rows(mxw->w2t_s, (int64_t)E * I,
+                                                                   H, w.sf_w2t, stream),
+                                           launch_scale_atoms_rows(mxw->w13t_s, (int64_t)E * H,
+                                                                   2 * I, w.sf_w13t, stream)),
+                               launch_scale_atoms_tiles_padded(w.tiles, w.tiles_cap, w.dy_s,
+                                                               sch->offsets, w.poff, H,
+                                                               w.sf_dy, stream)));
     const float *pre = recompute ? w.preact : (const float *)saved_preact;
     GemmGArgs ga{w.tiles, w.tiles_cap, sch->offsets, w.poff, (const uint16_t *)w2, w.dy_perm,
                  pre, sch->perm, topk_w, w.dA, w.sh, w.dS_part, H, I, status};
+    if (mx) {
+        ga.mxfp8 = true;
+        ga.w2t_q = mxw->w2t_q;
+        ga.sf_w2t = w.sf_w2t;
+        ga.dy_q = w.dy_q;
+        ga.sf_dy = w.sf_dy;
+        ga.dA_q = w.dA_q;
+        ga.dA_s = w.dA_s;
+    }
     MOK_LAUNCH(KK_GEMM_G, 1, launch_gemm_g_tc(ga, E, w.rpad_cap, stream));
     MOK_LAUNCH(KK_ROUTER_GRAD, 1,
                launch_router_grad(w.dS_part, gemm_tc_dS_parts(I), sch->inv, sch->offsets,
                                   topk_w, c->T, K, E, d_topk_w, d_logits, stream));
     GemmDgradArgs dg{w.tiles, w.tiles_cap, sch->offsets, w.poff, (const uint16_t *)w13, w.dA,
                      sch->perm, w.dx_slots, H, I, status};
+    if (mx) {
+        MOK_LAUNCH(KK_SCALE_ATOMS, 1,
+                   launch_scale_atoms_tiles_padded(w.tiles, w.tiles_cap, w.dA_s, sch->offsets,
+                                                   w.poff, 2 * I, w.sf_dA, stream));
+        dg.mxfp8 = true;
+        dg.w13t_q = mxw->w13t_q;
+        dg.sf_w13t = w.sf_w13t;
+        dg.dA_q = w.dA_q;
+        dg.sf_dA = w.sf_dA;
+    }
     MOK_LAUNCH(KK_GEMM_DGRAD, 1, launch_gemm_dgrad_tc(dg, E, w.rpad_cap, stream));
     MOK_LAUNCH(KK_DX_REDUCE, 1,
                launch_combine(w.dx_slots, nullptr, c->T, K, H, (float *)dx, stream));
@@ -420,6 +479,29 @@ mok_status mok_backward(const mok_config *c, const void *x, const mok_schedule *
                launch_wgrad_tc(sch->counts, w.poff, w.sh, w.dy_perm, (float *)dw2, E, I, H,
                                w.rpad_cap, status, stream));
     return MOK_OK;
+}
+}  // namespace mok
+
+extern "C" {
+
+mok_status mok_backward(const mok_config *c, const void *x, const mok_schedule *sch,
+                        const float *topk_w, const void *saved_preact, const void *w13,
+                        const void *w2, const void *dy, void *dx, void *dw13, void *dw2,
+                        float *d_topk_w, float *d_logits, void *ws, size_t ws_bytes,
+                        cudaStream_t stream) {
+    return backward_impl(c, x, sch, topk_w, saved_preact, w13, w2, nullptr, dy, dx, dw13, dw2,
+                         d_topk_w, d_logits, ws, ws_bytes, stream);
+}
+
+mok_status mok_backward_mxfp8(const mok_config *c, const void *x, const mok_schedule *sch,
+                              const float *topk_w, const void *saved_preact,
+                              const uint8_t *w13t_q, const uint8_t *w13t_s,
+                              const uint8_t *w2t_q, const uint8_t *w2t_s, const void *dy,
+                              void *dx, void *dw13, void *dw2, float *d_topk_w,
+                              float *d_logits, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    const MxBwdWeights mxw{w13t_q, w13t_s, w2t_q, w2t_s};
+    return backward_impl(c, x, sch, topk_w, saved_preact, nullptr, nullptr, &mxw, dy, dx, dw13,
+                         dw2, d_topk_w, d_logits, ws, ws_bytes, stream);
 }
 
 mok_status mok_shared_expert_forward(const mok_config *c, const void *x, const void *w13_s,
@@ -465,6 +547,23 @@ mok_status mok_quantize_mxfp8(const void *src_bf16, int64_t rows, int32_t cols, 
     if (!aligned16(src_bf16) || !aligned16(q)) return MOK_ERR_INVALID_ARG;
     MOK_LAUNCH(KK_QUANTIZE, 1,
                launch_quantize_mxfp8((const uint16_t *)src_bf16, rows, cols, q, scale, stream));
+    return MOK_OK;
+}
+
+mok_status mok_quantize_mxfp8_transposed(const void *src_bf16, int64_t batch, int32_t rows,
+                                         int32_t cols, uint8_t *q, uint8_t *scale,
+                                         cudaStream_t stream) {
+    int *status;
+    mok_status st = check_device(&status);
+    if (st != MOK_OK) return st;
+    if (batch < 0 || rows <= 0 || cols <= 0 || rows % 32 != 0) return MOK_ERR_INVALID_ARG;
+    if (batch == 0) return MOK_OK;
+    if (!src_bf16 || !q || !scale) return MOK_ERR_INVALID_ARG;
+    // each 32-byte block of q is written with two 16-byte stores
+    if (!aligned16(src_bf16) || !aligned16(q)) return MOK_ERR_INVALID_ARG;
+    MOK_LAUNCH(KK_QUANTIZE, 1,
+               launch_quantize_mxfp8_transposed((const uint16_t *)src_bf16, batch, rows, cols,
+                                                q, scale, stream));
     return MOK_OK;
 }
 

@@ -135,6 +135,45 @@ __global__ void __launch_bounds__(TPB)
     }
 }
 
+// Along rows, stored transposed: one thread per (matrix b, column c, 32-row block j); the
+// block src[b][32j..32j+31][c] (neighbouring threads read neighbouring columns) becomes
+// q[b][c][32j..32j+31] and scale[b][c][j].
+__global__ void __launch_bounds__(TPB)
+    quantize_transposed_kernel(const uint16_t *__restrict__ src, int64_t batch, int rows,
+                               int cols, uint8_t *__restrict__ q, uint8_t *__restrict__ sc) {
+    const int nb = rows / 32;
+    const int64_t total = batch * nb * cols;
+    const int64_t stride = (int64_t)gridDim.x * TPB;
+    for (int64_t i = (int64_t)blockIdx.x * TPB + threadIdx.x; i < total; i += stride) {
+        const int c = (int)(i % cols);
+        const int j = (int)((i / cols) % nb);
+        const int64_t b = i / ((int64_t)cols * nb);
+        const uint16_t *s0 = src + (b * rows + (int64_t)j * 32) * cols + c;
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+            w[k] = (uint32_t)__ldg(s0 + (int64_t)(2 * k) * cols) |
+                   ((uint32_t)__ldg(s0 + (int64_t)(2 * k + 1) * cols) << 16);
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+        const uint32_t sb = mx_scale_byte(amax);
+        const float inv = mx_inv_scale(sb);
+        uint32_t out[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t a = e4m3x2(bf16_lo(w[2 * k]) * inv, bf16_hi(w[2 * k]) * inv);
+            const uint32_t bb = e4m3x2(bf16_lo(w[2 * k + 1]) * inv, bf16_hi(w[2 * k + 1]) * inv);
+            out[k] = a | (bb << 16);
+        }
+        uint4 *qd = reinterpret_cast<uint4 *>(q + (b * cols + c) * (int64_t)rows + j * 32);
+        qd[0] = make_uint4(out[0], out[1], out[2], out[3]);
+        qd[1] = make_uint4(out[4], out[5], out[6], out[7]);
+        sc[(b * cols + c) * (int64_t)nb + j] = (uint8_t)sb;
+    }
+}
+
 // Token-major form (ring holds every row): one thread per 32-element block of token t,
 // quantized once and written to the ring rows of its K routed copies.
 __global__ void __launch_bounds__(TPB)
@@ -208,7 +247,8 @@ __global__ void __launch_bounds__(TPB)
     gather_bwd_kernel(const uint16_t *__restrict__ dy, const uint16_t *__restrict__ x,
                       const int32_t *__restrict__ inv, const int32_t *__restrict__ offsets,
                       const int32_t *__restrict__ poff, int E, int64_t T, int K, int H,
-                      uint16_t *__restrict__ dyp, uint16_t *__restrict__ xp) {
+                      uint16_t *__restrict__ dyp, uint16_t *__restrict__ xp,
+                      int32_t *__restrict__ prow) {
     const int lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * (TPB / 32);
     const int nv = H / 8;
@@ -222,6 +262,7 @@ __global__ void __launch_bounds__(TPB)
                 if (offsets[mid] <= r) lo = mid; else hi = mid - 1;
             }
             pk = poff[lo] + (int64_t)(r - offsets[lo]);
+            if (prow != nullptr) prow[t * K + lane] = (int32_t)pk;
         }
         for (int which = 0; which < 2; ++which) {
             const uint4 *src = reinterpret_cast<const uint4 *>((which ? x : dy) + t * H);
@@ -247,11 +288,37 @@ __global__ void __launch_bounds__(TPB)
     }
 }
 
+// MXFP8 backward: dy quantized along H into the padded layout, one thread per 32-element
+// block of token t, quantized once and written to the padded rows prow[t*K + k] of its K
+// routed copies.
+__global__ void __launch_bounds__(TPB)
+    quantize_dy_padded_kernel(const uint16_t *__restrict__ dy, const int32_t *__restrict__ prow,
+                              int64_t T, int K, int H, uint8_t *__restrict__ q,
+                              uint8_t *__restrict__ sc) {
+    const int nb = H / 32;
+    const int64_t total = T * nb;
+    const int64_t stride = (int64_t)gridDim.x * TPB;
+    for (int64_t i = (int64_t)blockIdx.x * TPB + threadIdx.x; i < total; i += stride) {
+        const int64_t t = i / nb;
+        const int b = (int)(i % nb);
+        uint32_t out[8];
+        const uint32_t sb = quant_block32_regs(dy + t * H + b * 32, out);
+        for (int k = 0; k < K; ++k) {
+            const int64_t p = __ldg(prow + t * K + k);
+            uint4 *qd = reinterpret_cast<uint4 *>(q + p * H + b * 32);
+            qd[0] = make_uint4(out[0], out[1], out[2], out[3]);
+            qd[1] = make_uint4(out[4], out[5], out[6], out[7]);
+            sc[p * nb + b] = (uint8_t)sb;
+        }
+    }
+}
+
 // The pad rows of every expert (at most 15) are zero in both padded arrays: one warp per
 // (expert, pad row).
 __global__ void __launch_bounds__(TPB)
     zero_pad_rows_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__ poff,
-                         int E, int H, uint16_t *__restrict__ dyp, uint16_t *__restrict__ xp) {
+                         int E, int H, uint16_t *__restrict__ dyp, uint16_t *__restrict__ xp,
+                         uint8_t *__restrict__ dyq, uint8_t *__restrict__ dys) {
     const int lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * (TPB / 32);
     const int nv = H / 8;
@@ -266,6 +333,11 @@ __global__ void __launch_bounds__(TPB)
         for (int v = lane; v < nv; v += 32) {
             d0[v] = z;
             d1[v] = z;
+        }
+        if (dyq != nullptr) {  // MXFP8 copy of dy: E4M3 bytes and scale bytes
+            uint4 *d2 = reinterpret_cast<uint4 *>(dyq + p * H);
+            for (int v = lane; v < H / 16; v += 32) d2[v] = z;
+            for (int v = lane; v < H / 32; v += 32) dys[p * (H / 32) + v] = 0;
         }
     }
 }
@@ -312,41 +384,79 @@ __global__ void __launch_bounds__(TPB)
 // The tensor cores read an operand's E8M0 scales as atoms of 128 rows x 4 K-blocks (512
 // bytes: 32 rows of 16 bytes, row i holding the 4 scales of rows i, i+32, i+64, i+96).
 // Weights: plain [rows][K/32] -> atom (row/128, kg) at ((row/128) * K/128 + kg) * 512.
-__global__ void __launch_bounds__(TPB)
-    scale_atoms_rows_kernel(const uint8_t *__restrict__ src, int64_t rows, int K,
-                            uint8_t *__restrict__ dst) {
-    const int kgn = K / 128;
-    const int64_t total = rows * kgn;
-    const int64_t stride = (int64_t)gridDim.x * TPB;
-    for (int64_t i = (int64_t)blockIdx.x * TPB + threadIdx.x; i < total; i += stride) {
-        const int64_t row = i / kgn;
-        const int kg = (int)(i % kgn);
-        const uint32_t v = *reinterpret_cast<const uint32_t *>(src + row * (K / 32) + 4 * kg);
-        uint8_t *o = dst + ((row / 128) * kgn + kg) * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4;
-        *reinterpret_cast<uint32_t *>(o) = v;
-    }
-}
-
 // Token tiles: the rows n < 128 of tile t = (e, r0, r1) (rows past the tile get byte 0) ->
-// one atom per 128-wide K block at (t * K/128 + kg) * 512.
-__global__ void __launch_bounds__(TPB)
-    scale_atoms_tiles_kernel(const int32_t *__restrict__ tiles, int64_t cap,
-                             const uint8_t *__restrict__ src, RingMap rm, int K,
-                             uint8_t *__restrict__ dst) {
-    const int kgn = K / 128;
-    const int64_t nt = tiles[-4] < cap ? tiles[-4] : cap;
-    const int64_t total = nt * 128 * kgn;
-    const int64_t stride = (int64_t)gridDim.x * TPB;
-    for (int64_t i = (int64_t)blockIdx.x * TPB + threadIdx.x; i < total; i += stride) {
-        const int kg = (int)(i % kgn);
-        const int n = (int)((i / kgn) % 128);
-        const int64_t t = i / ((int64_t)kgn * 128);
-        const int64_t r0 = tiles[4 * t + 1], r1 = tiles[4 * t + 2];
-        uint32_t v = 0;
-        if (n < r1 - r0)
-            v = *reinterpret_cast<const uint32_t *>(src + rm(r0 + n) * (K / 32) + 4 * kg);
-        uint8_t *o = dst + (t * kgn + kg) * 512 + (n % 32) * 16 + (n / 32) * 4;
-        *reinterpret_cast<uint32_t *>(o) = v;
+// one atom per 128-wide K block at (t * K/128 + kg) * 512; sorted row r sits at ring slot
+// rm(r), or, with poff (the backward's padded layout), at poff[e] + r - offsets[e].
+//
+// Both go through shared memory: one block iteration loads the scales of 128 rows x 8 K
+// groups (32 bytes per row, 16-byte loads) and writes the 8 atoms with 16-byte stores, so
+// neither side is a scatter of 4-byte accesses.
+constexpr int ATOM_KG = 8;  // K groups (atoms) per block iteration
+
+struct AtomRows {  // where row n of atom row-block b starts in the source (-1: absent)
+    const int32_t *tiles;   // nullptr: plain rows
+    int64_t rows;
+    RingMap rm;
+    const int32_t *offsets, *poff;
+    MOK_DEV int64_t operator()(int64_t b, int n, int rowbytes) const {
+        if (tiles == nullptr) {
+            const int64_t r = b * 128 + n;
+            return r < rows ? r * rowbytes : -1;
+        }
+        const int64_t r0 = tiles[4 * b + 1], r1 = tiles[4 * b + 2];
+        if (n >= r1 - r0) return -1;
+        const int e = tiles[4 * b];
+        const int64_t row = poff != nullptr ? poff[e] + (r0 - offsets[e]) + n : rm(r0 + n);
+        return row * rowbytes;
+    }
+};
+
+__global__ void __launch_bounds__(256)
+    scale_atoms_kernel(const uint8_t *__restrict__ src, int64_t n_blocks, int64_t cap, int K,
+                       AtomRows where, uint8_t *__restrict__ dst) {
+    __shared__ __align__(16) uint8_t tile[128][ATOM_KG * 4];
+    const int kgn = K / 128, rowbytes = K / 32;
+    const int nkc = (kgn + ATOM_KG - 1) / ATOM_KG;
+    int64_t nb = n_blocks;
+    if (where.tiles != nullptr) nb = where.tiles[-4] < cap ? where.tiles[-4] : cap;
+    for (int64_t it = blockIdx.x; it < nb * nkc; it += gridDim.x) {
+        const int64_t b = it / nkc;
+        const int kc = (int)(it % nkc);
+        const int nkg = kgn - kc * ATOM_KG < ATOM_KG ? kgn - kc * ATOM_KG : ATOM_KG;
+        {  // 128 rows x (4 * nkg) bytes: two threads per row, 16 bytes each
+            const int n = threadIdx.x >> 1, half = threadIdx.x & 1;
+            const int64_t at = where(b, n, rowbytes);
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (at >= 0 && half * 16 < nkg * 4) {
+                const uint8_t *sp = src + at + kc * ATOM_KG * 4 + half * 16;
+                const int left = nkg * 4 - half * 16;  // bytes of this row in the patch
+                // 16-byte loads only where every row starts on a 16-byte boundary (a row
+                // is K/32 bytes, a multiple of 4); else 4-byte loads
+                if (left >= 16 && rowbytes % 16 == 0) {
+                    v = *reinterpret_cast<const uint4 *>(sp);
+                } else {
+                    uint32_t w[4] = {0, 0, 0, 0};
+                    const int nw = left < 16 ? left / 4 : 4;
+                    for (int q = 0; q < nw; ++q)
+                        w[q] = *reinterpret_cast<const uint32_t *>(sp + 4 * q);
+                    v = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            *reinterpret_cast<uint4 *>(&tile[n][half * 16]) = v;
+        }
+        __syncthreads();
+        {  // atom a (K group kc*8 + a), its 16-byte row r16: scales of rows r16 + 32j
+            const int a = threadIdx.x >> 5, r16 = threadIdx.x & 31;
+            if (a < nkg) {
+                uint32_t w[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    w[j] = *reinterpret_cast<const uint32_t *>(&tile[r16 + 32 * j][a * 4]);
+                uint8_t *o = dst + (b * kgn + kc * ATOM_KG + a) * 512 + r16 * 16;
+                *reinterpret_cast<uint4 *>(o) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+        __syncthreads();
     }
 }
 
@@ -406,6 +516,15 @@ cudaError_t launch_quantize_mxfp8(const uint16_t *src, int64_t rows, int cols, u
     return cudaGetLastError();
 }
 
+cudaError_t launch_quantize_mxfp8_transposed(const uint16_t *src, int64_t batch, int rows,
+                                             int cols, uint8_t *q, uint8_t *scale,
+                                             cudaStream_t s) {
+    if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
+    quantize_transposed_kernel<<<grid_for(batch * (rows / 32) * cols, TPB, 152 * 16), TPB, 0,
+                                 s>>>(src, batch, rows, cols, q, scale);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const float *slots, const float *w, int64_t T, int K, int H,
                            float *y, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
@@ -416,13 +535,17 @@ cudaError_t launch_combine(const float *slots, const float *w, int64_t T, int K,
 cudaError_t launch_gather_bwd(const uint16_t *dy, const uint16_t *x, const int32_t *inv,
                               const int32_t *counts, const int32_t *offsets,
                               const int32_t *poff, int E, int64_t T, int K, int H,
-                              uint16_t *dy_perm, uint16_t *x_perm, cudaStream_t s) {
+                              uint16_t *dy_perm, uint16_t *x_perm, int32_t *prow, uint8_t *dy_q,
+                              uint8_t *dy_s, cudaStream_t s) {
     if (E == 0) return cudaSuccess;
     if (T > 0)
         gather_bwd_kernel<<<grid_for(T, TPB / 32, 152 * 16), TPB, 0, s>>>(
-            dy, x, inv, offsets, poff, E, T, K, H, dy_perm, x_perm);
+            dy, x, inv, offsets, poff, E, T, K, H, dy_perm, x_perm, prow);
+    if (T > 0 && dy_q != nullptr)
+        quantize_dy_padded_kernel<<<grid_for(T * (H / 32), TPB, 152 * 16), TPB, 0, s>>>(
+            dy, prow, T, K, H, dy_q, dy_s);
     zero_pad_rows_kernel<<<grid_for((int64_t)E * 16, TPB / 32, 152 * 16), TPB, 0, s>>>(
-        counts, poff, E, H, dy_perm, x_perm);
+        counts, poff, E, H, dy_perm, x_perm, dy_q, dy_s);
     return cudaGetLastError();
 }
 
@@ -442,8 +565,10 @@ namespace mok {
 cudaError_t launch_scale_atoms_rows(const uint8_t *src, int64_t rows, int K, uint8_t *dst,
                                     cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
-    scale_atoms_rows_kernel<<<grid_for(rows * (K / 128), TPB, 152 * 16), TPB, 0, s>>>(src, rows,
-                                                                                     K, dst);
+    const int64_t nb = (rows + 127) / 128;
+    const int nkc = (K / 128 + ATOM_KG - 1) / ATOM_KG;
+    scale_atoms_kernel<<<grid_for(nb * nkc, 1, 152 * 8), 256, 0, s>>>(
+        src, nb, 0, K, AtomRows{nullptr, rows, RingMap{1, 1, 0}, nullptr, nullptr}, dst);
     return cudaGetLastError();
 }
 
@@ -451,9 +576,20 @@ cudaError_t launch_scale_atoms_tiles(const int32_t *tiles, int64_t cap, const ui
                                      int64_t R, int MB, int n_slots, int K, uint8_t *dst,
                                      cudaStream_t s) {
     if (cap == 0) return cudaSuccess;
-    RingMap rm{R, MB, n_slots};
-    scale_atoms_tiles_kernel<<<grid_for(cap * 128 * (K / 128), TPB, 152 * 16), TPB, 0, s>>>(
-        tiles, cap, src, rm, K, dst);
+    const int nkc = (K / 128 + ATOM_KG - 1) / ATOM_KG;
+    scale_atoms_kernel<<<grid_for(cap * nkc, 1, 152 * 8), 256, 0, s>>>(
+        src, 0, cap, K, AtomRows{tiles, 0, RingMap{R, MB, n_slots}, nullptr, nullptr}, dst);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scale_atoms_tiles_padded(const int32_t *tiles, int64_t cap,
+                                            const uint8_t *src, const int32_t *offsets,
+                                            const int32_t *poff, int K, uint8_t *dst,
+                                            cudaStream_t s) {
+    if (cap == 0) return cudaSuccess;
+    const int nkc = (K / 128 + ATOM_KG - 1) / ATOM_KG;
+    scale_atoms_kernel<<<grid_for(cap * nkc, 1, 152 * 8), 256, 0, s>>>(
+        src, 0, cap, K, AtomRows{tiles, 0, RingMap{1, 1, 0}, offsets, poff}, dst);
     return cudaGetLastError();
 }
 

@@ -22,15 +22,17 @@
 // unit. Near the end of each unit its producer thread asks Cluster Launch Control to cancel
 // the launch of a CTA that has not started yet and takes over that CTA's unit, so about one
 // CTA per SM runs and units go, in launch order, to whichever CTA frees up first. (The G
-// GEMM instead strides statically over its units with one CTA per SM; see BwdG.) The producer passes each unit index to
-// the MMA thread and the epilogue warps through a small shared-memory queue. CTAs whose
-// index is past the device-side unit count return at once.
+// GEMM instead strides statically over its units with one CTA per SM; see BwdGT.) The
+// producer passes each unit index to the MMA thread and the epilogue warps through a small
+// shared-memory queue. CTAs whose index is past the device-side unit count return at once.
 // A problem policy supplies the work-unit decomposition, the operand majors and the
 // epilogue:
 //   FwdUp     A = W13 (K-major), B = x ring (K-major)      -> SwiGLU, h (bf16 / MXFP8)
 //   FwdDown   A = W2 (K-major),  B = h ring (K-major)      -> fp32 push scatter to slots
 //   BwdG      A = W2^T (MN-major), B = dy_perm (K-major)   -> SwiGLU backward, dA, w*h, dS
+//             (MXFP8: A = W2t K-major, B = quantized dy; dA also quantized)
 //   BwdDgrad  A = W13^T (MN-major), B = dA (K-major)       -> fp32 reverse-dispatch scatter
+//             (MXFP8: A = W13t K-major, B = quantized dA)
 //   Wgrad     A, B MN-major over an expert's padded rows   -> fp32 dW
 // Every GEMM puts the weight (or output-contiguous) dimension on M and the routed rows on
 // N or K, so ragged experts cost at most 15 padding rows. Every output element is one
@@ -224,11 +226,11 @@ struct FwdUpT {
                 if (!mxfp8) {
                     if (live) ((uint16_t *)hring)[rm(r) * I + i] = f32_to_bf16(h);
                 } else {
-                    // the warp's 32 lanes hold one 32-feature MXFP8 block of row r
-                    float amax = fabsf(h);
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1)
-                        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                    // the warp's 32 lanes hold one 32-feature MXFP8 block of row r; its
+                    // maximum magnitude by one integer reduction (non-negative floats'
+                    // bit patterns order like the floats)
+                    const float amax = __uint_as_float(
+                        __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(h))));
                     const uint32_t sb = mx_scale_byte(amax);
                     const uint32_t code = e4m3x2(h * mx_inv_scale(sb), 0.f) & 0xFFu;
                     if (live) {
@@ -330,15 +332,17 @@ struct FwdDownT {
 
 // backward G GEMM: g[r][i] = sum_c W2[e][c][i] dy_perm[p(r)][c]; A0/A1 = features
 // [mb*256, +128) and [mb*256+128, +128) of W2^T (MN-major: W2 rows are c).
-struct BwdG {
-    static constexpr bool A_MN = true, B_MN = false, MX = false;
-    static constexpr int A_MODE = A_MN4;
+// MXFP8: A = W2t [E*I][H] E4M3 (W2 quantized along H, stored transposed: K-major), B = dy
+// quantized along H; the epilogue also quantizes dA along 2I for the MXFP8 dgrad.
+template <bool MXv>
+struct BwdGT {
+    static constexpr bool A_MN = !MXv, B_MN = false, MX = MXv;
+    static constexpr int A_MODE = MXv ? A_ROWS256 : A_MN4;
     // static striding: the four units of a token tile (one per 256-feature block) then run
     // in lockstep on neighbouring CTAs, so their epilogues read the pre-activation rows
     // together; under Cluster Launch Control they drift apart and this epilogue-bound
     // kernel measured 16% slower
     static constexpr bool CLC = false;
-    static constexpr const uint8_t *sf_a = nullptr, *sf_b = nullptr;
     TileUnits tu;
     int H, I;
     const int32_t *offsets, *poff, *perm;
@@ -347,6 +351,8 @@ struct BwdG {
     float *dS_part;
     int n_parts;
     int *status;
+    const uint8_t *sf_a, *sf_b;  // MXFP8: scale atoms of W2t and of the dy tiles
+    uint8_t *dA_q, *dA_s;        // MXFP8: dA quantized along 2I [rpad][2I], [rpad][2I/32]
 
     MOK_DEV int64_t n_units() const { return tu.count(); }
     MOK_DEV Geom geom(int64_t u) const {
@@ -354,15 +360,28 @@ struct BwdG {
         int64_t r0, r1;
         tu.get(u, &e, &r0, &r1, &mb);
         Geom g;
-        g.ax0 = mb * 256;
-        g.ay0 = e * H;
-        g.ax1 = g.ax0 + 128;
-        g.ay1 = e * H;
+        if (MX) {
+            g.ax0 = 0;
+            g.ay0 = e * I + mb * 256;  // rows of W2t: features mb*256 .. +256 of expert e
+            g.ax1 = 0;
+            g.ay1 = g.ay0 + 128;
+            g.k_steps = H / 32;
+            const int64_t kg = H / 128;
+            g.sfa0 = (int64_t)(g.ay0 / 128) * kg * 512;
+            // when I is not a multiple of 256 the last block's A1 lies past this expert
+            g.sfa1 = mb * 256 + 128 < I ? (int64_t)(g.ay1 / 128) * kg * 512 : g.sfa0;
+            g.sfb = (u / tu.n_mblocks) * kg * 512;
+        } else {
+            g.ax0 = mb * 256;
+            g.ay0 = e * H;
+            g.ax1 = g.ax0 + 128;
+            g.ay1 = e * H;
+            g.k_steps = H / 16;
+        }
         g.bx = 0;
         g.by = (int32_t)(poff[e] + (r0 - offsets[e]));
         g.n_mma = (int)((r1 - r0 + 15) & ~15);
         g.nbox = 1;
-        g.k_steps = H / 16;
         return g;
     }
     template <class LD>
@@ -410,15 +429,43 @@ struct BwdG {
                         const float sl = ag[a][j] * sig;
                         const float h = sl * au[a][j];
                         const float dh = s * g;
-                        dA[p * 2 * I + i] =
-                            f32_to_bf16(dh * au[a][j] * sig * (1.0f + ag[a][j] * (1.0f - sig)));
-                        dA[p * 2 * I + I + i] = f32_to_bf16(dh * sl);
+                        const float dag = dh * au[a][j] * sig * (1.0f + ag[a][j] * (1.0f - sig));
+                        const float dau = dh * sl;
+                        dA[p * 2 * I + i] = f32_to_bf16(dag);
+                        dA[p * 2 * I + I + i] = f32_to_bf16(dau);
                         sh[p * I + i] = f32_to_bf16(s * h);
                         gh_sum += g * h;
+                        if (MX) {
+                            // the warp's 32 lanes hold one 32-feature block of the gate
+                            // half and one of the up half of row p; the block maxima of
+                            // the magnitudes come from one integer reduction each (the bit
+                            // patterns of non-negative floats order like the floats)
+                            const float mg = __uint_as_float(__reduce_max_sync(
+                                0xFFFFFFFFu, __float_as_uint(fabsf(dag))));
+                            const float mu = __uint_as_float(__reduce_max_sync(
+                                0xFFFFFFFFu, __float_as_uint(fabsf(dau))));
+                            const uint32_t sbg = mx_scale_byte(mg), sbu = mx_scale_byte(mu);
+                            const uint32_t c2 =
+                                e4m3x2(dag * mx_inv_scale(sbg), dau * mx_inv_scale(sbu));
+                            dA_q[p * 2 * I + i] = (uint8_t)(c2 & 0xFFu);
+                            dA_q[p * 2 * I + I + i] = (uint8_t)(c2 >> 8);
+                            if (lane == 0) {
+                                dA_s[p * (2 * I / 32) + i / 32] = (uint8_t)sbg;
+                                dA_s[p * (2 * I / 32) + (I + i) / 32] = (uint8_t)sbu;
+                            }
+                        }
                     } else if (last) {  // zero pad rows up to the next multiple of 16
                         dA[p * 2 * I + i] = 0;
                         dA[p * 2 * I + I + i] = 0;
                         sh[p * I + i] = 0;
+                        if (MX) {
+                            dA_q[p * 2 * I + i] = 0;
+                            dA_q[p * 2 * I + I + i] = 0;
+                            if (lane == 0) {
+                                dA_s[p * (2 * I / 32) + i / 32] = 0;
+                                dA_s[p * (2 * I / 32) + (I + i) / 32] = 0;
+                            }
+                        }
                     }
                 }
                 es.red[j][lane] = gh_sum;
@@ -437,17 +484,19 @@ struct BwdG {
 };
 
 // backward dgrad: dx_slots[perm[r]][c] = sum_j W13[e][j][c] dA[p(r)][j]; A = W13^T
-// (MN-major: W13 rows are j).
-struct BwdDgrad {
-    static constexpr bool A_MN = true, B_MN = false, MX = false;
-    static constexpr int A_MODE = A_MN4;
+// (MN-major: W13 rows are j). MXFP8: A = W13t [E*H][2I] E4M3 (W13 quantized along 2I,
+// stored transposed: K-major), B = dA quantized along 2I.
+template <bool MXv>
+struct BwdDgradT {
+    static constexpr bool A_MN = !MXv, B_MN = false, MX = MXv;
+    static constexpr int A_MODE = MXv ? A_ROWS256 : A_MN4;
     static constexpr bool CLC = true;
-    static constexpr const uint8_t *sf_a = nullptr, *sf_b = nullptr;
     TileUnits tu;
     int H, I;
     const int32_t *offsets, *poff, *perm;
     float *dx_slots;
     int *status;
+    const uint8_t *sf_a, *sf_b;  // MXFP8: scale atoms of W13t and of the dA tiles
 
     MOK_DEV int64_t n_units() const { return tu.count(); }
     MOK_DEV Geom geom(int64_t u) const {
@@ -455,15 +504,27 @@ struct BwdDgrad {
         int64_t r0, r1;
         tu.get(u, &e, &r0, &r1, &mb);
         Geom g;
-        g.ax0 = mb * 256;
-        g.ay0 = e * 2 * I;
-        g.ax1 = g.ax0 + 128;
-        g.ay1 = e * 2 * I;
+        if (MX) {
+            g.ax0 = 0;
+            g.ay0 = e * H + mb * 256;  // rows of W13t: columns mb*256 .. +256 of expert e
+            g.ax1 = 0;
+            g.ay1 = g.ay0 + 128;
+            g.k_steps = 2 * I / 32;
+            const int64_t kg = 2 * I / 128;
+            g.sfa0 = (int64_t)(g.ay0 / 128) * kg * 512;
+            g.sfa1 = mb * 256 + 128 < H ? (int64_t)(g.ay1 / 128) * kg * 512 : g.sfa0;
+            g.sfb = (u / tu.n_mblocks) * kg * 512;
+        } else {
+            g.ax0 = mb * 256;
+            g.ay0 = e * 2 * I;
+            g.ax1 = g.ax0 + 128;
+            g.ay1 = e * 2 * I;
+            g.k_steps = 2 * I / 16;
+        }
         g.bx = 0;
         g.by = (int32_t)(poff[e] + (r0 - offsets[e]));
         g.n_mma = (int)((r1 - r0 + 15) & ~15);
         g.nbox = 1;
-        g.k_steps = 2 * I / 16;
         return g;
     }
     template <class LD>
@@ -981,7 +1042,7 @@ cudaError_t launch_gemm_up_tc_mx(const GemmUpArgs &a, int64_t ring_rows, const u
     if ((e = make_map_w13_pairs(&ma, a.w13, a.E, a.I, a.H, true)) != cudaSuccess) return e;
     if ((e = make_map_u8(&mb, a.xring, ring_rows, a.H, KBOX_ROWS)) != cudaSuccess) return e;
     FwdUpT<true> p{TileUnits{a.tiles, a.tiles_cap, a.I / 128}, a.H, a.I, a.ring, a.hring,
-                   a.hring_s, nullptr, true, a.status, sf_w, sf_x, nullptr, nullptr};
+                   a.hring_s, a.preact, true, a.status, sf_w, sf_x, nullptr, nullptr};
     return launch(ma, mb, p, a.tiles_cap * (a.I / 128),
                   (ring_rows + TILE_ROWS_MX - 1) / TILE_ROWS_MX * (a.I / 128), s);
 }
@@ -1004,11 +1065,24 @@ cudaError_t launch_gemm_g_tc(const GemmGArgs &a, int E, int64_t rpad_cap, cudaSt
     cudaError_t e = init_host();
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb;  // A: W2 as [E*H][I] read MN-major; B: dy_perm [rpad][H]
-    if ((e = make_map_bf16(&ma, a.w2, (int64_t)E * a.H, a.I, 64)) != cudaSuccess) return e;
-    if ((e = make_map_bf16(&mb, a.dy_perm, rpad_cap, a.H, KBOX_ROWS)) != cudaSuccess) return e;
+    if (!a.mxfp8) {
+        if ((e = make_map_bf16(&ma, a.w2, (int64_t)E * a.H, a.I, 64)) != cudaSuccess) return e;
+        if ((e = make_map_bf16(&mb, a.dy_perm, rpad_cap, a.H, KBOX_ROWS)) != cudaSuccess)
+            return e;
+    }
     const int nmb = (a.I + 255) / 256;
-    BwdG p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff, a.perm, a.preact,
-           a.topk_w, a.dA, a.sh, a.dS_part, 4 * nmb, a.status};
+    if (a.mxfp8) {
+        // A: W2t E4M3 [E*I][H], 256-row boxes; B: quantized dy [rpad][H]
+        if ((e = make_map_u8(&ma, a.w2t_q, (int64_t)E * a.I, a.H, 256)) != cudaSuccess) return e;
+        if ((e = make_map_u8(&mb, a.dy_q, rpad_cap, a.H, KBOX_ROWS)) != cudaSuccess) return e;
+        BwdGT<true> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff, a.perm,
+                      a.preact, a.topk_w, a.dA, a.sh, a.dS_part, 4 * nmb, a.status,
+                      a.sf_w2t, a.sf_dy, a.dA_q, a.dA_s};
+        return launch(ma, mb, p, a.tiles_cap * nmb, a.tiles_cap * nmb, s);  // static striding
+    }
+    BwdGT<false> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff, a.perm,
+                   a.preact, a.topk_w, a.dA, a.sh, a.dS_part, 4 * nmb, a.status, nullptr,
+                   nullptr, nullptr, nullptr};
     return launch(ma, mb, p, a.tiles_cap * nmb, a.tiles_cap * nmb, s);  // static striding
 }
 
@@ -1019,11 +1093,22 @@ cudaError_t launch_gemm_dgrad_tc(const GemmDgradArgs &a, int E, int64_t rpad_cap
     cudaError_t e = init_host();
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb;  // A: W13 as [E*2I][H] read MN-major; B: dA [rpad][2I]
+    const int nmb = (a.H + 255) / 256;
+    if (a.mxfp8) {
+        // A: W13t E4M3 [E*H][2I], 256-row boxes; B: quantized dA [rpad][2I]
+        if ((e = make_map_u8(&ma, a.w13t_q, (int64_t)E * a.H, 2 * a.I, 256)) != cudaSuccess)
+            return e;
+        if ((e = make_map_u8(&mb, a.dA_q, rpad_cap, 2 * a.I, KBOX_ROWS)) != cudaSuccess)
+            return e;
+        BwdDgradT<true> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff,
+                          a.perm, a.dx_slots, a.status, a.sf_w13t, a.sf_dA};
+        return launch(ma, mb, p, a.tiles_cap * nmb,
+                      (rpad_cap + TILE_ROWS_MX - 1) / TILE_ROWS_MX * nmb, s);
+    }
     if ((e = make_map_bf16(&ma, a.w13, (int64_t)E * 2 * a.I, a.H, 64)) != cudaSuccess) return e;
     if ((e = make_map_bf16(&mb, a.dA, rpad_cap, 2 * a.I, KBOX_ROWS)) != cudaSuccess) return e;
-    const int nmb = (a.H + 255) / 256;
-    BwdDgrad p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff, a.perm,
-               a.dx_slots, a.status};
+    BwdDgradT<false> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff,
+                       a.perm, a.dx_slots, a.status, nullptr, nullptr};
     return launch(ma, mb, p, a.tiles_cap * nmb, (rpad_cap + TILE_ROWS - 1) / TILE_ROWS * nmb, s);
 }
 

@@ -61,16 +61,23 @@ cudaError_t launch_gather_mxfp8(const uint16_t *x, const int32_t *perm, int K, i
                                 uint8_t *ring_s, cudaStream_t s);
 cudaError_t launch_quantize_mxfp8(const uint16_t *src, int64_t rows, int cols, uint8_t *q,
                                   uint8_t *scale, cudaStream_t s);
+// along rows, stored transposed: src [batch][rows][cols] -> q [batch][cols][rows]
+cudaError_t launch_quantize_mxfp8_transposed(const uint16_t *src, int64_t batch, int rows,
+                                             int cols, uint8_t *q, uint8_t *scale,
+                                             cudaStream_t s);
 // y[t] = sum_k w[t,k] * slots[t*K+k] in fp32 (w == nullptr: plain sum), k ascending
 cudaError_t launch_combine(const float *slots, const float *w, int64_t T, int K, int H,
                            float *y, cudaStream_t s);
 
 // backward: padded row offsets (each expert's rows rounded up to 16) and gathers
 cudaError_t launch_pad_offsets(const int32_t *counts, int E, int32_t *poff, cudaStream_t s);
+// prow (nullable) receives the padded row of every flat id; with dy_q/dy_s (MXFP8) dy is
+// also quantized along H into the padded layout
 cudaError_t launch_gather_bwd(const uint16_t *dy, const uint16_t *x, const int32_t *inv,
                               const int32_t *counts, const int32_t *offsets,
                               const int32_t *poff, int E, int64_t T, int K, int H,
-                              uint16_t *dy_perm, uint16_t *x_perm, cudaStream_t s);
+                              uint16_t *dy_perm, uint16_t *x_perm, int32_t *prow, uint8_t *dy_q,
+                              uint8_t *dy_s, cudaStream_t s);
 cudaError_t launch_router_grad(const float *dS_part, int n_parts, const int32_t *inv,
                                const int32_t *offsets, const float *w, int64_t T, int K, int E,
                                float *d_topk, float *d_logits, cudaStream_t s);
@@ -147,6 +154,11 @@ cudaError_t launch_scale_atoms_rows(const uint8_t *src, int64_t rows, int K, uin
 cudaError_t launch_scale_atoms_tiles(const int32_t *tiles, int64_t cap, const uint8_t *src,
                                      int64_t R, int MB, int n_slots, int K, uint8_t *dst,
                                      cudaStream_t s);
+// the same for the backward's padded layout: sorted row r at poff[e] + r - offsets[e]
+cudaError_t launch_scale_atoms_tiles_padded(const int32_t *tiles, int64_t cap,
+                                            const uint8_t *src, const int32_t *offsets,
+                                            const int32_t *poff, int K, uint8_t *dst,
+                                            cudaStream_t s);
 
 // Backward G GEMM with the SwiGLU backward and router-weight gradient epilogue, per tile
 // (e, r0, r1) over sorted rows; p(r) = poff[e] + r - offsets[e] is the padded row:
@@ -169,6 +181,12 @@ struct GemmGArgs {
     float *dS_part;
     int H, I;
     int *status;
+    // MXFP8 (w2 and dy_perm unused): W2 quantized along H and stored as W2t [E*I][H],
+    // dy quantized along H [rpad][H]; the scale atoms of W2t and of the dy tiles; dA also
+    // quantized along 2I into dA_q [rpad][2I] / dA_s [rpad][2I/32]
+    bool mxfp8 = false;
+    const uint8_t *w2t_q = nullptr, *sf_w2t = nullptr, *dy_q = nullptr, *sf_dy = nullptr;
+    uint8_t *dA_q = nullptr, *dA_s = nullptr;
 };
 
 // Backward dgrad GEMM with the reverse-dispatch scatter, per tile (e, r0, r1):
@@ -184,6 +202,10 @@ struct GemmDgradArgs {
     float *dx_slots;
     int H, I;
     int *status;
+    // MXFP8 (w13 and dA unused): W13 quantized along 2I and stored as W13t [E*H][2I], dA
+    // quantized along 2I [rpad][2I]; the scale atoms of W13t and of the dA tiles
+    bool mxfp8 = false;
+    const uint8_t *w13t_q = nullptr, *sf_w13t = nullptr, *dA_q = nullptr, *sf_dA = nullptr;
 };
 cudaError_t launch_gemm_g_tc(const GemmGArgs &a, int E, int64_t rpad_cap, cudaStream_t s);
 cudaError_t launch_gemm_dgrad_tc(const GemmDgradArgs &a, int E, int64_t rpad_cap,

@@ -379,7 +379,21 @@ def run_mok(args):
     fwd_shared()
     ms_s = timed(fwd_shared, args.steps)
     phases["fwd_shared_bf16"] = {"ms": ms_s, "tflops": 6.0 * T * H * I / (ms_s * 1e-3) / 1e12}
-    del S, w13s, w2s
+
+    # and its backward (dx += its input gradient, its weight gradients), after a forward
+    # that saved its pre-activations
+    pre_s = torch.empty(T, 2 * I, dtype=torch.float32, device=dev)
+    dw13s = torch.empty(2 * I, H, dtype=torch.float32, device=dev)
+    dw2s = torch.empty(H, I, dtype=torch.float32, device=dev)
+    S.forward(x, w13s, w2s, y, saved_preact=pre_s, stream=stream)
+
+    def bwd_shared():
+        S.backward(x, w13s, w2s, pre_s, dy, dx, dw13s, dw2s, stream=stream)
+    bwd_shared()
+    ms_sb = timed(bwd_shared, args.steps)
+    phases["bwd_shared_bf16"] = {"ms": ms_sb,
+                                 "tflops": 12.0 * T * H * I / (ms_sb * 1e-3) / 1e12}
+    del S, w13s, w2s, pre_s, dw13s, dw2s
 
     # the imbalanced workload's forward (Zipf-skewed routing, 65536 tokens, a ring of 2960
     # rows, so many passes): eager, and replayed from a captured CUDA graph

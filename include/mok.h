@@ -67,7 +67,8 @@ typedef enum mok_workspace_kind {
     MOK_WS_FORWARD = 1,
     MOK_WS_BACKWARD = 2,
     MOK_WS_BACKWARD_RECOMPUTE = 3, /* backward without saved pre-activations */
-    MOK_WS_SHARED = 4              /* shared-expert forward */
+    MOK_WS_SHARED = 4,             /* shared-expert forward */
+    MOK_WS_SHARED_BACKWARD = 5     /* shared-expert backward */
 } mok_workspace_kind;
 
 /* Layer configuration. minibatch and ring_capacity are two of the pages' tunables
@@ -249,6 +250,24 @@ mok_status mok_backward_mxfp8(const mok_config *cfg, const void *x, const mok_sc
 mok_status mok_shared_expert_forward(const mok_config *cfg, const void *x, const void *w13_s,
                                      const void *w2_s, void *y, void *saved_preact_s, void *ws,
                                      size_t ws_bytes, cudaStream_t stream);
+
+/* Shared expert, backward: the gradients of y += W2s (silu(W13s[0:I] x) * W13s[I:2I] x)
+ * for every token, by the chain rule of mok_backward with one expert, weight one and no
+ * router gradient ([alphalab] section 一: the backward's expert gradient computation):
+ *   dx[t] += W13s^T dA_t                                    (fp32 add after the routed dx)
+ *   dw13_s = sum_t dA_t x_t^T, dw2_s = sum_t dy_t h_t^T      (sums over t ascending)
+ * with G = W2s^T dy_t, dA = (G * u * silu'(g), G * silu(g)) from the saved gate/up result
+ * (g, u), and dA and h rounded to bf16 where they enter GEMMs, as in mok_backward.
+ *   x, w13_s, w2_s as for mok_shared_expert_forward; saved_preact_s [T][2I] fp32 from it
+ *   (required); dy [T][H] bf16.
+ *   dx      [T][H] fp32, in and out (typically mok_backward's result).
+ *   dw13_s  [2I][H] fp32 out; dw2_s [H][I] fp32 out.
+ *   ws      at least mok_workspace_size(cfg, MOK_WS_SHARED_BACKWARD) bytes.
+ * BF16 only (else MOK_ERR_UNSUPPORTED). Asynchronous on `stream`. */
+mok_status mok_shared_expert_backward(const mok_config *cfg, const void *x, const void *w13_s,
+                                      const void *w2_s, const void *saved_preact_s,
+                                      const void *dy, void *dx, void *dw13_s, void *dw2_s,
+                                      void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /* MXFP8 quantization of a bf16 matrix along its rows ([arex] section "pull 代替 push":
  * pre-quantized weights). src [rows][cols] bf16 -> q [rows][cols] E4M3, scale

@@ -34,6 +34,7 @@ MOK_WS_FORWARD = 1
 MOK_WS_BACKWARD = 2
 MOK_WS_BACKWARD_RECOMPUTE = 3
 MOK_WS_SHARED = 4
+MOK_WS_SHARED_BACKWARD = 5
 
 EXPORTED = [
     "mok_abi_version", "mok_status_string", "mok_check_config", "mok_segment_capacity",
@@ -41,7 +42,7 @@ EXPORTED = [
     "mok_backward", "mok_quantize_mxfp8", "mok_read_device_status",
     "mok_clear_device_status", "mok_profile_enable", "mok_profile_read",
     "mok_build_schedule_noalloc", "mok_shared_expert_forward",
-    "mok_quantize_mxfp8_transposed", "mok_backward_mxfp8",
+    "mok_quantize_mxfp8_transposed", "mok_backward_mxfp8", "mok_shared_expert_backward",
 ]
 
 # bytes of the fixed scratch array behind mok_build_schedule_noalloc
@@ -95,6 +96,8 @@ def lib():
             "mok_backward": ([cfgp, p, schp, p, p, p, p, p, p, p, p, p, p, p, sz, p],
                              ctypes.c_int),
             "mok_shared_expert_forward": ([cfgp, p, p, p, p, p, p, sz, p], ctypes.c_int),
+            "mok_shared_expert_backward": ([cfgp, p, p, p, p, p, p, p, p, p, sz, p],
+                                           ctypes.c_int),
             "mok_backward_mxfp8": ([cfgp, p, schp, p, p, p, p, p, p, p, p, p, p, p, p, p, sz,
                                     p], ctypes.c_int),
             "mok_quantize_mxfp8": ([p, i64, i32, p, p, p], ctypes.c_int),
@@ -215,6 +218,14 @@ def mok_backward_mxfp8(cfg, x, sched, topk_w, saved_preact, w13t_q, w13t_s, w2t_
                                     _ptr(w13t_s), _ptr(w2t_q), _ptr(w2t_s), _ptr(dy), _ptr(dx),
                                     _ptr(dw13), _ptr(dw2), _ptr(d_topk_w), _ptr(d_logits),
                                     _ptr(ws), int(ws_bytes), _stream(stream))
+
+
+def mok_shared_expert_backward(cfg, x, w13_s, w2_s, saved_preact_s, dy, dx, dw13_s, dw2_s, ws,
+                               ws_bytes, stream=None) -> int:
+    return lib().mok_shared_expert_backward(ctypes.byref(cfg), _ptr(x), _ptr(w13_s),
+                                            _ptr(w2_s), _ptr(saved_preact_s), _ptr(dy),
+                                            _ptr(dx), _ptr(dw13_s), _ptr(dw2_s), _ptr(ws),
+                                            int(ws_bytes), _stream(stream))
 
 
 def mok_quantize_mxfp8(src, rows, cols, q, scale, stream=None) -> int:

@@ -115,6 +115,16 @@ class SharedExpert:
                                             self.ws, self.ws_n, stream), "shared forward")
         return y
 
+    def backward(self, x, w13_s, w2_s, saved_preact, dy, dx, dw13_s, dw2_s, stream=None):
+        """dx += the shared expert's input gradient; dw13_s, dw2_s = its weight gradients."""
+        if getattr(self, "ws_b", None) is None:
+            self.ws_b, self.ws_b_n = workspace(self.cfg, B.MOK_WS_SHARED_BACKWARD,
+                                               x.device)
+        B.check(B.mok_shared_expert_backward(self.cfg, x, w13_s, w2_s, saved_preact, dy, dx,
+                                             dw13_s, dw2_s, self.ws_b, self.ws_b_n, stream),
+                "shared backward")
+        return dx
+
 
 def quantize_mxfp8_transposed(src, stream=None):
     """MXFP8 of a [batch][rows][cols] bf16 tensor along rows, stored as [batch][cols][rows]

@@ -176,6 +176,37 @@ size_t carve_shared(const mok_config *c, void *ws, SharedWs *o) {
     return cv.off;
 }
 
+// shared-expert backward: the single expert's offsets, padded offsets, count, weights of
+// one and identity row map; its tile list; dA [Tpad][2I], h [Tpad][I] (bf16, rows past T
+// zero) and the G epilogue's (unused) router-gradient partials
+struct SharedBwdWs {
+    int32_t *offsets, *poff, *counts, *perm;
+    float *ones;
+    int32_t *tiles;
+    int64_t tiles_cap, tpad;
+    uint16_t *dA, *sh;
+    float *dS_part;
+};
+
+size_t carve_shared_bwd(const mok_config *c, void *ws, SharedBwdWs *o) {
+    Carver cv{(char *)ws};
+    SharedBwdWs w;
+    w.tpad = ((int64_t)c->T + 15) & ~(int64_t)15;
+    w.offsets = cv.take<int32_t>(2 * 4);
+    w.poff = cv.take<int32_t>(2 * 4);
+    w.counts = cv.take<int32_t>(4);
+    w.perm = cv.take<int32_t>((size_t)c->T * 4 + 4);
+    w.ones = cv.take<float>((size_t)c->T * 4 + 4);
+    w.tiles_cap = tile_list_cap(c->T, 1, gemm_tc_tile_rows(false));
+    int32_t *t = cv.take<int32_t>(16 + (size_t)w.tiles_cap * 16);
+    w.tiles = t ? t + 4 : nullptr;
+    w.dA = cv.take<uint16_t>((size_t)(w.tpad * 2 * c->I * 2));
+    w.sh = cv.take<uint16_t>((size_t)(w.tpad * c->I * 2));
+    w.dS_part = cv.take<float>((size_t)c->T * gemm_tc_dS_parts(c->I) * 4 + 4);
+    if (o) *o = w;
+    return cv.off;
+}
+
 cudaError_t first_error(cudaError_t a, cudaError_t b) { return a != cudaSuccess ? a : b; }
 
 mok_status check_ws(void *ws, size_t ws_bytes, size_t need) {
@@ -258,6 +289,7 @@ size_t mok_workspace_size(const mok_config *c, int which) {
         case MOK_WS_FORWARD: return carve_fwd(c, nullptr, nullptr);
         case MOK_WS_BACKWARD_RECOMPUTE: return carve_bwd(c, nullptr, nullptr, true);
         case MOK_WS_SHARED: return carve_shared(c, nullptr, nullptr);
+        case MOK_WS_SHARED_BACKWARD: return carve_shared_bwd(c, nullptr, nullptr);
         case MOK_WS_BACKWARD: return carve_bwd(c, nullptr, nullptr);
     }
     return 0;
@@ -473,11 +505,11 @@ mok_status backward_impl(const mok_config *c, const void *x, const mok_schedule 
     // dW13[e] is [2I][H]: rows j (N) x contiguous c (M)
     MOK_LAUNCH(KK_WGRAD13, 1,
                launch_wgrad_tc(sch->counts, w.poff, w.x_perm, w.dA, (float *)dw13, E, H, 2 * I,
-                               w.rpad_cap, status, stream));
+                               w.rpad_cap, w.rpad_cap, status, stream));
     // dW2[e] is [H][I]: rows c (N) x contiguous i (M)
     MOK_LAUNCH(KK_WGRAD2, 1,
                launch_wgrad_tc(sch->counts, w.poff, w.sh, w.dy_perm, (float *)dw2, E, I, H,
-                               w.rpad_cap, status, stream));
+                               w.rpad_cap, w.rpad_cap, status, stream));
     return MOK_OK;
 }
 }  // namespace mok
@@ -533,6 +565,53 @@ mok_status mok_shared_expert_forward(const mok_config *c, const void *x, const v
     GemmDownArgs da{w.tiles, w.tiles_cap, w.h, nullptr, w2_s, nullptr, nullptr, (float *)y,
                     c->H, c->I, 1, false, ring, status, true};
     MOK_LAUNCH(KK_SHARED_DOWN, 1, launch_gemm_down_tc(da, c->T, stream));
+    return MOK_OK;
+}
+
+mok_status mok_shared_expert_backward(const mok_config *c, const void *x, const void *w13_s,
+                                      const void *w2_s, const void *saved_preact_s,
+                                      const void *dy, void *dx, void *dw13_s, void *dw2_s,
+                                      void *ws, size_t ws_bytes, cudaStream_t stream) {
+    mok_status st = mok_check_config(c);
+    if (st != MOK_OK) return st;
+    int *status;
+    if ((st = check_device(&status)) != MOK_OK) return st;
+    if (c->prec != MOK_BF16) return MOK_ERR_UNSUPPORTED;
+    if (!x || !w13_s || !w2_s || !saved_preact_s || !dy || !dx || !dw13_s || !dw2_s)
+        return MOK_ERR_INVALID_ARG;
+    const void *ps[] = {x, w13_s, w2_s, saved_preact_s, dy, dx, dw13_s, dw2_s};
+    for (const void *p : ps)
+        if (!aligned16(p)) return MOK_ERR_INVALID_ARG;
+    const size_t need = carve_shared_bwd(c, nullptr, nullptr);
+    if ((st = check_ws(ws, ws_bytes, need)) != MOK_OK) return st;
+    SharedBwdWs w;
+    carve_shared_bwd(c, ws, &w);
+    const int64_t T = c->T;
+    const int H = c->H, I = c->I;
+    // one expert owning every token in token order, weight one: x and dy are read directly
+    MOK_LAUNCH(KK_SHARED_BWD, 2,
+               first_error(launch_single_expert_bwd_setup(w.offsets, w.poff, w.counts, w.ones,
+                                                          w.perm, T, stream),
+                           launch_build_tiles(w.offsets, 1, 0, T, gemm_tc_tile_rows(false),
+                                              w.tiles, w.tiles_cap, status, stream)));
+    if (T > 0) {
+        GemmGArgs ga{w.tiles, w.tiles_cap, w.offsets, w.poff, (const uint16_t *)w2_s,
+                     (const uint16_t *)dy, (const float *)saved_preact_s, w.perm, w.ones, w.dA,
+                     w.sh, w.dS_part, H, I, status};
+        MOK_LAUNCH(KK_SHARED_BWD, 1, launch_gemm_g_tc(ga, 1, T, stream));  // dy: T rows
+        GemmDgradArgs dg{w.tiles, w.tiles_cap, w.offsets, w.poff, (const uint16_t *)w13_s,
+                         w.dA, w.perm, (float *)dx, H, I, status};
+        dg.accumulate = true;
+        MOK_LAUNCH(KK_SHARED_BWD, 1, launch_gemm_dgrad_tc(dg, 1, w.tpad, stream));
+    }
+    // the weight gradients' K runs over the padded rows: x and dy rows past T read zeros
+    MOK_LAUNCH(KK_SHARED_BWD, 2,
+               first_error(launch_wgrad_tc(w.counts, w.poff, (const uint16_t *)x, w.dA,
+                                           (float *)dw13_s, 1, H, 2 * I, T > 0 ? T : 1,
+                                           w.tpad > 0 ? w.tpad : 1, status, stream),
+                           launch_wgrad_tc(w.counts, w.poff, w.sh, (const uint16_t *)dy,
+                                           (float *)dw2_s, 1, I, H, w.tpad > 0 ? w.tpad : 1,
+                                           T > 0 ? T : 1, status, stream)));
     return MOK_OK;
 }
 

@@ -482,6 +482,32 @@ cudaError_t launch_single_expert_offsets(int32_t *off, int64_t rows, cudaStream_
     return cudaGetLastError();
 }
 
+__global__ void __launch_bounds__(TPB)
+    single_expert_bwd_setup_kernel(int32_t *offsets, int32_t *poff, int32_t *counts,
+                                   float *ones, int32_t *perm, int64_t T) {
+    const int64_t i = (int64_t)blockIdx.x * TPB + threadIdx.x;
+    if (i < T) {
+        ones[i] = 1.0f;
+        perm[i] = (int32_t)i;
+    }
+    if (i == 0) {
+        offsets[0] = 0;
+        offsets[1] = (int32_t)T;
+        poff[0] = 0;
+        poff[1] = (int32_t)((T + 15) & ~(int64_t)15);
+        counts[0] = (int32_t)T;
+    }
+}
+
+cudaError_t launch_single_expert_bwd_setup(int32_t *offsets, int32_t *poff, int32_t *counts,
+                                           float *ones, int32_t *perm, int64_t T,
+                                           cudaStream_t s) {
+    single_expert_bwd_setup_kernel<<<(unsigned)((T + TPB - 1) / TPB > 0 ? (T + TPB - 1) / TPB
+                                                                          : 1),
+                                     TPB, 0, s>>>(offsets, poff, counts, ones, perm, T);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gather_tok_bf16(const uint16_t *x, const int32_t *inv, int64_t T, int K,
                                    int H, uint16_t *ring, cudaStream_t s) {
     if (T == 0) return cudaSuccess;

@@ -497,6 +497,7 @@ struct BwdDgradT {
     float *dx_slots;
     int *status;
     const uint8_t *sf_a, *sf_b;  // MXFP8: scale atoms of W13t and of the dA tiles
+    bool accumulate;             // add into the output rows (the shared expert adds into dx)
 
     MOK_DEV int64_t n_units() const { return tu.count(); }
     MOK_DEV Geom geom(int64_t u) const {
@@ -539,16 +540,32 @@ struct BwdDgradT {
         int *fcol = reinterpret_cast<int *>(es.col);  // slot of each column
         for (int n = lane; n < nr; n += 32) fcol[n] = perm[r0 + n];
         __syncwarp();
+        const bool has1 = c + 128 < H;
         for (int n0 = 16 * half; n0 < n_mma; n0 += 32) {
             float d0[16], d1[16];
             ld(n0, d0, d1);
+            if (accumulate) {  // every load of the chunk before any store (see FwdDownT)
+                float a0[16], a1[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const bool ok = n0 + j < nr;
+                    const float *o = dx_slots + (int64_t)fcol[ok ? n0 + j : 0] * H + c;
+                    a0[j] = ok ? o[0] : 0.f;
+                    a1[j] = ok && has1 ? o[128] : 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    d0[j] += a0[j];
+                    d1[j] += a1[j];
+                }
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int n = n0 + j;
                 if (n < nr) {
                     const int64_t f = fcol[n];
                     dx_slots[f * H + c] = d0[j];
-                    if (c + 128 < H) dx_slots[f * H + c + 128] = d1[j];
+                    if (has1) dx_slots[f * H + c + 128] = d1[j];
                 }
             }
         }
@@ -1101,26 +1118,26 @@ cudaError_t launch_gemm_dgrad_tc(const GemmDgradArgs &a, int E, int64_t rpad_cap
         if ((e = make_map_u8(&mb, a.dA_q, rpad_cap, 2 * a.I, KBOX_ROWS)) != cudaSuccess)
             return e;
         BwdDgradT<true> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff,
-                          a.perm, a.dx_slots, a.status, a.sf_w13t, a.sf_dA};
+                          a.perm, a.dx_slots, a.status, a.sf_w13t, a.sf_dA, a.accumulate};
         return launch(ma, mb, p, a.tiles_cap * nmb,
                       (rpad_cap + TILE_ROWS_MX - 1) / TILE_ROWS_MX * nmb, s);
     }
     if ((e = make_map_bf16(&ma, a.w13, (int64_t)E * 2 * a.I, a.H, 64)) != cudaSuccess) return e;
     if ((e = make_map_bf16(&mb, a.dA, rpad_cap, 2 * a.I, KBOX_ROWS)) != cudaSuccess) return e;
     BwdDgradT<false> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff,
-                       a.perm, a.dx_slots, a.status, nullptr, nullptr};
+                       a.perm, a.dx_slots, a.status, nullptr, nullptr, a.accumulate};
     return launch(ma, mb, p, a.tiles_cap * nmb, (rpad_cap + TILE_ROWS - 1) / TILE_ROWS * nmb, s);
 }
 
 // out [E][N][M] = per expert sum over padded rows of A[p][m] B[p][n]
 cudaError_t launch_wgrad_tc(const int32_t *counts, const int32_t *poff, const uint16_t *A,
                             const uint16_t *Bm, float *out, int E, int M, int N,
-                            int64_t rpad_cap, int *status, cudaStream_t s) {
+                            int64_t rows_a, int64_t rows_b, int *status, cudaStream_t s) {
     cudaError_t e = init_host();
     if (e != cudaSuccess) return e;
-    CUtensorMap ma, mb;
-    if ((e = make_map_bf16(&ma, A, rpad_cap, M, 64)) != cudaSuccess) return e;
-    if ((e = make_map_bf16(&mb, Bm, rpad_cap, N, 64)) != cudaSuccess) return e;
+    CUtensorMap ma, mb;  // rows past an operand's own rows read the copy engine's zero fill
+    if ((e = make_map_bf16(&ma, A, rows_a, M, 64)) != cudaSuccess) return e;
+    if ((e = make_map_bf16(&mb, Bm, rows_b, N, 64)) != cudaSuccess) return e;
     const int nmb = (M + 255) / 256, nnb = (N + TILE_ROWS - 1) / TILE_ROWS;
     Wgrad p{counts, poff, out, E, M, N, nmb, nnb, status};
     return launch(ma, mb, p, (int64_t)E * nmb * nnb, (int64_t)E * nmb * nnb, s);  // exact

@@ -13,7 +13,7 @@ enum KernelKind {
     KK_ROUTE = 0, KK_SCHEDULE, KK_TILES, KK_GATHER, KK_GEMM_UP, KK_GEMM_DOWN, KK_COMBINE,
     KK_QUANTIZE, KK_PAD, KK_GATHER_BWD, KK_GEMM_G, KK_ROUTER_GRAD, KK_GEMM_DGRAD,
     KK_DX_REDUCE, KK_WGRAD13, KK_WGRAD2, KK_SCALE_ATOMS, KK_SHARED_UP, KK_SHARED_DOWN,
-    KK_COUNT
+    KK_SHARED_BWD, KK_COUNT
 };
 // while profiling is on: brackets the launches between begin and end with events
 void prof_begin(int kind, cudaStream_t s);
@@ -51,6 +51,11 @@ cudaError_t launch_gather_bf16(const uint16_t *x, const int32_t *perm, int K, in
                                cudaStream_t s);
 // offsets of a single expert owning rows [0, rows): off[0] = 0, off[1] = rows
 cudaError_t launch_single_expert_offsets(int32_t *off, int64_t rows, cudaStream_t s);
+// the backward's view of a single expert owning every token in token order: offsets
+// [0, T], padded offsets [0, T rounded up to 16], counts [T], weight one and row r -> r
+cudaError_t launch_single_expert_bwd_setup(int32_t *offsets, int32_t *poff, int32_t *counts,
+                                           float *ones, int32_t *perm, int64_t T,
+                                           cudaStream_t s);
 // token-major gathers, for a ring that holds every row: ring[inv[t*K + k]] = x[t]
 cudaError_t launch_gather_tok_bf16(const uint16_t *x, const int32_t *inv, int64_t T, int K,
                                    int H, uint16_t *ring, cudaStream_t s);
@@ -206,13 +211,14 @@ struct GemmDgradArgs {
     // quantized along 2I [rpad][2I]; the scale atoms of W13t and of the dA tiles
     bool mxfp8 = false;
     const uint8_t *w13t_q = nullptr, *sf_w13t = nullptr, *dA_q = nullptr, *sf_dA = nullptr;
+    bool accumulate = false;  // add into the output rows (the shared expert adds into dx)
 };
 cudaError_t launch_gemm_g_tc(const GemmGArgs &a, int E, int64_t rpad_cap, cudaStream_t s);
 cudaError_t launch_gemm_dgrad_tc(const GemmDgradArgs &a, int E, int64_t rpad_cap,
                                  cudaStream_t s);
 // out [E][N][M] = per expert e, sum over its padded rows p of A[p][m] * B[p][n]
 cudaError_t launch_wgrad_tc(const int32_t *counts, const int32_t *poff, const uint16_t *A,
-                            const uint16_t *B, float *out, int E, int M, int N,
-                            int64_t rpad_cap, int *status, cudaStream_t s);
+                            const uint16_t *Bm, float *out, int E, int M, int N,
+                            int64_t rows_a, int64_t rows_b, int *status, cudaStream_t s);
 
 }  // namespace mok

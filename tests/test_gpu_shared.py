@@ -131,3 +131,62 @@ def test_mxfp8_config_is_unsupported():
     y = torch.zeros(64, 128, dtype=torch.float32, device="cuda")
     st = B.mok_shared_expert_forward(L.cfg, x, w13s, w2s, y, None, ws, ws.numel())
     assert st == B.MOK_ERR_UNSUPPORTED
+
+
+def gpu_step_with_shared(dims, x, logits, w13, w2, w13s, w2s, dy, MB=2368):
+    """Routed forward + shared forward, then routed backward + shared backward (which adds
+    into dx); returns dx after the routed part, dx in total, the shared weight gradients."""
+    import torch
+    T, H, I, E, K = dims
+    L = MoELayer(T, H, I, E, K, MB, 0, B.MOK_BF16, backward=True)
+    S = SharedExpert(L)
+    xd, dyd = to_dev(x), to_dev(dy)
+    w13d, w2d, w13sd, w2sd = to_dev(w13), to_dev(w2), to_dev(w13s), to_dev(w2s)
+    L.route(to_dev(logits))
+    L.schedule()
+    R = T * K
+    f32 = dict(dtype=torch.float32, device="cuda")
+    pre, pre_s = torch.empty(R, 2 * I, **f32), torch.empty(T, 2 * I, **f32)
+    y = torch.empty(T, H, **f32)
+    L.forward(xd, w13d, w2d, y, saved_preact=pre)
+    S.forward(xd, w13sd, w2sd, y, saved_preact=pre_s)
+    dx = torch.empty(T, H, **f32)
+    dw13, dw2 = torch.empty(E, 2 * I, H, **f32), torch.empty(E, H, I, **f32)
+    dtk = torch.empty(R, **f32)
+    L.backward(xd, pre, w13d, w2d, dyd, dx, dw13, dw2, dtk)
+    dx_routed = dx.clone()
+    dw13s, dw2s = torch.empty(2 * I, H, **f32), torch.empty(H, I, **f32)
+    S.backward(xd, w13sd, w2sd, pre_s, dyd, dx, dw13s, dw2s)
+    torch.cuda.synchronize()
+    st, dev = B.mok_read_device_status()
+    assert st == B.MOK_OK and dev == B.MOK_OK
+    idx = L.idx[:R].view(T, K).cpu().numpy()
+    w = L.w[:R].view(T, K).cpu().numpy().astype(np.float64)
+    return (dx_routed.cpu().numpy(), dx.cpu().numpy(), dw13s.cpu().numpy(),
+            dw2s.cpu().numpy(), idx, w)
+
+
+@pytest.mark.parametrize("dims", [(256, 256, 128, 8, 2), (300, 256, 128, 8, 2),
+                                  (517, 384, 256, 16, 4)])
+def test_backward_with_shared_expert(dims):
+    T, H, I, E, K = dims
+    r = np.random.default_rng(T + 2)
+    x = f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
+    lg = r.standard_normal((T, E)).astype(np.float32)
+    w13 = f32_to_bf16_bits((r.standard_normal((E, 2 * I, H)) * 0.05).astype(np.float32))
+    w2 = f32_to_bf16_bits((r.standard_normal((E, H, I)) * 0.05).astype(np.float32))
+    dy = f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
+    w13s, w2s = shared_weights(H, I, T + 3, 0.05)
+    dx_r, dx, dw13s, dw2s, idx, w = gpu_step_with_shared(dims, x, lg, w13, w2, w13s, w2s, dy)
+    xf, dyf = oracle.bf16_to_f64(x), oracle.bf16_to_f64(dy)
+    dx_ro, _, _, _, sdx_r, _, _ = oracle.backward(xf, idx, w, w13, w2, dyf, weight_grads=False,
+                                                  mode=oracle.BF16, with_slack=True)
+    # the shared expert: one expert, top-1 routing at weight one
+    dx_so, dw13_so, dw2_so, _, sdx_s, s13, s2 = oracle.backward(
+        xf, np.zeros((T, 1), np.int32), np.ones((T, 1)), w13s[None], w2s[None], dyf,
+        mode=oracle.BF16, with_slack=True)
+    assert rel_err(dx_r, dx_ro, sdx_r) <= TOL_BF16
+    assert rel_err(dx, dx_ro + dx_so, sdx_r + sdx_s) <= TOL_BF16
+    assert rel_err(dx - dx_r, dx_so, sdx_s) <= TOL_BF16
+    assert rel_err(dw13s, dw13_so[0], s13[0]) <= TOL_BF16
+    assert rel_err(dw2s, dw2_so[0], s2[0]) <= TOL_BF16

@@ -6,7 +6,10 @@
 // One warp per token. Each logit becomes a 64-bit key: an order-preserving image of the
 // fp32 value (with -0 folded onto +0) in the high half and (2^32-1 - expert) in the low
 // half, so the unsigned maximum is the largest logit and, among equal logits, the lowest
-// expert id. K rounds of a warp-wide maximum pick the experts in descending order.
+// expert id. Each lane keeps the maximum of its own keys; K rounds of a warp-wide maximum
+// over those pick the experts in descending order, and only the lane that owned the
+// winner retires it and rescans its keys. The chosen logit is read back from the key
+// (the image inverts; -0 comes back as +0, which has the same exponential).
 // HBM-bound: T*E*4 bytes read, T*K*8 bytes written.
 #include "common.cuh"
 #include "mok_internal.h"
@@ -19,6 +22,11 @@ MOK_DEV uint64_t logit_key(float v, uint32_t e) {
     if (u == 0x80000000u) u = 0u;  // -0 ties with +0
     const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
     return ((uint64_t)ord << 32) | (uint64_t)(0xFFFFFFFFu - e);
+}
+
+MOK_DEV float key_logit(uint64_t key) {
+    const uint32_t ord = (uint32_t)(key >> 32);
+    return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
 }
 
 MOK_DEV uint64_t warp_max_u64(uint64_t v) {
@@ -50,17 +58,22 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict
         float sel_logit = 0.f;  // lane k keeps the k-th chosen logit
         int sel_e = 0;
         float first = 0.f;
+        uint64_t mine = 0ull;  // this lane's largest remaining key
+#pragma unroll
+        for (int j = 0; j < PER; ++j) mine = key[j] > mine ? key[j] : mine;
         for (int k = 0; k < K; ++k) {
-            uint64_t best = 0ull;
-#pragma unroll
-            for (int j = 0; j < PER; ++j) best = key[j] > best ? key[j] : best;
-            best = warp_max_u64(best);
+            const uint64_t best = warp_max_u64(mine);
             const uint32_t e = 0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull);
-            // the owning lane retires the key; keys are unique, so exactly one matches
+            // keys are unique: exactly one lane owns the winner; it retires it and rescans
+            if (mine == best) {
+                mine = 0ull;
 #pragma unroll
-            for (int j = 0; j < PER; ++j)
-                if (key[j] == best) key[j] = 0ull;
-            const float lv = __ldg(row + e);
+                for (int j = 0; j < PER; ++j) {
+                    if (key[j] == best) key[j] = 0ull;
+                    mine = key[j] > mine ? key[j] : mine;
+                }
+            }
+            const float lv = key_logit(best);
             if (k == 0) first = lv;
             if (lane == k) {
                 sel_logit = lv;

@@ -142,3 +142,45 @@ def test_full_size_sampled():
             oracle.bf16_to_f64(d["dy"][t_e]), mode=oracle.MXFP8, with_slack=True)
         assert rel_err(host(g["dw13"][e]), dw13_o[0], s13[0]) <= TOL_MXFP8
         assert rel_err(host(g["dw2"][e]), dw2_o[0], s2[0]) <= TOL_MXFP8
+
+
+def test_argument_errors_are_reported():
+    import torch
+    T, H, I, E, K = 64, 128, 128, 4, 2
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    f32 = dict(dtype=torch.float32, device="cuda")
+    x = torch.zeros(T, H, dtype=torch.bfloat16, device="cuda")
+    dy = torch.zeros_like(x)
+    w13t = (torch.zeros(E, H, 2 * I, **u8), torch.zeros(E, H, 2 * I // 32, **u8))
+    w2t = (torch.zeros(E, I, H, **u8), torch.zeros(E, I, H // 32, **u8))
+    dx = torch.zeros(T, H, **f32)
+    dw13, dw2 = torch.zeros(E, 2 * I, H, **f32), torch.zeros(E, H, I, **f32)
+    dtk = torch.zeros(T * K, **f32)
+    pre = torch.zeros(T * K, 2 * I, **f32)
+    for prec, saved, want in ((B.MOK_MXFP8, None, B.MOK_ERR_INVALID_ARG),   # A is required
+                              (B.MOK_BF16, pre, B.MOK_ERR_INVALID_ARG)):    # not an MXFP8 layer
+        L = MoELayer(T, H, I, E, K, 64, 0, prec, backward=True)
+        L.route(torch.zeros(T, E, **f32))
+        L.schedule()
+        st = B.mok_backward_mxfp8(L.cfg, x, L.sched.struct, L.w, saved, w13t[0], w13t[1],
+                                  w2t[0], w2t[1], dy, dx, dw13, dw2, dtk, None, L.ws_b,
+                                  L.ws_b_n)
+        assert st == want, (prec, st)
+    # the shared expert's backward is BF16 only
+    Lm = MoELayer(T, H, I, E, K, 64, 0, B.MOK_MXFP8)
+    ws = torch.empty(max(1, B.mok_workspace_size(Lm.cfg, B.MOK_WS_SHARED_BACKWARD)), **u8)
+    st = B.mok_shared_expert_backward(Lm.cfg, x, torch.zeros(2 * I, H, dtype=torch.bfloat16,
+                                                             device="cuda"),
+                                      torch.zeros(H, I, dtype=torch.bfloat16, device="cuda"),
+                                      torch.zeros(T, 2 * I, **f32), dy, dx,
+                                      torch.zeros(2 * I, H, **f32), torch.zeros(H, I, **f32),
+                                      ws, ws.numel())
+    assert st == B.MOK_ERR_UNSUPPORTED
+    # rows of a transposed quantization come in blocks of 32
+    st = B.mok_quantize_mxfp8_transposed(torch.zeros(1, 48, 64, dtype=torch.bfloat16,
+                                                     device="cuda"), 1, 48, 64,
+                                         torch.zeros(64 * 48, **u8), torch.zeros(64 * 2, **u8))
+    assert st == B.MOK_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    st, dev = B.mok_read_device_status()
+    assert st == B.MOK_OK and dev == B.MOK_OK

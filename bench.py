@@ -415,6 +415,20 @@ def run_mok(args):
         ms_m = timed(fwd_mx, args.steps)
         phases["fwd_mxfp8"] = {"ms": ms_m, "tflops": cfg.fwd_flops() / (ms_m * 1e-3) / 1e12}
 
+        # the shared expert's MXFP8 forward on weights quantized once (untimed), added into y
+        from mixture_experts_layer_deterministic_gb300.buffers import SharedExpert
+        Sm = SharedExpert(Lm)
+        ws13 = quantize_mxfp8((torch.randn(2 * I, H, device=dev) * cfg.w_std).to(torch.bfloat16))
+        ws2 = quantize_mxfp8((torch.randn(H, I, device=dev) * cfg.w_std).to(torch.bfloat16))
+
+        def fwd_shared_mx():
+            Sm.forward(x, ws13, ws2, y, stream=stream)
+        fwd_shared_mx()
+        ms_sm = timed(fwd_shared_mx, args.steps)
+        phases["fwd_shared_mxfp8"] = {"ms": ms_sm,
+                                      "tflops": 6.0 * T * H * I / (ms_sm * 1e-3) / 1e12}
+        del Sm, ws13, ws2
+
         # MXFP8 backward (G and dgrad in MXFP8 on weights pre-quantized along their
         # contraction axes, untimed like the forward's; weight gradients BF16), after an
         # MXFP8 forward that saved its pre-activations

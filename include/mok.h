@@ -246,10 +246,24 @@ mok_status mok_backward_mxfp8(const mok_config *cfg, const void *x, const mok_sc
  *   y              [T][H] fp32, in and out (typically mok_forward's result).
  *   saved_preact_s NULL, or [T][2I] fp32 out: the shared expert's gate/up GEMM result.
  *   ws             at least mok_workspace_size(cfg, MOK_WS_SHARED) bytes.
- * BF16 only (cfg->prec == MOK_BF16, else MOK_ERR_UNSUPPORTED). Asynchronous on `stream`. */
+ * BF16 (cfg->prec == MOK_BF16, else MOK_ERR_UNSUPPORTED; MXFP8 configurations use
+ * mok_shared_expert_forward_mxfp8). Asynchronous on `stream`. */
 mok_status mok_shared_expert_forward(const mok_config *cfg, const void *x, const void *w13_s,
                                      const void *w2_s, void *y, void *saved_preact_s, void *ws,
                                      size_t ws_bytes, cudaStream_t stream);
+
+/* Shared expert, forward, MXFP8 (cfg->prec == MOK_MXFP8): as mok_shared_expert_forward with
+ * the MXFP8 mode's operands ([arex] section "pull 代替 push"): x quantized along H, h along
+ * I inside the gate/up GEMM's epilogue, pre-quantized weights.
+ *   w13s_q [2I][H] E4M3 with w13s_scale [2I][H/32], w2s_q [H][I] E4M3 with w2s_scale
+ *   [H][I/32] (as made by mok_quantize_mxfp8 from the bf16 shared weights).
+ *   Other arguments as for mok_shared_expert_forward; ws at least
+ *   mok_workspace_size(cfg, MOK_WS_SHARED) for this (MXFP8) configuration. */
+mok_status mok_shared_expert_forward_mxfp8(const mok_config *cfg, const void *x,
+                                           const uint8_t *w13s_q, const uint8_t *w13s_scale,
+                                           const uint8_t *w2s_q, const uint8_t *w2s_scale,
+                                           void *y, void *saved_preact_s, void *ws,
+                                           size_t ws_bytes, cudaStream_t stream);
 
 /* Shared expert, backward: the gradients of y += W2s (silu(W13s[0:I] x) * W13s[I:2I] x)
  * for every token, by the chain rule of mok_backward with one expert, weight one and no

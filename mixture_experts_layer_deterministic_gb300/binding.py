@@ -43,6 +43,7 @@ EXPORTED = [
     "mok_clear_device_status", "mok_profile_enable", "mok_profile_read",
     "mok_build_schedule_noalloc", "mok_shared_expert_forward",
     "mok_quantize_mxfp8_transposed", "mok_backward_mxfp8", "mok_shared_expert_backward",
+    "mok_shared_expert_forward_mxfp8",
 ]
 
 # bytes of the fixed scratch array behind mok_build_schedule_noalloc
@@ -96,6 +97,8 @@ def lib():
             "mok_backward": ([cfgp, p, schp, p, p, p, p, p, p, p, p, p, p, p, sz, p],
                              ctypes.c_int),
             "mok_shared_expert_forward": ([cfgp, p, p, p, p, p, p, sz, p], ctypes.c_int),
+            "mok_shared_expert_forward_mxfp8": ([cfgp, p, p, p, p, p, p, p, p, sz, p],
+                                                ctypes.c_int),
             "mok_shared_expert_backward": ([cfgp, p, p, p, p, p, p, p, p, p, sz, p],
                                            ctypes.c_int),
             "mok_backward_mxfp8": ([cfgp, p, schp, p, p, p, p, p, p, p, p, p, p, p, p, p, sz,
@@ -218,6 +221,14 @@ def mok_backward_mxfp8(cfg, x, sched, topk_w, saved_preact, w13t_q, w13t_s, w2t_
                                     _ptr(w13t_s), _ptr(w2t_q), _ptr(w2t_s), _ptr(dy), _ptr(dx),
                                     _ptr(dw13), _ptr(dw2), _ptr(d_topk_w), _ptr(d_logits),
                                     _ptr(ws), int(ws_bytes), _stream(stream))
+
+
+def mok_shared_expert_forward_mxfp8(cfg, x, w13s_q, w13s_scale, w2s_q, w2s_scale, y,
+                                    saved_preact_s, ws, ws_bytes, stream=None) -> int:
+    return lib().mok_shared_expert_forward_mxfp8(ctypes.byref(cfg), _ptr(x), _ptr(w13s_q),
+                                                 _ptr(w13s_scale), _ptr(w2s_q),
+                                                 _ptr(w2s_scale), _ptr(y), _ptr(saved_preact_s),
+                                                 _ptr(ws), int(ws_bytes), _stream(stream))
 
 
 def mok_shared_expert_backward(cfg, x, w13_s, w2_s, saved_preact_s, dy, dx, dw13_s, dw2_s, ws,

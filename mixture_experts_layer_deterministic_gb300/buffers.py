@@ -110,7 +110,14 @@ class SharedExpert:
         self.ws, self.ws_n = workspace(self.cfg, B.MOK_WS_SHARED, layer.device)
 
     def forward(self, x, w13_s, w2_s, y, saved_preact=None, stream=None):
-        """y += the shared expert's output for every token (after the routed forward)."""
+        """y += the shared expert's output for every token (after the routed forward).
+        MXFP8 layers take w13_s, w2_s as (q, scale) pairs from quantize_mxfp8."""
+        if self.cfg.prec == B.MOK_MXFP8:
+            B.check(B.mok_shared_expert_forward_mxfp8(self.cfg, x, w13_s[0], w13_s[1],
+                                                      w2_s[0], w2_s[1], y, saved_preact,
+                                                      self.ws, self.ws_n, stream),
+                    "shared forward mxfp8")
+            return y
         B.check(B.mok_shared_expert_forward(self.cfg, x, w13_s, w2_s, y, saved_preact,
                                             self.ws, self.ws_n, stream), "shared forward")
         return y

@@ -156,22 +156,37 @@ size_t carve_bwd(const mok_config *c, void *ws, BwdWs *o, bool recompute = false
     return cv.off;
 }
 
-// shared-expert forward: the expert's offsets, its tile list and h [T][I] bf16
+// shared-expert forward: the expert's offsets, its tile list and h [T][I] bf16; MXFP8:
+// x and h quantized (with scales) and the scale atoms of the weights and of the tiles
 struct SharedWs {
     int32_t *offsets;
     int32_t *tiles;
     int64_t tiles_cap;
     uint16_t *h;
+    uint8_t *x_q, *x_s, *h_q, *h_s, *sf_w13, *sf_w2, *sf_x, *sf_h;
 };
 
 size_t carve_shared(const mok_config *c, void *ws, SharedWs *o) {
     Carver cv{(char *)ws};
+    const bool mx = c->prec == MOK_MXFP8;
+    const int64_t T = c->T, H = c->H, I = c->I;
     SharedWs w;
     w.offsets = cv.take<int32_t>(2 * 4);
-    w.tiles_cap = tile_list_cap(c->T, 1, gemm_tc_tile_rows(false));
+    w.tiles_cap = tile_list_cap(T, 1, gemm_tc_tile_rows(mx));
     int32_t *t = cv.take<int32_t>(16 + (size_t)w.tiles_cap * 16);
     w.tiles = t ? t + 4 : nullptr;
-    w.h = cv.take<uint16_t>((size_t)c->T * c->I * 2);
+    w.h = mx ? nullptr : cv.take<uint16_t>((size_t)(T * I * 2));
+    w.x_q = w.x_s = w.h_q = w.h_s = w.sf_w13 = w.sf_w2 = w.sf_x = w.sf_h = nullptr;
+    if (mx) {
+        w.x_q = cv.take<uint8_t>((size_t)(T * H));
+        w.x_s = cv.take<uint8_t>((size_t)(T * (H / 32)));
+        w.h_q = cv.take<uint8_t>((size_t)(T * I));
+        w.h_s = cv.take<uint8_t>((size_t)(T * (I / 32)));
+        w.sf_w13 = cv.take<uint8_t>((size_t)(2 * I * H / 32));
+        w.sf_w2 = cv.take<uint8_t>((size_t)(H * I / 32));
+        w.sf_x = cv.take<uint8_t>((size_t)(w.tiles_cap * (H / 128) * 512));
+        w.sf_h = cv.take<uint8_t>((size_t)(w.tiles_cap * (I / 128) * 512));
+    }
     if (o) *o = w;
     return cv.off;
 }
@@ -565,6 +580,53 @@ mok_status mok_shared_expert_forward(const mok_config *c, const void *x, const v
     GemmDownArgs da{w.tiles, w.tiles_cap, w.h, nullptr, w2_s, nullptr, nullptr, (float *)y,
                     c->H, c->I, 1, false, ring, status, true};
     MOK_LAUNCH(KK_SHARED_DOWN, 1, launch_gemm_down_tc(da, c->T, stream));
+    return MOK_OK;
+}
+
+mok_status mok_shared_expert_forward_mxfp8(const mok_config *c, const void *x,
+                                           const uint8_t *w13s_q, const uint8_t *w13s_scale,
+                                           const uint8_t *w2s_q, const uint8_t *w2s_scale,
+                                           void *y, void *saved_preact_s, void *ws,
+                                           size_t ws_bytes, cudaStream_t stream) {
+    mok_status st = mok_check_config(c);
+    if (st != MOK_OK) return st;
+    int *status;
+    if ((st = check_device(&status)) != MOK_OK) return st;
+    if (c->prec != MOK_MXFP8) return MOK_ERR_INVALID_ARG;
+    if (!x || !w13s_q || !w13s_scale || !w2s_q || !w2s_scale || !y) return MOK_ERR_INVALID_ARG;
+    const void *ps[] = {x, w13s_q, w2s_q, y, saved_preact_s};
+    for (const void *p : ps)
+        if (p && !aligned16(p)) return MOK_ERR_INVALID_ARG;
+    const size_t need = carve_shared(c, nullptr, nullptr);
+    if ((st = check_ws(ws, ws_bytes, need)) != MOK_OK) return st;
+    if (c->T == 0) return MOK_OK;
+    SharedWs w;
+    carve_shared(c, ws, &w);
+    const int64_t T = c->T;
+    const int H = c->H, I = c->I;
+    const Ring ring{T, c->minibatch, 0};  // token order: row t is x[t]
+    MOK_LAUNCH(KK_TILES, 2,
+               first_error(launch_single_expert_offsets(w.offsets, T, stream),
+                           launch_build_tiles(w.offsets, 1, 0, T, gemm_tc_tile_rows(true),
+                                              w.tiles, w.tiles_cap, status, stream)));
+    MOK_LAUNCH(KK_QUANTIZE, 1,
+               launch_quantize_mxfp8((const uint16_t *)x, T, H, w.x_q, w.x_s, stream));
+    MOK_LAUNCH(KK_SCALE_ATOMS, 3,
+               first_error(first_error(launch_scale_atoms_rows(w13s_scale, 2 * (int64_t)I, H,
+                                                               w.sf_w13, stream),
+                                       launch_scale_atoms_rows(w2s_scale, H, I, w.sf_w2,
+                                                               stream)),
+                           launch_scale_atoms_tiles(w.tiles, w.tiles_cap, w.x_s, T,
+                                                    c->minibatch, 0, H, w.sf_x, stream)));
+    GemmUpArgs ua{w.tiles, w.tiles_cap, w.x_q, w.x_s, w13s_q, w13s_scale, w.h_q, w.h_s,
+                  (float *)saved_preact_s, H, I, 1, true, ring, status};
+    MOK_LAUNCH(KK_SHARED_UP, 1, launch_gemm_up_tc_mx(ua, T, w.sf_w13, w.sf_x, stream));
+    MOK_LAUNCH(KK_SCALE_ATOMS, 1,
+               launch_scale_atoms_tiles(w.tiles, w.tiles_cap, w.h_s, T, c->minibatch, 0, I,
+                                        w.sf_h, stream));
+    GemmDownArgs da{w.tiles, w.tiles_cap, w.h_q, w.h_s, w2s_q, w2s_scale, nullptr, (float *)y,
+                    H, I, 1, true, ring, status, true};
+    MOK_LAUNCH(KK_SHARED_DOWN, 1, launch_gemm_down_tc_mx(da, T, w.sf_w2, w.sf_h, stream));
     return MOK_OK;
 }
 

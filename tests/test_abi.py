@@ -88,6 +88,13 @@ def test_workspace_sizes(lib):
     # MXFP8 rings hold one byte per element
     assert B.mok_workspace_size(cfg(prec=B.MOK_MXFP8), B.MOK_WS_FORWARD) < \
         B.mok_workspace_size(c, B.MOK_WS_FORWARD)
+    # the shared expert: bf16 h [T][I]; MXFP8 holds x and h quantized with their scales and
+    # the scale atoms of the weights ([2I][H/32] + [H][I/32]) instead
+    T, H = c.T, c.H
+    sb = B.mok_workspace_size(c, B.MOK_WS_SHARED)
+    sm = B.mok_workspace_size(cfg(prec=B.MOK_MXFP8), B.MOK_WS_SHARED)
+    assert T * I * 2 <= sb
+    assert T * H + T * I + 3 * I * H // 32 <= sm
 
 
 def test_segment_capacity(lib):

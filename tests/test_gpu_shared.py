@@ -6,9 +6,10 @@ import numpy as np
 import pytest
 
 import oracle
-from harness import TOL_BF16, inputs, rel_err, sample_tokens, to_dev
+from harness import TOL_BF16, TOL_MXFP8, inputs, rel_err, sample_tokens, to_dev
 from mixture_experts_layer_deterministic_gb300 import binding as B
-from mixture_experts_layer_deterministic_gb300.buffers import MoELayer, SharedExpert
+from mixture_experts_layer_deterministic_gb300.buffers import (MoELayer, SharedExpert,
+                                                                 quantize_mxfp8)
 from workloads import CONFIGS
 from workloads.synth import f32_to_bf16_bits
 
@@ -120,7 +121,7 @@ def test_full_size_sampled_tokens():
           toks=sample_tokens(cfg.T, 128, seed=3))
 
 
-def test_mxfp8_config_is_unsupported():
+def test_mxfp8_config_needs_the_mxfp8_entry():
     import torch
     L = MoELayer(64, 128, 128, 4, 2, 64, 0, B.MOK_MXFP8)
     ws = torch.empty(max(1, B.mok_workspace_size(L.cfg, B.MOK_WS_SHARED)), dtype=torch.uint8,
@@ -131,6 +132,109 @@ def test_mxfp8_config_is_unsupported():
     y = torch.zeros(64, 128, dtype=torch.float32, device="cuda")
     st = B.mok_shared_expert_forward(L.cfg, x, w13s, w2s, y, None, ws, ws.numel())
     assert st == B.MOK_ERR_UNSUPPORTED
+    # and the MXFP8 entry point takes MXFP8 configurations only
+    Lb = MoELayer(64, 128, 128, 4, 2, 64, 0, B.MOK_BF16)
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    st = B.mok_shared_expert_forward_mxfp8(Lb.cfg, x, torch.zeros(256, 128, **u8),
+                                           torch.zeros(256, 4, **u8), torch.zeros(128, 128, **u8),
+                                           torch.zeros(128, 4, **u8), y, None, ws, ws.numel())
+    assert st == B.MOK_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    st, dev = B.mok_read_device_status()
+    assert st == B.MOK_OK and dev == B.MOK_OK
+
+
+def gpu_routed_plus_shared_mx(dims, x, logits, w13, w2, w13s, w2s, MB=2368, reps=1):
+    """MXFP8 layer: routed forward, then the shared expert added on pre-quantized weights."""
+    import torch
+    T, H, I, E, K = dims
+    L = MoELayer(T, H, I, E, K, MB, 0, B.MOK_MXFP8)
+    S = SharedExpert(L)
+    xd = to_dev(x)
+    q13, s13 = quantize_mxfp8(to_dev(w13))
+    q2, s2 = quantize_mxfp8(to_dev(w2))
+    ws13, ws2 = quantize_mxfp8(to_dev(w13s)), quantize_mxfp8(to_dev(w2s))
+    L.route(to_dev(logits))
+    L.schedule()
+    pre_s = torch.empty(max(T, 1), 2 * I, dtype=torch.float32, device="cuda")
+    outs = []
+    for _ in range(reps):
+        y = torch.empty(max(T, 1), H, dtype=torch.float32, device="cuda")
+        L.forward(xd, q13, q2, y, s13, s2)
+        y_routed = y[:T].clone()
+        S.forward(xd, ws13, ws2, y, saved_preact=pre_s)
+        outs.append((y_routed.cpu().numpy(), y[:T].cpu().numpy()))
+    torch.cuda.synchronize()
+    st, dev = B.mok_read_device_status()
+    assert st == B.MOK_OK and dev == B.MOK_OK
+    R = T * K
+    idx = L.idx[:R].view(T, K).cpu().numpy()
+    w = L.w[:R].view(T, K).cpu().numpy().astype(np.float64)
+    return outs, idx, w, pre_s[:T].cpu().numpy()
+
+
+def check_mx(outs, idx, w, pre_s, x, w13, w2, w13s, w2s, toks=None):
+    """The oracle's MXFP8 mode: the routed layer, and the shared expert as its own layer with
+    one expert and top-1 routing at weight one."""
+    y_routed, y_total = outs[0]
+    xs, idx_s, w_s, w13u, w2u = x, idx, w, w13, w2
+    if toks is not None:
+        used = np.unique(idx[toks])
+        remap = np.full(w13.shape[0], -1, np.int32)
+        remap[used] = np.arange(len(used), dtype=np.int32)
+        xs, idx_s, w_s, w13u, w2u = x[toks], remap[idx[toks]], w[toks], w13[used], w2[used]
+        y_routed, y_total, pre_s = y_routed[toks], y_total[toks], pre_s[toks]
+    xf = oracle.bf16_to_f64(xs)
+    q = lambda a: oracle.mxfp8_quantize_bf16(a)
+    yr, sr = oracle.forward(xf, idx_s, w_s, q(w13u), q(w2u), mode=oracle.MXFP8, with_slack=True)
+    T = xs.shape[0]
+    ys, ss = oracle.forward(xf, np.zeros((T, 1), np.int32), np.ones((T, 1)),
+                            q(w13s[None]), q(w2s[None]), mode=oracle.MXFP8, with_slack=True)
+    assert rel_err(y_routed, yr, sr) <= TOL_MXFP8
+    assert rel_err(y_total - y_routed, ys, ss) <= TOL_MXFP8
+    assert rel_err(y_total, yr + ys, sr + ss) <= TOL_MXFP8
+    # saved pre-activations: dot products of the dequantized x and W13s blocks (each product
+    # exact in fp32), accumulated by the tensor core; allow 2^-12 of the sum of |terms|
+    xq = oracle.mxfp8_dequantize(*oracle.mxfp8_quantize_bf16(xs))
+    wq = oracle.mxfp8_dequantize(*oracle.mxfp8_quantize_bf16(w13s))
+    a = xq @ wq.T
+    assert np.all(np.abs(pre_s - a) <= 2.0 ** -12 * (np.abs(xq) @ np.abs(wq).T) + 1e-30)
+
+
+def test_mxfp8_tiny_config():
+    cfg = CONFIGS["tiny"]
+    d = inputs(cfg)
+    w13s, w2s = shared_weights(cfg.H, cfg.I, 15, 0.05)
+    dims = (cfg.T, cfg.H, cfg.I, cfg.E, cfg.K)
+    outs, idx, w, pre_s = gpu_routed_plus_shared_mx(dims, d["x"], d["logits"], d["w13"],
+                                                    d["w2"], w13s, w2s, cfg.minibatch, reps=2)
+    check_mx(outs, idx, w, pre_s, d["x"], d["w13"], d["w2"], w13s, w2s)
+    np.testing.assert_array_equal(outs[0][1], outs[1][1])  # bitwise run to run
+
+
+@pytest.mark.parametrize("dims", [(300, 256, 128, 8, 2), (1, 128, 128, 4, 1),
+                                  (517, 384, 256, 16, 4)])
+def test_mxfp8_ragged_token_counts(dims):
+    T, H, I, E, K = dims
+    r = np.random.default_rng(T + 11)
+    x = f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
+    lg = r.standard_normal((T, E)).astype(np.float32)
+    w13 = f32_to_bf16_bits((r.standard_normal((E, 2 * I, H)) * 0.05).astype(np.float32))
+    w2 = f32_to_bf16_bits((r.standard_normal((E, H, I)) * 0.05).astype(np.float32))
+    w13s, w2s = shared_weights(H, I, T + 12, 0.05)
+    outs, idx, w, pre_s = gpu_routed_plus_shared_mx(dims, x, lg, w13, w2, w13s, w2s, 100)
+    check_mx(outs, idx, w, pre_s, x, w13, w2, w13s, w2s)
+
+
+def test_mxfp8_full_size_sampled_tokens():
+    cfg = CONFIGS["fwd_mxfp8"]
+    d = inputs(cfg)
+    w13s, w2s = shared_weights(cfg.H, cfg.I, 19, cfg.w_std)
+    dims = (cfg.T, cfg.H, cfg.I, cfg.E, cfg.K)
+    outs, idx, w, pre_s = gpu_routed_plus_shared_mx(dims, d["x"], d["logits"], d["w13"],
+                                                    d["w2"], w13s, w2s, cfg.minibatch)
+    check_mx(outs, idx, w, pre_s, d["x"], d["w13"], d["w2"], w13s, w2s,
+             toks=sample_tokens(cfg.T, 24, seed=5))
 
 
 def gpu_step_with_shared(dims, x, logits, w13, w2, w13s, w2s, dy, MB=2368):

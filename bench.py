@@ -427,7 +427,25 @@ def run_mok(args):
         ms_sm = timed(fwd_shared_mx, args.steps)
         phases["fwd_shared_mxfp8"] = {"ms": ms_sm,
                                       "tflops": 6.0 * T * H * I / (ms_sm * 1e-3) / 1e12}
-        del Sm, ws13, ws2
+        # and its MXFP8 backward on the transposed quantized weights (untimed), after a
+        # forward that saved its pre-activations
+        from mixture_experts_layer_deterministic_gb300.buffers import quantize_mxfp8_transposed
+        w13s_b = (torch.randn(1, 2 * I, H, device=dev) * cfg.w_std).to(torch.bfloat16)
+        w2s_b = (torch.randn(1, H, I, device=dev) * cfg.w_std).to(torch.bfloat16)
+        ws13, ws2 = quantize_mxfp8(w13s_b[0]), quantize_mxfp8(w2s_b[0])
+        wst13, wst2 = quantize_mxfp8_transposed(w13s_b), quantize_mxfp8_transposed(w2s_b)
+        pre_s = torch.empty(T, 2 * I, dtype=torch.float32, device=dev)
+        dw13s = torch.empty(2 * I, H, dtype=torch.float32, device=dev)
+        dw2s = torch.empty(H, I, dtype=torch.float32, device=dev)
+        Sm.forward(x, ws13, ws2, y, saved_preact=pre_s, stream=stream)
+
+        def bwd_shared_mx():
+            Sm.backward(x, wst13, wst2, pre_s, dy, dx, dw13s, dw2s, stream=stream)
+        bwd_shared_mx()
+        ms_smb = timed(bwd_shared_mx, args.steps)
+        phases["bwd_shared_mxfp8"] = {"ms": ms_smb,
+                                      "tflops": 12.0 * T * H * I / (ms_smb * 1e-3) / 1e12}
+        del Sm, ws13, ws2, w13s_b, w2s_b, wst13, wst2, pre_s, dw13s, dw2s
 
         # MXFP8 backward (G and dgrad in MXFP8 on weights pre-quantized along their
         # contraction axes, untimed like the forward's; weight gradients BF16), after an

@@ -277,11 +277,28 @@ mok_status mok_shared_expert_forward_mxfp8(const mok_config *cfg, const void *x,
  *   dx      [T][H] fp32, in and out (typically mok_backward's result).
  *   dw13_s  [2I][H] fp32 out; dw2_s [H][I] fp32 out.
  *   ws      at least mok_workspace_size(cfg, MOK_WS_SHARED_BACKWARD) bytes.
- * BF16 only (else MOK_ERR_UNSUPPORTED). Asynchronous on `stream`. */
+ * BF16 (cfg->prec == MOK_BF16, else MOK_ERR_UNSUPPORTED; MXFP8 configurations use
+ * mok_shared_expert_backward_mxfp8). Asynchronous on `stream`. */
 mok_status mok_shared_expert_backward(const mok_config *cfg, const void *x, const void *w13_s,
                                       const void *w2_s, const void *saved_preact_s,
                                       const void *dy, void *dx, void *dw13_s, void *dw2_s,
                                       void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Shared expert, backward, MXFP8 (cfg->prec == MOK_MXFP8): as mok_shared_expert_backward
+ * with the operands of mok_backward_mxfp8 — the G GEMM on dy and W2s quantized along H, the
+ * dgrad GEMM on dA and W13s quantized along 2I, the weight gradients on bf16 operands.
+ *   w13st_q [H][2I] E4M3 with w13st_scale [H][2I/32]; w2st_q [I][H] E4M3 with w2st_scale
+ *   [I][H/32] (mok_quantize_mxfp8_transposed of W13s with batch 1, rows 2I, cols H, and of
+ *   W2s with rows H, cols I).
+ *   saved_preact_s [T][2I] fp32 as written by mok_shared_expert_forward_mxfp8: required.
+ *   Other arguments as for mok_shared_expert_backward; ws at least
+ *   mok_workspace_size(cfg, MOK_WS_SHARED_BACKWARD) for this (MXFP8) configuration. */
+mok_status mok_shared_expert_backward_mxfp8(const mok_config *cfg, const void *x,
+                                            const uint8_t *w13st_q, const uint8_t *w13st_scale,
+                                            const uint8_t *w2st_q, const uint8_t *w2st_scale,
+                                            const void *saved_preact_s, const void *dy,
+                                            void *dx, void *dw13_s, void *dw2_s, void *ws,
+                                            size_t ws_bytes, cudaStream_t stream);
 
 /* MXFP8 quantization of a bf16 matrix along its rows ([arex] section "pull 代替 push":
  * pre-quantized weights). src [rows][cols] bf16 -> q [rows][cols] E4M3, scale

@@ -43,7 +43,7 @@ EXPORTED = [
     "mok_clear_device_status", "mok_profile_enable", "mok_profile_read",
     "mok_build_schedule_noalloc", "mok_shared_expert_forward",
     "mok_quantize_mxfp8_transposed", "mok_backward_mxfp8", "mok_shared_expert_backward",
-    "mok_shared_expert_forward_mxfp8",
+    "mok_shared_expert_forward_mxfp8", "mok_shared_expert_backward_mxfp8",
 ]
 
 # bytes of the fixed scratch array behind mok_build_schedule_noalloc
@@ -99,6 +99,8 @@ def lib():
             "mok_shared_expert_forward": ([cfgp, p, p, p, p, p, p, sz, p], ctypes.c_int),
             "mok_shared_expert_forward_mxfp8": ([cfgp, p, p, p, p, p, p, p, p, sz, p],
                                                 ctypes.c_int),
+            "mok_shared_expert_backward_mxfp8": ([cfgp, p, p, p, p, p, p, p, p, p, p, p, sz, p],
+                                                 ctypes.c_int),
             "mok_shared_expert_backward": ([cfgp, p, p, p, p, p, p, p, p, p, sz, p],
                                            ctypes.c_int),
             "mok_backward_mxfp8": ([cfgp, p, schp, p, p, p, p, p, p, p, p, p, p, p, p, p, sz,
@@ -229,6 +231,15 @@ def mok_shared_expert_forward_mxfp8(cfg, x, w13s_q, w13s_scale, w2s_q, w2s_scale
                                                  _ptr(w13s_scale), _ptr(w2s_q),
                                                  _ptr(w2s_scale), _ptr(y), _ptr(saved_preact_s),
                                                  _ptr(ws), int(ws_bytes), _stream(stream))
+
+
+def mok_shared_expert_backward_mxfp8(cfg, x, w13st_q, w13st_scale, w2st_q, w2st_scale,
+                                     saved_preact_s, dy, dx, dw13_s, dw2_s, ws, ws_bytes,
+                                     stream=None) -> int:
+    return lib().mok_shared_expert_backward_mxfp8(
+        ctypes.byref(cfg), _ptr(x), _ptr(w13st_q), _ptr(w13st_scale), _ptr(w2st_q),
+        _ptr(w2st_scale), _ptr(saved_preact_s), _ptr(dy), _ptr(dx), _ptr(dw13_s), _ptr(dw2_s),
+        _ptr(ws), int(ws_bytes), _stream(stream))
 
 
 def mok_shared_expert_backward(cfg, x, w13_s, w2_s, saved_preact_s, dy, dx, dw13_s, dw2_s, ws,

@@ -123,10 +123,18 @@ class SharedExpert:
         return y
 
     def backward(self, x, w13_s, w2_s, saved_preact, dy, dx, dw13_s, dw2_s, stream=None):
-        """dx += the shared expert's input gradient; dw13_s, dw2_s = its weight gradients."""
+        """dx += the shared expert's input gradient; dw13_s, dw2_s = its weight gradients.
+        MXFP8 layers take w13_s, w2_s as (q, scale) pairs from quantize_mxfp8_transposed
+        (of W13s[None] and W2s[None])."""
         if getattr(self, "ws_b", None) is None:
             self.ws_b, self.ws_b_n = workspace(self.cfg, B.MOK_WS_SHARED_BACKWARD,
                                                x.device)
+        if self.cfg.prec == B.MOK_MXFP8:
+            B.check(B.mok_shared_expert_backward_mxfp8(self.cfg, x, w13_s[0], w13_s[1],
+                                                       w2_s[0], w2_s[1], saved_preact, dy, dx,
+                                                       dw13_s, dw2_s, self.ws_b, self.ws_b_n,
+                                                       stream), "shared backward mxfp8")
+            return dx
         B.check(B.mok_shared_expert_backward(self.cfg, x, w13_s, w2_s, saved_preact, dy, dx,
                                              dw13_s, dw2_s, self.ws_b, self.ws_b_n, stream),
                 "shared backward")

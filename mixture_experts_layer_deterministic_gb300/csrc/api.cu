@@ -193,7 +193,9 @@ size_t carve_shared(const mok_config *c, void *ws, SharedWs *o) {
 
 // shared-expert backward: the single expert's offsets, padded offsets, count, weights of
 // one and identity row map; its tile list; dA [Tpad][2I], h [Tpad][I] (bf16, rows past T
-// zero) and the G epilogue's (unused) router-gradient partials
+// zero) and the G epilogue's (unused) router-gradient partials. MXFP8: dy quantized along
+// H [T][H], dA quantized along 2I [Tpad][2I] (with scales), and the scale atoms of the
+// transposed weights and of the dy and dA tiles.
 struct SharedBwdWs {
     int32_t *offsets, *poff, *counts, *perm;
     float *ones;
@@ -201,6 +203,7 @@ struct SharedBwdWs {
     int64_t tiles_cap, tpad;
     uint16_t *dA, *sh;
     float *dS_part;
+    uint8_t *dy_q, *dy_s, *dA_q, *dA_s, *sf_w2t, *sf_w13t, *sf_dy, *sf_dA;
 };
 
 size_t carve_shared_bwd(const mok_config *c, void *ws, SharedBwdWs *o) {
@@ -212,12 +215,25 @@ size_t carve_shared_bwd(const mok_config *c, void *ws, SharedBwdWs *o) {
     w.counts = cv.take<int32_t>(4);
     w.perm = cv.take<int32_t>((size_t)c->T * 4 + 4);
     w.ones = cv.take<float>((size_t)c->T * 4 + 4);
-    w.tiles_cap = tile_list_cap(c->T, 1, gemm_tc_tile_rows(false));
+    const bool mx = c->prec == MOK_MXFP8;
+    w.tiles_cap = tile_list_cap(c->T, 1, gemm_tc_tile_rows(mx));
     int32_t *t = cv.take<int32_t>(16 + (size_t)w.tiles_cap * 16);
     w.tiles = t ? t + 4 : nullptr;
     w.dA = cv.take<uint16_t>((size_t)(w.tpad * 2 * c->I * 2));
     w.sh = cv.take<uint16_t>((size_t)(w.tpad * c->I * 2));
     w.dS_part = cv.take<float>((size_t)c->T * gemm_tc_dS_parts(c->I) * 4 + 4);
+    w.dy_q = w.dy_s = w.dA_q = w.dA_s = w.sf_w2t = w.sf_w13t = w.sf_dy = w.sf_dA = nullptr;
+    if (mx) {
+        const int64_t T = c->T, H = c->H, I2 = 2 * (int64_t)c->I;
+        w.dy_q = cv.take<uint8_t>((size_t)(T * H));
+        w.dy_s = cv.take<uint8_t>((size_t)(T * (H / 32)));
+        w.dA_q = cv.take<uint8_t>((size_t)(w.tpad * I2));
+        w.dA_s = cv.take<uint8_t>((size_t)(w.tpad * (I2 / 32)));
+        w.sf_w2t = cv.take<uint8_t>((size_t)(c->I * H / 32));
+        w.sf_w13t = cv.take<uint8_t>((size_t)(H * I2 / 32));
+        w.sf_dy = cv.take<uint8_t>((size_t)(w.tiles_cap * (H / 128) * 512));
+        w.sf_dA = cv.take<uint8_t>((size_t)(w.tiles_cap * (I2 / 128) * 512));
+    }
     if (o) *o = w;
     return cv.off;
 }
@@ -630,20 +646,34 @@ mok_status mok_shared_expert_forward_mxfp8(const mok_config *c, const void *x,
     return MOK_OK;
 }
 
-mok_status mok_shared_expert_backward(const mok_config *c, const void *x, const void *w13_s,
-                                      const void *w2_s, const void *saved_preact_s,
-                                      const void *dy, void *dx, void *dw13_s, void *dw2_s,
-                                      void *ws, size_t ws_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+// the shared expert's transposed, MXFP8-quantized weights (its MXFP8 backward)
+struct MxSharedWeights {
+    const uint8_t *w13t_q, *w13t_s, *w2t_q, *w2t_s;
+};
+
+mok_status shared_backward_impl(const mok_config *c, const void *x, const void *w13_s,
+                                const void *w2_s, const MxSharedWeights *mxw,
+                                const void *saved_preact_s, const void *dy, void *dx,
+                                void *dw13_s, void *dw2_s, void *ws, size_t ws_bytes,
+                                cudaStream_t stream) {
     mok_status st = mok_check_config(c);
     if (st != MOK_OK) return st;
     int *status;
     if ((st = check_device(&status)) != MOK_OK) return st;
-    if (c->prec != MOK_BF16) return MOK_ERR_UNSUPPORTED;
-    if (!x || !w13_s || !w2_s || !saved_preact_s || !dy || !dx || !dw13_s || !dw2_s)
+    const bool mx = mxw != nullptr;
+    if (!mx && c->prec != MOK_BF16) return MOK_ERR_UNSUPPORTED;
+    if (mx && c->prec != MOK_MXFP8) return MOK_ERR_INVALID_ARG;
+    if (!x || !saved_preact_s || !dy || !dx || !dw13_s || !dw2_s) return MOK_ERR_INVALID_ARG;
+    if (!mx && (!w13_s || !w2_s)) return MOK_ERR_INVALID_ARG;
+    if (mx && (!mxw->w13t_q || !mxw->w13t_s || !mxw->w2t_q || !mxw->w2t_s))
         return MOK_ERR_INVALID_ARG;
-    const void *ps[] = {x, w13_s, w2_s, saved_preact_s, dy, dx, dw13_s, dw2_s};
+    const void *ps[] = {x, w13_s, w2_s, saved_preact_s, dy, dx, dw13_s, dw2_s,
+                        mx ? mxw->w13t_q : nullptr, mx ? mxw->w2t_q : nullptr};
     for (const void *p : ps)
-        if (!aligned16(p)) return MOK_ERR_INVALID_ARG;
+        if (p && !aligned16(p)) return MOK_ERR_INVALID_ARG;
     const size_t need = carve_shared_bwd(c, nullptr, nullptr);
     if ((st = check_ws(ws, ws_bytes, need)) != MOK_OK) return st;
     SharedBwdWs w;
@@ -654,16 +684,47 @@ mok_status mok_shared_expert_backward(const mok_config *c, const void *x, const 
     MOK_LAUNCH(KK_SHARED_BWD, 2,
                first_error(launch_single_expert_bwd_setup(w.offsets, w.poff, w.counts, w.ones,
                                                           w.perm, T, stream),
-                           launch_build_tiles(w.offsets, 1, 0, T, gemm_tc_tile_rows(false),
+                           launch_build_tiles(w.offsets, 1, 0, T, gemm_tc_tile_rows(mx),
                                               w.tiles, w.tiles_cap, status, stream)));
     if (T > 0) {
         GemmGArgs ga{w.tiles, w.tiles_cap, w.offsets, w.poff, (const uint16_t *)w2_s,
                      (const uint16_t *)dy, (const float *)saved_preact_s, w.perm, w.ones, w.dA,
                      w.sh, w.dS_part, H, I, status};
-        MOK_LAUNCH(KK_SHARED_BWD, 1, launch_gemm_g_tc(ga, 1, T, stream));  // dy: T rows
         GemmDgradArgs dg{w.tiles, w.tiles_cap, w.offsets, w.poff, (const uint16_t *)w13_s,
                          w.dA, w.perm, (float *)dx, H, I, status};
         dg.accumulate = true;
+        if (mx) {
+            // dy quantized along H in token order (the padded layout of a single expert is
+            // the token order; rows past T are outside the TMA map and read zero)
+            MOK_LAUNCH(KK_QUANTIZE, 1,
+                       launch_quantize_mxfp8((const uint16_t *)dy, T, H, w.dy_q, w.dy_s,
+                                             stream));
+            MOK_LAUNCH(KK_SCALE_ATOMS, 3,
+                       first_error(first_error(launch_scale_atoms_rows(mxw->w2t_s, I, H,
+                                                                       w.sf_w2t, stream),
+                                               launch_scale_atoms_rows(mxw->w13t_s, H, 2 * I,
+                                                                       w.sf_w13t, stream)),
+                                   launch_scale_atoms_tiles_padded(w.tiles, w.tiles_cap,
+                                                                   w.dy_s, w.offsets, w.poff,
+                                                                   H, w.sf_dy, stream)));
+            ga.mxfp8 = true;
+            ga.w2t_q = mxw->w2t_q;
+            ga.sf_w2t = w.sf_w2t;
+            ga.dy_q = w.dy_q;
+            ga.sf_dy = w.sf_dy;
+            ga.dA_q = w.dA_q;
+            ga.dA_s = w.dA_s;
+            dg.mxfp8 = true;
+            dg.w13t_q = mxw->w13t_q;
+            dg.sf_w13t = w.sf_w13t;
+            dg.dA_q = w.dA_q;
+            dg.sf_dA = w.sf_dA;
+        }
+        MOK_LAUNCH(KK_SHARED_BWD, 1, launch_gemm_g_tc(ga, 1, T, stream));  // dy: T rows
+        if (mx)
+            MOK_LAUNCH(KK_SCALE_ATOMS, 1,
+                       launch_scale_atoms_tiles_padded(w.tiles, w.tiles_cap, w.dA_s, w.offsets,
+                                                       w.poff, 2 * I, w.sf_dA, stream));
         MOK_LAUNCH(KK_SHARED_BWD, 1, launch_gemm_dgrad_tc(dg, 1, w.tpad, stream));
     }
     // the weight gradients' K runs over the padded rows: x and dy rows past T read zeros
@@ -675,6 +736,28 @@ mok_status mok_shared_expert_backward(const mok_config *c, const void *x, const 
                                            (float *)dw2_s, 1, I, H, w.tpad > 0 ? w.tpad : 1,
                                            T > 0 ? T : 1, status, stream)));
     return MOK_OK;
+}
+}  // namespace
+
+extern "C" {
+
+mok_status mok_shared_expert_backward(const mok_config *c, const void *x, const void *w13_s,
+                                      const void *w2_s, const void *saved_preact_s,
+                                      const void *dy, void *dx, void *dw13_s, void *dw2_s,
+                                      void *ws, size_t ws_bytes, cudaStream_t stream) {
+    return shared_backward_impl(c, x, w13_s, w2_s, nullptr, saved_preact_s, dy, dx, dw13_s,
+                                dw2_s, ws, ws_bytes, stream);
+}
+
+mok_status mok_shared_expert_backward_mxfp8(const mok_config *c, const void *x,
+                                            const uint8_t *w13st_q, const uint8_t *w13st_scale,
+                                            const uint8_t *w2st_q, const uint8_t *w2st_scale,
+                                            const void *saved_preact_s, const void *dy,
+                                            void *dx, void *dw13_s, void *dw2_s, void *ws,
+                                            size_t ws_bytes, cudaStream_t stream) {
+    const MxSharedWeights mxw{w13st_q, w13st_scale, w2st_q, w2st_scale};
+    return shared_backward_impl(c, x, nullptr, nullptr, &mxw, saved_preact_s, dy, dx, dw13_s,
+                                dw2_s, ws, ws_bytes, stream);
 }
 
 mok_status mok_quantize_mxfp8(const void *src_bf16, int64_t rows, int32_t cols, uint8_t *q,

@@ -166,7 +166,7 @@ def test_argument_errors_are_reported():
                                   w2t[0], w2t[1], dy, dx, dw13, dw2, dtk, None, L.ws_b,
                                   L.ws_b_n)
         assert st == want, (prec, st)
-    # the shared expert's backward is BF16 only
+    # the shared expert's BF16 backward refuses MXFP8 configurations
     Lm = MoELayer(T, H, I, E, K, 64, 0, B.MOK_MXFP8)
     ws = torch.empty(max(1, B.mok_workspace_size(Lm.cfg, B.MOK_WS_SHARED_BACKWARD)), **u8)
     st = B.mok_shared_expert_backward(Lm.cfg, x, torch.zeros(2 * I, H, dtype=torch.bfloat16,

@@ -294,3 +294,99 @@ def test_backward_with_shared_expert(dims):
     assert rel_err(dx - dx_r, dx_so, sdx_s) <= TOL_BF16
     assert rel_err(dw13s, dw13_so[0], s13[0]) <= TOL_BF16
     assert rel_err(dw2s, dw2_so[0], s2[0]) <= TOL_BF16
+
+
+def gpu_step_with_shared_mx(dims, x, logits, w13, w2, w13s, w2s, dy, MB=2368, reps=1):
+    """MXFP8 layer: routed and shared forward (both saving pre-activations), then the routed
+    MXFP8 backward and the shared MXFP8 backward, which adds into dx."""
+    import torch
+    from mixture_experts_layer_deterministic_gb300.buffers import (backward_mxfp8,
+                                                                     quantize_mxfp8_transposed)
+    T, H, I, E, K = dims
+    L = MoELayer(T, H, I, E, K, MB, 0, B.MOK_MXFP8, backward=True)
+    S = SharedExpert(L)
+    xd, dyd = to_dev(x), to_dev(dy)
+    w13d, w2d, w13sd, w2sd = to_dev(w13), to_dev(w2), to_dev(w13s), to_dev(w2s)
+    q13, s13 = quantize_mxfp8(w13d)
+    q2, s2 = quantize_mxfp8(w2d)
+    w13t, w2t = quantize_mxfp8_transposed(w13d), quantize_mxfp8_transposed(w2d)
+    ws13, ws2 = quantize_mxfp8(w13sd), quantize_mxfp8(w2sd)
+    wst13 = quantize_mxfp8_transposed(w13sd[None])
+    wst2 = quantize_mxfp8_transposed(w2sd[None])
+    L.route(to_dev(logits))
+    L.schedule()
+    R = T * K
+    f32 = dict(dtype=torch.float32, device="cuda")
+    pre, pre_s = torch.empty(max(R, 1), 2 * I, **f32), torch.empty(max(T, 1), 2 * I, **f32)
+    y = torch.empty(max(T, 1), H, **f32)
+    L.forward(xd, q13, q2, y, s13, s2, pre)
+    S.forward(xd, ws13, ws2, y, saved_preact=pre_s)
+    outs = []
+    for _ in range(reps):
+        dx = torch.empty(max(T, 1), H, **f32)
+        dw13, dw2 = torch.empty(E, 2 * I, H, **f32), torch.empty(E, H, I, **f32)
+        dtk = torch.empty(max(R, 1), **f32)
+        backward_mxfp8(L, xd, pre, w13t, w2t, dyd, dx, dw13, dw2, dtk)
+        dx_routed = dx[:T].clone()
+        dw13s, dw2s = torch.empty(2 * I, H, **f32), torch.empty(H, I, **f32)
+        S.backward(xd, wst13, wst2, pre_s, dyd, dx, dw13s, dw2s)
+        outs.append(dict(dx_r=dx_routed.cpu().numpy(), dx=dx[:T].cpu().numpy(),
+                         dw13s=dw13s.cpu().numpy(), dw2s=dw2s.cpu().numpy()))
+    torch.cuda.synchronize()
+    st, dev = B.mok_read_device_status()
+    assert st == B.MOK_OK and dev == B.MOK_OK
+    idx = L.idx[:R].view(T, K).cpu().numpy()
+    w = L.w[:R].view(T, K).cpu().numpy().astype(np.float64)
+    return outs, idx, w
+
+
+@pytest.mark.parametrize("dims", [(256, 256, 128, 8, 2), (300, 256, 128, 8, 2),
+                                  (517, 384, 256, 16, 4), (1, 128, 128, 4, 1)])
+def test_mxfp8_backward_with_shared_expert(dims):
+    T, H, I, E, K = dims
+    r = np.random.default_rng(T + 21)
+    x = f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
+    lg = r.standard_normal((T, E)).astype(np.float32)
+    w13 = f32_to_bf16_bits((r.standard_normal((E, 2 * I, H)) * 0.05).astype(np.float32))
+    w2 = f32_to_bf16_bits((r.standard_normal((E, H, I)) * 0.05).astype(np.float32))
+    dy = f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
+    w13s, w2s = shared_weights(H, I, T + 23, 0.05)
+    outs, idx, w = gpu_step_with_shared_mx(dims, x, lg, w13, w2, w13s, w2s, dy, reps=2)
+    g = outs[0]
+    xf, dyf = oracle.bf16_to_f64(x), oracle.bf16_to_f64(dy)
+    dx_ro, _, _, _, sdx_r, _, _ = oracle.backward(xf, idx, w, w13, w2, dyf, weight_grads=False,
+                                                  mode=oracle.MXFP8, with_slack=True)
+    # the shared expert in the oracle's MXFP8 mode: one expert, top-1 routing at weight one
+    dx_so, dw13_so, dw2_so, _, sdx_s, s13, s2 = oracle.backward(
+        xf, np.zeros((T, 1), np.int32), np.ones((T, 1)), w13s[None], w2s[None], dyf,
+        mode=oracle.MXFP8, with_slack=True)
+    assert rel_err(g["dx_r"], dx_ro, sdx_r) <= TOL_MXFP8
+    assert rel_err(g["dx"] - g["dx_r"], dx_so, sdx_s) <= TOL_MXFP8
+    assert rel_err(g["dx"], dx_ro + dx_so, sdx_r + sdx_s) <= TOL_MXFP8
+    assert rel_err(g["dw13s"], dw13_so[0], s13[0]) <= TOL_MXFP8
+    assert rel_err(g["dw2s"], dw2_so[0], s2[0]) <= TOL_MXFP8
+    for k in g:  # bitwise run to run
+        np.testing.assert_array_equal(g[k], outs[1][k])
+
+
+def test_mxfp8_shared_backward_argument_errors():
+    import torch
+    T, H, I = 64, 128, 128
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    f32 = dict(dtype=torch.float32, device="cuda")
+    x = torch.zeros(T, H, dtype=torch.bfloat16, device="cuda")
+    wt13 = (torch.zeros(H, 2 * I, **u8), torch.zeros(H, 2 * I // 32, **u8))
+    wt2 = (torch.zeros(I, H, **u8), torch.zeros(I, H // 32, **u8))
+    pre = torch.zeros(T, 2 * I, **f32)
+    dx = torch.zeros(T, H, **f32)
+    dw13s, dw2s = torch.zeros(2 * I, H, **f32), torch.zeros(H, I, **f32)
+    for prec, saved, want in ((B.MOK_MXFP8, None, B.MOK_ERR_INVALID_ARG),  # pre required
+                              (B.MOK_BF16, pre, B.MOK_ERR_INVALID_ARG)):   # not MXFP8
+        L = MoELayer(T, H, I, 4, 2, 64, 0, prec)
+        ws = torch.empty(max(1, B.mok_workspace_size(L.cfg, B.MOK_WS_SHARED_BACKWARD)), **u8)
+        st = B.mok_shared_expert_backward_mxfp8(L.cfg, x, wt13[0], wt13[1], wt2[0], wt2[1],
+                                                saved, x, dx, dw13s, dw2s, ws, ws.numel())
+        assert st == want, (prec, st)
+    torch.cuda.synchronize()
+    st, dev = B.mok_read_device_status()
+    assert st == B.MOK_OK and dev == B.MOK_OK

@@ -99,6 +99,20 @@ def test_ragged_and_empty_experts(dims, skew):
     check_all(res[0], idx, w, x, w13, w2, dy, dims[3])
 
 
+def test_large_experts_and_a_partial_column_block():
+    """Skewed routing gives two experts about 3x the rows of an even split (their weight
+    gradients run K over 1000 and 880 rows) and leaves three experts empty; I=384 makes the
+    last 256-wide column block of dW2 half past the end of its rows."""
+    dims = (1000, 256, 384, 8, 2)
+    x, lg, w13, w2, dy = small_case(*dims, seed=5, skew=4.0)
+    res, idx, w = gpu_backward(dims, x, lg, w13, w2, dy, 2368, reps=2)
+    counts = np.bincount(idx.reshape(-1), minlength=dims[3])
+    assert counts.max() > 2 * 352, counts
+    check_all(res[0], idx, w, x, w13, w2, dy, dims[3])
+    for k in res[0]:
+        assert same_bits(res[0][k], res[1][k]), k  # bitwise run to run
+
+
 @pytest.mark.parametrize("dims,MB", [((256, 256, 128, 8, 2), 64),
                                      ((600, 256, 256, 16, 4), 100),
                                      ((333, 384, 128, 24, 3), 2368)])

@@ -352,6 +352,15 @@ def run_mok(args):
     roof["kernel"] = dom
     roof["traffic"] = ncu_traffic(dom, args.workload)
 
+    def per_kernel(fn, n):
+        """ms per call of each kernel kind over n profiled calls of fn (library events on
+        the launching stream)"""
+        B.check(B.mok_profile_enable(1))
+        timed(fn, n)
+        pr = B.mok_profile_read()
+        B.check(B.mok_profile_enable(0))
+        return {k: round(t / n, 4) for k, (c, t) in sorted(pr.items(), key=lambda kv: -kv[1][1])}
+
     # phases: forward alone, backward alone, MXFP8 forward
     phases = {}
     ms_f = timed(fwd, args.steps)
@@ -413,7 +422,8 @@ def run_mok(args):
         for _ in range(2):
             fwd_mx()
         ms_m = timed(fwd_mx, args.steps)
-        phases["fwd_mxfp8"] = {"ms": ms_m, "tflops": cfg.fwd_flops() / (ms_m * 1e-3) / 1e12}
+        phases["fwd_mxfp8"] = {"ms": ms_m, "tflops": cfg.fwd_flops() / (ms_m * 1e-3) / 1e12,
+                               "kernels_ms": per_kernel(fwd_mx, args.steps)}
 
         # the shared expert's MXFP8 forward on weights quantized once (untimed), added into y
         from mixture_experts_layer_deterministic_gb300.buffers import SharedExpert
@@ -462,7 +472,8 @@ def run_mok(args):
         for _ in range(2):
             bwd_mx()
         ms_mb = timed(bwd_mx, args.steps)
-        phases["bwd_mxfp8"] = {"ms": ms_mb, "tflops": cfg.bwd_flops() / (ms_mb * 1e-3) / 1e12}
+        phases["bwd_mxfp8"] = {"ms": ms_mb, "tflops": cfg.bwd_flops() / (ms_mb * 1e-3) / 1e12,
+                               "kernels_ms": per_kernel(bwd_mx, args.steps)}
         del Lm, q13, s13, q2, s2, w13t, w2t
 
     # e2e through the public API with host buffers: every step copies its inputs (x, logits,

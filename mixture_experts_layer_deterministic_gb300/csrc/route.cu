@@ -3,13 +3,14 @@
 // [alphalab] "Mixture-of-Kittens" analysis (alphalab.site), section 四: the benchmark routes
 // by top-k over Gaussian router logits. Weights are a softmax over the chosen K logits.
 //
-// One warp per token. Each logit becomes a 64-bit key: an order-preserving image of the
-// fp32 value (with -0 folded onto +0) in the high half and (2^32-1 - expert) in the low
-// half, so the unsigned maximum is the largest logit and, among equal logits, the lowest
-// expert id. Each lane keeps the maximum of its own keys; K rounds of a warp-wide maximum
-// over those pick the experts in descending order, and only the lane that owned the
-// winner retires it and rescans its keys. The chosen logit is read back from the key
-// (the image inverts; -0 comes back as +0, which has the same exponential).
+// One warp per token; lane l holds the logits of experts 32j + l. Each logit becomes an
+// unsigned order-preserving image of its fp32 value (-0 folded onto +0; every finite
+// value maps above 0, which marks a retired or absent expert). Each lane keeps its largest
+// remaining value, the lowest j among equal ones. A round takes the warp-wide maximum
+// value with one integer reduction, then the lowest expert id among the lanes holding it
+// with a second, so the experts come out by descending logit with ties to the lower id;
+// only the winning lane retires that logit and rescans its own. The chosen logit is read
+// back from its image (-0 comes back as +0, which has the same exponential).
 // HBM-bound: T*E*4 bytes read, T*K*8 bytes written.
 #include "common.cuh"
 #include "mok_internal.h"
@@ -17,25 +18,14 @@
 namespace mok {
 namespace {
 
-MOK_DEV uint64_t logit_key(float v, uint32_t e) {
+MOK_DEV uint32_t logit_order(float v) {
     uint32_t u = __float_as_uint(v);
     if (u == 0x80000000u) u = 0u;  // -0 ties with +0
-    const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    return ((uint64_t)ord << 32) | (uint64_t)(0xFFFFFFFFu - e);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-MOK_DEV float key_logit(uint64_t key) {
-    const uint32_t ord = (uint32_t)(key >> 32);
+MOK_DEV float order_logit(uint32_t ord) {
     return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
-}
-
-MOK_DEV uint64_t warp_max_u64(uint64_t v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const uint64_t w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
-        v = w > v ? w : v;
-    }
-    return v;
 }
 
 // PER = logits per lane (E <= 32 * PER)
@@ -49,31 +39,42 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict
     for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
          t += warps_total) {
         const float *row = logits + t * E;
-        uint64_t key[PER];
+        uint32_t v[PER];
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
             const int e = j * 32 + lane;  // coalesced: lanes read consecutive experts
-            key[j] = (e < E) ? logit_key(__ldg(row + e), (uint32_t)e) : 0ull;
+            v[j] = (e < E) ? logit_order(__ldg(row + e)) : 0u;
         }
+        // this lane's largest remaining value and its slot (the lowest j among equals)
+        uint32_t best = 0u;
+        int bj = 0;
+#pragma unroll
+        for (int j = 0; j < PER; ++j)
+            if (v[j] > best) {
+                best = v[j];
+                bj = j;
+            }
         float sel_logit = 0.f;  // lane k keeps the k-th chosen logit
         int sel_e = 0;
         float first = 0.f;
-        uint64_t mine = 0ull;  // this lane's largest remaining key
-#pragma unroll
-        for (int j = 0; j < PER; ++j) mine = key[j] > mine ? key[j] : mine;
         for (int k = 0; k < K; ++k) {
-            const uint64_t best = warp_max_u64(mine);
-            const uint32_t e = 0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull);
-            // keys are unique: exactly one lane owns the winner; it retires it and rescans
-            if (mine == best) {
-                mine = 0ull;
+            const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
+            const uint32_t cand = best == top ? (uint32_t)(bj * 32 + lane) : 0xFFFFFFFFu;
+            const uint32_t e = __reduce_min_sync(0xFFFFFFFFu, cand);
+            if (cand == e) {  // the lane that held the winner retires it and rescans
 #pragma unroll
-                for (int j = 0; j < PER; ++j) {
-                    if (key[j] == best) key[j] = 0ull;
-                    mine = key[j] > mine ? key[j] : mine;
-                }
+                for (int j = 0; j < PER; ++j)
+                    if (j == bj) v[j] = 0u;
+                best = 0u;
+                bj = 0;
+#pragma unroll
+                for (int j = 0; j < PER; ++j)
+                    if (v[j] > best) {
+                        best = v[j];
+                        bj = j;
+                    }
             }
-            const float lv = key_logit(best);
+            const float lv = order_logit(top);
             if (k == 0) first = lv;
             if (lane == k) {
                 sel_logit = lv;

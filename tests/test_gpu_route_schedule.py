@@ -66,6 +66,11 @@ def test_route_ties_and_signed_zero():
     lg = r.choice(vals, size=(500, 64)).astype(np.float32)
     g = route_and_schedule(lg, 64, 8, 100)
     check_against_oracle(lg, 64, 8, 100, g)
+    # 512 experts (16 per lane) from three values: every round breaks ties both between
+    # lanes and between the experts one lane holds
+    lg = r.choice(np.array([-0.0, 0.25, 0.25, 1.0], np.float32), size=(300, 512))
+    g = route_and_schedule(lg.astype(np.float32), 512, 10, 2368)
+    check_against_oracle(lg.astype(np.float32), 512, 10, 2368, g)
 
 
 def test_route_one_hot_and_all_experts():

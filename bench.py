@@ -100,11 +100,19 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# the sources of the tensor-core GEMM engine's translation unit: the kernels whose DRAM
+# traffic per launch profiles/ncu_traffic.json records
+GEMM_SOURCES = ("mixture_experts_layer_deterministic_gb300/csrc/gemm_tc.cu",
+                "mixture_experts_layer_deterministic_gb300/csrc/tc.cuh",
+                "mixture_experts_layer_deterministic_gb300/csrc/common.cuh",
+                "mixture_experts_layer_deterministic_gb300/csrc/mok_internal.h",
+                "include/mok.h")
+
+
 def kernel_source_sha():
     h = hashlib.sha256()
-    d = os.path.join(ROOT, "mixture_experts_layer_deterministic_gb300", "csrc")
-    for fn in sorted(os.listdir(d)):
-        h.update(open(os.path.join(d, fn), "rb").read())
+    for fn in GEMM_SOURCES:
+        h.update(open(os.path.join(ROOT, fn), "rb").read())
     return h.hexdigest()[:16]
 
 

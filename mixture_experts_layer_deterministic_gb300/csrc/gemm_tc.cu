@@ -39,6 +39,8 @@
 // fixed-order fp32 dot product, independent of which CTA computes its unit.
 #include <cudaTypedefs.h>
 
+#include <cstddef>
+
 #include "common.cuh"
 #include "mok_internal.h"
 #include "tc.cuh"
@@ -72,7 +74,7 @@ __host__ __device__ constexpr int stage_bytes() { return 2 * A_BYTES + B_BYTES +
 
 // per epilogue warp: one value per token column of the unit (a routing weight or a slot
 // index) and a transpose buffer for fixed-order reductions over the warp's 32 lanes
-struct EpiScratch {
+struct alignas(16) EpiScratch {
     float col[TILE_ROWS];
     float red[16][33];
 };
@@ -91,6 +93,10 @@ struct Smem {
     int abort;
     EpiScratch epi[EPI_WARPS];
 };
+
+// the MXFP8 gate/up epilogue stages codes in EpiScratch::col with 16-byte accesses
+static_assert(sizeof(EpiScratch) % 16 == 0 && offsetof(Smem, epi) % 16 == 0,
+              "epilogue scratch alignment");
 
 template <bool MX>
 __host__ __device__ constexpr int smem_bytes() {
@@ -200,7 +206,7 @@ struct FwdUpT {
         return g;
     }
     template <class LD>
-    MOK_DEV void epilogue(int64_t u, const LD &ld, EpiScratch &, int q, int half,
+    MOK_DEV void epilogue(int64_t u, const LD &ld, EpiScratch &es, int q, int half,
                           int lane) const {
         int e, mb;
         int64_t r0, r1;
@@ -212,34 +218,50 @@ struct FwdUpT {
         for (int n0 = 16 * half; n0 < n_mma; n0 += 32) {
             float d0[16], d1[16];
             ld(n0, d0, d1);
+            float h[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int n = n0 + j;
-                const bool live = n < nr;
                 const int64_t r = r0 + n;
-                const float h = silu_f(d0[j]) * d1[j];
-                if (live && preact != nullptr) {
+                h[j] = silu_f(d0[j]) * d1[j];
+                if (n < nr && preact != nullptr) {
                     preact[r * 2 * I + i] = d0[j];
                     preact[r * 2 * I + I + i] = d1[j];
                 }
-                if (hring == nullptr) continue;
-                if (!mxfp8) {
-                    if (live) ((uint16_t *)hring)[rm(r) * I + i] = f32_to_bf16(h);
-                } else {
-                    // the warp's 32 lanes hold one 32-feature MXFP8 block of row r; its
-                    // maximum magnitude by one integer reduction (non-negative floats'
-                    // bit patterns order like the floats)
-                    const float amax = __uint_as_float(
-                        __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(h))));
-                    const uint32_t sb = mx_scale_byte(amax);
-                    const uint32_t code = e4m3x2(h * mx_inv_scale(sb), 0.f) & 0xFFu;
-                    if (live) {
-                        const int64_t slot = rm(r);
-                        ((uint8_t *)hring)[slot * I + i] = (uint8_t)code;
-                        if (lane == 0) hring_s[slot * (I / 32) + i / 32] = (uint8_t)sb;
-                    }
-                }
+                if (hring != nullptr && !mxfp8 && n < nr)
+                    ((uint16_t *)hring)[rm(r) * I + i] = f32_to_bf16(h[j]);
             }
+            if (hring == nullptr || !mxfp8) continue;
+            // MXFP8: the warp's 32 lanes hold one 32-feature block of each of the chunk's 16
+            // rows. A block's maximum magnitude comes from one integer reduction (the bit
+            // patterns of non-negative floats order like the floats); two rows share one
+            // conversion. The codes are staged in the warp's scratch as 16 rows x 32 bytes
+            // and written back one 16-byte piece per lane, the scales by lanes 0-15.
+            uint8_t *stage = reinterpret_cast<uint8_t *>(es.col);
+            uint32_t my_sb = 0;
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+                const float a0 = __uint_as_float(
+                    __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(h[j]))));
+                const float a1 = __uint_as_float(
+                    __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(h[j + 1]))));
+                const uint32_t sb0 = mx_scale_byte(a0), sb1 = mx_scale_byte(a1);
+                const uint32_t c2 = e4m3x2(h[j] * mx_inv_scale(sb0), h[j + 1] * mx_inv_scale(sb1));
+                stage[j * 32 + lane] = (uint8_t)(c2 & 0xFFu);
+                stage[(j + 1) * 32 + lane] = (uint8_t)(c2 >> 8);
+                if (lane == j) my_sb = sb0;
+                if (lane == j + 1) my_sb = sb1;
+            }
+            __syncwarp();
+            if (lane < 16 && n0 + lane < nr)
+                hring_s[rm(r0 + n0 + lane) * (I / 32) + (mb * 128 + q * 32) / 32] = (uint8_t)my_sb;
+            const int jr = lane >> 1, hb = lane & 1;
+            if (n0 + jr < nr) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(stage + jr * 32 + hb * 16);
+                *reinterpret_cast<uint4 *>((uint8_t *)hring + rm(r0 + n0 + jr) * I + mb * 128 +
+                                           q * 32 + hb * 16) = v;
+            }
+            __syncwarp();
         }
     }
 };

@@ -73,10 +73,12 @@ __host__ __device__ constexpr int stage_bytes() { return 2 * A_BYTES + B_BYTES +
 
 
 // per epilogue warp: one value per token column of the unit (a routing weight or a slot
-// index) and a transpose buffer for fixed-order reductions over the warp's 32 lanes
+// index), a transpose buffer for fixed-order reductions over the warp's 32 lanes, and a
+// staging area that turns per-lane byte results into 16-byte stores
 struct alignas(16) EpiScratch {
     float col[TILE_ROWS];
     float red[16][33];
+    alignas(16) uint8_t stage[512];
 };
 
 struct Smem {
@@ -94,9 +96,11 @@ struct Smem {
     EpiScratch epi[EPI_WARPS];
 };
 
-// the MXFP8 gate/up epilogue stages codes in EpiScratch::col with 16-byte accesses
+// the MXFP8 epilogues stage codes in EpiScratch with 16-byte accesses
 static_assert(sizeof(EpiScratch) % 16 == 0 && offsetof(Smem, epi) % 16 == 0,
               "epilogue scratch alignment");
+static_assert(STAGES * stage_bytes<true>() + 1024 + (int)sizeof(Smem) <= 232448,
+              "MXFP8 kernels exceed the shared memory of a CTA");
 
 template <bool MX>
 __host__ __device__ constexpr int smem_bytes() {
@@ -425,6 +429,7 @@ struct BwdGT {
             ld(n0, d[0], d[1]);
             // issue every pre-activation load of the chunk before using any
             float ag[2][16], au[2][16];
+            uint32_t my_sb = 0;  // MXFP8: the block scale this lane stores for its 4-row group
 #pragma unroll
             for (int a = 0; a < 2; ++a)
 #pragma unroll
@@ -469,28 +474,46 @@ struct BwdGT {
                             const uint32_t sbg = mx_scale_byte(mg), sbu = mx_scale_byte(mu);
                             const uint32_t c2 =
                                 e4m3x2(dag * mx_inv_scale(sbg), dau * mx_inv_scale(sbu));
-                            dA_q[p * 2 * I + i] = (uint8_t)(c2 & 0xFFu);
-                            dA_q[p * 2 * I + I + i] = (uint8_t)(c2 >> 8);
-                            if (lane == 0) {
-                                dA_s[p * (2 * I / 32) + i / 32] = (uint8_t)sbg;
-                                dA_s[p * (2 * I / 32) + (I + i) / 32] = (uint8_t)sbu;
-                            }
+                            const int pc = ((j & 3) * 2 + a) * 2;  // staged pieces of the row
+                            es.stage[pc * 32 + lane] = (uint8_t)(c2 & 0xFFu);
+                            es.stage[(pc + 1) * 32 + lane] = (uint8_t)(c2 >> 8);
+                            if (lane == pc) my_sb = sbg;
+                            if (lane == pc + 1) my_sb = sbu;
                         }
                     } else if (last) {  // zero pad rows up to the next multiple of 16
                         dA[p * 2 * I + i] = 0;
                         dA[p * 2 * I + I + i] = 0;
                         sh[p * I + i] = 0;
                         if (MX) {
-                            dA_q[p * 2 * I + i] = 0;
-                            dA_q[p * 2 * I + I + i] = 0;
-                            if (lane == 0) {
-                                dA_s[p * (2 * I / 32) + i / 32] = 0;
-                                dA_s[p * (2 * I / 32) + (I + i) / 32] = 0;
-                            }
+                            const int pc = ((j & 3) * 2 + a) * 2;
+                            es.stage[pc * 32 + lane] = 0;
+                            es.stage[(pc + 1) * 32 + lane] = 0;
+                            if (lane == pc || lane == pc + 1) my_sb = 0;
                         }
                     }
                 }
                 es.red[j][lane] = gh_sum;
+                if (MX && (j & 3) == 3) {
+                    // MXFP8 codes of the last 4 rows: 16 pieces of 32 bytes (row, feature
+                    // half a, gate or up) staged; one 16-byte store per lane, and the 16
+                    // block scales from lanes 0-15
+                    __syncwarp();
+                    const int pl = lane >> 1, hb = lane & 1;
+                    const int nl = n0 + j - 3 + (pl >> 2);
+                    const int ibl = mb * 256 + q * 32 + ((pl >> 1) & 1) * 128;
+                    if (ibl < I && (nl < nr || last))
+                        *reinterpret_cast<uint4 *>(dA_q + (pb + nl) * 2 * I + ((pl & 1) ? I : 0) +
+                                                   ibl + hb * 16) =
+                            *reinterpret_cast<const uint4 *>(es.stage + lane * 16);
+                    if (lane < 16) {
+                        const int ns = n0 + j - 3 + (lane >> 2);
+                        const int ibs = mb * 256 + q * 32 + ((lane >> 1) & 1) * 128;
+                        if (ibs < I && (ns < nr || last))
+                            dA_s[(pb + ns) * (2 * I / 32) + (((lane & 1) ? I : 0) + ibs) / 32] =
+                                (uint8_t)my_sb;
+                    }
+                    __syncwarp();
+                }
             }
             __syncwarp();
             // one partial per (row, weight block, warp): lanes summed in lane order; the

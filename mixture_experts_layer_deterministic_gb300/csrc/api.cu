@@ -2,6 +2,8 @@
 // and the stream-ordered sequence of kernels for each call.
 #include <string.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "mok_internal.h"
 
@@ -75,6 +77,12 @@ struct FwdWs {
     float *slots;
     uint8_t *sf_w13, *sf_w2;  // MXFP8 weight scales as tensor-core atoms
     uint8_t *sf_x, *sf_h;     // MXFP8 token-tile scales as atoms (per pass)
+    // a forward in several ring passes: second copies of what a pass's down GEMM reads
+    // (its tile list, the h ring and the h tiles' scale atoms), so that the down GEMM of
+    // one pass can run while the next pass is gathered and multiplied (else nullptr)
+    int32_t *tiles2;
+    void *hring2;
+    uint8_t *hring_s2, *sf_h2;
 };
 
 size_t carve_fwd(const mok_config *c, void *ws, FwdWs *o) {
@@ -102,8 +110,51 @@ size_t carve_fwd(const mok_config *c, void *ws, FwdWs *o) {
         w.sf_x = cv.take<uint8_t>((size_t)w.tiles_cap * (c->H / 128) * 512);
         w.sf_h = cv.take<uint8_t>((size_t)w.tiles_cap * (c->I / 128) * 512);
     }
+    w.tiles2 = nullptr;
+    w.hring2 = nullptr;
+    w.hring_s2 = w.sf_h2 = nullptr;
+    if (ns > 0 && R > c->minibatch) {
+        int32_t *t2 = cv.take<int32_t>(16 + (size_t)w.tiles_cap * 16);
+        w.tiles2 = t2 ? t2 + 4 : nullptr;
+        w.hring2 = cv.take<void>((size_t)rr * c->I * esz);
+        if (mx) {
+            w.hring_s2 = cv.take<uint8_t>((size_t)rr * (c->I / 32));
+            w.sf_h2 = cv.take<uint8_t>((size_t)w.tiles_cap * (c->I / 128) * 512);
+        }
+    }
     if (o) *o = w;
     return cv.off;
+}
+
+// The second stream of a forward in several ring passes, and its events, per device:
+// created on first use and kept for the life of the process.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, up[2] = {nullptr, nullptr},
+                down[2] = {nullptr, nullptr};
+};
+constexpr int MAX_DEVICES = 64;
+SideStream g_side[MAX_DEVICES];
+std::mutex g_side_mu;
+
+cudaError_t side_stream(SideStream **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    SideStream &ss = g_side[dev];
+    if (ss.s == nullptr) {
+        SideStream n;
+        e = cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking);
+        cudaEvent_t *evs[] = {&n.fork, &n.join, &n.up[0], &n.up[1], &n.down[0], &n.down[1]};
+        for (cudaEvent_t *ev : evs)
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+        if (e != cudaSuccess) return e;
+        ss = n;
+    }
+    *out = &ss;
+    return cudaSuccess;
 }
 
 struct BwdWs {
@@ -393,11 +444,39 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
                                launch_scale_atoms_rows(w2_scale, (int64_t)c->E * c->H, c->I,
                                                        w.sf_w2, stream)));
     }
+    // several passes: each pass's down GEMM runs on a second stream, after that pass's
+    // gate/up GEMM, so that it overlaps the next pass's tiles, gather and gate/up GEMM on
+    // the caller's stream; consecutive passes alternate between two copies of the buffers
+    // the down GEMM reads, and a pass waits until the down GEMM two passes back has
+    // released its copy
+    const bool overlap = n_pass > 1 && w.tiles2 != nullptr;
+    SideStream *ss = nullptr;
+    if (overlap) {
+        if (side_stream(&ss) != cudaSuccess) return MOK_ERR_CUDA;
+        if (cudaEventRecord(ss->fork, stream) != cudaSuccess ||
+            cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
+            return MOK_ERR_CUDA;
+    }
+    const FwdWs w0 = w;
     for (int64_t m = 0; m < n_pass; ++m) {
         const int64_t p0 = n_slots == 0 ? 0 : m * c->minibatch;
         const int64_t p1 = n_slots == 0 ? R : (p0 + c->minibatch < R ? p0 + c->minibatch : R);
         const int chunk = gemm_tc_tile_rows(mx);
         const int64_t cap = tile_list_cap(p1 - p0, c->E, chunk);
+        const int b = overlap ? (int)(m & 1) : 0;
+        if (b == 1) {
+            w.tiles = w0.tiles2;
+            w.hring = w0.hring2;
+            w.hring_s = w0.hring_s2;
+            w.sf_h = w0.sf_h2;
+        } else {
+            w.tiles = w0.tiles;
+            w.hring = w0.hring;
+            w.hring_s = w0.hring_s;
+            w.sf_h = w0.sf_h;
+        }
+        if (overlap && m >= 2 && cudaStreamWaitEvent(stream, ss->down[b], 0) != cudaSuccess)
+            return MOK_ERR_CUDA;
         MOK_LAUNCH(KK_TILES, 1,
                    launch_build_tiles(sch->offsets, c->E, p0, p1, chunk, w.tiles, cap, status,
                                       stream));
@@ -433,13 +512,29 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
             MOK_LAUNCH(KK_SCALE_ATOMS, 1,
                        launch_scale_atoms_tiles(w.tiles, cap, w.hring_s, R, c->minibatch, n_slots,
                                                 c->I, w.sf_h, stream));
-            MOK_LAUNCH(KK_GEMM_DOWN, 1,
-                       launch_gemm_down_tc_mx(da, ring_rows, w.sf_w2, w.sf_h, stream));
         } else {
             MOK_LAUNCH(KK_GEMM_UP, 1, launch_gemm_up_tc(ua, ring_rows, stream));
-            MOK_LAUNCH(KK_GEMM_DOWN, 1, launch_gemm_down_tc(da, ring_rows, stream));
+        }
+        {
+            cudaStream_t outer = stream;
+            if (overlap) {
+                if (cudaEventRecord(ss->up[b], outer) != cudaSuccess ||
+                    cudaStreamWaitEvent(ss->s, ss->up[b], 0) != cudaSuccess)
+                    return MOK_ERR_CUDA;
+            }
+            cudaStream_t stream = overlap ? ss->s : outer;  // the down GEMM's stream
+            if (mx)
+                MOK_LAUNCH(KK_GEMM_DOWN, 1,
+                           launch_gemm_down_tc_mx(da, ring_rows, w.sf_w2, w.sf_h, stream));
+            else
+                MOK_LAUNCH(KK_GEMM_DOWN, 1, launch_gemm_down_tc(da, ring_rows, stream));
+            if (overlap && cudaEventRecord(ss->down[b], stream) != cudaSuccess)
+                return MOK_ERR_CUDA;
         }
     }
+    if (overlap && (cudaEventRecord(ss->join, ss->s) != cudaSuccess ||
+                    cudaStreamWaitEvent(stream, ss->join, 0) != cudaSuccess))
+        return MOK_ERR_CUDA;
     MOK_LAUNCH(KK_COMBINE, 1,
                launch_combine(w.slots, topk_w, c->T, c->K, c->H, (float *)y, stream));
     return MOK_OK;

@@ -186,7 +186,14 @@ mok_status mok_build_schedule_noalloc(const mok_config *cfg, const int32_t *topk
  *   saved_preact  NULL, or [R][2I] fp32 out: the gate/up GEMM result of sorted row r
  *           (needed by mok_backward, or by mok_backward_mxfp8 after an MXFP8 forward).
  * GEMMs accumulate in fp32; values that are only stored (expert outputs, saved
- * pre-activations) stay fp32. */
+ * pre-activations) stay fp32.
+ * A ring smaller than R rows (cfg->ring_capacity) makes the forward run in passes of
+ * cfg->minibatch sorted rows. Then each pass's down GEMM runs on a second stream that the
+ * library keeps per device, ordered by events after that pass's gate/up GEMM, so it
+ * overlaps the next pass. The call still orders itself after earlier work on `stream`, and
+ * later work on `stream` after all of it, so it may also be captured into a CUDA graph
+ * from `stream`. Calls on one device from several host threads share that second stream's
+ * events and must not overlap in time. */
 mok_status mok_forward(const mok_config *cfg, const void *x, const mok_schedule *sched,
                        const float *topk_w, const void *w13, const uint8_t *w13_scale,
                        const void *w2, const uint8_t *w2_scale, void *y, void *saved_preact,

@@ -100,13 +100,12 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# the sources of the tensor-core GEMM engine's translation unit: the kernels whose DRAM
-# traffic per launch profiles/ncu_traffic.json records
+# the sources of the tensor-core GEMM engine (its translation unit, less the public header's
+# declarations): the kernels whose DRAM traffic per launch profiles/ncu_traffic.json records
 GEMM_SOURCES = ("mixture_experts_layer_deterministic_gb300/csrc/gemm_tc.cu",
                 "mixture_experts_layer_deterministic_gb300/csrc/tc.cuh",
                 "mixture_experts_layer_deterministic_gb300/csrc/common.cuh",
-                "mixture_experts_layer_deterministic_gb300/csrc/mok_internal.h",
-                "include/mok.h")
+                "mixture_experts_layer_deterministic_gb300/csrc/mok_internal.h")
 
 
 def kernel_source_sha():

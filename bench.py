@@ -486,9 +486,10 @@ def run_mok(args):
     # e2e through the public API with host buffers: every step copies its inputs (x, logits,
     # dy) from pinned host memory and reads its results (y, dx) back. As a training loop
     # prefetches its next batch, the copies run on their own streams: the H2D of step i+1
-    # and the D2H of step i-1 overlap step i's kernels, with double-buffered device inputs
-    # and outputs ordered by events. The first H2D and the last D2H are inside the timed
-    # region.
+    # overlaps step i's kernels, dy is waited for only by the backward, y is read back
+    # while the backward runs and dx during the next step, with double-buffered device
+    # inputs and outputs ordered by events. The first H2D and the last D2H are inside the
+    # timed region.
     hy = pinned((T, H), torch.float32)
     hdx = pinned((T, H), torch.float32)
     xin = [x, torch.empty_like(x)]
@@ -500,7 +501,9 @@ def run_mok(args):
     d2h_s = torch.cuda.Stream(dev)
 
     def e2e_run(n):
-        ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of buffer b have landed
+        ev_in_f = [torch.cuda.Event() for _ in range(2)]  # x, logits of buffer b have landed
+        ev_in_b = [torch.cuda.Event() for _ in range(2)]  # dy of buffer b has landed
+        ev_fwd = [torch.cuda.Event() for _ in range(2)]   # the forward on buffer b is done
         ev_used = [torch.cuda.Event() for _ in range(2)]  # the step on buffer b is done
         ev_out = [torch.cuda.Event() for _ in range(2)]   # outputs of buffer b are on host
         barrier()
@@ -515,25 +518,30 @@ def run_mok(args):
                 h2d_s.wait_event(ev_used[b])  # step i-2 has finished with buffer b
                 xin[b].view(torch.int16).copy_(hx, non_blocking=True)
                 lgin[b].copy_(hlg, non_blocking=True)
-                dyin[b].view(torch.int16).copy_(hdy, non_blocking=True)
-                ev_in[b].record(h2d_s)
+                ev_in_f[b].record(h2d_s)
+                dyin[b].view(torch.int16).copy_(hdy, non_blocking=True)  # needed by the bwd
+                ev_in_b[b].record(h2d_s)
 
         h2d(0)
         for i in range(n):
             b = i % 2
             if i + 1 < n:
                 h2d(i + 1)
-            stream.wait_event(ev_in[b])
+            stream.wait_event(ev_in_f[b])
             stream.wait_event(ev_out[b])  # the D2H of step i-2 has read outputs b
             L.route(lgin[b], stream)
             L.schedule(stream=stream)
             L.forward(xin[b], w13, w2, yout[b], saved_preact=pre, stream=stream)
+            ev_fwd[b].record(stream)
+            with torch.cuda.stream(d2h_s):  # y leaves while the backward runs
+                d2h_s.wait_event(ev_fwd[b])
+                hy.copy_(yout[b], non_blocking=True)
+            stream.wait_event(ev_in_b[b])
             L.backward(xin[b], pre, w13, w2, dyin[b], dxout[b], dw13, dw2, dtk, dlg,
                        stream=stream)
             ev_used[b].record(stream)
             with torch.cuda.stream(d2h_s):
                 d2h_s.wait_event(ev_used[b])
-                hy.copy_(yout[b], non_blocking=True)
                 hdx.copy_(dxout[b], non_blocking=True)
                 ev_out[b].record(d2h_s)
         stream.wait_event(ev_out[(n - 1) % 2])

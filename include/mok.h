@@ -345,6 +345,14 @@ mok_status mok_profile_read(int32_t max, int32_t *n_kinds, const char **names,
 mok_status mok_read_device_status(mok_status *out);
 mok_status mok_clear_device_status(void);
 
+/* A check of the device-side failure path that faults and hangs nothing. One thread waits,
+ * through the same bounded wait every tensor-core GEMM role uses (a timeout records
+ * MOK_ERR_TIMEOUT and the kernel returns), on an mbarrier that nothing completes, with a
+ * limit of limit_us microseconds (1 .. 1000000) instead of the GEMMs' 2 s. After it the
+ * device status word reads MOK_ERR_TIMEOUT and the context stays usable.
+ * Asynchronous on `stream`; MOK_ERR_INVALID_ARG for a limit out of range. */
+mok_status mok_selftest_bounded_wait(uint32_t limit_us, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

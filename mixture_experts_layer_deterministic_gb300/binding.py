@@ -44,6 +44,7 @@ EXPORTED = [
     "mok_build_schedule_noalloc", "mok_shared_expert_forward",
     "mok_quantize_mxfp8_transposed", "mok_backward_mxfp8", "mok_shared_expert_backward",
     "mok_shared_expert_forward_mxfp8", "mok_shared_expert_backward_mxfp8",
+    "mok_selftest_bounded_wait",
 ]
 
 # bytes of the fixed scratch array behind mok_build_schedule_noalloc
@@ -101,6 +102,7 @@ def lib():
                                                 ctypes.c_int),
             "mok_shared_expert_backward_mxfp8": ([cfgp, p, p, p, p, p, p, p, p, p, p, p, sz, p],
                                                  ctypes.c_int),
+            "mok_selftest_bounded_wait": ([ctypes.c_uint32, p], ctypes.c_int),
             "mok_shared_expert_backward": ([cfgp, p, p, p, p, p, p, p, p, p, sz, p],
                                            ctypes.c_int),
             "mok_backward_mxfp8": ([cfgp, p, schp, p, p, p, p, p, p, p, p, p, p, p, p, p, sz,
@@ -231,6 +233,10 @@ def mok_shared_expert_forward_mxfp8(cfg, x, w13s_q, w13s_scale, w2s_q, w2s_scale
                                                  _ptr(w13s_scale), _ptr(w2s_q),
                                                  _ptr(w2s_scale), _ptr(y), _ptr(saved_preact_s),
                                                  _ptr(ws), int(ws_bytes), _stream(stream))
+
+
+def mok_selftest_bounded_wait(limit_us, stream=None) -> int:
+    return lib().mok_selftest_bounded_wait(int(limit_us), _stream(stream))
 
 
 def mok_shared_expert_backward_mxfp8(cfg, x, w13st_q, w13st_scale, w2st_q, w2st_scale,

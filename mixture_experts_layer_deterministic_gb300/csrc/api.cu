@@ -886,6 +886,16 @@ mok_status mok_quantize_mxfp8_transposed(const void *src_bf16, int64_t batch, in
     return MOK_OK;
 }
 
+mok_status mok_selftest_bounded_wait(uint32_t limit_us, cudaStream_t stream) {
+    int *status;
+    mok_status st = check_device(&status);
+    if (st != MOK_OK) return st;
+    if (limit_us == 0 || limit_us > 1000000u) return MOK_ERR_INVALID_ARG;
+    if (launch_bounded_wait_probe(status, (uint64_t)limit_us * 1000ull, stream) != cudaSuccess)
+        return MOK_ERR_CUDA;
+    return MOK_OK;
+}
+
 mok_status mok_read_device_status(mok_status *out) {
     if (out == nullptr) return MOK_ERR_INVALID_ARG;
     int *status;

@@ -129,20 +129,7 @@ MOK_DEV float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
 // bounded wait; gives up when another role has aborted or after the wall-time limit
 MOK_DEV bool wait_or_abort(uint64_t *bar, uint32_t parity, int *status, volatile int *abort) {
-    if (tc::mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = tc::globaltimer();
-    uint32_t n = 0;
-    while (!tc::mbar_try_wait(bar, parity)) {
-        if ((++n & 255u) == 0) {
-            if (*abort) return false;
-            if (tc::globaltimer() - t0 > tc::WAIT_LIMIT_NS) {
-                raise_status(status, MOK_ERR_TIMEOUT);
-                *abort = 1;
-                return false;
-            }
-        }
-    }
-    return true;
+    return tc::wait_bounded(bar, parity, status, abort, tc::WAIT_LIMIT_NS);
 }
 
 // ---------------------------------------------------------------- problem policies

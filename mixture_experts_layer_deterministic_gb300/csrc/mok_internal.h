@@ -51,6 +51,8 @@ cudaError_t launch_gather_bf16(const uint16_t *x, const int32_t *perm, int K, in
                                cudaStream_t s);
 // offsets of a single expert owning rows [0, rows): off[0] = 0, off[1] = rows
 cudaError_t launch_single_expert_offsets(int32_t *off, int64_t rows, cudaStream_t s);
+// one thread waits, through the GEMM roles' bounded wait, on an mbarrier nothing completes
+cudaError_t launch_bounded_wait_probe(int *status, uint64_t limit_ns, cudaStream_t s);
 // the backward's view of a single expert owning every token in token order: offsets
 // [0, T], padded offsets [0, T rounded up to 16], counts [T], weight one and row r -> r
 cudaError_t launch_single_expert_bwd_setup(int32_t *offsets, int32_t *poff, int32_t *counts,

@@ -60,6 +60,27 @@ MOK_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// bounded wait on phase `parity` of `bar`; gives up when another role has raised `abort`,
+// or after limit_ns of wall time, when it records MOK_ERR_TIMEOUT in the status word and
+// raises `abort` itself
+MOK_DEV bool wait_bounded(uint64_t *bar, uint32_t parity, int *status, volatile int *abort,
+                          uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    uint32_t n = 0;
+    while (!mbar_try_wait(bar, parity)) {
+        if ((++n & 255u) == 0) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > limit_ns) {
+                raise_status(status, MOK_ERR_TIMEOUT);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------- TMA
 MOK_DEV void prefetch_tmap(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)m) : "memory");

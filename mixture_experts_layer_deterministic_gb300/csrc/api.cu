@@ -42,15 +42,29 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 int64_t rows_R(const mok_config *c) { return (int64_t)c->T * c->K; }
 
-// ring geometry: n_slots == 0 means the ring holds every routed row
-void ring_geom(const mok_config *c, int32_t *n_slots, int64_t *ring_rows) {
+// ring geometry: n_slots == 0 means the ring holds every routed row (one pass). Else the
+// forward runs in passes of `pass` sorted rows through n_slots slots of `pass` rows:
+//   BF16: one minibatch per pass, floor(capacity / minibatch) slots;
+//   MXFP8: the whole ring per pass (one slot of `capacity` rows).
+// Either gives the same results bit for bit. Passes cannot overlap a pass's gather with the
+// previous pass's gate/up GEMM (they share the ring), so fuller passes waste less of each
+// GEMM's last wave; on the 65536-token imbalanced workload (ring 1.25 minibatches) that made
+// the MXFP8 forward 17% faster but the BF16 one 10% slower, whose full-ring pass (24 MB of
+// x rows, 48 MB of fp32 slot writes besides the experts' weights) nears L2's size.
+void ring_geom(const mok_config *c, int32_t *n_slots, int64_t *ring_rows, int32_t *pass) {
     const int64_t R = rows_R(c);
     if (c->ring_capacity == 0 || (int64_t)c->ring_capacity >= R) {
         *n_slots = 0;
         *ring_rows = R;
+        *pass = c->minibatch;
+    } else if (c->prec == MOK_MXFP8) {
+        *n_slots = 1;
+        *ring_rows = c->ring_capacity;
+        *pass = c->ring_capacity;
     } else {
         *n_slots = c->ring_capacity / c->minibatch;
         *ring_rows = (int64_t)(*n_slots) * c->minibatch;
+        *pass = c->minibatch;
     }
 }
 
@@ -88,10 +102,10 @@ struct FwdWs {
 size_t carve_fwd(const mok_config *c, void *ws, FwdWs *o) {
     Carver cv{(char *)ws};
     const int64_t R = rows_R(c);
-    int32_t ns;
+    int32_t ns, pr;
     int64_t rr;
-    ring_geom(c, &ns, &rr);
-    const int64_t pass_rows = ns == 0 ? R : c->minibatch;
+    ring_geom(c, &ns, &rr, &pr);
+    const int64_t pass_rows = ns == 0 ? R : pr;
     const bool mx = c->prec == MOK_MXFP8;
     const int esz = mx ? 1 : 2;
     FwdWs w;
@@ -113,7 +127,7 @@ size_t carve_fwd(const mok_config *c, void *ws, FwdWs *o) {
     w.tiles2 = nullptr;
     w.hring2 = nullptr;
     w.hring_s2 = w.sf_h2 = nullptr;
-    if (ns > 0 && R > c->minibatch) {
+    if (ns > 0 && R > pr) {
         int32_t *t2 = cv.take<int32_t>(16 + (size_t)w.tiles_cap * 16);
         w.tiles2 = t2 ? t2 + 4 : nullptr;
         w.hring2 = cv.take<void>((size_t)rr * c->I * esz);
@@ -431,11 +445,11 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
     if (R == 0) return MOK_OK;
     FwdWs w;
     carve_fwd(c, ws, &w);
-    int32_t n_slots;
+    int32_t n_slots, pass;  // pass: rows per pass
     int64_t ring_rows;
-    ring_geom(c, &n_slots, &ring_rows);
-    Ring ring{R, c->minibatch, n_slots};
-    const int64_t n_pass = n_slots == 0 ? 1 : (R + c->minibatch - 1) / c->minibatch;
+    ring_geom(c, &n_slots, &ring_rows, &pass);
+    Ring ring{R, pass, n_slots};
+    const int64_t n_pass = n_slots == 0 ? 1 : (R + pass - 1) / pass;
     if (mx) {
         // the weights' scales in the tensor cores' atom layout, once per call
         MOK_LAUNCH(KK_SCALE_ATOMS, 2,
@@ -459,8 +473,8 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
     }
     const FwdWs w0 = w;
     for (int64_t m = 0; m < n_pass; ++m) {
-        const int64_t p0 = n_slots == 0 ? 0 : m * c->minibatch;
-        const int64_t p1 = n_slots == 0 ? R : (p0 + c->minibatch < R ? p0 + c->minibatch : R);
+        const int64_t p0 = n_slots == 0 ? 0 : m * pass;
+        const int64_t p1 = n_slots == 0 ? R : (p0 + pass < R ? p0 + pass : R);
         const int chunk = gemm_tc_tile_rows(mx);
         const int64_t cap = tile_list_cap(p1 - p0, c->E, chunk);
         const int b = overlap ? (int)(m & 1) : 0;
@@ -489,7 +503,7 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
         else if (!mx)
             MOK_LAUNCH(KK_GATHER, 1,
                        launch_gather_bf16((const uint16_t *)x, sch->perm, c->K, c->H, p0, p1, R,
-                                          c->minibatch, n_slots, (uint16_t *)w.xring, stream));
+                                          pass, n_slots, (uint16_t *)w.xring, stream));
         else if (n_slots == 0)
             MOK_LAUNCH(KK_GATHER, 1,
                        launch_gather_tok_mxfp8((const uint16_t *)x, sch->inv, c->T, c->K, c->H,
@@ -497,7 +511,7 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
         else
             MOK_LAUNCH(KK_GATHER, 1,
                        launch_gather_mxfp8((const uint16_t *)x, sch->perm, c->K, c->H, p0, p1,
-                                           R, c->minibatch, n_slots, (uint8_t *)w.xring,
+                                           R, pass, n_slots, (uint8_t *)w.xring,
                                            w.xring_s, stream));
         GemmUpArgs ua{w.tiles, cap, w.xring, w.xring_s, w13, w13_scale, w.hring,
                       w.hring_s, (float *)saved_preact, c->H, c->I, c->E, mx, ring, status};
@@ -505,12 +519,12 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
                         w.slots, c->H, c->I, c->E, mx, ring, status, false};
         if (mx) {
             MOK_LAUNCH(KK_SCALE_ATOMS, 1,
-                       launch_scale_atoms_tiles(w.tiles, cap, w.xring_s, R, c->minibatch, n_slots,
+                       launch_scale_atoms_tiles(w.tiles, cap, w.xring_s, R, pass, n_slots,
                                                 c->H, w.sf_x, stream));
             MOK_LAUNCH(KK_GEMM_UP, 1,
                        launch_gemm_up_tc_mx(ua, ring_rows, w.sf_w13, w.sf_x, stream));
             MOK_LAUNCH(KK_SCALE_ATOMS, 1,
-                       launch_scale_atoms_tiles(w.tiles, cap, w.hring_s, R, c->minibatch, n_slots,
+                       launch_scale_atoms_tiles(w.tiles, cap, w.hring_s, R, pass, n_slots,
                                                 c->I, w.sf_h, stream));
         } else {
             MOK_LAUNCH(KK_GEMM_UP, 1, launch_gemm_up_tc(ua, ring_rows, stream));

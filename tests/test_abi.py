@@ -97,6 +97,21 @@ def test_workspace_sizes(lib):
     assert T * H + T * I + 3 * I * H // 32 <= sm
 
 
+def test_ring_passes_per_precision(lib):
+    """A ring smaller than R: BF16 runs one minibatch per pass through floor(C/MB) slots,
+    so a capacity that is not a multiple of the minibatch leaves the rest unused; MXFP8
+    fills the whole ring per pass, so its x and h rings grow with the capacity."""
+    T, K, MB = 4096, 2, 1000  # R = 8192 routed rows
+    ws = lambda prec, C: B.mok_workspace_size(cfg(T=T, K=K, minibatch=MB, ring_capacity=C,
+                                                  prec=prec), B.MOK_WS_FORWARD)
+    assert ws(B.MOK_BF16, 2500) == ws(B.MOK_BF16, 2000)
+    assert ws(B.MOK_BF16, 3000) > ws(B.MOK_BF16, 2999)
+    assert ws(B.MOK_MXFP8, 2500) > ws(B.MOK_MXFP8, 2000)
+    # the extra 500 rows: x ring (H bytes + scales) and both h rings (I bytes + scales)
+    H, I = 256, 128
+    assert ws(B.MOK_MXFP8, 2500) - ws(B.MOK_MXFP8, 2000) >= 500 * (H + H // 32 + 2 * (I + I // 32))
+
+
 def test_segment_capacity(lib):
     # E + ceil(R / MB) - 1
     assert B.mok_segment_capacity(cfg()) == 8 + (512 + 63) // 64 - 1

@@ -36,6 +36,25 @@ def test_exports_every_declared_symbol(lib):
     assert names <= set(B.EXPORTED)
 
 
+def test_header_is_plain_c(tmp_path):
+    """include/mok.h is a C header: a C11 translation unit that includes it and takes the
+    address of every declared entry point compiles cleanly with gcc (no C++ needed)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    if gcc is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("gcc or the CUDA headers are not available")
+    names = sorted(declared_entry_points())
+    src = tmp_path / "uses_mok.c"
+    src.write_text('#include "mok.h"\n' + "".join(
+        "void *p_%s(void) { return (void *)&%s; }\n" % (n, n) for n in names))
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-fsyntax-only",
+                        "-I" + os.path.join(ROOT, "include"), "-I" + cuda_inc, str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_abi_version_and_strings(lib):
     assert B.mok_abi_version() == B.MOK_ABI_VERSION
     for s in range(8):

@@ -46,11 +46,12 @@ int64_t rows_R(const mok_config *c) { return (int64_t)c->T * c->K; }
 // forward runs in passes of `pass` sorted rows through n_slots slots of `pass` rows:
 //   BF16: one minibatch per pass, floor(capacity / minibatch) slots;
 //   MXFP8: the whole ring per pass (one slot of `capacity` rows).
-// Either gives the same results bit for bit. Passes cannot overlap a pass's gather with the
-// previous pass's gate/up GEMM (they share the ring), so fuller passes waste less of each
-// GEMM's last wave; on the 65536-token imbalanced workload (ring 1.25 minibatches) that made
-// the MXFP8 forward 17% faster but the BF16 one 10% slower, whose full-ring pass (24 MB of
-// x rows, 48 MB of fp32 slot writes besides the experts' weights) nears L2's size.
+// Either gives the same results bit for bit. A pass carries a fixed cost (launches, pipeline
+// fill, tile list, gather) that bigger passes amortize, and a gate/up GEMM of T tiles takes
+// ceil(8T / 152) SM waves at I = 1024. On the 65536-token imbalanced workload (ring 1.25
+// minibatches): an MXFP8 pass (112-row tiles) is two waves at either size, so the whole ring
+// per pass ran 17% faster; a BF16 minibatch inside one expert is exactly one wave (19
+// tiles), the whole ring two (24), and it ran 10% slower.
 void ring_geom(const mok_config *c, int32_t *n_slots, int64_t *ring_rows, int32_t *pass) {
     const int64_t R = rows_R(c);
     if (c->ring_capacity == 0 || (int64_t)c->ring_capacity >= R) {

@@ -92,10 +92,12 @@ struct FwdWs {
     float *slots;
     uint8_t *sf_w13, *sf_w2;  // MXFP8 weight scales as tensor-core atoms
     uint8_t *sf_x, *sf_h;     // MXFP8 token-tile scales as atoms (per pass)
-    // a forward in several ring passes: second copies of what a pass's down GEMM reads
-    // (its tile list, the h ring and the h tiles' scale atoms), so that the down GEMM of
-    // one pass can run while the next pass is gathered and multiplied (else nullptr)
-    int32_t *tiles2;
+    // the tile lists of all passes, built by one launch: pass m's list (count at [-4])
+    // starts at tiles + m * list_stride
+    int64_t n_lists, list_stride;
+    // a forward in several ring passes: second copies of the h ring and the h tiles' scale
+    // atoms, so that the down GEMM of one pass can run while the next pass is gathered and
+    // multiplied (else nullptr)
     void *hring2;
     uint8_t *hring_s2, *sf_h2;
 };
@@ -111,7 +113,9 @@ size_t carve_fwd(const mok_config *c, void *ws, FwdWs *o) {
     const int esz = mx ? 1 : 2;
     FwdWs w;
     w.tiles_cap = tile_list_cap(pass_rows, c->E, gemm_tc_tile_rows(mx));
-    int32_t *t = cv.take<int32_t>(16 + (size_t)w.tiles_cap * 16);
+    w.n_lists = ns == 0 ? 1 : (R + pr - 1) / pr;
+    w.list_stride = 4 + 4 * w.tiles_cap;  // int32s: a 16-byte header and the tiles
+    int32_t *t = cv.take<int32_t>((size_t)(w.n_lists * w.list_stride) * 4);
     w.tiles = t ? t + 4 : nullptr;
     w.xring = cv.take<void>((size_t)rr * c->H * esz);
     w.xring_s = mx ? cv.take<uint8_t>((size_t)rr * (c->H / 32)) : nullptr;
@@ -125,12 +129,9 @@ size_t carve_fwd(const mok_config *c, void *ws, FwdWs *o) {
         w.sf_x = cv.take<uint8_t>((size_t)w.tiles_cap * (c->H / 128) * 512);
         w.sf_h = cv.take<uint8_t>((size_t)w.tiles_cap * (c->I / 128) * 512);
     }
-    w.tiles2 = nullptr;
     w.hring2 = nullptr;
     w.hring_s2 = w.sf_h2 = nullptr;
     if (ns > 0 && R > pr) {
-        int32_t *t2 = cv.take<int32_t>(16 + (size_t)w.tiles_cap * 16);
-        w.tiles2 = t2 ? t2 + 4 : nullptr;
         w.hring2 = cv.take<void>((size_t)rr * c->I * esz);
         if (mx) {
             w.hring_s2 = cv.take<uint8_t>((size_t)rr * (c->I / 32));
@@ -459,12 +460,18 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
                                launch_scale_atoms_rows(w2_scale, (int64_t)c->E * c->H, c->I,
                                                        w.sf_w2, stream)));
     }
+    // every pass's tile list, in one launch
+    const int chunk = gemm_tc_tile_rows(mx);
+    const int64_t cap = w.tiles_cap;
+    MOK_LAUNCH(KK_TILES, 1,
+               launch_build_tiles_passes(sch->offsets, c->E, R, n_slots == 0 ? R : pass, n_pass,
+                                         chunk, w.tiles, w.list_stride, cap, status, stream));
     // several passes: each pass's down GEMM runs on a second stream, after that pass's
-    // gate/up GEMM, so that it overlaps the next pass's tiles, gather and gate/up GEMM on
-    // the caller's stream; consecutive passes alternate between two copies of the buffers
-    // the down GEMM reads, and a pass waits until the down GEMM two passes back has
-    // released its copy
-    const bool overlap = n_pass > 1 && w.tiles2 != nullptr;
+    // gate/up GEMM, so that it overlaps the next pass's gather and gate/up GEMM on the
+    // caller's stream; consecutive passes alternate between two copies of the h ring (and
+    // its scale atoms), and a pass waits until the down GEMM two passes back has released
+    // its copy
+    const bool overlap = n_pass > 1 && w.hring2 != nullptr;
     SideStream *ss = nullptr;
     if (overlap) {
         if (side_stream(&ss) != cudaSuccess) return MOK_ERR_CUDA;
@@ -476,25 +483,19 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
     for (int64_t m = 0; m < n_pass; ++m) {
         const int64_t p0 = n_slots == 0 ? 0 : m * pass;
         const int64_t p1 = n_slots == 0 ? R : (p0 + pass < R ? p0 + pass : R);
-        const int chunk = gemm_tc_tile_rows(mx);
-        const int64_t cap = tile_list_cap(p1 - p0, c->E, chunk);
         const int b = overlap ? (int)(m & 1) : 0;
+        w.tiles = w0.tiles + m * w0.list_stride;
         if (b == 1) {
-            w.tiles = w0.tiles2;
             w.hring = w0.hring2;
             w.hring_s = w0.hring_s2;
             w.sf_h = w0.sf_h2;
         } else {
-            w.tiles = w0.tiles;
             w.hring = w0.hring;
             w.hring_s = w0.hring_s;
             w.sf_h = w0.sf_h;
         }
         if (overlap && m >= 2 && cudaStreamWaitEvent(stream, ss->down[b], 0) != cudaSuccess)
             return MOK_ERR_CUDA;
-        MOK_LAUNCH(KK_TILES, 1,
-                   launch_build_tiles(sch->offsets, c->E, p0, p1, chunk, w.tiles, cap, status,
-                                      stream));
         // a ring that holds every row is filled token by token (each x row read once);
         // a smaller ring pass by pass in sorted-row order
         if (!mx && n_slots == 0)

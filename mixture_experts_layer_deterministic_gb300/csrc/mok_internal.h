@@ -44,6 +44,12 @@ cudaError_t launch_build_schedule(const int32_t *idx, int64_t R, int E, int MB,
 int64_t tile_list_cap(int64_t rows, int E, int chunk);
 cudaError_t launch_build_tiles(const int32_t *offsets, int E, int64_t p0, int64_t p1, int chunk,
                                int32_t *list, int64_t cap, int *status, cudaStream_t s);
+// the tile lists of every pass of a forward through a partial ring, in one launch: pass m
+// covers rows [m*pass, min((m+1)*pass, R)) and its list (count at [-4]) starts at
+// list0 + m*stride
+cudaError_t launch_build_tiles_passes(const int32_t *offsets, int E, int64_t R, int64_t pass,
+                                      int64_t n_pass, int chunk, int32_t *list0, int64_t stride,
+                                      int64_t cap, int *status, cudaStream_t s);
 
 // ---------------------------------------------------------------- dispatch / combine
 cudaError_t launch_gather_bf16(const uint16_t *x, const int32_t *perm, int K, int H, int64_t p0,

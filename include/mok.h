@@ -188,8 +188,9 @@ mok_status mok_build_schedule_noalloc(const mok_config *cfg, const int32_t *topk
  * GEMMs accumulate in fp32; values that are only stored (expert outputs, saved
  * pre-activations) stay fp32.
  * A ring smaller than R rows (cfg->ring_capacity) makes the forward run in passes of
- * cfg->minibatch sorted rows. Then each pass's down GEMM runs on a second stream that the
- * library keeps per device, ordered by events after that pass's gate/up GEMM, so it
+ * sorted rows: cfg->minibatch rows per pass in BF16, the whole ring in MXFP8 (results are
+ * the same bit for bit either way). Then each pass's down GEMM runs on a second stream that
+ * the library keeps per device, ordered by events after that pass's gate/up GEMM, so it
  * overlaps the next pass. The call still orders itself after earlier work on `stream`, and
  * later work on `stream` after all of it, so it may also be captured into a CUDA graph
  * from `stream`. Calls on one device from several host threads share that second stream's

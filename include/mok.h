@@ -83,10 +83,11 @@ typedef struct mok_config {
     int32_t minibatch;
     /* Rows of the fixed-size dispatch ring ("macrobatch", [arex] section "pull 代替 push",
      * point 2). 0, or any value >= R, means the ring holds every routed row and the
-     * forward runs as one pass. Otherwise the ring is floor(ring_capacity / minibatch)
-     * minibatch slots (at least one: ring_capacity >= minibatch is required), minibatch m
-     * uses slot m mod slots, and the forward runs one pass per minibatch. No routed row is
-     * ever dropped. */
+     * forward runs as one pass. Otherwise ring_capacity >= minibatch is required and the
+     * forward runs in passes of sorted rows: in BF16 the ring is floor(ring_capacity /
+     * minibatch) minibatch slots, minibatch m uses slot m mod slots, and each pass is one
+     * minibatch; in MXFP8 each pass fills the whole ring. Results are the same bit for bit
+     * for every ring setting. No routed row is ever dropped. */
     int32_t ring_capacity;
     int32_t prec; /* mok_precision of the forward; the backward is MOK_BF16 */
 } mok_config;

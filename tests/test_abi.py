@@ -55,6 +55,24 @@ def test_header_is_plain_c(tmp_path):
     assert r.returncode == 0, r.stderr
 
 
+def test_c_client_builds(lib, tmp_path):
+    """tests/c_client/c_forward.c, a client that uses nothing but include/mok.h and the CUDA
+    runtime, compiles and links against libmok.so (it runs in the GPU tests)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    if gcc is None or not os.path.exists(os.path.join(cuda, "include", "cuda_runtime_api.h")):
+        pytest.skip("gcc or the CUDA toolkit is not available")
+    r = subprocess.run([gcc, "-std=c11", "-O2", "-Wall", "-Wextra", "-Werror",
+                        "-I" + os.path.join(ROOT, "include"), "-I" + os.path.join(cuda, "include"),
+                        os.path.join(ROOT, "tests", "c_client", "c_forward.c"),
+                        "-L" + os.path.dirname(B.LIB_PATH), "-lmok",
+                        "-L" + os.path.join(cuda, "lib64"), "-lcudart",
+                        "-o", str(tmp_path / "c_forward")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_abi_version_and_strings(lib):
     assert B.mok_abi_version() == B.MOK_ABI_VERSION
     for s in range(8):

@@ -194,9 +194,10 @@ mok_status mok_build_schedule_noalloc(const mok_config *cfg, const int32_t *topk
  * the library keeps per device, ordered by events after that pass's gate/up GEMM, so it
  * overlaps the next pass. The call still orders itself after earlier work on `stream`, and
  * later work on `stream` after all of it, so it may also be captured into a CUDA graph
- * from `stream`. The first such call on a device creates that stream and its events: make
- * it outside any stream capture. Calls on one device from several host threads share that
- * second stream's events and must not overlap in time. */
+ * from `stream`. The first such call on a device outside stream capture creates that stream
+ * and its events; a captured call made before then runs its passes on `stream` alone (same
+ * results, no overlap). Calls on one device from several host threads share that second
+ * stream's events and must not overlap in time. */
 mok_status mok_forward(const mok_config *cfg, const void *x, const mok_schedule *sched,
                        const float *topk_w, const void *w13, const uint8_t *w13_scale,
                        const void *w2, const uint8_t *w2_scale, void *y, void *saved_preact,

@@ -153,13 +153,17 @@ constexpr int MAX_DEVICES = 64;
 SideStream g_side[MAX_DEVICES];
 std::mutex g_side_mu;
 
-cudaError_t side_stream(SideStream **out) {
+// *out is nullptr (and nothing is created) when the stream does not exist yet and `may_create`
+// is false
+cudaError_t side_stream(SideStream **out, bool may_create) {
+    *out = nullptr;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_side_mu);
     SideStream &ss = g_side[dev];
+    if (ss.s == nullptr && !may_create) return cudaSuccess;
     if (ss.s == nullptr) {
         SideStream n;
         e = cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking);
@@ -471,10 +475,18 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
     // caller's stream; consecutive passes alternate between two copies of the h ring (and
     // its scale atoms), and a pass waits until the down GEMM two passes back has released
     // its copy
-    const bool overlap = n_pass > 1 && w.hring2 != nullptr;
+    bool overlap = n_pass > 1 && w.hring2 != nullptr;
     SideStream *ss = nullptr;
     if (overlap) {
-        if (side_stream(&ss) != cudaSuccess) return MOK_ERR_CUDA;
+        // the second stream is created outside stream capture; a captured call made before
+        // it exists runs its passes on the caller's stream alone
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return MOK_ERR_CUDA;
+        if (side_stream(&ss, cs == cudaStreamCaptureStatusNone) != cudaSuccess)
+            return MOK_ERR_CUDA;
+        overlap = ss != nullptr;
+    }
+    if (overlap) {
         if (cudaEventRecord(ss->fork, stream) != cudaSuccess ||
             cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
             return MOK_ERR_CUDA;

@@ -71,6 +71,20 @@ def test_c_client_builds(lib, tmp_path):
                         "-L" + os.path.join(cuda, "lib64"), "-lcudart",
                         "-o", str(tmp_path / "c_forward")], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+    # its failure paths need no GPU: the library's host validation rejects H = 100 before
+    # any CUDA call, and missing inputs are reported; neither crashes
+    env = dict(os.environ, LD_LIBRARY_PATH=os.pathsep.join(
+        [os.path.dirname(B.LIB_PATH), os.path.join(cuda, "lib64"),
+         os.environ.get("LD_LIBRARY_PATH", "")]))
+    exe = str(tmp_path / "c_forward")
+    bad = subprocess.run([exe, "256", "100", "128", "8", "2", "64", "0", str(tmp_path)],
+                         env=env, capture_output=True, text=True, timeout=60)
+    assert bad.returncode == 1 and "mok_check_config" in bad.stderr
+    assert "invalid argument" in bad.stderr
+    missing = subprocess.run([exe, "256", "256", "128", "8", "2", "64", "0",
+                              str(tmp_path / "absent")], env=env, capture_output=True,
+                             text=True, timeout=60)
+    assert missing.returncode == 1 and "missing or short input file" in missing.stderr
 
 
 def test_abi_version_and_strings(lib):

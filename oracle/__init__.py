@@ -44,9 +44,11 @@ def lib():
         L.oracle_mxfp8_quantize.argtypes = [i64, i64, p, p, p]
         L.oracle_mxfp8_dequantize.argtypes = [i64, i64, p, p, p]
         L.oracle_mxfp8_quantize_bf16.argtypes = [i64, i64, p, p, p]
-        L.oracle_forward.argtypes = [i64, i32, i32, i32, i32, p, p, p, i32, p, p, p, p, i32, p, p]
+        L.oracle_forward.argtypes = [i64, i32, i32, i32, i32, p, p, p, i32, p, p, p, p, i32,
+                                     i32, p, p, p]
         L.oracle_backward.argtypes = [i64, i32, i32, i32, i32, p, p, p, i32, p, p, p, p, i32,
-                                      p, p, p, p, p, p, p, p, p]
+                                      i32, p, p, p, p, p, p, p, p, p, p]
+        L.oracle_mxfp8_qdq_slack.argtypes = [i64, p, p, p, p, p, p]
         L.oracle_bf16_slack.argtypes = [ctypes.c_double, ctypes.c_double]
         L.oracle_bf16_slack.restype = ctypes.c_double
         L.oracle_round_bf16.argtypes = [ctypes.c_double]
@@ -137,6 +139,68 @@ def mxfp8_dequantize(q, scale):
 
 W_F64, W_BF16, W_MXFP8 = 0, 1, 2
 EXACT, BF16, MXFP8 = 0, 1, 2  # operand precision modes
+STORE_F32, STORE_BF16 = 0, 1  # storage of the values that are only stored (oracle.h)
+DOT_REL = 2.0 ** -19          # ORACLE_DOT_REL: fp32 dot-product error bound / sum|terms|
+SLACK_REL = 2.0 ** -20        # ORACLE_SLACK_REL: elementwise fp32 error bound / |value|
+SUM_ULP = 2.0 ** -24          # ORACLE_SUM_ULP: fp32 unit roundoff
+
+
+class _Rows(ctypes.Structure):
+    """oracle_rows: optional per-routed-row intermediates (oracle.h)."""
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "a", "a_mag", "a_slack", "h", "h_slack", "h_q", "h_scale", "da", "da_slack", "sh",
+        "sh_slack", "da_q", "da_scale", "daq_slack", "h_in", "a_in", "da_in", "sh_in",
+        "daq_in")]
+
+
+_INPUTS = ("h_in", "a_in", "da_in", "sh_in", "daq_in")
+
+
+def _rows(R, I, names, mx, given=None):
+    """numpy arrays for the requested intermediates and the struct pointing at them; `given`
+    maps *_in names to arrays of given intermediates (kept alive in the returned dict)."""
+    shapes = dict(a=(R, 2 * I, np.float64), a_mag=(R, 2 * I, np.float64),
+                  a_slack=(R, 2 * I, np.float64), h=(R, I, np.float64),
+                  h_slack=(R, I, np.float64), h_q=(R, I, np.uint8),
+                  h_scale=(R, I // 32, np.uint8), da=(R, 2 * I, np.float64),
+                  da_slack=(R, 2 * I, np.float64), sh=(R, I, np.float64),
+                  sh_slack=(R, I, np.float64), da_q=(R, 2 * I, np.uint8),
+                  da_scale=(R, 2 * I // 32, np.uint8), daq_slack=(R, 2 * I, np.float64))
+    out = {}
+    st = _Rows()
+    for n in names:
+        r, c, dt = shapes[n]
+        a = np.zeros((max(r, 1), c), dt)
+        out[n] = a
+        setattr(st, n, a.ctypes.data)
+    keep = {}
+    for n, v in (given or {}).items():
+        assert n in _INPUTS, n
+        want = 2 * I if n in ("a_in", "da_in", "daq_in") else I
+        a = np.ascontiguousarray(v, np.float64).reshape(R, want)
+        keep[n] = a
+        setattr(st, n, a.ctypes.data)
+    return (out, keep), st
+
+
+def mxfp8_qdq_slack(v, err):
+    """MXFP8 quantize-dequantize along the last axis of v, each value known to within err:
+    (dequantized, slack, q, scale) -- oracle_mxfp8_qdq_slack row by row."""
+    v = _f64(v)
+    err = np.broadcast_to(_f64(err), v.shape).copy()
+    n = v.shape[-1]
+    assert n % 32 == 0
+    rows = v.size // n
+    out = np.empty(v.shape, np.float64)
+    sl = np.empty(v.shape, np.float64)
+    q = np.empty(v.shape, np.uint8)
+    sc = np.empty(v.shape[:-1] + (n // 32,), np.uint8)
+    for r in range(rows):
+        o = r * n
+        lib().oracle_mxfp8_qdq_slack(
+            n, v.ctypes.data + 8 * o, err.ctypes.data + 8 * o, out.ctypes.data + 8 * o,
+            sl.ctypes.data + 8 * o, q.ctypes.data + o, sc.ctypes.data + (o // 32))
+    return out, sl, q, sc
 
 
 def round_bf16(v: float) -> float:
@@ -161,11 +225,16 @@ def bf16_slack(v: float, err: float = 0.0) -> float:
     return float(lib().oracle_bf16_slack(float(v), float(err)))
 
 
-def forward(x, idx, w, w13, w2, mode=EXACT, with_slack=False):
+def forward(x, idx, w, w13, w2, mode=EXACT, with_slack=False, store=STORE_F32, rows=(),
+            given=None):
     """Layer forward in fp64: y [T,H], with the operand rounding of `mode` (EXACT, BF16 or
-    MXFP8). Weights as described in _weights (both of the same kind). With with_slack,
-    returns (y, slack): the per-element bound on how far a correct result may lie from y
-    because of rounding decisions taken on values within fp32 error of a midpoint."""
+    MXFP8) and the storage rounding of `store` (STORE_F32 or STORE_BF16). Weights as
+    described in _weights (both of the same kind). With with_slack, returns (y, slack): the
+    per-element bound on how far a correct result may lie from y because of rounding
+    decisions taken on values within fp32 error of a midpoint. `rows` names per-routed-row
+    intermediates (oracle_rows fields: a, a_mag, h, h_slack, h_q, h_scale) to return as a
+    dict after the other results; `given` = {"h_in": [T*K, I]} feeds the down GEMM the
+    given h (rows in flat id order t*K + k) instead of the oracle's own."""
     x, w = _f64(x), _f64(w)
     idx = _i32(idx)
     k13, d13, s13, sh13 = _weights(w13)
@@ -176,17 +245,27 @@ def forward(x, idx, w, w13, w2, mode=EXACT, with_slack=False):
     K = idx.shape[1]
     y = np.empty((T, H), np.float64)
     sl = np.empty((T, H), np.float64) if with_slack else None
+    (rv, _keep), rs = _rows(T * K, I2 // 2, rows, mode == MXFP8, given)
     lib().oracle_forward(T, H, I2 // 2, E, K, _p(x), _p(idx), _p(w), k13, _p(d13),
                          None if s13 is None else _p(s13), _p(d2),
-                         None if s2 is None else _p(s2), int(mode), _p(y),
-                         None if sl is None else _p(sl))
-    return (y, sl) if with_slack else y
+                         None if s2 is None else _p(s2), int(mode), int(store), _p(y),
+                         None if sl is None else _p(sl),
+                         ctypes.addressof(rs) if (rows or given) else None)
+    out = (y, sl) if with_slack else (y,)
+    if rows:
+        out = out + (rv,)
+    return out if len(out) > 1 else out[0]
 
 
-def backward(x, idx, w, w13, w2, dy, weight_grads=True, mode=EXACT, with_slack=False):
+def backward(x, idx, w, w13, w2, dy, weight_grads=True, mode=EXACT, with_slack=False,
+             store=STORE_F32, rows=(), given=None):
     """Layer backward in fp64: (dx, dw13, dw2, dtopk), with the operand rounding of `mode`
-    (EXACT, BF16 or MXFP8); dw13/dw2 are None when weight_grads is False. With with_slack,
-    also the slacks of dx, dw13, dw2 (see forward).
+    (EXACT, BF16 or MXFP8) and the storage rounding of `store`; dw13/dw2 are None when
+    weight_grads is False. With with_slack, also the slacks of dx, dw13, dw2 (see forward).
+    `rows` names per-routed-row intermediates (a, a_slack, da, da_slack, sh, sh_slack,
+    da_q, da_scale, daq_slack) to return as a dict after the other results; `given` maps
+    a_in, da_in, sh_in, daq_in to arrays ([T*K, 2I] or [T*K, I], flat id order) that replace
+    the oracle's own values where they enter the next step.
 
     In MXFP8 mode w13 and w2 are the bf16 weights (uint16 bit patterns). A is recomputed
     with the forward's operands (x and W13 quantized along H); G uses dy and W2 quantized
@@ -214,18 +293,18 @@ def backward(x, idx, w, w13, w2, dy, weight_grads=True, mode=EXACT, with_slack=F
     sdx = np.empty((T, H), np.float64) if with_slack else None
     sdw13 = np.empty(sh13, np.float64) if (with_slack and weight_grads) else None
     sdw2 = np.empty(sh2, np.float64) if (with_slack and weight_grads) else None
+    (rv, _keep), rs = _rows(T * K, I2 // 2, rows, mode == MXFP8, given)
     n = lambda a: None if a is None else _p(a)  # noqa: E731
     lib().oracle_backward(T, H, I2 // 2, E, K, _p(x), _p(idx), _p(w), k13, _p(d13), n(s13),
-                          _p(d2), _p(dy), int(mode), n(w13d), n(w2g), _p(dx), n(dw13),
-                          n(dw2), _p(dtopk), n(sdx), n(sdw13), n(sdw2))
+                          _p(d2), _p(dy), int(mode), int(store), n(w13d), n(w2g), _p(dx),
+                          n(dw13), n(dw2), _p(dtopk), n(sdx), n(sdw13), n(sdw2),
+                          ctypes.addressof(rs) if (rows or given) else None)
+    out = (dx, dw13, dw2, dtopk)
     if with_slack:
-        if sdx is not None and mode == EXACT:
-            sdx[:] = 0.0
-            if sdw13 is not None:
-                sdw13[:] = 0.0
-                sdw2[:] = 0.0
-        return dx, dw13, dw2, dtopk, sdx, sdw13, sdw2
-    return dx, dw13, dw2, dtopk
+        out = out + (sdx, sdw13, sdw2)
+    if rows:
+        out = out + (rv,)
+    return out
 
 
 def mxfp8_qdq_axis_bf16(bits, axis):

@@ -246,47 +246,52 @@ static void qdq_row(int64_t n, double *v)
 
 double oracle_bf16_slack(double v, double err)
 {
-    if (v == 0.0 || !isfinite(v))
+    if (!isfinite(v))
         return 0.0;
-    int ex;
-    frexp(fabs(v), &ex);
-    int e = ex - 1;
-    if (e < -126)
-        e = -126;
-    const double ulp = ldexp(1.0, e - 7);
-    const double q = fabs(v) / ulp;
-    const double dist = fabs((q - floor(q)) - 0.5) * ulp;
-    return dist <= err + ORACLE_SLACK_REL * fabs(v) ? ulp : 0.0;
+    /* the roundings of the extreme values the kernel may hold, v - E and v + E, nudged
+     * outward so that a tie on either end counts as the farther neighbour; rounding is
+     * monotone, so every other outcome lies between them */
+    const double E = err + ORACLE_SLACK_REL * fabs(v);
+    const double r = oracle_round_bf16(v);
+    const double hi = v + E, lo = v - E;
+    const double up = fabs(oracle_round_bf16(hi + fabs(hi) * 0x1p-50) - r);
+    const double dn = fabs(oracle_round_bf16(lo - fabs(lo) * 0x1p-50) - r);
+    return up > dn ? up : dn;
 }
 
-/* slack of the E4M3 code of a scaled value u known to within err_u (saturation at 448 is
- * one-sided: none) */
+/* E4M3 quantize-dequantize of a scaled value (saturating at 448) */
+static double e4m3_qdq(double u) { return oracle_e4m3_decode(oracle_e4m3_encode(u)); }
+
+/* distance from the code chosen for u to the farthest code that a scaled value within
+ * err_u of u may take (the same interval rule as oracle_bf16_slack) */
 static double e4m3_slack(double u, double err_u)
 {
-    const double a = fabs(u);
-    if (a == 0.0 || a >= 448.0)
-        return 0.0;
-    int ex;
-    frexp(a, &ex);
-    int e = ex - 1;
-    if (e < -6)
-        e = -6;
-    const double sp = ldexp(1.0, e - 3);
-    const double q = a / sp;
-    const double dist = fabs((q - floor(q)) - 0.5) * sp;
-    return dist <= err_u + ORACLE_SLACK_REL * a ? sp : 0.0;
+    const double E = err_u + ORACLE_SLACK_REL * fabs(u);
+    const double r = e4m3_qdq(u);
+    const double hi = u + E, lo = u - E;
+    const double up = fabs(e4m3_qdq(hi + fabs(hi) * 0x1p-50) - r);
+    const double dn = fabs(e4m3_qdq(lo - fabs(lo) * 0x1p-50) - r);
+    return up > dn ? up : dn;
 }
 
-/* MXFP8 quantize-dequantize of one row along its 32-element blocks, with each element's
- * slack: the code decision's slack, and when the block's amax is that close to a power of
- * two (the shared exponent could go either way) the difference to the other exponent's
- * result as well. */
-static void qdq_row_slack(int64_t n, double *v, const double *err, double *slack)
+/* E8M0 exponent of a 32-element block with maximum magnitude amax: floor(log2 amax) - 8,
+ * clamped to [-127, 127]; -127 for an all-zero block */
+static int mx_block_exp(double amax)
 {
-    double alt[32];
+    if (amax <= 0.0)
+        return -127;
+    int ex;
+    frexp(amax, &ex);
+    int s = (ex - 1) - 8;
+    return s < -127 ? -127 : (s > 127 ? 127 : s);
+}
+
+void oracle_mxfp8_qdq_slack(int64_t n, const double *v, const double *err, double *out,
+                            double *slack, uint8_t *q, uint8_t *scale)
+{
     for (int64_t b = 0; b < n / 32; ++b) {
-        double *blk = v + b * 32, *sl = slack + b * 32;
-        const double *eb = err + b * 32;
+        const double *blk = v + b * 32, *eb = err + b * 32;
+        double *ob = out + b * 32, *sl = slack + b * 32;
         double amax = 0.0, emax = 0.0;
         for (int i = 0; i < 32; ++i) {
             if (fabs(blk[i]) > amax)
@@ -294,38 +299,56 @@ static void qdq_row_slack(int64_t n, double *v, const double *err, double *slack
             if (eb[i] > emax)
                 emax = eb[i];
         }
-        int ex = 0;
-        if (amax > 0.0)
-            frexp(amax, &ex);
-        const int sexp = amax > 0.0 ? (ex - 1) - 8 : -127;
-        /* the nearer power of two decides which other exponent is possible */
-        const double p_lo = ldexp(1.0, ex - 1), p_hi = ldexp(1.0, ex);
+        const int sx = mx_block_exp(amax);
+        /* the shared exponent is floor(log2 amax) - 8: a block whose amax lies within its
+         * error of the power of two below (or above) it may take the exponent one lower (or
+         * one higher) */
         int other = 0;
-        const double tol = emax + ORACLE_SLACK_REL * amax;
-        if (amax > 0.0 && sexp > -127 && amax - p_lo <= tol)
-            other = -1;
-        else if (amax > 0.0 && p_hi - amax <= tol)
-            other = +1;
-        const int sx = sexp < -127 ? -127 : sexp;
+        if (amax > 0.0) {
+            int ex;
+            frexp(amax, &ex);
+            const double p_lo = ldexp(1.0, ex - 1), p_hi = ldexp(1.0, ex);
+            const double tol = emax + ORACLE_SLACK_REL * amax;
+            if (sx > -127 && amax - p_lo <= tol)
+                other = -1;
+            else if (sx < 127 && p_hi - amax <= tol)
+                other = +1;
+        }
+        uint8_t qb[32], sb;
+        oracle_mxfp8_quantize(1, 32, blk, qb, &sb);
+        oracle_mxfp8_dequantize(1, 32, qb, &sb, ob);
         for (int i = 0; i < 32; ++i)
             sl[i] = ldexp(e4m3_slack(ldexp(blk[i], -sx), ldexp(eb[i], -sx)), sx);
         if (other != 0) {
-            int s2 = sexp + other;
-            if (s2 < -127)
-                s2 = -127;
-            for (int i = 0; i < 32; ++i)
-                alt[i] = ldexp(oracle_e4m3_decode(oracle_e4m3_encode(ldexp(blk[i], -s2))), s2);
-        }
-        uint8_t q[32], sc;
-        oracle_mxfp8_quantize(1, 32, blk, q, &sc);
-        oracle_mxfp8_dequantize(1, 32, q, &sc, blk);
-        if (other != 0)
+            /* the other exponent's result, itself possibly one code away */
+            const int s2 = sx + other;
             for (int i = 0; i < 32; ++i) {
-                const double d = fabs(alt[i] - blk[i]);
-                if (d > sl[i])
-                    sl[i] = d;
+                const double u = ldexp(blk[i], -s2), E = ldexp(eb[i], -s2) +
+                                                       ORACLE_SLACK_REL * fabs(u);
+                const double hi = u + E, lo = u - E;
+                const double alt[3] = {e4m3_qdq(u), e4m3_qdq(hi + fabs(hi) * 0x1p-50),
+                                       e4m3_qdq(lo - fabs(lo) * 0x1p-50)};
+                for (int m = 0; m < 3; ++m) {
+                    const double d = fabs(ldexp(alt[m], s2) - ob[i]);
+                    if (d > sl[i])
+                        sl[i] = d;
+                }
             }
+        }
+        if (q)
+            memcpy(q + b * 32, qb, 32);
+        if (scale)
+            scale[b] = sb;
     }
+}
+
+/* A value v that a kernel computes to within err (its fp32 arithmetic) and that earlier
+ * decisions may move by up to up, rounded to bf16: returns the rounding and sets *slack to
+ * the distance within which a correct result lies from it. */
+static double round_bf16_with_slack(double v, double err, double up, double *slack)
+{
+    *slack = up + oracle_bf16_slack(v, err + up);
+    return oracle_round_bf16(v);
 }
 
 /* ---------------------------------------------------------------- forward */
@@ -345,29 +368,36 @@ static double d2silu(double g)
 void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
                     const int32_t *idx, const double *w, int32_t wkind, const void *w13,
                     const uint8_t *w13_s, const void *w2, const uint8_t *w2_s, int32_t mode,
-                    double *y, double *slack)
+                    int32_t store, double *y, double *slack, oracle_rows *rows)
 {
     (void)E;
+    const int rnd = mode != ORACLE_EXACT;            /* operand rounding */
+    const int sto = rnd && store == ORACLE_STORE_BF16; /* storage rounding */
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t t = 0; t < T; ++t) {
         double *xt = (double *)malloc(sizeof(double) * (size_t)H);
         double *a = (double *)malloc(sizeof(double) * 2 * (size_t)I);
-        double *h = (double *)malloc(sizeof(double) * (size_t)I);
-        double *hs = (double *)calloc((size_t)I, sizeof(double));
         double *aa = (double *)malloc(sizeof(double) * 2 * (size_t)I); /* sum |W13||x| */
+        double *h = (double *)malloc(sizeof(double) * (size_t)I);
+        double *hr = (double *)malloc(sizeof(double) * (size_t)I);     /* h as rounded */
+        double *hs = (double *)calloc((size_t)I, sizeof(double));      /* its slack */
         double *he = (double *)malloc(sizeof(double) * (size_t)I);     /* error bound of h */
+        double *o = (double *)malloc(sizeof(double) * (size_t)H);
+        double *om = (double *)malloc(sizeof(double) * (size_t)H);     /* sum |W2||h| */
+        double *ou = (double *)malloc(sizeof(double) * (size_t)H);     /* slack of o */
+        double *ym = (double *)calloc((size_t)H, sizeof(double));      /* sum_k |w o| */
+        double *sy = (double *)calloc((size_t)H, sizeof(double));      /* slack of the sum */
+        uint8_t *hq = (uint8_t *)malloc((size_t)I);
+        uint8_t *hsc = (uint8_t *)malloc((size_t)(I / 32 + 1));
         double *yt = y + t * (int64_t)H;
-        double *st = slack ? slack + t * (int64_t)H : NULL;
         memcpy(xt, x + t * (int64_t)H, sizeof(double) * (size_t)H);
         if (mode == ORACLE_MXFP8)
             qdq_row(H, xt);
         for (int32_t c = 0; c < H; ++c)
             yt[c] = 0.0;
-        if (st)
-            for (int32_t c = 0; c < H; ++c)
-                st[c] = 0.0;
         for (int32_t k = 0; k < K; ++k) {
-            const int64_t e = idx[t * K + k];
+            const int64_t f = t * K + k;
+            const int64_t e = idx[f];
             const int64_t b13 = e * 2 * (int64_t)I * H, b2 = e * (int64_t)H * I;
             for (int32_t j = 0; j < 2 * I; ++j) {
                 double acc = 0.0, mag = 0.0;
@@ -384,38 +414,83 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
                 /* how far a kernel's fp32 h can be from this one */
                 he[i] = fabs(dsilu(a[i]) * a[I + i]) * ORACLE_DOT_REL * aa[i] +
                         fabs(silu(a[i])) * ORACLE_DOT_REL * aa[I + i];
+                hr[i] = h[i];
+                hs[i] = 0.0;
             }
             if (mode == ORACLE_MXFP8) {
-                qdq_row_slack(I, h, he, hs);
+                oracle_mxfp8_qdq_slack(I, h, he, hr, hs, hq, hsc);
             } else if (mode == ORACLE_BF16) {
-                for (int32_t i = 0; i < I; ++i) {
-                    hs[i] = oracle_bf16_slack(h[i], he[i]);
-                    h[i] = oracle_round_bf16(h[i]);
-                }
-            }
-            const double s = w[t * K + k];
-            for (int32_t c = 0; c < H; ++c) {
-                double o = 0.0;
                 for (int32_t i = 0; i < I; ++i)
-                    o += wget(wkind, w2, w2_s, I, b2 + (int64_t)c * I + i) * h[i];
-                yt[c] += s * o;
+                    hr[i] = round_bf16_with_slack(h[i], he[i], 0.0, &hs[i]);
             }
-            /* slack of y: the h decisions that could go either way, through |W2| */
-            if (st && mode != ORACLE_EXACT)
+            if (rows) {
+                if (rows->a)
+                    memcpy(rows->a + f * 2 * I, a, sizeof(double) * 2 * (size_t)I);
+                if (rows->a_mag)
+                    memcpy(rows->a_mag + f * 2 * I, aa, sizeof(double) * 2 * (size_t)I);
+                if (rows->h)
+                    memcpy(rows->h + f * I, hr, sizeof(double) * (size_t)I);
+                if (rows->h_slack)
+                    memcpy(rows->h_slack + f * I, hs, sizeof(double) * (size_t)I);
+                if (mode == ORACLE_MXFP8 && rows->h_q)
+                    memcpy(rows->h_q + f * I, hq, (size_t)I);
+                if (mode == ORACLE_MXFP8 && rows->h_scale)
+                    memcpy(rows->h_scale + f * (I / 32), hsc, (size_t)(I / 32));
+            }
+            if (rows && rows->h_in) { /* the given h enters the down GEMM */
+                memcpy(hr, rows->h_in + f * I, sizeof(double) * (size_t)I);
+                memset(hs, 0, sizeof(double) * (size_t)I);
+            }
+            /* o = W2 h: its dot-product bound, and the slack carried in from h */
+            for (int32_t c = 0; c < H; ++c) {
+                double acc = 0.0, mag = 0.0;
+                for (int32_t i = 0; i < I; ++i) {
+                    const double wv = wget(wkind, w2, w2_s, I, b2 + (int64_t)c * I + i);
+                    acc += wv * hr[i];
+                    mag += fabs(wv * hr[i]);
+                }
+                o[c] = acc;
+                om[c] = mag;
+                ou[c] = 0.0;
+            }
+            if (rnd)
                 for (int32_t i = 0; i < I; ++i) {
                     if (hs[i] == 0.0)
                         continue;
                     for (int32_t c = 0; c < H; ++c)
-                        st[c] += fabs(s * wget(wkind, w2, w2_s, I, b2 + (int64_t)c * I + i)) *
-                                 hs[i];
+                        ou[c] += fabs(wget(wkind, w2, w2_s, I, b2 + (int64_t)c * I + i)) * hs[i];
                 }
+            const double s = w[f];
+            for (int32_t c = 0; c < H; ++c) {
+                double so = ou[c];
+                if (sto) /* the (token, k) slot holds bf16(o) */
+                    o[c] = round_bf16_with_slack(o[c], ORACLE_DOT_REL * om[c], ou[c], &so);
+                yt[c] += s * o[c];
+                ym[c] += fabs(s * o[c]);
+                sy[c] += fabs(s) * so;
+            }
+        }
+        for (int32_t c = 0; c < H; ++c) {
+            double sc = sy[c];
+            if (sto) /* y = bf16 of the fixed-order fp32 k-sum */
+                yt[c] = round_bf16_with_slack(yt[c], K * ORACLE_SUM_ULP * ym[c], sy[c], &sc);
+            if (slack)
+                slack[t * (int64_t)H + c] = sc;
         }
         free(xt);
         free(a);
-        free(h);
-        free(hs);
         free(aa);
+        free(h);
+        free(hr);
+        free(hs);
         free(he);
+        free(o);
+        free(om);
+        free(ou);
+        free(ym);
+        free(sy);
+        free(hq);
+        free(hsc);
     }
 }
 
@@ -424,20 +499,20 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
 void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
                      const int32_t *idx, const double *w, int32_t wkind, const void *w13,
                      const uint8_t *w13_s, const void *w2, const double *dy, int32_t mode,
-                     const double *w13d, const double *w2g, double *dx, double *dw13,
-                     double *dw2, double *dtopk, double *sdx, double *sdw13, double *sdw2)
+                     int32_t store, const double *w13d, const double *w2g, double *dx,
+                     double *dw13, double *dw2, double *dtopk, double *sdx, double *sdw13,
+                     double *sdw2, oracle_rows *rows)
 {
     const int64_t R = T * K;
     const int mx = mode == ORACLE_MXFP8;
-    const int want_slack = (sdx != NULL) && mode != ORACLE_EXACT;
-    /* per routed row: da = dL/da [2I] and sh = w * h [I], kept for the weight gradients,
-     * and the slack of their bf16 decisions */
+    const int rnd = mode != ORACLE_EXACT;
+    const int sto = rnd && store == ORACLE_STORE_BF16;
+    /* per routed row: da = dL/da [2I] and sh = w * h [I] as the weight gradients read them
+     * (bf16 in the rounding modes), with the slack of those values */
     double *da_all = (double *)malloc(sizeof(double) * (size_t)(R * 2 * I));
     double *sh_all = (double *)malloc(sizeof(double) * (size_t)(R * I));
-    double *das_all = want_slack ? (double *)calloc((size_t)(R * 2 * I), sizeof(double)) : NULL;
-    double *shs_all = want_slack ? (double *)calloc((size_t)(R * I), sizeof(double)) : NULL;
-    if (sdx != NULL)
-        memset(sdx, 0, sizeof(double) * (size_t)(T * (int64_t)H));
+    double *das_all = (double *)calloc((size_t)(R * 2 * I), sizeof(double));
+    double *shs_all = (double *)calloc((size_t)(R * I), sizeof(double));
 
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t t = 0; t < T; ++t) {
@@ -445,16 +520,26 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
         const double *dyt = dy + t * (int64_t)H;
         double *dxt = dx + t * (int64_t)H;
         double *a = (double *)malloc(sizeof(double) * 2 * (size_t)I);
+        double *ea = (double *)malloc(sizeof(double) * 2 * (size_t)I); /* fp32 error of a */
+        double *ua = (double *)malloc(sizeof(double) * 2 * (size_t)I); /* slack of a */
         double *g = (double *)malloc(sizeof(double) * (size_t)I);
-        double *aa = (double *)malloc(sizeof(double) * 2 * (size_t)I); /* sum |W13||x| */
         double *gg = (double *)malloc(sizeof(double) * (size_t)I);     /* sum |W2||dy| */
+        double *dae = (double *)malloc(sizeof(double) * 2 * (size_t)I);
+        double *dau = (double *)malloc(sizeof(double) * 2 * (size_t)I);
+        double *xs = (double *)malloc(sizeof(double) * (size_t)H);     /* one slot's dgrad */
+        double *xm = (double *)malloc(sizeof(double) * (size_t)H);
+        double *xu = (double *)malloc(sizeof(double) * (size_t)H);
+        double *dxm = (double *)calloc((size_t)H, sizeof(double));
+        double *sdt = (double *)calloc((size_t)H, sizeof(double));
         /* MXFP8: the forward's quantized x (operand of the recomputed A), dy quantized along
          * H (operand of G), and dA quantized along 2I with its slack (operand of dgrad) */
         double *xq = mx ? (double *)malloc(sizeof(double) * (size_t)H) : NULL;
         double *dyq = mx ? (double *)malloc(sizeof(double) * (size_t)H) : NULL;
         double *daq = mx ? (double *)malloc(sizeof(double) * 2 * (size_t)I) : NULL;
-        double *dae = mx ? (double *)malloc(sizeof(double) * 2 * (size_t)I) : NULL;
         double *daqs = mx ? (double *)malloc(sizeof(double) * 2 * (size_t)I) : NULL;
+        double *daqe = mx ? (double *)malloc(sizeof(double) * 2 * (size_t)I) : NULL;
+        uint8_t *daqc = mx ? (uint8_t *)malloc(2 * (size_t)I) : NULL;
+        uint8_t *daqb = mx ? (uint8_t *)malloc(2 * (size_t)I / 32 + 1) : NULL;
         if (mx) {
             memcpy(xq, xt, sizeof(double) * (size_t)H);
             qdq_row(H, xq);
@@ -471,6 +556,8 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
             const double s = w[f];
             double *da = da_all + f * 2 * I;
             double *sh = sh_all + f * I;
+            double *das = das_all + f * 2 * I;
+            double *shs = shs_all + f * I;
             for (int32_t j = 0; j < 2 * I; ++j) {
                 double acc = 0.0, mag = 0.0;
                 for (int32_t c = 0; c < H; ++c) {
@@ -478,8 +565,26 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
                     acc += wv * xa[c];
                     mag += fabs(wv * xa[c]);
                 }
-                a[j] = acc;
-                aa[j] = mag;
+                /* the saved A: bf16 under bf16 storage (its only uncertainty is then the
+                 * slack of that rounding), else the kernel's fp32 value; or the given A */
+                if (rows && rows->a_in) {
+                    a[j] = rows->a_in[f * 2 * I + j];
+                    ua[j] = 0.0;
+                    ea[j] = sto ? 0.0 : ORACLE_DOT_REL * mag;
+                } else if (sto) {
+                    a[j] = round_bf16_with_slack(acc, ORACLE_DOT_REL * mag, 0.0, &ua[j]);
+                    ea[j] = 0.0;
+                } else {
+                    a[j] = acc;
+                    ua[j] = 0.0;
+                    ea[j] = ORACLE_DOT_REL * mag;
+                }
+            }
+            if (rows) {
+                if (rows->a)
+                    memcpy(rows->a + f * 2 * I, a, sizeof(double) * 2 * (size_t)I);
+                if (rows->a_slack)
+                    memcpy(rows->a_slack + f * 2 * I, ua, sizeof(double) * 2 * (size_t)I);
             }
             /* g = W2^T dy */
             for (int32_t i = 0; i < I; ++i) {
@@ -505,121 +610,174 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
                 da[i] = dh * au * sig * (1.0 + ag * (1.0 - sig));
                 da[I + i] = dh * sl;
                 sh[i] = s * hi;
-            }
-            if (mode != ORACLE_EXACT) {
-                if (want_slack || mx)
-                    for (int32_t i = 0; i < I; ++i) {
-                        /* how far a kernel's fp32 values can be from these: first-order
-                         * propagation of the dot products' error bounds */
-                        const double ag = a[i], au = a[I + i], gi = g[i];
-                        const double eag = ORACLE_DOT_REL * aa[i];
-                        const double eau = ORACLE_DOT_REL * aa[I + i];
-                        const double eg = ORACLE_DOT_REL * gg[i];
-                        const double sl = silu(ag), d1 = dsilu(ag), d2 = d2silu(ag);
-                        const double e_dag = fabs(s) * (fabs(au * d1) * eg + fabs(gi * d1) * eau +
-                                                         fabs(gi * au * d2) * eag);
-                        const double e_dau = fabs(s) * (fabs(sl) * eg + fabs(gi * d1) * eag);
-                        const double e_sh = fabs(s) * (fabs(d1 * au) * eag + fabs(sl) * eau);
-                        if (mx) {
-                            dae[i] = e_dag;
-                            dae[I + i] = e_dau;
-                        }
-                        if (want_slack) {
-                            das_all[f * 2 * I + i] = oracle_bf16_slack(da[i], e_dag);
-                            das_all[f * 2 * I + I + i] = oracle_bf16_slack(da[I + i], e_dau);
-                            shs_all[f * I + i] = oracle_bf16_slack(sh[i], e_sh);
-                        }
-                    }
-                if (mx) { /* dgrad operand: dA quantized in 32-blocks along 2I */
-                    memcpy(daq, da, sizeof(double) * 2 * (size_t)I);
-                    qdq_row_slack(2 * (int64_t)I, daq, dae, daqs);
+                /* how far a kernel's values can be from these, to first order: its fp32 error
+                 * (dot-product bounds of g and, with fp32 storage, of a) and the slack of a */
+                const double d1 = dsilu(ag), d2 = d2silu(ag);
+                const double eg = ORACLE_DOT_REL * gg[i];
+                const double as = fabs(s);
+                dae[i] = as * (fabs(au * d1) * eg + fabs(g[i] * d1) * ea[I + i] +
+                               fabs(g[i] * au * d2) * ea[i]);
+                dau[i] = as * (fabs(g[i] * d1) * ua[I + i] + fabs(g[i] * au * d2) * ua[i]);
+                dae[I + i] = as * (fabs(sl) * eg + fabs(g[i] * d1) * ea[i]);
+                dau[I + i] = as * fabs(g[i] * d1) * ua[i];
+                if (rnd) {
+                    const double e_sh = as * (fabs(d1 * au) * ea[i] + fabs(sl) * ea[I + i]);
+                    const double u_sh = as * (fabs(d1 * au) * ua[i] + fabs(sl) * ua[I + i]);
+                    sh[i] = round_bf16_with_slack(sh[i], e_sh, u_sh, &shs[i]);
                 }
+            }
+            if (mx) { /* dgrad operand: dA quantized in 32-blocks along 2I */
                 for (int32_t j = 0; j < 2 * I; ++j)
-                    da[j] = oracle_round_bf16(da[j]);
-                for (int32_t i = 0; i < I; ++i)
-                    sh[i] = oracle_round_bf16(sh[i]);
+                    daqe[j] = dae[j] + dau[j];
+                oracle_mxfp8_qdq_slack(2 * (int64_t)I, da, daqe, daq, daqs, daqc, daqb);
+                for (int32_t j = 0; j < 2 * I; ++j)
+                    daqs[j] += dau[j];
             }
+            if (rnd)
+                for (int32_t j = 0; j < 2 * I; ++j)
+                    da[j] = round_bf16_with_slack(da[j], dae[j], dau[j], &das[j]);
             dtopk[f] = dS;
-            /* dx += W13^T da (MXFP8: W13 quantized along 2I times dA quantized along 2I) */
-            const double *dad = mx ? daq : da;
-            for (int32_t c = 0; c < H; ++c) {
-                double acc = 0.0;
-                for (int32_t j = 0; j < 2 * I; ++j) {
-                    const int64_t o = b13 + (int64_t)j * H + c;
-                    acc += (mx ? w13d[o] : wget(wkind, w13, w13_s, H, o)) * dad[j];
-                }
-                dxt[c] += acc;
+            if (rows) {
+                if (rows->da)
+                    memcpy(rows->da + f * 2 * I, da, sizeof(double) * 2 * (size_t)I);
+                if (rows->da_slack)
+                    memcpy(rows->da_slack + f * 2 * I, das, sizeof(double) * 2 * (size_t)I);
+                if (rows->sh)
+                    memcpy(rows->sh + f * I, sh, sizeof(double) * (size_t)I);
+                if (rows->sh_slack)
+                    memcpy(rows->sh_slack + f * I, shs, sizeof(double) * (size_t)I);
+                if (mx && rows->da_q)
+                    memcpy(rows->da_q + f * 2 * I, daqc, 2 * (size_t)I);
+                if (mx && rows->da_scale)
+                    memcpy(rows->da_scale + f * (2 * I / 32), daqb, (size_t)(2 * I / 32));
+                if (mx && rows->daq_slack)
+                    memcpy(rows->daq_slack + f * 2 * I, daqs, sizeof(double) * 2 * (size_t)I);
             }
-            if (want_slack)
-                for (int32_t j = 0; j < 2 * I; ++j) {
-                    const double sj = mx ? daqs[j] : das_all[f * 2 * I + j];
-                    if (sj == 0.0)
-                        continue;
-                    for (int32_t c = 0; c < H; ++c) {
-                        const int64_t o = b13 + (int64_t)j * H + c;
-                        sdx[t * (int64_t)H + c] +=
-                            fabs(mx ? w13d[o] : wget(wkind, w13, w13_s, H, o)) * sj;
-                    }
+            if (rows && rows->da_in) { /* the given operands of the following GEMMs */
+                memcpy(da, rows->da_in + f * 2 * I, sizeof(double) * 2 * (size_t)I);
+                memset(das, 0, sizeof(double) * 2 * (size_t)I);
+            }
+            if (rows && rows->sh_in) {
+                memcpy(sh, rows->sh_in + f * I, sizeof(double) * (size_t)I);
+                memset(shs, 0, sizeof(double) * (size_t)I);
+            }
+            if (mx && rows && rows->daq_in) {
+                memcpy(daq, rows->daq_in + f * 2 * I, sizeof(double) * 2 * (size_t)I);
+                memset(daqs, 0, sizeof(double) * 2 * (size_t)I);
+            }
+            /* this slot's dgrad result W13^T da (MXFP8: W13 quantized along 2I times dA
+             * quantized along 2I), summed over j ascending for every column */
+            const double *dad = mx ? daq : da;
+            const double *dads = mx ? daqs : das;
+            for (int32_t c = 0; c < H; ++c) {
+                xs[c] = 0.0;
+                xm[c] = 0.0;
+                xu[c] = 0.0;
+            }
+            for (int32_t j = 0; j < 2 * I; ++j) {
+                const double dj = dad[j], sj = dads[j];
+                for (int32_t c = 0; c < H; ++c) {
+                    const int64_t o = b13 + (int64_t)j * H + c;
+                    const double wv = mx ? w13d[o] : wget(wkind, w13, w13_s, H, o);
+                    xs[c] += wv * dj;
+                    xm[c] += fabs(wv * dj);
+                    xu[c] += fabs(wv) * sj;
                 }
+            }
+            for (int32_t c = 0; c < H; ++c) {
+                double sx = xu[c];
+                if (sto) /* the slot holds bf16 of its dgrad result */
+                    xs[c] = round_bf16_with_slack(xs[c], ORACLE_DOT_REL * xm[c], xu[c], &sx);
+                dxt[c] += xs[c];
+                dxm[c] += fabs(xs[c]);
+                sdt[c] += sx;
+            }
+        }
+        for (int32_t c = 0; c < H; ++c) {
+            double sc = sdt[c];
+            if (sto) /* dx = bf16 of the fixed-order fp32 k-sum */
+                dxt[c] = round_bf16_with_slack(dxt[c], K * ORACLE_SUM_ULP * dxm[c], sdt[c], &sc);
+            if (sdx)
+                sdx[t * (int64_t)H + c] = sc;
         }
         free(a);
+        free(ea);
+        free(ua);
         free(g);
-        free(aa);
         free(gg);
+        free(dae);
+        free(dau);
+        free(xs);
+        free(xm);
+        free(xu);
+        free(dxm);
+        free(sdt);
         free(xq);
         free(dyq);
         free(daq);
-        free(dae);
         free(daqs);
+        free(daqe);
+        free(daqc);
+        free(daqb);
     }
 
-    if (dw13 == NULL || dw2 == NULL) {
-        free(da_all);
-        free(sh_all);
-        free(das_all);
-        free(shs_all);
-        return;
-    }
+    if (dw13 != NULL && dw2 != NULL) {
 #pragma omp parallel for schedule(dynamic, 1)
-    for (int32_t e = 0; e < E; ++e) {
-        double *DW13 = dw13 + (int64_t)e * 2 * I * H;
-        double *DW2 = dw2 + (int64_t)e * H * I;
-        memset(DW13, 0, sizeof(double) * (size_t)(2 * (int64_t)I * H));
-        memset(DW2, 0, sizeof(double) * (size_t)((int64_t)H * I));
-        double *S13 = sdw13 ? sdw13 + (int64_t)e * 2 * I * H : NULL;
-        double *S2 = sdw2 ? sdw2 + (int64_t)e * H * I : NULL;
-        if (S13)
-            memset(S13, 0, sizeof(double) * (size_t)(2 * (int64_t)I * H));
-        if (S2)
-            memset(S2, 0, sizeof(double) * (size_t)((int64_t)H * I));
-        for (int64_t f = 0; f < R; ++f) {
-            if (idx[f] != e)
-                continue;
-            const int64_t t = f / K;
-            const double *xt = x + t * (int64_t)H;
-            const double *dyt = dy + t * (int64_t)H;
-            const double *da = da_all + f * 2 * I;
-            const double *sh = sh_all + f * I;
-            for (int32_t j = 0; j < 2 * I; ++j)
+        for (int32_t e = 0; e < E; ++e) {
+            const int64_t n13 = 2 * (int64_t)I * H, n2 = (int64_t)H * I;
+            double *DW13 = dw13 + (int64_t)e * n13;
+            double *DW2 = dw2 + (int64_t)e * n2;
+            /* per element: the sum of absolute terms (dot-product bound) and the slack
+             * carried in from dA and w*h */
+            double *M13 = (double *)calloc((size_t)n13, sizeof(double));
+            double *M2 = (double *)calloc((size_t)n2, sizeof(double));
+            double *U13 = (double *)calloc((size_t)n13, sizeof(double));
+            double *U2 = (double *)calloc((size_t)n2, sizeof(double));
+            memset(DW13, 0, sizeof(double) * (size_t)n13);
+            memset(DW2, 0, sizeof(double) * (size_t)n2);
+            for (int64_t f = 0; f < R; ++f) {
+                if (idx[f] != e)
+                    continue;
+                const int64_t t = f / K;
+                const double *xt = x + t * (int64_t)H;
+                const double *dyt = dy + t * (int64_t)H;
+                const double *da = da_all + f * 2 * I, *das = das_all + f * 2 * I;
+                const double *sh = sh_all + f * I, *shs = shs_all + f * I;
+                for (int32_t j = 0; j < 2 * I; ++j)
+                    for (int32_t c = 0; c < H; ++c) {
+                        const int64_t o = (int64_t)j * H + c;
+                        DW13[o] += da[j] * xt[c];
+                        M13[o] += fabs(da[j] * xt[c]);
+                        U13[o] += das[j] * fabs(xt[c]);
+                    }
                 for (int32_t c = 0; c < H; ++c)
-                    DW13[(int64_t)j * H + c] += da[j] * xt[c];
-            for (int32_t c = 0; c < H; ++c)
-                for (int32_t i = 0; i < I; ++i)
-                    DW2[(int64_t)c * I + i] += dyt[c] * sh[i];
-            if (want_slack && S13 && S2) {
-                for (int32_t j = 0; j < 2 * I; ++j) {
-                    const double sj = das_all[f * 2 * I + j];
-                    if (sj != 0.0)
-                        for (int32_t c = 0; c < H; ++c)
-                            S13[(int64_t)j * H + c] += sj * fabs(xt[c]);
-                }
-                for (int32_t i = 0; i < I; ++i) {
-                    const double si = shs_all[f * I + i];
-                    if (si != 0.0)
-                        for (int32_t c = 0; c < H; ++c)
-                            S2[(int64_t)c * I + i] += fabs(dyt[c]) * si;
-                }
+                    for (int32_t i = 0; i < I; ++i) {
+                        const int64_t o = (int64_t)c * I + i;
+                        DW2[o] += dyt[c] * sh[i];
+                        M2[o] += fabs(dyt[c] * sh[i]);
+                        U2[o] += fabs(dyt[c]) * shs[i];
+                    }
             }
+            double *S13 = sdw13 ? sdw13 + (int64_t)e * n13 : NULL;
+            double *S2 = sdw2 ? sdw2 + (int64_t)e * n2 : NULL;
+            for (int64_t o = 0; o < n13; ++o) {
+                double sl = U13[o];
+                if (sto) /* dW = bf16 of the sum over the expert's rows */
+                    DW13[o] = round_bf16_with_slack(DW13[o], ORACLE_DOT_REL * M13[o], U13[o], &sl);
+                if (S13)
+                    S13[o] = sl;
+            }
+            for (int64_t o = 0; o < n2; ++o) {
+                double sl = U2[o];
+                if (sto)
+                    DW2[o] = round_bf16_with_slack(DW2[o], ORACLE_DOT_REL * M2[o], U2[o], &sl);
+                if (S2)
+                    S2[o] = sl;
+            }
+            free(M13);
+            free(M2);
+            free(U13);
+            free(U2);
         }
     }
     free(da_all);

@@ -62,19 +62,36 @@ void oracle_mxfp8_quantize_bf16(int64_t rows, int64_t cols, const uint16_t *src,
 /* bf16 rounding of a real value: nearest, ties to even, with bf16 subnormals. */
 double oracle_round_bf16(double v);
 
-/* Rounding slack. A kernel computes the value it rounds (h, dA, w*h) in fp32 from fp32 dot
- * products, so its value may differ from the exact one by about ORACLE_DOT_REL times the
- * sum of the dot products' absolute terms (propagated through the SwiGLU formulas), plus
- * ORACLE_SLACK_REL of the value for the elementwise operations. When the exact value lies
- * within that bound of a rounding midpoint, the kernel may round to the other neighbour
- * and both results are correct. The slack of such a decision is the distance between its
- * two possible results (for MXFP8 also when the block's amax lies that close to a power of
- * two, which decides the shared exponent); otherwise it is 0. The forward and backward
- * propagate these slacks linearly (through |weights|, |x|, |dy|) to bounds on how far a
- * correct result may lie from the oracle's; parity tests subtract them before comparing. */
+/* Rounding slack. A kernel computes the value it rounds (h, dA, w*h, a stored result) in
+ * fp32 from fp32 dot products, so its value may differ from the exact one by up to
+ * ORACLE_DOT_REL times the sum of the dot products' absolute terms (propagated through the
+ * SwiGLU formulas), plus ORACLE_SLACK_REL of the value for the elementwise operations. A
+ * fixed-order fp32 sum of n terms (the k-sums of the combine and of dx) is within
+ * n * 2^-24 of the sum of its absolute terms (the textbook bound for recursive summation
+ * with unit roundoff 2^-24). When the exact value lies within its bound of a rounding
+ * midpoint, the kernel may round to the other neighbour and both results are correct. The
+ * slack of such a decision is the distance between its two possible results (for MXFP8
+ * also when the block's amax lies that close to a power of two, which decides the shared
+ * exponent); otherwise it is 0. A value that depends on earlier decisions carries their
+ * slack (propagated linearly through |weights|, |x|, |dy| and the SwiGLU derivatives), and
+ * that slack widens the window in which its own rounding is ambiguous. Parity tests
+ * subtract the resulting per-element slack before comparing.
+ *
+ * ORACLE_DOT_REL is a measured property of the hardware, not of the pages: on GB300 tensor
+ * cores (bf16 operands, fp32 accumulation, K = 320 .. 4096, random-sign terms) the largest
+ * |fp32 result - exact| / sum|terms| seen over 4-8 million outputs per GEMM was 2^-20.2
+ * (median 2^-24); the block-scaled MXFP8 path stayed below 2^-22.5. The oracle takes 2^-19. */
 #define ORACLE_SLACK_REL 9.5367431640625e-07 /* 2^-20 */
-#define ORACLE_DOT_REL 2.384185791015625e-07 /* 2^-22 */
+#define ORACLE_DOT_REL 1.9073486328125e-06   /* 2^-19 */
+#define ORACLE_SUM_ULP 5.9604644775390625e-08 /* 2^-24: fp32 unit roundoff */
 double oracle_bf16_slack(double v, double err);
+
+/* MXFP8 quantize-dequantize of n values (n a multiple of 32) in 32-element blocks, each
+ * value known to within err[i]: out = the dequantized values, slack = the distance to the
+ * other correct result of each decision (see above), q / scale = the codes and E8M0 bytes
+ * (both nullable). */
+void oracle_mxfp8_qdq_slack(int64_t n, const double *v, const double *err, double *out,
+                            double *slack, uint8_t *q, uint8_t *scale);
 
 /* Precision modes ([arex] section "pull 代替 push": the layer has a BF16 and an MXFP8
  * mode; in MXFP8 mode activations are quantized where they enter the GEMMs, at dispatch
@@ -83,42 +100,90 @@ double oracle_bf16_slack(double v, double err);
  *   ORACLE_BF16:  h is rounded to bf16 before the down GEMM (backward: dA and w*h are
  *                 rounded to bf16 before the dgrad and weight-gradient GEMMs);
  *   ORACLE_MXFP8: x is MXFP8-quantized along H before the gate/up GEMM and h along I
- *                 before the down GEMM (forward only). */
+ *                 before the down GEMM (backward: see oracle_backward). */
 enum { ORACLE_EXACT = 0, ORACLE_BF16 = 1, ORACLE_MXFP8 = 2 };
+
+/* Storage of the values that are only stored, never multiplied on the tensor cores: the
+ * expert output of each (token, k) slot, the layer outputs y, dx, dW13, dW2, the saved
+ * gate/up pre-activations A read by the backward, and the per-slot dgrad results.
+ *   ORACLE_STORE_F32:  kept unrounded (a kernel keeps them in fp32);
+ *   ORACLE_STORE_BF16: each is rounded to bf16 where it is stored. [alphalab] section
+ *                      三 benchmarks the layer as a BF16 (or MXFP8) layer and checks its
+ *                      outputs and gradients against a reference within a tolerance; the
+ *                      pages fix no storage type, and the reading here is that such a
+ *                      layer hands bf16 tensors between its steps: o -> bf16 before the
+ *                      weighted k-sum, y = bf16(sum), A -> bf16 before the backward reads
+ *                      it, each slot's dgrad result -> bf16 before the k-sum, dx =
+ *                      bf16(sum), dW = bf16(sum over rows).
+ * In ORACLE_EXACT mode nothing is rounded whatever the storage. */
+enum { ORACLE_STORE_F32 = 0, ORACLE_STORE_BF16 = 1 };
+
+/* Optional per-routed-row intermediates (row f = t*K + k), each pointer nullable:
+ *   a        [R][2I] forward: the exact gate/up pre-activations; backward: A as the
+ *                    backward reads it (bf16 under ORACLE_STORE_BF16)
+ *   a_mag    [R][2I] forward: sum over c of |W13[e][j][c] x[t][c]| (the dot-product bound)
+ *   a_slack  [R][2I] backward: slack of the stored A
+ *   h, h_slack [R][I] forward: h as it enters the down GEMM (bf16 or MXFP8 value)
+ *   h_q [R][I], h_scale [R][I/32]  forward, MXFP8: the codes and scale bytes of h
+ *   da, da_slack [R][2I]  backward: dA rounded to bf16 (the weight-gradient operand)
+ *   sh, sh_slack [R][I]   backward: w*h rounded to bf16
+ *   da_q [R][2I], da_scale [R][2I/32], daq_slack [R][2I]  backward, MXFP8: dA quantized
+ *                    along 2I (the dgrad operand) and the slack of its dequantized value
+ * and optional given values, which replace the oracle's own at the point where they enter
+ * the next step (each with zero slack). They let a test check one step at a time: the
+ * step's own rounding decisions on the values a kernel actually fed it.
+ *   h_in   [R][I]  forward: h as it enters the down GEMM
+ *   a_in   [R][2I] backward: A as the backward reads it
+ *   da_in  [R][2I], sh_in [R][I]  backward: the bf16 dA and w*h of the weight-gradient
+ *                  GEMMs (and, in BF16 mode, dA of the dgrad GEMM)
+ *   daq_in [R][2I] backward, MXFP8: the dequantized dA of the dgrad GEMM */
+typedef struct oracle_rows {
+    double *a, *a_mag, *a_slack;
+    double *h, *h_slack;
+    uint8_t *h_q, *h_scale;
+    double *da, *da_slack, *sh, *sh_slack;
+    uint8_t *da_q, *da_scale;
+    double *daq_slack;
+    const double *h_in, *a_in, *da_in, *sh_in, *daq_in;
+} oracle_rows;
 
 /* Forward of the layer, per token, with no schedule and no permutation:
  *   a = W13[e] x  (gate rows 0..I-1, up rows I..2I-1), h = silu(a_g) * a_u,
  *   o = W2[e] h,  y_t = sum over k ascending of w[t,k] * o_k,
- * with the operand rounding of `mode` (ORACLE_*). Weights are stored as `wkind`
- * (ORACLE_W_*); for ORACLE_W_MXFP8, w13_s and w2_s hold the E8M0 scales along each
- * weight row. x [T][H], idx/w [T][K], w13 [E][2I][H], w2 [E][H][I], y [T][H]. */
+ * with the operand rounding of `mode` (ORACLE_*) and the storage rounding of `store`
+ * (ORACLE_STORE_*). Weights are stored as `wkind` (ORACLE_W_*); for ORACLE_W_MXFP8, w13_s
+ * and w2_s hold the E8M0 scales along each weight row. x [T][H], idx/w [T][K],
+ * w13 [E][2I][H], w2 [E][H][I], y [T][H]; slack [T][H] and rows are nullable. */
 void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
                     const int32_t *idx, const double *w, int32_t wkind, const void *w13,
                     const uint8_t *w13_s, const void *w2, const uint8_t *w2_s, int32_t mode,
-                    double *y, double *slack /* nullable [T][H] */);
+                    int32_t store, double *y, double *slack, oracle_rows *rows);
 
-/* Backward of the BF16 layer by the chain rule, given dy [T][H]:
+/* Backward of the layer by the chain rule, given dy [T][H]:
  *   g = W2[e]^T dy_t, dS[t,k] = <g, h>, dh = w g,
  *   da_g = dh * a_u * silu'(a_g), da_u = dh * silu(a_g),
  *   dx_t = sum_k W13[e]^T da, dW13[e] = sum da x^T, dW2[e] = sum dy (w h)^T
  * ([arex] section "pull 代替 push": router-weight gradient computed with the SwiGLU
  * backward; [alphalab] section 一: expert gradient computation). Sums over routed rows run
- * in ascending flat id. mode is ORACLE_EXACT, ORACLE_BF16 (dA and w*h rounded to bf16
- * where they enter the dgrad and weight-gradient GEMMs) or ORACLE_MXFP8 ([arex] section
- * "pull 代替 push": MXFP8 activations and pre-quantized weights): A is recomputed from the
- * forward's quantized operands (x quantized along H, W13 given as ORACLE_W_MXFP8 with
- * w13_s), G = W2g^T Q(dy) with dy quantized along H and W2g = W2 quantized along H
- * (w2g [E][H][I], dequantized), dx = W13d^T Q(dA) with dA quantized in 32-blocks along 2I
- * and W13d = W13 quantized along 2I (w13d [E][2I][H], dequantized); the weight gradients
- * take dA and w*h rounded to bf16 as in ORACLE_BF16. Weights are ORACLE_W_F64 or
- * ORACLE_W_BF16 (ORACLE_W_MXFP8 for w13 in MXFP8 mode; w13d, w2g are NULL otherwise).
+ * in ascending flat id, sums over k in ascending k. a and h are those of the forward (a
+ * rounded to bf16 first under ORACLE_STORE_BF16, as the backward reads the saved A). mode
+ * is ORACLE_EXACT, ORACLE_BF16 (dA and w*h rounded to bf16 where they enter the dgrad and
+ * weight-gradient GEMMs) or ORACLE_MXFP8 ([arex] section "pull 代替 push": MXFP8
+ * activations and pre-quantized weights): A is recomputed from the forward's quantized
+ * operands (x quantized along H, W13 given as ORACLE_W_MXFP8 with w13_s), G = W2g^T Q(dy)
+ * with dy quantized along H and W2g = W2 quantized along H (w2g [E][H][I], dequantized),
+ * dx = W13d^T Q(dA) with dA quantized in 32-blocks along 2I and W13d = W13 quantized along
+ * 2I (w13d [E][2I][H], dequantized); the weight gradients take dA and w*h rounded to bf16
+ * as in ORACLE_BF16. store is ORACLE_STORE_*. Weights are ORACLE_W_F64 or ORACLE_W_BF16
+ * (ORACLE_W_MXFP8 for w13 in MXFP8 mode; w13d, w2g are NULL otherwise).
  * Outputs: dx [T][H], dw13 [E][2I][H], dw2 [E][H][I], dtopk [T][K] (= dS); dw13/dw2 may be
- * NULL (skipped). */
+ * NULL (skipped); the slacks sdx, sdw13, sdw2 and rows are nullable. */
 void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
                      const int32_t *idx, const double *w, int32_t wkind, const void *w13,
                      const uint8_t *w13_s, const void *w2, const double *dy, int32_t mode,
-                     const double *w13d, const double *w2g, double *dx, double *dw13,
-                     double *dw2, double *dtopk, double *sdx, double *sdw13, double *sdw2);
+                     int32_t store, const double *w13d, const double *w2g, double *dx,
+                     double *dw13, double *dw2, double *dtopk, double *sdx, double *sdw13,
+                     double *sdw2, oracle_rows *rows);
 
 /* Router-logit gradient through the top-k softmax: for a chosen expert j = idx[t,k],
  * dlogits[t,j] = w_k (dS_k - sum_m w_m dS_m); every other logit gets 0. */

@@ -460,7 +460,7 @@ def test_forward_slack_in_the_identity_structure():
     a = x @ w13[0].T
     h = _silu(a[:, :I]) * a[:, I:]
     # the h error bound: dot-product bounds through the partial derivatives of silu(g)*u
-    mag = np.abs(x) @ np.abs(w13[0]).T * 2.0 ** -22
+    mag = np.abs(x) @ np.abs(w13[0]).T * oracle.DOT_REL
     sig = 1 / (1 + np.exp(-a[:, :I]))
     dsl = sig * (1 + a[:, :I] * (1 - sig))
     err = np.abs(dsl * a[:, I:]) * mag[:, :I] + np.abs(_silu(a[:, :I])) * mag[:, I:]
@@ -470,15 +470,17 @@ def test_forward_slack_in_the_identity_structure():
     assert np.all(sl0 == 0.0)  # exact mode rounds nothing
 
 
-def test_backward_slack_zero_in_exact_mode_and_bounds_flipped_operands():
+def test_backward_slack_zero_in_exact_mode():
     T, H, I, E, K = 16, 32, 32, 2, 2
     x, logits, w13, w2 = _rand_layer(T, H, I, E, K, seed=23)
     dy = np.random.default_rng(24).standard_normal((T, H))
     idx, w = oracle.route(logits, K)
-    out0 = oracle.backward(x, idx, w, w13, w2, dy, with_slack=True)
-    assert all(np.all(s == 0) for s in out0[4:])
-    out = oracle.backward(x, idx, w, w13, w2, dy, mode=oracle.BF16, with_slack=True)
-    assert all(np.all(s >= 0) for s in out[4:])
+    for store in (oracle.STORE_F32, oracle.STORE_BF16):
+        out0 = oracle.backward(x, idx, w, w13, w2, dy, with_slack=True, store=store)
+        assert all(np.all(s == 0) for s in out0[4:])
+        ref = oracle.backward(x, idx, w, w13, w2, dy)
+        for a, b in zip(out0[:4], ref):  # nothing is rounded in exact mode
+            np.testing.assert_array_equal(a, b)
 
 
 # ---------------------------------------------------------------- MXFP8 backward
@@ -555,3 +557,291 @@ def test_mxfp8_backward_g_uses_the_quantized_operands():
     _, _, _, dtk_b = oracle.backward(oracle.bf16_to_f64(x), idx, w, w13, w2,
                                      oracle.bf16_to_f64(dy), mode=oracle.BF16)
     assert not np.array_equal(dtk, dtk_b)
+
+
+# ---------------------------------------------------------------- rounding slack
+# The slack of a rounding decision is pinned against a stand-in kernel (tests/emulate.py)
+# that recomputes the layer with numpy and torch and errs, at random, anywhere inside the
+# fp32 bounds the oracle assumes. Each draw is a result a correct kernel could give; the
+# oracle's value must equal it wherever the oracle flags no decision, and lie within the
+# slack of it everywhere. A dropped propagation term, a wrong exponent direction or a
+# missing storage rounding lets some draw escape its slack.
+import emulate  # noqa: E402
+
+
+def _bf16_case(T, H, I, E, K, seed):
+    r = np.random.default_rng(seed)
+    b = lambda a: oracle.bf16_to_f64(f32_to_bf16_bits(a.astype(np.float32)))  # noqa: E731
+    x = b(r.standard_normal((T, H)))
+    w13 = b(r.standard_normal((E, 2 * I, H)) / np.sqrt(H))
+    w2 = b(r.standard_normal((E, H, I)) / np.sqrt(I))
+    dy = b(r.standard_normal((T, H)))
+    idx, w = oracle.route(r.standard_normal((T, E)), K)
+    # routing weights as a kernel holds them (fp32)
+    return x, idx, w.astype(np.float32).astype(np.float64), w13, w2, dy
+
+
+def _covers(draw, ref, slack, what):
+    d = np.abs(draw - ref)
+    # where nothing is flagged the draw is the oracle's value itself
+    assert np.all(d[slack == 0] == 0), (what, int((d[slack == 0] > 0).sum()))
+    assert np.all(d <= slack * (1 + 1e-9)), (what, float((d - slack).max()))
+    return int((d > 0).sum())
+
+
+def _step(v):
+    """bf16 step (ulp) at each value"""
+    return np.ldexp(1.0, np.frexp(np.maximum(np.abs(v), 1e-300))[1] - 8)
+
+
+def _fwd_case(mode):
+    T, H, I, E, K = 24, 64, 64, 4, 2
+    x, idx, w, w13, w2, _ = _bf16_case(T, H, I, E, K, seed=60 + mode)
+    if mode == oracle.MXFP8:  # pre-quantized weights: both sides read the same values
+        w13, w2 = emulate.mx_qdq_rows(w13), emulate.mx_qdq_rows(w2)
+    return x, idx, w, w13, w2
+
+
+@pytest.mark.parametrize("mode", [oracle.BF16, oracle.MXFP8])
+def test_forward_slack_covers_every_kernel_draw(mode):
+    """End to end: the slack of y covers every draw of the stand-in kernel, and the slack
+    of each h decision covers the draw's h."""
+    x, idx, w, w13, w2 = _fwd_case(mode)
+    y, sl, rows = oracle.forward(x, idx, w, w13, w2, mode=mode, with_slack=True,
+                                 store=oracle.STORE_BF16, rows=("h", "h_slack"))
+    np.testing.assert_array_equal(y, emulate.bf16(y))  # y is stored as bf16
+    r = np.random.default_rng(1)
+    moved = 0
+    for _ in range(12):
+        gy, gh = emulate.forward(r, x, idx, w, w13, w2, mode)
+        moved += _covers(gy, y, sl, "y") + _covers(gh, rows["h"], rows["h_slack"], "h")
+    assert moved > 0  # some draws really took the other neighbour
+
+
+@pytest.mark.parametrize("mode", [oracle.BF16, oracle.MXFP8])
+def test_forward_slack_given_h_is_the_down_steps_own(mode):
+    """Given the h a kernel fed its down GEMM, the slack of y is that of the slot and
+    output roundings alone: it covers every draw and is at most two bf16 steps of each
+    weighted slot plus two of y."""
+    x, idx, w, w13, w2 = _fwd_case(mode)
+    r = np.random.default_rng(3)
+    T, K = idx.shape
+    moved = 0
+    for _ in range(6):
+        _, gh = emulate.forward(r, x, idx, w, w13, w2, mode)
+        y, sl = oracle.forward(x, idx, w, w13, w2, mode=mode, with_slack=True,
+                               store=oracle.STORE_BF16, given={"h_in": gh})
+        gy, _ = emulate.forward(r, x, idx, w, w13, w2, mode, h_in=gh)
+        moved += _covers(gy, y, sl, "y")
+        o = np.stack([np.stack([w2[idx[t, k]] @ gh[t * K + k] for k in range(K)])
+                      for t in range(T)])                    # [T, K, H]
+        bound = 2 * (np.abs(w)[:, :, None] * _step(o)).sum(1) + 2 * _step(y)
+        assert np.all(sl <= bound)
+    assert moved > 0
+
+
+@pytest.mark.parametrize("mode", [oracle.BF16, oracle.MXFP8])
+def test_backward_slack_covers_every_kernel_draw(mode):
+    T, H, I, E, K = 16, 64, 64, 3, 2
+    x, idx, w, w13, w2, dy = _bf16_case(T, H, I, E, K, seed=70 + mode)
+    bits = lambda a: f32_to_bf16_bits(a.astype(np.float32))  # noqa: E731
+    w13b, w2b = (bits(w13), bits(w2)) if mode == oracle.MXFP8 else (w13, w2)
+    names = ("a", "a_slack", "da", "da_slack", "sh", "sh_slack")
+    dx, dw13, dw2, _, sdx, s13, s2, rows = oracle.backward(
+        x, idx, w, w13b, w2b, dy, mode=mode, with_slack=True, store=oracle.STORE_BF16,
+        rows=names)
+    r = np.random.default_rng(2)
+    moved = 0
+    for _ in range(6):
+        gx, g13, g2, gr = emulate.backward(r, x, idx, w, w13, w2, dy, mode)
+        moved += _covers(gx, dx, sdx, "dx") + _covers(g13, dw13, s13, "dw13") + \
+            _covers(g2, dw2, s2, "dw2") + _covers(gr["a"], rows["a"], rows["a_slack"], "a")
+    assert moved > 0
+
+
+@pytest.mark.parametrize("mode", [oracle.BF16, oracle.MXFP8])
+def test_backward_slack_given_each_steps_inputs(mode):
+    """Step by step: given the kernel's A, the slacks of dA and w*h cover every draw of its
+    dA and w*h; given also its dA and w*h (and MXFP8 dgrad operand), the slacks of dx, dW13
+    and dW2 cover every draw of its results. Each slack is at most twice the spread the
+    draws reach plus two bf16 steps: no wider than the decisions the kernel can take."""
+    T, H, I, E, K = 16, 64, 64, 3, 2
+    x, idx, w, w13, w2, dy = _bf16_case(T, H, I, E, K, seed=74 + mode)
+    bits = lambda a: f32_to_bf16_bits(a.astype(np.float32))  # noqa: E731
+    w13b, w2b = (bits(w13), bits(w2)) if mode == oracle.MXFP8 else (w13, w2)
+    r = np.random.default_rng(4)
+
+    def tight(sl, ref, spread, what):
+        assert np.all(sl <= 2 * spread + 2 * _step(ref)), what
+
+    _, _, _, g0 = emulate.backward(r, x, idx, w, w13, w2, dy, mode)
+    *_, rows = oracle.backward(x, idx, w, w13b, w2b, dy, mode=mode, store=oracle.STORE_BF16,
+                               given={"a_in": g0["a"]},
+                               rows=("da", "da_slack", "sh", "sh_slack"))
+    sp_da = np.zeros_like(rows["da"])
+    sp_sh = np.zeros_like(rows["sh"])
+    moved = 0
+    for _ in range(10):
+        _, _, _, gr = emulate.backward(r, x, idx, w, w13, w2, dy, mode, given={"a_in": g0["a"]})
+        moved += _covers(gr["da"], rows["da"], rows["da_slack"], "da")
+        moved += _covers(gr["sh"], rows["sh"], rows["sh_slack"], "sh")
+        sp_da = np.maximum(sp_da, np.abs(gr["da"] - rows["da"]))
+        sp_sh = np.maximum(sp_sh, np.abs(gr["sh"] - rows["sh"]))
+    tight(rows["da_slack"], rows["da"], sp_da, "da")
+    tight(rows["sh_slack"], rows["sh"], sp_sh, "sh")
+    # dx, dW given every operand the kernel fed its dgrad and weight-gradient GEMMs
+    given = {"a_in": gr["a"], "da_in": gr["da"], "sh_in": gr["sh"]}
+    if mode == oracle.MXFP8:
+        given["daq_in"] = gr["daq"]
+    dx, dw13, dw2, _, sdx, s13, s2 = oracle.backward(
+        x, idx, w, w13b, w2b, dy, mode=mode, with_slack=True, store=oracle.STORE_BF16,
+        given=given)
+    sp = [np.zeros_like(dx), np.zeros_like(dw13), np.zeros_like(dw2)]
+    slot_steps = np.zeros_like(dx)
+    for _ in range(10):
+        *outs, gr = emulate.backward(r, x, idx, w, w13, w2, dy, mode, given=given)
+        for i, (g, ref, sl, nm) in enumerate(zip(outs, (dx, dw13, dw2), (sdx, s13, s2),
+                                                 ("dx", "dw13", "dw2"))):
+            moved += _covers(g, ref, sl, nm)
+            sp[i] = np.maximum(sp[i], np.abs(g - ref))
+        slot_steps = np.maximum(slot_steps, _step(gr["slot"]).reshape(T, K, H).sum(1))
+    # dx sums K rounded slots: each may be a step or two off, whatever the size of dx
+    tight(sdx, dx, sp[0] + slot_steps, "dx")
+    tight(s13, dw13, sp[1], "dw13")
+    tight(s2, dw2, sp[2], "dw2")
+    assert moved > 0
+
+
+def test_storage_rounding_is_where_the_definition_puts_it():
+    """With one expert, K=1, weight 1, W2 = identity (H = I): the slot is bf16(h), which is
+    already bf16, and y = bf16(h); with two experts at weights 1/2, y = bf16(o_0/2 + o_1/2)
+    of the two rounded slots. A missing or extra rounding changes these values."""
+    T, H, I = 32, 32, 32
+    r = np.random.default_rng(80)
+    x = r.standard_normal((T, H))
+    w13 = r.standard_normal((2, 2 * I, H)) * 0.3
+    w2 = np.stack([np.eye(H), np.eye(H) * 1.5])
+    _, rows = oracle.forward(x, np.zeros((T, 1), np.int32), np.ones((T, 1)), w13[:1], w2[:1],
+                             mode=oracle.BF16, store=oracle.STORE_BF16, rows=("h",))
+    y1 = oracle.forward(x, np.zeros((T, 1), np.int32), np.ones((T, 1)), w13[:1], w2[:1],
+                        mode=oracle.BF16, store=oracle.STORE_BF16)
+    np.testing.assert_array_equal(y1, rows["h"])
+    idx = np.tile(np.array([[0, 1]], np.int32), (T, 1))
+    y2, rows2 = oracle.forward(x, idx, np.full((T, 2), 0.5), w13, w2, mode=oracle.BF16,
+                               store=oracle.STORE_BF16, rows=("h",))
+    h = rows2["h"].reshape(T, 2, I)
+    o1 = emulate.bf16(1.5 * h[:, 1])  # slot of expert 1: bf16 of 1.5 h
+    np.testing.assert_array_equal(y2, emulate.bf16(0.5 * h[:, 0] + 0.5 * o1))
+    assert not np.array_equal(o1, 1.5 * h[:, 1])  # that slot rounding is not a no-op
+
+
+def test_backward_reads_the_saved_pre_activations_in_bf16():
+    """Under bf16 storage the backward's A is bf16(W13 x), and dS = <G, silu(A_g) A_u>
+    uses it; under fp32 storage A is exact."""
+    T, H, I, E, K = 8, 64, 32, 2, 1
+    x, idx, w, w13, w2, dy = _bf16_case(T, H, I, E, K, seed=81)
+    for store in (oracle.STORE_F32, oracle.STORE_BF16):
+        *_, dtk, rows = oracle.backward(x, idx, w, w13, w2, dy, mode=oracle.BF16,
+                                        store=store, rows=("a",))
+        a = np.stack([w13[idx[t, 0]] @ x[t] for t in range(T)])
+        want = emulate.bf16(a) if store == oracle.STORE_BF16 else a
+        near = np.abs(rows["a"] - want) > 0
+        assert near.mean() < 0.01  # only values within fp32 error of a bf16 midpoint
+        ag, au = rows["a"][:, :I], rows["a"][:, I:]
+        g = np.stack([w2[idx[t, 0]].T @ dy[t] for t in range(T)])
+        np.testing.assert_allclose(dtk[:, 0], (g * _silu(ag) * au).sum(1), rtol=1e-12)
+
+
+def _mx_block_exp(v):
+    return int(np.frexp(np.abs(v).max())[1] - 1 - 8)
+
+
+def _e4m3_torch(u):
+    return torch.tensor(np.clip(u, -448, 448)).float().to(torch.float8_e4m3fn).double().numpy()
+
+
+def test_mxfp8_slack_near_a_power_of_two_is_the_other_exponents_result():
+    r = np.random.default_rng(90)
+    blk = r.uniform(-0.9, 0.9, 32)
+    blk[7] = 1.0 - 2.0 ** -20            # amax just below 1: exponent -9, or -8 above 1
+    err = np.full(32, 2.0 ** -18)        # the error reaches across 1.0
+    out, sl, q, sc = oracle.mxfp8_qdq_slack(blk[None], err[None])
+    s = _mx_block_exp(blk)
+    assert s == -9 and sc[0, 0] == 127 - 9
+    chosen = np.ldexp(_e4m3_torch(np.ldexp(blk, -s)), s)
+    alt = np.ldexp(_e4m3_torch(np.ldexp(blk, -(s + 1))), s + 1)
+    np.testing.assert_array_equal(out[0], chosen)
+    # no code decision is near a midpoint here, so the slack is the exponent alternative
+    u = np.ldexp(blk, -s)
+    sp = np.ldexp(1.0, np.maximum(np.frexp(np.abs(u))[1] - 1, -6) - 3)
+    frac = np.abs(u) / sp - np.floor(np.abs(u) / sp)
+    assert np.all(np.abs(frac - 0.5) * sp > np.ldexp(err, -s) + 2.0 ** -20 * np.abs(u))
+    ua = np.ldexp(blk, -(s + 1))
+    spa = np.ldexp(1.0, np.maximum(np.frexp(np.abs(ua))[1] - 1, -6) - 3)
+    fa = np.abs(ua) / spa - np.floor(np.abs(ua) / spa)
+    clear = np.abs(fa - 0.5) * spa > np.ldexp(err, -(s + 1)) + 2.0 ** -20 * np.abs(ua)
+    np.testing.assert_array_equal(sl[0][clear], np.abs(alt - chosen)[clear])
+    assert np.all(sl[0] >= np.abs(alt - chosen))
+    assert np.abs(alt - chosen).max() > 0
+
+
+def test_mxfp8_slack_zero_far_from_every_decision_and_one_step_at_a_midpoint():
+    s = -8  # amax in [1, 2)
+    codes = np.array([1.0, 1.125, 1.25, 1.5, -1.75, 0.5, 0.625, -0.25] * 4)
+    blk = np.ldexp(codes, s + 8) * 1.0  # exactly representable: far from every midpoint
+    blk[0] = 1.5 * 1.0                  # amax 1.5: exponent -8, not near a power of two
+    err = np.full(32, 2.0 ** -30)
+    out, sl, _, _ = oracle.mxfp8_qdq_slack(blk[None], err[None])
+    np.testing.assert_array_equal(out[0], blk)
+    assert np.all(sl == 0)
+    mid = blk.copy()
+    mid[3] = (1.5 + 1.625) / 2           # a code midpoint (ties to even: 1.5)
+    out, sl, _, _ = oracle.mxfp8_qdq_slack(mid[None], err[None])
+    assert out[0, 3] == 1.5 and sl[0, 3] == 0.125
+    assert np.all(np.delete(sl[0], 3) == 0)
+
+
+def test_mxfp8_slack_covers_random_perturbations():
+    r = np.random.default_rng(91)
+    v = r.standard_normal((400, 64)) * np.exp(r.uniform(-5, 5, (400, 1)))
+    # push some block maxima onto powers of two and some values onto code midpoints
+    v[::7, 0] = np.ldexp(1.0, r.integers(-5, 5, v[::7, 0].shape)) * (1 - 2.0 ** -22)
+    err = np.abs(v) * 2.0 ** -19
+    out, sl, _, _ = oracle.mxfp8_qdq_slack(v, err)
+    moved = 0
+    for _ in range(20):
+        p = v + err * r.uniform(-1, 1, v.shape)
+        d = np.abs(emulate.mx_qdq_rows(p) - out)
+        assert np.all(d[sl == 0] == 0)
+        assert np.all(d <= sl * (1 + 1e-12))
+        moved += int((d > 0).sum())
+    assert moved > 0
+
+
+def test_mxfp8_dgrad_reads_da_quantized_along_2i():
+    """dx of the MXFP8 backward (fp32 storage, nothing else rounded on its path) is
+    sum_k W13q^T Q(dA) with W13 quantized along 2I (an explicit transpose fed to the row
+    quantizer) and dA quantized in 32-blocks along 2I, dA computed here from the forward's
+    quantized operands; the same sum with unquantized dA is far from it."""
+    T, H, I, E, K = 6, 64, 64, 2, 2
+    x, idx, w, w13, w2, dy = _bf16_case(T, H, I, E, K, seed=92)
+    bits = lambda a: f32_to_bf16_bits(a.astype(np.float32))  # noqa: E731
+    dx, *_ = oracle.backward(x, idx, w, bits(w13), bits(w2), dy, mode=oracle.MXFP8)
+    rowq = lambda m: oracle.mxfp8_dequantize(*oracle.mxfp8_quantize(m))  # noqa: E731
+    tq = lambda m: np.swapaxes(rowq(np.ascontiguousarray(np.swapaxes(m, -1, -2))), -1, -2)  # noqa
+    xq, dyq, w13h = rowq(x), rowq(dy), rowq(w13)
+    w13i, w2h = tq(w13), tq(w2)
+    ref = np.zeros_like(dx)
+    ref_plain = np.zeros_like(dx)
+    for t in range(T):
+        for k in range(K):
+            e, s = idx[t, k], w[t, k]
+            a = w13h[e] @ xq[t]
+            ag, au = a[:I], a[I:]
+            g = w2h[e].T @ dyq[t]
+            sig = 1 / (1 + np.exp(-ag))
+            da = np.concatenate([s * g * au * sig * (1 + ag * (1 - sig)), s * g * ag * sig])
+            ref[t] += w13i[e].T @ rowq(da[None])[0]
+            ref_plain[t] += w13i[e].T @ da
+    np.testing.assert_allclose(dx, ref, rtol=1e-11, atol=1e-13)
+    assert np.abs(ref - ref_plain).max() > 1e-3 * np.abs(ref).max()

@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define MOK_ABI_VERSION 1u
+#define MOK_ABI_VERSION 2u
 
 typedef enum mok_status {
     MOK_OK = 0,
@@ -61,6 +61,16 @@ typedef enum mok_precision {
     MOK_BF16 = 0, /* bf16 operands, fp32 accumulation */
     MOK_MXFP8 = 1 /* E4M3 operands with an E8M0 scale per 32 elements along K */
 } mok_precision;
+
+/* mok_config.flags */
+/* Keep every value that is only stored, never fed to a tensor-core GEMM, in fp32 instead of
+ * bf16: the expert output of each (token, k) slot, the outputs y, dx, dw13, dw2 (and the
+ * shared expert's), the saved pre-activations and the per-slot dgrad results. Without the
+ * flag they are bf16 (round to nearest even of the fp32 accumulation), the storage a BF16
+ * layer hands between its steps ([alphalab] section 三: the layer is benchmarked as a BF16
+ * or MXFP8 layer and checked against a reference within a tolerance). Every accumulation
+ * is fp32 either way; the flag changes what is stored and what later steps read. */
+#define MOK_FLAG_FP32_STORAGE 1u
 
 typedef enum mok_workspace_kind {
     MOK_WS_SCHEDULE = 0,
@@ -89,7 +99,8 @@ typedef struct mok_config {
      * minibatch; in MXFP8 each pass fills the whole ring. Results are the same bit for bit
      * for every ring setting. No routed row is ever dropped. */
     int32_t ring_capacity;
-    int32_t prec; /* mok_precision of the forward; the backward is MOK_BF16 */
+    int32_t prec;   /* mok_precision of the forward; the backward is MOK_BF16 */
+    uint32_t flags; /* MOK_FLAG_* (0: bf16 storage) */
 } mok_config;
 
 /* The schedule table ([arex] section "pull 代替 push": one schedule serves dispatch,
@@ -128,6 +139,53 @@ int64_t mok_segment_capacity(const mok_config *cfg);
  * must be 256-byte aligned; its contents on entry do not matter. */
 size_t mok_workspace_size(const mok_config *cfg, int which);
 
+/* Intermediates a call leaves in its workspace, for inspection and testing (the pages have
+ * no counterpart; the layer's own outputs never need them). Rows are sorted rows (the
+ * schedule's order) in the forward, padded rows in the backward (expert e owns rows
+ * [poff[e], poff[e+1]), its counts[e] real rows first, poff[e] = sum over experts before e
+ * of counts rounded up to 16). After a forward that ran as one pass (the ring holds every
+ * routed row) the ring rows are all R sorted rows; after one in several passes they hold
+ * the last pass's rows (ring slots as described for ring_capacity).
+ *   MOK_ITEM_X_RING       forward: gathered x [ring rows][H], bf16 or (MXFP8) E4M3
+ *   MOK_ITEM_X_RING_SCALE forward, MXFP8: its E8M0 scales [ring rows][H/32]
+ *   MOK_ITEM_H_RING       forward: h entering the down GEMM [ring rows][I], bf16 or E4M3
+ *                         (after a forward in several passes: the copy of the last pass
+ *                         with an even index)
+ *   MOK_ITEM_H_RING_SCALE forward, MXFP8: its E8M0 scales [ring rows][I/32]
+ *   MOK_ITEM_SLOTS        forward: expert output of each flat id t*K + k [R][H] (bf16, or
+ *                         fp32 under MOK_FLAG_FP32_STORAGE); backward: the per-slot dgrad
+ *                         results, likewise
+ *   MOK_ITEM_PAD_OFFSETS  backward: poff [E+1] int32
+ *   MOK_ITEM_DA           backward: dA = dL/d(gate, up) [padded rows][2I] bf16
+ *   MOK_ITEM_WH           backward: topk_w * h [padded rows][I] bf16
+ *   MOK_ITEM_DA_Q         backward, MXFP8: dA quantized along 2I [padded rows][2I] E4M3
+ *   MOK_ITEM_DA_SCALE     backward, MXFP8: its E8M0 scales [padded rows][2I/32]
+ *   MOK_ITEM_DY_Q         backward, MXFP8: dy quantized along H [padded rows][H] E4M3
+ *   MOK_ITEM_DY_SCALE     backward, MXFP8: its E8M0 scales [padded rows][H/32]
+ * For the shared expert (MOK_WS_SHARED / MOK_WS_SHARED_BACKWARD) the rows are token rows:
+ *   MOK_ITEM_H_RING (bf16 h [T][I], or E4M3 with MOK_ITEM_H_RING_SCALE), MOK_ITEM_X_RING /
+ *   MOK_ITEM_X_RING_SCALE (MXFP8 x [T][H]); backward MOK_ITEM_DA, MOK_ITEM_WH (rows padded
+ *   to a multiple of 16), MOK_ITEM_DA_Q / _SCALE, MOK_ITEM_DY_Q / _SCALE.
+ * Sets *offset (bytes from the workspace start) and *bytes. Host only. MOK_ERR_INVALID_ARG
+ * for an invalid configuration, workspace kind or item, or an item that kind (or that
+ * precision) does not hold. */
+typedef enum mok_ws_item {
+    MOK_ITEM_X_RING = 0,
+    MOK_ITEM_X_RING_SCALE = 1,
+    MOK_ITEM_H_RING = 2,
+    MOK_ITEM_H_RING_SCALE = 3,
+    MOK_ITEM_SLOTS = 4,
+    MOK_ITEM_PAD_OFFSETS = 5,
+    MOK_ITEM_DA = 6,
+    MOK_ITEM_WH = 7,
+    MOK_ITEM_DA_Q = 8,
+    MOK_ITEM_DA_SCALE = 9,
+    MOK_ITEM_DY_Q = 10,
+    MOK_ITEM_DY_SCALE = 11
+} mok_ws_item;
+mok_status mok_workspace_item(const mok_config *cfg, int which, int item, size_t *offset,
+                              size_t *bytes);
+
 /* ---- the hot path --------------------------------------------------------------- */
 
 /* Top-k routing ([alphalab] section 四: top-k over router logits).
@@ -164,7 +222,9 @@ mok_status mok_build_schedule(const mok_config *cfg, const int32_t *topk_idx,
  *     anything is enqueued (with E = 512 that is more than 2,097,152 routed rows).
  *   - Every call shares the one array and leaves its contents behind; nothing in it needs
  *     to start at zero. Calls whose work overlaps on the GPU (other streams, other host
- *     threads) race on the array and give undefined results: order them on one stream. */
+ *     threads) race on the array and give undefined results: order them on one stream.
+ *   - While profiling is on (mok_profile_enable), its kernels are timed under the same kind
+ *     as mok_build_schedule's. */
 #define MOK_NOALLOC_SCHEDULE_SCRATCH_BYTES (4u << 20)
 mok_status mok_build_schedule_noalloc(const mok_config *cfg, const int32_t *topk_idx,
                                       const mok_schedule *sched, cudaStream_t stream);
@@ -182,12 +242,15 @@ mok_status mok_build_schedule_noalloc(const mok_config *cfg, const int32_t *topk
  *          x is quantized to MXFP8 along H inside the gather and h along I inside the
  *          gate/up GEMM's epilogue ([arex] section "pull 代替 push": weights pre-quantized,
  *          activation quantization fused into dispatch, GEMM and SwiGLU).
- *   y       [T][H] fp32 out: y[t] = sum over k = 0..K-1, in that order, of
- *           topk_w[t,k] * o[t,k], fp32 throughout (o is the fp32 down-GEMM result).
- *   saved_preact  NULL, or [R][2I] fp32 out: the gate/up GEMM result of sorted row r
- *           (needed by mok_backward, or by mok_backward_mxfp8 after an MXFP8 forward).
+ *   y       [T][H] bf16 out (fp32 under MOK_FLAG_FP32_STORAGE): y[t] = sum over
+ *           k = 0..K-1, in that order, of topk_w[t,k] * o[t,k] in fp32, rounded once at the
+ *           end; o[t,k] is the down GEMM's fp32 result stored in the (t, k) slot as bf16
+ *           (fp32 under the flag).
+ *   saved_preact  NULL, or [R][2I] bf16 out (fp32 under the flag): the gate/up GEMM result
+ *           of sorted row r (needed by mok_backward, or by mok_backward_mxfp8 after an
+ *           MXFP8 forward, with the same flags).
  * GEMMs accumulate in fp32; values that are only stored (expert outputs, saved
- * pre-activations) stay fp32.
+ * pre-activations, y) take the storage type of cfg->flags.
  * A ring smaller than R rows (cfg->ring_capacity) makes the forward run in passes of
  * sorted rows: cfg->minibatch rows per pass in BF16, the whole ring in MXFP8 (results are
  * the same bit for bit either way). Then each pass's down GEMM runs on a second stream that
@@ -209,14 +272,18 @@ mok_status mok_forward(const mok_config *cfg, const void *x, const mok_schedule 
  * pull reverse-combine, push reverse-dispatch, router-weight gradient fused into the
  * SwiGLU backward; [alphalab] section 一: expert gradient computation).
  *   x, topk_w, w13, w2 as in mok_forward (BF16), dy [T][H] bf16 upstream gradient.
- *   saved_preact  [R][2I] fp32 from mok_forward, or NULL: the backward then recomputes
+ *   saved_preact  [R][2I] from mok_forward (bf16, or fp32 under MOK_FLAG_FP32_STORAGE; the
+ *            flags must match the forward's), or NULL: the backward then recomputes
  *            the gate/up GEMM from x and W13 ([alphalab] section 一, the backward's
  *            recompute of forward activations), with the same tiles and accumulation order
  *            as the forward, so the results are those of the saved-A path. The workspace
  *            must then be of size mok_workspace_size(cfg, MOK_WS_BACKWARD_RECOMPUTE),
- *            which adds an [R][2I] fp32 buffer for the recomputed pre-activations.
- *   dx       [T][H] fp32 out (sum over k in order of the fp32 per-slot dgrad results).
- *   dw13     [E][2I][H] fp32 out, dw2 [E][H][I] fp32 out (experts with no rows get 0).
+ *            which adds an [R][2I] buffer for the recomputed pre-activations (stored as
+ *            a saved one would be).
+ *   dx       [T][H] bf16 out (fp32 under the flag): the fp32 sum over k in order of the
+ *            per-slot dgrad results, each stored as bf16 (fp32 under the flag), rounded once.
+ *   dw13     [E][2I][H], dw2 [E][H][I] bf16 out (fp32 under the flag): fp32 sums over each
+ *            expert's rows in ascending flat id, rounded once (experts with no rows get 0).
  *   d_topk_w [T][K] fp32 out: dL/dtopk_w.
  *   d_logits NULL or [T][E] fp32 out: gradient through the top-k softmax (0 for logits
  *            that were not chosen).
@@ -232,7 +299,7 @@ mok_status mok_backward(const mok_config *cfg, const void *x, const mok_schedule
  * that saved its pre-activations (required here). The G GEMM contracts over H with dy and
  * W2 quantized along H; the dgrad GEMM over 2I with dA and W13 quantized along 2I (dA is
  * quantized in the G GEMM's epilogue). The weight-gradient GEMMs stay BF16 (dA and w*h
- * rounded to bf16): their time is the fp32 dW writes, which MXFP8 would not shorten.
+ * rounded to bf16), as in mok_backward.
  *   w13t_q [E][H][2I] E4M3, w13t_s [E][H][2I/32]: W13 quantized along 2I, transposed;
  *   w2t_q  [E][I][H] E4M3,  w2t_s  [E][I][H/32]:  W2 quantized along H, transposed (both as
  *          made by mok_quantize_mxfp8_transposed from the bf16 weights).
@@ -249,13 +316,16 @@ mok_status mok_backward_mxfp8(const mok_config *cfg, const void *x, const mok_sc
  * forward runs the FFN/SwiGLU of the shared and of the routed experts). Every token passes
  * through one more SwiGLU expert, with weight one and no routing, and its output is added
  * to y after the routed combine:
- *   y[t] += W2s (silu(W13s[0:I] x_t) * W13s[I:2I] x_t)      (fp32 add, one writer per element)
+ *   y[t] += W2s (silu(W13s[0:I] x_t) * W13s[I:2I] x_t)      (one writer per element)
  * The shared expert has the routed experts' shape (H, I of cfg) and the mode's operand
  * rounding (h to bf16 before the down GEMM).
  *   x              [T][H] bf16, as for mok_forward.
  *   w13_s          [2I][H] bf16 (gate rows, then up rows); w2_s [H][I] bf16.
- *   y              [T][H] fp32, in and out (typically mok_forward's result).
- *   saved_preact_s NULL, or [T][2I] fp32 out: the shared expert's gate/up GEMM result.
+ *   y              [T][H], in and out (typically mok_forward's result): bf16, the fp32
+ *                  down-GEMM result added to it in fp32 and rounded once (fp32 storage
+ *                  under MOK_FLAG_FP32_STORAGE).
+ *   saved_preact_s NULL, or [T][2I] out (bf16, or fp32 under the flag): the shared
+ *                  expert's gate/up GEMM result.
  *   ws             at least mok_workspace_size(cfg, MOK_WS_SHARED) bytes.
  * BF16 (cfg->prec == MOK_BF16, else MOK_ERR_UNSUPPORTED; MXFP8 configurations use
  * mok_shared_expert_forward_mxfp8). Asynchronous on `stream`. */
@@ -279,14 +349,15 @@ mok_status mok_shared_expert_forward_mxfp8(const mok_config *cfg, const void *x,
 /* Shared expert, backward: the gradients of y += W2s (silu(W13s[0:I] x) * W13s[I:2I] x)
  * for every token, by the chain rule of mok_backward with one expert, weight one and no
  * router gradient ([alphalab] section 一: the backward's expert gradient computation):
- *   dx[t] += W13s^T dA_t                                    (fp32 add after the routed dx)
+ *   dx[t] += W13s^T dA_t                                    (added after the routed dx)
  *   dw13_s = sum_t dA_t x_t^T, dw2_s = sum_t dy_t h_t^T      (sums over t ascending)
  * with G = W2s^T dy_t, dA = (G * u * silu'(g), G * silu(g)) from the saved gate/up result
  * (g, u), and dA and h rounded to bf16 where they enter GEMMs, as in mok_backward.
- *   x, w13_s, w2_s as for mok_shared_expert_forward; saved_preact_s [T][2I] fp32 from it
- *   (required); dy [T][H] bf16.
- *   dx      [T][H] fp32, in and out (typically mok_backward's result).
- *   dw13_s  [2I][H] fp32 out; dw2_s [H][I] fp32 out.
+ *   x, w13_s, w2_s as for mok_shared_expert_forward; saved_preact_s [T][2I] from it
+ *   (required, same flags); dy [T][H] bf16.
+ *   dx      [T][H], in and out (typically mok_backward's result): bf16, the fp32 dgrad
+ *           result added in fp32 and rounded once (fp32 under MOK_FLAG_FP32_STORAGE).
+ *   dw13_s  [2I][H] out; dw2_s [H][I] out (bf16, or fp32 under the flag).
  *   ws      at least mok_workspace_size(cfg, MOK_WS_SHARED_BACKWARD) bytes.
  * BF16 (cfg->prec == MOK_BF16, else MOK_ERR_UNSUPPORTED; MXFP8 configurations use
  * mok_shared_expert_backward_mxfp8). Asynchronous on `stream`. */
@@ -301,7 +372,7 @@ mok_status mok_shared_expert_backward(const mok_config *cfg, const void *x, cons
  *   w13st_q [H][2I] E4M3 with w13st_scale [H][2I/32]; w2st_q [I][H] E4M3 with w2st_scale
  *   [I][H/32] (mok_quantize_mxfp8_transposed of W13s with batch 1, rows 2I, cols H, and of
  *   W2s with rows H, cols I).
- *   saved_preact_s [T][2I] fp32 as written by mok_shared_expert_forward_mxfp8: required.
+ *   saved_preact_s [T][2I] as written by mok_shared_expert_forward_mxfp8: required.
  *   Other arguments as for mok_shared_expert_backward; ws at least
  *   mok_workspace_size(cfg, MOK_WS_SHARED_BACKWARD) for this (MXFP8) configuration. */
 mok_status mok_shared_expert_backward_mxfp8(const mok_config *cfg, const void *x,

@@ -12,7 +12,10 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libmok.so")
 
-MOK_ABI_VERSION = 1
+MOK_ABI_VERSION = 2
+
+# mok_config.flags
+MOK_FLAG_FP32_STORAGE = 1
 
 # mok_status
 MOK_OK = 0
@@ -36,6 +39,20 @@ MOK_WS_BACKWARD_RECOMPUTE = 3
 MOK_WS_SHARED = 4
 MOK_WS_SHARED_BACKWARD = 5
 
+# mok_ws_item
+MOK_ITEM_X_RING = 0
+MOK_ITEM_X_RING_SCALE = 1
+MOK_ITEM_H_RING = 2
+MOK_ITEM_H_RING_SCALE = 3
+MOK_ITEM_SLOTS = 4
+MOK_ITEM_PAD_OFFSETS = 5
+MOK_ITEM_DA = 6
+MOK_ITEM_WH = 7
+MOK_ITEM_DA_Q = 8
+MOK_ITEM_DA_SCALE = 9
+MOK_ITEM_DY_Q = 10
+MOK_ITEM_DY_SCALE = 11
+
 EXPORTED = [
     "mok_abi_version", "mok_status_string", "mok_check_config", "mok_segment_capacity",
     "mok_workspace_size", "mok_route_topk", "mok_build_schedule", "mok_forward",
@@ -44,7 +61,7 @@ EXPORTED = [
     "mok_build_schedule_noalloc", "mok_shared_expert_forward",
     "mok_quantize_mxfp8_transposed", "mok_backward_mxfp8", "mok_shared_expert_backward",
     "mok_shared_expert_forward_mxfp8", "mok_shared_expert_backward_mxfp8",
-    "mok_selftest_bounded_wait",
+    "mok_selftest_bounded_wait", "mok_workspace_item",
 ]
 
 # bytes of the fixed scratch array behind mok_build_schedule_noalloc
@@ -55,7 +72,7 @@ class MokConfig(ctypes.Structure):
     _fields_ = [("abi_version", ctypes.c_uint32), ("T", ctypes.c_int32), ("H", ctypes.c_int32),
                 ("I", ctypes.c_int32), ("E", ctypes.c_int32), ("K", ctypes.c_int32),
                 ("minibatch", ctypes.c_int32), ("ring_capacity", ctypes.c_int32),
-                ("prec", ctypes.c_int32)]
+                ("prec", ctypes.c_int32), ("flags", ctypes.c_uint32)]
 
 
 class MokSchedule(ctypes.Structure):
@@ -91,6 +108,8 @@ def lib():
             "mok_check_config": ([cfgp], ctypes.c_int),
             "mok_segment_capacity": ([cfgp], i64),
             "mok_workspace_size": ([cfgp, ctypes.c_int], sz),
+            "mok_workspace_item": ([cfgp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(sz),
+                                    ctypes.POINTER(sz)], ctypes.c_int),
             "mok_route_topk": ([cfgp, p, p, p, p], ctypes.c_int),
             "mok_build_schedule": ([cfgp, p, schp, p, sz, p], ctypes.c_int),
             "mok_build_schedule_noalloc": ([cfgp, p, schp, p], ctypes.c_int),
@@ -144,8 +163,8 @@ def _stream(s):
 
 
 def make_config(T, H, I, E, K, minibatch=2368, ring_capacity=0, prec=MOK_BF16,
-                abi_version=MOK_ABI_VERSION) -> MokConfig:
-    return MokConfig(abi_version, T, H, I, E, K, minibatch, ring_capacity, prec)
+                abi_version=MOK_ABI_VERSION, flags=0) -> MokConfig:
+    return MokConfig(abi_version, T, H, I, E, K, minibatch, ring_capacity, prec, flags)
 
 
 def make_schedule(counts, offsets, perm, inv, segs, n_segs) -> MokSchedule:
@@ -178,6 +197,15 @@ def mok_segment_capacity(cfg) -> int:
 
 def mok_workspace_size(cfg, which) -> int:
     return int(lib().mok_workspace_size(ctypes.byref(cfg), int(which)))
+
+
+def mok_workspace_item(cfg, which, item):
+    """(status, offset, bytes) of an intermediate inside a workspace (see include/mok.h)."""
+    off = ctypes.c_size_t(0)
+    n = ctypes.c_size_t(0)
+    st = lib().mok_workspace_item(ctypes.byref(cfg), int(which), int(item), ctypes.byref(off),
+                                  ctypes.byref(n))
+    return st, off.value, n.value
 
 
 def mok_route_topk(cfg, logits, topk_idx, topk_w, stream=None) -> int:

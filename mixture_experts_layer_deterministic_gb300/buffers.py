@@ -37,12 +37,26 @@ def workspace(cfg, which, device):
     return _empty(n, torch.uint8, device), n
 
 
+def workspace_item(ws, cfg, which, item):
+    """The bytes of one intermediate inside workspace tensor `ws` (a uint8 view, see
+    mok_workspace_item); callers view it with the item's dtype and shape."""
+    st, off, n = B.mok_workspace_item(cfg, which, item)
+    B.check(st, "workspace item")
+    return ws[off: off + n]
+
+
+def stored_dtype(cfg):
+    """torch dtype of the values the layer only stores (outputs, slots, saved A)."""
+    return torch.float32 if cfg.flags & B.MOK_FLAG_FP32_STORAGE else torch.bfloat16
+
+
 class MoELayer:
     """One layer configuration with its buffers on `device` (a CUDA device)."""
 
     def __init__(self, T, H, I, E, K, minibatch=2368, ring_capacity=0, prec=B.MOK_BF16,
-                 device="cuda", backward=False):
-        self.cfg = B.make_config(T, H, I, E, K, minibatch, ring_capacity, prec)
+                 device="cuda", backward=False, flags=0):
+        self.cfg = B.make_config(T, H, I, E, K, minibatch, ring_capacity, prec, flags=flags)
+        self.dtype = stored_dtype(self.cfg)
         B.check(B.mok_check_config(self.cfg), "config")
         self.device = torch.device(device)
         self.T, self.H, self.I, self.E, self.K = T, H, I, E, K

@@ -2,6 +2,7 @@
 // and the stream-ordered sequence of kernels for each call.
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -40,6 +41,10 @@ mok_status check_device(int **status) {
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+// values that are only stored are fp32 under MOK_FLAG_FP32_STORAGE, else bf16
+bool f32_storage(const mok_config *c) { return (c->flags & MOK_FLAG_FP32_STORAGE) != 0; }
+size_t stored_bytes(const mok_config *c) { return f32_storage(c) ? 4 : 2; }
+
 int64_t rows_R(const mok_config *c) { return (int64_t)c->T * c->K; }
 
 // ring geometry: n_slots == 0 means the ring holds every routed row (one pass). Else the
@@ -76,11 +81,16 @@ struct Carver {
     template <class T>
     T *take(size_t bytes) {
         off = (off + 255) & ~(size_t)255;
-        T *p = base ? (T *)(base + off) : nullptr;
+        T *p = base ? (T *)((uintptr_t)base + off) : nullptr;
         off += bytes;
         return p;
     }
 };
+
+// A stand-in workspace address for locating pieces without a workspace: carving against it
+// gives each piece's offset (never dereferenced).
+char *const kVirtualWs = (char *)(uintptr_t)(1u << 20);
+size_t ws_offset(const void *p) { return (size_t)((uintptr_t)p - (uintptr_t)kVirtualWs); }
 
 struct FwdWs {
     int32_t *tiles;  // points past a 16-byte header holding the count
@@ -89,7 +99,7 @@ struct FwdWs {
     uint8_t *xring_s;
     void *hring;
     uint8_t *hring_s;
-    float *slots;
+    void *slots;              // [R][H], the storage type of cfg->flags
     uint8_t *sf_w13, *sf_w2;  // MXFP8 weight scales as tensor-core atoms
     uint8_t *sf_x, *sf_h;     // MXFP8 token-tile scales as atoms (per pass)
     // the tile lists of all passes, built by one launch: pass m's list (count at [-4])
@@ -121,7 +131,7 @@ size_t carve_fwd(const mok_config *c, void *ws, FwdWs *o) {
     w.xring_s = mx ? cv.take<uint8_t>((size_t)rr * (c->H / 32)) : nullptr;
     w.hring = cv.take<void>((size_t)rr * c->I * esz);
     w.hring_s = mx ? cv.take<uint8_t>((size_t)rr * (c->I / 32)) : nullptr;
-    w.slots = cv.take<float>((size_t)R * c->H * 4);
+    w.slots = cv.take<void>((size_t)R * c->H * stored_bytes(c));
     w.sf_w13 = w.sf_w2 = w.sf_x = w.sf_h = nullptr;
     if (mx) {
         w.sf_w13 = cv.take<uint8_t>((size_t)c->E * 2 * c->I * (c->H / 32));
@@ -183,9 +193,9 @@ struct BwdWs {
     int64_t tiles_cap;
     int64_t rpad_cap;
     uint16_t *dy_perm, *x_perm, *dA, *sh;
-    float *dx_slots;
+    void *dx_slots;  // [R][H], the storage type of cfg->flags
     float *dS_part;
-    float *preact;  // recomputed pre-activations [R][2I] (recompute workspace only)
+    void *preact;    // recomputed pre-activations [R][2I] (recompute workspace only)
     // MXFP8: padded row of every flat id; dy and dA quantized along H / 2I; scale atoms of
     // the transposed weights and of the dy and dA tiles
     int32_t *prow;
@@ -207,8 +217,8 @@ size_t carve_bwd(const mok_config *c, void *ws, BwdWs *o, bool recompute = false
     w.dA = cv.take<uint16_t>((size_t)w.rpad_cap * 2 * c->I * 2);
     w.sh = cv.take<uint16_t>((size_t)w.rpad_cap * c->I * 2);
     w.dS_part = cv.take<float>((size_t)R * gemm_tc_dS_parts(c->I) * 4);
-    w.dx_slots = cv.take<float>((size_t)R * c->H * 4);
-    w.preact = recompute ? cv.take<float>((size_t)R * 2 * c->I * 4) : nullptr;
+    w.dx_slots = cv.take<void>((size_t)R * c->H * stored_bytes(c));
+    w.preact = recompute ? cv.take<void>((size_t)R * 2 * c->I * stored_bytes(c)) : nullptr;
     w.prow = nullptr;
     w.dy_q = w.dy_s = w.dA_q = w.dA_s = w.sf_w2t = w.sf_w13t = w.sf_dy = w.sf_dA = nullptr;
     if (mx) {
@@ -331,6 +341,20 @@ mok_status check_sched(const mok_config *c, const mok_schedule *s) {
 
 namespace mok {
 mok_status current_device_status_word(int **status) { return check_device(status); }
+
+int device_sm_count() {
+    static std::atomic<int> cache[MAX_DEV];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) return 1;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            n < 1)
+            n = 1;
+        cache[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
 }  // namespace mok
 
 // a launch of `nk` kernels of one kind, bracketed by events while profiling is on
@@ -374,6 +398,7 @@ mok_status mok_check_config(const mok_config *c) {
         c->ring_capacity < c->minibatch)
         return MOK_ERR_INVALID_ARG;
     if (c->prec != MOK_BF16 && c->prec != MOK_MXFP8) return MOK_ERR_INVALID_ARG;
+    if ((c->flags & ~MOK_FLAG_FP32_STORAGE) != 0) return MOK_ERR_INVALID_ARG;
     return MOK_OK;
 }
 
@@ -382,6 +407,77 @@ int64_t mok_segment_capacity(const mok_config *c) {
     const int64_t R = rows_R(c);
     const int64_t cap = (int64_t)c->E + (R + c->minibatch - 1) / c->minibatch - 1;
     return cap > 0 ? cap : 1;
+}
+
+mok_status mok_workspace_item(const mok_config *c, int which, int item, size_t *offset,
+                              size_t *bytes) {
+    if (offset == nullptr || bytes == nullptr) return MOK_ERR_INVALID_ARG;
+    if (mok_check_config(c) != MOK_OK) return MOK_ERR_INVALID_ARG;
+    const bool mx = c->prec == MOK_MXFP8;
+    const size_t H = (size_t)c->H, I = (size_t)c->I, R = (size_t)rows_R(c), T = (size_t)c->T;
+    const void *p = nullptr;
+    size_t n = 0;
+    if (which == MOK_WS_FORWARD) {
+        FwdWs w;
+        carve_fwd(c, kVirtualWs, &w);
+        int32_t ns, pr;
+        int64_t rr;
+        ring_geom(c, &ns, &rr, &pr);
+        const size_t esz = mx ? 1 : 2;
+        switch (item) {
+            case MOK_ITEM_X_RING: p = w.xring; n = (size_t)rr * H * esz; break;
+            case MOK_ITEM_X_RING_SCALE: p = w.xring_s; n = (size_t)rr * (H / 32); break;
+            case MOK_ITEM_H_RING: p = w.hring; n = (size_t)rr * I * esz; break;
+            case MOK_ITEM_H_RING_SCALE: p = w.hring_s; n = (size_t)rr * (I / 32); break;
+            case MOK_ITEM_SLOTS: p = w.slots; n = R * H * stored_bytes(c); break;
+            default: break;
+        }
+    } else if (which == MOK_WS_BACKWARD || which == MOK_WS_BACKWARD_RECOMPUTE) {
+        BwdWs w;
+        carve_bwd(c, kVirtualWs, &w, which == MOK_WS_BACKWARD_RECOMPUTE);
+        const size_t rp = (size_t)w.rpad_cap;
+        switch (item) {
+            case MOK_ITEM_PAD_OFFSETS: p = w.poff; n = ((size_t)c->E + 1) * 4; break;
+            case MOK_ITEM_DA: p = w.dA; n = rp * 2 * I * 2; break;
+            case MOK_ITEM_WH: p = w.sh; n = rp * I * 2; break;
+            case MOK_ITEM_SLOTS: p = w.dx_slots; n = R * H * stored_bytes(c); break;
+            case MOK_ITEM_DA_Q: p = w.dA_q; n = rp * 2 * I; break;
+            case MOK_ITEM_DA_SCALE: p = w.dA_s; n = rp * (2 * I / 32); break;
+            case MOK_ITEM_DY_Q: p = w.dy_q; n = rp * H; break;
+            case MOK_ITEM_DY_SCALE: p = w.dy_s; n = rp * (H / 32); break;
+            default: break;
+        }
+    } else if (which == MOK_WS_SHARED) {
+        SharedWs w;
+        carve_shared(c, kVirtualWs, &w);
+        switch (item) {
+            case MOK_ITEM_H_RING:
+                p = mx ? (const void *)w.h_q : (const void *)w.h;
+                n = T * I * (mx ? 1 : 2);
+                break;
+            case MOK_ITEM_H_RING_SCALE: p = w.h_s; n = T * (I / 32); break;
+            case MOK_ITEM_X_RING: p = w.x_q; n = T * H; break;
+            case MOK_ITEM_X_RING_SCALE: p = w.x_s; n = T * (H / 32); break;
+            default: break;
+        }
+    } else if (which == MOK_WS_SHARED_BACKWARD) {
+        SharedBwdWs w;
+        carve_shared_bwd(c, kVirtualWs, &w);
+        const size_t tp = (size_t)w.tpad;
+        switch (item) {
+            case MOK_ITEM_DA: p = w.dA; n = tp * 2 * I * 2; break;
+            case MOK_ITEM_WH: p = w.sh; n = tp * I * 2; break;
+            case MOK_ITEM_DA_Q: p = w.dA_q; n = tp * 2 * I; break;
+            case MOK_ITEM_DA_SCALE: p = w.dA_s; n = tp * (2 * I / 32); break;
+            case MOK_ITEM_DY_Q: p = w.dy_q; n = T * H; break;
+            case MOK_ITEM_DY_SCALE: p = w.dy_s; n = T * (H / 32); break;
+            default: break;
+        }
+    }
+    if (p == nullptr) return MOK_ERR_INVALID_ARG;
+    *offset = ws_offset(p);
+    *bytes = n;
+    return MOK_OK;
 }
 
 size_t mok_workspace_size(const mok_config *c, int which) {
@@ -528,9 +624,11 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
                                            R, pass, n_slots, (uint8_t *)w.xring,
                                            w.xring_s, stream));
         GemmUpArgs ua{w.tiles, cap, w.xring, w.xring_s, w13, w13_scale, w.hring,
-                      w.hring_s, (float *)saved_preact, c->H, c->I, c->E, mx, ring, status};
+                      w.hring_s, saved_preact, c->H, c->I, c->E, mx, ring, status};
+        ua.preact_f32 = f32_storage(c);
         GemmDownArgs da{w.tiles, cap, w.hring, w.hring_s, w2, w2_scale, sch->perm,
                         w.slots, c->H, c->I, c->E, mx, ring, status, false};
+        da.out_f32 = f32_storage(c);
         if (mx) {
             MOK_LAUNCH(KK_SCALE_ATOMS, 1,
                        launch_scale_atoms_tiles(w.tiles, cap, w.xring_s, R, pass, n_slots,
@@ -564,7 +662,7 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
                     cudaStreamWaitEvent(stream, ss->join, 0) != cudaSuccess))
         return MOK_ERR_CUDA;
     MOK_LAUNCH(KK_COMBINE, 1,
-               launch_combine(w.slots, topk_w, c->T, c->K, c->H, (float *)y, stream));
+               launch_combine(w.slots, topk_w, c->T, c->K, c->H, y, f32_storage(c), stream));
     return MOK_OK;
 }
 
@@ -614,8 +712,8 @@ mok_status backward_impl(const mok_config *c, const void *x, const mok_schedule 
     if (recompute)
         MOK_LAUNCH(KK_GEMM_UP, 1,
                    launch_gemm_up_recompute_tc(w.tiles, w.tiles_cap, w.x_perm, w.rpad_cap, w13,
-                                               sch->offsets, w.poff, w.preact, H, I, E, status,
-                                               stream));
+                                               sch->offsets, w.poff, w.preact, f32_storage(c),
+                                               H, I, E, status, stream));
     if (mx)  // the tensor cores' scale atoms of W2t, W13t and of the dy tiles
         MOK_LAUNCH(KK_SCALE_ATOMS, 3,
                    first_error(first_error(launch_scale_atoms_rows(mxw->w2t_s, (int64_t)E * I,
@@ -625,9 +723,10 @@ mok_status backward_impl(const mok_config *c, const void *x, const mok_schedule 
                                launch_scale_atoms_tiles_padded(w.tiles, w.tiles_cap, w.dy_s,
                                                                sch->offsets, w.poff, H,
                                                                w.sf_dy, stream)));
-    const float *pre = recompute ? w.preact : (const float *)saved_preact;
+    const void *pre = recompute ? w.preact : saved_preact;
     GemmGArgs ga{w.tiles, w.tiles_cap, sch->offsets, w.poff, (const uint16_t *)w2, w.dy_perm,
                  pre, sch->perm, topk_w, w.dA, w.sh, w.dS_part, H, I, status};
+    ga.preact_f32 = f32_storage(c);
     if (mx) {
         ga.mxfp8 = true;
         ga.w2t_q = mxw->w2t_q;
@@ -643,6 +742,7 @@ mok_status backward_impl(const mok_config *c, const void *x, const mok_schedule 
                                   topk_w, c->T, K, E, d_topk_w, d_logits, stream));
     GemmDgradArgs dg{w.tiles, w.tiles_cap, sch->offsets, w.poff, (const uint16_t *)w13, w.dA,
                      sch->perm, w.dx_slots, H, I, status};
+    dg.out_f32 = f32_storage(c);
     if (mx) {
         MOK_LAUNCH(KK_SCALE_ATOMS, 1,
                    launch_scale_atoms_tiles_padded(w.tiles, w.tiles_cap, w.dA_s, sch->offsets,
@@ -655,15 +755,15 @@ mok_status backward_impl(const mok_config *c, const void *x, const mok_schedule 
     }
     MOK_LAUNCH(KK_GEMM_DGRAD, 1, launch_gemm_dgrad_tc(dg, E, w.rpad_cap, stream));
     MOK_LAUNCH(KK_DX_REDUCE, 1,
-               launch_combine(w.dx_slots, nullptr, c->T, K, H, (float *)dx, stream));
+               launch_combine(w.dx_slots, nullptr, c->T, K, H, dx, f32_storage(c), stream));
     // dW13[e] is [2I][H]: rows j (N) x contiguous c (M)
     MOK_LAUNCH(KK_WGRAD13, 1,
-               launch_wgrad_tc(sch->counts, w.poff, w.x_perm, w.dA, (float *)dw13, E, H, 2 * I,
-                               w.rpad_cap, w.rpad_cap, status, stream));
+               launch_wgrad_tc(sch->counts, w.poff, w.x_perm, w.dA, dw13, f32_storage(c), E, H,
+                               2 * I, w.rpad_cap, w.rpad_cap, status, stream));
     // dW2[e] is [H][I]: rows c (N) x contiguous i (M)
     MOK_LAUNCH(KK_WGRAD2, 1,
-               launch_wgrad_tc(sch->counts, w.poff, w.sh, w.dy_perm, (float *)dw2, E, I, H,
-                               w.rpad_cap, w.rpad_cap, status, stream));
+               launch_wgrad_tc(sch->counts, w.poff, w.sh, w.dy_perm, dw2, f32_storage(c), E, I,
+                               H, w.rpad_cap, w.rpad_cap, status, stream));
     return MOK_OK;
 }
 }  // namespace mok
@@ -714,10 +814,12 @@ mok_status mok_shared_expert_forward(const mok_config *c, const void *x, const v
                            launch_build_tiles(w.offsets, 1, 0, c->T, gemm_tc_tile_rows(false),
                                               w.tiles, w.tiles_cap, status, stream)));
     GemmUpArgs ua{w.tiles, w.tiles_cap, x, nullptr, w13_s, nullptr, w.h, nullptr,
-                  (float *)saved_preact_s, c->H, c->I, 1, false, ring, status};
+                  saved_preact_s, c->H, c->I, 1, false, ring, status};
+    ua.preact_f32 = f32_storage(c);
     MOK_LAUNCH(KK_SHARED_UP, 1, launch_gemm_up_tc(ua, c->T, stream));
-    GemmDownArgs da{w.tiles, w.tiles_cap, w.h, nullptr, w2_s, nullptr, nullptr, (float *)y,
+    GemmDownArgs da{w.tiles, w.tiles_cap, w.h, nullptr, w2_s, nullptr, nullptr, y,
                     c->H, c->I, 1, false, ring, status, true};
+    da.out_f32 = f32_storage(c);
     MOK_LAUNCH(KK_SHARED_DOWN, 1, launch_gemm_down_tc(da, c->T, stream));
     return MOK_OK;
 }
@@ -758,13 +860,15 @@ mok_status mok_shared_expert_forward_mxfp8(const mok_config *c, const void *x,
                            launch_scale_atoms_tiles(w.tiles, w.tiles_cap, w.x_s, T,
                                                     c->minibatch, 0, H, w.sf_x, stream)));
     GemmUpArgs ua{w.tiles, w.tiles_cap, w.x_q, w.x_s, w13s_q, w13s_scale, w.h_q, w.h_s,
-                  (float *)saved_preact_s, H, I, 1, true, ring, status};
+                  saved_preact_s, H, I, 1, true, ring, status};
+    ua.preact_f32 = f32_storage(c);
     MOK_LAUNCH(KK_SHARED_UP, 1, launch_gemm_up_tc_mx(ua, T, w.sf_w13, w.sf_x, stream));
     MOK_LAUNCH(KK_SCALE_ATOMS, 1,
                launch_scale_atoms_tiles(w.tiles, w.tiles_cap, w.h_s, T, c->minibatch, 0, I,
                                         w.sf_h, stream));
-    GemmDownArgs da{w.tiles, w.tiles_cap, w.h_q, w.h_s, w2s_q, w2s_scale, nullptr, (float *)y,
+    GemmDownArgs da{w.tiles, w.tiles_cap, w.h_q, w.h_s, w2s_q, w2s_scale, nullptr, y,
                     H, I, 1, true, ring, status, true};
+    da.out_f32 = f32_storage(c);
     MOK_LAUNCH(KK_SHARED_DOWN, 1, launch_gemm_down_tc_mx(da, T, w.sf_w2, w.sf_h, stream));
     return MOK_OK;
 }
@@ -811,11 +915,13 @@ mok_status shared_backward_impl(const mok_config *c, const void *x, const void *
                                               w.tiles, w.tiles_cap, status, stream)));
     if (T > 0) {
         GemmGArgs ga{w.tiles, w.tiles_cap, w.offsets, w.poff, (const uint16_t *)w2_s,
-                     (const uint16_t *)dy, (const float *)saved_preact_s, w.perm, w.ones, w.dA,
+                     (const uint16_t *)dy, saved_preact_s, w.perm, w.ones, w.dA,
                      w.sh, w.dS_part, H, I, status};
+        ga.preact_f32 = f32_storage(c);
         GemmDgradArgs dg{w.tiles, w.tiles_cap, w.offsets, w.poff, (const uint16_t *)w13_s,
-                         w.dA, w.perm, (float *)dx, H, I, status};
+                         w.dA, w.perm, dx, H, I, status};
         dg.accumulate = true;
+        dg.out_f32 = f32_storage(c);
         if (mx) {
             // dy quantized along H in token order (the padded layout of a single expert is
             // the token order; rows past T are outside the TMA map and read zero)
@@ -852,11 +958,11 @@ mok_status shared_backward_impl(const mok_config *c, const void *x, const void *
     }
     // the weight gradients' K runs over the padded rows: x and dy rows past T read zeros
     MOK_LAUNCH(KK_SHARED_BWD, 2,
-               first_error(launch_wgrad_tc(w.counts, w.poff, (const uint16_t *)x, w.dA,
-                                           (float *)dw13_s, 1, H, 2 * I, T > 0 ? T : 1,
+               first_error(launch_wgrad_tc(w.counts, w.poff, (const uint16_t *)x, w.dA, dw13_s,
+                                           f32_storage(c), 1, H, 2 * I, T > 0 ? T : 1,
                                            w.tpad > 0 ? w.tpad : 1, status, stream),
-                           launch_wgrad_tc(w.counts, w.poff, w.sh, (const uint16_t *)dy,
-                                           (float *)dw2_s, 1, I, H, w.tpad > 0 ? w.tpad : 1,
+                           launch_wgrad_tc(w.counts, w.poff, w.sh, (const uint16_t *)dy, dw2_s,
+                                           f32_storage(c), 1, I, H, w.tpad > 0 ? w.tpad : 1,
                                            T > 0 ? T : 1, status, stream)));
     return MOK_OK;
 }

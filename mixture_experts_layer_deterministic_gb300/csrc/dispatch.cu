@@ -15,7 +15,10 @@ namespace {
 
 constexpr int TPB = 256;
 
-inline unsigned grid_for(int64_t items, int per_block, int64_t cap = 152 * 32) {
+// blocks for `items` work items at `per_block` items per block (grid-stride loops), capped
+// at `per_sm` blocks per streaming multiprocessor of the device
+inline unsigned grid_for(int64_t items, int per_block, int per_sm = 32) {
+    const int64_t cap = (int64_t)device_sm_count() * per_sm;
     int64_t b = (items + per_block - 1) / per_block;
     if (b > cap) b = cap;
     if (b < 1) b = 1;
@@ -214,26 +217,49 @@ __global__ void __launch_bounds__(TPB)
 // ---------------------------------------------------------------- combine
 // y[t][c..c+3] = sum over k = 0..K-1 of w[t,k] * slots[t*K+k][c..c+3] in fp32, k ascending
 // (fmaf from zero); w == nullptr sums with weight one.
+// y[t] = sum over k ascending of w[t,k] * slots[t*K + k], fp32 fused multiply-adds; each
+// thread owns 4 (fp32) or 8 (bf16) consecutive columns and reads every slot with one
+// 16-byte load. bf16 storage rounds y once, after the sum.
+template <bool F32>
 __global__ void __launch_bounds__(TPB)
-    combine_kernel(const float *__restrict__ slots, const float *__restrict__ w, int64_t T,
-                   int K, int H, float *__restrict__ y) {
-    const int nv = H / 4;
+    combine_kernel(const void *__restrict__ slots, const float *__restrict__ w, int64_t T,
+                   int K, int H, void *__restrict__ y) {
+    constexpr int PER = F32 ? 4 : 8;  // columns per thread
+    const int nv = H / PER;
     const int64_t total = T * nv;
     const int64_t stride = (int64_t)gridDim.x * TPB;
     for (int64_t i = (int64_t)blockIdx.x * TPB + threadIdx.x; i < total; i += stride) {
         const int64_t t = i / nv;
         const int v = (int)(i % nv);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float acc[PER];
+#pragma unroll
+        for (int q = 0; q < PER; ++q) acc[q] = 0.f;
         for (int k = 0; k < K; ++k) {
             const int64_t f = t * K + k;
-            const uint4 o = ldg_nc_v4(slots + f * H + v * 4);
             const float s = (w != nullptr) ? __ldg(w + f) : 1.0f;
-            acc.x = fmaf(s, __uint_as_float(o.x), acc.x);
-            acc.y = fmaf(s, __uint_as_float(o.y), acc.y);
-            acc.z = fmaf(s, __uint_as_float(o.z), acc.z);
-            acc.w = fmaf(s, __uint_as_float(o.w), acc.w);
+            const uint4 o = ldg_nc_v4(static_cast<const uint8_t *>(slots) +
+                                      (f * H + (int64_t)v * PER) * (F32 ? 4 : 2));
+            const uint32_t u[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (F32) {
+                    acc[q] = fmaf(s, __uint_as_float(u[q]), acc[q]);
+                } else {
+                    acc[2 * q] = fmaf(s, bf16_lo(u[q]), acc[2 * q]);
+                    acc[2 * q + 1] = fmaf(s, bf16_hi(u[q]), acc[2 * q + 1]);
+                }
+            }
         }
-        *reinterpret_cast<float4 *>(y + t * H + v * 4) = acc;
+        uint4 r;
+        if (F32) {
+            r = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                           __float_as_uint(acc[2]), __float_as_uint(acc[3]));
+        } else {
+            r = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                           pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+        }
+        *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(y) +
+                                   (t * H + (int64_t)v * PER) * (F32 ? 4 : 2)) = r;
     }
 }
 
@@ -467,7 +493,7 @@ cudaError_t launch_gather_bf16(const uint16_t *x, const int32_t *perm, int K, in
                                cudaStream_t s) {
     if (p1 <= p0) return cudaSuccess;
     RingMap rm{R, MB, n_slots};
-    gather_bf16_kernel<<<grid_for(p1 - p0, TPB / 32, 152 * 16), TPB, 0, s>>>(x, perm, K, H, p0,
+    gather_bf16_kernel<<<grid_for(p1 - p0, TPB / 32, 16), TPB, 0, s>>>(x, perm, K, H, p0,
                                                                              p1, rm, ring);
     return cudaGetLastError();
 }
@@ -511,7 +537,7 @@ cudaError_t launch_single_expert_bwd_setup(int32_t *offsets, int32_t *poff, int3
 cudaError_t launch_gather_tok_bf16(const uint16_t *x, const int32_t *inv, int64_t T, int K,
                                    int H, uint16_t *ring, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    gather_tok_bf16_kernel<<<grid_for(T, TPB / 32, 152 * 16), TPB, 0, s>>>(x, inv, T, K, H,
+    gather_tok_bf16_kernel<<<grid_for(T, TPB / 32, 16), TPB, 0, s>>>(x, inv, T, K, H,
                                                                            ring);
     return cudaGetLastError();
 }
@@ -519,7 +545,7 @@ cudaError_t launch_gather_tok_bf16(const uint16_t *x, const int32_t *inv, int64_
 cudaError_t launch_gather_tok_mxfp8(const uint16_t *x, const int32_t *inv, int64_t T, int K,
                                     int H, uint8_t *ring_q, uint8_t *ring_s, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    gather_tok_mxfp8_kernel<<<grid_for(T * (H / 32), TPB, 152 * 16), TPB, 0, s>>>(
+    gather_tok_mxfp8_kernel<<<grid_for(T * (H / 32), TPB, 16), TPB, 0, s>>>(
         x, inv, T, K, H, ring_q, ring_s);
     return cudaGetLastError();
 }
@@ -529,7 +555,7 @@ cudaError_t launch_gather_mxfp8(const uint16_t *x, const int32_t *perm, int K, i
                                 uint8_t *ring_s, cudaStream_t s) {
     if (p1 <= p0) return cudaSuccess;
     RingMap rm{R, MB, n_slots};
-    gather_mxfp8_kernel<<<grid_for((p1 - p0) * (H / 32), TPB, 152 * 16), TPB, 0, s>>>(
+    gather_mxfp8_kernel<<<grid_for((p1 - p0) * (H / 32), TPB, 16), TPB, 0, s>>>(
         x, perm, K, H, p0, p1, rm, ring_q, ring_s);
     return cudaGetLastError();
 }
@@ -537,7 +563,7 @@ cudaError_t launch_gather_mxfp8(const uint16_t *x, const int32_t *perm, int K, i
 cudaError_t launch_quantize_mxfp8(const uint16_t *src, int64_t rows, int cols, uint8_t *q,
                                   uint8_t *scale, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
-    quantize_kernel<<<grid_for(rows * (cols / 32), TPB, 152 * 16), TPB, 0, s>>>(src, rows, cols,
+    quantize_kernel<<<grid_for(rows * (cols / 32), TPB, 16), TPB, 0, s>>>(src, rows, cols,
                                                                                 q, scale);
     return cudaGetLastError();
 }
@@ -546,15 +572,18 @@ cudaError_t launch_quantize_mxfp8_transposed(const uint16_t *src, int64_t batch,
                                              int cols, uint8_t *q, uint8_t *scale,
                                              cudaStream_t s) {
     if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
-    quantize_transposed_kernel<<<grid_for(batch * (rows / 32) * cols, TPB, 152 * 16), TPB, 0,
+    quantize_transposed_kernel<<<grid_for(batch * (rows / 32) * cols, TPB, 16), TPB, 0,
                                  s>>>(src, batch, rows, cols, q, scale);
     return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const float *slots, const float *w, int64_t T, int K, int H,
-                           float *y, cudaStream_t s) {
+cudaError_t launch_combine(const void *slots, const float *w, int64_t T, int K, int H,
+                           void *y, bool f32, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    combine_kernel<<<grid_for(T * (H / 4), TPB, 152 * 16), TPB, 0, s>>>(slots, w, T, K, H, y);
+    if (f32)
+        combine_kernel<true><<<grid_for(T * (H / 4), TPB, 16), TPB, 0, s>>>(slots, w, T, K, H, y);
+    else
+        combine_kernel<false><<<grid_for(T * (H / 8), TPB, 16), TPB, 0, s>>>(slots, w, T, K, H, y);
     return cudaGetLastError();
 }
 
@@ -565,12 +594,12 @@ cudaError_t launch_gather_bwd(const uint16_t *dy, const uint16_t *x, const int32
                               uint8_t *dy_s, cudaStream_t s) {
     if (E == 0) return cudaSuccess;
     if (T > 0)
-        gather_bwd_kernel<<<grid_for(T, TPB / 32, 152 * 16), TPB, 0, s>>>(
+        gather_bwd_kernel<<<grid_for(T, TPB / 32, 16), TPB, 0, s>>>(
             dy, x, inv, offsets, poff, E, T, K, H, dy_perm, x_perm, prow);
     if (T > 0 && dy_q != nullptr)
-        quantize_dy_padded_kernel<<<grid_for(T * (H / 32), TPB, 152 * 16), TPB, 0, s>>>(
+        quantize_dy_padded_kernel<<<grid_for(T * (H / 32), TPB, 16), TPB, 0, s>>>(
             dy, prow, T, K, H, dy_q, dy_s);
-    zero_pad_rows_kernel<<<grid_for((int64_t)E * 16, TPB / 32, 152 * 16), TPB, 0, s>>>(
+    zero_pad_rows_kernel<<<grid_for((int64_t)E * 16, TPB / 32, 16), TPB, 0, s>>>(
         counts, poff, E, H, dy_perm, x_perm, dy_q, dy_s);
     return cudaGetLastError();
 }
@@ -579,7 +608,7 @@ cudaError_t launch_router_grad(const float *dS_part, int n_parts, const int32_t 
                                const int32_t *offsets, const float *w, int64_t T, int K, int E,
                                float *d_topk, float *d_logits, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    router_grad_kernel<<<grid_for(T, TPB / 32, 152 * 16), TPB, 0, s>>>(
+    router_grad_kernel<<<grid_for(T, TPB / 32, 16), TPB, 0, s>>>(
         dS_part, n_parts, inv, offsets, w, T, K, E, d_topk, d_logits);
     return cudaGetLastError();
 }
@@ -593,7 +622,7 @@ cudaError_t launch_scale_atoms_rows(const uint8_t *src, int64_t rows, int K, uin
     if (rows == 0) return cudaSuccess;
     const int64_t nb = (rows + 127) / 128;
     const int nkc = (K / 128 + ATOM_KG - 1) / ATOM_KG;
-    scale_atoms_kernel<<<grid_for(nb * nkc, 1, 152 * 8), 256, 0, s>>>(
+    scale_atoms_kernel<<<grid_for(nb * nkc, 1, 8), 256, 0, s>>>(
         src, nb, 0, K, AtomRows{nullptr, rows, RingMap{1, 1, 0}, nullptr, nullptr}, dst);
     return cudaGetLastError();
 }
@@ -603,7 +632,7 @@ cudaError_t launch_scale_atoms_tiles(const int32_t *tiles, int64_t cap, const ui
                                      cudaStream_t s) {
     if (cap == 0) return cudaSuccess;
     const int nkc = (K / 128 + ATOM_KG - 1) / ATOM_KG;
-    scale_atoms_kernel<<<grid_for(cap * nkc, 1, 152 * 8), 256, 0, s>>>(
+    scale_atoms_kernel<<<grid_for(cap * nkc, 1, 8), 256, 0, s>>>(
         src, 0, cap, K, AtomRows{tiles, 0, RingMap{R, MB, n_slots}, nullptr, nullptr}, dst);
     return cudaGetLastError();
 }
@@ -614,7 +643,7 @@ cudaError_t launch_scale_atoms_tiles_padded(const int32_t *tiles, int64_t cap,
                                             cudaStream_t s) {
     if (cap == 0) return cudaSuccess;
     const int nkc = (K / 128 + ATOM_KG - 1) / ATOM_KG;
-    scale_atoms_kernel<<<grid_for(cap * nkc, 1, 152 * 8), 256, 0, s>>>(
+    scale_atoms_kernel<<<grid_for(cap * nkc, 1, 8), 256, 0, s>>>(
         src, 0, cap, K, AtomRows{tiles, 0, RingMap{1, 1, 0}, offsets, poff}, dst);
     return cudaGetLastError();
 }

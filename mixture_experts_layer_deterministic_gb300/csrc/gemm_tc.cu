@@ -28,17 +28,20 @@
 // A problem policy supplies the work-unit decomposition, the operand majors and the
 // epilogue:
 //   FwdUp     A = W13 (K-major), B = x ring (K-major)      -> SwiGLU, h (bf16 / MXFP8)
-//   FwdDown   A = W2 (K-major),  B = h ring (K-major)      -> fp32 push scatter to slots
+//   FwdDown   A = W2 (K-major),  B = h ring (K-major)      -> push scatter to slots
 //   BwdG      A = W2^T (MN-major), B = dy_perm (K-major)   -> SwiGLU backward, dA, w*h, dS
 //             (MXFP8: A = W2t K-major, B = quantized dy; dA also quantized)
-//   BwdDgrad  A = W13^T (MN-major), B = dA (K-major)       -> fp32 reverse-dispatch scatter
+//   BwdDgrad  A = W13^T (MN-major), B = dA (K-major)       -> reverse-dispatch scatter
 //             (MXFP8: A = W13t K-major, B = quantized dA)
-//   Wgrad     A, B MN-major over an expert's padded rows   -> fp32 dW
+//   Wgrad     A, B MN-major over an expert's padded rows   -> dW
+// Values that are only stored (saved pre-activations, slots, dx slots, dW) are bf16, or fp32
+// when the caller asks for fp32 storage; every accumulation is fp32.
 // Every GEMM puts the weight (or output-contiguous) dimension on M and the routed rows on
 // N or K, so ragged experts cost at most 15 padding rows. Every output element is one
 // fixed-order fp32 dot product, independent of which CTA computes its unit.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstddef>
 
 #include "common.cuh"
@@ -127,6 +130,18 @@ struct Geom {
 
 MOK_DEV float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
+// element i of a stored-value array held as fp32 (f32) or bf16
+MOK_DEV void st_val(void *p, int64_t i, float v, bool f32) {
+    if (f32)
+        static_cast<float *>(p)[i] = v;
+    else
+        static_cast<uint16_t *>(p)[i] = f32_to_bf16(v);
+}
+MOK_DEV float ld_val(const void *p, int64_t i, bool f32) {
+    return f32 ? static_cast<const float *>(p)[i]
+               : bf16_to_f32(static_cast<const uint16_t *>(p)[i]);
+}
+
 // bounded wait; gives up when another role has aborted or after the wall-time limit
 MOK_DEV bool wait_or_abort(uint64_t *bar, uint32_t parity, int *status, volatile int *abort) {
     return tc::wait_bounded(bar, parity, status, abort, tc::WAIT_LIMIT_NS);
@@ -166,7 +181,8 @@ struct FwdUpT {
     Ring ring;
     void *hring;
     uint8_t *hring_s;
-    float *preact;
+    void *preact;        // [R][2I] pre-activations (fp32 if preact_f32, else bf16), or nullptr
+    bool preact_f32;
     bool mxfp8;
     int *status;
     const uint8_t *sf_a, *sf_b;
@@ -216,8 +232,8 @@ struct FwdUpT {
                 const int64_t r = r0 + n;
                 h[j] = silu_f(d0[j]) * d1[j];
                 if (n < nr && preact != nullptr) {
-                    preact[r * 2 * I + i] = d0[j];
-                    preact[r * 2 * I + I + i] = d1[j];
+                    st_val(preact, r * 2 * I + i, d0[j], preact_f32);
+                    st_val(preact, r * 2 * I + I + i, d1[j], preact_f32);
                 }
                 if (hring != nullptr && !mxfp8 && n < nr)
                     ((uint16_t *)hring)[rm(r) * I + i] = f32_to_bf16(h[j]);
@@ -266,7 +282,8 @@ struct FwdDownT {
     int H, I;
     Ring ring;
     const int32_t *perm;  // output row of each sorted row (nullptr: the row itself)
-    float *slots;
+    void *slots;          // [rows][H], fp32 if out_f32, else bf16
+    bool out_f32;
     int *status;
     const uint8_t *sf_a, *sf_b;
     bool accumulate;      // add into the output (the shared expert adds into y)
@@ -319,9 +336,9 @@ struct FwdDownT {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const bool ok = n0 + j < nr;
-                    const float *o = slots + (int64_t)fcol[ok ? n0 + j : 0] * H + c;
-                    a0[j] = ok ? o[0] : 0.f;
-                    a1[j] = ok && has1 ? o[128] : 0.f;
+                    const int64_t o = (int64_t)fcol[ok ? n0 + j : 0] * H + c;
+                    a0[j] = ok ? ld_val(slots, o, out_f32) : 0.f;
+                    a1[j] = ok && has1 ? ld_val(slots, o + 128, out_f32) : 0.f;
                 }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
@@ -333,9 +350,9 @@ struct FwdDownT {
             for (int j = 0; j < 16; ++j) {
                 const int n = n0 + j;
                 if (n < nr) {
-                    float *o = slots + (int64_t)fcol[n] * H + c;
-                    o[0] = d0[j];
-                    if (has1) o[128] = d1[j];
+                    const int64_t o = (int64_t)fcol[n] * H + c;
+                    st_val(slots, o, d0[j], out_f32);
+                    if (has1) st_val(slots, o + 128, d1[j], out_f32);
                 }
             }
         }
@@ -347,7 +364,7 @@ struct FwdDownT {
 // [mb*256, +128) and [mb*256+128, +128) of W2^T (MN-major: W2 rows are c).
 // MXFP8: A = W2t [E*I][H] E4M3 (W2 quantized along H, stored transposed: K-major), B = dy
 // quantized along H; the epilogue also quantizes dA along 2I for the MXFP8 dgrad.
-template <bool MXv>
+template <bool MXv, bool PF32 = false>
 struct BwdGT {
     static constexpr bool A_MN = !MXv, B_MN = false, MX = MXv;
     static constexpr int A_MODE = MXv ? A_ROWS256 : A_MN4;
@@ -359,7 +376,8 @@ struct BwdGT {
     TileUnits tu;
     int H, I;
     const int32_t *offsets, *poff, *perm;
-    const float *preact, *topk_w;
+    const void *preact;  // [R][2I], fp32 if PF32, else bf16
+    const float *topk_w;
     uint16_t *dA, *sh;
     float *dS_part;
     int n_parts;
@@ -415,7 +433,10 @@ struct BwdGT {
             float d[2][16];
             ld(n0, d[0], d[1]);
             // issue every pre-activation load of the chunk before using any
-            float ag[2][16], au[2][16];
+            // the pre-activations as raw bits: fp32 words, or bf16 values zero-extended by
+            // their 16-bit loads and moved into place only where they are used, so that all
+            // the loads are in flight before the first one is waited for
+            uint32_t rg[2][16], ru[2][16];
             uint32_t my_sb = 0;  // MXFP8: the block scale this lane stores for its 4-row group
 #pragma unroll
             for (int a = 0; a < 2; ++a)
@@ -424,9 +445,19 @@ struct BwdGT {
                     const int i = i0 + a * 128;
                     const int64_t r = r0 + n0 + j;
                     const bool ok = (n0 + j < nr) && i < I;
-                    ag[a][j] = ok ? preact[r * 2 * I + i] : 0.f;
-                    au[a][j] = ok ? preact[r * 2 * I + I + i] : 0.f;
+                    if (PF32) {
+                        const uint32_t *pf = static_cast<const uint32_t *>(preact);
+                        rg[a][j] = ok ? pf[r * 2 * I + i] : 0u;
+                        ru[a][j] = ok ? pf[r * 2 * I + I + i] : 0u;
+                    } else {
+                        const unsigned short *ph = static_cast<const unsigned short *>(preact);
+                        rg[a][j] = ok ? (uint32_t)ph[r * 2 * I + i] : 0u;
+                        ru[a][j] = ok ? (uint32_t)ph[r * 2 * I + I + i] : 0u;
+                    }
                 }
+            auto pre_val = [](uint32_t raw) {
+                return __uint_as_float(PF32 ? raw : raw << 16);
+            };
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int n = n0 + j;
@@ -439,11 +470,12 @@ struct BwdGT {
                     if (n < nr) {
                         const float s = es.col[n];
                         const float g = d[a][j];
-                        const float sig = 1.0f / (1.0f + expf(-ag[a][j]));
-                        const float sl = ag[a][j] * sig;
-                        const float h = sl * au[a][j];
+                        const float agv = pre_val(rg[a][j]), auv = pre_val(ru[a][j]);
+                        const float sig = 1.0f / (1.0f + expf(-agv));
+                        const float sl = agv * sig;
+                        const float h = sl * auv;
                         const float dh = s * g;
-                        const float dag = dh * au[a][j] * sig * (1.0f + ag[a][j] * (1.0f - sig));
+                        const float dag = dh * auv * sig * (1.0f + agv * (1.0f - sig));
                         const float dau = dh * sl;
                         dA[p * 2 * I + i] = f32_to_bf16(dag);
                         dA[p * 2 * I + I + i] = f32_to_bf16(dau);
@@ -526,7 +558,8 @@ struct BwdDgradT {
     TileUnits tu;
     int H, I;
     const int32_t *offsets, *poff, *perm;
-    float *dx_slots;
+    void *dx_slots;              // [rows][H], fp32 if out_f32, else bf16
+    bool out_f32;
     int *status;
     const uint8_t *sf_a, *sf_b;  // MXFP8: scale atoms of W13t and of the dA tiles
     bool accumulate;             // add into the output rows (the shared expert adds into dx)
@@ -581,9 +614,9 @@ struct BwdDgradT {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const bool ok = n0 + j < nr;
-                    const float *o = dx_slots + (int64_t)fcol[ok ? n0 + j : 0] * H + c;
-                    a0[j] = ok ? o[0] : 0.f;
-                    a1[j] = ok && has1 ? o[128] : 0.f;
+                    const int64_t o = (int64_t)fcol[ok ? n0 + j : 0] * H + c;
+                    a0[j] = ok ? ld_val(dx_slots, o, out_f32) : 0.f;
+                    a1[j] = ok && has1 ? ld_val(dx_slots, o + 128, out_f32) : 0.f;
                 }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
@@ -596,8 +629,8 @@ struct BwdDgradT {
                 const int n = n0 + j;
                 if (n < nr) {
                     const int64_t f = fcol[n];
-                    dx_slots[f * H + c] = d0[j];
-                    if (has1) dx_slots[f * H + c + 128] = d1[j];
+                    st_val(dx_slots, f * H + c, d0[j], out_f32);
+                    if (has1) st_val(dx_slots, f * H + c + 128, d1[j], out_f32);
                 }
             }
         }
@@ -613,7 +646,8 @@ struct Wgrad {
     static constexpr bool CLC = true;
     static constexpr const uint8_t *sf_a = nullptr, *sf_b = nullptr;
     const int32_t *counts, *poff;
-    float *out;
+    void *out;       // fp32 if out_f32, else bf16
+    bool out_f32;
     int E, M, N;     // out is [E][N][M]
     int nmb, nnb;    // ceil(M/256), ceil(N/128)
     int *status;
@@ -649,15 +683,15 @@ struct Wgrad {
         const int nn = N - nb * TILE_ROWS < TILE_ROWS ? N - nb * TILE_ROWS : TILE_ROWS;
         const bool any = counts[e] > 0;
         const int m = mb * 256 + q * 32 + lane;
-        float *o = out + (int64_t)e * N * M;
+        const int64_t base = (int64_t)e * N * M;
         for (int n0 = 16 * half; n0 < nn; n0 += 32) {
             float d0[16], d1[16];
             ld(n0, d0, d1);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const int64_t row = (int64_t)(nb * TILE_ROWS + n0 + j) * M;
-                o[row + m] = any ? d0[j] : 0.f;
-                if (m + 128 < M) o[row + m + 128] = any ? d1[j] : 0.f;
+                const int64_t row = base + (int64_t)(nb * TILE_ROWS + n0 + j) * M;
+                st_val(out, row + m, any ? d0[j] : 0.f, out_f32);
+                if (m + 128 < M) st_val(out, row + m + 128, any ? d1[j] : 0.f, out_f32);
             }
         }
     }
@@ -942,26 +976,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-int g_num_sms = 0;
+// the driver's tensor-map encoder: one process-wide entry point, looked up once
+std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode{nullptr};
 
 cudaError_t init_host() {
-    if (g_encode == nullptr) {
+    if (g_encode.load(std::memory_order_acquire) == nullptr) {
         cudaDriverEntryPointQueryResult q;
         void *fn = nullptr;
         cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
                                                          cudaEnableDefault, &q);
         if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
             return cudaErrorNotSupported;
-        g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
-    }
-    if (g_num_sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaError_t e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
+        g_encode.store((PFN_cuTensorMapEncodeTiled_v12000)fn, std::memory_order_release);
     }
     return cudaSuccess;
+}
+
+CUresult encode(CUtensorMap *m, CUtensorMapDataType t, cuuint32_t rank, void *ptr,
+                const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box,
+                const cuuint32_t *estr) {
+    return g_encode.load(std::memory_order_acquire)(
+        m, t, rank, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 // row-major bf16 matrix [rows][cols] -> 2D map of 64-column x box_rows boxes with
@@ -972,10 +1009,8 @@ cudaError_t make_map_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t
     cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
     cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims,
+                        strides, box, estr);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -987,10 +1022,8 @@ cudaError_t make_map_u8(CUtensorMap *m, const void *ptr, int64_t rows, int64_t c
     cuuint64_t strides[1] = {(cuuint64_t)cols};
     cuuint32_t box[2] = {(cuuint32_t)BK_MX, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims,
+                        strides, box, estr);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -1005,10 +1038,8 @@ cudaError_t make_map_w13_pairs(CUtensorMap *m, const void *ptr, int64_t E, int64
                              (cuuint64_t)(I * H * es), (cuuint64_t)(2 * I * H * es)};
     cuuint32_t box[5] = {(cuuint32_t)(mx ? BK_MX : BK), 128, 1, 2, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    CUresult r = g_encode(m, mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                          5, const_cast<void *>(ptr), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode(m, mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        5, const_cast<void *>(ptr), dims, strides, box, estr);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -1021,19 +1052,26 @@ template <class P>
 cudaError_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const P &p, int64_t units_cap,
                    int64_t units_min, cudaStream_t s) {
     constexpr int SMEM = smem_bytes<P::MX>();
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<P>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    // the shared-memory opt-in is a per-device function attribute: set once per device
+    static std::atomic<uint64_t> attr_set[2] = {{0}, {0}};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    const uint64_t bit = 1ull << (dev & 63);
+    if ((attr_set[dev >> 6].load(std::memory_order_acquire) & bit) == 0) {
+        e = cudaFuncSetAttribute(tc_gemm_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM);
         if (e != cudaSuccess) return e;
-        attr = true;
+        attr_set[dev >> 6].fetch_or(bit, std::memory_order_acq_rel);
     }
     // Cluster Launch Control: one CTA per unit, running CTAs take over the units of CTAs
     // not yet launched; static striding: one CTA per SM
     if (units_cap < 1) return cudaSuccess;
     if (units_cap > 0x7FFFFFFF) return cudaErrorInvalidValue;
     const bool clc = P::CLC && units_cap <= 2 * units_min;
-    const int grid = clc || units_cap < g_num_sms ? (int)units_cap : g_num_sms;
+    const int n_sms = device_sm_count();
+    const int grid = clc || units_cap < n_sms ? (int)units_cap : n_sms;
     tc_gemm_kernel<P><<<grid, NTHREADS, SMEM, s>>>(ma, mb, p, clc ? 1 : 0);
     return cudaGetLastError();
 }
@@ -1049,7 +1087,8 @@ cudaError_t launch_gemm_up_tc(const GemmUpArgs &a, int64_t ring_rows, cudaStream
     if ((e = make_map_w13_pairs(&ma, a.w13, a.E, a.I, a.H, false)) != cudaSuccess) return e;
     if ((e = make_map_bf16(&mb, a.xring, ring_rows, a.H, KBOX_ROWS)) != cudaSuccess) return e;
     FwdUpT<false> p{TileUnits{a.tiles, a.tiles_cap, a.I / 128}, a.H, a.I, a.ring, a.hring,
-                    a.hring_s, a.preact, false, a.status, nullptr, nullptr, nullptr, nullptr};
+                    a.hring_s, a.preact, a.preact_f32, false, a.status, nullptr, nullptr,
+                    nullptr, nullptr};
     return launch(ma, mb, p, a.tiles_cap * (a.I / 128),
                   (ring_rows + TILE_ROWS - 1) / TILE_ROWS * (a.I / 128), s);
 }
@@ -1057,15 +1096,15 @@ cudaError_t launch_gemm_up_tc(const GemmUpArgs &a, int64_t ring_rows, cudaStream
 cudaError_t launch_gemm_up_recompute_tc(const int32_t *tiles, int64_t tiles_cap,
                                         const uint16_t *x_perm, int64_t rpad_cap,
                                         const void *w13, const int32_t *offsets,
-                                        const int32_t *poff, float *preact, int H, int I,
-                                        int E, int *status, cudaStream_t s) {
+                                        const int32_t *poff, void *preact, bool preact_f32,
+                                        int H, int I, int E, int *status, cudaStream_t s) {
     cudaError_t e = init_host();
     if (e != cudaSuccess) return e;
     CUtensorMap ma, mb;  // A: W13 gate/up block pairs; B: x in the padded layout [rpad][H]
     if ((e = make_map_w13_pairs(&ma, w13, E, I, H, false)) != cudaSuccess) return e;
     if ((e = make_map_bf16(&mb, x_perm, rpad_cap, H, KBOX_ROWS)) != cudaSuccess) return e;
     FwdUpT<false> p{TileUnits{tiles, tiles_cap, I / 128}, H, I, Ring{1, 1, 0}, nullptr,
-                    nullptr, preact, false, status, nullptr, nullptr, offsets, poff};
+                    nullptr, preact, preact_f32, false, status, nullptr, nullptr, offsets, poff};
     // the padded rows overestimate the real ones by at most 15 per expert
     return launch(ma, mb, p, tiles_cap * (I / 128),
                   (rpad_cap + TILE_ROWS - 1) / TILE_ROWS * (I / 128), s);
@@ -1079,7 +1118,7 @@ cudaError_t launch_gemm_down_tc(const GemmDownArgs &a, int64_t ring_rows, cudaSt
     if ((e = make_map_bf16(&mb, a.hring, ring_rows, a.I, KBOX_ROWS)) != cudaSuccess) return e;
     const int nmb = (a.H + 255) / 256;
     FwdDownT<false> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.ring, a.perm, a.slots,
-                      a.status, nullptr, nullptr, a.accumulate};
+                      a.out_f32, a.status, nullptr, nullptr, a.accumulate};
     return launch(ma, mb, p, a.tiles_cap * nmb, (ring_rows + TILE_ROWS - 1) / TILE_ROWS * nmb, s);
 }
 
@@ -1091,7 +1130,8 @@ cudaError_t launch_gemm_up_tc_mx(const GemmUpArgs &a, int64_t ring_rows, const u
     if ((e = make_map_w13_pairs(&ma, a.w13, a.E, a.I, a.H, true)) != cudaSuccess) return e;
     if ((e = make_map_u8(&mb, a.xring, ring_rows, a.H, KBOX_ROWS)) != cudaSuccess) return e;
     FwdUpT<true> p{TileUnits{a.tiles, a.tiles_cap, a.I / 128}, a.H, a.I, a.ring, a.hring,
-                   a.hring_s, a.preact, true, a.status, sf_w, sf_x, nullptr, nullptr};
+                   a.hring_s, a.preact, a.preact_f32, true, a.status, sf_w, sf_x, nullptr,
+                   nullptr};
     return launch(ma, mb, p, a.tiles_cap * (a.I / 128),
                   (ring_rows + TILE_ROWS_MX - 1) / TILE_ROWS_MX * (a.I / 128), s);
 }
@@ -1105,9 +1145,20 @@ cudaError_t launch_gemm_down_tc_mx(const GemmDownArgs &a, int64_t ring_rows, con
     if ((e = make_map_u8(&mb, a.hring, ring_rows, a.I, KBOX_ROWS)) != cudaSuccess) return e;
     const int nmb = (a.H + 255) / 256;
     FwdDownT<true> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.ring, a.perm, a.slots,
-                     a.status, sf_w, sf_h, a.accumulate};
+                     a.out_f32, a.status, sf_w, sf_h, a.accumulate};
     return launch(ma, mb, p, a.tiles_cap * nmb,
                   (ring_rows + TILE_ROWS_MX - 1) / TILE_ROWS_MX * nmb, s);
+}
+
+// the G GEMM with its epilogue's operand types fixed at compile time; static striding
+template <bool MX, bool PF32>
+cudaError_t launch_g(const CUtensorMap &ma, const CUtensorMap &mb, const GemmGArgs &a, int nmb,
+                     cudaStream_t s) {
+    BwdGT<MX, PF32> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff,
+                      a.perm, a.preact, a.topk_w, a.dA, a.sh, a.dS_part, 4 * nmb, a.status,
+                      MX ? a.sf_w2t : nullptr, MX ? a.sf_dy : nullptr,
+                      MX ? a.dA_q : nullptr, MX ? a.dA_s : nullptr};
+    return launch(ma, mb, p, a.tiles_cap * nmb, a.tiles_cap * nmb, s);
 }
 
 cudaError_t launch_gemm_g_tc(const GemmGArgs &a, int E, int64_t rpad_cap, cudaStream_t s) {
@@ -1124,15 +1175,12 @@ cudaError_t launch_gemm_g_tc(const GemmGArgs &a, int E, int64_t rpad_cap, cudaSt
         // A: W2t E4M3 [E*I][H], 256-row boxes; B: quantized dy [rpad][H]
         if ((e = make_map_u8(&ma, a.w2t_q, (int64_t)E * a.I, a.H, 256)) != cudaSuccess) return e;
         if ((e = make_map_u8(&mb, a.dy_q, rpad_cap, a.H, KBOX_ROWS)) != cudaSuccess) return e;
-        BwdGT<true> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff, a.perm,
-                      a.preact, a.topk_w, a.dA, a.sh, a.dS_part, 4 * nmb, a.status,
-                      a.sf_w2t, a.sf_dy, a.dA_q, a.dA_s};
-        return launch(ma, mb, p, a.tiles_cap * nmb, a.tiles_cap * nmb, s);  // static striding
+        if (a.preact_f32)
+            return launch_g<true, true>(ma, mb, a, nmb, s);
+        return launch_g<true, false>(ma, mb, a, nmb, s);
     }
-    BwdGT<false> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff, a.perm,
-                   a.preact, a.topk_w, a.dA, a.sh, a.dS_part, 4 * nmb, a.status, nullptr,
-                   nullptr, nullptr, nullptr};
-    return launch(ma, mb, p, a.tiles_cap * nmb, a.tiles_cap * nmb, s);  // static striding
+    if (a.preact_f32) return launch_g<false, true>(ma, mb, a, nmb, s);
+    return launch_g<false, false>(ma, mb, a, nmb, s);
 }
 
 int gemm_tc_dS_parts(int I) { return 4 * ((I + 255) / 256); }
@@ -1150,20 +1198,21 @@ cudaError_t launch_gemm_dgrad_tc(const GemmDgradArgs &a, int E, int64_t rpad_cap
         if ((e = make_map_u8(&mb, a.dA_q, rpad_cap, 2 * a.I, KBOX_ROWS)) != cudaSuccess)
             return e;
         BwdDgradT<true> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff,
-                          a.perm, a.dx_slots, a.status, a.sf_w13t, a.sf_dA, a.accumulate};
+                          a.perm, a.dx_slots, a.out_f32, a.status, a.sf_w13t, a.sf_dA,
+                          a.accumulate};
         return launch(ma, mb, p, a.tiles_cap * nmb,
                       (rpad_cap + TILE_ROWS_MX - 1) / TILE_ROWS_MX * nmb, s);
     }
     if ((e = make_map_bf16(&ma, a.w13, (int64_t)E * 2 * a.I, a.H, 64)) != cudaSuccess) return e;
     if ((e = make_map_bf16(&mb, a.dA, rpad_cap, 2 * a.I, KBOX_ROWS)) != cudaSuccess) return e;
     BwdDgradT<false> p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff,
-                       a.perm, a.dx_slots, a.status, nullptr, nullptr, a.accumulate};
+                       a.perm, a.dx_slots, a.out_f32, a.status, nullptr, nullptr, a.accumulate};
     return launch(ma, mb, p, a.tiles_cap * nmb, (rpad_cap + TILE_ROWS - 1) / TILE_ROWS * nmb, s);
 }
 
 // out [E][N][M] = per expert sum over padded rows of A[p][m] B[p][n]
 cudaError_t launch_wgrad_tc(const int32_t *counts, const int32_t *poff, const uint16_t *A,
-                            const uint16_t *Bm, float *out, int E, int M, int N,
+                            const uint16_t *Bm, void *out, bool out_f32, int E, int M, int N,
                             int64_t rows_a, int64_t rows_b, int *status, cudaStream_t s) {
     cudaError_t e = init_host();
     if (e != cudaSuccess) return e;
@@ -1171,7 +1220,7 @@ cudaError_t launch_wgrad_tc(const int32_t *counts, const int32_t *poff, const ui
     if ((e = make_map_bf16(&ma, A, rows_a, M, 64)) != cudaSuccess) return e;
     if ((e = make_map_bf16(&mb, Bm, rows_b, N, 64)) != cudaSuccess) return e;
     const int nmb = (M + 255) / 256, nnb = (N + TILE_ROWS - 1) / TILE_ROWS;
-    Wgrad p{counts, poff, out, E, M, N, nmb, nnb, status};
+    Wgrad p{counts, poff, out, out_f32, E, M, N, nmb, nnb, status};
     return launch(ma, mb, p, (int64_t)E * nmb * nnb, (int64_t)E * nmb * nnb, s);  // exact
 }
 

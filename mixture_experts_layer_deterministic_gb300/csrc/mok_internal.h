@@ -23,6 +23,10 @@ bool prof_on();
 // the entry points' device check (compute capability 10.3) and the device's status word
 mok_status current_device_status_word(int **status);
 
+// streaming multiprocessors of the current device (queried once per device), for sizing
+// grids in whole waves; 1 if the query fails
+int device_sm_count();
+
 // ---------------------------------------------------------------- routing / schedule
 cudaError_t launch_route_topk(const float *logits, int64_t T, int E, int K, int32_t *idx,
                               float *w, int *status, cudaStream_t s);
@@ -78,9 +82,10 @@ cudaError_t launch_quantize_mxfp8(const uint16_t *src, int64_t rows, int cols, u
 cudaError_t launch_quantize_mxfp8_transposed(const uint16_t *src, int64_t batch, int rows,
                                              int cols, uint8_t *q, uint8_t *scale,
                                              cudaStream_t s);
-// y[t] = sum_k w[t,k] * slots[t*K+k] in fp32 (w == nullptr: plain sum), k ascending
-cudaError_t launch_combine(const float *slots, const float *w, int64_t T, int K, int H,
-                           float *y, cudaStream_t s);
+// y[t] = sum_k w[t,k] * slots[t*K+k] in fp32 (w == nullptr: plain sum), k ascending;
+// slots and y are fp32 when f32, else bf16 (y rounded once, after the sum)
+cudaError_t launch_combine(const void *slots, const float *w, int64_t T, int K, int H,
+                           void *y, bool f32, cudaStream_t s);
 
 // backward: padded row offsets (each expert's rows rounded up to 16) and gathers
 cudaError_t launch_pad_offsets(const int32_t *counts, int E, int32_t *poff, cudaStream_t s);
@@ -106,7 +111,7 @@ struct Ring {
 // Forward gate/up GEMM with the SwiGLU epilogue, per tile (e, r0, r1):
 //   a[r][j] = sum_c W13[e][j][c] * xring[ring(r)][c]   (j < 2I)
 //   h[ring(r)][i] = silu(a[r][i]) * a[r][I+i]          (bf16, or MXFP8 along I)
-//   preact[r][j] = a[r][j] (fp32) when preact != nullptr
+//   preact[r][j] = a[r][j] (fp32 if preact_f32, else bf16) when preact != nullptr
 struct GemmUpArgs {
     const int32_t *tiles;
     int64_t tiles_cap;
@@ -116,15 +121,16 @@ struct GemmUpArgs {
     const uint8_t *w13_s;
     void *hring;
     uint8_t *hring_s;
-    float *preact;
+    void *preact;
     int H, I, E;
     bool mxfp8;
     Ring ring;
     int *status;
+    bool preact_f32;
 };
 
 // Forward down GEMM with the push scatter, per tile (e, r0, r1):
-//   slots[perm[r]][c] = sum_i W2[e][c][i] * hring[ring(r)][i]   (fp32)
+//   slots[perm[r]][c] = sum_i W2[e][c][i] * hring[ring(r)][i]   (fp32 if out_f32, else bf16)
 struct GemmDownArgs {
     const int32_t *tiles;
     int64_t tiles_cap;
@@ -133,12 +139,13 @@ struct GemmDownArgs {
     const void *w2;
     const uint8_t *w2_s;
     const int32_t *perm;  // slot of each sorted row; nullptr: row r -> output row r
-    float *slots;
+    void *slots;
     int H, I, E;
     bool mxfp8;
     Ring ring;
     int *status;
     bool accumulate;      // add into the output rows instead of storing
+    bool out_f32;
 };
 // The GEMMs run on the tensor cores (gemm_tc.cu). Tiles are cut at gemm_tc_tile_rows()
 // rows; ring_rows / rpad_cap are the rows of the buffers the TMA maps cover.
@@ -147,12 +154,12 @@ int gemm_tc_dS_parts(int I);
 cudaError_t launch_gemm_up_tc(const GemmUpArgs &a, int64_t ring_rows, cudaStream_t s);
 // The gate/up GEMM again, for a backward without saved pre-activations: B is the gathered
 // x in the padded expert layout (row poff[e] + r - offsets[e] holds sorted row r), and only
-// the fp32 pre-activations of each sorted row are written.
+// the pre-activations of each sorted row are written (fp32 if preact_f32, else bf16).
 cudaError_t launch_gemm_up_recompute_tc(const int32_t *tiles, int64_t tiles_cap,
                                         const uint16_t *x_perm, int64_t rpad_cap,
                                         const void *w13, const int32_t *offsets,
-                                        const int32_t *poff, float *preact, int H, int I,
-                                        int E, int *status, cudaStream_t s);
+                                        const int32_t *poff, void *preact, bool preact_f32,
+                                        int H, int I, int E, int *status, cudaStream_t s);
 cudaError_t launch_gemm_down_tc(const GemmDownArgs &a, int64_t ring_rows, cudaStream_t s);
 // MXFP8: E4M3 operands with scale atoms (see launch_scale_atoms_*): sf_w for the weights,
 // sf_x / sf_h for the token tiles
@@ -186,7 +193,7 @@ struct GemmGArgs {
     const int32_t *poff;
     const uint16_t *w2;
     const uint16_t *dy_perm;
-    const float *preact;
+    const void *preact;  // fp32 if preact_f32, else bf16
     const int32_t *perm;
     const float *topk_w;
     uint16_t *dA;
@@ -200,10 +207,11 @@ struct GemmGArgs {
     bool mxfp8 = false;
     const uint8_t *w2t_q = nullptr, *sf_w2t = nullptr, *dy_q = nullptr, *sf_dy = nullptr;
     uint8_t *dA_q = nullptr, *dA_s = nullptr;
+    bool preact_f32 = false;
 };
 
 // Backward dgrad GEMM with the reverse-dispatch scatter, per tile (e, r0, r1):
-//   dx_slots[perm[r]][c] = sum_j W13[e][j][c] * dA[p(r)][j]   (fp32)
+//   dx_slots[perm[r]][c] = sum_j W13[e][j][c] * dA[p(r)][j]   (fp32 if out_f32, else bf16)
 struct GemmDgradArgs {
     const int32_t *tiles;
     int64_t tiles_cap;
@@ -212,7 +220,7 @@ struct GemmDgradArgs {
     const uint16_t *w13;
     const uint16_t *dA;
     const int32_t *perm;
-    float *dx_slots;
+    void *dx_slots;
     int H, I;
     int *status;
     // MXFP8 (w13 and dA unused): W13 quantized along 2I and stored as W13t [E*H][2I], dA
@@ -220,13 +228,15 @@ struct GemmDgradArgs {
     bool mxfp8 = false;
     const uint8_t *w13t_q = nullptr, *sf_w13t = nullptr, *dA_q = nullptr, *sf_dA = nullptr;
     bool accumulate = false;  // add into the output rows (the shared expert adds into dx)
+    bool out_f32 = false;
 };
 cudaError_t launch_gemm_g_tc(const GemmGArgs &a, int E, int64_t rpad_cap, cudaStream_t s);
 cudaError_t launch_gemm_dgrad_tc(const GemmDgradArgs &a, int E, int64_t rpad_cap,
                                  cudaStream_t s);
 // out [E][N][M] = per expert e, sum over its padded rows p of A[p][m] * B[p][n]
+// (fp32 if out_f32, else bf16)
 cudaError_t launch_wgrad_tc(const int32_t *counts, const int32_t *poff, const uint16_t *A,
-                            const uint16_t *Bm, float *out, int E, int M, int N,
+                            const uint16_t *Bm, void *out, bool out_f32, int E, int M, int N,
                             int64_t rows_a, int64_t rows_b, int *status, cudaStream_t s);
 
 }  // namespace mok

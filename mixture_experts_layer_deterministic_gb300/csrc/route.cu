@@ -99,7 +99,8 @@ cudaError_t launch_per(const float *logits, int64_t T, int E, int K, int32_t *id
                        cudaStream_t s) {
     const int threads = 256;
     int64_t blocks = (T + 7) / 8;
-    if (blocks > 152 * 64) blocks = 152 * 64;
+    const int64_t cap = (int64_t)device_sm_count() * 64;
+    if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     route_topk_kernel<PER><<<(unsigned)blocks, threads, 0, s>>>(logits, T, E, K, idx, w);
     return cudaGetLastError();

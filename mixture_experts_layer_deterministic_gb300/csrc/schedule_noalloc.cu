@@ -9,6 +9,8 @@
 // in a fixed array in the library's own device memory instead. The array is a file-scope
 // __device__ variable of MOK_NOALLOC_SCHEDULE_SCRATCH_BYTES (4 MiB): every GPU that loads
 // the library holds it until the process exits, and the entry point allocates nothing.
+#include <atomic>
+
 #include "common.cuh"
 #include "mok_internal.h"
 
@@ -20,8 +22,9 @@ static __device__ __align__(256) int32_t
 constexpr int MAX_DEV = 64;
 // Device address of the scratch array, per device. In host code the array's name is only
 // a host-side stand-in, never a device address, so the address is looked up once per
-// device (with that device current) and cached here.
-int32_t *g_scratch_dev[MAX_DEV];
+// device (with that device current) and cached here. Host threads may make their first
+// call on a device at the same time: the cache is atomic, and both store the same address.
+std::atomic<int32_t *> g_scratch_dev[MAX_DEV];
 
 }  // namespace
 
@@ -44,16 +47,21 @@ extern "C" mok_status mok_build_schedule_noalloc(const mok_config *cfg,
         return MOK_ERR_WORKSPACE;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) return MOK_ERR_CUDA;
-    if (g_scratch_dev[dev] == nullptr) {
+    int32_t *scratch = g_scratch_dev[dev].load(std::memory_order_acquire);
+    if (scratch == nullptr) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_sched_scratch) != cudaSuccess || p == nullptr)
             return MOK_ERR_CUDA;
-        g_scratch_dev[dev] = (int32_t *)p;
+        scratch = (int32_t *)p;
+        g_scratch_dev[dev].store(scratch, std::memory_order_release);
     }
     // Nothing in the scratch has to start at zero: the first kernel writes every
     // histogram entry that the later kernels read.
-    mok::ScheduleWs w = mok::schedule_ws_carve(g_scratch_dev[dev], R, cfg->E);
+    mok::ScheduleWs w = mok::schedule_ws_carve(scratch, R, cfg->E);
+    // timed under the same kind as mok_build_schedule while profiling is on
+    mok::prof_begin(mok::KK_SCHEDULE, stream);
     const cudaError_t e =
         mok::launch_build_schedule(topk_idx, R, cfg->E, cfg->minibatch, *sched, w, status, stream);
+    mok::prof_end(mok::KK_SCHEDULE, stream, R > 0 ? 4 : 1);
     return e == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;
 }

@@ -47,13 +47,14 @@ def lib():
         L.oracle_forward.argtypes = [i64, i32, i32, i32, i32, p, p, p, i32, p, p, p, p, i32,
                                      i32, p, p, p]
         L.oracle_backward.argtypes = [i64, i32, i32, i32, i32, p, p, p, i32, p, p, p, p, i32,
-                                      i32, p, p, p, p, p, p, p, p, p, p]
+                                      i32, p, p, p, p, p, p, p, p, p, p, p, p]
         L.oracle_mxfp8_qdq_slack.argtypes = [i64, p, p, p, p, p, p]
         L.oracle_bf16_slack.argtypes = [ctypes.c_double, ctypes.c_double]
         L.oracle_bf16_slack.restype = ctypes.c_double
         L.oracle_round_bf16.argtypes = [ctypes.c_double]
         L.oracle_round_bf16.restype = ctypes.c_double
         L.oracle_router_grad.argtypes = [i64, i32, i32, p, p, p, p]
+        L.oracle_router_grad_slack.argtypes = [i64, i32, i32, p, p, p, p]
         _lib = L
     return _lib
 
@@ -149,11 +150,11 @@ class _Rows(ctypes.Structure):
     """oracle_rows: optional per-routed-row intermediates (oracle.h)."""
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "a", "a_mag", "a_slack", "h", "h_slack", "h_q", "h_scale", "da", "da_slack", "sh",
-        "sh_slack", "da_q", "da_scale", "daq_slack", "h_in", "a_in", "da_in", "sh_in",
-        "daq_in")]
+        "sh_slack", "da_q", "da_scale", "daq_slack", "dtopk_slack", "h_in", "a_in", "da_in",
+        "sh_in", "daq_in", "y_in", "dx_in")]
 
 
-_INPUTS = ("h_in", "a_in", "da_in", "sh_in", "daq_in")
+_INPUTS = ("h_in", "a_in", "da_in", "sh_in", "daq_in", "y_in", "dx_in")
 
 
 def _rows(R, I, names, mx, given=None):
@@ -165,7 +166,8 @@ def _rows(R, I, names, mx, given=None):
                   h_scale=(R, I // 32, np.uint8), da=(R, 2 * I, np.float64),
                   da_slack=(R, 2 * I, np.float64), sh=(R, I, np.float64),
                   sh_slack=(R, I, np.float64), da_q=(R, 2 * I, np.uint8),
-                  da_scale=(R, 2 * I // 32, np.uint8), daq_slack=(R, 2 * I, np.float64))
+                  da_scale=(R, 2 * I // 32, np.uint8), daq_slack=(R, 2 * I, np.float64),
+                  dtopk_slack=(R, 1, np.float64))
     out = {}
     st = _Rows()
     for n in names:
@@ -176,6 +178,11 @@ def _rows(R, I, names, mx, given=None):
     keep = {}
     for n, v in (given or {}).items():
         assert n in _INPUTS, n
+        if n in ("y_in", "dx_in"):  # [T][H], per token
+            a = np.ascontiguousarray(v, np.float64)
+            keep[n] = a
+            setattr(st, n, a.ctypes.data)
+            continue
         want = 2 * I if n in ("a_in", "da_in", "daq_in") else I
         a = np.ascontiguousarray(v, np.float64).reshape(R, want)
         keep[n] = a
@@ -234,7 +241,8 @@ def forward(x, idx, w, w13, w2, mode=EXACT, with_slack=False, store=STORE_F32, r
     decisions taken on values within fp32 error of a midpoint. `rows` names per-routed-row
     intermediates (oracle_rows fields: a, a_mag, h, h_slack, h_q, h_scale) to return as a
     dict after the other results; `given` = {"h_in": [T*K, I]} feeds the down GEMM the
-    given h (rows in flat id order t*K + k) instead of the oracle's own."""
+    given h (rows in flat id order t*K + k) instead of the oracle's own, and {"y_in": [T, H]}
+    adds the expert outputs to y_in (see oracle_rows)."""
     x, w = _f64(x), _f64(w)
     idx = _i32(idx)
     k13, d13, s13, sh13 = _weights(w13)
@@ -257,29 +265,41 @@ def forward(x, idx, w, w13, w2, mode=EXACT, with_slack=False, store=STORE_F32, r
     return out if len(out) > 1 else out[0]
 
 
+def quantize_transposed_bf16(bits):
+    """MXFP8 codes and scales of the transpose of each [rows][cols] matrix of `bits` (bf16
+    patterns [E][rows][cols]), quantized along its rows: (q [E][cols][rows],
+    scale [E][cols][rows/32]) -- the oracle's row quantizer on an explicit transpose."""
+    return mxfp8_quantize_bf16(np.ascontiguousarray(np.swapaxes(bits, -1, -2)))
+
+
 def backward(x, idx, w, w13, w2, dy, weight_grads=True, mode=EXACT, with_slack=False,
-             store=STORE_F32, rows=(), given=None):
+             store=STORE_F32, rows=(), given=None, mx_weights=None):
     """Layer backward in fp64: (dx, dw13, dw2, dtopk), with the operand rounding of `mode`
     (EXACT, BF16 or MXFP8) and the storage rounding of `store`; dw13/dw2 are None when
     weight_grads is False. With with_slack, also the slacks of dx, dw13, dw2 (see forward).
     `rows` names per-routed-row intermediates (a, a_slack, da, da_slack, sh, sh_slack,
     da_q, da_scale, daq_slack) to return as a dict after the other results; `given` maps
     a_in, da_in, sh_in, daq_in to arrays ([T*K, 2I] or [T*K, I], flat id order) that replace
-    the oracle's own values where they enter the next step.
+    the oracle's own values where they enter the next step, and dx_in [T, H] to a dx that
+    the results are added to (see oracle_rows).
 
     In MXFP8 mode w13 and w2 are the bf16 weights (uint16 bit patterns). A is recomputed
     with the forward's operands (x and W13 quantized along H); G uses dy and W2 quantized
     along H; dgrad uses dA and W13 quantized along 2I; the weight gradients use bf16 dA
-    and w*h."""
+    and w*h. mx_weights may give those three quantizations, as made by this module
+    (mxfp8_quantize_bf16(w13), quantize_transposed_bf16(w13), quantize_transposed_bf16(w2)),
+    so that a caller running many backward calls on the same weights computes them once."""
     x, w, dy = _f64(x), _f64(w), _f64(dy)
     idx = _i32(idx)
-    w13d = w2g = None
+    mxw = (None,) * 4
     s13 = None
     if mode == MXFP8:
         assert w13.dtype == np.uint16 and w2.dtype == np.uint16
-        w13d = mxfp8_qdq_axis_bf16(w13, axis=1)   # W13 [E][2I][H] along 2I
-        w2g = mxfp8_qdq_axis_bf16(w2, axis=1)     # W2 [E][H][I] along H
-        w13 = mxfp8_quantize_bf16(w13)            # the forward's W13, along H
+        if mx_weights is None:
+            mx_weights = (mxfp8_quantize_bf16(w13), quantize_transposed_bf16(w13),
+                          quantize_transposed_bf16(w2))
+        w13, w13t, w2t = mx_weights               # W13 along H; W13 along 2I; W2 along H
+        mxw = tuple(np.ascontiguousarray(a, np.uint8) for a in (*w13t, *w2t))
     k13, d13, s13, sh13 = _weights(w13)
     k2, d2, _, sh2 = _weights(w2)
     assert k2 != W_MXFP8 and (k13 != W_MXFP8 or mode == MXFP8)
@@ -296,7 +316,7 @@ def backward(x, idx, w, w13, w2, dy, weight_grads=True, mode=EXACT, with_slack=F
     (rv, _keep), rs = _rows(T * K, I2 // 2, rows, mode == MXFP8, given)
     n = lambda a: None if a is None else _p(a)  # noqa: E731
     lib().oracle_backward(T, H, I2 // 2, E, K, _p(x), _p(idx), _p(w), k13, _p(d13), n(s13),
-                          _p(d2), _p(dy), int(mode), int(store), n(w13d), n(w2g), _p(dx),
+                          _p(d2), _p(dy), int(mode), int(store), *(n(a) for a in mxw), _p(dx),
                           n(dw13), n(dw2), _p(dtopk), n(sdx), n(sdw13), n(sdw2),
                           ctypes.addressof(rs) if (rows or given) else None)
     out = (dx, dw13, dw2, dtopk)
@@ -333,3 +353,12 @@ def router_grad(idx, w, dtopk, E):
     lib().oracle_router_grad(T, E, K, _p(idx), _p(w), _p(dtopk), _p(dl))
     return dl
 
+
+
+def router_grad_slack(idx, w, sdtopk, E):
+    """Slack of router_grad's logit gradients given the slack of each dS (oracle.h)."""
+    idx, w, sdtopk = _i32(idx), _f64(w), _f64(sdtopk)
+    T, K = idx.shape
+    sl = np.empty((T, E), np.float64)
+    lib().oracle_router_grad_slack(T, E, K, _p(idx), _p(w), _p(sdtopk), _p(sl))
+    return sl

@@ -213,6 +213,17 @@ static double wget(int32_t kind, const void *data, const uint8_t *scale, int64_t
                  (int)scale[row * (row_len / 32) + col / 32] - 127);
 }
 
+/* element [e][r][col] of a weight given as the MXFP8 codes q [E][ncol][nrow] and scales
+ * s [E][ncol][nrow/32] of its transpose, quantized along the transposed rows (that is,
+ * along r in 32-blocks) */
+static double wq_t(const uint8_t *q, const uint8_t *s, int64_t e, int64_t ncol, int64_t nrow,
+                   int64_t r, int64_t col)
+{
+    const int64_t row_t = e * ncol + col;
+    return ldexp(oracle_e4m3_decode(q[row_t * nrow + r]),
+                 (int)s[row_t * (nrow / 32) + r / 32] - 127);
+}
+
 double oracle_round_bf16(double v)
 {
     if (v == 0.0 || isnan(v) || isinf(v))
@@ -359,6 +370,14 @@ static double dsilu(double g)
     const double sg = 1.0 / (1.0 + exp(-g));
     return sg * (1.0 + g * (1.0 - sg));
 }
+/* how far h = silu(a_g) a_u can move when a_g and a_u move by up to ug and uu: by the
+ * mean-value theorem, with the second derivative of silu at most 1/2 in magnitude,
+ * (|silu'(a_g)| + ug / 2) ug (|a_u| + uu) + |silu(a_g)| uu, where sl = silu(a_g) */
+static double dh_of_a(double ag, double au, double sl, double ug, double uu)
+{
+    return (fabs(dsilu(ag)) + 0.5 * ug) * ug * (fabs(au) + uu) + fabs(sl) * uu;
+}
+
 static double d2silu(double g)
 {
     const double sg = 1.0 / (1.0 + exp(-g));
@@ -390,11 +409,17 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
         uint8_t *hq = (uint8_t *)malloc((size_t)I);
         uint8_t *hsc = (uint8_t *)malloc((size_t)(I / 32 + 1));
         double *yt = y + t * (int64_t)H;
+        /* an output added to an existing one: no slot, the fp32 error of each o and of the
+         * additions carried into the final rounding */
+        const double *y0 = (rows && rows->y_in) ? rows->y_in + t * (int64_t)H : NULL;
+        double *ye = (double *)calloc((size_t)H, sizeof(double));
         memcpy(xt, x + t * (int64_t)H, sizeof(double) * (size_t)H);
         if (mode == ORACLE_MXFP8)
             qdq_row(H, xt);
-        for (int32_t c = 0; c < H; ++c)
-            yt[c] = 0.0;
+        for (int32_t c = 0; c < H; ++c) {
+            yt[c] = y0 ? y0[c] : 0.0;
+            ym[c] = y0 ? fabs(y0[c]) : 0.0;
+        }
         for (int32_t k = 0; k < K; ++k) {
             const int64_t f = t * K + k;
             const int64_t e = idx[f];
@@ -463,8 +488,10 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
             const double s = w[f];
             for (int32_t c = 0; c < H; ++c) {
                 double so = ou[c];
-                if (sto) /* the (token, k) slot holds bf16(o) */
+                if (sto && !y0) /* the (token, k) slot holds bf16(o) */
                     o[c] = round_bf16_with_slack(o[c], ORACLE_DOT_REL * om[c], ou[c], &so);
+                if (y0)
+                    ye[c] += fabs(s) * ORACLE_DOT_REL * om[c];
                 yt[c] += s * o[c];
                 ym[c] += fabs(s * o[c]);
                 sy[c] += fabs(s) * so;
@@ -473,10 +500,13 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
         for (int32_t c = 0; c < H; ++c) {
             double sc = sy[c];
             if (sto) /* y = bf16 of the fixed-order fp32 k-sum */
-                yt[c] = round_bf16_with_slack(yt[c], K * ORACLE_SUM_ULP * ym[c], sy[c], &sc);
+                yt[c] = round_bf16_with_slack(yt[c], (K + (y0 ? 1 : 0)) * ORACLE_SUM_ULP * ym[c] +
+                                                         ye[c],
+                                              sy[c], &sc);
             if (slack)
                 slack[t * (int64_t)H + c] = sc;
         }
+        free(ye);
         free(xt);
         free(a);
         free(aa);
@@ -499,7 +529,8 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
 void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
                      const int32_t *idx, const double *w, int32_t wkind, const void *w13,
                      const uint8_t *w13_s, const void *w2, const double *dy, int32_t mode,
-                     int32_t store, const double *w13d, const double *w2g, double *dx,
+                     int32_t store, const uint8_t *w13d_q, const uint8_t *w13d_s,
+                     const uint8_t *w2g_q, const uint8_t *w2g_s, double *dx,
                      double *dw13, double *dw2, double *dtopk, double *sdx, double *sdw13,
                      double *sdw2, oracle_rows *rows)
 {
@@ -547,8 +578,14 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
             qdq_row(H, dyq);
         }
         const double *xa = mx ? xq : xt, *dyg = mx ? dyq : dyt;
-        for (int32_t c = 0; c < H; ++c)
-            dxt[c] = 0.0;
+        /* a dx added to an existing one: no slots, each dgrad result's fp32 error and the
+         * additions' carried into the final rounding */
+        const double *dx0 = (rows && rows->dx_in) ? rows->dx_in + t * (int64_t)H : NULL;
+        double *dxe = (double *)calloc((size_t)H, sizeof(double));
+        for (int32_t c = 0; c < H; ++c) {
+            dxt[c] = dx0 ? dx0[c] : 0.0;
+            dxm[c] = dx0 ? fabs(dx0[c]) : 0.0;
+        }
         for (int32_t k = 0; k < K; ++k) {
             const int64_t f = t * K + k;
             const int64_t e = idx[f];
@@ -590,7 +627,7 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
             for (int32_t i = 0; i < I; ++i) {
                 double acc = 0.0, mag = 0.0;
                 for (int32_t c = 0; c < H; ++c) {
-                    const double wv = mx ? w2g[b2 + (int64_t)c * I + i]
+                    const double wv = mx ? wq_t(w2g_q, w2g_s, e, I, H, c, i)
                                          : wget(wkind, w2, NULL, I, b2 + (int64_t)c * I + i);
                     acc += wv * dyg[c];
                     mag += fabs(wv * dyg[c]);
@@ -598,13 +635,15 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
                 g[i] = acc;
                 gg[i] = mag;
             }
-            double dS = 0.0;
+            double dS = 0.0, sdS = 0.0;
             for (int32_t i = 0; i < I; ++i) {
                 const double ag = a[i], au = a[I + i];
                 const double sig = 1.0 / (1.0 + exp(-ag));
                 const double sl = ag * sig;
                 const double hi = sl * au;
                 dS += g[i] * hi;
+                /* h moves with the stored A's decisions (mean-value bound, dh_of_a) */
+                sdS += fabs(g[i]) * dh_of_a(ag, au, sl, ua[i], ua[I + i]);
                 const double dh = s * g[i];
                 /* silu'(g) = sig * (1 + g * (1 - sig)) */
                 da[i] = dh * au * sig * (1.0 + ag * (1.0 - sig));
@@ -615,14 +654,24 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
                 const double d1 = dsilu(ag), d2 = d2silu(ag);
                 const double eg = ORACLE_DOT_REL * gg[i];
                 const double as = fabs(s);
+                /* silu'(a_g) = sig * (1 + a_g * (1 - sig)) cancels near a_g = -1.28: the
+                 * kernel's fp32 evaluation is off by a few ulps of the terms, not of the
+                 * result, so its absolute error is bounded by ORACLE_SLACK_REL * sig *
+                 * (1 + |a_g|) */
+                const double e_d1 = ORACLE_SLACK_REL * sig * (1.0 + fabs(ag));
                 dae[i] = as * (fabs(au * d1) * eg + fabs(g[i] * d1) * ea[I + i] +
-                               fabs(g[i] * au * d2) * ea[i]);
-                dau[i] = as * (fabs(g[i] * d1) * ua[I + i] + fabs(g[i] * au * d2) * ua[i]);
+                               fabs(g[i] * au * d2) * ea[i] + fabs(g[i] * au) * e_d1);
+                /* slack carried from the stored A, by the mean-value theorem over the
+                 * flipped interval, with the second and third derivatives of silu at
+                 * most 1/2 in magnitude everywhere */
+                dau[i] = as * fabs(g[i]) * (fabs(d1) * ua[I + i] +
+                                            (fabs(au) + ua[I + i]) *
+                                                (fabs(d2) + 0.5 * ua[i]) * ua[i]);
                 dae[I + i] = as * (fabs(sl) * eg + fabs(g[i] * d1) * ea[i]);
-                dau[I + i] = as * fabs(g[i] * d1) * ua[i];
+                dau[I + i] = as * fabs(g[i]) * (fabs(d1) + 0.5 * ua[i]) * ua[i];
                 if (rnd) {
                     const double e_sh = as * (fabs(d1 * au) * ea[i] + fabs(sl) * ea[I + i]);
-                    const double u_sh = as * (fabs(d1 * au) * ua[i] + fabs(sl) * ua[I + i]);
+                    const double u_sh = as * dh_of_a(ag, au, sl, ua[i], ua[I + i]);
                     sh[i] = round_bf16_with_slack(sh[i], e_sh, u_sh, &shs[i]);
                 }
             }
@@ -637,6 +686,8 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
                 for (int32_t j = 0; j < 2 * I; ++j)
                     da[j] = round_bf16_with_slack(da[j], dae[j], dau[j], &das[j]);
             dtopk[f] = dS;
+            if (rows && rows->dtopk_slack)
+                rows->dtopk_slack[f] = sdS;
             if (rows) {
                 if (rows->da)
                     memcpy(rows->da + f * 2 * I, da, sizeof(double) * 2 * (size_t)I);
@@ -678,7 +729,8 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
                 const double dj = dad[j], sj = dads[j];
                 for (int32_t c = 0; c < H; ++c) {
                     const int64_t o = b13 + (int64_t)j * H + c;
-                    const double wv = mx ? w13d[o] : wget(wkind, w13, w13_s, H, o);
+                    const double wv = mx ? wq_t(w13d_q, w13d_s, e, H, 2 * (int64_t)I, j, c)
+                                         : wget(wkind, w13, w13_s, H, o);
                     xs[c] += wv * dj;
                     xm[c] += fabs(wv * dj);
                     xu[c] += fabs(wv) * sj;
@@ -686,8 +738,10 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
             }
             for (int32_t c = 0; c < H; ++c) {
                 double sx = xu[c];
-                if (sto) /* the slot holds bf16 of its dgrad result */
+                if (sto && !dx0) /* the slot holds bf16 of its dgrad result */
                     xs[c] = round_bf16_with_slack(xs[c], ORACLE_DOT_REL * xm[c], xu[c], &sx);
+                if (dx0)
+                    dxe[c] += ORACLE_DOT_REL * xm[c];
                 dxt[c] += xs[c];
                 dxm[c] += fabs(xs[c]);
                 sdt[c] += sx;
@@ -696,10 +750,12 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
         for (int32_t c = 0; c < H; ++c) {
             double sc = sdt[c];
             if (sto) /* dx = bf16 of the fixed-order fp32 k-sum */
-                dxt[c] = round_bf16_with_slack(dxt[c], K * ORACLE_SUM_ULP * dxm[c], sdt[c], &sc);
+                dxt[c] = round_bf16_with_slack(
+                    dxt[c], (K + (dx0 ? 1 : 0)) * ORACLE_SUM_ULP * dxm[c] + dxe[c], sdt[c], &sc);
             if (sdx)
                 sdx[t * (int64_t)H + c] = sc;
         }
+        free(dxe);
         free(a);
         free(ea);
         free(ua);
@@ -799,5 +855,21 @@ void oracle_router_grad(int64_t T, int32_t E, int32_t K, const int32_t *idx, con
             sw += w[t * K + k] * dtopk[t * K + k];
         for (int32_t k = 0; k < K; ++k)
             dl[idx[t * K + k]] = w[t * K + k] * (dtopk[t * K + k] - sw);
+    }
+}
+
+void oracle_router_grad_slack(int64_t T, int32_t E, int32_t K, const int32_t *idx,
+                              const double *w, const double *sdtopk, double *sdlogits)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        double *sl = sdlogits + t * (int64_t)E;
+        for (int32_t e = 0; e < E; ++e)
+            sl[e] = 0.0;
+        double sw = 0.0;
+        for (int32_t k = 0; k < K; ++k)
+            sw += fabs(w[t * K + k]) * sdtopk[t * K + k];
+        for (int32_t k = 0; k < K; ++k)
+            sl[idx[t * K + k]] = fabs(w[t * K + k]) * (sdtopk[t * K + k] + sw);
     }
 }

@@ -65,7 +65,8 @@ double oracle_round_bf16(double v);
 /* Rounding slack. A kernel computes the value it rounds (h, dA, w*h, a stored result) in
  * fp32 from fp32 dot products, so its value may differ from the exact one by up to
  * ORACLE_DOT_REL times the sum of the dot products' absolute terms (propagated through the
- * SwiGLU formulas), plus ORACLE_SLACK_REL of the value for the elementwise operations. A
+ * SwiGLU formulas), plus ORACLE_SLACK_REL of the value for the elementwise operations
+ * (of the terms, where a formula cancels: silu'(g) = sig (1 + g (1 - sig)) near its root). A
  * fixed-order fp32 sum of n terms (the k-sums of the combine and of dx) is within
  * n * 2^-24 of the sum of its absolute terms (the textbook bound for recursive summation
  * with unit roundoff 2^-24). When the exact value lies within its bound of a rounding
@@ -129,6 +130,8 @@ enum { ORACLE_STORE_F32 = 0, ORACLE_STORE_BF16 = 1 };
  *   sh, sh_slack [R][I]   backward: w*h rounded to bf16
  *   da_q [R][2I], da_scale [R][2I/32], daq_slack [R][2I]  backward, MXFP8: dA quantized
  *                    along 2I (the dgrad operand) and the slack of its dequantized value
+ *   dtopk_slack [R]  backward: slack of dS = <g, h> carried in from the stored A's
+ *                    decisions (h moves with A); dS itself is not rounded
  * and optional given values, which replace the oracle's own at the point where they enter
  * the next step (each with zero slack). They let a test check one step at a time: the
  * step's own rounding decisions on the values a kernel actually fed it.
@@ -136,7 +139,13 @@ enum { ORACLE_STORE_F32 = 0, ORACLE_STORE_BF16 = 1 };
  *   a_in   [R][2I] backward: A as the backward reads it
  *   da_in  [R][2I], sh_in [R][I]  backward: the bf16 dA and w*h of the weight-gradient
  *                  GEMMs (and, in BF16 mode, dA of the dgrad GEMM)
- *   daq_in [R][2I] backward, MXFP8: the dequantized dA of the dgrad GEMM */
+ *   daq_in [R][2I] backward, MXFP8: the dequantized dA of the dgrad GEMM
+ * and, for an expert whose output is added to an existing output (a shared expert):
+ *   y_in   [T][H] forward: y starts from y_in[t], and each k's weighted expert output is
+ *                  added to it directly in fp32 (no slot in between); only the final y is
+ *                  stored (bf16 under ORACLE_STORE_BF16)
+ *   dx_in  [T][H] backward: likewise, dx starts from dx_in[t] and each k's dgrad result is
+ *                  added directly */
 typedef struct oracle_rows {
     double *a, *a_mag, *a_slack;
     double *h, *h_slack;
@@ -144,7 +153,9 @@ typedef struct oracle_rows {
     double *da, *da_slack, *sh, *sh_slack;
     uint8_t *da_q, *da_scale;
     double *daq_slack;
+    double *dtopk_slack;
     const double *h_in, *a_in, *da_in, *sh_in, *daq_in;
+    const double *y_in, *dx_in;
 } oracle_rows;
 
 /* Forward of the layer, per token, with no schedule and no permutation:
@@ -171,17 +182,21 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
  * weight-gradient GEMMs) or ORACLE_MXFP8 ([arex] section "pull 代替 push": MXFP8
  * activations and pre-quantized weights): A is recomputed from the forward's quantized
  * operands (x quantized along H, W13 given as ORACLE_W_MXFP8 with w13_s), G = W2g^T Q(dy)
- * with dy quantized along H and W2g = W2 quantized along H (w2g [E][H][I], dequantized),
- * dx = W13d^T Q(dA) with dA quantized in 32-blocks along 2I and W13d = W13 quantized along
- * 2I (w13d [E][2I][H], dequantized); the weight gradients take dA and w*h rounded to bf16
- * as in ORACLE_BF16. store is ORACLE_STORE_*. Weights are ORACLE_W_F64 or ORACLE_W_BF16
- * (ORACLE_W_MXFP8 for w13 in MXFP8 mode; w13d, w2g are NULL otherwise).
+ * with dy quantized along H and W2g = W2 quantized along H, dx = W13d^T Q(dA) with dA
+ * quantized in 32-blocks along 2I and W13d = W13 quantized along 2I; the weight gradients
+ * take dA and w*h rounded to bf16 as in ORACLE_BF16. W13d and W2g are given as the codes
+ * and scales of the transposed weights quantized along their rows: w13d_q [E][H][2I] with
+ * w13d_s [E][H][2I/32] (W13d[e][j][c] from code [e][c][j]) and w2g_q [E][I][H] with w2g_s
+ * [E][I][H/32] (W2g[e][c][i] from code [e][i][c]). store is ORACLE_STORE_*. Weights are
+ * ORACLE_W_F64 or ORACLE_W_BF16 (ORACLE_W_MXFP8 for w13 in MXFP8 mode; the w13d and w2g
+ * arrays are NULL otherwise).
  * Outputs: dx [T][H], dw13 [E][2I][H], dw2 [E][H][I], dtopk [T][K] (= dS); dw13/dw2 may be
  * NULL (skipped); the slacks sdx, sdw13, sdw2 and rows are nullable. */
 void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const double *x,
                      const int32_t *idx, const double *w, int32_t wkind, const void *w13,
                      const uint8_t *w13_s, const void *w2, const double *dy, int32_t mode,
-                     int32_t store, const double *w13d, const double *w2g, double *dx,
+                     int32_t store, const uint8_t *w13d_q, const uint8_t *w13d_s,
+                     const uint8_t *w2g_q, const uint8_t *w2g_s, double *dx,
                      double *dw13, double *dw2, double *dtopk, double *sdx, double *sdw13,
                      double *sdw2, oracle_rows *rows);
 
@@ -189,6 +204,11 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
  * dlogits[t,j] = w_k (dS_k - sum_m w_m dS_m); every other logit gets 0. */
 void oracle_router_grad(int64_t T, int32_t E, int32_t K, const int32_t *idx, const double *w,
                         const double *dtopk, double *dlogits);
+
+/* The slack of those logit gradients given the slack sdtopk [T][K] of each dS: for a chosen
+ * expert j = idx[t,k], w_k (sdtopk[t,k] + sum_m w_m sdtopk[t,m]); 0 elsewhere. */
+void oracle_router_grad_slack(int64_t T, int32_t E, int32_t K, const int32_t *idx,
+                              const double *w, const double *sdtopk, double *sdlogits);
 
 #ifdef __cplusplus
 }

@@ -5,7 +5,7 @@
  * usage: c_forward T H I E K minibatch ring_capacity dir
  *   dir/x.bin      bf16 [T][H]       dir/logits.bin  fp32 [T][E]
  *   dir/w13.bin    bf16 [E][2I][H]   dir/w2.bin      bf16 [E][H][I]
- * writes dir/y.bin (fp32 [T][H]) and dir/idx.bin (int32 [T][K]); exit status 0 on success. */
+ * writes dir/y.bin (bf16 [T][H]) and dir/idx.bin (int32 [T][K]); exit status 0 on success. */
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -69,6 +69,7 @@ int main(int argc, char **argv) {
     cfg.minibatch = atoi(argv[6]);
     cfg.ring_capacity = atoi(argv[7]);
     cfg.prec = MOK_BF16;
+    cfg.flags = 0; /* bf16 storage: y is bf16 */
     const char *dir = argv[8];
     MOK_CHECK(mok_check_config(&cfg));
 
@@ -93,7 +94,7 @@ int main(int argc, char **argv) {
     CUDA_CHECK(cudaMalloc(&logits, nl));
     CUDA_CHECK(cudaMalloc(&w13, n13));
     CUDA_CHECK(cudaMalloc(&w2, n2));
-    CUDA_CHECK(cudaMalloc(&y, T * H * 4));
+    CUDA_CHECK(cudaMalloc(&y, T * H * 2));
     CUDA_CHECK(cudaMalloc((void **)&idx, R * 4));
     CUDA_CHECK(cudaMalloc((void **)&topk_w, R * 4));
     CUDA_CHECK(cudaMalloc((void **)&counts, E * 4));
@@ -125,12 +126,12 @@ int main(int argc, char **argv) {
         return 1;
     }
 
-    float *hy = (float *)malloc(T * H * 4);
+    uint16_t *hy = (uint16_t *)malloc(T * H * 2);
     int32_t *hidx = (int32_t *)malloc(R * 4);
     if (!hy || !hidx) return 1;
-    CUDA_CHECK(cudaMemcpy(hy, y, T * H * 4, cudaMemcpyDeviceToHost));
+    CUDA_CHECK(cudaMemcpy(hy, y, T * H * 2, cudaMemcpyDeviceToHost));
     CUDA_CHECK(cudaMemcpy(hidx, idx, R * 4, cudaMemcpyDeviceToHost));
-    if (write_file(dir, "y.bin", hy, T * H * 4) || write_file(dir, "idx.bin", hidx, R * 4)) {
+    if (write_file(dir, "y.bin", hy, T * H * 2) || write_file(dir, "idx.bin", hidx, R * 4)) {
         fprintf(stderr, "cannot write outputs to %s\n", dir);
         return 1;
     }

@@ -57,15 +57,16 @@ def _elem(rng, v):
     return v * (1.0 + 0.9 * SLACK_REL * rng.uniform(-1.0, 1.0, np.shape(v)))
 
 
-def forward(rng, x, idx, w, w13, w2, mode, h_in=None):
+def forward(rng, x, idx, w, w13, w2, mode, h_in=None, y_in=None):
     """One possible kernel result of the forward with bf16 storage: (y [T, H], h [T*K, I]),
     h as it entered the down GEMM (rows in flat id order t*K + k). With h_in, that h is
-    used instead of computing one."""
+    used instead of computing one; with y_in, the weighted expert outputs are added to y_in
+    in fp32 with no bf16 slot in between (an expert added to an existing output)."""
     T, H = x.shape
     K = idx.shape[1]
     I = w13.shape[1] // 2
     xa = mx_qdq_rows(x) if mode == oracle.MXFP8 else x
-    y = np.zeros((T, H), np.float32)
+    y = np.zeros((T, H), np.float32) if y_in is None else np.asarray(y_in, np.float32)
     hs = np.zeros((T * K, I))
     for k in range(K):
         o = np.empty((T, H))
@@ -78,16 +79,19 @@ def forward(rng, x, idx, w, w13, w2, mode, h_in=None):
             else:
                 h = h_in[t * K + k]
             hs[t * K + k] = h
-            o[t] = bf16(_dot(rng, w2[e], h))            # the (token, k) slot
+            o[t] = _dot(rng, w2[e], h)
+            if y_in is None:
+                o[t] = bf16(o[t])                       # the (token, k) slot
         y = y + (w[:, k:k + 1].astype(np.float32) * o.astype(np.float32))  # fp32, k ascending
     return bf16(y), hs
 
 
-def backward(rng, x, idx, w, w13, w2, dy, mode, given=None):
+def backward(rng, x, idx, w, w13, w2, dy, mode, given=None, dx_in=None):
     """One possible kernel result of the backward with bf16 storage: dx, dw13, dw2 and a
     dict of the intermediates (rows in flat id order): a (saved A), da, sh (bf16), daq
     (MXFP8: dequantized dgrad operand), slot (each slot's bf16 dgrad result). `given` may hold a_in, da_in, sh_in, daq_in to use
-    instead of computing them."""
+    instead of computing them. With dx_in, each dgrad result is added to dx_in in fp32 with
+    no bf16 slot in between."""
     given = given or {}
     T, H = x.shape
     K = idx.shape[1]
@@ -100,7 +104,7 @@ def backward(rng, x, idx, w, w13, w2, dy, mode, given=None):
     w2g = qcols(w2) if mx else w2                # G's W2 (along H)
     xa = mx_qdq_rows(x) if mx else x
     dyg = mx_qdq_rows(dy) if mx else dy
-    dx = np.zeros((T, H), np.float32)
+    dx = np.zeros((T, H), np.float32) if dx_in is None else np.asarray(dx_in, np.float32)
     rows = dict(a=np.zeros((T * K, I2)), da=np.zeros((T * K, I2)), sh=np.zeros((T * K, I)),
                 daq=np.zeros((T * K, I2)), slot=np.zeros((T * K, H)))
     for k in range(K):
@@ -115,8 +119,11 @@ def backward(rng, x, idx, w, w13, w2, dy, mode, given=None):
             ag, au = a[:I], a[I:]
             g = _dot(rng, w2g[e].T, dyg[t])
             sig = 1.0 / (1.0 + np.exp(-ag))
-            da = np.concatenate([_elem(rng, s * g * au * _dsilu(ag)),
-                                 _elem(rng, s * g * ag * sig)])
+            # silu'(a_g) = sig (1 + a_g (1 - sig)) evaluated in fp32 cancels near its root:
+            # its error is a few ulps of the terms (1, |a_g|), not of the result
+            d1 = _dsilu(ag) + 0.9 * SLACK_REL * sig * (1.0 + np.abs(ag)) * \
+                rng.uniform(-1.0, 1.0, ag.shape)
+            da = np.concatenate([_elem(rng, s * g * au * d1), _elem(rng, s * g * ag * sig)])
             sh = bf16(_elem(rng, s * ag * sig * au))
             daq = mx_qdq_rows(da) if mx else None
             da = bf16(da)
@@ -129,7 +136,9 @@ def backward(rng, x, idx, w, w13, w2, dy, mode, given=None):
             rows["a"][f], rows["da"][f], rows["sh"][f] = a, da, sh
             if mx:
                 rows["daq"][f] = daq
-            xs[t] = bf16(_dot(rng, w13d[e].T, daq if mx else da))  # the slot's dgrad result
+            xs[t] = _dot(rng, w13d[e].T, daq if mx else da)
+            if dx_in is None:
+                xs[t] = bf16(xs[t])                    # the slot's dgrad result
             rows["slot"][f] = xs[t]
         dx = dx + xs.astype(np.float32)
     dw13 = np.zeros(w13.shape)

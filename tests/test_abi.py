@@ -116,6 +116,8 @@ def cfg(**kw):
     (dict(prec=5), B.MOK_ERR_INVALID_ARG),
     (dict(T=1 << 28, K=8, E=8), B.MOK_ERR_INVALID_ARG),  # R >= 2^31
     (dict(abi_version=99), B.MOK_ERR_ABI),
+    (dict(flags=B.MOK_FLAG_FP32_STORAGE), B.MOK_OK),
+    (dict(flags=2), B.MOK_ERR_INVALID_ARG),       # unknown flag
 ])
 def test_check_config(lib, kw, want):
     assert B.mok_check_config(cfg(**kw)) == want
@@ -125,11 +127,19 @@ def test_workspace_sizes(lib):
     c = cfg()
     for which in (B.MOK_WS_SCHEDULE, B.MOK_WS_FORWARD, B.MOK_WS_BACKWARD):
         assert B.mok_workspace_size(c, which) > 0
-    # the recompute backward adds the [R][2I] fp32 pre-activations (plus alignment)
-    extra = (B.mok_workspace_size(c, B.MOK_WS_BACKWARD_RECOMPUTE) -
-             B.mok_workspace_size(c, B.MOK_WS_BACKWARD))
+    # the recompute backward adds the [R][2I] pre-activations (plus alignment): bf16, or
+    # fp32 under fp32 storage
     R, I = c.T * c.K, c.I
-    assert R * 2 * I * 4 <= extra < R * 2 * I * 4 + 256
+    for flags, esz in ((0, 2), (B.MOK_FLAG_FP32_STORAGE, 4)):
+        cf = cfg(flags=flags)
+        extra = (B.mok_workspace_size(cf, B.MOK_WS_BACKWARD_RECOMPUTE) -
+                 B.mok_workspace_size(cf, B.MOK_WS_BACKWARD))
+        assert R * 2 * I * esz <= extra < R * 2 * I * esz + 256
+    # fp32 storage doubles the (token, k) slots of the forward
+    H = c.H
+    d = (B.mok_workspace_size(cfg(flags=B.MOK_FLAG_FP32_STORAGE), B.MOK_WS_FORWARD) -
+         B.mok_workspace_size(c, B.MOK_WS_FORWARD))
+    assert R * H * 2 <= d < R * H * 2 + 256
     assert B.mok_workspace_size(c, 99) == 0
     assert B.mok_workspace_size(cfg(K=9), B.MOK_WS_FORWARD) == 0
     # a smaller ring needs a smaller forward workspace
@@ -175,3 +185,56 @@ def test_device_calls_fail_cleanly_without_gpu(lib):
         pytest.skip("a GPU is present")
     st = B.lib().mok_route_topk(B.ctypes.byref(cfg()), None, None, None, None)
     assert st in (B.MOK_ERR_CUDA, B.MOK_ERR_UNSUPPORTED)
+
+
+ITEMS = {
+    B.MOK_WS_FORWARD: [B.MOK_ITEM_X_RING, B.MOK_ITEM_H_RING, B.MOK_ITEM_SLOTS],
+    B.MOK_WS_BACKWARD: [B.MOK_ITEM_PAD_OFFSETS, B.MOK_ITEM_DA, B.MOK_ITEM_WH, B.MOK_ITEM_SLOTS],
+    B.MOK_WS_SHARED: [B.MOK_ITEM_H_RING],
+    B.MOK_WS_SHARED_BACKWARD: [B.MOK_ITEM_DA, B.MOK_ITEM_WH],
+}
+MX_ITEMS = {
+    B.MOK_WS_FORWARD: [B.MOK_ITEM_X_RING_SCALE, B.MOK_ITEM_H_RING_SCALE],
+    B.MOK_WS_BACKWARD: [B.MOK_ITEM_DA_Q, B.MOK_ITEM_DA_SCALE, B.MOK_ITEM_DY_Q,
+                        B.MOK_ITEM_DY_SCALE],
+    B.MOK_WS_SHARED: [B.MOK_ITEM_X_RING, B.MOK_ITEM_X_RING_SCALE, B.MOK_ITEM_H_RING_SCALE],
+    B.MOK_WS_SHARED_BACKWARD: [B.MOK_ITEM_DA_Q, B.MOK_ITEM_DA_SCALE, B.MOK_ITEM_DY_Q,
+                               B.MOK_ITEM_DY_SCALE],
+}
+
+
+@pytest.mark.parametrize("prec", [B.MOK_BF16, B.MOK_MXFP8])
+@pytest.mark.parametrize("ring", [0, 100])
+def test_workspace_items_lie_inside_their_workspace_and_apart(lib, prec, ring):
+    c = cfg(prec=prec, ring_capacity=ring)
+    R, H, I, T = c.T * c.K, c.H, c.I, c.T
+    for which, items in ITEMS.items():
+        items = items + (MX_ITEMS[which] if prec == B.MOK_MXFP8 else [])
+        size = B.mok_workspace_size(c, which)
+        spans = []
+        for it in items:
+            st, off, n = B.mok_workspace_item(c, which, it)
+            assert st == B.MOK_OK, (which, it)
+            assert off % 256 == 0 and n > 0 and off + n <= size, (which, it, off, n, size)
+            spans.append((off, off + n))
+        spans.sort()
+        for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+            assert a1 <= b0  # no two items overlap
+    # sizes follow the documented shapes
+    # a BF16 ring holds floor(capacity / minibatch) minibatch slots; MXFP8 the capacity
+    rows = R if ring == 0 else (100 if prec == B.MOK_MXFP8 else 64)
+    esz = 1 if prec == B.MOK_MXFP8 else 2
+    assert B.mok_workspace_item(c, B.MOK_WS_FORWARD, B.MOK_ITEM_X_RING)[2] == rows * H * esz
+    assert B.mok_workspace_item(c, B.MOK_WS_FORWARD, B.MOK_ITEM_SLOTS)[2] == R * H * 2
+    assert B.mok_workspace_item(c, B.MOK_WS_BACKWARD, B.MOK_ITEM_PAD_OFFSETS)[2] == 4 * (c.E + 1)
+    rpad = R + 15 * c.E
+    assert B.mok_workspace_item(c, B.MOK_WS_BACKWARD, B.MOK_ITEM_DA)[2] == rpad * 2 * I * 2
+    # an item a workspace does not hold, an unknown item, an invalid configuration
+    if prec == B.MOK_BF16:
+        assert B.mok_workspace_item(c, B.MOK_WS_FORWARD, B.MOK_ITEM_X_RING_SCALE)[0] == \
+            B.MOK_ERR_INVALID_ARG
+    assert B.mok_workspace_item(c, B.MOK_WS_FORWARD, B.MOK_ITEM_DA)[0] == B.MOK_ERR_INVALID_ARG
+    assert B.mok_workspace_item(c, B.MOK_WS_FORWARD, 99)[0] == B.MOK_ERR_INVALID_ARG
+    assert B.mok_workspace_item(c, 99, B.MOK_ITEM_SLOTS)[0] == B.MOK_ERR_INVALID_ARG
+    assert B.mok_workspace_item(cfg(K=9), B.MOK_WS_FORWARD, B.MOK_ITEM_SLOTS)[0] == \
+        B.MOK_ERR_INVALID_ARG

@@ -1,13 +1,15 @@
 """GPU parity of the MXFP8 layer backward against the oracle's MXFP8 backward mode: the G
 GEMM on dy and W2 quantized along H, the dgrad GEMM on dA and W13 quantized along 2I, the
-weight gradients on bf16 operands. Bit-exact pre-quantized (transposed) weights; dx, dW13,
-dW2 and the router gradients within the MXFP8 tolerance; run to run; full size on
-samples."""
+weight gradients on bf16 operands. Bit-exact pre-quantized (transposed) weights; step by
+step (tests/bwd_checks.py: the saved A, dA and its MXFP8 codes and scales, w*h, dx, dW13,
+dW2, d_topk_w, d_logits) and end to end within the MXFP8 tolerance; run to run; full size
+on 128 sampled tokens and 4 experts."""
 import numpy as np
 import pytest
 
 import oracle
-from harness import TOL_MXFP8, inputs, rel_err, sample_tokens, to_dev
+from bwd_checks import check_expert, check_tokens, gpu_state
+from harness import inputs, same_bits, sample_tokens, to_dev
 from mixture_experts_layer_deterministic_gb300 import binding as B
 from mixture_experts_layer_deterministic_gb300.buffers import (MoELayer, backward_mxfp8,
                                                                  quantize_mxfp8,
@@ -36,44 +38,30 @@ def gpu_backward_mx(dims, x, logits, w13, w2, dy, MB, reps=1):
     q13, s13 = quantize_mxfp8(w13d)
     q2, s2 = quantize_mxfp8(w2d)
     w13t, w2t = quantize_mxfp8_transposed(w13d), quantize_mxfp8_transposed(w2d)
+    del w13d, w2d
     L.route(to_dev(logits))
     L.schedule()
     R = T * K
+    st = dict(dtype=L.dtype, device="cuda")
     f32 = dict(dtype=torch.float32, device="cuda")
-    pre = torch.empty(max(R, 1), 2 * I, **f32)
-    y = torch.empty(max(T, 1), H, **f32)
+    pre = torch.empty(max(R, 1), 2 * I, **st)
+    y = torch.empty(max(T, 1), H, **st)
     L.forward(xd, q13, q2, y, s13, s2, pre)
     outs = []
     for _ in range(reps):
-        dx = torch.empty(max(T, 1), H, **f32)
-        dw13 = torch.empty(E, 2 * I, H, **f32)
-        dw2 = torch.empty(E, H, I, **f32)
+        dx = torch.empty(max(T, 1), H, **st)
+        dw13 = torch.empty(E, 2 * I, H, **st)
+        dw2 = torch.empty(E, H, I, **st)
         dtk = torch.empty(max(R, 1), **f32)
         dlg = torch.empty(max(T, 1), E, **f32)
         backward_mxfp8(L, xd, pre, w13t, w2t, dyd, dx, dw13, dw2, dtk, dlg)
         outs.append(dict(dx=dx[:T], dw13=dw13, dw2=dw2, dtk=dtk[:R].view(T, K), dlg=dlg[:T]))
     torch.cuda.synchronize()
-    st, dev = B.mok_read_device_status()
-    assert st == B.MOK_OK and dev == B.MOK_OK
-    idx = L.idx[:R].view(T, K).cpu().numpy()
-    w = L.w[:R].view(T, K).cpu().numpy().astype(np.float64)
-    return outs, idx, w
-
-
-def host(t):
-    return t.cpu().numpy()
-
-
-def check_all(g, idx, w, x, w13, w2, dy, E):
-    dx_o, dw13_o, dw2_o, dtk_o, sdx, sdw13, sdw2 = oracle.backward(
-        oracle.bf16_to_f64(x), idx, w, w13, w2, oracle.bf16_to_f64(dy), mode=oracle.MXFP8,
-        with_slack=True)
-    dl_o = oracle.router_grad(idx, w, dtk_o, E)
-    for name, got, want, sl in (("dx", g["dx"], dx_o, sdx), ("dw13", g["dw13"], dw13_o, sdw13),
-                                ("dw2", g["dw2"], dw2_o, sdw2), ("d_topk_w", g["dtk"], dtk_o, None),
-                                ("d_logits", g["dlg"], dl_o, None)):
-        err = rel_err(host(got).reshape(want.shape), want, sl)
-        assert err <= TOL_MXFP8, (name, err, rel_err(host(got).reshape(want.shape), want))
+    s, dev = B.mok_read_device_status()
+    assert s == B.MOK_OK and dev == B.MOK_OK
+    g = dict(idx=L.idx[:R].view(T, K).cpu().numpy(),
+             w=L.w[:R].view(T, K).cpu().numpy().astype(np.float64), T=T, K=K, E=E)
+    return outs, g, L, pre
 
 
 def small_case(T, H, I, E, K, seed, scale=0.05, skew=0.0):
@@ -86,62 +74,55 @@ def small_case(T, H, I, E, K, seed, scale=0.05, skew=0.0):
     return x, lg, w13, w2, dy
 
 
+def check_all(outs, g, L, pre, x, w13, w2, dy, tokens=None, experts=None, mxw=None, tag=""):
+    st = gpu_state(L, L.ws_b, B.MOK_WS_BACKWARD, pre)
+    gg = dict(g, **outs[0])
+    tokens = np.arange(L.T) if tokens is None else tokens
+    check_tokens(gg, st, x, w13, w2, dy, True, tokens, mxw=mxw, tag=" mx" + tag)
+    for e in (range(L.E) if experts is None else experts):
+        check_expert(gg, st, x, w13, w2, dy, True, int(e), mxw=mxw, tag=" mx" + tag)
+
+
 def test_tiny_config():
     cfg = CONFIGS["tiny"]
     d = inputs(cfg)
     r = np.random.default_rng(78)
     dy = f32_to_bf16_bits(r.standard_normal((cfg.T, cfg.H)).astype(np.float32))
     dims = (cfg.T, cfg.H, cfg.I, cfg.E, cfg.K)
-    outs, idx, w = gpu_backward_mx(dims, d["x"], d["logits"], d["w13"], d["w2"], dy,
-                                   cfg.minibatch, reps=2)
-    check_all(outs[0], idx, w, d["x"], d["w13"], d["w2"], dy, cfg.E)
-    import torch
+    outs, g, L, pre = gpu_backward_mx(dims, d["x"], d["logits"], d["w13"], d["w2"], dy,
+                                      cfg.minibatch, reps=2)
+    check_all(outs, g, L, pre, d["x"], d["w13"], d["w2"], dy)
     for k in outs[0]:  # bitwise run to run
-        assert torch.equal(outs[0][k].view(torch.int32), outs[1][k].view(torch.int32)), k
+        assert same_bits(outs[0][k], outs[1][k]), k
 
 
 @pytest.mark.parametrize("dims,skew", [((600, 256, 256, 16, 4), 0.0),
                                        ((333, 384, 128, 24, 3), 3.0)])
 def test_ragged_and_empty_experts(dims, skew):
     x, lg, w13, w2, dy = small_case(*dims, seed=dims[0] + 1, skew=skew)
-    outs, idx, w = gpu_backward_mx(dims, x, lg, w13, w2, dy, 100)
+    outs, g, L, pre = gpu_backward_mx(dims, x, lg, w13, w2, dy, 100)
     if skew:
-        assert len(np.unique(idx)) < dims[3]  # some experts get no rows
-    check_all(outs[0], idx, w, x, w13, w2, dy, dims[3])
+        assert len(np.unique(g["idx"])) < dims[3]  # some experts get no rows
+    check_all(outs, g, L, pre, x, w13, w2, dy)
 
 
 def test_full_size_sampled():
+    """128 sampled tokens and 4 sampled experts, the hottest among them; the oracle's
+    three MXFP8 quantizations of the weights are computed once, by the oracle."""
     cfg = CONFIGS["bwd_bf16"]
     d = inputs(cfg)
     dims = (cfg.T, cfg.H, cfg.I, cfg.E, cfg.K)
-    outs, idx, w = gpu_backward_mx(dims, d["x"], d["logits"], d["w13"], d["w2"], d["dy"],
-                                   cfg.minibatch)
-    g = outs[0]
-    # few tokens: the oracle's MXFP8 mode holds the used experts' weights in float64
-    toks = sample_tokens(cfg.T, 6, seed=cfg.seed + 7)
-    idx_s = idx[toks]
-    used = np.unique(idx_s)
-    remap = np.full(cfg.E, -1, np.int32)
-    remap[used] = np.arange(len(used), dtype=np.int32)
-    dx_o, _, _, dtk_o, sdx, _, _ = oracle.backward(
-        oracle.bf16_to_f64(d["x"][toks]), remap[idx_s], w[toks], d["w13"][used],
-        d["w2"][used], oracle.bf16_to_f64(d["dy"][toks]), weight_grads=False,
-        mode=oracle.MXFP8, with_slack=True)
-    assert rel_err(host(g["dx"])[toks], dx_o, sdx) <= TOL_MXFP8
-    assert rel_err(host(g["dtk"])[toks], dtk_o) <= TOL_MXFP8
-    # weight gradients of a sampled expert: its own rows only
+    outs, g, L, pre = gpu_backward_mx(dims, d["x"], d["logits"], d["w13"], d["w2"], d["dy"],
+                                      cfg.minibatch)
+    mxw = (oracle.mxfp8_quantize_bf16(d["w13"]), oracle.quantize_transposed_bf16(d["w13"]),
+           oracle.quantize_transposed_bf16(d["w2"]))
+    toks = sample_tokens(cfg.T, 128, seed=cfg.seed + 7)
+    counts = np.bincount(g["idx"].reshape(-1), minlength=cfg.E)
     r = np.random.default_rng(9)
-    counts = np.bincount(idx.reshape(-1), minlength=cfg.E)
-    for e in r.choice(np.nonzero(counts)[0], size=1, replace=False):
-        rows = np.argwhere(idx == e)
-        t_e = rows[:, 0]
-        idx_e = np.zeros((len(t_e), 1), np.int32)
-        w_e = w[rows[:, 0], rows[:, 1]][:, None]
-        _, dw13_o, dw2_o, _, _, s13, s2 = oracle.backward(
-            oracle.bf16_to_f64(d["x"][t_e]), idx_e, w_e, d["w13"][[e]], d["w2"][[e]],
-            oracle.bf16_to_f64(d["dy"][t_e]), mode=oracle.MXFP8, with_slack=True)
-        assert rel_err(host(g["dw13"][e]), dw13_o[0], s13[0]) <= TOL_MXFP8
-        assert rel_err(host(g["dw2"][e]), dw2_o[0], s2[0]) <= TOL_MXFP8
+    experts = list(r.choice(np.flatnonzero(counts > 0), 3, replace=False)) + \
+        [int(np.argmax(counts))]
+    check_all(outs, g, L, pre, d["x"], d["w13"], d["w2"], d["dy"], tokens=toks,
+              experts=experts, mxw=mxw, tag=" full")
 
 
 def test_argument_errors_are_reported():

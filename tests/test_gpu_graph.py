@@ -4,7 +4,7 @@ results bit for bit (single-pass and multi-pass rings)."""
 import numpy as np
 import pytest
 
-from harness import to_dev
+from harness import same_bits, to_dev
 from mixture_experts_layer_deterministic_gb300 import binding as B
 from mixture_experts_layer_deterministic_gb300.buffers import MoELayer, SharedExpert
 from workloads.synth import f32_to_bf16_bits
@@ -29,9 +29,10 @@ def test_captured_step_replays_eager_results(dims, MB, ring):
     S = SharedExpert(L)
     R = T * K
     f32 = dict(dtype=torch.float32, device="cuda")
-    pre = torch.empty(R, 2 * I, **f32)
-    y, dx = torch.empty(T, H, **f32), torch.empty(T, H, **f32)
-    dw13, dw2 = torch.empty(E, 2 * I, H, **f32), torch.empty(E, H, I, **f32)
+    st = dict(dtype=L.dtype, device="cuda")
+    pre = torch.empty(R, 2 * I, **st)
+    y, dx = torch.empty(T, H, **st), torch.empty(T, H, **st)
+    dw13, dw2 = torch.empty(E, 2 * I, H, **st), torch.empty(E, H, I, **st)
     dtk, dlg = torch.empty(R, **f32), torch.empty(T, E, **f32)
     s = torch.cuda.Stream()
 
@@ -60,7 +61,7 @@ def test_captured_step_replays_eager_results(dims, MB, ring):
     st, dev = B.mok_read_device_status()
     assert st == B.MOK_OK and dev == B.MOK_OK
     for a, b in zip(outs, eager):
-        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+        assert same_bits(a, b)
 
 
 def test_captured_mxfp8_multi_pass_forward_replays_eager_results():
@@ -77,9 +78,9 @@ def test_captured_mxfp8_multi_pass_forward_replays_eager_results():
     q2, s2 = quantize_mxfp8(to_dev(f32_to_bf16_bits(
         (r.standard_normal((E, H, I)) * 0.05).astype(np.float32))))
     L = MoELayer(T, H, I, E, K, MB, ring, B.MOK_MXFP8)
-    f32 = dict(dtype=torch.float32, device="cuda")
-    pre = torch.empty(T * K, 2 * I, **f32)
-    y = torch.empty(T, H, **f32)
+    st = dict(dtype=L.dtype, device="cuda")
+    pre = torch.empty(T * K, 2 * I, **st)
+    y = torch.empty(T, H, **st)
     s = torch.cuda.Stream()
 
     def fwd():
@@ -93,7 +94,7 @@ def test_captured_mxfp8_multi_pass_forward_replays_eager_results():
     eager = [y.clone(), pre.clone()]
     # the single-pass forward of the same layer gives the same y, bit for bit
     L1 = MoELayer(T, H, I, E, K, MB, 0, B.MOK_MXFP8)
-    y1 = torch.empty(T, H, **f32)
+    y1 = torch.empty(T, H, **st)
     with torch.cuda.stream(s):
         L1.route(lg, s)
         L1.schedule(stream=s)
@@ -108,11 +109,11 @@ def test_captured_mxfp8_multi_pass_forward_replays_eager_results():
         g.replay()
         g.replay()
     torch.cuda.synchronize()
-    st, dev = B.mok_read_device_status()
-    assert st == B.MOK_OK and dev == B.MOK_OK
-    assert torch.equal(y.view(torch.int32), eager[0].view(torch.int32))
-    assert torch.equal(pre.view(torch.int32), eager[1].view(torch.int32))
-    assert torch.equal(y1.view(torch.int32), eager[0].view(torch.int32))
+    s_, dev = B.mok_read_device_status()
+    assert s_ == B.MOK_OK and dev == B.MOK_OK
+    assert same_bits(y, eager[0])
+    assert same_bits(pre, eager[1])
+    assert same_bits(y1, eager[0])
 
 
 _FIRST_CALL_CAPTURED = r"""
@@ -131,7 +132,7 @@ lg = to_dev(r.standard_normal((T, E)).astype(np.float32))
 w13 = to_dev(f32_to_bf16_bits((r.standard_normal((E, 2 * I, H)) * 0.05).astype(np.float32)))
 w2 = to_dev(f32_to_bf16_bits((r.standard_normal((E, H, I)) * 0.05).astype(np.float32)))
 L = MoELayer(T, H, I, E, K, MB, ring, B.MOK_BF16)
-y = torch.empty(T, H, dtype=torch.float32, device="cuda")
+y = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
 s = torch.cuda.Stream()
 g = torch.cuda.CUDAGraph()
 with torch.cuda.graph(g, stream=s):  # the first multi-pass forward of the process
@@ -150,7 +151,7 @@ with torch.cuda.stream(s):  # eager: creates the second stream and overlaps the 
 torch.cuda.synchronize()
 st, dev = B.mok_read_device_status()
 assert st == B.MOK_OK and dev == B.MOK_OK, (st, dev)
-assert torch.equal(captured.view(torch.int32), y.view(torch.int32))
+assert torch.equal(captured.view(torch.int16), y.view(torch.int16))
 print("OK")
 """
 

@@ -114,5 +114,5 @@ def test_host_validation_rejects_bad_arguments():
     assert B.mok_route_topk(L.cfg, None, L.idx, L.w) == B.MOK_ERR_INVALID_ARG
     assert B.mok_build_schedule(L.cfg, L.idx, L.sched.struct, L.ws_s, 16) == B.MOK_ERR_WORKSPACE
     assert B.mok_build_schedule(L.cfg, L.idx, L.sched.struct, None, 0) == B.MOK_ERR_WORKSPACE
-    bad = B.make_config(64, 256, 128, 8, 2, 16, 0, B.MOK_BF16, abi_version=2)
+    bad = B.make_config(64, 256, 128, 8, 2, 16, 0, B.MOK_BF16, abi_version=B.MOK_ABI_VERSION + 1)
     assert B.mok_route_topk(bad, lg, L.idx, L.w) == B.MOK_ERR_ABI

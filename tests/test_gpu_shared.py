@@ -1,15 +1,23 @@
-"""GPU parity of the shared-expert forward against the oracle: every token also passes
-through one SwiGLU expert with weight one, added to the routed output. The oracle of the
-shared expert is its own layer forward with one expert and top-1 routing at weight one
-(the E=1, K=1 case, pinned on the CPU as a plain SwiGLU FFN)."""
+"""GPU parity of the shared expert against the oracle: every token also passes through one
+SwiGLU expert with weight one, whose output is added to the routed output (and, in the
+backward, whose input gradient is added to the routed dx). The oracle of the shared expert
+is its own layer with one expert and top-1 routing at weight one (the E=1, K=1 case, pinned
+on the CPU as a plain SwiGLU FFN), adding to a given output (oracle_rows y_in / dx_in).
+
+Step by step: the shared expert's h (or its MXFP8 codes), its saved pre-activations, y =
+bf16(y_routed + o) from the GPU's own routed y and h; in the backward its dA, w*h (and MXFP8
+dA codes) from the GPU's own A, dx = bf16(dx_routed + W13s^T dA) and its weight gradients
+from the GPU's own dA and w*h. End to end within the stated tolerance."""
 import numpy as np
 import pytest
 
 import oracle
-from harness import TOL_BF16, TOL_MXFP8, inputs, rel_err, sample_tokens, to_dev
+from harness import (TOL_BF16, TOL_MXFP8, check_codes, check_exact, check_tol, host, inputs,
+                     oracle_forward_tokens, same_bits, sample_tokens, to_dev)
 from mixture_experts_layer_deterministic_gb300 import binding as B
 from mixture_experts_layer_deterministic_gb300.buffers import (MoELayer, SharedExpert,
-                                                                 quantize_mxfp8)
+                                                                 quantize_mxfp8,
+                                                                 workspace_item)
 from workloads import CONFIGS
 from workloads.synth import f32_to_bf16_bits
 
@@ -23,102 +31,130 @@ def shared_weights(H, I, seed, scale):
     return w13s, w2s
 
 
-def gpu_routed_plus_shared(dims, x, logits, w13, w2, w13s, w2s, MB=2368, reps=1):
+def _step(v):
+    return np.ldexp(1.0, np.frexp(np.maximum(np.abs(v), 1e-300))[1] - 8)
+
+
+def gpu_routed_plus_shared(dims, x, logits, w13, w2, w13s, w2s, prec, MB=2368, reps=1):
     import torch
     T, H, I, E, K = dims
-    L = MoELayer(T, H, I, E, K, MB, 0, B.MOK_BF16)
+    L = MoELayer(T, H, I, E, K, MB, 0, prec)
     S = SharedExpert(L)
-    xd, w13d, w2d, w13sd, w2sd = to_dev(x), to_dev(w13), to_dev(w2), to_dev(w13s), to_dev(w2s)
+    xd = to_dev(x)
+    if prec == B.MOK_MXFP8:
+        q13, s13 = quantize_mxfp8(to_dev(w13))
+        q2, s2 = quantize_mxfp8(to_dev(w2))
+        ws13, ws2 = quantize_mxfp8(to_dev(w13s)), quantize_mxfp8(to_dev(w2s))
+    else:
+        q13, s13, q2, s2 = to_dev(w13), None, to_dev(w2), None
+        ws13, ws2 = to_dev(w13s), to_dev(w2s)
     L.route(to_dev(logits))
     L.schedule()
-    pre_s = torch.empty(max(T, 1), 2 * I, dtype=torch.float32, device="cuda")
+    pre_s = torch.empty(max(T, 1), 2 * I, dtype=L.dtype, device="cuda")
     outs = []
     for _ in range(reps):
-        y = torch.empty(max(T, 1), H, dtype=torch.float32, device="cuda")
-        L.forward(xd, w13d, w2d, y)
+        y = torch.empty(max(T, 1), H, dtype=L.dtype, device="cuda")
+        L.forward(xd, q13, q2, y, s13, s2)
         y_routed = y[:T].clone()
-        S.forward(xd, w13sd, w2sd, y, saved_preact=pre_s)
-        outs.append((y_routed.cpu().numpy(), y[:T].cpu().numpy()))
+        S.forward(xd, ws13, ws2, y, saved_preact=pre_s)
+        outs.append((y_routed, y[:T]))
     torch.cuda.synchronize()
     st, dev = B.mok_read_device_status()
     assert st == B.MOK_OK and dev == B.MOK_OK
     R = T * K
-    idx = L.idx[:R].view(T, K).cpu().numpy()
-    w = L.w[:R].view(T, K).cpu().numpy().astype(np.float64)
-    return outs, idx, w, pre_s[:T].cpu().numpy()
-
-
-def oracle_shared(x_bits, w13s, w2s):
-    T = x_bits.shape[0]
-    return oracle.forward(oracle.bf16_to_f64(x_bits), np.zeros((T, 1), np.int32),
-                          np.ones((T, 1)), w13s[None], w2s[None], mode=oracle.BF16,
-                          with_slack=True)
-
-
-def check(outs, idx, w, pre_s, x, w13, w2, w13s, w2s, toks=None):
-    y_routed, y_total = outs[0]
-    if toks is not None:
-        idx_s = idx[toks]
-        used = np.unique(idx_s)
-        remap = np.full(w13.shape[0], -1, np.int32)
-        remap[used] = np.arange(len(used), dtype=np.int32)
-        yr, sr = oracle.forward(oracle.bf16_to_f64(x[toks]), remap[idx_s], w[toks], w13[used],
-                                w2[used], mode=oracle.BF16, with_slack=True)
-        ys, ss = oracle_shared(x[toks], w13s, w2s)
-        y_routed, y_total, pre_s, xs = y_routed[toks], y_total[toks], pre_s[toks], x[toks]
+    g = dict(idx=L.idx[:R].view(T, K).cpu().numpy(),
+             w=L.w[:R].view(T, K).cpu().numpy().astype(np.float64),
+             y_routed=host(outs[0][0]), y=host(outs[0][1]), pre_s=host(pre_s[:T]), outs=outs)
+    if prec == B.MOK_MXFP8:
+        g["h_q"] = workspace_item(S.ws, L.cfg, B.MOK_WS_SHARED, B.MOK_ITEM_H_RING).view(
+            -1, I)[:T].cpu().numpy()
+        g["h_s"] = workspace_item(S.ws, L.cfg, B.MOK_WS_SHARED, B.MOK_ITEM_H_RING_SCALE).view(
+            -1, I // 32)[:T].cpu().numpy()
+        g["h"] = oracle.mxfp8_dequantize(g["h_q"], g["h_s"])
     else:
-        yr, sr = oracle.forward(oracle.bf16_to_f64(x), idx, w, w13, w2, mode=oracle.BF16,
-                                with_slack=True)
-        ys, ss = oracle_shared(x, w13s, w2s)
-        xs = x
-    # the routed part is untouched and the total is the routed plus the shared output
-    assert rel_err(y_routed, yr, sr) <= TOL_BF16
-    assert rel_err(y_total, yr + ys, sr + ss) <= TOL_BF16
-    # the shared output alone, as the GPU's fp32 difference
-    assert rel_err(y_total - y_routed, ys, ss) <= TOL_BF16
-    # saved pre-activations: fp32 dot products of the bf16 operands, whose products are
-    # exact in fp32; n-term fp32 summation stays within n * 2^-24 * sum|terms| of the exact
-    # sum (the recursive-summation bound), elementwise
-    xf, wf = oracle.bf16_to_f64(xs), oracle.bf16_to_f64(w13s)
-    a = xf @ wf.T
-    bound = xf.shape[1] * 2.0 ** -24 * (np.abs(xf) @ np.abs(wf).T)
-    assert np.all(np.abs(pre_s - a) <= bound)
+        g["h"] = host(workspace_item(S.ws, L.cfg, B.MOK_WS_SHARED, B.MOK_ITEM_H_RING)
+                      .view(torch.bfloat16).view(-1, I)[:T])
+    return g
 
 
-def test_tiny_config():
+def check_forward(g, x, w13, w2, w13s, w2s, mx, toks=None, tag=""):
+    T = x.shape[0]
+    toks = np.arange(T) if toks is None else toks
+    mode, tol = (oracle.MXFP8, TOL_MXFP8) if mx else (oracle.BF16, TOL_BF16)
+    q = oracle.mxfp8_quantize_bf16
+    w13o, w2o = (q(w13), q(w2)) if mx else (w13, w2)
+    w13so, w2so = (q(w13s[None]), q(w2s[None])) if mx else (w13s[None], w2s[None])
+    n = len(toks)
+    xf = oracle.bf16_to_f64(x[toks])
+    one = dict(idx=np.zeros((n, 1), np.int32), w=np.ones((n, 1)))
+    # routed part, end to end
+    yr, sr = oracle_forward_tokens(toks, x, g["idx"], g["w"], w13o, w2o, mode)
+    check_tol("shared: routed y e2e" + tag, g["y_routed"][toks], yr, sr, tol,
+              max_slack_rms=1.2 if mx else 0.4)
+    # the shared expert's h against its own chain from x
+    _, _, ro = oracle.forward(xf, one["idx"], one["w"], w13so, w2so, mode=mode, with_slack=True,
+                              store=oracle.STORE_BF16, rows=("h", "h_slack", "h_q", "h_scale"))
+    if mx:
+        check_codes("shared h codes" + tag, g["h_q"][toks], g["h_s"][toks], ro["h_q"],
+                    ro["h_scale"], ro["h_slack"])
+    else:
+        check_exact("shared h" + tag, g["h"][toks], ro["h"], ro["h_slack"])
+    # y = bf16(y_routed + o) from the GPU's own routed y and h
+    y_s, sl_s = oracle.forward(xf, one["idx"], one["w"], w13so, w2so, mode=mode, with_slack=True,
+                               store=oracle.STORE_BF16,
+                               given={"h_in": g["h"][toks], "y_in": g["y_routed"][toks]})
+    check_exact("shared y | gpu routed y, h" + tag, g["y"][toks], y_s, sl_s)
+    # end to end: the oracle's routed y with the shared output added (its slack widened by
+    # the routed slack and one step of the final rounding)
+    y_e, sl_e = oracle.forward(xf, one["idx"], one["w"], w13so, w2so, mode=mode,
+                               with_slack=True, store=oracle.STORE_BF16, given={"y_in": yr})
+    check_tol("shared y e2e" + tag, g["y"][toks], y_e, sl_e + sr + _step(y_e), tol,
+              max_slack_rms=0.3)
+    # the saved pre-activations: bf16 of the exact gate/up product
+    *_, ra = oracle.backward(xf, one["idx"], one["w"], w13s[None] if mx else w13s[None],
+                             w2s[None], np.zeros((n, x.shape[1])), weight_grads=False,
+                             mode=mode, store=oracle.STORE_BF16, rows=("a", "a_slack"))
+    check_exact("shared saved A" + tag, g["pre_s"][toks], ra["a"], ra["a_slack"])
+
+
+@pytest.mark.parametrize("prec", [B.MOK_BF16, B.MOK_MXFP8])
+def test_tiny_config(prec):
     cfg = CONFIGS["tiny"]
     d = inputs(cfg)
     w13s, w2s = shared_weights(cfg.H, cfg.I, 5, 0.05)
     dims = (cfg.T, cfg.H, cfg.I, cfg.E, cfg.K)
-    outs, idx, w, pre_s = gpu_routed_plus_shared(dims, d["x"], d["logits"], d["w13"], d["w2"],
-                                                 w13s, w2s, cfg.minibatch, reps=2)
-    check(outs, idx, w, pre_s, d["x"], d["w13"], d["w2"], w13s, w2s)
-    np.testing.assert_array_equal(outs[0][1], outs[1][1])  # bitwise run to run
+    g = gpu_routed_plus_shared(dims, d["x"], d["logits"], d["w13"], d["w2"], w13s, w2s, prec,
+                               cfg.minibatch, reps=2)
+    check_forward(g, d["x"], d["w13"], d["w2"], w13s, w2s, prec == B.MOK_MXFP8)
+    assert same_bits(g["outs"][0][1], g["outs"][1][1])  # bitwise run to run
 
 
+@pytest.mark.parametrize("prec", [B.MOK_BF16, B.MOK_MXFP8])
 @pytest.mark.parametrize("dims", [(300, 256, 128, 8, 2), (1, 128, 128, 4, 1),
                                   (517, 384, 256, 16, 4)])
-def test_ragged_token_counts(dims):
+def test_ragged_token_counts(dims, prec):
     T, H, I, E, K = dims
-    r = np.random.default_rng(T)
+    r = np.random.default_rng(T + prec)
     x = f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
     lg = r.standard_normal((T, E)).astype(np.float32)
     w13 = f32_to_bf16_bits((r.standard_normal((E, 2 * I, H)) * 0.05).astype(np.float32))
     w2 = f32_to_bf16_bits((r.standard_normal((E, H, I)) * 0.05).astype(np.float32))
     w13s, w2s = shared_weights(H, I, T + 1, 0.05)
-    outs, idx, w, pre_s = gpu_routed_plus_shared(dims, x, lg, w13, w2, w13s, w2s, 100)
-    check(outs, idx, w, pre_s, x, w13, w2, w13s, w2s)
+    g = gpu_routed_plus_shared(dims, x, lg, w13, w2, w13s, w2s, prec, 100)
+    check_forward(g, x, w13, w2, w13s, w2s, prec == B.MOK_MXFP8)
 
 
-def test_full_size_sampled_tokens():
-    cfg = CONFIGS["fwd_bf16"]
+@pytest.mark.parametrize("name", ["fwd_bf16", "fwd_mxfp8"])
+def test_full_size_sampled_tokens(name):
+    cfg = CONFIGS[name]
     d = inputs(cfg)
     w13s, w2s = shared_weights(cfg.H, cfg.I, 9, cfg.w_std)
     dims = (cfg.T, cfg.H, cfg.I, cfg.E, cfg.K)
-    outs, idx, w, pre_s = gpu_routed_plus_shared(dims, d["x"], d["logits"], d["w13"], d["w2"],
-                                                 w13s, w2s, cfg.minibatch)
-    check(outs, idx, w, pre_s, d["x"], d["w13"], d["w2"], w13s, w2s,
-          toks=sample_tokens(cfg.T, 128, seed=3))
+    prec = B.MOK_MXFP8 if cfg.prec == "mxfp8" else B.MOK_BF16
+    g = gpu_routed_plus_shared(dims, d["x"], d["logits"], d["w13"], d["w2"], w13s, w2s, prec,
+                               cfg.minibatch)
+    check_forward(g, d["x"], d["w13"], d["w2"], w13s, w2s, prec == B.MOK_MXFP8,
+                  toks=sample_tokens(cfg.T, 128, seed=3), tag=" full")
 
 
 def test_mxfp8_config_needs_the_mxfp8_entry():
@@ -129,7 +165,7 @@ def test_mxfp8_config_needs_the_mxfp8_entry():
     x = torch.zeros(64, 128, dtype=torch.bfloat16, device="cuda")
     w13s = torch.zeros(256, 128, dtype=torch.bfloat16, device="cuda")
     w2s = torch.zeros(128, 128, dtype=torch.bfloat16, device="cuda")
-    y = torch.zeros(64, 128, dtype=torch.float32, device="cuda")
+    y = torch.zeros(64, 128, dtype=torch.bfloat16, device="cuda")
     st = B.mok_shared_expert_forward(L.cfg, x, w13s, w2s, y, None, ws, ws.numel())
     assert st == B.MOK_ERR_UNSUPPORTED
     # and the MXFP8 entry point takes MXFP8 configurations only
@@ -144,242 +180,138 @@ def test_mxfp8_config_needs_the_mxfp8_entry():
     assert st == B.MOK_OK and dev == B.MOK_OK
 
 
-def gpu_routed_plus_shared_mx(dims, x, logits, w13, w2, w13s, w2s, MB=2368, reps=1):
-    """MXFP8 layer: routed forward, then the shared expert added on pre-quantized weights."""
+# ---------------------------------------------------------------- backward
+
+def gpu_step_with_shared(dims, x, logits, w13, w2, w13s, w2s, dy, prec, MB=2368, reps=1):
+    """Routed and shared forward (both saving pre-activations), then the routed backward and
+    the shared backward, which adds into dx; dx after the routed part, dx in total and the
+    shared weight gradients, with the shared backward's workspace intermediates."""
     import torch
+    from mixture_experts_layer_deterministic_gb300.buffers import (backward_mxfp8,
+                                                                     quantize_mxfp8_transposed)
     T, H, I, E, K = dims
-    L = MoELayer(T, H, I, E, K, MB, 0, B.MOK_MXFP8)
-    S = SharedExpert(L)
-    xd = to_dev(x)
-    q13, s13 = quantize_mxfp8(to_dev(w13))
-    q2, s2 = quantize_mxfp8(to_dev(w2))
-    ws13, ws2 = quantize_mxfp8(to_dev(w13s)), quantize_mxfp8(to_dev(w2s))
-    L.route(to_dev(logits))
-    L.schedule()
-    pre_s = torch.empty(max(T, 1), 2 * I, dtype=torch.float32, device="cuda")
-    outs = []
-    for _ in range(reps):
-        y = torch.empty(max(T, 1), H, dtype=torch.float32, device="cuda")
-        L.forward(xd, q13, q2, y, s13, s2)
-        y_routed = y[:T].clone()
-        S.forward(xd, ws13, ws2, y, saved_preact=pre_s)
-        outs.append((y_routed.cpu().numpy(), y[:T].cpu().numpy()))
-    torch.cuda.synchronize()
-    st, dev = B.mok_read_device_status()
-    assert st == B.MOK_OK and dev == B.MOK_OK
-    R = T * K
-    idx = L.idx[:R].view(T, K).cpu().numpy()
-    w = L.w[:R].view(T, K).cpu().numpy().astype(np.float64)
-    return outs, idx, w, pre_s[:T].cpu().numpy()
-
-
-def check_mx(outs, idx, w, pre_s, x, w13, w2, w13s, w2s, toks=None):
-    """The oracle's MXFP8 mode: the routed layer, and the shared expert as its own layer with
-    one expert and top-1 routing at weight one."""
-    y_routed, y_total = outs[0]
-    xs, idx_s, w_s, w13u, w2u = x, idx, w, w13, w2
-    if toks is not None:
-        used = np.unique(idx[toks])
-        remap = np.full(w13.shape[0], -1, np.int32)
-        remap[used] = np.arange(len(used), dtype=np.int32)
-        xs, idx_s, w_s, w13u, w2u = x[toks], remap[idx[toks]], w[toks], w13[used], w2[used]
-        y_routed, y_total, pre_s = y_routed[toks], y_total[toks], pre_s[toks]
-    xf = oracle.bf16_to_f64(xs)
-    q = lambda a: oracle.mxfp8_quantize_bf16(a)
-    yr, sr = oracle.forward(xf, idx_s, w_s, q(w13u), q(w2u), mode=oracle.MXFP8, with_slack=True)
-    T = xs.shape[0]
-    ys, ss = oracle.forward(xf, np.zeros((T, 1), np.int32), np.ones((T, 1)),
-                            q(w13s[None]), q(w2s[None]), mode=oracle.MXFP8, with_slack=True)
-    assert rel_err(y_routed, yr, sr) <= TOL_MXFP8
-    assert rel_err(y_total - y_routed, ys, ss) <= TOL_MXFP8
-    assert rel_err(y_total, yr + ys, sr + ss) <= TOL_MXFP8
-    # saved pre-activations: dot products of the dequantized x and W13s blocks (each product
-    # exact in fp32), accumulated by the tensor core; allow 2^-12 of the sum of |terms|
-    xq = oracle.mxfp8_dequantize(*oracle.mxfp8_quantize_bf16(xs))
-    wq = oracle.mxfp8_dequantize(*oracle.mxfp8_quantize_bf16(w13s))
-    a = xq @ wq.T
-    assert np.all(np.abs(pre_s - a) <= 2.0 ** -12 * (np.abs(xq) @ np.abs(wq).T) + 1e-30)
-
-
-def test_mxfp8_tiny_config():
-    cfg = CONFIGS["tiny"]
-    d = inputs(cfg)
-    w13s, w2s = shared_weights(cfg.H, cfg.I, 15, 0.05)
-    dims = (cfg.T, cfg.H, cfg.I, cfg.E, cfg.K)
-    outs, idx, w, pre_s = gpu_routed_plus_shared_mx(dims, d["x"], d["logits"], d["w13"],
-                                                    d["w2"], w13s, w2s, cfg.minibatch, reps=2)
-    check_mx(outs, idx, w, pre_s, d["x"], d["w13"], d["w2"], w13s, w2s)
-    np.testing.assert_array_equal(outs[0][1], outs[1][1])  # bitwise run to run
-
-
-@pytest.mark.parametrize("dims", [(300, 256, 128, 8, 2), (1, 128, 128, 4, 1),
-                                  (517, 384, 256, 16, 4)])
-def test_mxfp8_ragged_token_counts(dims):
-    T, H, I, E, K = dims
-    r = np.random.default_rng(T + 11)
-    x = f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
-    lg = r.standard_normal((T, E)).astype(np.float32)
-    w13 = f32_to_bf16_bits((r.standard_normal((E, 2 * I, H)) * 0.05).astype(np.float32))
-    w2 = f32_to_bf16_bits((r.standard_normal((E, H, I)) * 0.05).astype(np.float32))
-    w13s, w2s = shared_weights(H, I, T + 12, 0.05)
-    outs, idx, w, pre_s = gpu_routed_plus_shared_mx(dims, x, lg, w13, w2, w13s, w2s, 100)
-    check_mx(outs, idx, w, pre_s, x, w13, w2, w13s, w2s)
-
-
-def test_mxfp8_full_size_sampled_tokens():
-    cfg = CONFIGS["fwd_mxfp8"]
-    d = inputs(cfg)
-    w13s, w2s = shared_weights(cfg.H, cfg.I, 19, cfg.w_std)
-    dims = (cfg.T, cfg.H, cfg.I, cfg.E, cfg.K)
-    outs, idx, w, pre_s = gpu_routed_plus_shared_mx(dims, d["x"], d["logits"], d["w13"],
-                                                    d["w2"], w13s, w2s, cfg.minibatch)
-    check_mx(outs, idx, w, pre_s, d["x"], d["w13"], d["w2"], w13s, w2s,
-             toks=sample_tokens(cfg.T, 24, seed=5))
-
-
-def gpu_step_with_shared(dims, x, logits, w13, w2, w13s, w2s, dy, MB=2368):
-    """Routed forward + shared forward, then routed backward + shared backward (which adds
-    into dx); returns dx after the routed part, dx in total, the shared weight gradients."""
-    import torch
-    T, H, I, E, K = dims
-    L = MoELayer(T, H, I, E, K, MB, 0, B.MOK_BF16, backward=True)
+    L = MoELayer(T, H, I, E, K, MB, 0, prec, backward=True)
     S = SharedExpert(L)
     xd, dyd = to_dev(x), to_dev(dy)
     w13d, w2d, w13sd, w2sd = to_dev(w13), to_dev(w2), to_dev(w13s), to_dev(w2s)
+    mx = prec == B.MOK_MXFP8
+    if mx:
+        q13, s13 = quantize_mxfp8(w13d)
+        q2, s2 = quantize_mxfp8(w2d)
+        w13t, w2t = quantize_mxfp8_transposed(w13d), quantize_mxfp8_transposed(w2d)
+        ws13, ws2 = quantize_mxfp8(w13sd), quantize_mxfp8(w2sd)
+        wst13 = quantize_mxfp8_transposed(w13sd[None])
+        wst2 = quantize_mxfp8_transposed(w2sd[None])
     L.route(to_dev(logits))
     L.schedule()
     R = T * K
+    st = dict(dtype=L.dtype, device="cuda")
     f32 = dict(dtype=torch.float32, device="cuda")
-    pre, pre_s = torch.empty(R, 2 * I, **f32), torch.empty(T, 2 * I, **f32)
-    y = torch.empty(T, H, **f32)
-    L.forward(xd, w13d, w2d, y, saved_preact=pre)
-    S.forward(xd, w13sd, w2sd, y, saved_preact=pre_s)
-    dx = torch.empty(T, H, **f32)
-    dw13, dw2 = torch.empty(E, 2 * I, H, **f32), torch.empty(E, H, I, **f32)
-    dtk = torch.empty(R, **f32)
-    L.backward(xd, pre, w13d, w2d, dyd, dx, dw13, dw2, dtk)
-    dx_routed = dx.clone()
-    dw13s, dw2s = torch.empty(2 * I, H, **f32), torch.empty(H, I, **f32)
-    S.backward(xd, w13sd, w2sd, pre_s, dyd, dx, dw13s, dw2s)
+    pre, pre_s = torch.empty(max(R, 1), 2 * I, **st), torch.empty(max(T, 1), 2 * I, **st)
+    y = torch.empty(max(T, 1), H, **st)
+    if mx:
+        L.forward(xd, q13, q2, y, s13, s2, pre)
+        S.forward(xd, ws13, ws2, y, saved_preact=pre_s)
+    else:
+        L.forward(xd, w13d, w2d, y, saved_preact=pre)
+        S.forward(xd, w13sd, w2sd, y, saved_preact=pre_s)
+    outs = []
+    for _ in range(reps):
+        dx = torch.empty(max(T, 1), H, **st)
+        dw13, dw2 = torch.empty(E, 2 * I, H, **st), torch.empty(E, H, I, **st)
+        dtk = torch.empty(max(R, 1), **f32)
+        if mx:
+            backward_mxfp8(L, xd, pre, w13t, w2t, dyd, dx, dw13, dw2, dtk)
+        else:
+            L.backward(xd, pre, w13d, w2d, dyd, dx, dw13, dw2, dtk)
+        dx_routed = dx[:T].clone()
+        dw13s, dw2s = torch.empty(2 * I, H, **st), torch.empty(H, I, **st)
+        if mx:
+            S.backward(xd, wst13, wst2, pre_s, dyd, dx, dw13s, dw2s)
+        else:
+            S.backward(xd, w13sd, w2sd, pre_s, dyd, dx, dw13s, dw2s)
+        outs.append(dict(dx_r=dx_routed, dx=dx[:T], dw13s=dw13s, dw2s=dw2s))
     torch.cuda.synchronize()
-    st, dev = B.mok_read_device_status()
-    assert st == B.MOK_OK and dev == B.MOK_OK
+    s, dev = B.mok_read_device_status()
+    assert s == B.MOK_OK and dev == B.MOK_OK
+    item = lambda it: workspace_item(S.ws_b, L.cfg, B.MOK_WS_SHARED_BACKWARD, it)  # noqa
+    gi = dict(a=host(pre_s[:T]),
+              da=host(item(B.MOK_ITEM_DA).view(torch.bfloat16).view(-1, 2 * I)[:T]),
+              sh=host(item(B.MOK_ITEM_WH).view(torch.bfloat16).view(-1, I)[:T]))
+    if mx:
+        gi["da_q"] = item(B.MOK_ITEM_DA_Q).view(-1, 2 * I)[:T].cpu().numpy()
+        gi["da_s"] = item(B.MOK_ITEM_DA_SCALE).view(-1, 2 * I // 32)[:T].cpu().numpy()
+        gi["daq"] = oracle.mxfp8_dequantize(gi["da_q"], gi["da_s"])
     idx = L.idx[:R].view(T, K).cpu().numpy()
     w = L.w[:R].view(T, K).cpu().numpy().astype(np.float64)
-    return (dx_routed.cpu().numpy(), dx.cpu().numpy(), dw13s.cpu().numpy(),
-            dw2s.cpu().numpy(), idx, w)
+    return outs, gi, idx, w
 
 
+def check_backward(outs, gi, idx, w, x, w13, w2, w13s, w2s, dy, mx):
+    T, H = x.shape
+    mode, tol = (oracle.MXFP8, TOL_MXFP8) if mx else (oracle.BF16, TOL_BF16)
+    g = {k: host(v) for k, v in outs[0].items()}
+    xf, dyf = oracle.bf16_to_f64(x), oracle.bf16_to_f64(dy)
+    one_idx, one_w = np.zeros((T, 1), np.int32), np.ones((T, 1))
+    dx_ro, _, _, _, sdx_r, _, _ = oracle.backward(xf, idx, w, w13, w2, dyf, weight_grads=False,
+                                                  mode=mode, store=oracle.STORE_BF16,
+                                                  with_slack=True)
+    check_tol("shared: routed dx e2e", g["dx_r"], dx_ro, sdx_r, tol,
+              max_slack_rms=1.2 if mx else 0.4)
+    run = lambda **kw: oracle.backward(xf, one_idx, one_w, w13s[None], w2s[None], dyf,  # noqa
+                                       mode=mode, store=oracle.STORE_BF16, **kw)
+    # dA, w*h (and MXFP8 dA codes) from the GPU's own A
+    names = ("da", "da_slack", "sh", "sh_slack") + (("da_q", "da_scale", "daq_slack")
+                                                    if mx else ())
+    *_, ra = run(weight_grads=False, given={"a_in": gi["a"]}, rows=names)
+    check_exact("shared bwd dA | gpu A", gi["da"], ra["da"], ra["da_slack"])
+    check_exact("shared bwd w*h | gpu A", gi["sh"], ra["sh"], ra["sh_slack"])
+    if mx:
+        check_codes("shared bwd dA codes | gpu A", gi["da_q"], gi["da_s"], ra["da_q"],
+                    ra["da_scale"], ra["daq_slack"])
+    # dx = bf16(dx_routed + W13s^T dA) and the weight gradients from the GPU's operands
+    given = {"a_in": gi["a"], "da_in": gi["da"], "sh_in": gi["sh"], "dx_in": g["dx_r"]}
+    if mx:
+        given["daq_in"] = gi["daq"]
+    dx_s, d13, d2, _, sdx_s, s13, s2 = run(with_slack=True, given=given)
+    check_exact("shared dx | gpu routed dx, dA", g["dx"], dx_s, sdx_s)
+    check_exact("shared dW13 | gpu dA", g["dw13s"], d13[0], s13[0])
+    check_exact("shared dW2 | gpu w*h", g["dw2s"], d2[0], s2[0])
+    # end to end
+    _, d13o, d2o, _, _, s13o, s2o = run(with_slack=True)
+    check_tol("shared dW13 e2e", g["dw13s"], d13o[0], s13o[0], tol, max_slack_rms=0.6)
+    check_tol("shared dW2 e2e", g["dw2s"], d2o[0], s2o[0], tol, max_slack_rms=0.6)
+
+
+@pytest.mark.parametrize("prec", [B.MOK_BF16, B.MOK_MXFP8])
 @pytest.mark.parametrize("dims", [(256, 256, 128, 8, 2), (300, 256, 128, 8, 2),
-                                  (517, 384, 256, 16, 4)])
-def test_backward_with_shared_expert(dims):
+                                  (517, 384, 256, 16, 4), (1, 128, 128, 4, 1)])
+def test_backward_with_shared_expert(dims, prec):
     T, H, I, E, K = dims
-    r = np.random.default_rng(T + 2)
+    r = np.random.default_rng(T + 2 + 19 * prec)
     x = f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
     lg = r.standard_normal((T, E)).astype(np.float32)
     w13 = f32_to_bf16_bits((r.standard_normal((E, 2 * I, H)) * 0.05).astype(np.float32))
     w2 = f32_to_bf16_bits((r.standard_normal((E, H, I)) * 0.05).astype(np.float32))
     dy = f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
     w13s, w2s = shared_weights(H, I, T + 3, 0.05)
-    dx_r, dx, dw13s, dw2s, idx, w = gpu_step_with_shared(dims, x, lg, w13, w2, w13s, w2s, dy)
-    xf, dyf = oracle.bf16_to_f64(x), oracle.bf16_to_f64(dy)
-    dx_ro, _, _, _, sdx_r, _, _ = oracle.backward(xf, idx, w, w13, w2, dyf, weight_grads=False,
-                                                  mode=oracle.BF16, with_slack=True)
-    # the shared expert: one expert, top-1 routing at weight one
-    dx_so, dw13_so, dw2_so, _, sdx_s, s13, s2 = oracle.backward(
-        xf, np.zeros((T, 1), np.int32), np.ones((T, 1)), w13s[None], w2s[None], dyf,
-        mode=oracle.BF16, with_slack=True)
-    assert rel_err(dx_r, dx_ro, sdx_r) <= TOL_BF16
-    assert rel_err(dx, dx_ro + dx_so, sdx_r + sdx_s) <= TOL_BF16
-    assert rel_err(dx - dx_r, dx_so, sdx_s) <= TOL_BF16
-    assert rel_err(dw13s, dw13_so[0], s13[0]) <= TOL_BF16
-    assert rel_err(dw2s, dw2_so[0], s2[0]) <= TOL_BF16
-
-
-def gpu_step_with_shared_mx(dims, x, logits, w13, w2, w13s, w2s, dy, MB=2368, reps=1):
-    """MXFP8 layer: routed and shared forward (both saving pre-activations), then the routed
-    MXFP8 backward and the shared MXFP8 backward, which adds into dx."""
-    import torch
-    from mixture_experts_layer_deterministic_gb300.buffers import (backward_mxfp8,
-                                                                     quantize_mxfp8_transposed)
-    T, H, I, E, K = dims
-    L = MoELayer(T, H, I, E, K, MB, 0, B.MOK_MXFP8, backward=True)
-    S = SharedExpert(L)
-    xd, dyd = to_dev(x), to_dev(dy)
-    w13d, w2d, w13sd, w2sd = to_dev(w13), to_dev(w2), to_dev(w13s), to_dev(w2s)
-    q13, s13 = quantize_mxfp8(w13d)
-    q2, s2 = quantize_mxfp8(w2d)
-    w13t, w2t = quantize_mxfp8_transposed(w13d), quantize_mxfp8_transposed(w2d)
-    ws13, ws2 = quantize_mxfp8(w13sd), quantize_mxfp8(w2sd)
-    wst13 = quantize_mxfp8_transposed(w13sd[None])
-    wst2 = quantize_mxfp8_transposed(w2sd[None])
-    L.route(to_dev(logits))
-    L.schedule()
-    R = T * K
-    f32 = dict(dtype=torch.float32, device="cuda")
-    pre, pre_s = torch.empty(max(R, 1), 2 * I, **f32), torch.empty(max(T, 1), 2 * I, **f32)
-    y = torch.empty(max(T, 1), H, **f32)
-    L.forward(xd, q13, q2, y, s13, s2, pre)
-    S.forward(xd, ws13, ws2, y, saved_preact=pre_s)
-    outs = []
-    for _ in range(reps):
-        dx = torch.empty(max(T, 1), H, **f32)
-        dw13, dw2 = torch.empty(E, 2 * I, H, **f32), torch.empty(E, H, I, **f32)
-        dtk = torch.empty(max(R, 1), **f32)
-        backward_mxfp8(L, xd, pre, w13t, w2t, dyd, dx, dw13, dw2, dtk)
-        dx_routed = dx[:T].clone()
-        dw13s, dw2s = torch.empty(2 * I, H, **f32), torch.empty(H, I, **f32)
-        S.backward(xd, wst13, wst2, pre_s, dyd, dx, dw13s, dw2s)
-        outs.append(dict(dx_r=dx_routed.cpu().numpy(), dx=dx[:T].cpu().numpy(),
-                         dw13s=dw13s.cpu().numpy(), dw2s=dw2s.cpu().numpy()))
-    torch.cuda.synchronize()
-    st, dev = B.mok_read_device_status()
-    assert st == B.MOK_OK and dev == B.MOK_OK
-    idx = L.idx[:R].view(T, K).cpu().numpy()
-    w = L.w[:R].view(T, K).cpu().numpy().astype(np.float64)
-    return outs, idx, w
-
-
-@pytest.mark.parametrize("dims", [(256, 256, 128, 8, 2), (300, 256, 128, 8, 2),
-                                  (517, 384, 256, 16, 4), (1, 128, 128, 4, 1)])
-def test_mxfp8_backward_with_shared_expert(dims):
-    T, H, I, E, K = dims
-    r = np.random.default_rng(T + 21)
-    x = f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
-    lg = r.standard_normal((T, E)).astype(np.float32)
-    w13 = f32_to_bf16_bits((r.standard_normal((E, 2 * I, H)) * 0.05).astype(np.float32))
-    w2 = f32_to_bf16_bits((r.standard_normal((E, H, I)) * 0.05).astype(np.float32))
-    dy = f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
-    w13s, w2s = shared_weights(H, I, T + 23, 0.05)
-    outs, idx, w = gpu_step_with_shared_mx(dims, x, lg, w13, w2, w13s, w2s, dy, reps=2)
-    g = outs[0]
-    xf, dyf = oracle.bf16_to_f64(x), oracle.bf16_to_f64(dy)
-    dx_ro, _, _, _, sdx_r, _, _ = oracle.backward(xf, idx, w, w13, w2, dyf, weight_grads=False,
-                                                  mode=oracle.MXFP8, with_slack=True)
-    # the shared expert in the oracle's MXFP8 mode: one expert, top-1 routing at weight one
-    dx_so, dw13_so, dw2_so, _, sdx_s, s13, s2 = oracle.backward(
-        xf, np.zeros((T, 1), np.int32), np.ones((T, 1)), w13s[None], w2s[None], dyf,
-        mode=oracle.MXFP8, with_slack=True)
-    assert rel_err(g["dx_r"], dx_ro, sdx_r) <= TOL_MXFP8
-    assert rel_err(g["dx"] - g["dx_r"], dx_so, sdx_s) <= TOL_MXFP8
-    assert rel_err(g["dx"], dx_ro + dx_so, sdx_r + sdx_s) <= TOL_MXFP8
-    assert rel_err(g["dw13s"], dw13_so[0], s13[0]) <= TOL_MXFP8
-    assert rel_err(g["dw2s"], dw2_so[0], s2[0]) <= TOL_MXFP8
-    for k in g:  # bitwise run to run
-        np.testing.assert_array_equal(g[k], outs[1][k])
+    outs, gi, idx, w = gpu_step_with_shared(dims, x, lg, w13, w2, w13s, w2s, dy, prec, reps=2)
+    check_backward(outs, gi, idx, w, x, w13, w2, w13s, w2s, dy, prec == B.MOK_MXFP8)
+    for k in outs[0]:  # bitwise run to run
+        assert same_bits(outs[0][k], outs[1][k]), k
 
 
 def test_mxfp8_shared_backward_argument_errors():
     import torch
     T, H, I = 64, 128, 128
     u8 = dict(dtype=torch.uint8, device="cuda")
-    f32 = dict(dtype=torch.float32, device="cuda")
-    x = torch.zeros(T, H, dtype=torch.bfloat16, device="cuda")
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros(T, H, **bf)
     wt13 = (torch.zeros(H, 2 * I, **u8), torch.zeros(H, 2 * I // 32, **u8))
     wt2 = (torch.zeros(I, H, **u8), torch.zeros(I, H // 32, **u8))
-    pre = torch.zeros(T, 2 * I, **f32)
-    dx = torch.zeros(T, H, **f32)
-    dw13s, dw2s = torch.zeros(2 * I, H, **f32), torch.zeros(H, I, **f32)
+    pre = torch.zeros(T, 2 * I, **bf)
+    dx = torch.zeros(T, H, **bf)
+    dw13s, dw2s = torch.zeros(2 * I, H, **bf), torch.zeros(H, I, **bf)
     for prec, saved, want in ((B.MOK_MXFP8, None, B.MOK_ERR_INVALID_ARG),  # pre required
                               (B.MOK_BF16, pre, B.MOK_ERR_INVALID_ARG)):   # not MXFP8
         L = MoELayer(T, H, I, 4, 2, 64, 0, prec)

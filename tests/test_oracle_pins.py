@@ -845,3 +845,72 @@ def test_mxfp8_dgrad_reads_da_quantized_along_2i():
             ref_plain[t] += w13i[e].T @ da
     np.testing.assert_allclose(dx, ref, rtol=1e-11, atol=1e-13)
     assert np.abs(ref - ref_plain).max() > 1e-3 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("mode", [oracle.BF16, oracle.MXFP8])
+def test_added_expert_slack_covers_every_kernel_draw(mode):
+    """An expert whose output is added to an existing bf16 output (a shared expert, K=1,
+    weight one): y = bf16(y_in + o) and dx = bf16(dx_in + W13^T dA) with no slot between;
+    given the kernel's h (forward) or A, dA and w*h (backward), every draw lies within the
+    slack, equal to the oracle where nothing is flagged."""
+    T, H, I = 24, 64, 64
+    x, _, _, w13, w2, dy = _bf16_case(T, H, I, 1, 1, seed=95 + mode)
+    idx, w = np.zeros((T, 1), np.int32), np.ones((T, 1))
+    r = np.random.default_rng(7)
+    y_in = emulate.bf16(r.standard_normal((T, H)) * 0.5)
+    wq = (emulate.mx_qdq_rows(w13), emulate.mx_qdq_rows(w2)) if mode == oracle.MXFP8 \
+        else (w13, w2)
+    moved = 0
+    for _ in range(6):
+        _, gh = emulate.forward(r, x, idx, w, wq[0], wq[1], mode)
+        y, sl = oracle.forward(x, idx, w, wq[0], wq[1], mode=mode, with_slack=True,
+                               store=oracle.STORE_BF16, given={"h_in": gh, "y_in": y_in})
+        gy, _ = emulate.forward(r, x, idx, w, wq[0], wq[1], mode, h_in=gh, y_in=y_in)
+        moved += _covers(gy, y, sl, "y added")
+        assert np.all(sl <= 2 * _step(y) + 2 * _step(y - y_in))
+    bits = lambda a: f32_to_bf16_bits(a.astype(np.float32))  # noqa: E731
+    w13b, w2b = (bits(w13), bits(w2)) if mode == oracle.MXFP8 else (w13, w2)
+    dx_in = emulate.bf16(r.standard_normal((T, H)) * 0.5)
+    for _ in range(4):
+        _, _, _, gr = emulate.backward(r, x, idx, w, w13, w2, dy, mode)
+        given = {"a_in": gr["a"], "da_in": gr["da"], "sh_in": gr["sh"], "dx_in": dx_in}
+        if mode == oracle.MXFP8:
+            given["daq_in"] = gr["daq"]
+        dx, _, _, _, sdx, _, _ = oracle.backward(x, idx, w, w13b, w2b, dy, mode=mode,
+                                                 with_slack=True, store=oracle.STORE_BF16,
+                                                 given=given)
+        gx, _, _, _ = emulate.backward(r, x, idx, w, w13, w2, dy, mode, given=given,
+                                       dx_in=dx_in)
+        moved += _covers(gx, dx, sdx, "dx added")
+    assert moved > 0
+
+
+def test_router_gradient_slack_covers_the_saved_a_decisions():
+    """dS = <G, h> moves with the stored A's rounding decisions (h is recomputed from A):
+    with G exact, dS from each draw's A lies within dtopk_slack, and the logit gradients
+    from it within router_grad_slack."""
+    T, H, I, E, K = 16, 64, 64, 3, 2
+    x, idx, w, w13, w2, dy = _bf16_case(T, H, I, E, K, seed=97)
+    *_, dtk, sdx, _, _, ro = oracle.backward(x, idx, w, w13, w2, dy, mode=oracle.BF16,
+                                             store=oracle.STORE_BF16, with_slack=True,
+                                             rows=("dtopk_slack",))
+    sdtk = ro["dtopk_slack"].reshape(T, K)
+    sdl = oracle.router_grad_slack(idx, w, sdtk, E)
+    dl = oracle.router_grad(idx, w, dtk, E)
+    assert sdtk.max() > 0
+    r = np.random.default_rng(5)
+    moved = 0
+    for _ in range(8):
+        _, _, _, gr = emulate.backward(r, x, idx, w, w13, w2, dy, oracle.BF16)
+        a = gr["a"].reshape(T, K, 2 * I)
+        ds = np.empty((T, K))
+        for t in range(T):
+            for k in range(K):
+                g = w2[idx[t, k]].T @ dy[t]
+                ds[t, k] = g @ (_silu(a[t, k, :I]) * a[t, k, I:])
+        d = np.abs(ds - dtk)
+        assert np.all(d <= sdtk * (1 + 1e-9) + 1e-12 * np.abs(dtk)), float((d - sdtk).max())
+        dld = np.abs(oracle.router_grad(idx, w, ds, E) - dl)
+        assert np.all(dld <= sdl * (1 + 1e-9) + 1e-12 * np.abs(dl).max())
+        moved += int((d > 1e-12 * np.abs(dtk)).sum())
+    assert moved > 0

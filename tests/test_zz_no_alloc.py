@@ -6,8 +6,12 @@ or they run a time-critical loop that cannot pay cudaMalloc's latency and implic
 synchronisation. For them the library offers a schedule builder whose scratch lives in a
 fixed array inside the library. These tests call it through the C ABI and check that it
 produces exactly what the workspace-based mok_build_schedule produces, on two calls in a
-row (the second call inherits the first call's leftovers in the shared array), and that
-it refuses sizes its array cannot hold. This file is collected last on purpose.
+row (the second call inherits the first call's leftovers in the shared array), that a call
+takes no device memory, and that it refuses sizes its array cannot hold.
+
+The file is named to be collected last, so that a run stopping at its first failure has
+run every other test before this one; it passes alone in a fresh process and after the
+rest of the suite alike.
 """
 import numpy as np
 import pytest
@@ -50,6 +54,29 @@ def test_noalloc_schedule_equals_workspace_schedule_on_two_calls():
     want, got = both_ways(1000, 64, 6, 300, seed=2, skew=2.0)
     for k in want:
         np.testing.assert_array_equal(got[k], want[k], err_msg=k)
+
+
+def test_noalloc_schedule_takes_no_device_memory():
+    """After a warm-up call (which looks up the array's address on this device), another
+    call changes neither the device's free memory nor torch's allocator statistics."""
+    import torch
+    T, E, K = 4096, 256, 8
+    L = MoELayer(T, 256, 128, E, K, 2368, 0, B.MOK_BF16)
+    lg = np.random.default_rng(4).standard_normal((T, E)).astype(np.float32)
+    L.route(torch.from_numpy(lg).cuda())
+    other = Schedule(L.cfg, L.device)
+    B.check(B.mok_build_schedule_noalloc(L.cfg, L.idx, other.struct), "warm-up")
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    stats0 = torch.cuda.memory_stats()
+    B.check(B.mok_build_schedule_noalloc(L.cfg, L.idx, other.struct), "second call")
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    stats1 = torch.cuda.memory_stats()
+    assert free1 == free0, (free0, free1)
+    for k in ("allocation.all.allocated", "reserved_bytes.all.current",
+              "allocated_bytes.all.current"):
+        assert stats1.get(k) == stats0.get(k), k
 
 
 def test_noalloc_schedule_rejects_sizes_beyond_its_array():

@@ -247,8 +247,10 @@ mok_status mok_build_schedule_noalloc(const mok_config *cfg, const int32_t *topk
  *           end; o[t,k] is the down GEMM's fp32 result stored in the (t, k) slot as bf16
  *           (fp32 under the flag).
  *   saved_preact  NULL, or [R][2I] bf16 out (fp32 under the flag): the gate/up GEMM result
- *           of sorted row r (needed by mok_backward, or by mok_backward_mxfp8 after an
- *           MXFP8 forward, with the same flags).
+ *           a = W13[e] x of sorted row r (needed by mok_backward, or by mok_backward_mxfp8
+ *           after an MXFP8 forward, with the same flags). Each row holds I pairs, one per
+ *           feature i: the gate value a[i] at 2i and the up value a[I+i] at 2i+1, so that
+ *           the backward reads both halves of a feature with one access.
  * GEMMs accumulate in fp32; values that are only stored (expert outputs, saved
  * pre-activations, y) take the storage type of cfg->flags.
  * A ring smaller than R rows (cfg->ring_capacity) makes the forward run in passes of
@@ -325,7 +327,8 @@ mok_status mok_backward_mxfp8(const mok_config *cfg, const void *x, const mok_sc
  *                  down-GEMM result added to it in fp32 and rounded once (fp32 storage
  *                  under MOK_FLAG_FP32_STORAGE).
  *   saved_preact_s NULL, or [T][2I] out (bf16, or fp32 under the flag): the shared
- *                  expert's gate/up GEMM result.
+ *                  expert's gate/up GEMM result, in the (gate, up) pair layout of
+ *                  mok_forward's saved_preact.
  *   ws             at least mok_workspace_size(cfg, MOK_WS_SHARED) bytes.
  * BF16 (cfg->prec == MOK_BF16, else MOK_ERR_UNSUPPORTED; MXFP8 configurations use
  * mok_shared_expert_forward_mxfp8). Asynchronous on `stream`. */

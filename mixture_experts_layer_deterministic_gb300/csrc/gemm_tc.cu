@@ -130,6 +130,10 @@ struct Geom {
 
 MOK_DEV float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
+// Saved pre-activations of a row: [I] pairs (gate, up) of one feature each, so that the lane
+// holding feature i stores and loads both halves with one access (a bf16 pair is one 32-bit
+// word, an fp32 pair one 64-bit word) and a warp's 32 consecutive features are one run.
+
 // element i of a stored-value array held as fp32 (f32) or bf16
 MOK_DEV void st_val(void *p, int64_t i, float v, bool f32) {
     if (f32)
@@ -232,8 +236,10 @@ struct FwdUpT {
                 const int64_t r = r0 + n;
                 h[j] = silu_f(d0[j]) * d1[j];
                 if (n < nr && preact != nullptr) {
-                    st_val(preact, r * 2 * I + i, d0[j], preact_f32);
-                    st_val(preact, r * 2 * I + I + i, d1[j], preact_f32);
+                    if (preact_f32)
+                        static_cast<float2 *>(preact)[r * I + i] = make_float2(d0[j], d1[j]);
+                    else
+                        static_cast<uint32_t *>(preact)[r * I + i] = pack_bf16x2(d0[j], d1[j]);
                 }
                 if (hring != nullptr && !mxfp8 && n < nr)
                     ((uint16_t *)hring)[rm(r) * I + i] = f32_to_bf16(h[j]);
@@ -433,31 +439,27 @@ struct BwdGT {
             float d[2][16];
             ld(n0, d[0], d[1]);
             // issue every pre-activation load of the chunk before using any
-            // the pre-activations as raw bits: fp32 words, or bf16 values zero-extended by
-            // their 16-bit loads and moved into place only where they are used, so that all
-            // the loads are in flight before the first one is waited for
-            uint32_t rg[2][16], ru[2][16];
+            // the pre-activation pairs (gate, up) of the lane's features, every load of the
+            // chunk issued before the first is used: a 32-bit word of two bf16, or two fp32
+            float2 pg[2][16];
+            uint32_t pw[2][16];
             uint32_t my_sb = 0;  // MXFP8: the block scale this lane stores for its 4-row group
+            const int64_t row0 = (r0 + n0) * (int64_t)I;
 #pragma unroll
             for (int a = 0; a < 2; ++a)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int i = i0 + a * 128;
-                    const int64_t r = r0 + n0 + j;
                     const bool ok = (n0 + j < nr) && i < I;
-                    if (PF32) {
-                        const uint32_t *pf = static_cast<const uint32_t *>(preact);
-                        rg[a][j] = ok ? pf[r * 2 * I + i] : 0u;
-                        ru[a][j] = ok ? pf[r * 2 * I + I + i] : 0u;
-                    } else {
-                        const unsigned short *ph = static_cast<const unsigned short *>(preact);
-                        rg[a][j] = ok ? (uint32_t)ph[r * 2 * I + i] : 0u;
-                        ru[a][j] = ok ? (uint32_t)ph[r * 2 * I + I + i] : 0u;
-                    }
+                    const int64_t o = row0 + (int64_t)j * I + i;
+                    if (PF32)
+                        pg[a][j] = ok ? static_cast<const float2 *>(preact)[o]
+                                      : make_float2(0.f, 0.f);
+                    else
+                        pw[a][j] = ok ? static_cast<const uint32_t *>(preact)[o] : 0u;
                 }
-            auto pre_val = [](uint32_t raw) {
-                return __uint_as_float(PF32 ? raw : raw << 16);
-            };
+            auto gate_of = [&](int a, int j) { return PF32 ? pg[a][j].x : bf16_lo(pw[a][j]); };
+            auto up_of = [&](int a, int j) { return PF32 ? pg[a][j].y : bf16_hi(pw[a][j]); };
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int n = n0 + j;
@@ -470,7 +472,7 @@ struct BwdGT {
                     if (n < nr) {
                         const float s = es.col[n];
                         const float g = d[a][j];
-                        const float agv = pre_val(rg[a][j]), auv = pre_val(ru[a][j]);
+                        const float agv = gate_of(a, j), auv = up_of(a, j);
                         const float sig = 1.0f / (1.0f + expf(-agv));
                         const float sl = agv * sig;
                         const float h = sl * auv;

@@ -111,7 +111,8 @@ struct Ring {
 // Forward gate/up GEMM with the SwiGLU epilogue, per tile (e, r0, r1):
 //   a[r][j] = sum_c W13[e][j][c] * xring[ring(r)][c]   (j < 2I)
 //   h[ring(r)][i] = silu(a[r][i]) * a[r][I+i]          (bf16, or MXFP8 along I)
-//   preact[r][j] = a[r][j] (fp32 if preact_f32, else bf16) when preact != nullptr
+//   preact[r] = a[r] (fp32 if preact_f32, else bf16) when preact != nullptr, in the saved
+//   layout of (gate, up) pairs: preact[r][2i] = a[r][i], preact[r][2i+1] = a[r][I+i]
 struct GemmUpArgs {
     const int32_t *tiles;
     int64_t tiles_cap;

@@ -13,7 +13,7 @@ import numpy as np
 
 import oracle
 from harness import (TOL_BF16, TOL_MXFP8, check_codes, check_exact, check_tol, host,
-                     padded_rows, remap_experts, sorted_rows)
+                     padded_rows, preact_rows, remap_experts, sorted_rows)
 from mixture_experts_layer_deterministic_gb300 import binding as B
 from mixture_experts_layer_deterministic_gb300.buffers import workspace_item
 
@@ -44,7 +44,8 @@ def _rows_of(st, sorted_r):
     pr = padded_rows(sorted_r, st["offsets"], st["poff"])
     rt = torch.from_numpy(np.asarray(sorted_r, np.int64)).cuda()
     pt = torch.from_numpy(np.asarray(pr, np.int64)).cuda()
-    out = dict(a=host(st["pre"][rt]), da=host(st["dA"][pt]), sh=host(st["sh"][pt]))
+    out = dict(a=preact_rows(host(st["pre"][rt])), da=host(st["dA"][pt]),
+               sh=host(st["sh"][pt]))
     if "dA_q" in st:
         out["da_q"] = st["dA_q"][pt].cpu().numpy()
         out["da_s"] = st["dA_s"][pt].cpu().numpy()

@@ -60,6 +60,15 @@ def host(t):
     return t.cpu().numpy().astype(np.float64)
 
 
+def preact_rows(a):
+    """Saved pre-activations [n, 2I] in the layer's layout ((gate, up) pairs per feature)
+    -> the plain [n, 2I] order (gate features 0..I-1, then up)."""
+    a = np.asarray(a)
+    n, i2 = a.shape
+    pr = a.reshape(n, i2 // 2, 2)
+    return np.concatenate([pr[:, :, 0], pr[:, :, 1]], axis=1)
+
+
 def same_bits(a, b):
     T = torch()
     u8 = lambda t: t.contiguous().view(T.uint8) if t.dtype != T.uint8 else t  # noqa: E731

@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 from harness import (TOL_BF16, TOL_MXFP8, check_codes, check_exact, check_tol, host, inputs,
-                     oracle_forward_tokens, remap_experts, same_bits, sample_tokens,
+                     oracle_forward_tokens, preact_rows, same_bits, sample_tokens,
                      sorted_rows, to_dev)
 from mixture_experts_layer_deterministic_gb300 import binding as B
 from mixture_experts_layer_deterministic_gb300.buffers import (MoELayer, quantize_mxfp8,
@@ -151,7 +151,7 @@ def test_fp32_storage(prec):
                                         store=oracle.STORE_F32, rows=("a", "a_mag"))
     check_tol("fwd y e2e fp32 storage", g["y"][0], y_o, sl, TOL_MXFP8 if mx else TOL_BF16)
     perm = g["L"].sched.perm[:T * K].cpu().numpy()
-    pre = host(g["pre"][:T * K])[np.argsort(perm)]   # sorted rows -> flat id order
+    pre = preact_rows(host(g["pre"][:T * K]))[np.argsort(perm)]  # flat id order
     ratio = np.abs(pre - ro["a"]) / np.maximum(ro["a_mag"], 1e-300)
     assert ratio.max() <= oracle.DOT_REL, ratio.max()
 
@@ -195,7 +195,7 @@ def test_saved_preact_is_bf16_of_the_gate_up_product():
     x, lg, w13, w2 = small_case(*dims, seed=5)
     g = gpu_forward(dims, x, lg, w13, w2, B.MOK_BF16, 32, 0, preact=True)
     perm = g["L"].sched.perm[:T * K].cpu().numpy()
-    pre = host(g["pre"][:T * K])[np.argsort(perm)]   # flat id order
+    pre = preact_rows(host(g["pre"][:T * K]))[np.argsort(perm)]  # flat id order
     *_, ro = oracle.backward(oracle.bf16_to_f64(x), g["idx"], g["w"], w13, w2,
                              np.zeros((T, H)), mode=oracle.BF16, store=oracle.STORE_BF16,
                              weight_grads=False, rows=("a", "a_slack"))

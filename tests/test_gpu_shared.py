@@ -13,7 +13,7 @@ import pytest
 
 import oracle
 from harness import (TOL_BF16, TOL_MXFP8, check_codes, check_exact, check_tol, host, inputs,
-                     oracle_forward_tokens, same_bits, sample_tokens, to_dev)
+                     oracle_forward_tokens, preact_rows, same_bits, sample_tokens, to_dev)
 from mixture_experts_layer_deterministic_gb300 import binding as B
 from mixture_experts_layer_deterministic_gb300.buffers import (MoELayer, SharedExpert,
                                                                  quantize_mxfp8,
@@ -64,7 +64,8 @@ def gpu_routed_plus_shared(dims, x, logits, w13, w2, w13s, w2s, prec, MB=2368, r
     R = T * K
     g = dict(idx=L.idx[:R].view(T, K).cpu().numpy(),
              w=L.w[:R].view(T, K).cpu().numpy().astype(np.float64),
-             y_routed=host(outs[0][0]), y=host(outs[0][1]), pre_s=host(pre_s[:T]), outs=outs)
+             y_routed=host(outs[0][0]), y=host(outs[0][1]),
+             pre_s=preact_rows(host(pre_s[:T])), outs=outs)
     if prec == B.MOK_MXFP8:
         g["h_q"] = workspace_item(S.ws, L.cfg, B.MOK_WS_SHARED, B.MOK_ITEM_H_RING).view(
             -1, I)[:T].cpu().numpy()
@@ -235,7 +236,7 @@ def gpu_step_with_shared(dims, x, logits, w13, w2, w13s, w2s, dy, prec, MB=2368,
     s, dev = B.mok_read_device_status()
     assert s == B.MOK_OK and dev == B.MOK_OK
     item = lambda it: workspace_item(S.ws_b, L.cfg, B.MOK_WS_SHARED_BACKWARD, it)  # noqa
-    gi = dict(a=host(pre_s[:T]),
+    gi = dict(a=preact_rows(host(pre_s[:T])),
               da=host(item(B.MOK_ITEM_DA).view(torch.bfloat16).view(-1, 2 * I)[:T]),
               sh=host(item(B.MOK_ITEM_WH).view(torch.bfloat16).view(-1, I)[:T]))
     if mx:

@@ -203,11 +203,14 @@ def kernel_table(prof, calls, c, pk, prec="bf16", save_pre=True, used=None):
             v.update(bound=r["bound"], frac=r["frac"], frac_tensor=r["frac_tensor"],
                      frac_hbm=r["frac_hbm"])
         table[k] = v
-    dom = max(prof, key=lambda k: prof[k][1])
+    # the dominant kernel among those with an algorithmic roofline
+    ranked = sorted((k for k in prof if "bound" in table[k]), key=lambda k: -prof[k][1])
+    if not ranked:
+        return table, None
+    dom = ranked[0]
     roof = roofline_of(dom, c, table[dom]["launches_per_call"], table[dom]["avg_ms"], pk, prec,
                        save_pre, used)
-    if roof is not None:
-        roof["kernel"] = dom
+    roof["kernel"] = dom
     return table, roof
 
 
@@ -395,6 +398,13 @@ def run_mok(args):
     roof["traffic"] = tr
     if tr is not None:
         roof["traffic_over_algorithmic"] = tr / roof["bytes_per_launch"]
+    # DRAM traffic of every GEMM against its algorithmic bytes, where the committed ncu
+    # summary applies to these kernel sources
+    for k, v in kernels.items():
+        t = ncu_traffic(k, args.workload)
+        r = roofline_of(k, cfg, v["launches_per_call"], v["avg_ms"], pk)
+        if t is not None and r is not None:
+            v["traffic_over_algorithmic"] = t / r["bytes_per_launch"]
 
     def profile(fn, c, prec, save_pre, used=None):
         """per-kernel table and dominant-kernel roofline of a phase (library events on the

@@ -141,9 +141,25 @@ MOK_DEV void st_val(void *p, int64_t i, float v, bool f32) {
     else
         static_cast<uint16_t *>(p)[i] = f32_to_bf16(v);
 }
-MOK_DEV float ld_val(const void *p, int64_t i, bool f32) {
-    return f32 ? static_cast<const float *>(p)[i]
-               : bf16_to_f32(static_cast<const uint16_t *>(p)[i]);
+// the values an accumulating epilogue adds to: rows fcol[n0 + j] (j < 16, rows past nr read
+// as 0), columns c and c + 128 (the latter when has1), all loads issued before any is used
+template <bool F32>
+MOK_DEV void load_rows16(const void *p, const int *fcol, int n0, int nr, int H, int c,
+                         bool has1, float (&a0)[16], float (&a1)[16]) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const bool ok = n0 + j < nr;
+        const int64_t o = (int64_t)fcol[ok ? n0 + j : 0] * H + c;
+        if (F32) {
+            const float *pf = static_cast<const float *>(p);
+            a0[j] = ok ? pf[o] : 0.f;
+            a1[j] = ok && has1 ? pf[o + 128] : 0.f;
+        } else {
+            const uint16_t *pb = static_cast<const uint16_t *>(p);
+            a0[j] = ok ? bf16_to_f32(pb[o]) : 0.f;
+            a1[j] = ok && has1 ? bf16_to_f32(pb[o + 128]) : 0.f;
+        }
+    }
 }
 
 // bounded wait; gives up when another role has aborted or after the wall-time limit
@@ -339,13 +355,10 @@ struct FwdDownT {
                 // every load of the chunk before any store: a store to one row may alias
                 // the next row's load, which would otherwise serialise the round trips
                 float a0[16], a1[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const bool ok = n0 + j < nr;
-                    const int64_t o = (int64_t)fcol[ok ? n0 + j : 0] * H + c;
-                    a0[j] = ok ? ld_val(slots, o, out_f32) : 0.f;
-                    a1[j] = ok && has1 ? ld_val(slots, o + 128, out_f32) : 0.f;
-                }
+                if (out_f32)
+                    load_rows16<true>(slots, fcol, n0, nr, H, c, has1, a0, a1);
+                else
+                    load_rows16<false>(slots, fcol, n0, nr, H, c, has1, a0, a1);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     d0[j] += a0[j];
@@ -613,13 +626,10 @@ struct BwdDgradT {
             ld(n0, d0, d1);
             if (accumulate) {  // every load of the chunk before any store (see FwdDownT)
                 float a0[16], a1[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const bool ok = n0 + j < nr;
-                    const int64_t o = (int64_t)fcol[ok ? n0 + j : 0] * H + c;
-                    a0[j] = ok ? ld_val(dx_slots, o, out_f32) : 0.f;
-                    a1[j] = ok && has1 ? ld_val(dx_slots, o + 128, out_f32) : 0.f;
-                }
+                if (out_f32)
+                    load_rows16<true>(dx_slots, fcol, n0, nr, H, c, has1, a0, a1);
+                else
+                    load_rows16<false>(dx_slots, fcol, n0, nr, H, c, has1, a0, a1);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     d0[j] += a0[j];

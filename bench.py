@@ -103,6 +103,8 @@ class Clocks:
 # the sources of the tensor-core GEMM engine (its translation unit, less the public header's
 # declarations): the kernels whose DRAM traffic per launch profiles/ncu_traffic.json records
 GEMM_SOURCES = ("mixture_experts_layer_deterministic_gb300/csrc/gemm_tc.cu",
+                "mixture_experts_layer_deterministic_gb300/csrc/gemm_tc_core.cuh",
+                "mixture_experts_layer_deterministic_gb300/csrc/ring_fwd.cu",
                 "mixture_experts_layer_deterministic_gb300/csrc/tc.cuh",
                 "mixture_experts_layer_deterministic_gb300/csrc/common.cuh",
                 "mixture_experts_layer_deterministic_gb300/csrc/mok_internal.h")
@@ -145,6 +147,7 @@ def algorithmic(kind, c, prec="bf16", save_pre=True, used=None):
     row_h, row_i = 2.0 * R * H, 2.0 * R * I      # bf16 rows of width H / I
     pre = 2.0 * R * 2 * I if save_pre else 0.0   # saved pre-activations (bf16)
     flops = {"gemm_up_swiglu": 4.0 * R * H * I, "gemm_down_push": 2.0 * R * H * I,
+             "ring_forward": 6.0 * R * H * I,
              "gemm_g_swiglu_bwd": 2.0 * R * H * I, "gemm_dgrad_push": 4.0 * R * H * I,
              "wgrad_w13": 4.0 * R * H * I, "wgrad_w2": 2.0 * R * H * I}
     dA_q = (1.0 + 1.0 / 32) * R * 2 * I if mx else 0.0
@@ -155,6 +158,10 @@ def algorithmic(kind, c, prec="bf16", save_pre=True, used=None):
            "gemm_dgrad_push": w13 + (dA_q if mx else 2 * row_i) + row_h,  # dx slots, bf16
            "wgrad_w13": 2.0 * R * H + 2 * row_i + w13b,
            "wgrad_w2": row_i + 2.0 * R * H + w2b,
+           # the forward through a smaller ring, one launch: weights, x (read per token,
+           # MXFP8 quantized), saved pre-activations and slots; h stays in the ring (L2)
+           "ring_forward": w13 + w2 + ob * T * H + pre + row_h,
+           "quantize_mxfp8": 2.0 * T * H + ob * T * H,
            "gather": 2.0 * T * H + xr, "combine": row_h + 2.0 * T * H + 4.0 * R,
            "dx_reduce": row_h + 2.0 * T * H, "route_topk": 4.0 * T * c.E + 8.0 * T * K,
            "gather_bwd": 2 * (2.0 * T * H) + 2 * row_h + (ob * R * H if mx else 0.0)}

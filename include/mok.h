@@ -91,13 +91,15 @@ typedef struct mok_config {
      * size that fills at least two SM waves per grouped GEMM ([arex] section "pull 代替
      * push", point 3: about 2,368 tokens for one shape). */
     int32_t minibatch;
-    /* Rows of the fixed-size dispatch ring ("macrobatch", [arex] section "pull 代替 push",
-     * point 2). 0, or any value >= R, means the ring holds every routed row and the
-     * forward runs as one pass. Otherwise ring_capacity >= minibatch is required and the
-     * forward runs in passes of sorted rows: in BF16 the ring is floor(ring_capacity /
-     * minibatch) minibatch slots, minibatch m uses slot m mod slots, and each pass is one
-     * minibatch; in MXFP8 each pass fills the whole ring. Results are the same bit for bit
-     * for every ring setting. No routed row is ever dropped. */
+    /* Rows of the fixed-size ring ("macrobatch", [arex] section "pull 代替 push", point 2).
+     * 0, or any value >= R, means the ring holds every routed row: the forward gathers all
+     * of them, then runs each GEMM over every tile. Otherwise ring_capacity >= minibatch is
+     * required and the forward is one persistent launch in which sorted row r passes
+     * through row r mod ring_capacity of two rings: gather units pull their tokens' x rows
+     * into the x ring, gate/up units read them and write h into the h ring, down units
+     * read h back and push to the slots; a ring row is rewritten only after the units
+     * that read its previous row have finished. Results are the same bit for bit for
+     * every ring setting. No routed row is ever dropped. */
     int32_t ring_capacity;
     int32_t prec;   /* mok_precision of the forward; the backward is MOK_BF16 */
     uint32_t flags; /* MOK_FLAG_* (0: bf16 storage) */
@@ -143,15 +145,26 @@ size_t mok_workspace_size(const mok_config *cfg, int which);
  * no counterpart; the layer's own outputs never need them). Rows are sorted rows (the
  * schedule's order) in the forward, padded rows in the backward (expert e owns rows
  * [poff[e], poff[e+1]), its counts[e] real rows first, poff[e] = sum over experts before e
- * of counts rounded up to 16). After a forward that ran as one pass (the ring holds every
- * routed row) the ring rows are all R sorted rows; after one in several passes they hold
- * the last pass's rows (ring slots as described for ring_capacity).
+ * of counts rounded up to 16). After a forward through a ring that holds every routed row
+ * the ring rows are the R sorted rows; through a smaller ring of C rows, ring row j holds
+ * the last sorted row r with r mod C = j.
  *   MOK_ITEM_X_RING       forward: gathered x [ring rows][H], bf16 or (MXFP8) E4M3
- *   MOK_ITEM_X_RING_SCALE forward, MXFP8: its E8M0 scales [ring rows][H/32]
+ *   MOK_ITEM_X_RING_SCALE forward, MXFP8: its E8M0 scales [R][H/32] (ring of every row);
+ *                         through a smaller ring, x is quantized once per token and this
+ *                         is [T][H/32], the scales of x's token rows
  *   MOK_ITEM_H_RING       forward: h entering the down GEMM [ring rows][I], bf16 or E4M3
- *                         (after a forward in several passes: the copy of the last pass
- *                         with an even index)
  *   MOK_ITEM_H_RING_SCALE forward, MXFP8: its E8M0 scales [ring rows][I/32]
+ *   MOK_ITEM_RING_TILES   forward, smaller ring: the tiles (int32 expert, first row, end
+ *                         row, 0) of sorted rows cut at expert boundaries, at multiples of
+ *                         the ring capacity and at the tile height; int32 [4] header whose
+ *                         first word is the tile count, then the tiles
+ *   MOK_ITEM_RING_ORDER   forward, smaller ring: the order in which units are claimed,
+ *                         int32 pairs (tile, kind << 16 | weight block), kind 0 for a
+ *                         gate/up unit (one per 128 features of I), 1 for a down unit (one
+ *                         per 256 features of H), 2 for the tile's gather (block 0)
+ *   MOK_ITEM_RING_DEPS    forward, smaller ring: per tile, int32 pair (first, last) of the
+ *                         tiles one ring lap back whose ring rows its gather and gate/up
+ *                         units overwrite (last < first: none)
  *   MOK_ITEM_SLOTS        forward: expert output of each flat id t*K + k [R][H] (bf16, or
  *                         fp32 under MOK_FLAG_FP32_STORAGE); backward: the per-slot dgrad
  *                         results, likewise
@@ -181,7 +194,10 @@ typedef enum mok_ws_item {
     MOK_ITEM_DA_Q = 8,
     MOK_ITEM_DA_SCALE = 9,
     MOK_ITEM_DY_Q = 10,
-    MOK_ITEM_DY_SCALE = 11
+    MOK_ITEM_DY_SCALE = 11,
+    MOK_ITEM_RING_TILES = 12,
+    MOK_ITEM_RING_ORDER = 13,
+    MOK_ITEM_RING_DEPS = 14
 } mok_ws_item;
 mok_status mok_workspace_item(const mok_config *cfg, int which, int item, size_t *offset,
                               size_t *bytes);
@@ -253,16 +269,14 @@ mok_status mok_build_schedule_noalloc(const mok_config *cfg, const int32_t *topk
  *           the backward reads both halves of a feature with one access.
  * GEMMs accumulate in fp32; values that are only stored (expert outputs, saved
  * pre-activations, y) take the storage type of cfg->flags.
- * A ring smaller than R rows (cfg->ring_capacity) makes the forward run in passes of
- * sorted rows: cfg->minibatch rows per pass in BF16, the whole ring in MXFP8 (results are
- * the same bit for bit either way). Then each pass's down GEMM runs on a second stream that
- * the library keeps per device, ordered by events after that pass's gate/up GEMM, so it
- * overlaps the next pass. The call still orders itself after earlier work on `stream`, and
- * later work on `stream` after all of it, so it may also be captured into a CUDA graph
- * from `stream`. The first such call on a device outside stream capture creates that stream
- * and its events; a captured call made before then runs its passes on `stream` alone (same
- * results, no overlap). Calls on one device from several host threads share that second
- * stream's events and must not overlap in time. */
+ * A ring smaller than R rows (cfg->ring_capacity) makes the forward one persistent launch
+ * (one CTA per SM) that takes units from a device-side counter in a fixed order and waits,
+ * before loading a unit's operands, for the units it depends on (a gate/up unit on its
+ * tile's gather, a down unit on its tile's gate/up units; a gather or gate/up unit on the
+ * units that read, one lap back, the ring rows it overwrites). The order makes every wait one on an earlier unit, so the launch always
+ * completes; each wait is still bounded (2 s), after which MOK_ERR_TIMEOUT is recorded in
+ * the device status word and the launch returns early with y undefined. In MXFP8, x is
+ * quantized along H once per token before that launch. Everything runs on `stream`. */
 mok_status mok_forward(const mok_config *cfg, const void *x, const mok_schedule *sched,
                        const float *topk_w, const void *w13, const uint8_t *w13_scale,
                        const void *w2, const uint8_t *w2_scale, void *y, void *saved_preact,
@@ -430,6 +444,15 @@ mok_status mok_clear_device_status(void);
  * device status word reads MOK_ERR_TIMEOUT and the context stays usable.
  * Asynchronous on `stream`; MOK_ERR_INVALID_ARG for a limit out of range. */
 mok_status mok_selftest_bounded_wait(uint32_t limit_us, cudaStream_t stream);
+
+/* The same check for the ring forward's waits (mok_forward through a ring smaller than R):
+ * one thread waits, through the bounded spin its producers use, on a device counter that
+ * nothing raises, with a limit of limit_us microseconds (1 .. 1000000) instead of 2 s.
+ * If the status word already holds a problem the wait gives up at once (as a producer does
+ * once another CTA has given up). Afterwards the status word reads MOK_ERR_TIMEOUT (or the
+ * earlier problem) and the context stays usable. Asynchronous on `stream`;
+ * MOK_ERR_INVALID_ARG for a limit out of range. */
+mok_status mok_selftest_bounded_count_wait(uint32_t limit_us, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -52,6 +52,9 @@ MOK_ITEM_DA_Q = 8
 MOK_ITEM_DA_SCALE = 9
 MOK_ITEM_DY_Q = 10
 MOK_ITEM_DY_SCALE = 11
+MOK_ITEM_RING_TILES = 12
+MOK_ITEM_RING_ORDER = 13
+MOK_ITEM_RING_DEPS = 14
 
 EXPORTED = [
     "mok_abi_version", "mok_status_string", "mok_check_config", "mok_segment_capacity",
@@ -61,7 +64,7 @@ EXPORTED = [
     "mok_build_schedule_noalloc", "mok_shared_expert_forward",
     "mok_quantize_mxfp8_transposed", "mok_backward_mxfp8", "mok_shared_expert_backward",
     "mok_shared_expert_forward_mxfp8", "mok_shared_expert_backward_mxfp8",
-    "mok_selftest_bounded_wait", "mok_workspace_item",
+    "mok_selftest_bounded_wait", "mok_selftest_bounded_count_wait", "mok_workspace_item",
 ]
 
 # bytes of the fixed scratch array behind mok_build_schedule_noalloc
@@ -122,6 +125,7 @@ def lib():
             "mok_shared_expert_backward_mxfp8": ([cfgp, p, p, p, p, p, p, p, p, p, p, p, sz, p],
                                                  ctypes.c_int),
             "mok_selftest_bounded_wait": ([ctypes.c_uint32, p], ctypes.c_int),
+            "mok_selftest_bounded_count_wait": ([ctypes.c_uint32, p], ctypes.c_int),
             "mok_shared_expert_backward": ([cfgp, p, p, p, p, p, p, p, p, p, sz, p],
                                            ctypes.c_int),
             "mok_backward_mxfp8": ([cfgp, p, schp, p, p, p, p, p, p, p, p, p, p, p, p, p, sz,
@@ -265,6 +269,10 @@ def mok_shared_expert_forward_mxfp8(cfg, x, w13s_q, w13s_scale, w2s_q, w2s_scale
 
 def mok_selftest_bounded_wait(limit_us, stream=None) -> int:
     return lib().mok_selftest_bounded_wait(int(limit_us), _stream(stream))
+
+
+def mok_selftest_bounded_count_wait(limit_us, stream=None) -> int:
+    return lib().mok_selftest_bounded_count_wait(int(limit_us), _stream(stream))
 
 
 def mok_shared_expert_backward_mxfp8(cfg, x, w13st_q, w13st_scale, w2st_q, w2st_scale,

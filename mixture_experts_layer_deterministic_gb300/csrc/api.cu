@@ -47,32 +47,17 @@ size_t stored_bytes(const mok_config *c) { return f32_storage(c) ? 4 : 2; }
 
 int64_t rows_R(const mok_config *c) { return (int64_t)c->T * c->K; }
 
-// ring geometry: n_slots == 0 means the ring holds every routed row (one pass). Else the
-// forward runs in passes of `pass` sorted rows through n_slots slots of `pass` rows:
-//   BF16: one minibatch per pass, floor(capacity / minibatch) slots;
-//   MXFP8: the whole ring per pass (one slot of `capacity` rows).
-// Either gives the same results bit for bit. A pass carries a fixed cost (launches, pipeline
-// fill, tile list, gather) that bigger passes amortize, and a gate/up GEMM of T tiles takes
-// ceil(8T / 152) SM waves at I = 1024. On the 65536-token imbalanced workload (ring 1.25
-// minibatches): an MXFP8 pass (112-row tiles) is two waves at either size, so the whole ring
-// per pass ran 17% faster; a BF16 minibatch inside one expert is exactly one wave (19
-// tiles), the whole ring two (24), and it ran 10% slower.
-void ring_geom(const mok_config *c, int32_t *n_slots, int64_t *ring_rows, int32_t *pass) {
-    const int64_t R = rows_R(c);
-    if (c->ring_capacity == 0 || (int64_t)c->ring_capacity >= R) {
-        *n_slots = 0;
-        *ring_rows = R;
-        *pass = c->minibatch;
-    } else if (c->prec == MOK_MXFP8) {
-        *n_slots = 1;
-        *ring_rows = c->ring_capacity;
-        *pass = c->ring_capacity;
-    } else {
-        *n_slots = c->ring_capacity / c->minibatch;
-        *ring_rows = (int64_t)(*n_slots) * c->minibatch;
-        *pass = c->minibatch;
-    }
+// The forward runs in one of two ways:
+//   a ring that holds every routed row (capacity 0 or >= R): gather every row, then the
+//   gate/up and down GEMMs over all tiles (three launches);
+//   a partial ring (capacity C < R): one persistent launch over rows cycling through a ring of
+//   C rows, row r in ring row r mod C (ring_fwd.cu).
+// Both give the same results bit for bit.
+bool partial_ring(const mok_config *c) {
+    return c->ring_capacity != 0 && (int64_t)c->ring_capacity < rows_R(c);
 }
+// rows of the h ring (and, for the full ring, of the x ring)
+int64_t ring_rows(const mok_config *c) { return partial_ring(c) ? c->ring_capacity : rows_R(c); }
 
 // ---------------------------------------------------------------- workspace layouts
 struct Carver {
@@ -95,40 +80,43 @@ size_t ws_offset(const void *p) { return (size_t)((uintptr_t)p - (uintptr_t)kVir
 struct FwdWs {
     int32_t *tiles;  // points past a 16-byte header holding the count
     int64_t tiles_cap;
-    void *xring;
-    uint8_t *xring_s;
-    void *hring;
-    uint8_t *hring_s;
+    void *xring;              // gathered x [ring rows][H]
+    uint8_t *xring_s;         // MXFP8, full ring: its scales [R][H/32]
+    void *xq;                 // MXFP8, partial ring: x quantized token-major [T][H] and
+    uint8_t *xq_s;            // its scales [T][H/32]
+    void *hring;              // [ring rows][I]
+    uint8_t *hring_s;         // MXFP8: [ring rows][I/32]
     void *slots;              // [R][H], the storage type of cfg->flags
     uint8_t *sf_w13, *sf_w2;  // MXFP8 weight scales as tensor-core atoms
-    uint8_t *sf_x, *sf_h;     // MXFP8 token-tile scales as atoms (per pass)
-    // the tile lists of all passes, built by one launch: pass m's list (count at [-4])
-    // starts at tiles + m * list_stride
-    int64_t n_lists, list_stride;
-    // a forward in several ring passes: second copies of the h ring and the h tiles' scale
-    // atoms, so that the down GEMM of one pass can run while the next pass is gathered and
-    // multiplied (else nullptr)
-    void *hring2;
-    uint8_t *hring_s2, *sf_h2;
+    uint8_t *sf_x, *sf_h;     // MXFP8 token-tile scales as atoms, per tile of the list
+    // partial ring: each tile's dependencies, the claim order, the unit count and claim
+    // counter, per-tile completion counters
+    int2 *dep, *umap;
+    int32_t *hdr, *done_up, *done_dn, *done_g;
+    int chunk;
 };
 
 size_t carve_fwd(const mok_config *c, void *ws, FwdWs *o) {
     Carver cv{(char *)ws};
     const int64_t R = rows_R(c);
-    int32_t ns, pr;
-    int64_t rr;
-    ring_geom(c, &ns, &rr, &pr);
-    const int64_t pass_rows = ns == 0 ? R : pr;
     const bool mx = c->prec == MOK_MXFP8;
+    const bool part = partial_ring(c);
+    const int64_t rr = ring_rows(c);
     const int esz = mx ? 1 : 2;
     FwdWs w;
-    w.tiles_cap = tile_list_cap(pass_rows, c->E, gemm_tc_tile_rows(mx));
-    w.n_lists = ns == 0 ? 1 : (R + pr - 1) / pr;
-    w.list_stride = 4 + 4 * w.tiles_cap;  // int32s: a 16-byte header and the tiles
-    int32_t *t = cv.take<int32_t>((size_t)(w.n_lists * w.list_stride) * 4);
+    w.chunk = part ? ring_tile_rows(mx, c->ring_capacity) : gemm_tc_tile_rows(mx);
+    w.tiles_cap = part ? ring_tiles_cap(R, c->E, c->ring_capacity, w.chunk)
+                       : tile_list_cap(R, c->E, w.chunk);
+    int32_t *t = cv.take<int32_t>(16 + (size_t)w.tiles_cap * 16);
     w.tiles = t ? t + 4 : nullptr;
     w.xring = cv.take<void>((size_t)rr * c->H * esz);
-    w.xring_s = mx ? cv.take<uint8_t>((size_t)rr * (c->H / 32)) : nullptr;
+    w.xring_s = mx && !part ? cv.take<uint8_t>((size_t)R * (c->H / 32)) : nullptr;
+    w.xq = nullptr;
+    w.xq_s = nullptr;
+    if (part && mx) {
+        w.xq = cv.take<void>((size_t)c->T * c->H);
+        w.xq_s = cv.take<uint8_t>((size_t)c->T * (c->H / 32));
+    }
     w.hring = cv.take<void>((size_t)rr * c->I * esz);
     w.hring_s = mx ? cv.take<uint8_t>((size_t)rr * (c->I / 32)) : nullptr;
     w.slots = cv.take<void>((size_t)R * c->H * stored_bytes(c));
@@ -139,52 +127,19 @@ size_t carve_fwd(const mok_config *c, void *ws, FwdWs *o) {
         w.sf_x = cv.take<uint8_t>((size_t)w.tiles_cap * (c->H / 128) * 512);
         w.sf_h = cv.take<uint8_t>((size_t)w.tiles_cap * (c->I / 128) * 512);
     }
-    w.hring2 = nullptr;
-    w.hring_s2 = w.sf_h2 = nullptr;
-    if (ns > 0 && R > pr) {
-        w.hring2 = cv.take<void>((size_t)rr * c->I * esz);
-        if (mx) {
-            w.hring_s2 = cv.take<uint8_t>((size_t)rr * (c->I / 32));
-            w.sf_h2 = cv.take<uint8_t>((size_t)w.tiles_cap * (c->I / 128) * 512);
-        }
+    w.dep = w.umap = nullptr;
+    w.hdr = w.done_up = w.done_dn = w.done_g = nullptr;
+    if (part) {
+        const int64_t units = w.tiles_cap * (1 + c->I / 128 + (c->H + 255) / 256);
+        w.dep = cv.take<int2>((size_t)w.tiles_cap * sizeof(int2));
+        w.umap = cv.take<int2>((size_t)units * sizeof(int2));
+        w.hdr = cv.take<int32_t>(16);
+        w.done_up = cv.take<int32_t>((size_t)w.tiles_cap * 4);
+        w.done_dn = cv.take<int32_t>((size_t)w.tiles_cap * 4);
+        w.done_g = cv.take<int32_t>((size_t)w.tiles_cap * 4);
     }
     if (o) *o = w;
     return cv.off;
-}
-
-// The second stream of a forward in several ring passes, and its events, per device:
-// created on first use and kept for the life of the process.
-struct SideStream {
-    cudaStream_t s = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr, up[2] = {nullptr, nullptr},
-                down[2] = {nullptr, nullptr};
-};
-constexpr int MAX_DEVICES = 64;
-SideStream g_side[MAX_DEVICES];
-std::mutex g_side_mu;
-
-// *out is nullptr (and nothing is created) when the stream does not exist yet and `may_create`
-// is false
-cudaError_t side_stream(SideStream **out, bool may_create) {
-    *out = nullptr;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_side_mu);
-    SideStream &ss = g_side[dev];
-    if (ss.s == nullptr && !may_create) return cudaSuccess;
-    if (ss.s == nullptr) {
-        SideStream n;
-        e = cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking);
-        cudaEvent_t *evs[] = {&n.fork, &n.join, &n.up[0], &n.up[1], &n.down[0], &n.down[1]};
-        for (cudaEvent_t *ev : evs)
-            if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
-        if (e != cudaSuccess) return e;
-        ss = n;
-    }
-    *out = &ss;
-    return cudaSuccess;
 }
 
 struct BwdWs {
@@ -420,16 +375,27 @@ mok_status mok_workspace_item(const mok_config *c, int which, int item, size_t *
     if (which == MOK_WS_FORWARD) {
         FwdWs w;
         carve_fwd(c, kVirtualWs, &w);
-        int32_t ns, pr;
-        int64_t rr;
-        ring_geom(c, &ns, &rr, &pr);
+        const size_t rr = (size_t)ring_rows(c);
+        const bool part = partial_ring(c);
         const size_t esz = mx ? 1 : 2;
         switch (item) {
-            case MOK_ITEM_X_RING: p = w.xring; n = (size_t)rr * H * esz; break;
-            case MOK_ITEM_X_RING_SCALE: p = w.xring_s; n = (size_t)rr * (H / 32); break;
+            case MOK_ITEM_X_RING: p = w.xring; n = rr * H * esz; break;
+            case MOK_ITEM_X_RING_SCALE:  // a partial ring: the scales of x's token rows
+                p = part ? (const void *)w.xq_s : (const void *)w.xring_s;
+                n = (part ? T : R) * (H / 32);
+                break;
             case MOK_ITEM_H_RING: p = w.hring; n = (size_t)rr * I * esz; break;
             case MOK_ITEM_H_RING_SCALE: p = w.hring_s; n = (size_t)rr * (I / 32); break;
             case MOK_ITEM_SLOTS: p = w.slots; n = R * H * stored_bytes(c); break;
+            case MOK_ITEM_RING_TILES:
+                p = w.dep ? (const void *)(w.tiles - 4) : nullptr;
+                n = 16 + (size_t)w.tiles_cap * 16;
+                break;
+            case MOK_ITEM_RING_ORDER:
+                p = w.umap;
+                n = (size_t)w.tiles_cap * (1 + I / 128 + (H + 255) / 256) * 8;
+                break;
+            case MOK_ITEM_RING_DEPS: p = w.dep; n = (size_t)w.tiles_cap * 8; break;
             default: break;
         }
     } else if (which == MOK_WS_BACKWARD || which == MOK_WS_BACKWARD_RECOMPUTE) {
@@ -547,11 +513,8 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
     if (R == 0) return MOK_OK;
     FwdWs w;
     carve_fwd(c, ws, &w);
-    int32_t n_slots, pass;  // pass: rows per pass
-    int64_t ring_rows;
-    ring_geom(c, &n_slots, &ring_rows, &pass);
-    Ring ring{R, pass, n_slots};
-    const int64_t n_pass = n_slots == 0 ? 1 : (R + pass - 1) / pass;
+    const int chunk = w.chunk;
+    const int64_t cap = w.tiles_cap;
     if (mx) {
         // the weights' scales in the tensor cores' atom layout, once per call
         MOK_LAUNCH(KK_SCALE_ATOMS, 2,
@@ -560,69 +523,66 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
                                launch_scale_atoms_rows(w2_scale, (int64_t)c->E * c->H, c->I,
                                                        w.sf_w2, stream)));
     }
-    // every pass's tile list, in one launch
-    const int chunk = gemm_tc_tile_rows(mx);
-    const int64_t cap = w.tiles_cap;
-    MOK_LAUNCH(KK_TILES, 1,
-               launch_build_tiles_passes(sch->offsets, c->E, R, n_slots == 0 ? R : pass, n_pass,
-                                         chunk, w.tiles, w.list_stride, cap, status, stream));
-    // several passes: each pass's down GEMM runs on a second stream, after that pass's
-    // gate/up GEMM, so that it overlaps the next pass's gather and gate/up GEMM on the
-    // caller's stream; consecutive passes alternate between two copies of the h ring (and
-    // its scale atoms), and a pass waits until the down GEMM two passes back has released
-    // its copy
-    bool overlap = n_pass > 1 && w.hring2 != nullptr;
-    SideStream *ss = nullptr;
-    if (overlap) {
-        // the second stream is created outside stream capture; a captured call made before
-        // it exists runs its passes on the caller's stream alone
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return MOK_ERR_CUDA;
-        if (side_stream(&ss, cs == cudaStreamCaptureStatusNone) != cudaSuccess)
-            return MOK_ERR_CUDA;
-        overlap = ss != nullptr;
-    }
-    if (overlap) {
-        if (cudaEventRecord(ss->fork, stream) != cudaSuccess ||
-            cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
-            return MOK_ERR_CUDA;
-    }
-    const FwdWs w0 = w;
-    for (int64_t m = 0; m < n_pass; ++m) {
-        const int64_t p0 = n_slots == 0 ? 0 : m * pass;
-        const int64_t p1 = n_slots == 0 ? R : (p0 + pass < R ? p0 + pass : R);
-        const int b = overlap ? (int)(m & 1) : 0;
-        w.tiles = w0.tiles + m * w0.list_stride;
-        if (b == 1) {
-            w.hring = w0.hring2;
-            w.hring_s = w0.hring_s2;
-            w.sf_h = w0.sf_h2;
-        } else {
-            w.hring = w0.hring;
-            w.hring_s = w0.hring_s;
-            w.sf_h = w0.sf_h;
-        }
-        if (overlap && m >= 2 && cudaStreamWaitEvent(stream, ss->down[b], 0) != cudaSuccess)
-            return MOK_ERR_CUDA;
-        // a ring that holds every row is filled token by token (each x row read once);
-        // a smaller ring pass by pass in sorted-row order
-        if (!mx && n_slots == 0)
+    if (partial_ring(c)) {
+        // one persistent launch through the ring; MXFP8 quantizes x once, token-major
+        if (mx)
+            MOK_LAUNCH(KK_QUANTIZE, 1,
+                       launch_quantize_mxfp8((const uint16_t *)x, c->T, c->H,
+                                             (uint8_t *)w.xq, w.xq_s, stream));
+        RingFwdArgs ra{};
+        ra.offsets = sch->offsets;
+        ra.perm = sch->perm;
+        ra.tiles = w.tiles;
+        ra.tiles_cap = cap;
+        ra.dep = w.dep;
+        ra.umap = w.umap;
+        ra.hdr = w.hdr;
+        ra.done_up = w.done_up;
+        ra.done_dn = w.done_dn;
+        ra.done_g = w.done_g;
+        ra.x = mx ? (const void *)w.xq : x;
+        ra.xs = w.xq_s;
+        ra.xring = w.xring;
+        ra.w13 = w13;
+        ra.w2 = w2;
+        ra.sf_w13 = w.sf_w13;
+        ra.sf_w2 = w.sf_w2;
+        ra.sf_x = w.sf_x;
+        ra.sf_h = w.sf_h;
+        ra.hring = w.hring;
+        ra.hring_s = w.hring_s;
+        ra.preact = saved_preact;
+        ra.preact_f32 = f32_storage(c);
+        ra.slots = w.slots;
+        ra.out_f32 = f32_storage(c);
+        ra.T = c->T;
+        ra.R = R;
+        ra.C = c->ring_capacity;
+        ra.chunk = chunk;
+        ra.lag = ring_lag(mx, c->ring_capacity);
+        ra.lag_gather = ra.lag;
+        ra.H = c->H;
+        ra.I = c->I;
+        ra.E = c->E;
+        ra.K = c->K;
+        ra.mx = mx;
+        ra.status = status;
+        MOK_LAUNCH(KK_RING_FWD, mx ? 3 : 2, launch_ring_forward(ra, stream));
+    } else {
+        // a ring that holds every row: filled token by token (each x row read once), then
+        // the two GEMMs over every tile
+        const Ring ring{R, c->minibatch, 0};
+        MOK_LAUNCH(KK_TILES, 1,
+                   launch_build_tiles(sch->offsets, c->E, 0, R, chunk, w.tiles, cap, status,
+                                      stream));
+        if (!mx)
             MOK_LAUNCH(KK_GATHER, 1,
                        launch_gather_tok_bf16((const uint16_t *)x, sch->inv, c->T, c->K, c->H,
                                               (uint16_t *)w.xring, stream));
-        else if (!mx)
-            MOK_LAUNCH(KK_GATHER, 1,
-                       launch_gather_bf16((const uint16_t *)x, sch->perm, c->K, c->H, p0, p1, R,
-                                          pass, n_slots, (uint16_t *)w.xring, stream));
-        else if (n_slots == 0)
+        else
             MOK_LAUNCH(KK_GATHER, 1,
                        launch_gather_tok_mxfp8((const uint16_t *)x, sch->inv, c->T, c->K, c->H,
                                                (uint8_t *)w.xring, w.xring_s, stream));
-        else
-            MOK_LAUNCH(KK_GATHER, 1,
-                       launch_gather_mxfp8((const uint16_t *)x, sch->perm, c->K, c->H, p0, p1,
-                                           R, pass, n_slots, (uint8_t *)w.xring,
-                                           w.xring_s, stream));
         GemmUpArgs ua{w.tiles, cap, w.xring, w.xring_s, w13, w13_scale, w.hring,
                       w.hring_s, saved_preact, c->H, c->I, c->E, mx, ring, status};
         ua.preact_f32 = f32_storage(c);
@@ -631,36 +591,19 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
         da.out_f32 = f32_storage(c);
         if (mx) {
             MOK_LAUNCH(KK_SCALE_ATOMS, 1,
-                       launch_scale_atoms_tiles(w.tiles, cap, w.xring_s, R, pass, n_slots,
+                       launch_scale_atoms_tiles(w.tiles, cap, w.xring_s, R, c->minibatch, 0,
                                                 c->H, w.sf_x, stream));
-            MOK_LAUNCH(KK_GEMM_UP, 1,
-                       launch_gemm_up_tc_mx(ua, ring_rows, w.sf_w13, w.sf_x, stream));
+            MOK_LAUNCH(KK_GEMM_UP, 1, launch_gemm_up_tc_mx(ua, R, w.sf_w13, w.sf_x, stream));
             MOK_LAUNCH(KK_SCALE_ATOMS, 1,
-                       launch_scale_atoms_tiles(w.tiles, cap, w.hring_s, R, pass, n_slots,
+                       launch_scale_atoms_tiles(w.tiles, cap, w.hring_s, R, c->minibatch, 0,
                                                 c->I, w.sf_h, stream));
+            MOK_LAUNCH(KK_GEMM_DOWN, 1,
+                       launch_gemm_down_tc_mx(da, R, w.sf_w2, w.sf_h, stream));
         } else {
-            MOK_LAUNCH(KK_GEMM_UP, 1, launch_gemm_up_tc(ua, ring_rows, stream));
-        }
-        {
-            cudaStream_t outer = stream;
-            if (overlap) {
-                if (cudaEventRecord(ss->up[b], outer) != cudaSuccess ||
-                    cudaStreamWaitEvent(ss->s, ss->up[b], 0) != cudaSuccess)
-                    return MOK_ERR_CUDA;
-            }
-            cudaStream_t stream = overlap ? ss->s : outer;  // the down GEMM's stream
-            if (mx)
-                MOK_LAUNCH(KK_GEMM_DOWN, 1,
-                           launch_gemm_down_tc_mx(da, ring_rows, w.sf_w2, w.sf_h, stream));
-            else
-                MOK_LAUNCH(KK_GEMM_DOWN, 1, launch_gemm_down_tc(da, ring_rows, stream));
-            if (overlap && cudaEventRecord(ss->down[b], stream) != cudaSuccess)
-                return MOK_ERR_CUDA;
+            MOK_LAUNCH(KK_GEMM_UP, 1, launch_gemm_up_tc(ua, R, stream));
+            MOK_LAUNCH(KK_GEMM_DOWN, 1, launch_gemm_down_tc(da, R, stream));
         }
     }
-    if (overlap && (cudaEventRecord(ss->join, ss->s) != cudaSuccess ||
-                    cudaStreamWaitEvent(stream, ss->join, 0) != cudaSuccess))
-        return MOK_ERR_CUDA;
     MOK_LAUNCH(KK_COMBINE, 1,
                launch_combine(w.slots, topk_w, c->T, c->K, c->H, y, f32_storage(c), stream));
     return MOK_OK;
@@ -1026,6 +969,16 @@ mok_status mok_selftest_bounded_wait(uint32_t limit_us, cudaStream_t stream) {
     if (st != MOK_OK) return st;
     if (limit_us == 0 || limit_us > 1000000u) return MOK_ERR_INVALID_ARG;
     if (launch_bounded_wait_probe(status, (uint64_t)limit_us * 1000ull, stream) != cudaSuccess)
+        return MOK_ERR_CUDA;
+    return MOK_OK;
+}
+
+mok_status mok_selftest_bounded_count_wait(uint32_t limit_us, cudaStream_t stream) {
+    int *status;
+    mok_status st = check_device(&status);
+    if (st != MOK_OK) return st;
+    if (limit_us == 0 || limit_us > 1000000u) return MOK_ERR_INVALID_ARG;
+    if (launch_bounded_count_probe(status, (uint64_t)limit_us * 1000ull, stream) != cudaSuccess)
         return MOK_ERR_CUDA;
     return MOK_OK;
 }

@@ -64,9 +64,10 @@ MOK_DEV float e4m3_to_f32(uint32_t c) {
 }
 
 // ---------------------------------------------------------------- ring mapping
-// Ring slot of sorted row r ([arex] section "pull 代替 push", point 2: a fixed ring cycled
-// at minibatch granularity): identity when the ring holds every row, otherwise minibatch
-// m = r / MB occupies slot m mod n_slots.
+// Ring row of sorted row r ([arex] section "pull 代替 push", point 2: a fixed ring that
+// rows cycle through): identity when the ring holds every row, otherwise row
+// ((r / MB) mod n_slots) * MB + r mod MB; the forward through a ring of C rows uses MB = C,
+// n_slots = 1, i.e. row r mod C.
 struct RingMap {
     int64_t R;
     int32_t MB;

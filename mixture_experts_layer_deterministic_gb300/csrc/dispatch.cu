@@ -26,24 +26,7 @@ inline unsigned grid_for(int64_t items, int per_block, int per_sm = 32) {
 }
 
 // ---------------------------------------------------------------- BF16 gather
-// One warp per sorted row r in [p0, p1): ring[ring(r)] = x[perm[r] / K].
-__global__ void __launch_bounds__(TPB)
-    gather_bf16_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm, int K,
-                       int H, int64_t p0, int64_t p1, RingMap rm, uint16_t *__restrict__ ring) {
-    const int lane = threadIdx.x & 31;
-    const int64_t nw = (int64_t)gridDim.x * (TPB / 32);
-    const int nv = H / 8;  // 16-byte vectors per row
-    for (int64_t r = p0 + (int64_t)blockIdx.x * (TPB / 32) + (threadIdx.x >> 5); r < p1;
-         r += nw) {
-        const int64_t t = perm[r] / K;
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + t * H);
-        uint4 *dst = reinterpret_cast<uint4 *>(ring + rm(r) * H);
-#pragma unroll 4
-        for (int v = lane; v < nv; v += 32) dst[v] = ldg_nc_v4(src + v);
-    }
-}
-
-// Token-major form, when the ring holds every row (slot r = r): one warp per token t reads
+// Token-major, into a ring that holds every row (slot r = r): one warp per token t reads
 // x[t] once and writes it to the ring rows inv[t*K + k] of its K routed copies. Reading
 // each token row once keeps the gather at the bytes it must write, where the sorted-order
 // form re-reads every row K times from scattered positions.
@@ -119,23 +102,6 @@ MOK_DEV void quant_block32(const uint16_t *__restrict__ src, uint8_t *__restrict
     qd[0] = make_uint4(out[0], out[1], out[2], out[3]);
     qd[1] = make_uint4(out[4], out[5], out[6], out[7]);
     *sbyte = (uint8_t)sb;
-}
-
-// One thread per 32-element block of the rows [p0, p1) of the sorted stream.
-__global__ void __launch_bounds__(TPB)
-    gather_mxfp8_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm, int K,
-                        int H, int64_t p0, int64_t p1, RingMap rm, uint8_t *__restrict__ rq,
-                        uint8_t *__restrict__ rs) {
-    const int nb = H / 32;
-    const int64_t total = (p1 - p0) * nb;
-    const int64_t stride = (int64_t)gridDim.x * TPB;
-    for (int64_t i = (int64_t)blockIdx.x * TPB + threadIdx.x; i < total; i += stride) {
-        const int64_t r = p0 + i / nb;
-        const int b = (int)(i % nb);
-        const int64_t t = perm[r] / K;
-        const int64_t slot = rm(r);
-        quant_block32(x + t * H + b * 32, rq + slot * H + b * 32, rs + slot * nb + b);
-    }
 }
 
 // Along rows, stored transposed: one thread per (matrix b, column c, 32-row block j); the
@@ -488,16 +454,6 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-cudaError_t launch_gather_bf16(const uint16_t *x, const int32_t *perm, int K, int H, int64_t p0,
-                               int64_t p1, int64_t R, int MB, int n_slots, uint16_t *ring,
-                               cudaStream_t s) {
-    if (p1 <= p0) return cudaSuccess;
-    RingMap rm{R, MB, n_slots};
-    gather_bf16_kernel<<<grid_for(p1 - p0, TPB / 32, 16), TPB, 0, s>>>(x, perm, K, H, p0,
-                                                                             p1, rm, ring);
-    return cudaGetLastError();
-}
-
 __global__ void single_expert_offsets_kernel(int32_t *off, int64_t rows) {
     off[0] = 0;
     off[1] = (int32_t)rows;
@@ -547,16 +503,6 @@ cudaError_t launch_gather_tok_mxfp8(const uint16_t *x, const int32_t *inv, int64
     if (T == 0) return cudaSuccess;
     gather_tok_mxfp8_kernel<<<grid_for(T * (H / 32), TPB, 16), TPB, 0, s>>>(
         x, inv, T, K, H, ring_q, ring_s);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_gather_mxfp8(const uint16_t *x, const int32_t *perm, int K, int H, int64_t p0,
-                                int64_t p1, int64_t R, int MB, int n_slots, uint8_t *ring_q,
-                                uint8_t *ring_s, cudaStream_t s) {
-    if (p1 <= p0) return cudaSuccess;
-    RingMap rm{R, MB, n_slots};
-    gather_mxfp8_kernel<<<grid_for((p1 - p0) * (H / 32), TPB, 16), TPB, 0, s>>>(
-        x, perm, K, H, p0, p1, rm, ring_q, ring_s);
     return cudaGetLastError();
 }
 

@@ -13,7 +13,7 @@ enum KernelKind {
     KK_ROUTE = 0, KK_SCHEDULE, KK_TILES, KK_GATHER, KK_GEMM_UP, KK_GEMM_DOWN, KK_COMBINE,
     KK_QUANTIZE, KK_PAD, KK_GATHER_BWD, KK_GEMM_G, KK_ROUTER_GRAD, KK_GEMM_DGRAD,
     KK_DX_REDUCE, KK_WGRAD13, KK_WGRAD2, KK_SCALE_ATOMS, KK_SHARED_UP, KK_SHARED_DOWN,
-    KK_SHARED_BWD, KK_COUNT
+    KK_SHARED_BWD, KK_RING_FWD, KK_COUNT
 };
 // while profiling is on: brackets the launches between begin and end with events
 void prof_begin(int kind, cudaStream_t s);
@@ -48,21 +48,15 @@ cudaError_t launch_build_schedule(const int32_t *idx, int64_t R, int E, int MB,
 int64_t tile_list_cap(int64_t rows, int E, int chunk);
 cudaError_t launch_build_tiles(const int32_t *offsets, int E, int64_t p0, int64_t p1, int chunk,
                                int32_t *list, int64_t cap, int *status, cudaStream_t s);
-// the tile lists of every pass of a forward through a partial ring, in one launch: pass m
-// covers rows [m*pass, min((m+1)*pass, R)) and its list (count at [-4]) starts at
-// list0 + m*stride
-cudaError_t launch_build_tiles_passes(const int32_t *offsets, int E, int64_t R, int64_t pass,
-                                      int64_t n_pass, int chunk, int32_t *list0, int64_t stride,
-                                      int64_t cap, int *status, cudaStream_t s);
 
 // ---------------------------------------------------------------- dispatch / combine
-cudaError_t launch_gather_bf16(const uint16_t *x, const int32_t *perm, int K, int H, int64_t p0,
-                               int64_t p1, int64_t R, int MB, int n_slots, uint16_t *ring,
-                               cudaStream_t s);
 // offsets of a single expert owning rows [0, rows): off[0] = 0, off[1] = rows
 cudaError_t launch_single_expert_offsets(int32_t *off, int64_t rows, cudaStream_t s);
 // one thread waits, through the GEMM roles' bounded wait, on an mbarrier nothing completes
 cudaError_t launch_bounded_wait_probe(int *status, uint64_t limit_ns, cudaStream_t s);
+// one thread waits, through the ring forward's bounded counter wait, on a counter nothing
+// raises
+cudaError_t launch_bounded_count_probe(int *status, uint64_t limit_ns, cudaStream_t s);
 // the backward's view of a single expert owning every token in token order: offsets
 // [0, T], padded offsets [0, T rounded up to 16], counts [T], weight one and row r -> r
 cudaError_t launch_single_expert_bwd_setup(int32_t *offsets, int32_t *poff, int32_t *counts,
@@ -73,9 +67,6 @@ cudaError_t launch_gather_tok_bf16(const uint16_t *x, const int32_t *inv, int64_
                                    int H, uint16_t *ring, cudaStream_t s);
 cudaError_t launch_gather_tok_mxfp8(const uint16_t *x, const int32_t *inv, int64_t T, int K,
                                     int H, uint8_t *ring_q, uint8_t *ring_s, cudaStream_t s);
-cudaError_t launch_gather_mxfp8(const uint16_t *x, const int32_t *perm, int K, int H, int64_t p0,
-                                int64_t p1, int64_t R, int MB, int n_slots, uint8_t *ring_q,
-                                uint8_t *ring_s, cudaStream_t s);
 cudaError_t launch_quantize_mxfp8(const uint16_t *src, int64_t rows, int cols, uint8_t *q,
                                   uint8_t *scale, cudaStream_t s);
 // along rows, stored transposed: src [batch][rows][cols] -> q [batch][cols][rows]
@@ -180,6 +171,47 @@ cudaError_t launch_scale_atoms_tiles_padded(const int32_t *tiles, int64_t cap,
                                             const uint8_t *src, const int32_t *offsets,
                                             const int32_t *poff, int K, uint8_t *dst,
                                             cudaStream_t s);
+
+// The forward through a partial ring (capacity C < R) in one persistent launch
+// (ring_fwd.cu): tiles cut at expert boundaries, at multiples of C and at `chunk` rows;
+// gather units copy the x rows of their tokens (MXFP8: x quantized token-major, xs its
+// scales) into x ring rows r mod C, gate/up units read them and write h into h ring rows
+// r mod C, down units read those and push to the slots. In half rows, a tile's gather is
+// ordered `lag_gather` before its gate/up units and its down units `lag` after them;
+// 1 <= lag_gather, lag <= 2 (C - chunk) + 1 keeps every wait on an earlier claim.
+struct RingFwdArgs {
+    const int32_t *offsets;  // schedule offsets [E+1]
+    const int32_t *perm;     // flat id of each sorted row
+    int32_t *tiles;          // flat tile list (count at [-4]), tiles_cap entries
+    int64_t tiles_cap;
+    int2 *dep;               // [tiles_cap] tiles one lap back over each tile's ring rows
+    int2 *umap;              // [tiles_cap * (1 + I/128 + H/256)] claim order
+    int32_t *hdr;            // [2] unit count, claim counter
+    int32_t *done_up, *done_dn, *done_g;  // [tiles_cap] per-tile completion counters
+    const void *x;           // bf16 x [T][H], or (MXFP8) E4M3 x quantized along H
+    const uint8_t *xs;       // MXFP8: x's scales [T][H/32]
+    void *xring;             // [C][H] bf16 or E4M3
+    const void *w13, *w2;
+    const uint8_t *sf_w13, *sf_w2;  // MXFP8: weight scale atoms
+    uint8_t *sf_x, *sf_h;    // MXFP8: per-tile scale atoms of x and h ([tiles_cap][K/128][512])
+    void *hring;             // [C][I] bf16 or E4M3
+    uint8_t *hring_s;        // MXFP8: [C][I/32]
+    void *preact;            // saved pre-activations (nullable)
+    bool preact_f32;
+    void *slots;             // [R][H]
+    bool out_f32;
+    int64_t T, R, C;
+    int chunk;
+    int64_t lag_gather, lag;
+    int H, I, E, K;
+    bool mx;
+    int *status;
+};
+// tile rows of the ring forward, its default lags (both) and its tile-list capacity
+int ring_tile_rows(bool mxfp8, int64_t C);
+int64_t ring_lag(bool mxfp8, int64_t C);
+int64_t ring_tiles_cap(int64_t R, int E, int64_t C, int chunk);
+cudaError_t launch_ring_forward(const RingFwdArgs &a, cudaStream_t s);
 
 // Backward G GEMM with the SwiGLU backward and router-weight gradient epilogue, per tile
 // (e, r0, r1) over sorted rows; p(r) = poff[e] + r - offsets[e] is the padded row:

@@ -11,7 +11,7 @@ const char *const kNames[KK_COUNT] = {
     "route_topk", "schedule", "build_tiles", "gather", "gemm_up_swiglu", "gemm_down_push",
     "combine", "quantize_mxfp8", "pad_offsets", "gather_bwd", "gemm_g_swiglu_bwd",
     "router_grad", "gemm_dgrad_push", "dx_reduce", "wgrad_w13", "wgrad_w2", "scale_atoms",
-    "shared_up_swiglu", "shared_down_add", "shared_backward"};
+    "shared_up_swiglu", "shared_down_add", "shared_backward", "ring_forward"};
 
 struct Rec {
     int kind;

@@ -168,10 +168,10 @@ __global__ void __launch_bounds__(SCHED_WARPS * 32)
 }
 
 // ---------------------------------------------------------------- tile lists
-// One block per pass m: for each expert, the part of its rows inside [p0, p1) with
+// One block per row window m: for each expert, the part of its rows inside [p0, p1) with
 // p0 = first + m * span and p1 = min(p0 + span, last), cut into tiles of at most `chunk`
 // rows (balanced heights, multiples of 16 but for the last), written in expert order to the
-// pass's list at list0 + m * stride. count at list[-4].
+// window's list at list0 + m * stride. count at list[-4].
 __global__ void __launch_bounds__(MAX_E)
     build_tiles(const int32_t *__restrict__ offsets, int E, int64_t first, int64_t span,
                 int64_t last, int chunk, int32_t *__restrict__ list0, int64_t stride,
@@ -296,16 +296,6 @@ int64_t tile_list_cap(int64_t rows, int E, int chunk) {
 cudaError_t launch_build_tiles(const int32_t *offsets, int E, int64_t p0, int64_t p1, int chunk,
                                int32_t *list, int64_t cap, int *status, cudaStream_t s) {
     build_tiles<<<1, MAX_E, 0, s>>>(offsets, E, p0, p1 - p0, p1, chunk, list, 0, cap, status);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_build_tiles_passes(const int32_t *offsets, int E, int64_t R, int64_t pass,
-                                      int64_t n_pass, int chunk, int32_t *list0, int64_t stride,
-                                      int64_t cap, int *status, cudaStream_t s) {
-    if (n_pass < 1) return cudaSuccess;
-    if (n_pass > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    build_tiles<<<(unsigned)n_pass, MAX_E, 0, s>>>(offsets, E, 0, pass, R, chunk, list0, stride,
-                                                   cap, status);
     return cudaGetLastError();
 }
 

@@ -81,6 +81,33 @@ MOK_DEV bool wait_bounded(uint64_t *bar, uint32_t parity, int *status, volatile 
     return true;
 }
 
+// bounded spin until the global counter *ctr reaches `target` (an acquire load, so what its
+// writers stored before raising it is visible after); gives up when another role has raised
+// `abort`, or when the status word already holds a problem (another CTA gave up: raises
+// `abort`), or after limit_ns of wall time (records MOK_ERR_TIMEOUT, raises `abort`)
+MOK_DEV bool wait_count_bounded(const int32_t *ctr, int32_t target, int *status,
+                                volatile int *abort, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 0;; ++n) {
+        int32_t v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= target) return true;
+        if ((n & 31u) == 31u) {
+            if (*abort) return false;
+            if (*(volatile int *)status != MOK_OK) {
+                *abort = 1;
+                return false;
+            }
+            if (globaltimer() - t0 > limit_ns) {
+                raise_status(status, MOK_ERR_TIMEOUT);
+                *abort = 1;
+                return false;
+            }
+        }
+        __nanosleep(64);
+    }
+}
+
 // ---------------------------------------------------------------- TMA
 MOK_DEV void prefetch_tmap(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)m) : "memory");
@@ -104,6 +131,12 @@ MOK_DEV void tma_load_5d(void *smem_dst, const CUtensorMap *m, uint64_t *bar, in
         : "memory");
 }
 
+// orders this thread's global accesses of the generic proxy (plain loads and stores) with
+// those of the async proxy (TMA copies), in both directions
+MOK_DEV void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // 1D bulk copy global -> shared (16-byte aligned, size a multiple of 16), counted on `bar`
 MOK_DEV void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
     asm volatile(
@@ -111,6 +144,26 @@ MOK_DEV void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_
             "r"(smem_u32(smem_dst)),
         "l"((uint64_t)gsrc), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// 1D bulk copy shared -> global (16-byte aligned, size a multiple of 16) in this thread's
+// current bulk group; commit_group closes the group, wait_group_read<N> waits until the
+// shared-memory sources of all but the N most recent groups have been read, wait_group<N>
+// until their writes are complete
+MOK_DEV void bulk_store(void *gdst, const void *smem_src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     (uint64_t)gdst),
+                 "r"(smem_u32(smem_src)), "r"(bytes)
+                 : "memory");
+}
+MOK_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+MOK_DEV void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+MOK_DEV void bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---------------------------------------------------------------- Cluster Launch Control

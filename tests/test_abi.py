@@ -111,7 +111,7 @@ def cfg(**kw):
     (dict(I=64), B.MOK_ERR_INVALID_ARG),          # I < 128
     (dict(minibatch=0), B.MOK_ERR_INVALID_ARG),
     (dict(ring_capacity=32), B.MOK_ERR_INVALID_ARG),  # smaller than a minibatch
-    (dict(ring_capacity=100), B.MOK_OK),              # one minibatch slot
+    (dict(ring_capacity=100), B.MOK_OK),              # a ring smaller than R
     (dict(ring_capacity=10000), B.MOK_OK),            # >= R: holds every row
     (dict(prec=5), B.MOK_ERR_INVALID_ARG),
     (dict(T=1 << 28, K=8, E=8), B.MOK_ERR_INVALID_ARG),  # R >= 2^31
@@ -158,19 +158,44 @@ def test_workspace_sizes(lib):
     assert T * H + T * I + 3 * I * H // 32 <= sm
 
 
-def test_ring_passes_per_precision(lib):
-    """A ring smaller than R: BF16 runs one minibatch per pass through floor(C/MB) slots,
-    so a capacity that is not a multiple of the minibatch leaves the rest unused; MXFP8
-    fills the whole ring per pass, so its x and h rings grow with the capacity."""
-    T, K, MB = 4096, 2, 1000  # R = 8192 routed rows
-    ws = lambda prec, C: B.mok_workspace_size(cfg(T=T, K=K, minibatch=MB, ring_capacity=C,
-                                                  prec=prec), B.MOK_WS_FORWARD)
-    assert ws(B.MOK_BF16, 2500) == ws(B.MOK_BF16, 2000)
-    assert ws(B.MOK_BF16, 3000) > ws(B.MOK_BF16, 2999)
-    assert ws(B.MOK_MXFP8, 2500) > ws(B.MOK_MXFP8, 2000)
-    # the extra 500 rows: x ring (H bytes + scales) and both h rings (I bytes + scales)
-    H, I = 256, 128
-    assert ws(B.MOK_MXFP8, 2500) - ws(B.MOK_MXFP8, 2000) >= 500 * (H + H // 32 + 2 * (I + I // 32))
+def test_partial_ring_workspace(lib):
+    """A ring of C < R rows: the x and h rings grow with C (H and I elements per row, and in
+    MXFP8 I/32 scales of h); MXFP8 also holds x quantized once per token; the unit order
+    (pairs of int32 per unit) and tile lists grow with the tiles a capacity cuts."""
+    T, K, MB, H, I, E = 4096, 2, 1000, 256, 128, 8  # R = 8192 routed rows
+    c = lambda prec, C: cfg(T=T, K=K, minibatch=MB, ring_capacity=C, prec=prec)  # noqa: E731
+    ws = lambda prec, C: B.mok_workspace_size(c(prec, C), B.MOK_WS_FORWARD)  # noqa: E731
+    full_bf16 = B.mok_workspace_size(cfg(T=T, K=K, minibatch=MB), B.MOK_WS_FORWARD)
+    assert ws(B.MOK_BF16, 2000) < full_bf16 - (T * K - 2000) * H * 2  # no [R][H] x ring
+    # 500 more ring rows, less a lap's worth of tile bookkeeping
+    assert ws(B.MOK_BF16, 2500) - ws(B.MOK_BF16, 2000) >= 500 * (H + I) * 2 - 4096
+    assert ws(B.MOK_MXFP8, 2500) - ws(B.MOK_MXFP8, 2000) >= 500 * (H + I + I // 32) - 4096
+    for prec in (B.MOK_BF16, B.MOK_MXFP8):
+        esz = 1 if prec == B.MOK_MXFP8 else 2
+        for it, width in ((B.MOK_ITEM_H_RING, I), (B.MOK_ITEM_X_RING, H)):
+            st, _, n = B.mok_workspace_item(c(prec, 2000), B.MOK_WS_FORWARD, it)
+            assert st == B.MOK_OK and n == 2000 * width * esz
+    # MXFP8: the scales of x's token rows (quantized once per token)
+    st, _, n = B.mok_workspace_item(c(B.MOK_MXFP8, 2000), B.MOK_WS_FORWARD,
+                                    B.MOK_ITEM_X_RING_SCALE)
+    assert st == B.MOK_OK and n == T * H // 32
+    # tiles: at most ceil(R / chunk) + E + laps of the ring; units per tile: one gather,
+    # I/128 gate/up and H/256 down units
+    R = T * K
+    # (a ring below two tile heights cuts tiles of half the ring)
+    for C, chunk in ((2000, 128), (200, 100), (1000, 128), (17, 8)):
+        cc = cfg(T=T, K=K, minibatch=min(MB, C), ring_capacity=C)
+        st, _, n = B.mok_workspace_item(cc, B.MOK_WS_FORWARD, B.MOK_ITEM_RING_TILES)
+        cap = -(-R // chunk) + E + -(-R // C)
+        assert st == B.MOK_OK and n == 16 + 16 * cap, (C, n, cap)
+        st, _, n = B.mok_workspace_item(cc, B.MOK_WS_FORWARD, B.MOK_ITEM_RING_ORDER)
+        assert st == B.MOK_OK and n == 8 * cap * (1 + I // 128 + H // 256)
+        st, _, n = B.mok_workspace_item(cc, B.MOK_WS_FORWARD, B.MOK_ITEM_RING_DEPS)
+        assert st == B.MOK_OK and n == 8 * cap
+    # a ring that holds every row has no unit order
+    for it in (B.MOK_ITEM_RING_TILES, B.MOK_ITEM_RING_ORDER, B.MOK_ITEM_RING_DEPS):
+        assert B.mok_workspace_item(cfg(T=T, K=K, minibatch=MB), B.MOK_WS_FORWARD,
+                                    it)[0] == B.MOK_ERR_INVALID_ARG
 
 
 def test_segment_capacity(lib):
@@ -210,6 +235,10 @@ def test_workspace_items_lie_inside_their_workspace_and_apart(lib, prec, ring):
     R, H, I, T = c.T * c.K, c.H, c.I, c.T
     for which, items in ITEMS.items():
         items = items + (MX_ITEMS[which] if prec == B.MOK_MXFP8 else [])
+        if which == B.MOK_WS_FORWARD and ring:
+            # a ring smaller than R: the unit order of its one launch
+            items = items + [B.MOK_ITEM_RING_TILES, B.MOK_ITEM_RING_ORDER,
+                             B.MOK_ITEM_RING_DEPS]
         size = B.mok_workspace_size(c, which)
         spans = []
         for it in items:
@@ -220,11 +249,11 @@ def test_workspace_items_lie_inside_their_workspace_and_apart(lib, prec, ring):
         spans.sort()
         for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
             assert a1 <= b0  # no two items overlap
-    # sizes follow the documented shapes
-    # a BF16 ring holds floor(capacity / minibatch) minibatch slots; MXFP8 the capacity
-    rows = R if ring == 0 else (100 if prec == B.MOK_MXFP8 else 64)
+    # sizes follow the documented shapes: the x and h rings hold the ring's rows
+    rows = R if ring == 0 else ring
     esz = 1 if prec == B.MOK_MXFP8 else 2
     assert B.mok_workspace_item(c, B.MOK_WS_FORWARD, B.MOK_ITEM_X_RING)[2] == rows * H * esz
+    assert B.mok_workspace_item(c, B.MOK_WS_FORWARD, B.MOK_ITEM_H_RING)[2] == rows * I * esz
     assert B.mok_workspace_item(c, B.MOK_WS_FORWARD, B.MOK_ITEM_SLOTS)[2] == R * H * 2
     assert B.mok_workspace_item(c, B.MOK_WS_BACKWARD, B.MOK_ITEM_PAD_OFFSETS)[2] == 4 * (c.E + 1)
     rpad = R + 15 * c.E

@@ -7,7 +7,9 @@ Step by step, on the intermediates the GPU left in its workspace:
     neighbour only where it does (MXFP8: codes and scales bit-exact per unflagged block);
   * y from the GPU's own h: bit-exact except flagged slot and output roundings.
 End to end, y within the stated tolerance of the oracle run from the inputs alone. Run to
-run and across ring settings y is bitwise identical. Full-size configurations are checked
+run and across ring settings y is bitwise identical: a ring smaller than the routed rows
+runs the whole forward as one persistent launch, whose device-built unit order is checked
+against its rule (every wait is on an earlier claim). Full-size configurations are checked
 on sampled tokens (outputs are token-local)."""
 import numpy as np
 import pytest
@@ -157,18 +159,84 @@ def test_fp32_storage(prec):
 
 
 @pytest.mark.parametrize("prec", [B.MOK_BF16, B.MOK_MXFP8])
-def test_ragged_multi_pass_rings(prec):
-    """Several tiles per expert, ragged tails, 1 and 2 ring slots and a full ring: every
-    ring setting gives the same bits, and the single-pass run passes every check."""
+def test_ragged_ring_settings(prec):
+    """Several tiles per expert, ragged tails, rings from one row up to every row: every
+    ring setting gives the same bits (y and the saved pre-activations), and the run through
+    a ring of every row passes every check."""
     dims = (1000, 512, 256, 16, 4)
     x, lg, w13, w2 = small_case(*dims, seed=11)
     outs = []
-    for MB, ring in ((300, 0), (300, 700), (300, 300), (128, 0), (1000, 1000)):
-        g = gpu_forward(dims, x, lg, w13, w2, prec, MB, ring)
+    for MB, ring in ((300, 0), (300, 700), (300, 300), (128, 0), (1000, 1000), (40, 40),
+                     (16, 17), (1, 1), (300, 3999)):
+        g = gpu_forward(dims, x, lg, w13, w2, prec, MB, ring, preact=True)
         outs.append(g)
     for g in outs[1:]:
-        assert same_bits(g["y_dev"][0], outs[0]["y_dev"][0])
+        assert same_bits(g["y_dev"][0], outs[0]["y_dev"][0]), g["L"].cfg.ring_capacity
+        assert same_bits(g["pre"], outs[0]["pre"]), g["L"].cfg.ring_capacity
     check_forward(outs[0], x, w13, w2, prec == B.MOK_MXFP8)
+
+
+def ring_order(L):
+    """The unit order a ring forward built on the device (host copies): tiles [n][4],
+    order [units][2], deps [n][2]."""
+    import torch
+    ws, cfg = L.ws_f, L.cfg
+    item = lambda it: workspace_item(ws, cfg, B.MOK_WS_FORWARD, it).view(  # noqa: E731
+        torch.int32).cpu().numpy()
+    t = item(B.MOK_ITEM_RING_TILES)
+    n = int(t[0])
+    tiles = t[4:4 + 4 * n].reshape(n, 4)
+    nu = n * (1 + L.I // 128 + (L.H + 255) // 256)
+    order = item(B.MOK_ITEM_RING_ORDER)[:2 * nu].reshape(nu, 2)
+    deps = item(B.MOK_ITEM_RING_DEPS)[:2 * n].reshape(n, 2)
+    return tiles, order, deps
+
+
+@pytest.mark.parametrize("prec", [B.MOK_BF16, B.MOK_MXFP8])
+@pytest.mark.parametrize("MB,ring", [(300, 700), (40, 40), (1, 1), (100, 250)])
+def test_ring_unit_order(prec, MB, ring):
+    """The device-built order of a ring forward against its rule: tiles cover the sorted
+    rows in order, each inside one expert and one lap of the ring and at most the tile
+    height; every unit appears once; a tile's gather comes before its gate/up units, which
+    come before its down units; a gather comes after the gate/up units, and a gate/up unit
+    after the down units, of the tiles one lap back whose ring rows it overwrites, and those
+    are exactly the tiles listed for it."""
+    dims = (1000, 512, 256, 16, 4)
+    T, H, I, E, K = dims
+    x, lg, w13, w2 = small_case(*dims, seed=11)
+    g = gpu_forward(dims, x, lg, w13, w2, prec, MB, ring)
+    L = g["L"]
+    tiles, order, deps = ring_order(L)
+    R, C = T * K, ring
+    offsets = L.sched.offsets[:E + 1].cpu().numpy()
+    chunk = 112 if prec == B.MOK_MXFP8 else 128
+    chunk = chunk if C >= 2 * chunk else max(1, C // 2)
+    e, r0, r1 = tiles[:, 0], tiles[:, 1], tiles[:, 2]
+    assert r0[0] == 0 and r1[-1] == R and np.array_equal(r0[1:], r1[:-1])
+    assert np.all(r1 > r0) and np.all(r1 - r0 <= chunk)
+    assert np.all(offsets[e] <= r0) and np.all(r1 <= offsets[e + 1])
+    assert np.all(r0 // C == (r1 - 1) // C)  # one lap: contiguous ring rows
+    n_up, n_dn, nt = I // 128, (H + 255) // 256, len(tiles)
+    kind, mb = order[:, 1] >> 16, order[:, 1] & 0xFFFF
+    assert np.all(kind <= 2) and np.all(mb[kind == 2] == 0)
+    codes = order[:, 0].astype(np.int64) * 192 + kind * 64 + mb
+    tt = np.arange(nt)[:, None] * 192
+    up_c, dn_c, g_c = tt + np.arange(n_up)[None], tt + 64 + np.arange(n_dn)[None], tt + 128
+    want = np.concatenate([up_c, dn_c, g_c], axis=1).reshape(-1)
+    assert np.array_equal(np.sort(codes), np.sort(want))  # every unit exactly once
+    pos = np.full(nt * 192, -1, np.int64)
+    pos[codes] = np.arange(len(codes))
+    up, dn, ga = pos[up_c], pos[dn_c], pos[g_c][:, 0]
+    assert np.all(ga < up.min(1)) and np.all(up.max(1) < dn.min(1))
+    for t in range(nt):
+        lo, hi = r0[t] - C, r1[t] - C  # the same ring rows one lap back
+        over = np.flatnonzero((r1 > lo) & (r0 < hi)) if hi > 0 else np.array([], int)
+        if len(over) == 0:
+            assert deps[t, 1] < deps[t, 0], t
+            continue
+        assert (deps[t, 0], deps[t, 1]) == (over[0], over[-1]), (t, deps[t], over)
+        assert dn[over].max() < up[t].min(), t  # h ring rows
+        assert up[over].max() < ga[t], t         # x ring rows
 
 
 @pytest.mark.parametrize("dims", [(40, 128, 128, 8, 8), (300, 256, 128, 1, 1),

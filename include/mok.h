@@ -158,13 +158,12 @@ size_t mok_workspace_size(const mok_config *cfg, int which);
  *                         row, 0) of sorted rows cut at expert boundaries, at multiples of
  *                         the ring capacity and at the tile height; int32 [4] header whose
  *                         first word is the tile count, then the tiles
- *   MOK_ITEM_RING_ORDER   forward, smaller ring: the order in which units are claimed,
- *                         int32 pairs (tile, kind << 16 | weight block), kind 0 for a
- *                         gate/up unit (one per 128 features of I), 1 for a down unit (one
- *                         per 256 features of H), 2 for the tile's gather (block 0)
- *   MOK_ITEM_RING_DEPS    forward, smaller ring: per tile, int32 pair (first, last) of the
- *                         tiles one ring lap back whose ring rows its gather and gate/up
- *                         units overwrite (last < first: none)
+ *   MOK_ITEM_RING_ORDER   forward, smaller ring: the units in the order they are claimed,
+ *                         8 int32 each: tile, kind << 16 | weight block, expert, first
+ *                         row, end row, first and last tile one ring lap back whose ring
+ *                         rows the unit's tile overwrites (last < first: none), 0. Kind 0
+ *                         is a gate/up unit (one per 128 features of I), 1 a down unit (one
+ *                         per 256 features of H), 2 the tile's gather (block 0)
  *   MOK_ITEM_SLOTS        forward: expert output of each flat id t*K + k [R][H] (bf16, or
  *                         fp32 under MOK_FLAG_FP32_STORAGE); backward: the per-slot dgrad
  *                         results, likewise
@@ -196,8 +195,7 @@ typedef enum mok_ws_item {
     MOK_ITEM_DY_Q = 10,
     MOK_ITEM_DY_SCALE = 11,
     MOK_ITEM_RING_TILES = 12,
-    MOK_ITEM_RING_ORDER = 13,
-    MOK_ITEM_RING_DEPS = 14
+    MOK_ITEM_RING_ORDER = 13
 } mok_ws_item;
 mok_status mok_workspace_item(const mok_config *cfg, int which, int item, size_t *offset,
                               size_t *bytes);

@@ -54,7 +54,6 @@ MOK_ITEM_DY_Q = 10
 MOK_ITEM_DY_SCALE = 11
 MOK_ITEM_RING_TILES = 12
 MOK_ITEM_RING_ORDER = 13
-MOK_ITEM_RING_DEPS = 14
 
 EXPORTED = [
     "mok_abi_version", "mok_status_string", "mok_check_config", "mok_segment_capacity",

@@ -89,11 +89,12 @@ struct FwdWs {
     void *slots;              // [R][H], the storage type of cfg->flags
     uint8_t *sf_w13, *sf_w2;  // MXFP8 weight scales as tensor-core atoms
     uint8_t *sf_x, *sf_h;     // MXFP8 token-tile scales as atoms, per tile of the list
-    // partial ring: each tile's dependencies, the claim order, the unit count and claim
-    // counter, per-tile completion counters
-    int2 *dep, *umap;
+    // partial ring: the unit records in claim order, the unit count and claim counter,
+    // per-tile completion counters
+    void *units;
     int32_t *hdr, *done_up, *done_dn, *done_g;
     int chunk;
+    int gather_pieces;
 };
 
 size_t carve_fwd(const mok_config *c, void *ws, FwdWs *o) {
@@ -105,6 +106,7 @@ size_t carve_fwd(const mok_config *c, void *ws, FwdWs *o) {
     const int esz = mx ? 1 : 2;
     FwdWs w;
     w.chunk = part ? ring_tile_rows(mx, c->ring_capacity) : gemm_tc_tile_rows(mx);
+    w.gather_pieces = part ? ring_gather_pieces(mx, c->ring_capacity, c->H) : 0;
     w.tiles_cap = part ? ring_tiles_cap(R, c->E, c->ring_capacity, w.chunk)
                        : tile_list_cap(R, c->E, w.chunk);
     int32_t *t = cv.take<int32_t>(16 + (size_t)w.tiles_cap * 16);
@@ -127,12 +129,12 @@ size_t carve_fwd(const mok_config *c, void *ws, FwdWs *o) {
         w.sf_x = cv.take<uint8_t>((size_t)w.tiles_cap * (c->H / 128) * 512);
         w.sf_h = cv.take<uint8_t>((size_t)w.tiles_cap * (c->I / 128) * 512);
     }
-    w.dep = w.umap = nullptr;
+    w.units = nullptr;
     w.hdr = w.done_up = w.done_dn = w.done_g = nullptr;
     if (part) {
-        const int64_t units = w.tiles_cap * (1 + c->I / 128 + (c->H + 255) / 256);
-        w.dep = cv.take<int2>((size_t)w.tiles_cap * sizeof(int2));
-        w.umap = cv.take<int2>((size_t)units * sizeof(int2));
+        const int64_t units =
+            w.tiles_cap * (w.gather_pieces + c->I / 128 + (c->H + 255) / 256);
+        w.units = cv.take<void>((size_t)units * 32);
         w.hdr = cv.take<int32_t>(16);
         w.done_up = cv.take<int32_t>((size_t)w.tiles_cap * 4);
         w.done_dn = cv.take<int32_t>((size_t)w.tiles_cap * 4);
@@ -388,14 +390,13 @@ mok_status mok_workspace_item(const mok_config *c, int which, int item, size_t *
             case MOK_ITEM_H_RING_SCALE: p = w.hring_s; n = (size_t)rr * (I / 32); break;
             case MOK_ITEM_SLOTS: p = w.slots; n = R * H * stored_bytes(c); break;
             case MOK_ITEM_RING_TILES:
-                p = w.dep ? (const void *)(w.tiles - 4) : nullptr;
+                p = w.units ? (const void *)(w.tiles - 4) : nullptr;
                 n = 16 + (size_t)w.tiles_cap * 16;
                 break;
             case MOK_ITEM_RING_ORDER:
-                p = w.umap;
-                n = (size_t)w.tiles_cap * (1 + I / 128 + (H + 255) / 256) * 8;
+                p = w.units;
+                n = (size_t)w.tiles_cap * (w.gather_pieces + I / 128 + (H + 255) / 256) * 32;
                 break;
-            case MOK_ITEM_RING_DEPS: p = w.dep; n = (size_t)w.tiles_cap * 8; break;
             default: break;
         }
     } else if (which == MOK_WS_BACKWARD || which == MOK_WS_BACKWARD_RECOMPUTE) {
@@ -534,8 +535,7 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
         ra.perm = sch->perm;
         ra.tiles = w.tiles;
         ra.tiles_cap = cap;
-        ra.dep = w.dep;
-        ra.umap = w.umap;
+        ra.units = w.units;
         ra.hdr = w.hdr;
         ra.done_up = w.done_up;
         ra.done_dn = w.done_dn;
@@ -559,8 +559,8 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
         ra.R = R;
         ra.C = c->ring_capacity;
         ra.chunk = chunk;
-        ra.lag = ring_lag(mx, c->ring_capacity);
-        ra.lag_gather = ra.lag;
+        ra.gather_pieces = w.gather_pieces;
+        ring_lags(mx, c->ring_capacity, &ra.lag_gather, &ra.lag);
         ra.H = c->H;
         ra.I = c->I;
         ra.E = c->E;

@@ -185,6 +185,10 @@ struct FwdUpT {
         int e, mb;
         int64_t r0, r1;
         tu.get(u, &e, &r0, &r1, &mb);
+        return geom_of(u / tu.n_mblocks, e, r0, r1, mb);
+    }
+    // the unit of tile t = (e, r0, r1) and weight block mb
+    MOK_DEV Geom geom_of(int64_t t, int e, int64_t r0, int64_t r1, int mb) const {
         const RingMap rm{ring.R, ring.MB, ring.n_slots};
         Geom g;
         g.ax0 = 0;
@@ -200,7 +204,7 @@ struct FwdUpT {
         const int64_t gate_row = (int64_t)e * 2 * I + mb * 128;
         g.sfa0 = (gate_row / 128) * kg * 512;
         g.sfa1 = ((gate_row + I) / 128) * kg * 512;
-        g.sfb = (u / tu.n_mblocks) * kg * 512;
+        g.sfb = t * kg * 512;
         return g;
     }
     template <class LD>
@@ -211,7 +215,8 @@ struct FwdUpT {
         tu.get(u, &e, &r0, &r1, &mb);
         const int nr = (int)(r1 - r0);
         const int n_mma = (nr + 15) & ~15;
-        const RingMap rm{ring.R, ring.MB, ring.n_slots};
+        // a tile never straddles a lap of the ring: its rows are consecutive ring rows
+        const int64_t hrow0 = RingMap{ring.R, ring.MB, ring.n_slots}(r0);
         const int i = mb * 128 + q * 32 + lane;  // gate feature; its up feature is I + i
         for (int n0 = 16 * half; n0 < n_mma; n0 += 32) {
             float d0[16], d1[16];
@@ -229,7 +234,7 @@ struct FwdUpT {
                         static_cast<uint32_t *>(preact)[r * I + i] = pack_bf16x2(d0[j], d1[j]);
                 }
                 if (hring != nullptr && !mxfp8 && n < nr)
-                    ((uint16_t *)hring)[rm(r) * I + i] = f32_to_bf16(h[j]);
+                    ((uint16_t *)hring)[(hrow0 + n) * I + i] = f32_to_bf16(h[j]);
             }
             if (hring == nullptr || !mxfp8) continue;
             // MXFP8: the warp's 32 lanes hold one 32-feature block of each of the chunk's 16
@@ -254,7 +259,8 @@ struct FwdUpT {
             }
             __syncwarp();
             if (lane < 16 && n0 + lane < nr) {
-                hring_s[rm(r0 + n0 + lane) * (I / 32) + (mb * 128 + q * 32) / 32] = (uint8_t)my_sb;
+                hring_s[(hrow0 + n0 + lane) * (I / 32) + (mb * 128 + q * 32) / 32] =
+                    (uint8_t)my_sb;
                 if (ATOMS) {
                     const int n = n0 + lane;
                     hs_atoms[((u / tu.n_mblocks) * (I / 128) + mb) * 512 + (n & 31) * 16 +
@@ -264,8 +270,8 @@ struct FwdUpT {
             const int jr = lane >> 1, hb = lane & 1;
             if (n0 + jr < nr) {
                 const uint4 v = *reinterpret_cast<const uint4 *>(stage + jr * 32 + hb * 16);
-                *reinterpret_cast<uint4 *>((uint8_t *)hring + rm(r0 + n0 + jr) * I + mb * 128 +
-                                           q * 32 + hb * 16) = v;
+                *reinterpret_cast<uint4 *>((uint8_t *)hring + (hrow0 + n0 + jr) * I +
+                                           mb * 128 + q * 32 + hb * 16) = v;
             }
             __syncwarp();
         }
@@ -293,6 +299,10 @@ struct FwdDownT {
         int e, mb;
         int64_t r0, r1;
         tu.get(u, &e, &r0, &r1, &mb);
+        return geom_of(u / tu.n_mblocks, e, r0, r1, mb);
+    }
+    // the unit of tile t = (e, r0, r1) and weight block mb
+    MOK_DEV Geom geom_of(int64_t t, int e, int64_t r0, int64_t r1, int mb) const {
         const RingMap rm{ring.R, ring.MB, ring.n_slots};
         Geom g;
         g.ax0 = 0;
@@ -309,7 +319,7 @@ struct FwdDownT {
         // when H is not a multiple of 256 the last block's A1 lies past this expert (its
         // results are discarded); keep its scale reads inside the expert
         g.sfa1 = mb * 256 + 128 < H ? (int64_t)(g.ay1 / 128) * kg * 512 : g.sfa0;
-        g.sfb = (u / tu.n_mblocks) * kg * 512;
+        g.sfb = t * kg * 512;
         return g;
     }
     template <class LD>

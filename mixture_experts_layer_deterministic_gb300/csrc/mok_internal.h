@@ -184,8 +184,8 @@ struct RingFwdArgs {
     const int32_t *perm;     // flat id of each sorted row
     int32_t *tiles;          // flat tile list (count at [-4]), tiles_cap entries
     int64_t tiles_cap;
-    int2 *dep;               // [tiles_cap] tiles one lap back over each tile's ring rows
-    int2 *umap;              // [tiles_cap * (1 + I/128 + H/256)] claim order
+    void *units;             // [tiles_cap * (gather_pieces + I/128 + H/256)] 32-byte unit
+                             // records in claim order
     int32_t *hdr;            // [2] unit count, claim counter
     int32_t *done_up, *done_dn, *done_g;  // [tiles_cap] per-tile completion counters
     const void *x;           // bf16 x [T][H], or (MXFP8) E4M3 x quantized along H
@@ -202,14 +202,17 @@ struct RingFwdArgs {
     bool out_f32;
     int64_t T, R, C;
     int chunk;
+    int gather_pieces;       // gather units per tile (ring_gather_pieces)
     int64_t lag_gather, lag;
     int H, I, E, K;
     bool mx;
     int *status;
 };
-// tile rows of the ring forward, its default lags (both) and its tile-list capacity
+// tile rows of the ring forward, its lags and its tile-list capacity
 int ring_tile_rows(bool mxfp8, int64_t C);
-int64_t ring_lag(bool mxfp8, int64_t C);
+void ring_lags(bool mxfp8, int64_t C, int64_t *lag_gather, int64_t *lag);
+int ring_stage_rows(bool mxfp8, int H);
+int ring_gather_pieces(bool mxfp8, int64_t C, int H);
 int64_t ring_tiles_cap(int64_t R, int E, int64_t C, int chunk);
 cudaError_t launch_ring_forward(const RingFwdArgs &a, cudaStream_t s);
 

@@ -41,8 +41,15 @@
 namespace mok {
 namespace {
 
-// unit code: .x = tile of the flat list, .y = (kind << 16) | weight block
 constexpr int KIND_UP = 0, KIND_DOWN = 1, KIND_GATHER = 2;
+
+// One claimable unit, all the producer needs to start it with one 32-byte read: its tile,
+// kind and weight block (code = kind << 16 | block), the tile's expert and rows, and the
+// tiles one lap back over the tile's ring rows (dep_lo > dep_hi: none).
+struct alignas(16) UnitRec {
+    int32_t t, code, e, r0;
+    int32_t r1, dep_lo, dep_hi, pad;
+};
 
 template <bool MXv>
 struct RingFwdT {
@@ -51,8 +58,7 @@ struct RingFwdT {
     static constexpr bool FUSED = true;
     FwdUpT<MXv, true> up;     // over the flat tile list; hring = the ring, RingMap{R, C, 1}
     FwdDownT<MXv> dn;
-    const int2 *umap;   // unit code of each claim index
-    const int2 *dep;    // per tile: first and last tile one lap back over its ring rows
+    const UnitRec *units;  // the unit of each claim index
     int32_t *hdr;       // [0] units, [1] next claim index
     int32_t *done_up;   // per tile: epilogue warps that finished one of its gate/up units
     int32_t *done_dn;   // likewise for its down units
@@ -65,31 +71,33 @@ struct RingFwdT {
     int64_t C;
     int row_bytes;
     int rows_per_stage; // x rows a stage holds in a gather (<= 32)
+    int gather_pieces;  // gather units per tile, of gather_rows rows each (the last ones of
+    int gather_rows;    // a short tile may be empty)
 
     MOK_DEV int64_t n_units() const { return hdr[0]; }
-    MOK_DEV bool is_copy(int64_t u) const { return (umap[u].y >> 16) == KIND_GATHER; }
-    MOK_DEV Geom geom(int64_t u) const {
-        const int2 c = umap[u];
-        const int mb = c.y & 0xFFFF;
-        if ((c.y >> 16) == KIND_DOWN) return dn.geom((int64_t)c.x * dn.tu.n_mblocks + mb);
-        return up.geom((int64_t)c.x * up.tu.n_mblocks + mb);
+    MOK_DEV bool is_copy(int64_t u) const { return (units[u].code >> 16) == KIND_GATHER; }
+    MOK_DEV Geom geom(int64_t u) const { return geom_rec(units[u]); }
+    MOK_DEV Geom geom_rec(const UnitRec &r) const {
+        const int mb = r.code & 0xFFFF;
+        if ((r.code >> 16) == KIND_DOWN) return dn.geom_of(r.t, r.e, r.r0, r.r1, mb);
+        return up.geom_of(r.t, r.e, r.r0, r.r1, mb);
     }
     template <class LD>
     MOK_DEV void epilogue(int64_t u, const LD &ld, EpiScratch &es, int q, int half,
                           int lane) const {
-        const int2 c = umap[u];
-        const int mb = c.y & 0xFFFF;
-        const bool down = (c.y >> 16) == KIND_DOWN;
+        const int4 a = *reinterpret_cast<const int4 *>(&units[u]);  // t, code
+        const int mb = a.y & 0xFFFF;
+        const bool down = (a.y >> 16) == KIND_DOWN;
         if (down)
-            dn.epilogue((int64_t)c.x * dn.tu.n_mblocks + mb, ld, es, q, half, lane);
+            dn.epilogue((int64_t)a.x * dn.tu.n_mblocks + mb, ld, es, q, half, lane);
         else
-            up.epilogue((int64_t)c.x * up.tu.n_mblocks + mb, ld, es, q, half, lane);
+            up.epilogue((int64_t)a.x * up.tu.n_mblocks + mb, ld, es, q, half, lane);
         // publish this warp's stores to the units that wait on them
         tc::fence_proxy_async_global();
         __syncwarp();
         if (lane == 0) {
             __threadfence();
-            atomicAdd(down ? &done_dn[c.x] : &done_up[c.x], 1);
+            atomicAdd(down ? &done_dn[a.x] : &done_up[a.x], 1);
         }
     }
 
@@ -102,34 +110,47 @@ struct RingFwdT {
     MOK_DEV bool wait_count(const int32_t *ctr, int32_t target, volatile int *abort) const {
         return tc::wait_count_bounded(ctr, target, status, abort, tc::WAIT_LIMIT_NS);
     }
+    MOK_DEV UnitRec load_rec(int32_t u) const {
+        const int4 *p = reinterpret_cast<const int4 *>(&units[u]);
+        const int4 a = p[0], b = p[1];
+        return UnitRec{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    }
     // the units a claimed unit depends on have finished (see the order above)
-    MOK_DEV bool wait_inputs(int32_t u, volatile int *abort) const {
-        const int2 c = umap[u];
-        const int kind = c.y >> 16;
+    MOK_DEV bool wait_inputs(const UnitRec &r, volatile int *abort) const {
+        const int kind = r.code >> 16;
         bool ok = true;
         if (kind == KIND_DOWN) {
-            ok = wait_count(&done_up[c.x], up.tu.n_mblocks * EPI_WARPS, abort);
+            ok = wait_count(&done_up[r.t], up.tu.n_mblocks * EPI_WARPS, abort);
         } else {
             // both rings: the same rows one lap back
-            const int2 d = dep[c.x];
-            if (kind == KIND_UP) ok = wait_count(&done_g[c.x], 1, abort);
+            if (kind == KIND_UP) ok = wait_count(&done_g[r.t], gather_pieces, abort);
             const int32_t *ctr = kind == KIND_UP ? done_dn : done_up;
             const int32_t target =
                 (kind == KIND_UP ? dn.tu.n_mblocks : up.tu.n_mblocks) * EPI_WARPS;
-            for (int t = d.x; ok && t <= d.y; ++t) ok = wait_count(&ctr[t], target, abort);
+            for (int t = r.dep_lo; ok && t <= r.dep_hi; ++t)
+                ok = wait_count(&ctr[t], target, abort);
         }
         tc::fence_proxy_async_global();  // the TMA reads that follow see those stores
         return ok;
     }
 
+    // the sorted rows [*q0, *q1) a gather unit copies: piece `block` of its tile's rows
+    MOK_DEV void gather_span(const UnitRec &r, int64_t *q0, int64_t *q1) const {
+        const int64_t a = r.r0 + (int64_t)(r.code & 0xFFFF) * gather_rows;
+        *q0 = a < r.r1 ? a : r.r1;
+        *q1 = a + gather_rows < r.r1 ? a + gather_rows : r.r1;
+        if (*q1 < *q0) *q1 = *q0;
+    }
     // The MMA thread's side of a gather: per stage, the rows that landed go back out to
     // their x ring rows; the stage is freed once they have been read, and the tile's
     // counter raised once every store is complete.
     MOK_DEV bool copy_out(int64_t u, uint8_t *base, uint64_t *full, uint64_t *empty, int &s,
                           uint32_t &ph, volatile int *abort) const {
         constexpr int SB = stage_bytes<MX>();
-        const int64_t t = umap[u].x;
-        const int64_t r0 = up.tu.tiles[4 * t + 1], r1 = up.tu.tiles[4 * t + 2];
+        const UnitRec r = load_rec((int32_t)u);
+        const int64_t t = r.t;
+        int64_t r0, r1;
+        gather_span(r, &r0, &r1);
         for (int64_t q0 = r0; q0 < r1; q0 += rows_per_stage) {
             if (!wait_or_abort(&full[s], ph, status, abort)) return false;
             const int m = (int)(r1 - q0 < rows_per_stage ? r1 - q0 : rows_per_stage);
@@ -152,8 +173,18 @@ struct RingFwdT {
         return true;
     }
 
+    MOK_DEV static UnitRec shfl_rec(const UnitRec &r) {
+        constexpr uint32_t FULL = 0xFFFFFFFFu;
+        return UnitRec{__shfl_sync(FULL, r.t, 0),      __shfl_sync(FULL, r.code, 0),
+                       __shfl_sync(FULL, r.e, 0),      __shfl_sync(FULL, r.r0, 0),
+                       __shfl_sync(FULL, r.r1, 0),     __shfl_sync(FULL, r.dep_lo, 0),
+                       __shfl_sync(FULL, r.dep_hi, 0), 0};
+    }
+
     // The producer, run by the whole warp: lane 0 claims, waits and issues the boxes of a
-    // GEMM unit; for a gather, lane i copies row i of each stage's rows.
+    // GEMM unit; for a gather, lane i copies row i of each stage's rows. Lane 0 claims the
+    // next unit six stages before the end of the current one and reads its record three
+    // stages before, so that both reads are in flight while the stages are issued.
     MOK_DEV void produce(Smem *sm, uint8_t *base, int lane, const CUtensorMap *tm_w13,
                          const CUtensorMap *tm_w2, const CUtensorMap *tm_x,
                          const CUtensorMap *tm_h) const {
@@ -168,14 +199,20 @@ struct RingFwdT {
         int s = 0;
         uint32_t ph = 0;
         int64_t issued = 0, j = 0;
-        int32_t u = lane == 0 ? claim() : 0;
+        int32_t u = -1;
+        UnitRec rec{};
+        if (lane == 0) {
+            u = claim();
+            if (u >= 0) rec = load_rec(u);
+        }
         u = __shfl_sync(FULL, u, 0);
+        rec = shfl_rec(rec);
         for (;;) {
             // wait for the unit's inputs, then publish it (or the end marker) to the MMA
             // thread and the epilogue warps
             int ok = 1;
             if (lane == 0) {
-                if (u >= 0) ok = wait_inputs(u, abort);
+                if (u >= 0) ok = wait_inputs(rec, abort);
                 const int slot = (int)(j % QD);
                 if (ok)
                     ok = wait_or_abort(&sm->qempty[slot], (uint32_t)(((j / QD) & 1) ^ 1),
@@ -188,17 +225,31 @@ struct RingFwdT {
             if (!__shfl_sync(FULL, ok, 0)) break;
             ++j;
             if (u < 0) break;
-            const int2 c = umap[u];
-            const int kind = c.y >> 16;
-            const int64_t t = c.x;
-            const int mb = c.y & 0xFFFF;
+            const int kind = rec.code >> 16;
+            // lane 0: the next unit, claimed at step claim_at of this unit's n_steps and its
+            // record read at step rec_at (or after the last step)
             int32_t next = -1;
+            UnitRec nrec{};
+            bool claimed = false, have = false;
+            auto prefetch = [&](int64_t k, int64_t n_steps) {
+                const int64_t claim_at = n_steps > 6 ? n_steps - 6 : 0;
+                const int64_t rec_at = n_steps > 3 ? n_steps - 3 : n_steps;
+                if (k == claim_at) {
+                    next = claim();
+                    claimed = true;
+                }
+                if (k == rec_at && next >= 0) {
+                    nrec = load_rec(next);
+                    have = true;
+                }
+            };
             if (kind == KIND_GATHER) {
-                const int64_t r0 = up.tu.tiles[4 * t + 1], r1 = up.tu.tiles[4 * t + 2];
+                int64_t r0, r1;
+                gather_span(rec, &r0, &r1);
                 const int64_t n_st = (r1 - r0 + rows_per_stage - 1) / rows_per_stage;
                 for (int64_t si = 0; si < n_st; ++si) {
                     if (lane == 0) {
-                        if (si == (n_st > 2 ? n_st - 2 : 0)) next = claim();
+                        prefetch(si, n_st);
                         ok = wait_or_abort(&sm->empty[s], ph ^ 1u, status, abort);
                     }
                     if (!__shfl_sync(FULL, ok, 0)) break;
@@ -220,16 +271,13 @@ struct RingFwdT {
                 }
             } else if (lane == 0) {
                 const bool down = kind == KIND_DOWN;
-                const Geom g = down ? dn.geom(t * dn.tu.n_mblocks + mb)
-                                    : up.geom(t * up.tu.n_mblocks + mb);
+                const Geom g = geom_rec(rec);
                 const int kblocks = (g.k_steps + 3) / 4;
-                // claim the next unit while the last two stages of this one are issued
-                const int ask_at = kblocks > 2 ? kblocks - 2 : 0;
                 const uint32_t tx = 2 * A_BYTES + B_BYTES + (MX ? 1536 : 0);
                 const uint8_t *sfa = down ? dn.sf_a : up.sf_a;
                 const uint8_t *sfb = down ? dn.sf_b : up.sf_b;
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    if (kb == ask_at) next = claim();
+                    prefetch(kb, kblocks);
                     if (!wait_or_abort(&sm->empty[s], ph ^ 1u, status, abort)) {
                         ok = 0;
                         break;
@@ -258,12 +306,16 @@ struct RingFwdT {
                     }
                 }
             }
-            // lane 0 holds the loop state of a GEMM unit: broadcast it
+            // a unit without steps (an empty gather piece) claims its successor here
+            if (lane == 0 && ok && !claimed) next = claim();
+            if (lane == 0 && next >= 0 && !have) nrec = load_rec(next);
+            // lane 0 holds the loop state of a GEMM unit and the next unit: broadcast them
             if (!__shfl_sync(FULL, ok, 0)) break;
             s = __shfl_sync(FULL, s, 0);
             ph = __shfl_sync(FULL, ph, 0);
             issued = __shfl_sync(FULL, issued, 0);
             u = __shfl_sync(FULL, next, 0);
+            rec = shfl_rec(nrec);
         }
         // do not leave while copies this CTA issued may still be landing
         if (lane == 0) {
@@ -330,14 +382,15 @@ MOK_DEV int64_t upper_bound_key(const int32_t *tiles, int64_t n, int64_t add, in
     return lo;
 }
 
-// One block: the flat tile list (count at tiles[-4]), each tile's ring dependencies, the
-// claim order of all units, zeroed counters and the unit count. Group keys in half rows:
+// One block: the flat tile list (count at tiles[-4]), the unit records in claim order,
+// zeroed counters and the unit count. Group keys in half rows:
 // gather 2 r0 - g, gate/up 2 r0, down 2 r0 + d; on equal keys gather, then gate/up, then
 // down.
 __global__ void __launch_bounds__(BUILD_THREADS)
     build_ring_units(const int32_t *__restrict__ offsets, int E, int64_t C, int chunk,
-                     int64_t g, int64_t d, int n_up, int n_dn, int32_t *__restrict__ tiles,
-                     int64_t cap, int2 *__restrict__ dep, int2 *__restrict__ umap,
+                     int64_t g, int64_t d, int n_g, int n_up, int n_dn,
+                     int32_t *__restrict__ tiles,
+                     int64_t cap, UnitRec *__restrict__ units,
                      int32_t *__restrict__ hdr, int32_t *__restrict__ done_up,
                      int32_t *__restrict__ done_dn, int32_t *__restrict__ done_g,
                      int *status) {
@@ -395,24 +448,30 @@ __global__ void __launch_bounds__(BUILD_THREADS)
             dp.x = (int)(upper_bound_key(tiles, t, 0, 2 * lo) - 1);
             dp.y = (int)(upper_bound_key(tiles, t, 0, 2 * (r1 - 1 - C)) - 1);
         }
-        dep[t] = dp;
+        const int e = tiles[4 * t];
+        const UnitRec base{(int)t, 0, e, (int)r0, (int)r1, dp.x, dp.y, 0};
+        auto put = [&](int64_t o, int kind, int m) {
+            UnitRec r = base;
+            r.code = (kind << 16) | m;
+            units[o] = r;
+        };
         // gather group (key 2 r0 - g): gate/up and down groups with smaller keys before it
         const int64_t kg = 2 * r0 - g, ku = 2 * r0, kd = 2 * r0 + d;
-        int64_t o = t + at_most(0, kg - 1) * n_up + at_most(d, kg - 1) * n_dn;
-        umap[o] = make_int2((int)t, KIND_GATHER << 16);
+        int64_t o = t * n_g + at_most(0, kg - 1) * n_up + at_most(d, kg - 1) * n_dn;
+        for (int m = 0; m < n_g; ++m) put(o + m, KIND_GATHER, m);
         // gate/up group: gathers at or below its key, down groups below it
-        o = at_most(-g, ku) + t * n_up + at_most(d, ku - 1) * n_dn;
-        for (int m = 0; m < n_up; ++m) umap[o + m] = make_int2((int)t, (KIND_UP << 16) | m);
+        o = at_most(-g, ku) * n_g + t * n_up + at_most(d, ku - 1) * n_dn;
+        for (int m = 0; m < n_up; ++m) put(o + m, KIND_UP, m);
         // down group: gathers and gate/up groups at or below its key
-        o = at_most(-g, kd) + at_most(0, kd) * n_up + t * n_dn;
-        for (int m = 0; m < n_dn; ++m) umap[o + m] = make_int2((int)t, (KIND_DOWN << 16) | m);
+        o = at_most(-g, kd) * n_g + at_most(0, kd) * n_up + t * n_dn;
+        for (int m = 0; m < n_dn; ++m) put(o + m, KIND_DOWN, m);
         done_up[t] = 0;
         done_dn[t] = 0;
         done_g[t] = 0;
     }
     if (threadIdx.x == 0) {
         tiles[-4] = (int32_t)nt;
-        hdr[0] = (int32_t)(nt * (1 + n_up + n_dn));
+        hdr[0] = (int32_t)(nt * (n_g + n_up + n_dn));
         hdr[1] = 0;
     }
 }
@@ -478,8 +537,7 @@ cudaError_t launch_ring(const RingFwdArgs &a, cudaStream_t s) {
     p.dn = FwdDownT<MX>{TileUnits{a.tiles, a.tiles_cap, nmb_dn}, a.H, a.I, ring, a.perm,
                         a.slots, a.out_f32, a.status, MX ? a.sf_w2 : nullptr,
                         MX ? a.sf_h : nullptr, false};
-    p.umap = a.umap;
-    p.dep = a.dep;
+    p.units = static_cast<const UnitRec *>(a.units);
     p.hdr = a.hdr;
     p.done_up = a.done_up;
     p.done_dn = a.done_dn;
@@ -491,8 +549,9 @@ cudaError_t launch_ring(const RingFwdArgs &a, cudaStream_t s) {
     p.xring = static_cast<uint8_t *>(a.xring);
     p.C = a.C;
     p.row_bytes = a.H * (MX ? 1 : 2);
-    const int stage_rows = (2 * A_BYTES + B_BYTES) / p.row_bytes;
-    p.rows_per_stage = stage_rows < 32 ? stage_rows : 32;
+    p.rows_per_stage = ring_stage_rows(MX, a.H);
+    p.gather_pieces = a.gather_pieces;
+    p.gather_rows = (a.chunk + a.gather_pieces - 1) / a.gather_pieces;
     tc_ring_kernel<P><<<device_sm_count(), NTHREADS, SMEM, s>>>(m_w13, m_w2, m_x, m_h, p);
     return cudaGetLastError();
 }
@@ -505,9 +564,31 @@ int ring_tile_rows(bool mxfp8, int64_t C) {
     return C / 2 > 1 ? (int)(C / 2) : 1;
 }
 
-int64_t ring_lag(bool mxfp8, int64_t C) {
+// The lags, in half rows, of a tile's gather before its gate/up units (g) and of its down
+// units after them (d): g = C and d = 3C/2, both capped at 2 (C - chunk) + 1. On the
+// 65536-token imbalanced workload (2960-row ring) a sweep of g, d over C/4 .. 1.9 C found
+// this pair fastest; d = g = C was 2.4% slower, d = C/4 nearly twice as slow.
+void ring_lags(bool mxfp8, int64_t C, int64_t *g, int64_t *d) {
     const int64_t most = 2 * (C - ring_tile_rows(mxfp8, C)) + 1;
-    return C < most ? C : most;
+    *g = C < most ? C : most;
+    *d = C + C / 2 < most ? C + C / 2 : most;
+}
+
+// x rows of one stage in a gather: a stage's operand bytes (48 KB) over a row's, at most
+// one per lane
+int ring_stage_rows(bool mxfp8, int H) {
+    const int n = (2 * A_BYTES + B_BYTES) / (H * (mxfp8 ? 1 : 2));
+    return n < 32 ? n : 32;
+}
+
+// gather units per tile: pieces of at most four stages (one fill of the stage ring), so a
+// tile's rows are gathered by several CTAs at once. A tile's gate/up units wait for all of
+// its pieces; on the 65536-token imbalanced workload a whole-tile gather took 28 us and
+// gated 61% of the gate/up units' waits.
+int ring_gather_pieces(bool mxfp8, int64_t C, int H) {
+    const int per = 4 * ring_stage_rows(mxfp8, H);
+    const int chunk = ring_tile_rows(mxfp8, C);
+    return (chunk + per - 1) / per;
 }
 
 int64_t ring_tiles_cap(int64_t R, int E, int64_t C, int chunk) {
@@ -520,8 +601,10 @@ cudaError_t launch_ring_forward(const RingFwdArgs &a, cudaStream_t s) {
     if (a.R < 1 || a.C < 1 || a.E > BUILD_THREADS) return cudaErrorInvalidValue;
     const int nmb_up = a.I / 128, nmb_dn = (a.H + 255) / 256;
     build_ring_units<<<1, BUILD_THREADS, 0, s>>>(a.offsets, a.E, a.C, a.chunk, a.lag_gather,
-                                                 a.lag, nmb_up, nmb_dn, a.tiles, a.tiles_cap,
-                                                 a.dep, a.umap, a.hdr, a.done_up, a.done_dn,
+                                                 a.lag, a.gather_pieces, nmb_up, nmb_dn,
+                                                 a.tiles, a.tiles_cap,
+                                                 static_cast<UnitRec *>(a.units), a.hdr,
+                                                 a.done_up, a.done_dn,
                                                  a.done_g, a.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (a.mx) {

@@ -179,8 +179,8 @@ def test_partial_ring_workspace(lib):
     st, _, n = B.mok_workspace_item(c(B.MOK_MXFP8, 2000), B.MOK_WS_FORWARD,
                                     B.MOK_ITEM_X_RING_SCALE)
     assert st == B.MOK_OK and n == T * H // 32
-    # tiles: at most ceil(R / chunk) + E + laps of the ring; units per tile: one gather,
-    # I/128 gate/up and H/256 down units
+    # tiles: at most ceil(R / chunk) + E + laps of the ring; units per tile (32-byte
+    # records): the gather's pieces, I/128 gate/up and H/256 down units
     R = T * K
     # (a ring below two tile heights cuts tiles of half the ring)
     for C, chunk in ((2000, 128), (200, 100), (1000, 128), (17, 8)):
@@ -189,11 +189,10 @@ def test_partial_ring_workspace(lib):
         cap = -(-R // chunk) + E + -(-R // C)
         assert st == B.MOK_OK and n == 16 + 16 * cap, (C, n, cap)
         st, _, n = B.mok_workspace_item(cc, B.MOK_WS_FORWARD, B.MOK_ITEM_RING_ORDER)
-        assert st == B.MOK_OK and n == 8 * cap * (1 + I // 128 + H // 256)
-        st, _, n = B.mok_workspace_item(cc, B.MOK_WS_FORWARD, B.MOK_ITEM_RING_DEPS)
-        assert st == B.MOK_OK and n == 8 * cap
+        n_g = -(-chunk // (4 * min(32, 49152 // (H * 2))))  # gather pieces of 4 stages
+        assert st == B.MOK_OK and n == 32 * cap * (n_g + I // 128 + H // 256)
     # a ring that holds every row has no unit order
-    for it in (B.MOK_ITEM_RING_TILES, B.MOK_ITEM_RING_ORDER, B.MOK_ITEM_RING_DEPS):
+    for it in (B.MOK_ITEM_RING_TILES, B.MOK_ITEM_RING_ORDER):
         assert B.mok_workspace_item(cfg(T=T, K=K, minibatch=MB), B.MOK_WS_FORWARD,
                                     it)[0] == B.MOK_ERR_INVALID_ARG
 
@@ -237,8 +236,7 @@ def test_workspace_items_lie_inside_their_workspace_and_apart(lib, prec, ring):
         items = items + (MX_ITEMS[which] if prec == B.MOK_MXFP8 else [])
         if which == B.MOK_WS_FORWARD and ring:
             # a ring smaller than R: the unit order of its one launch
-            items = items + [B.MOK_ITEM_RING_TILES, B.MOK_ITEM_RING_ORDER,
-                             B.MOK_ITEM_RING_DEPS]
+            items = items + [B.MOK_ITEM_RING_TILES, B.MOK_ITEM_RING_ORDER]
         size = B.mok_workspace_size(c, which)
         spans = []
         for it in items:

@@ -176,9 +176,25 @@ def test_ragged_ring_settings(prec):
     check_forward(outs[0], x, w13, w2, prec == B.MOK_MXFP8)
 
 
-def ring_order(L):
+@pytest.mark.parametrize("prec", [B.MOK_BF16, B.MOK_MXFP8])
+@pytest.mark.parametrize("dims,rings", [((300, 4096, 128, 4, 2), (150, 400)),
+                                        ((3000, 4096, 128, 64, 4), (300, 1000))])
+def test_ring_gather_pieces(prec, dims, rings):
+    """A wide x row (H = 4096) makes each tile's gather several units of a few rows each,
+    the last ones of a short tile empty (the second shape has more empty pieces than the
+    GPU has SMs): smaller rings give the bits of the ring that holds every row."""
+    x, lg, w13, w2 = small_case(*dims, seed=21)
+    outs = [gpu_forward(dims, x, lg, w13, w2, prec, min(64, r or 64), r, preact=True)
+            for r in (0,) + rings]
+    for g in outs[1:]:
+        assert same_bits(g["y_dev"][0], outs[0]["y_dev"][0])
+        assert same_bits(g["pre"], outs[0]["pre"])
+    check_forward(outs[0], x, w13, w2, prec == B.MOK_MXFP8)
+
+
+def ring_order(L, n_g):
     """The unit order a ring forward built on the device (host copies): tiles [n][4],
-    order [units][2], deps [n][2]."""
+    unit records [units][8] in claim order (n_g gather units per tile)."""
     import torch
     ws, cfg = L.ws_f, L.cfg
     item = lambda it: workspace_item(ws, cfg, B.MOK_WS_FORWARD, it).view(  # noqa: E731
@@ -186,48 +202,67 @@ def ring_order(L):
     t = item(B.MOK_ITEM_RING_TILES)
     n = int(t[0])
     tiles = t[4:4 + 4 * n].reshape(n, 4)
-    nu = n * (1 + L.I // 128 + (L.H + 255) // 256)
-    order = item(B.MOK_ITEM_RING_ORDER)[:2 * nu].reshape(nu, 2)
-    deps = item(B.MOK_ITEM_RING_DEPS)[:2 * n].reshape(n, 2)
-    return tiles, order, deps
+    nu = n * (n_g + L.I // 128 + (L.H + 255) // 256)
+    return tiles, item(B.MOK_ITEM_RING_ORDER)[:8 * nu].reshape(nu, 8)
+
+
+def ring_gather_pieces(prec, H, chunk):
+    """Gather units per tile: pieces of at most four stages of rows, a stage holding
+    48 KB of x rows (at most 32)."""
+    esz = 1 if prec == B.MOK_MXFP8 else 2
+    per = 4 * min(32, 49152 // (H * esz))
+    return -(-chunk // per)
 
 
 @pytest.mark.parametrize("prec", [B.MOK_BF16, B.MOK_MXFP8])
-@pytest.mark.parametrize("MB,ring", [(300, 700), (40, 40), (1, 1), (100, 250)])
-def test_ring_unit_order(prec, MB, ring):
+@pytest.mark.parametrize("dims,MB,ring", [((1000, 512, 256, 16, 4), 300, 700),
+                                          ((1000, 512, 256, 16, 4), 40, 40),
+                                          ((1000, 512, 256, 16, 4), 1, 1),
+                                          ((1000, 512, 256, 16, 4), 100, 250),
+                                          ((300, 4096, 128, 4, 2), 150, 150),
+                                          ((300, 4096, 128, 4, 2), 64, 400)])
+def test_ring_unit_order(prec, dims, MB, ring):
     """The device-built order of a ring forward against its rule: tiles cover the sorted
     rows in order, each inside one expert and one lap of the ring and at most the tile
     height; every unit appears once; a tile's gather comes before its gate/up units, which
     come before its down units; a gather comes after the gate/up units, and a gate/up unit
     after the down units, of the tiles one lap back whose ring rows it overwrites, and those
     are exactly the tiles listed for it."""
-    dims = (1000, 512, 256, 16, 4)
     T, H, I, E, K = dims
     x, lg, w13, w2 = small_case(*dims, seed=11)
     g = gpu_forward(dims, x, lg, w13, w2, prec, MB, ring)
     L = g["L"]
-    tiles, order, deps = ring_order(L)
     R, C = T * K, ring
     offsets = L.sched.offsets[:E + 1].cpu().numpy()
     chunk = 112 if prec == B.MOK_MXFP8 else 128
     chunk = chunk if C >= 2 * chunk else max(1, C // 2)
+    n_g = ring_gather_pieces(prec, H, chunk)
+    tiles, rec = ring_order(L, n_g)
     e, r0, r1 = tiles[:, 0], tiles[:, 1], tiles[:, 2]
     assert r0[0] == 0 and r1[-1] == R and np.array_equal(r0[1:], r1[:-1])
     assert np.all(r1 > r0) and np.all(r1 - r0 <= chunk)
     assert np.all(offsets[e] <= r0) and np.all(r1 <= offsets[e + 1])
     assert np.all(r0 // C == (r1 - 1) // C)  # one lap: contiguous ring rows
     n_up, n_dn, nt = I // 128, (H + 255) // 256, len(tiles)
-    kind, mb = order[:, 1] >> 16, order[:, 1] & 0xFFFF
-    assert np.all(kind <= 2) and np.all(mb[kind == 2] == 0)
-    codes = order[:, 0].astype(np.int64) * 192 + kind * 64 + mb
+    kind, mb = rec[:, 1] >> 16, rec[:, 1] & 0xFFFF
+    assert np.all(kind <= 2) and np.all(mb[kind == 2] < n_g)
+    # each record repeats its tile's expert and rows
+    tr = rec[:, 0]
+    assert np.array_equal(rec[:, 2:5], tiles[tr][:, :3]) and np.all(rec[:, 7] == 0)
+    codes = tr.astype(np.int64) * 192 + kind * 64 + mb
     tt = np.arange(nt)[:, None] * 192
-    up_c, dn_c, g_c = tt + np.arange(n_up)[None], tt + 64 + np.arange(n_dn)[None], tt + 128
+    up_c, dn_c = tt + np.arange(n_up)[None], tt + 64 + np.arange(n_dn)[None]
+    g_c = tt + 128 + np.arange(n_g)[None]
     want = np.concatenate([up_c, dn_c, g_c], axis=1).reshape(-1)
     assert np.array_equal(np.sort(codes), np.sort(want))  # every unit exactly once
     pos = np.full(nt * 192, -1, np.int64)
     pos[codes] = np.arange(len(codes))
-    up, dn, ga = pos[up_c], pos[dn_c], pos[g_c][:, 0]
-    assert np.all(ga < up.min(1)) and np.all(up.max(1) < dn.min(1))
+    up, dn, gp = pos[up_c], pos[dn_c], pos[g_c]
+    ga = gp.min(1)  # a tile's first gather piece
+    assert np.all(gp.max(1) < up.min(1)) and np.all(up.max(1) < dn.min(1))
+    deps = np.zeros((nt, 2), np.int64)
+    deps[tr] = rec[:, 5:7]
+    assert np.array_equal(rec[:, 5:7], deps[tr])  # the same for every unit of a tile
     for t in range(nt):
         lo, hi = r0[t] - C, r1[t] - C  # the same ring rows one lap back
         over = np.flatnonzero((r1 > lo) & (r0 < hi)) if hi > 0 else np.array([], int)

@@ -63,6 +63,11 @@ CONFIGS = {
     "fwd_bf16_e32": LayerConfig(name="fwd_bf16_e32", T=1024, seed=0, prec="bf16",
                                 passes="fwd", **{**_BIG, "E": 32}),
     "bwd_bf16": LayerConfig(name="bwd_bf16", T=8192, seed=2, prec="bf16", passes="bwd", **_BIG),
+    # counter-capture case of the ring forward: the imbalanced routing and ring with 64
+    # experts and 8192 tokens (about 4 GB held on the device)
+    "ring_bf16_e64": LayerConfig(name="ring_bf16_e64", T=8192, seed=3, prec="bf16",
+                                 passes="fwd", **{**_BIG, "E": 64, "zipf_bias": True,
+                                                  "ring_capacity": 2960}),
     "imbalanced_bf16": LayerConfig(name="imbalanced_bf16", T=65536, seed=3, prec="bf16",
                                    passes="fwd", **{**_BIG, "zipf_bias": True,
                                                     "ring_capacity": 2960}),

@@ -142,8 +142,9 @@ struct RingFwdT {
         if (*q1 < *q0) *q1 = *q0;
     }
     // The MMA thread's side of a gather: per stage, the rows that landed go back out to
-    // their x ring rows; the stage is freed once they have been read, and the tile's
-    // counter raised once every store is complete.
+    // their x ring rows. A stage is freed once its stores have read it, one stage behind (the
+    // stores of two stages in flight), and the tile's counter raised once every store is
+    // complete.
     MOK_DEV bool copy_out(int64_t u, uint8_t *base, uint64_t *full, uint64_t *empty, int &s,
                           uint32_t &ph, volatile int *abort) const {
         constexpr int SB = stage_bytes<MX>();
@@ -151,20 +152,32 @@ struct RingFwdT {
         const int64_t t = r.t;
         int64_t r0, r1;
         gather_span(r, &r0, &r1);
+        int prev = -1;  // the stage of the newest committed stores but one
         for (int64_t q0 = r0; q0 < r1; q0 += rows_per_stage) {
-            if (!wait_or_abort(&full[s], ph, status, abort)) return false;
+            if (!wait_or_abort(&full[s], ph, status, abort)) {
+                tc::bulk_wait<0>();
+                return false;
+            }
             const int m = (int)(r1 - q0 < rows_per_stage ? r1 - q0 : rows_per_stage);
             const uint8_t *st = base + s * SB;
+            const int64_t x0 = q0 % C;  // a tile stays within a lap: consecutive ring rows
             for (int i = 0; i < m; ++i)
-                tc::bulk_store(xring + ((q0 + i) % C) * row_bytes, st + i * row_bytes,
+                tc::bulk_store(xring + (x0 + i) * row_bytes, st + i * row_bytes,
                                (uint32_t)row_bytes);
             tc::bulk_commit();
-            tc::bulk_wait_read<0>();
-            tc::mbar_arrive(&empty[s]);
+            if (prev >= 0) {
+                tc::bulk_wait_read<1>();
+                tc::mbar_arrive(&empty[prev]);
+            }
+            prev = s;
             if (++s == STAGES) {
                 s = 0;
                 ph ^= 1u;
             }
+        }
+        if (prev >= 0) {
+            tc::bulk_wait_read<0>();
+            tc::mbar_arrive(&empty[prev]);
         }
         tc::bulk_wait<0>();
         tc::fence_proxy_async_global();

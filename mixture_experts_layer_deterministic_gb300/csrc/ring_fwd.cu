@@ -42,6 +42,7 @@ namespace mok {
 namespace {
 
 constexpr int KIND_UP = 0, KIND_DOWN = 1, KIND_GATHER = 2;
+constexpr int REC_AHEAD = 64;  // unit records a producer asks L2 for ahead of its claim
 
 // One claimable unit, all the producer needs to start it with one 32-byte read: its tile,
 // kind and weight block (code = kind << 16 | block), the tile's expert and rows, and the
@@ -254,6 +255,10 @@ struct RingFwdT {
                 if (k == rec_at && next >= 0) {
                     nrec = load_rec(next);
                     have = true;
+                    // records are claimed in order by every SM in turn: warm L2 with the
+                    // one 64 claims ahead
+                    if (next + REC_AHEAD < hdr[0])
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(units + next + REC_AHEAD));
                 }
             };
             if (kind == KIND_GATHER) {

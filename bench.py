@@ -168,6 +168,46 @@ def algorithmic(kind, c, prec="bf16", save_pre=True, used=None):
     return flops.get(kind), hbm.get(kind)
 
 
+# Of those bytes, the ones each kernel kind writes (the rest it reads).
+def algorithmic_writes(kind, c, prec="bf16", save_pre=True, used=None):
+    R, H, I, T, K = c.R, c.H, c.I, c.T, c.K
+    E = c.E if used is None else used
+    mx = prec == "mxfp8"
+    ob = (1.0 + 1.0 / 32) if mx else 2.0
+    row_h, row_i = 2.0 * R * H, 2.0 * R * I
+    pre = 2.0 * R * 2 * I if save_pre else 0.0
+    dA_q = (1.0 + 1.0 / 32) * R * 2 * I if mx else 0.0
+    w = {"gemm_up_swiglu": ob * R * I + pre, "gemm_down_push": row_h,
+         "gemm_g_swiglu_bwd": 3 * row_i + dA_q, "gemm_dgrad_push": row_h,
+         "wgrad_w13": 2.0 * E * 2 * I * H, "wgrad_w2": 2.0 * E * H * I,
+         "ring_forward": pre + row_h, "quantize_mxfp8": ob * T * H, "gather": ob * R * H,
+         "combine": 2.0 * T * H, "dx_reduce": 2.0 * T * H, "route_topk": 8.0 * T * K,
+         "gather_bwd": 2 * row_h + (ob * R * H if mx else 0.0)}
+    return w.get(kind)
+
+
+def measure_bandwidth(torch, dev):
+    """HBM bandwidth of plain torch kernels on this GPU, now: write-only (memset of 2 GiB),
+    read-only (a sum over 2 GiB), best of 5 each."""
+    x = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev)
+    out = {}
+    for name, fn in (("write_only_gbs", lambda: x.zero_()), ("read_only_gbs", lambda: x.sum())):
+        fn()
+        best = float("inf")
+        for _ in range(5):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b))
+        out[name] = x.numel() * 2 / (best * 1e-3) / 1e9
+    del x
+    out["how"] = "torch zero_() and sum() over 2 GiB of bf16, best of 5, CUDA events"
+    return out
+
+
 def roofline_of(kind, c, launches, avg_ms, pk, prec="bf16", save_pre=True, used=None):
     """Both fractions of the kernel's roofline (tensor: algorithmic FLOPs over the measured
     launch time against the dense peak of its operand type; hbm: algorithmic bytes over the
@@ -187,6 +227,16 @@ def roofline_of(kind, c, launches, avg_ms, pk, prec="bf16", save_pre=True, used=
            "tflops": flops / s / 1e12, "gbs": nbytes / s / 1e9,
            "frac_tensor": flops / s / 1e12 / tpk, "frac_hbm": nbytes / s / 1e9 / pk["hbm"],
            "tensor_peak": tpk, "tensor_peak_kind": tkind}
+    # a second HBM floor that prices written bytes at the measured write-only bandwidth and
+    # read bytes at the read-only one (each term, and the copy-bandwidth one, is a lower
+    # bound on the kernel's DRAM time); reported beside the official fraction
+    wr = algorithmic_writes(kind, c, prec, save_pre, used)
+    if wr is not None and pk.get("hbm_write") and pk.get("hbm_read"):
+        wr /= launches
+        floor = max(wr / (pk["hbm_write"] * 1e9), (nbytes - wr) / (pk["hbm_read"] * 1e9),
+                    nbytes / (pk["hbm"] * 1e9))
+        out["hbm_rw_floor_ms"] = floor * 1e3
+        out["frac_hbm_rw"] = floor / s
     if flops / (tpk * 1e12) >= nbytes / (pk["hbm"] * 1e9):
         out.update(bound="tensor", achieved=out["tflops"], peak=tpk, unit="TFLOP/s",
                    frac=out["frac_tensor"], peak_kind=tkind, algorithmic_per_launch=flops)
@@ -395,6 +445,8 @@ def run_mok(args):
 
     # per-kernel timing on the launching stream over a second timed region
     pk = peaks()
+    bw = measure_bandwidth(torch, dev)
+    pk["hbm_write"], pk["hbm_read"] = bw["write_only_gbs"], bw["read_only_gbs"]
     B.check(B.mok_profile_enable(1))
     timed(step, args.steps)
     prof = B.mok_profile_read()
@@ -648,7 +700,8 @@ def run_mok(args):
         "config": {"workload": "fwd+bwd BF16, %d experts, H=%d, I=%d, top-%d, T=%d" % (
                        E, H, I, K, T),
                    "T": T, "H": H, "I": I, "E": E, "K": K, "minibatch": cfg.minibatch,
-                   "ring_capacity": "all rows", "l2": "inputs larger than L2 (%.1f GB of "
+                   "ring_capacity": cfg.ring_capacity or "all rows",
+                   "l2": "inputs larger than L2 (%.1f GB of "
                    "expert weights read per step)" % (3.0 * E * H * I * 2 / 1e9),
                    "parallelism": "replicas" if world > 1
                    else "single GPU"},
@@ -661,6 +714,7 @@ def run_mok(args):
                         for kk, vv in v.items()} for k, v in kernels.items()},
         "clocks": clk,
         "peaks": pk,
+        "bandwidth": bw,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(cfg, cpu_inputs, budget_s=args.cpu_seconds)

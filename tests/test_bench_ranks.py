@@ -65,3 +65,26 @@ def test_reference_arm_prints_only_on_rank_zero(monkeypatch):
     with redirect_stdout(buf):
         bench.run_reference(args)
     assert buf.getvalue() == ""
+
+
+def test_write_aware_floor_is_a_lower_bound_of_each_kind():
+    """The write-aware HBM floor is the largest of three lower bounds: written bytes at the
+    write-only rate, read bytes at the read-only rate, all bytes at the copy rate; written
+    bytes never exceed a kernel's algorithmic bytes."""
+    import bench
+    from workloads import CONFIGS
+    c = CONFIGS["fwd_bf16"]
+    pk = dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="test", hbm_write=4000.0,
+              hbm_read=7000.0)
+    for k in ("gemm_up_swiglu", "gemm_down_push", "gemm_g_swiglu_bwd", "gemm_dgrad_push",
+              "wgrad_w13", "wgrad_w2", "gather", "combine", "gather_bwd", "dx_reduce"):
+        _, nbytes = bench.algorithmic(k, c)
+        wr = bench.algorithmic_writes(k, c)
+        assert 0 < wr <= nbytes, k
+        r = bench.roofline_of(k, c, 1, 1.0, pk)
+        floor = r["hbm_rw_floor_ms"] * 1e-3
+        assert floor >= nbytes / 6800e9 - 1e-12 and floor >= wr / 4000e9 - 1e-12
+        assert abs(r["frac_hbm_rw"] - floor / 1e-3) < 1e-9
+    # dW13 is bound by its bf16 writes: 8.6 GB at the write-only rate
+    r = bench.roofline_of("wgrad_w13", c, 1, 1.0, pk)
+    assert abs(r["hbm_rw_floor_ms"] - 2.0 * c.E * 2 * c.I * c.H / 4000e9 * 1e3) < 1e-9

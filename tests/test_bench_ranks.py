@@ -68,14 +68,13 @@ def test_reference_arm_prints_only_on_rank_zero(monkeypatch):
 
 
 def test_write_aware_floor_is_a_lower_bound_of_each_kind():
-    """The write-aware HBM floor is the largest of three lower bounds: written bytes at the
-    write-only rate, read bytes at the read-only rate, all bytes at the copy rate; written
-    bytes never exceed a kernel's algorithmic bytes."""
+    """The write-aware HBM floor is the larger of two lower bounds: written bytes at the
+    write-only rate, all bytes at the copy rate; written bytes never exceed a kernel's
+    algorithmic bytes."""
     import bench
     from workloads import CONFIGS
     c = CONFIGS["fwd_bf16"]
-    pk = dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="test", hbm_write=4000.0,
-              hbm_read=7000.0)
+    pk = dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="test", hbm_write=4000.0)
     for k in ("gemm_up_swiglu", "gemm_down_push", "gemm_g_swiglu_bwd", "gemm_dgrad_push",
               "wgrad_w13", "wgrad_w2", "gather", "combine", "gather_bwd", "dx_reduce"):
         _, nbytes = bench.algorithmic(k, c)

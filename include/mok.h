@@ -71,6 +71,15 @@ typedef enum mok_precision {
  * or MXFP8 layer and checked against a reference within a tolerance). Every accumulation
  * is fp32 either way; the flag changes what is stored and what later steps read. */
 #define MOK_FLAG_FP32_STORAGE 1u
+/* Which kernel computes the weight gradients (dw13, dw2 and the shared expert's); the
+ * results are the same bit for bit ([alphalab] section 五: warp specialization and PTX).
+ * By default, pairs of SMs that share their operand tiles (the two-SM tensor-core MMA) take
+ * them when an expert averages at least 512 rows (T*K/E; T for the shared expert), where
+ * the MMAs and their operand feed bound the time, and one SM per output tile below that,
+ * where writing dW bounds it. MOK_FLAG_WGRAD_ONE_SM forces one SM per tile,
+ * MOK_FLAG_WGRAD_SM_PAIRS forces pairs; setting both is MOK_ERR_INVALID_ARG. */
+#define MOK_FLAG_WGRAD_ONE_SM 2u
+#define MOK_FLAG_WGRAD_SM_PAIRS 4u
 
 typedef enum mok_workspace_kind {
     MOK_WS_SCHEDULE = 0,

@@ -23,6 +23,9 @@ bool prof_on();
 // the entry points' device check (compute capability 10.3) and the device's status word
 mok_status current_device_status_word(int **status);
 
+// devices a process may use (per-device caches are arrays of this size)
+constexpr int MAX_DEV = 64;
+
 // streaming multiprocessors of the current device (queried once per device), for sizing
 // grids in whole waves; 1 if the query fails
 int device_sm_count();
@@ -274,5 +277,12 @@ cudaError_t launch_gemm_dgrad_tc(const GemmDgradArgs &a, int E, int64_t rpad_cap
 cudaError_t launch_wgrad_tc(const int32_t *counts, const int32_t *poff, const uint16_t *A,
                             const uint16_t *Bm, void *out, bool out_f32, int E, int M, int N,
                             int64_t rows_a, int64_t rows_b, int *status, cudaStream_t s);
+// the same on pairs of SMs sharing their operand tiles (tcgen05 cta_group::2), bit for bit
+// equal; needs N % 128 == 0 (wgrad_pair_supported)
+bool wgrad_pair_supported(int M, int N);
+cudaError_t launch_wgrad_pair_tc(const int32_t *counts, const int32_t *poff, const uint16_t *A,
+                                 const uint16_t *Bm, void *out, bool out_f32, int E, int M,
+                                 int N, int64_t rows_a, int64_t rows_b, int *status,
+                                 cudaStream_t s);
 
 }  // namespace mok

@@ -19,12 +19,11 @@ namespace {
 static __device__ __align__(256) int32_t
     g_noalloc_sched_scratch[MOK_NOALLOC_SCHEDULE_SCRATCH_BYTES / sizeof(int32_t)];
 
-constexpr int MAX_DEV = 64;
 // Device address of the scratch array, per device. In host code the array's name is only
 // a host-side stand-in, never a device address, so the address is looked up once per
 // device (with that device current) and cached here. Host threads may make their first
 // call on a device at the same time: the cache is atomic, and both store the same address.
-std::atomic<int32_t *> g_scratch_dev[MAX_DEV];
+std::atomic<int32_t *> g_scratch_dev[mok::MAX_DEV];
 
 }  // namespace
 
@@ -46,7 +45,7 @@ extern "C" mok_status mok_build_schedule_noalloc(const mok_config *cfg,
     if (mok::schedule_ws_bytes(R, cfg->E) > MOK_NOALLOC_SCHEDULE_SCRATCH_BYTES)
         return MOK_ERR_WORKSPACE;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) return MOK_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= mok::MAX_DEV) return MOK_ERR_CUDA;
     int32_t *scratch = g_scratch_dev[dev].load(std::memory_order_acquire);
     if (scratch == nullptr) {
         void *p = nullptr;

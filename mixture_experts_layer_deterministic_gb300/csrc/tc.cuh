@@ -263,6 +263,117 @@ MOK_DEV void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 }
 MOK_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ---------------------------------------------------------------- pairs of SMs
+// A cluster of two CTAs on two SMs shares one MMA (cta_group::2): the CTA of rank 0 issues
+// it, each CTA supplies half of each operand from its own shared memory and receives its
+// half of the accumulator in its own TMEM. Every tcgen05 instruction of such a kernel
+// names cta_group::2; allocation, relinquish and deallocation are issued by one warp of
+// each CTA of the pair.
+MOK_DEV uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+MOK_DEV uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+MOK_DEV uint32_t cluster_count_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// the shared::cluster address of this CTA's shared variable `p` in the CTA of rank `rank`
+MOK_DEV uint32_t cluster_addr(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+// arrive on an mbarrier given by its shared::cluster address (this CTA's or another's)
+MOK_DEV void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                     bar_cluster)
+                 : "memory");
+}
+MOK_DEV bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], "
+        "%2;\nselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// wait_bounded for a barrier that other CTAs of the cluster arrive on
+MOK_DEV bool wait_bounded_cluster(uint64_t *bar, uint32_t parity, int *status,
+                                  volatile int *abort, uint64_t limit_ns) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    uint32_t n = 0;
+    while (!mbar_try_wait_cluster(bar, parity)) {
+        if ((++n & 255u) == 0) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > limit_ns) {
+                raise_status(status, MOK_ERR_TIMEOUT);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+    return true;
+}
+// every thread of both CTAs (non-aligned forms: threads may arrive from diverged paths)
+MOK_DEV void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\nbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// 2D tile load into this CTA's shared memory whose transaction bytes complete on an
+// mbarrier of either CTA of the pair (its shared::cluster address)
+MOK_DEV void tma_load_2d_pair(void *smem_dst, const CUtensorMap *m, uint32_t bar_cluster,
+                              int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"((uint64_t)m), "r"(bar_cluster), "r"(x), "r"(y)
+        : "memory");
+}
+MOK_DEV void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+MOK_DEV void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+MOK_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                 "r"(ncols)
+                 : "memory");
+}
+// D (+)= A B^T over the pair: M = 256 (rows 0-127 from rank 0's A, 128-255 from rank 1's),
+// N columns (the first N/2 from rank 0's B, the rest from rank 1's); each CTA's TMEM gets
+// its 128 rows x N. Issued by one thread of rank 0; descriptors name this CTA's tiles, the
+// peer's sit at the same shared-memory offsets.
+MOK_DEV void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                          uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// arrive once on the mbarrier at `bar`'s offset in each CTA of `cta_mask` when every
+// tcgen05 operation issued so far by this thread is done
+MOK_DEV void mma_commit_pair(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile whose 8-row groups
 // of 128-byte rows are `sbo` bytes apart (1024 for densely stacked rows) and whose

@@ -119,6 +119,25 @@ def test_recompute_matches_saved_preact(dims, MB):
         assert same_bits(a[0][k], b[0][k]), k
 
 
+@pytest.mark.parametrize("dims,skew,flags", [
+    ((600, 256, 256, 16, 4), 0.0, B.MOK_FLAG_WGRAD_SM_PAIRS),
+    ((333, 384, 128, 24, 3), 3.0, B.MOK_FLAG_WGRAD_SM_PAIRS),
+    ((1000, 256, 384, 8, 2), 4.0, B.MOK_FLAG_WGRAD_SM_PAIRS),
+    ((40, 128, 128, 4, 2), 0.0, B.MOK_FLAG_WGRAD_SM_PAIRS),
+    ((2048, 256, 128, 4, 2), 0.0, 0)])
+def test_wgrad_pairs_equal_one_sm(dims, skew, flags):
+    """The weight gradients on SM pairs equal the one-SM kernel's bit for bit: the same
+    fixed-order dot products. The shapes give 256-wide and 128-wide last M blocks (in the
+    latter rank 1's A half lies wholly past the end), 128-column N blocks, empty experts and
+    experts with 3x the rows of an even split; the last shape (1024 rows per expert) takes
+    the pairs by default, the others are forced onto them."""
+    x, lg, w13, w2, dy = small_case(*dims, seed=dims[0] + 1, skew=skew)
+    a, _, _, _ = gpu_backward(dims, x, lg, w13, w2, dy, 100, flags=flags)
+    b, _, _, _ = gpu_backward(dims, x, lg, w13, w2, dy, 100, flags=B.MOK_FLAG_WGRAD_ONE_SM)
+    for k in a[0]:
+        assert same_bits(a[0][k], b[0][k]), k
+
+
 def test_fp32_storage_backward():
     """Under MOK_FLAG_FP32_STORAGE (fp32 A, dx slots, dx and dW) the outputs stay within
     tolerance of the oracle's fp32-storage backward."""
@@ -150,6 +169,12 @@ def test_full_size_bwd():
     for k in outs[0]:
         assert same_bits(outs[0][k], rc[0][k]), ("recompute", k)
     del rc
+    # the weight gradients on SM pairs equal those of the one-SM kernel (the default here)
+    pr, _, _, _ = gpu_backward(dims, d["x"], d["logits"], d["w13"], d["w2"], d["dy"],
+                               cfg.minibatch, flags=B.MOK_FLAG_WGRAD_SM_PAIRS)
+    for k in outs[0]:
+        assert same_bits(outs[0][k], pr[0][k]), ("SM pairs", k)
+    del pr
     # token-local outputs on 128 sampled tokens; weight gradients of 8 sampled experts,
     # the hottest among them
     toks = sample_tokens(cfg.T, 128, seed=cfg.seed)

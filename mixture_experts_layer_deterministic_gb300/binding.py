@@ -16,8 +16,8 @@ MOK_ABI_VERSION = 2
 
 # mok_config.flags
 MOK_FLAG_FP32_STORAGE = 1
-MOK_FLAG_WGRAD_ONE_SM = 2
-MOK_FLAG_WGRAD_SM_PAIRS = 4
+MOK_FLAG_ONE_SM_GEMMS = 2
+MOK_FLAG_SM_PAIR_GEMMS = 4
 
 # mok_status
 MOK_OK = 0

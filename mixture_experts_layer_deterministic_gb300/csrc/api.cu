@@ -50,12 +50,19 @@ size_t stored_bytes(const mok_config *c) { return f32_storage(c) ? 4 : 2; }
 // from 640 rows per expert up, 2-16% slower at 320 rows and below, where the dW writes
 // bound both kernels and the pair's two epilogues must both finish before its next MMA.
 constexpr int64_t WGRAD_PAIR_ROWS = 512;
+
+// the BF16 dx GEMM on SM pairs unless one SM per tile is forced (the MXFP8 dx GEMM runs on
+// one SM: its scale atoms are cut per 128-row tile)
+bool dgrad_pairs(const mok_config *c, bool mx) {
+    return !mx && (c->flags & MOK_FLAG_ONE_SM_GEMMS) == 0;
+}
 cudaError_t launch_wgrad(const mok_config *c, int64_t avg_rows, const int32_t *counts,
                          const int32_t *poff, const uint16_t *A, const uint16_t *Bm, void *out,
                          int E, int M, int N, int64_t rows_a, int64_t rows_b, int *status,
                          cudaStream_t s) {
-    const bool pairs = (c->flags & MOK_FLAG_WGRAD_SM_PAIRS) != 0 ||
-                       ((c->flags & MOK_FLAG_WGRAD_ONE_SM) == 0 && avg_rows >= WGRAD_PAIR_ROWS);
+    const bool pairs = (c->flags & MOK_FLAG_SM_PAIR_GEMMS) != 0 ||
+                       ((c->flags & MOK_FLAG_ONE_SM_GEMMS) == 0 &&
+                        avg_rows >= WGRAD_PAIR_ROWS);
     if (pairs && wgrad_pair_supported(M, N))
         return launch_wgrad_pair_tc(counts, poff, A, Bm, out, f32_storage(c), E, M, N, rows_a,
                                     rows_b, status, s);
@@ -373,9 +380,10 @@ mok_status mok_check_config(const mok_config *c) {
         c->ring_capacity < c->minibatch)
         return MOK_ERR_INVALID_ARG;
     if (c->prec != MOK_BF16 && c->prec != MOK_MXFP8) return MOK_ERR_INVALID_ARG;
-    const uint32_t known = MOK_FLAG_FP32_STORAGE | MOK_FLAG_WGRAD_ONE_SM | MOK_FLAG_WGRAD_SM_PAIRS;
+    const uint32_t known =
+        MOK_FLAG_FP32_STORAGE | MOK_FLAG_ONE_SM_GEMMS | MOK_FLAG_SM_PAIR_GEMMS;
     if ((c->flags & ~known) != 0) return MOK_ERR_INVALID_ARG;
-    if ((c->flags & MOK_FLAG_WGRAD_ONE_SM) && (c->flags & MOK_FLAG_WGRAD_SM_PAIRS))
+    if ((c->flags & MOK_FLAG_ONE_SM_GEMMS) && (c->flags & MOK_FLAG_SM_PAIR_GEMMS))
         return MOK_ERR_INVALID_ARG;
     return MOK_OK;
 }
@@ -717,7 +725,16 @@ mok_status backward_impl(const mok_config *c, const void *x, const mok_schedule 
         dg.dA_q = w.dA_q;
         dg.sf_dA = w.sf_dA;
     }
-    MOK_LAUNCH(KK_GEMM_DGRAD, 1, launch_gemm_dgrad_tc(dg, E, w.rpad_cap, stream));
+    if (dgrad_pairs(c, mx)) {
+        // the pair form's tiles hold up to 256 rows; the list is rebuilt in place (nothing
+        // after this GEMM reads it)
+        MOK_LAUNCH(KK_TILES, 1,
+                   launch_build_tiles(sch->offsets, E, 0, R, PAIR_DGRAD_TILE_ROWS, w.tiles,
+                                      w.tiles_cap, status, stream));
+        MOK_LAUNCH(KK_GEMM_DGRAD, 1, launch_gemm_dgrad_pair_tc(dg, E, w.rpad_cap, stream));
+    } else {
+        MOK_LAUNCH(KK_GEMM_DGRAD, 1, launch_gemm_dgrad_tc(dg, E, w.rpad_cap, stream));
+    }
     MOK_LAUNCH(KK_DX_REDUCE, 1,
                launch_combine(w.dx_slots, nullptr, c->T, K, H, dx, f32_storage(c), stream));
     // dW13[e] is [2I][H]: rows j (N) x contiguous c (M)
@@ -919,7 +936,14 @@ mok_status shared_backward_impl(const mok_config *c, const void *x, const void *
             MOK_LAUNCH(KK_SCALE_ATOMS, 1,
                        launch_scale_atoms_tiles_padded(w.tiles, w.tiles_cap, w.dA_s, w.offsets,
                                                        w.poff, 2 * I, w.sf_dA, stream));
-        MOK_LAUNCH(KK_SHARED_BWD, 1, launch_gemm_dgrad_tc(dg, 1, w.tpad, stream));
+        if (dgrad_pairs(c, mx)) {
+            MOK_LAUNCH(KK_TILES, 1,
+                       launch_build_tiles(w.offsets, 1, 0, T, PAIR_DGRAD_TILE_ROWS, w.tiles,
+                                          w.tiles_cap, status, stream));
+            MOK_LAUNCH(KK_SHARED_BWD, 1, launch_gemm_dgrad_pair_tc(dg, 1, w.tpad, stream));
+        } else {
+            MOK_LAUNCH(KK_SHARED_BWD, 1, launch_gemm_dgrad_tc(dg, 1, w.tpad, stream));
+        }
     }
     // the weight gradients' K runs over the padded rows: x and dy rows past T read zeros
     MOK_LAUNCH(KK_SHARED_BWD, 2,

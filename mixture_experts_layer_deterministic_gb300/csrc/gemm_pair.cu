@@ -1,0 +1,494 @@
+// gemm_pair.cu -- expert GEMMs on pairs of SMs that share their operand tiles.
+//
+// [alphalab] "Mixture-of-Kittens" (alphalab.site), section 一: the backward computes the
+// expert gradients dW13 = dA^T x and dW2 = (w*h)^T dy per expert over its routed rows, and
+// reverse-dispatches dx = dA W13; section 五: warp specialization and PTX.
+// [arex] "Cursor 放出 MoK" (arex-research.com), section "pull 代替 push": the backward's dx
+// rows are pushed back to their (token, k) slots.
+//
+// A cluster of two CTAs on two SMs computes one output tile with the two-SM MMA (tcgen05
+// cta_group::2, M = 256): rank r holds rows [128r, +128) of the tile's 256 M rows as its A
+// half and loads half of the tile's N columns as its B half; the MMA gives each CTA its 128
+// M rows against all N columns. Per 64-element K block a SM loads 128 A rows and N/2 B rows
+// for 128 x N outputs, where the one-SM engine loads 256 A rows and N B rows (N <= 128) for
+// 256 x N: at N = 256 the operand feed per FLOP falls by a third, the weight tiles' by half.
+// Each output element is the same fixed-order fp32 dot product as in the one-SM engine (K
+// in 16-element steps from the first), so the results are the same bit for bit.
+//
+// Per CTA, 320 threads:
+//   warp 0     TMA producer (both ranks): its own A half (two 64-wide MN-major boxes) and B
+//              half into a 6-stage ring; the copies of both ranks complete on rank 0's full
+//              barrier of the stage, whose expected bytes rank 0 sets
+//   warp 1     TMEM owner (both ranks: the pair allocates together); on rank 0 the MMA
+//              issuer, whose commits arrive on the stage-free and accumulator-full barriers
+//              of both CTAs
+//   warps 2-9  epilogue (both ranks): TMEM -> the policy's epilogue; each warp then arrives
+//              on rank 0's accumulator-free barrier
+// Two accumulator sets of 256 columns alternate between consecutive units. The clusters
+// take the units in a static stride; consecutive units share operand tiles, so the clusters
+// running at one time share them in L2.
+//
+// Problems (policies):
+//   WgradPair  A, B MN-major over an expert's padded rows -> dW (output rows on M)
+//   DgradPair  A = W13^T (MN-major), B = dA (K-major) in token tiles of <= 256 rows
+//              -> reverse-dispatch scatter to the dx slots (features on M)
+//
+// Every wait is bounded (2 s); a CTA that gives up records MOK_ERR_TIMEOUT and leaves its
+// loops, and both CTAs meet at a cluster barrier before TMEM is freed.
+#include "gemm_tc_core.cuh"
+
+namespace mok {
+namespace {
+
+constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_BOX = 64 * 128;           // one 64 x 64 bf16 MN-major box
+constexpr int PAIR_A = 2 * PAIR_BOX;         // A half: 128 M rows x 64 K
+constexpr int PAIR_STAGE = 4 * PAIR_BOX;     // A half + B half (<= 128 rows of 128 bytes)
+constexpr uint32_t PAIR_SET_COLS = 256;      // TMEM columns of one accumulator set
+constexpr int PAIR_TILE = 256;               // max N of a unit (token rows or dW columns)
+
+struct PairSmem {
+    uint64_t full[PAIR_STAGES];   // rank 0: both CTAs' copies of the stage have landed
+    uint64_t empty[PAIR_STAGES];  // each CTA: the MMAs that read the stage are done
+    uint64_t tmem_full[2];        // each CTA: accumulator set b holds a finished unit
+    uint64_t tmem_empty[2];       // rank 0: both CTAs' epilogues have drained set b
+    uint32_t tmem_base;
+    int abort;
+    int32_t col[EPI_WARPS][PAIR_TILE];  // per epilogue warp: one index per column of a unit
+};
+
+constexpr int PAIR_SMEM = PAIR_STAGES * PAIR_STAGE + 1024 + (int)sizeof(PairSmem);
+static_assert(PAIR_SMEM <= 232448, "pair kernel exceeds the shared memory of a CTA");
+
+// One unit as one CTA of the pair loads and multiplies it.
+struct PairGeom {
+    int32_t ax, ay;  // A half: MN-major boxes at (ax, ay + k) and (ax + 64, ay + k)
+    int32_t bx, by;  // B half: MN-major, nbox boxes at (bx + 64j, by + k); K-major, one
+                     // 128-row box at (k, by) of which the MMA reads n_mma / 2 rows
+    int nbox;
+    int n_mma;       // N of the pair MMA: multiple of 16 (K-major B), of 128 (MN-major B)
+    int k_steps;     // 16-element K steps; 0 leaves the accumulators unwritten
+};
+
+// weight gradient: out[e][n][m] = sum over the expert's padded rows p of A[p][m] B[p][n];
+// a unit is (expert, 256-column block nb, 256-row block mb)
+struct WgradPair {
+    static constexpr bool B_MN = true;
+    const int32_t *counts, *poff;
+    void *out;     // [E][N][M], fp32 if out_f32, else bf16
+    bool out_f32;
+    int E, M, N;
+    int nmb, nnb;  // ceil(M / 256), ceil(N / 256) (N is a multiple of 128)
+    int *status;
+
+    MOK_DEV int64_t n_units() const { return (int64_t)E * nmb * nnb; }
+    MOK_DEV void get(int64_t u, int *e, int *mb, int *nb) const {
+        *e = (int)(u / ((int64_t)nmb * nnb));
+        const int rest = (int)(u % ((int64_t)nmb * nnb));
+        *nb = rest / nmb;
+        *mb = rest % nmb;
+    }
+    MOK_DEV int cols(int nb) const { return N - nb * 256 < 256 ? N - nb * 256 : 256; }
+    MOK_DEV PairGeom geom(int64_t u, uint32_t rank) const {
+        int e, mb, nb;
+        get(u, &e, &mb, &nb);
+        PairGeom g;
+        g.n_mma = cols(nb);
+        const int half = g.n_mma / 2;  // 64 or 128 columns of B per CTA
+        g.ax = mb * 256 + (int)rank * 128;
+        g.ay = poff[e];
+        g.bx = nb * 256 + (int)rank * half;
+        g.by = poff[e];
+        g.nbox = half / 64;
+        g.k_steps = ((counts[e] + 15) & ~15) / 16;
+        return g;
+    }
+    template <class LD>
+    MOK_DEV void epilogue(int64_t u, uint32_t rank, const LD &ld, int32_t *, int q, int hw,
+                          int lane) const {
+        int e, mb, nb;
+        get(u, &e, &mb, &nb);
+        const int nn = cols(nb);
+        const bool any = counts[e] > 0;
+        const int m = mb * 256 + (int)rank * 128 + q * 32 + lane;
+        const bool mok = m < M;
+        const int64_t row0 = (int64_t)e * N + (int64_t)nb * 256;
+        // 32 columns per TMEM round trip (nn is a multiple of 128)
+        for (int n0 = 32 * hw; n0 < nn; n0 += 64) {
+            float v0[16], v1[16];
+            ld(n0, v0, v1);
+            if (mok) {
+                const int64_t o = (row0 + n0) * M + m;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    st_val(out, o + (int64_t)j * M, any ? v0[j] : 0.f, out_f32);
+                    st_val(out, o + (int64_t)(16 + j) * M, any ? v1[j] : 0.f, out_f32);
+                }
+            }
+        }
+    }
+};
+
+// reverse dispatch: dx_slots[perm[r]][c] (+)= sum_j dA[r][j] W13[e][j][c] over the rows r
+// of a token tile (e, r0, r1) of <= 256 rows; a unit is (tile, 256-feature block mb)
+struct DgradPair {
+    static constexpr bool B_MN = false;
+    TileUnits tu;
+    int H, I;
+    const int32_t *offsets, *poff, *perm;
+    void *dx_slots;   // [rows][H], fp32 if out_f32, else bf16
+    bool out_f32;
+    bool accumulate;  // add into the output rows (the shared expert adds into dx)
+    int *status;
+
+    MOK_DEV int64_t n_units() const { return tu.count(); }
+    MOK_DEV PairGeom geom(int64_t u, uint32_t rank) const {
+        int e, mb;
+        int64_t r0, r1;
+        tu.get(u, &e, &r0, &r1, &mb);
+        PairGeom g;
+        g.n_mma = (int)((r1 - r0 + 15) & ~15);
+        g.ax = mb * 256 + (int)rank * 128;
+        g.ay = e * 2 * I;
+        g.bx = 0;
+        g.by = (int32_t)(poff[e] + (r0 - offsets[e])) + (int)rank * (g.n_mma / 2);
+        g.nbox = 1;
+        g.k_steps = 2 * I / 16;
+        return g;
+    }
+    template <class LD>
+    MOK_DEV void epilogue(int64_t u, uint32_t rank, const LD &ld, int32_t *fcol, int q,
+                          int hw, int lane) const {
+        int e, mb;
+        int64_t r0, r1;
+        tu.get(u, &e, &r0, &r1, &mb);
+        const int nr = (int)(r1 - r0);
+        const int n_mma = (nr + 15) & ~15;
+        const int c = mb * 256 + (int)rank * 128 + q * 32 + lane;
+        const bool cok = c < H;
+        for (int n = lane; n < nr; n += 32) fcol[n] = perm[r0 + n];
+        __syncwarp();
+        for (int n0 = 32 * hw; n0 < n_mma; n0 += 64) {
+            float v[32];
+            ld(n0, *reinterpret_cast<float(*)[16]>(v), *reinterpret_cast<float(*)[16]>(v + 16));
+            if (accumulate && cok) {
+                // every load of the chunk before any store: a store to one row may alias
+                // the next row's load, which would otherwise serialise the round trips
+                float a[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const bool ok = n0 + j < nr;
+                    const int64_t o = (int64_t)fcol[ok ? n0 + j : 0] * H + c;
+                    a[j] = !ok ? 0.f
+                           : out_f32 ? static_cast<const float *>(dx_slots)[o]
+                                     : bf16_to_f32(static_cast<const uint16_t *>(dx_slots)[o]);
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] += a[j];
+            }
+            if (cok) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (n0 + j < nr) st_val(dx_slots, (int64_t)fcol[n0 + j] * H + c, v[j], out_f32);
+            }
+        }
+        __syncwarp();
+    }
+};
+
+MOK_DEV bool pair_wait(uint64_t *bar, uint32_t parity, int *status, volatile int *abort) {
+    return tc::wait_bounded_cluster(bar, parity, status, abort, tc::WAIT_LIMIT_NS);
+}
+
+// bounded drain of a barrier phase on the way out (no status: the loops already ended)
+MOK_DEV void pair_drain(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = tc::globaltimer();
+    while (!tc::mbar_try_wait_cluster(bar, parity) && tc::globaltimer() - t0 < 100000000ull) {
+    }
+}
+
+template <class P>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    tc_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB, const P p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the same offset in both CTAs: the MMA finds the peer's tiles where this CTA has its own
+    uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    PairSmem *sm = (PairSmem *)(base + PAIR_STAGES * PAIR_STAGE);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = tc::cluster_rank();
+    const int64_t cid = tc::cluster_id_x(), ncl = tc::cluster_count_x();
+    const int64_t n_units = p.n_units();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PAIR_STAGES; ++s) {
+            tc::mbar_init(&sm->full[s], 1);
+            tc::mbar_init(&sm->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&sm->tmem_full[b], 1);
+            tc::mbar_init(&sm->tmem_empty[b], 2 * EPI_WARPS);
+        }
+        sm->abort = 0;
+        tc::fence_mbar_init();
+        tc::prefetch_tmap(&tmA);
+        tc::prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc_pair(&sm->tmem_base, TMEM_COLS);
+        tc::tmem_relinquish_pair();
+    }
+    // both CTAs' barriers exist and TMEM is allocated before either CTA touches the other
+    tc::tc_fence_before();
+    tc::cluster_sync();
+    tc::tc_fence_after();
+    const uint32_t tmem = sm->tmem_base;
+    volatile int *abort = &sm->abort;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (tc::elect_one()) {
+            const uint32_t full0 = tc::cluster_addr(&sm->full[0], 0);  // rank 0's full[0]
+            int s = 0;
+            uint32_t ph = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int64_t u = cid; u < n_units && ok; u += ncl) {
+                const PairGeom g = p.geom(u, rank);
+                const uint32_t tx = PAIR_A + (P::B_MN ? g.nbox * PAIR_BOX : 2 * PAIR_BOX);
+                const int kblocks = (g.k_steps + 3) / 4;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!pair_wait(&sm->empty[s], ph ^ 1u, p.status, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    if (rank == 0) tc::mbar_arrive_expect_tx(&sm->full[s], 2 * tx);
+                    const uint32_t fb = full0 + (uint32_t)s * 8u;
+                    uint8_t *st = base + s * PAIR_STAGE;
+                    const int k0 = kb * BK;
+                    tc::tma_load_2d_pair(st, &tmA, fb, g.ax, g.ay + k0);
+                    tc::tma_load_2d_pair(st + PAIR_BOX, &tmA, fb, g.ax + 64, g.ay + k0);
+                    if (P::B_MN) {
+                        for (int j = 0; j < g.nbox; ++j)
+                            tc::tma_load_2d_pair(st + PAIR_A + j * PAIR_BOX, &tmB, fb,
+                                                 g.bx + 64 * j, g.by + k0);
+                    } else {
+                        tc::tma_load_2d_pair(st + PAIR_A, &tmB, fb, k0, g.by);
+                    }
+                    ++issued;
+                    if (++s == PAIR_STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            // do not leave while copies may still be landing: the MMAs that read the last
+            // stages have finished (bounded)
+            for (int q = 0; q < PAIR_STAGES && q < issued; ++q) {
+                if (--s < 0) {
+                    s = PAIR_STAGES - 1;
+                    ph ^= 1u;
+                }
+                pair_drain(&sm->empty[s], ph);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (rank 0)
+        if (rank == 0 && tc::elect_one()) {
+            int s = 0;
+            uint32_t ph = 0;
+            int64_t a = 0;  // units so far: unit a uses accumulator set a % 2
+            bool ok = true;
+            for (int64_t u = cid; u < n_units && ok; u += ncl, ++a) {
+                const PairGeom g = p.geom(u, 0);
+                const uint32_t idesc = tc::idesc_bf16(256, g.n_mma, true, P::B_MN);
+                const int ab = (int)(a & 1);
+                const uint32_t use = (uint32_t)((a >> 1) & 1);
+                if (!pair_wait(&sm->tmem_empty[ab], use ^ 1u, p.status, abort)) break;
+                tc::tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)ab * PAIR_SET_COLS;
+                const int kblocks = (g.k_steps + 3) / 4;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!pair_wait(&sm->full[s], ph, p.status, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    const uint32_t sa = tc::smem_u32(base + s * PAIR_STAGE);
+                    const uint32_t sb = sa + PAIR_A;
+                    const int steps = g.k_steps - kb * 4 < 4 ? g.k_steps - kb * 4 : 4;
+                    for (int kk = 0; kk < steps; ++kk) {
+                        // MN-major: 16 K rows = 2 groups of eight 128-byte rows, the two
+                        // 64-wide blocks of a half PAIR_BOX apart; K-major: 16 elements =
+                        // 32 bytes along the swizzled row
+                        const uint64_t da = tc::sdesc_sw128(sa + kk * 2048, PAIR_BOX, 1024);
+                        const uint64_t db =
+                            P::B_MN ? tc::sdesc_sw128(sb + kk * 2048, PAIR_BOX, 1024)
+                                    : tc::sdesc_sw128(sb + kk * 32, 16, 1024);
+                        tc::mma_f16_pair(d, da, db, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc::mma_commit_pair(&sm->empty[s], 3);  // frees the stage in both CTAs
+                    if (++s == PAIR_STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc::mma_commit_pair(&sm->tmem_full[ab], 3);
+            }
+            // do not free TMEM under MMAs still in flight (bounded)
+            if (a > 0) {
+                const int lb = (int)((a - 1) & 1);
+                pair_drain(&sm->tmem_full[lb], (uint32_t)(((a - 1) >> 1) & 1));
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;            // TMEM lane quadrant this warp may access
+        const int hw = (warp - 2) >> 2;    // which alternate 32-column chunks it takes
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const uint32_t empty0 = tc::cluster_addr(&sm->tmem_empty[0], 0);
+        int32_t *col = sm->col[warp - 2];
+        uint32_t c = 0;  // TMEM address of the current unit's accumulator, this quadrant
+        auto ld = [&](int n0, float (&v0)[16], float (&v1)[16]) {
+            tc::tmem_ld16(c + n0, v0);
+            tc::tmem_ld16(c + n0 + 16, v1);
+            tc::tmem_ld_wait();
+        };
+        int64_t a = 0;
+        for (int64_t u = cid; u < n_units; u += ncl, ++a) {
+            const int ab = (int)(a & 1);
+            if (!pair_wait(&sm->tmem_full[ab], (uint32_t)((a >> 1) & 1), p.status, abort))
+                break;
+            tc::tc_fence_after();
+            c = tmem + lane_base + (uint32_t)ab * PAIR_SET_COLS;
+            p.epilogue(u, rank, ld, col, q, hw, lane);
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive_cluster(empty0 + (uint32_t)ab * 8u);
+        }
+    }
+
+    // no MMA, copy or arrival of either CTA targets the other past this point
+    tc::tc_fence_before();
+    tc::cluster_sync();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc_pair(tmem, TMEM_COLS);
+    }
+}
+
+// clusters of two that fit on a device at once, per device and kernel; queried once per
+// device outside stream capture (a launch under capture before then uses one cluster per
+// two SMs)
+template <class P>
+cudaError_t pair_clusters(int *out, cudaStream_t s) {
+    static std::atomic<int> cache[MAX_DEV];
+    static std::atomic<uint64_t> attr_set[2] = {{0}, {0}};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= MAX_DEV) return cudaErrorInvalidDevice;
+    const uint64_t bit = 1ull << (dev & 63);
+    if ((attr_set[dev >> 6].load(std::memory_order_acquire) & bit) == 0) {
+        e = cudaFuncSetAttribute(tc_pair_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PAIR_SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set[dev >> 6].fetch_or(bit, std::memory_order_acq_rel);
+    }
+    int nc = cache[dev].load(std::memory_order_acquire);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (nc == 0 && cudaStreamIsCapturing(s, &cs) == cudaSuccess &&
+        cs != cudaStreamCaptureStatusNone) {
+        *out = device_sm_count() / 2 > 0 ? device_sm_count() / 2 : 1;
+        return cudaSuccess;
+    }
+    if (nc == 0) {
+        cudaLaunchConfig_t q = {};
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        q.gridDim = dim3((unsigned)(2 * device_sm_count()), 1, 1);
+        q.blockDim = dim3(NTHREADS, 1, 1);
+        q.dynamicSmemBytes = PAIR_SMEM;
+        q.attrs = at;
+        q.numAttrs = 1;
+        // where the query fails, one cluster per two SMs: clusters that do not fit wait for
+        // a free pair and take their units then (the static stride still covers them all)
+        if (cudaOccupancyMaxActiveClusters(&nc, tc_pair_kernel<P>, &q) != cudaSuccess ||
+            nc < 1) {
+            (void)cudaGetLastError();
+            nc = device_sm_count() / 2 > 0 ? device_sm_count() / 2 : 1;
+        }
+        cache[dev].store(nc, std::memory_order_release);
+    }
+    *out = nc;
+    return cudaSuccess;
+}
+
+// units_cap: a host-side bound on the device-side unit count
+template <class P>
+cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const P &p,
+                        int64_t units_cap, cudaStream_t s) {
+    if (units_cap < 1) return cudaSuccess;
+    if (units_cap > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    int nc = 0;
+    cudaError_t e = pair_clusters<P>(&nc, s);
+    if (e != cudaSuccess) return e;
+    const int64_t clusters = units_cap < nc ? units_cap : nc;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+    cfg.blockDim = dim3(NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = PAIR_SMEM;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, tc_pair_kernel<P>, ma, mb, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool wgrad_pair_supported(int M, int N) { return M > 0 && N > 0 && N % 128 == 0; }
+
+// out [E][N][M] = per expert sum over padded rows of A[p][m] B[p][n]; N % 128 == 0
+cudaError_t launch_wgrad_pair_tc(const int32_t *counts, const int32_t *poff, const uint16_t *A,
+                                 const uint16_t *Bm, void *out, bool out_f32, int E, int M,
+                                 int N, int64_t rows_a, int64_t rows_b, int *status,
+                                 cudaStream_t s) {
+    if (!wgrad_pair_supported(M, N)) return cudaErrorInvalidValue;
+    cudaError_t e = init_host();
+    if (e != cudaSuccess) return e;
+    CUtensorMap ma, mb;  // rows past an operand's own rows read the copy engine's zero fill
+    if ((e = make_map_bf16(&ma, A, rows_a, M, 64)) != cudaSuccess) return e;
+    if ((e = make_map_bf16(&mb, Bm, rows_b, N, 64)) != cudaSuccess) return e;
+    const int nmb = (M + 255) / 256, nnb = (N + 255) / 256;
+    WgradPair p{counts, poff, out, out_f32, E, M, N, nmb, nnb, status};
+    return launch_pair(ma, mb, p, (int64_t)E * nmb * nnb, s);
+}
+
+// BF16 dgrad over a tile list of <= 256-row tiles (PAIR_DGRAD_TILE_ROWS)
+cudaError_t launch_gemm_dgrad_pair_tc(const GemmDgradArgs &a, int E, int64_t rpad_cap,
+                                      cudaStream_t s) {
+    if (a.mxfp8) return cudaErrorInvalidValue;
+    cudaError_t e = init_host();
+    if (e != cudaSuccess) return e;
+    CUtensorMap ma, mb;  // A: W13 as [E*2I][H] (MN-major over H); B: dA [rpad][2I]
+    if ((e = make_map_bf16(&ma, a.w13, (int64_t)E * 2 * a.I, a.H, 64)) != cudaSuccess) return e;
+    if ((e = make_map_bf16(&mb, a.dA, rpad_cap, 2 * a.I, KBOX_ROWS)) != cudaSuccess) return e;
+    const int nmb = (a.H + 255) / 256;
+    DgradPair p{TileUnits{a.tiles, a.tiles_cap, nmb}, a.H, a.I, a.offsets, a.poff, a.perm,
+                a.dx_slots, a.out_f32, a.accumulate, a.status};
+    return launch_pair(ma, mb, p, a.tiles_cap * nmb, s);
+}
+
+}  // namespace mok

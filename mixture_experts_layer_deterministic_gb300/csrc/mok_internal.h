@@ -272,6 +272,11 @@ struct GemmDgradArgs {
 cudaError_t launch_gemm_g_tc(const GemmGArgs &a, int E, int64_t rpad_cap, cudaStream_t s);
 cudaError_t launch_gemm_dgrad_tc(const GemmDgradArgs &a, int E, int64_t rpad_cap,
                                  cudaStream_t s);
+// BF16 dgrad on pairs of SMs sharing their operand tiles (tcgen05 cta_group::2), bit for
+// bit equal to launch_gemm_dgrad_tc; a.tiles holds tiles of <= PAIR_DGRAD_TILE_ROWS rows
+constexpr int PAIR_DGRAD_TILE_ROWS = 256;
+cudaError_t launch_gemm_dgrad_pair_tc(const GemmDgradArgs &a, int E, int64_t rpad_cap,
+                                      cudaStream_t s);
 // out [E][N][M] = per expert e, sum over its padded rows p of A[p][m] * B[p][n]
 // (fp32 if out_f32, else bf16)
 cudaError_t launch_wgrad_tc(const int32_t *counts, const int32_t *poff, const uint16_t *A,

@@ -117,9 +117,9 @@ def cfg(**kw):
     (dict(T=1 << 28, K=8, E=8), B.MOK_ERR_INVALID_ARG),  # R >= 2^31
     (dict(abi_version=99), B.MOK_ERR_ABI),
     (dict(flags=B.MOK_FLAG_FP32_STORAGE), B.MOK_OK),
-    (dict(flags=B.MOK_FLAG_WGRAD_ONE_SM), B.MOK_OK),
-    (dict(flags=B.MOK_FLAG_WGRAD_SM_PAIRS), B.MOK_OK),
-    (dict(flags=B.MOK_FLAG_WGRAD_ONE_SM | B.MOK_FLAG_WGRAD_SM_PAIRS), B.MOK_ERR_INVALID_ARG),
+    (dict(flags=B.MOK_FLAG_ONE_SM_GEMMS), B.MOK_OK),
+    (dict(flags=B.MOK_FLAG_SM_PAIR_GEMMS), B.MOK_OK),
+    (dict(flags=B.MOK_FLAG_ONE_SM_GEMMS | B.MOK_FLAG_SM_PAIR_GEMMS), B.MOK_ERR_INVALID_ARG),
     (dict(flags=8), B.MOK_ERR_INVALID_ARG),       # unknown flag
 ])
 def test_check_config(lib, kw, want):

@@ -120,20 +120,21 @@ def test_recompute_matches_saved_preact(dims, MB):
 
 
 @pytest.mark.parametrize("dims,skew,flags", [
-    ((600, 256, 256, 16, 4), 0.0, B.MOK_FLAG_WGRAD_SM_PAIRS),
-    ((333, 384, 128, 24, 3), 3.0, B.MOK_FLAG_WGRAD_SM_PAIRS),
-    ((1000, 256, 384, 8, 2), 4.0, B.MOK_FLAG_WGRAD_SM_PAIRS),
-    ((40, 128, 128, 4, 2), 0.0, B.MOK_FLAG_WGRAD_SM_PAIRS),
+    ((600, 256, 256, 16, 4), 0.0, B.MOK_FLAG_SM_PAIR_GEMMS),
+    ((333, 384, 128, 24, 3), 3.0, B.MOK_FLAG_SM_PAIR_GEMMS),
+    ((1000, 256, 384, 8, 2), 4.0, B.MOK_FLAG_SM_PAIR_GEMMS),
+    ((40, 128, 128, 4, 2), 0.0, B.MOK_FLAG_SM_PAIR_GEMMS),
     ((2048, 256, 128, 4, 2), 0.0, 0)])
-def test_wgrad_pairs_equal_one_sm(dims, skew, flags):
-    """The weight gradients on SM pairs equal the one-SM kernel's bit for bit: the same
-    fixed-order dot products. The shapes give 256-wide and 128-wide last M blocks (in the
-    latter rank 1's A half lies wholly past the end), 128-column N blocks, empty experts and
-    experts with 3x the rows of an even split; the last shape (1024 rows per expert) takes
-    the pairs by default, the others are forced onto them."""
+def test_pair_gemms_equal_one_sm(dims, skew, flags):
+    """The weight gradients and the dx GEMM on SM pairs equal the one-SM kernels' results
+    bit for bit: the same fixed-order dot products. The shapes give 256-wide and 128-wide
+    last M blocks (in the latter rank 1's A half lies wholly past the end), 128-column N
+    blocks of dW, token tiles from 16 to 256 rows, empty experts and experts with 3x the
+    rows of an even split; the last shape (1024 rows per expert) takes the pairs by
+    default, the others are forced onto them."""
     x, lg, w13, w2, dy = small_case(*dims, seed=dims[0] + 1, skew=skew)
     a, _, _, _ = gpu_backward(dims, x, lg, w13, w2, dy, 100, flags=flags)
-    b, _, _, _ = gpu_backward(dims, x, lg, w13, w2, dy, 100, flags=B.MOK_FLAG_WGRAD_ONE_SM)
+    b, _, _, _ = gpu_backward(dims, x, lg, w13, w2, dy, 100, flags=B.MOK_FLAG_ONE_SM_GEMMS)
     for k in a[0]:
         assert same_bits(a[0][k], b[0][k]), k
 
@@ -171,7 +172,7 @@ def test_full_size_bwd():
     del rc
     # the weight gradients on SM pairs equal those of the one-SM kernel (the default here)
     pr, _, _, _ = gpu_backward(dims, d["x"], d["logits"], d["w13"], d["w2"], d["dy"],
-                               cfg.minibatch, flags=B.MOK_FLAG_WGRAD_SM_PAIRS)
+                               cfg.minibatch, flags=B.MOK_FLAG_SM_PAIR_GEMMS)
     for k in outs[0]:
         assert same_bits(outs[0][k], pr[0][k]), ("SM pairs", k)
     del pr

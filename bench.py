@@ -104,6 +104,7 @@ class Clocks:
 # the kernels whose DRAM traffic per launch profiles/ncu_traffic.json records (the ring
 # forward, built on the same engine in its own file, is not among them)
 GEMM_SOURCES = ("mixture_experts_layer_deterministic_gb300/csrc/gemm_tc.cu",
+                "mixture_experts_layer_deterministic_gb300/csrc/gemm_pair.cu",
                 "mixture_experts_layer_deterministic_gb300/csrc/gemm_tc_core.cuh",
                 "mixture_experts_layer_deterministic_gb300/csrc/tc.cuh",
                 "mixture_experts_layer_deterministic_gb300/csrc/common.cuh",

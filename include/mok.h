@@ -71,16 +71,17 @@ typedef enum mok_precision {
  * or MXFP8 layer and checked against a reference within a tolerance). Every accumulation
  * is fp32 either way; the flag changes what is stored and what later steps read. */
 #define MOK_FLAG_FP32_STORAGE 1u
-/* Which kernels compute the expert GEMMs that have two forms: the weight gradients (dw13,
- * dw2 and the shared expert's) and the BF16 reverse-dispatch GEMM (dx). One form gives each
- * output tile to one SM; the other to a pair of SMs that share their operand tiles (the
- * two-SM tensor-core MMA), which cuts the operand bytes each SM loads per FLOP. The results
- * are the same bit for bit ([alphalab] section 五: warp specialization and PTX). By default
- * the weight gradients run on pairs when an expert averages at least 512 rows (T*K/E; T for
- * the shared expert), where the MMAs and their operand feed bound the time, and on one SM
- * below that, where writing dW bounds it; the dx GEMM runs on pairs.
- * MOK_FLAG_ONE_SM_GEMMS forces one SM per tile, MOK_FLAG_SM_PAIR_GEMMS forces pairs; setting
- * both is MOK_ERR_INVALID_ARG. */
+/* Which kernels compute the BF16 expert GEMMs. Each has two forms: one gives each output
+ * tile to one SM; the other gives it to a pair of SMs that share their operand tiles (the
+ * two-SM tensor-core MMA), so each SM loads fewer operand bytes per FLOP. The results are
+ * the same bit for bit ([alphalab] section 五: warp specialization and PTX). By default the
+ * routed experts' down GEMM and dx GEMM run on pairs; the gate/up GEMM and the weight
+ * gradients (dw13, dw2) run on pairs when an expert averages at least 512 rows (T*K/E; T for
+ * the shared expert) and on one SM below that, where the pair measured slower; the shared
+ * expert's down and dx GEMMs, which add into y and dx, run on one SM. The MXFP8 GEMMs
+ * always run on one SM. MOK_FLAG_ONE_SM_GEMMS forces one SM per tile,
+ * MOK_FLAG_SM_PAIR_GEMMS forces pairs for every BF16 GEMM; setting both is
+ * MOK_ERR_INVALID_ARG. */
 #define MOK_FLAG_ONE_SM_GEMMS 2u
 #define MOK_FLAG_SM_PAIR_GEMMS 4u
 

@@ -44,26 +44,30 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 bool f32_storage(const mok_config *c) { return (c->flags & MOK_FLAG_FP32_STORAGE) != 0; }
 size_t stored_bytes(const mok_config *c) { return f32_storage(c) ? 4 : 2; }
 
-// the weight gradients on SM pairs where an expert averages at least WGRAD_PAIR_ROWS rows
-// (avg_rows), else on one SM per tile, unless the caller forces one or the other; the
-// results are the same bit for bit. Measured on 4096 x 1024 experts: pairs 18-23% faster
-// from 640 rows per expert up, 2-16% slower at 320 rows and below, where the dW writes
-// bound both kernels and the pair's two epilogues must both finish before its next MMA.
-constexpr int64_t WGRAD_PAIR_ROWS = 512;
-
-// the BF16 dx GEMM on SM pairs unless one SM per tile is forced (the MXFP8 dx GEMM runs on
-// one SM: its scale atoms are cut per 128-row tile)
-bool dgrad_pairs(const mok_config *c, bool mx) {
-    return !mx && (c->flags & MOK_FLAG_ONE_SM_GEMMS) == 0;
+// Which GEMMs run on SM pairs (the results are the same bit for bit). Unless the caller
+// forces one form, the BF16 down and dx GEMMs of the routed experts always do, and the
+// weight gradients and the gate/up GEMM when an expert averages at least PAIR_ROWS rows.
+// Measured on 4096 x 1024 experts, pairs against one SM: down 5-9% and dx 6-16% faster
+// from 160 rows per expert up; weight gradients 18-23% and gate/up 13% faster from 640 and
+// 1280 rows, but 2-16% and 9-30% slower at 320 rows and below. There the dW writes bound
+// the weight gradients, and gate/up units keep N <= 128 columns (two MMAs per step); the
+// pair's two pipelines must both finish a stage or a unit before it moves on, which costs
+// more than the operand bytes it saves. The same holds for GEMMs that add into their output
+// (the shared expert's down and dx: 19% slower on pairs): their epilogues wait on the
+// loads of the values they add to. The MXFP8 GEMMs run on one SM: their scale atoms are
+// cut per one-SM tile.
+constexpr int64_t PAIR_ROWS = 512;
+bool gemm_pairs(const mok_config *c, bool mx, bool by_default) {
+    if (mx || (c->flags & MOK_FLAG_ONE_SM_GEMMS) != 0) return false;
+    return (c->flags & MOK_FLAG_SM_PAIR_GEMMS) != 0 || by_default;
 }
+
+// the weight gradients; avg_rows: an expert's average rows
 cudaError_t launch_wgrad(const mok_config *c, int64_t avg_rows, const int32_t *counts,
                          const int32_t *poff, const uint16_t *A, const uint16_t *Bm, void *out,
                          int E, int M, int N, int64_t rows_a, int64_t rows_b, int *status,
                          cudaStream_t s) {
-    const bool pairs = (c->flags & MOK_FLAG_SM_PAIR_GEMMS) != 0 ||
-                       ((c->flags & MOK_FLAG_ONE_SM_GEMMS) == 0 &&
-                        avg_rows >= WGRAD_PAIR_ROWS);
-    if (pairs && wgrad_pair_supported(M, N))
+    if (gemm_pairs(c, false, avg_rows >= PAIR_ROWS) && wgrad_pair_supported(M, N))
         return launch_wgrad_pair_tc(counts, poff, A, Bm, out, f32_storage(c), E, M, N, rows_a,
                                     rows_b, status, s);
     return launch_wgrad_tc(counts, poff, A, Bm, out, f32_storage(c), E, M, N, rows_a, rows_b,
@@ -629,8 +633,13 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
             MOK_LAUNCH(KK_GEMM_DOWN, 1,
                        launch_gemm_down_tc_mx(da, R, w.sf_w2, w.sf_h, stream));
         } else {
-            MOK_LAUNCH(KK_GEMM_UP, 1, launch_gemm_up_tc(ua, R, stream));
-            MOK_LAUNCH(KK_GEMM_DOWN, 1, launch_gemm_down_tc(da, R, stream));
+            const bool up2 = gemm_pairs(c, mx, R / c->E >= PAIR_ROWS);
+            MOK_LAUNCH(KK_GEMM_UP, 1,
+                       up2 ? launch_gemm_up_pair_tc(ua, R, stream)
+                           : launch_gemm_up_tc(ua, R, stream));
+            MOK_LAUNCH(KK_GEMM_DOWN, 1,
+                       gemm_pairs(c, mx, true) ? launch_gemm_down_pair_tc(da, R, stream)
+                                               : launch_gemm_down_tc(da, R, stream));
         }
     }
     MOK_LAUNCH(KK_COMBINE, 1,
@@ -725,7 +734,7 @@ mok_status backward_impl(const mok_config *c, const void *x, const mok_schedule 
         dg.dA_q = w.dA_q;
         dg.sf_dA = w.sf_dA;
     }
-    if (dgrad_pairs(c, mx)) {
+    if (gemm_pairs(c, mx, true)) {
         // the pair form's tiles hold up to 256 rows; the list is rebuilt in place (nothing
         // after this GEMM reads it)
         MOK_LAUNCH(KK_TILES, 1,
@@ -798,11 +807,15 @@ mok_status mok_shared_expert_forward(const mok_config *c, const void *x, const v
     GemmUpArgs ua{w.tiles, w.tiles_cap, x, nullptr, w13_s, nullptr, w.h, nullptr,
                   saved_preact_s, c->H, c->I, 1, false, ring, status};
     ua.preact_f32 = f32_storage(c);
-    MOK_LAUNCH(KK_SHARED_UP, 1, launch_gemm_up_tc(ua, c->T, stream));
+    MOK_LAUNCH(KK_SHARED_UP, 1,
+               gemm_pairs(c, false, c->T >= PAIR_ROWS) ? launch_gemm_up_pair_tc(ua, c->T, stream)
+                                                       : launch_gemm_up_tc(ua, c->T, stream));
     GemmDownArgs da{w.tiles, w.tiles_cap, w.h, nullptr, w2_s, nullptr, nullptr, y,
                     c->H, c->I, 1, false, ring, status, true};
     da.out_f32 = f32_storage(c);
-    MOK_LAUNCH(KK_SHARED_DOWN, 1, launch_gemm_down_tc(da, c->T, stream));
+    MOK_LAUNCH(KK_SHARED_DOWN, 1,
+               gemm_pairs(c, false, false) ? launch_gemm_down_pair_tc(da, c->T, stream)
+                                           : launch_gemm_down_tc(da, c->T, stream));
     return MOK_OK;
 }
 
@@ -936,7 +949,7 @@ mok_status shared_backward_impl(const mok_config *c, const void *x, const void *
             MOK_LAUNCH(KK_SCALE_ATOMS, 1,
                        launch_scale_atoms_tiles_padded(w.tiles, w.tiles_cap, w.dA_s, w.offsets,
                                                        w.poff, 2 * I, w.sf_dA, stream));
-        if (dgrad_pairs(c, mx)) {
+        if (gemm_pairs(c, mx, false)) {  // dx adds into the routed part
             MOK_LAUNCH(KK_TILES, 1,
                        launch_build_tiles(w.offsets, 1, 0, T, PAIR_DGRAD_TILE_ROWS, w.tiles,
                                           w.tiles_cap, status, stream));

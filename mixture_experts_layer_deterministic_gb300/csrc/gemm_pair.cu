@@ -40,40 +40,60 @@
 namespace mok {
 namespace {
 
-constexpr int PAIR_STAGES = 6;
-constexpr int PAIR_BOX = 64 * 128;           // one 64 x 64 bf16 MN-major box
-constexpr int PAIR_A = 2 * PAIR_BOX;         // A half: 128 M rows x 64 K
-constexpr int PAIR_STAGE = 4 * PAIR_BOX;     // A half + B half (<= 128 rows of 128 bytes)
+constexpr int PAIR_BOX = 64 * 128;           // one 64 x 64 bf16 box (8 KB)
 constexpr uint32_t PAIR_SET_COLS = 256;      // TMEM columns of one accumulator set
 constexpr int PAIR_TILE = 256;               // max N of a unit (token rows or dW columns)
+constexpr int PAIR_MAX_STAGES = 6;
 
 struct PairSmem {
-    uint64_t full[PAIR_STAGES];   // rank 0: both CTAs' copies of the stage have landed
-    uint64_t empty[PAIR_STAGES];  // each CTA: the MMAs that read the stage are done
-    uint64_t tmem_full[2];        // each CTA: accumulator set b holds a finished unit
-    uint64_t tmem_empty[2];       // rank 0: both CTAs' epilogues have drained set b
+    uint64_t full[PAIR_MAX_STAGES];   // rank 0: both CTAs' copies of the stage have landed
+    uint64_t empty[PAIR_MAX_STAGES];  // each CTA: the MMAs that read the stage are done
+    uint64_t tmem_full[2];            // each CTA: accumulator set b holds a finished unit
+    uint64_t tmem_empty[2];           // rank 0: both CTAs' epilogues have drained set b
     uint32_t tmem_base;
     int abort;
     int32_t col[EPI_WARPS][PAIR_TILE];  // per epilogue warp: one index per column of a unit
 };
 
-constexpr int PAIR_SMEM = PAIR_STAGES * PAIR_STAGE + 1024 + (int)sizeof(PairSmem);
-static_assert(PAIR_SMEM <= 232448, "pair kernel exceeds the shared memory of a CTA");
+template <class P>
+__host__ __device__ constexpr int pair_smem() {
+    return P::STAGES * P::STAGE_BYTES + 1024 + (int)sizeof(PairSmem);
+}
 
-// One unit as one CTA of the pair loads and multiplies it.
+// One unit as one CTA of the pair loads and multiplies it: the policy's coordinates and
+// the MMA's shape.
 struct PairGeom {
-    int32_t ax, ay;  // A half: MN-major boxes at (ax, ay + k) and (ax + 64, ay + k)
-    int32_t bx, by;  // B half: MN-major, nbox boxes at (bx + 64j, by + k); K-major, one
-                     // 128-row box at (k, by) of which the MMA reads n_mma / 2 rows
+    int32_t ax, ay, ay2;  // A half (per policy)
+    int32_t bx, by;       // B half (per policy)
     int nbox;
-    int n_mma;       // N of the pair MMA: multiple of 16 (K-major B), of 128 (MN-major B)
-    int k_steps;     // 16-element K steps; 0 leaves the accumulators unwritten
+    int n_mma;            // N of each pair MMA (multiple of 16; of 128 for MN-major B)
+    int k_steps;          // 16-element K steps; 0 leaves the accumulators unwritten
 };
+
+// 32 accumulator columns from TMEM address c (this warp's lane quadrant), one round trip
+MOK_DEV void tmem_ld32(uint32_t c, float (&v)[32]) {
+    float a[16], b[16];
+    tc::tmem_ld16(c, a);
+    tc::tmem_ld16(c + 16, b);
+    tc::tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        v[j] = a[j];
+        v[16 + j] = b[j];
+    }
+}
+
+// Policy interface: STAGES x STAGE_BYTES of operand ring, the A region (A_BYTES) first in
+// each stage; A_MN / B_MN operand majors; TWO: two MMAs per K step, on A rows 0-127 and
+// 128-255 of the A region into accumulator columns 0 and 128 of a set (N <= 128), else one
+// on A rows 0-127 into columns 0 (N <= 256); tx(g): bytes one CTA loads per stage;
+// load(..): its copies of one stage; epilogue(..): TMEM -> outputs.
 
 // weight gradient: out[e][n][m] = sum over the expert's padded rows p of A[p][m] B[p][n];
 // a unit is (expert, 256-column block nb, 256-row block mb)
 struct WgradPair {
-    static constexpr bool B_MN = true;
+    static constexpr bool A_MN = true, B_MN = true, TWO = false;
+    static constexpr int A_BYTES = 2 * PAIR_BOX, STAGE_BYTES = 4 * PAIR_BOX, STAGES = 6;
     const int32_t *counts, *poff;
     void *out;     // [E][N][M], fp32 if out_f32, else bf16
     bool out_f32;
@@ -97,14 +117,24 @@ struct WgradPair {
         const int half = g.n_mma / 2;  // 64 or 128 columns of B per CTA
         g.ax = mb * 256 + (int)rank * 128;
         g.ay = poff[e];
+        g.ay2 = 0;
         g.bx = nb * 256 + (int)rank * half;
         g.by = poff[e];
         g.nbox = half / 64;
         g.k_steps = ((counts[e] + 15) & ~15) / 16;
         return g;
     }
-    template <class LD>
-    MOK_DEV void epilogue(int64_t u, uint32_t rank, const LD &ld, int32_t *, int q, int hw,
+    MOK_DEV uint32_t tx(const PairGeom &g) const { return A_BYTES + g.nbox * PAIR_BOX; }
+    // A: two 64-wide MN-major boxes of the CTA's 128 M rows; B: its columns, 64 per box
+    MOK_DEV void load(uint8_t *st, uint32_t fb, const PairGeom &g, int k0,
+                      const CUtensorMap *tmA, const CUtensorMap *tmB) const {
+        tc::tma_load_2d_pair(st, tmA, fb, g.ax, g.ay + k0);
+        tc::tma_load_2d_pair(st + PAIR_BOX, tmA, fb, g.ax + 64, g.ay + k0);
+        for (int j = 0; j < g.nbox; ++j)
+            tc::tma_load_2d_pair(st + A_BYTES + j * PAIR_BOX, tmB, fb, g.bx + 64 * j,
+                                 g.by + k0);
+    }
+    MOK_DEV void epilogue(int64_t u, uint32_t rank, uint32_t c, int32_t *, int q, int hw,
                           int lane) const {
         int e, mb, nb;
         get(u, &e, &mb, &nb);
@@ -115,24 +145,47 @@ struct WgradPair {
         const int64_t row0 = (int64_t)e * N + (int64_t)nb * 256;
         // 32 columns per TMEM round trip (nn is a multiple of 128)
         for (int n0 = 32 * hw; n0 < nn; n0 += 64) {
-            float v0[16], v1[16];
-            ld(n0, v0, v1);
+            float v[32];
+            tmem_ld32(c + n0, v);
             if (mok) {
                 const int64_t o = (row0 + n0) * M + m;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    st_val(out, o + (int64_t)j * M, any ? v0[j] : 0.f, out_f32);
-                    st_val(out, o + (int64_t)(16 + j) * M, any ? v1[j] : 0.f, out_f32);
-                }
+                for (int j = 0; j < 32; ++j)
+                    st_val(out, o + (int64_t)j * M, any ? v[j] : 0.f, out_f32);
             }
         }
     }
 };
 
+// Scatter of 32 accumulator columns n0.. of a token tile to output rows fcol[n] (< nr),
+// column c; accumulate: add into the stored values (every load of the chunk before any
+// store: a store to one row may alias the next row's load, which would otherwise
+// serialise the round trips)
+MOK_DEV void scatter32(void *outp, bool out_f32, bool accumulate, const int32_t *fcol, int n0,
+                       int nr, int64_t ld_out, int c, float (&v)[32]) {
+    if (accumulate) {
+        float a[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const bool ok = n0 + j < nr;
+            const int64_t o = (int64_t)fcol[ok ? n0 + j : 0] * ld_out + c;
+            a[j] = !ok ? 0.f
+                   : out_f32 ? static_cast<const float *>(outp)[o]
+                             : bf16_to_f32(static_cast<const uint16_t *>(outp)[o]);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += a[j];
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        if (n0 + j < nr) st_val(outp, (int64_t)fcol[n0 + j] * ld_out + c, v[j], out_f32);
+}
+
 // reverse dispatch: dx_slots[perm[r]][c] (+)= sum_j dA[r][j] W13[e][j][c] over the rows r
 // of a token tile (e, r0, r1) of <= 256 rows; a unit is (tile, 256-feature block mb)
 struct DgradPair {
-    static constexpr bool B_MN = false;
+    static constexpr bool A_MN = true, B_MN = false, TWO = false;
+    static constexpr int A_BYTES = 2 * PAIR_BOX, STAGE_BYTES = 4 * PAIR_BOX, STAGES = 6;
     TileUnits tu;
     int H, I;
     const int32_t *offsets, *poff, *perm;
@@ -150,47 +203,177 @@ struct DgradPair {
         g.n_mma = (int)((r1 - r0 + 15) & ~15);
         g.ax = mb * 256 + (int)rank * 128;
         g.ay = e * 2 * I;
+        g.ay2 = 0;
         g.bx = 0;
         g.by = (int32_t)(poff[e] + (r0 - offsets[e])) + (int)rank * (g.n_mma / 2);
         g.nbox = 1;
         g.k_steps = 2 * I / 16;
         return g;
     }
-    template <class LD>
-    MOK_DEV void epilogue(int64_t u, uint32_t rank, const LD &ld, int32_t *fcol, int q,
-                          int hw, int lane) const {
+    MOK_DEV uint32_t tx(const PairGeom &) const { return A_BYTES + 2 * PAIR_BOX; }
+    // A: two 64-wide MN-major boxes of W13^T; B: one 128-row K-major box of dA, of which
+    // the MMA reads n_mma / 2 rows
+    MOK_DEV void load(uint8_t *st, uint32_t fb, const PairGeom &g, int k0,
+                      const CUtensorMap *tmA, const CUtensorMap *tmB) const {
+        tc::tma_load_2d_pair(st, tmA, fb, g.ax, g.ay + k0);
+        tc::tma_load_2d_pair(st + PAIR_BOX, tmA, fb, g.ax + 64, g.ay + k0);
+        tc::tma_load_2d_pair(st + A_BYTES, tmB, fb, k0, g.by);
+    }
+    MOK_DEV void epilogue(int64_t u, uint32_t rank, uint32_t c, int32_t *fcol, int q, int hw,
+                          int lane) const {
         int e, mb;
         int64_t r0, r1;
         tu.get(u, &e, &r0, &r1, &mb);
         const int nr = (int)(r1 - r0);
         const int n_mma = (nr + 15) & ~15;
-        const int c = mb * 256 + (int)rank * 128 + q * 32 + lane;
-        const bool cok = c < H;
+        const int f = mb * 256 + (int)rank * 128 + q * 32 + lane;
         for (int n = lane; n < nr; n += 32) fcol[n] = perm[r0 + n];
         __syncwarp();
         for (int n0 = 32 * hw; n0 < n_mma; n0 += 64) {
             float v[32];
-            ld(n0, *reinterpret_cast<float(*)[16]>(v), *reinterpret_cast<float(*)[16]>(v + 16));
-            if (accumulate && cok) {
-                // every load of the chunk before any store: a store to one row may alias
-                // the next row's load, which would otherwise serialise the round trips
-                float a[32];
+            tmem_ld32(c + n0, v);
+            if (f < H) scatter32(dx_slots, out_f32, accumulate, fcol, n0, nr, H, f, v);
+        }
+        __syncwarp();
+    }
+};
+
+// forward gate/up with SwiGLU (BF16): a[r][j] = sum_c W13[e][j][c] xring[r][c],
+// h[r][i] = silu(a[r][i]) a[r][I+i]; a unit is (tile of <= 128 rows, 256-feature block pb),
+// rank r taking features [pb*256 + 128r, +128) with their gate rows and up rows as A rows
+// 0-127 and 128-255: two MMAs per K step (gate, up), both halves of a feature on one lane
+struct UpPair {
+    static constexpr bool A_MN = false, B_MN = false, TWO = true;
+    static constexpr int A_BYTES = 4 * PAIR_BOX, STAGE_BYTES = 5 * PAIR_BOX, STAGES = 5;
+    TileUnits tu;  // n_mblocks = I / 256
+    int H, I;
+    Ring ring;
+    void *hring;    // [rows][I] bf16
+    void *preact;   // [R][I] (gate, up) pairs, fp32 if preact_f32, else bf16; or nullptr
+    bool preact_f32;
+    int *status;
+
+    MOK_DEV int64_t n_units() const { return tu.count(); }
+    MOK_DEV PairGeom geom(int64_t u, uint32_t rank) const {
+        int e, pb;
+        int64_t r0, r1;
+        tu.get(u, &e, &r0, &r1, &pb);
+        PairGeom g;
+        g.n_mma = (int)((r1 - r0 + 15) & ~15);
+        g.ax = 0;
+        g.ay = 2 * pb + (int)rank;  // 128-feature block of the CTA
+        g.ay2 = e;
+        g.bx = 0;
+        // a tile never straddles a lap of the ring: its rows are consecutive ring rows
+        g.by = (int32_t)RingMap{ring.R, ring.MB, ring.n_slots}(r0) + (int)rank * (g.n_mma / 2);
+        g.nbox = 1;
+        g.k_steps = H / 16;
+        return g;
+    }
+    MOK_DEV uint32_t tx(const PairGeom &) const { return A_BYTES + PAIR_BOX; }
+    // A: the CTA's gate block and up block (one 5D box); B: 64 K-major rows of the x ring,
+    // of which the MMA reads n_mma / 2
+    MOK_DEV void load(uint8_t *st, uint32_t fb, const PairGeom &g, int k0,
+                      const CUtensorMap *tmA, const CUtensorMap *tmB) const {
+        tc::tma_load_5d_pair(st, tmA, fb, k0, 0, g.ay, 0, g.ay2);
+        tc::tma_load_2d_pair(st + A_BYTES, tmB, fb, k0, g.by);
+    }
+    MOK_DEV void epilogue(int64_t u, uint32_t rank, uint32_t c, int32_t *, int q, int hw,
+                          int lane) const {
+        int e, pb;
+        int64_t r0, r1;
+        tu.get(u, &e, &r0, &r1, &pb);
+        const int nr = (int)(r1 - r0);
+        const int n_mma = (nr + 15) & ~15;
+        const int64_t hrow0 = RingMap{ring.R, ring.MB, ring.n_slots}(r0);
+        const int i = pb * 256 + (int)rank * 128 + q * 32 + lane;  // gate feature; up: I + i
+        if (pb * 256 + (int)rank * 128 >= I) return;  // past I when I % 256 == 128
+        for (int n0 = 16 * hw; n0 < n_mma; n0 += 32) {
+            float d0[16], d1[16];
+            tc::tmem_ld16(c + n0, d0);
+            tc::tmem_ld16(c + 128 + n0, d1);
+            tc::tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const bool ok = n0 + j < nr;
-                    const int64_t o = (int64_t)fcol[ok ? n0 + j : 0] * H + c;
-                    a[j] = !ok ? 0.f
-                           : out_f32 ? static_cast<const float *>(dx_slots)[o]
-                                     : bf16_to_f32(static_cast<const uint16_t *>(dx_slots)[o]);
+            for (int j = 0; j < 16; ++j) {
+                const int n = n0 + j;
+                if (n < nr) {
+                    const int64_t r = r0 + n;
+                    if (preact != nullptr) {
+                        if (preact_f32)
+                            static_cast<float2 *>(preact)[r * I + i] = make_float2(d0[j], d1[j]);
+                        else
+                            static_cast<uint32_t *>(preact)[r * I + i] =
+                                pack_bf16x2(d0[j], d1[j]);
+                    }
+                    ((uint16_t *)hring)[(hrow0 + n) * I + i] =
+                        f32_to_bf16(silu_f(d0[j]) * d1[j]);
                 }
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] += a[j];
             }
-            if (cok) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (n0 + j < nr) st_val(dx_slots, (int64_t)fcol[n0 + j] * H + c, v[j], out_f32);
-            }
+        }
+    }
+};
+
+// forward down with the push scatter (BF16): slots[perm[r]][c] (+)= sum_i W2[e][c][i]
+// hring[r][i]; a unit is (tile of <= 128 rows, 512-feature block pb), rank r taking
+// features [pb*512 + 128r, +128) and [pb*512 + 256 + 128r, +128) as A rows 0-127 and
+// 128-255: two MMAs per K step
+struct DownPair {
+    static constexpr bool A_MN = false, B_MN = false, TWO = true;
+    static constexpr int A_BYTES = 4 * PAIR_BOX, STAGE_BYTES = 5 * PAIR_BOX, STAGES = 5;
+    TileUnits tu;  // n_mblocks = ceil(H / 512)
+    int H, I;
+    Ring ring;
+    const int32_t *perm;  // output row of each sorted row (nullptr: the row itself)
+    void *slots;          // [rows][H], fp32 if out_f32, else bf16
+    bool out_f32;
+    bool accumulate;      // add into the output (the shared expert adds into y)
+    int *status;
+
+    MOK_DEV int64_t n_units() const { return tu.count(); }
+    MOK_DEV PairGeom geom(int64_t u, uint32_t rank) const {
+        int e, pb;
+        int64_t r0, r1;
+        tu.get(u, &e, &r0, &r1, &pb);
+        PairGeom g;
+        g.n_mma = (int)((r1 - r0 + 15) & ~15);
+        g.ax = 0;
+        // rows past this expert's H (a partial last block) read the next expert's rows or
+        // the zero fill; their results are discarded
+        g.ay = e * H + pb * 512 + (int)rank * 128;
+        g.ay2 = g.ay + 256;
+        g.bx = 0;
+        g.by = (int32_t)RingMap{ring.R, ring.MB, ring.n_slots}(r0) + (int)rank * (g.n_mma / 2);
+        g.nbox = 1;
+        g.k_steps = I / 16;
+        return g;
+    }
+    MOK_DEV uint32_t tx(const PairGeom &) const { return A_BYTES + PAIR_BOX; }
+    // A: two 128-row K-major boxes of W2; B: 64 K-major rows of the h ring
+    MOK_DEV void load(uint8_t *st, uint32_t fb, const PairGeom &g, int k0,
+                      const CUtensorMap *tmA, const CUtensorMap *tmB) const {
+        tc::tma_load_2d_pair(st, tmA, fb, k0, g.ay);
+        tc::tma_load_2d_pair(st + 2 * PAIR_BOX, tmA, fb, k0, g.ay2);
+        tc::tma_load_2d_pair(st + A_BYTES, tmB, fb, k0, g.by);
+    }
+    MOK_DEV void epilogue(int64_t u, uint32_t rank, uint32_t c, int32_t *fcol, int q, int hw,
+                          int lane) const {
+        int e, pb;
+        int64_t r0, r1;
+        tu.get(u, &e, &r0, &r1, &pb);
+        const int nr = (int)(r1 - r0);
+        const int n_mma = (nr + 15) & ~15;
+        const int f0 = pb * 512 + (int)rank * 128 + q * 32 + lane, f1 = f0 + 256;
+        for (int n = lane; n < nr; n += 32)
+            fcol[n] = perm != nullptr ? perm[r0 + n] : (int)(r0 + n);
+        __syncwarp();
+        // warps of hw 0 drain accumulator 0 (features f0), of hw 1 accumulator 1 (f1), 32
+        // columns per TMEM round trip
+        const int f = hw ? f1 : f0;
+        const uint32_t ca = c + (hw ? 128u : 0u);
+        for (int n0 = 0; n0 < n_mma; n0 += 32) {
+            float v[32];
+            tmem_ld32(ca + n0, v);
+            if (f < H) scatter32(slots, out_f32, accumulate, fcol, n0, nr, H, f, v);
         }
         __syncwarp();
     }
@@ -211,17 +394,19 @@ template <class P>
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const P p) {
+    constexpr int NS = P::STAGES, SB = P::STAGE_BYTES;
+    static_assert(NS <= PAIR_MAX_STAGES && pair_smem<P>() <= 232448, "pair kernel smem");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the same offset in both CTAs: the MMA finds the peer's tiles where this CTA has its own
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    PairSmem *sm = (PairSmem *)(base + PAIR_STAGES * PAIR_STAGE);
+    PairSmem *sm = (PairSmem *)(base + NS * SB);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = tc::cluster_rank();
     const int64_t cid = tc::cluster_id_x(), ncl = tc::cluster_count_x();
     const int64_t n_units = p.n_units();
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < PAIR_STAGES; ++s) {
+        for (int s = 0; s < NS; ++s) {
             tc::mbar_init(&sm->full[s], 1);
             tc::mbar_init(&sm->empty[s], 1);
         }
@@ -255,7 +440,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             bool ok = true;
             for (int64_t u = cid; u < n_units && ok; u += ncl) {
                 const PairGeom g = p.geom(u, rank);
-                const uint32_t tx = PAIR_A + (P::B_MN ? g.nbox * PAIR_BOX : 2 * PAIR_BOX);
+                const uint32_t tx = p.tx(g);
                 const int kblocks = (g.k_steps + 3) / 4;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!pair_wait(&sm->empty[s], ph ^ 1u, p.status, abort)) {
@@ -263,20 +448,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         break;
                     }
                     if (rank == 0) tc::mbar_arrive_expect_tx(&sm->full[s], 2 * tx);
-                    const uint32_t fb = full0 + (uint32_t)s * 8u;
-                    uint8_t *st = base + s * PAIR_STAGE;
-                    const int k0 = kb * BK;
-                    tc::tma_load_2d_pair(st, &tmA, fb, g.ax, g.ay + k0);
-                    tc::tma_load_2d_pair(st + PAIR_BOX, &tmA, fb, g.ax + 64, g.ay + k0);
-                    if (P::B_MN) {
-                        for (int j = 0; j < g.nbox; ++j)
-                            tc::tma_load_2d_pair(st + PAIR_A + j * PAIR_BOX, &tmB, fb,
-                                                 g.bx + 64 * j, g.by + k0);
-                    } else {
-                        tc::tma_load_2d_pair(st + PAIR_A, &tmB, fb, k0, g.by);
-                    }
+                    p.load(base + s * SB, full0 + (uint32_t)s * 8u, g, kb * BK, &tmA, &tmB);
                     ++issued;
-                    if (++s == PAIR_STAGES) {
+                    if (++s == NS) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -284,9 +458,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             // do not leave while copies may still be landing: the MMAs that read the last
             // stages have finished (bounded)
-            for (int q = 0; q < PAIR_STAGES && q < issued; ++q) {
+            for (int q = 0; q < NS && q < issued; ++q) {
                 if (--s < 0) {
-                    s = PAIR_STAGES - 1;
+                    s = NS - 1;
                     ph ^= 1u;
                 }
                 pair_drain(&sm->empty[s], ph);
@@ -301,7 +475,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             bool ok = true;
             for (int64_t u = cid; u < n_units && ok; u += ncl, ++a) {
                 const PairGeom g = p.geom(u, 0);
-                const uint32_t idesc = tc::idesc_bf16(256, g.n_mma, true, P::B_MN);
+                const uint32_t idesc = tc::idesc_bf16(256, g.n_mma, P::A_MN, P::B_MN);
                 const int ab = (int)(a & 1);
                 const uint32_t use = (uint32_t)((a >> 1) & 1);
                 if (!pair_wait(&sm->tmem_empty[ab], use ^ 1u, p.status, abort)) break;
@@ -314,21 +488,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         break;
                     }
                     tc::tc_fence_after();
-                    const uint32_t sa = tc::smem_u32(base + s * PAIR_STAGE);
-                    const uint32_t sb = sa + PAIR_A;
+                    const uint32_t sa = tc::smem_u32(base + s * SB);
+                    const uint32_t sb = sa + P::A_BYTES;
                     const int steps = g.k_steps - kb * 4 < 4 ? g.k_steps - kb * 4 : 4;
                     for (int kk = 0; kk < steps; ++kk) {
                         // MN-major: 16 K rows = 2 groups of eight 128-byte rows, the two
-                        // 64-wide blocks of a half PAIR_BOX apart; K-major: 16 elements =
-                        // 32 bytes along the swizzled row
-                        const uint64_t da = tc::sdesc_sw128(sa + kk * 2048, PAIR_BOX, 1024);
+                        // 64-wide blocks of 128 M rows PAIR_BOX apart; K-major: 16 elements
+                        // = 32 bytes along the swizzled row, 128 rows = 16 KB
                         const uint64_t db =
                             P::B_MN ? tc::sdesc_sw128(sb + kk * 2048, PAIR_BOX, 1024)
                                     : tc::sdesc_sw128(sb + kk * 32, 16, 1024);
-                        tc::mma_f16_pair(d, da, db, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+#pragma unroll
+                        for (int h = 0; h < (P::TWO ? 2 : 1); ++h) {
+                            const uint32_t sah = sa + (uint32_t)h * 2 * PAIR_BOX;
+                            const uint64_t da =
+                                P::A_MN ? tc::sdesc_sw128(sah + kk * 2048, PAIR_BOX, 1024)
+                                        : tc::sdesc_sw128(sah + kk * 32, 16, 1024);
+                            tc::mma_f16_pair(d + (uint32_t)h * 128, da, db, idesc, acc);
+                        }
                     }
                     tc::mma_commit_pair(&sm->empty[s], 3);  // frees the stage in both CTAs
-                    if (++s == PAIR_STAGES) {
+                    if (++s == NS) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -350,20 +531,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const uint32_t empty0 = tc::cluster_addr(&sm->tmem_empty[0], 0);
         int32_t *col = sm->col[warp - 2];
-        uint32_t c = 0;  // TMEM address of the current unit's accumulator, this quadrant
-        auto ld = [&](int n0, float (&v0)[16], float (&v1)[16]) {
-            tc::tmem_ld16(c + n0, v0);
-            tc::tmem_ld16(c + n0 + 16, v1);
-            tc::tmem_ld_wait();
-        };
         int64_t a = 0;
         for (int64_t u = cid; u < n_units; u += ncl, ++a) {
             const int ab = (int)(a & 1);
             if (!pair_wait(&sm->tmem_full[ab], (uint32_t)((a >> 1) & 1), p.status, abort))
                 break;
             tc::tc_fence_after();
-            c = tmem + lane_base + (uint32_t)ab * PAIR_SET_COLS;
-            p.epilogue(u, rank, ld, col, q, hw, lane);
+            // this quadrant's lanes of the unit's accumulator set
+            p.epilogue(u, rank, tmem + lane_base + (uint32_t)ab * PAIR_SET_COLS, col, q, hw,
+                       lane);
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster(empty0 + (uint32_t)ab * 8u);
@@ -393,7 +569,7 @@ cudaError_t pair_clusters(int *out, cudaStream_t s) {
     const uint64_t bit = 1ull << (dev & 63);
     if ((attr_set[dev >> 6].load(std::memory_order_acquire) & bit) == 0) {
         e = cudaFuncSetAttribute(tc_pair_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 PAIR_SMEM);
+                                 pair_smem<P>());
         if (e != cudaSuccess) return e;
         attr_set[dev >> 6].fetch_or(bit, std::memory_order_acq_rel);
     }
@@ -413,7 +589,7 @@ cudaError_t pair_clusters(int *out, cudaStream_t s) {
         at[0].val.clusterDim.z = 1;
         q.gridDim = dim3((unsigned)(2 * device_sm_count()), 1, 1);
         q.blockDim = dim3(NTHREADS, 1, 1);
-        q.dynamicSmemBytes = PAIR_SMEM;
+        q.dynamicSmemBytes = pair_smem<P>();
         q.attrs = at;
         q.numAttrs = 1;
         // where the query fails, one cluster per two SMs: clusters that do not fit wait for
@@ -447,7 +623,7 @@ cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const P &p
     at[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
     cfg.blockDim = dim3(NTHREADS, 1, 1);
-    cfg.dynamicSmemBytes = PAIR_SMEM;
+    cfg.dynamicSmemBytes = pair_smem<P>();
     cfg.stream = s;
     cfg.attrs = at;
     cfg.numAttrs = 1;
@@ -474,6 +650,34 @@ cudaError_t launch_wgrad_pair_tc(const int32_t *counts, const int32_t *poff, con
     const int nmb = (M + 255) / 256, nnb = (N + 255) / 256;
     WgradPair p{counts, poff, out, out_f32, E, M, N, nmb, nnb, status};
     return launch_pair(ma, mb, p, (int64_t)E * nmb * nnb, s);
+}
+
+// BF16 forward gate/up over tiles of <= 128 rows
+cudaError_t launch_gemm_up_pair_tc(const GemmUpArgs &a, int64_t ring_rows, cudaStream_t s) {
+    if (a.mxfp8) return cudaErrorInvalidValue;
+    cudaError_t e = init_host();
+    if (e != cudaSuccess) return e;
+    CUtensorMap ma, mb;  // A: W13 gate/up block pairs; B: the x ring, 64-row boxes
+    if ((e = make_map_w13_pairs(&ma, a.w13, a.E, a.I, a.H, false)) != cudaSuccess) return e;
+    if ((e = make_map_bf16(&mb, a.xring, ring_rows, a.H, 64)) != cudaSuccess) return e;
+    const int npb = (a.I + 255) / 256;
+    UpPair p{TileUnits{a.tiles, a.tiles_cap, npb}, a.H, a.I, a.ring, a.hring, a.preact,
+             a.preact_f32, a.status};
+    return launch_pair(ma, mb, p, a.tiles_cap * npb, s);
+}
+
+// BF16 forward down with the push scatter over tiles of <= 128 rows
+cudaError_t launch_gemm_down_pair_tc(const GemmDownArgs &a, int64_t ring_rows, cudaStream_t s) {
+    if (a.mxfp8) return cudaErrorInvalidValue;
+    cudaError_t e = init_host();
+    if (e != cudaSuccess) return e;
+    CUtensorMap ma, mb;  // A: W2 as [E*H][I], 128-row boxes; B: the h ring, 64-row boxes
+    if ((e = make_map_bf16(&ma, a.w2, (int64_t)a.E * a.H, a.I, 128)) != cudaSuccess) return e;
+    if ((e = make_map_bf16(&mb, a.hring, ring_rows, a.I, 64)) != cudaSuccess) return e;
+    const int npb = (a.H + 511) / 512;
+    DownPair p{TileUnits{a.tiles, a.tiles_cap, npb}, a.H, a.I, a.ring, a.perm, a.slots,
+               a.out_f32, a.accumulate, a.status};
+    return launch_pair(ma, mb, p, a.tiles_cap * npb, s);
 }
 
 // BF16 dgrad over a tile list of <= 256-row tiles (PAIR_DGRAD_TILE_ROWS)

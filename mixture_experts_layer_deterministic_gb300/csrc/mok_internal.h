@@ -272,6 +272,11 @@ struct GemmDgradArgs {
 cudaError_t launch_gemm_g_tc(const GemmGArgs &a, int E, int64_t rpad_cap, cudaStream_t s);
 cudaError_t launch_gemm_dgrad_tc(const GemmDgradArgs &a, int E, int64_t rpad_cap,
                                  cudaStream_t s);
+// BF16 forward gate/up and down on pairs of SMs sharing their operand tiles (tcgen05
+// cta_group::2), bit for bit equal to launch_gemm_up_tc / launch_gemm_down_tc, over the
+// same tiles of <= gemm_tc_tile_rows(false) rows
+cudaError_t launch_gemm_up_pair_tc(const GemmUpArgs &a, int64_t ring_rows, cudaStream_t s);
+cudaError_t launch_gemm_down_pair_tc(const GemmDownArgs &a, int64_t ring_rows, cudaStream_t s);
 // BF16 dgrad on pairs of SMs sharing their operand tiles (tcgen05 cta_group::2), bit for
 // bit equal to launch_gemm_dgrad_tc; a.tiles holds tiles of <= PAIR_DGRAD_TILE_ROWS rows
 constexpr int PAIR_DGRAD_TILE_ROWS = 256;

@@ -38,7 +38,9 @@ MOK_DEV bool elect_one() {
 MOK_DEV void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
 }
-MOK_DEV void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+MOK_DEV void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
 MOK_DEV void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
                  : "memory");
@@ -336,6 +338,15 @@ MOK_DEV void tma_load_2d_pair(void *smem_dst, const CUtensorMap *m, uint32_t bar
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
         "l"((uint64_t)m), "r"(bar_cluster), "r"(x), "r"(y)
+        : "memory");
+}
+// 5D tile load (coordinates innermost first), likewise completing on either CTA's mbarrier
+MOK_DEV void tma_load_5d_pair(void *smem_dst, const CUtensorMap *m, uint32_t bar_cluster,
+                              int32_t c0, int32_t c1, int32_t c2, int32_t c3, int32_t c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"((uint64_t)m), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
         : "memory");
 }
 MOK_DEV void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {

@@ -282,6 +282,23 @@ def test_edge_shapes(dims):
     check_forward(g, x, w13, w2, False)
 
 
+@pytest.mark.parametrize("dims", [(1000, 512, 256, 16, 4), (333, 384, 384, 24, 3),
+                                  (129, 640, 128, 64, 1), (2048, 256, 256, 4, 2)])
+def test_pair_gemms_equal_one_sm(dims):
+    """The BF16 forward's gate/up and down GEMMs on SM pairs (the default) give the one-SM
+    kernels' bits: y and the saved pre-activations. I=384 and I=128 leave rank 1 of the last
+    256-feature gate/up block past I; H=384 and H=640 leave partial 512-feature blocks of
+    the down GEMM; tiles run from 16 to 128 rows."""
+    x, lg, w13, w2 = small_case(*dims, seed=dims[0] + 7)
+    a = gpu_forward(dims, x, lg, w13, w2, B.MOK_BF16, 300, 0, preact=True,
+                    flags=B.MOK_FLAG_SM_PAIR_GEMMS)
+    b = gpu_forward(dims, x, lg, w13, w2, B.MOK_BF16, 300, 0, preact=True,
+                    flags=B.MOK_FLAG_ONE_SM_GEMMS)
+    assert same_bits(a["y_dev"][0], b["y_dev"][0])
+    assert same_bits(a["pre"], b["pre"])
+    check_forward(a, x, w13, w2, False)
+
+
 def test_empty_batch():
     import torch
     L = MoELayer(0, 256, 128, 8, 2, 16, 0, B.MOK_BF16)

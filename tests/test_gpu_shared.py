@@ -35,10 +35,11 @@ def _step(v):
     return np.ldexp(1.0, np.frexp(np.maximum(np.abs(v), 1e-300))[1] - 8)
 
 
-def gpu_routed_plus_shared(dims, x, logits, w13, w2, w13s, w2s, prec, MB=2368, reps=1):
+def gpu_routed_plus_shared(dims, x, logits, w13, w2, w13s, w2s, prec, MB=2368, reps=1,
+                           flags=0):
     import torch
     T, H, I, E, K = dims
-    L = MoELayer(T, H, I, E, K, MB, 0, prec)
+    L = MoELayer(T, H, I, E, K, MB, 0, prec, flags=flags)
     S = SharedExpert(L)
     xd = to_dev(x)
     if prec == B.MOK_MXFP8:
@@ -183,7 +184,8 @@ def test_mxfp8_config_needs_the_mxfp8_entry():
 
 # ---------------------------------------------------------------- backward
 
-def gpu_step_with_shared(dims, x, logits, w13, w2, w13s, w2s, dy, prec, MB=2368, reps=1):
+def gpu_step_with_shared(dims, x, logits, w13, w2, w13s, w2s, dy, prec, MB=2368, reps=1,
+                         flags=0):
     """Routed and shared forward (both saving pre-activations), then the routed backward and
     the shared backward, which adds into dx; dx after the routed part, dx in total and the
     shared weight gradients, with the shared backward's workspace intermediates."""
@@ -191,7 +193,7 @@ def gpu_step_with_shared(dims, x, logits, w13, w2, w13s, w2s, dy, prec, MB=2368,
     from mixture_experts_layer_deterministic_gb300.buffers import (backward_mxfp8,
                                                                      quantize_mxfp8_transposed)
     T, H, I, E, K = dims
-    L = MoELayer(T, H, I, E, K, MB, 0, prec, backward=True)
+    L = MoELayer(T, H, I, E, K, MB, 0, prec, backward=True, flags=flags)
     S = SharedExpert(L)
     xd, dyd = to_dev(x), to_dev(dy)
     w13d, w2d, w13sd, w2sd = to_dev(w13), to_dev(w2), to_dev(w13s), to_dev(w2s)
@@ -300,6 +302,28 @@ def test_backward_with_shared_expert(dims, prec):
     check_backward(outs, gi, idx, w, x, w13, w2, w13s, w2s, dy, prec == B.MOK_MXFP8)
     for k in outs[0]:  # bitwise run to run
         assert same_bits(outs[0][k], outs[1][k]), k
+
+
+@pytest.mark.parametrize("dims", [(517, 384, 256, 16, 4), (600, 256, 384, 8, 2)])
+def test_shared_pair_gemms_equal_one_sm(dims):
+    """The shared expert's GEMMs on SM pairs, including the down and dx GEMMs that add into
+    y and dx, give the one-SM kernels' bits (y, dx, dW13s, dW2s)."""
+    T, H, I, E, K = dims
+    r = np.random.default_rng(T + 5)
+    x = f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
+    lg = r.standard_normal((T, E)).astype(np.float32)
+    w13 = f32_to_bf16_bits((r.standard_normal((E, 2 * I, H)) * 0.05).astype(np.float32))
+    w2 = f32_to_bf16_bits((r.standard_normal((E, H, I)) * 0.05).astype(np.float32))
+    dy = f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
+    w13s, w2s = shared_weights(H, I, T + 6, 0.05)
+    runs = [gpu_step_with_shared(dims, x, lg, w13, w2, w13s, w2s, dy, B.MOK_BF16, flags=f)[0]
+            for f in (B.MOK_FLAG_SM_PAIR_GEMMS, B.MOK_FLAG_ONE_SM_GEMMS)]
+    ys = [gpu_routed_plus_shared(dims, x, lg, w13, w2, w13s, w2s, B.MOK_BF16, flags=f)
+          for f in (B.MOK_FLAG_SM_PAIR_GEMMS, B.MOK_FLAG_ONE_SM_GEMMS)]
+    for k in runs[0][0]:
+        assert same_bits(runs[0][0][k], runs[1][0][k]), k
+    assert same_bits(ys[0]["outs"][0][1], ys[1]["outs"][0][1])
+    assert np.array_equal(ys[0]["pre_s"], ys[1]["pre_s"])
 
 
 def test_mxfp8_shared_backward_argument_errors():

@@ -75,9 +75,9 @@ typedef enum mok_precision {
  * tile to one SM; the other gives it to a pair of SMs that share their operand tiles (the
  * two-SM tensor-core MMA), so each SM loads fewer operand bytes per FLOP. The results are
  * the same bit for bit ([alphalab] section 五: warp specialization and PTX). By default the
- * routed experts' down GEMM and dx GEMM run on pairs; the gate/up GEMM and the weight
- * gradients (dw13, dw2) run on pairs when an expert averages at least 512 rows (T*K/E; T for
- * the shared expert) and on one SM below that, where the pair measured slower; the shared
+ * gate/up GEMM and the routed experts' down and dx GEMMs run on pairs; the weight gradients
+ * (dw13, dw2) run on pairs when an expert averages at least 512 rows (T*K/E; T for the
+ * shared expert) and on one SM below that, where the pair measured slower; the shared
  * expert's down and dx GEMMs, which add into y and dx, run on one SM. The MXFP8 GEMMs
  * always run on one SM. MOK_FLAG_ONE_SM_GEMMS forces one SM per tile,
  * MOK_FLAG_SM_PAIR_GEMMS forces pairs for every BF16 GEMM; setting both is
@@ -284,8 +284,9 @@ mok_status mok_build_schedule_noalloc(const mok_config *cfg, const int32_t *topk
  * (one CTA per SM) that takes units from a device-side counter in a fixed order and waits,
  * before loading a unit's operands, for the units it depends on (a gate/up unit on its
  * tile's gather, a down unit on its tile's gate/up units; a gather or gate/up unit on the
- * units that read, one lap back, the ring rows it overwrites). The order makes every wait one on an earlier unit, so the launch always
- * completes; each wait is still bounded (2 s), after which MOK_ERR_TIMEOUT is recorded in
+ * units that read, one lap back, the ring rows it overwrites). The order makes every wait
+ * one on an earlier unit, so the launch always completes; each wait is still bounded (2 s),
+ * after which MOK_ERR_TIMEOUT is recorded in
  * the device status word and the launch returns early with y undefined. In MXFP8, x is
  * quantized along H once per token before that launch. Everything runs on `stream`. */
 mok_status mok_forward(const mok_config *cfg, const void *x, const mok_schedule *sched,

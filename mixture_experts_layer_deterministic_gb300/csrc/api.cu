@@ -45,17 +45,16 @@ bool f32_storage(const mok_config *c) { return (c->flags & MOK_FLAG_FP32_STORAGE
 size_t stored_bytes(const mok_config *c) { return f32_storage(c) ? 4 : 2; }
 
 // Which GEMMs run on SM pairs (the results are the same bit for bit). Unless the caller
-// forces one form, the BF16 down and dx GEMMs of the routed experts always do, and the
-// weight gradients and the gate/up GEMM when an expert averages at least PAIR_ROWS rows.
-// Measured on 4096 x 1024 experts, pairs against one SM: down 5-9% and dx 6-16% faster
-// from 160 rows per expert up; weight gradients 18-23% and gate/up 13% faster from 640 and
-// 1280 rows, but 2-16% and 9-30% slower at 320 rows and below. There the dW writes bound
-// the weight gradients, and gate/up units keep N <= 128 columns (two MMAs per step); the
-// pair's two pipelines must both finish a stage or a unit before it moves on, which costs
-// more than the operand bytes it saves. The same holds for GEMMs that add into their output
-// (the shared expert's down and dx: 19% slower on pairs): their epilogues wait on the
-// loads of the values they add to. The MXFP8 GEMMs run on one SM: their scale atoms are
-// cut per one-SM tile.
+// forces one form, the BF16 gate/up, down and dx GEMMs of the routed experts always do, the
+// shared expert's gate/up too, and the weight gradients when an expert averages at least
+// PAIR_ROWS rows. Measured on 4096 x 1024 experts, pairs against one SM: gate/up 6-16%, dx
+// 6-16% and down 2-9% faster from 160 rows per expert up (down once 4% slower at 1280);
+// weight gradients 18-23% faster from 640 rows, but 2-16% slower at 320 rows and below.
+// There the dW writes bound the kernel, and the pair's two pipelines must both finish a
+// unit before it moves on, which costs more than the operand bytes it saves. The same
+// holds for GEMMs that add into their output (the shared expert's down and dx: 19% slower
+// on pairs), whose epilogues wait on the loads of the values they add to. The MXFP8 GEMMs
+// run on one SM: their scale atoms are cut per one-SM tile.
 constexpr int64_t PAIR_ROWS = 512;
 bool gemm_pairs(const mok_config *c, bool mx, bool by_default) {
     if (mx || (c->flags & MOK_FLAG_ONE_SM_GEMMS) != 0) return false;
@@ -605,9 +604,12 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
         // a ring that holds every row: filled token by token (each x row read once), then
         // the two GEMMs over every tile
         const Ring ring{R, c->minibatch, 0};
+        // the gate/up GEMM on SM pairs takes tiles of up to 256 rows, the down GEMM (either
+        // form) tiles of up to 128: the list is rebuilt in place between the two
+        const bool up_pairs = gemm_pairs(c, mx, true);
         MOK_LAUNCH(KK_TILES, 1,
-                   launch_build_tiles(sch->offsets, c->E, 0, R, chunk, w.tiles, cap, status,
-                                      stream));
+                   launch_build_tiles(sch->offsets, c->E, 0, R, up_pairs ? PAIR_TILE_ROWS : chunk,
+                                      w.tiles, cap, status, stream));
         if (!mx)
             MOK_LAUNCH(KK_GATHER, 1,
                        launch_gather_tok_bf16((const uint16_t *)x, sch->inv, c->T, c->K, c->H,
@@ -633,10 +635,14 @@ mok_status mok_forward(const mok_config *c, const void *x, const mok_schedule *s
             MOK_LAUNCH(KK_GEMM_DOWN, 1,
                        launch_gemm_down_tc_mx(da, R, w.sf_w2, w.sf_h, stream));
         } else {
-            const bool up2 = gemm_pairs(c, mx, R / c->E >= PAIR_ROWS);
-            MOK_LAUNCH(KK_GEMM_UP, 1,
-                       up2 ? launch_gemm_up_pair_tc(ua, R, stream)
-                           : launch_gemm_up_tc(ua, R, stream));
+            if (up_pairs) {
+                MOK_LAUNCH(KK_GEMM_UP, 1, launch_gemm_up_pair_tc(ua, R, stream));
+                MOK_LAUNCH(KK_TILES, 1,
+                           launch_build_tiles(sch->offsets, c->E, 0, R, chunk, w.tiles, cap,
+                                              status, stream));
+            } else {
+                MOK_LAUNCH(KK_GEMM_UP, 1, launch_gemm_up_tc(ua, R, stream));
+            }
             MOK_LAUNCH(KK_GEMM_DOWN, 1,
                        gemm_pairs(c, mx, true) ? launch_gemm_down_pair_tc(da, R, stream)
                                                : launch_gemm_down_tc(da, R, stream));
@@ -738,7 +744,7 @@ mok_status backward_impl(const mok_config *c, const void *x, const mok_schedule 
         // the pair form's tiles hold up to 256 rows; the list is rebuilt in place (nothing
         // after this GEMM reads it)
         MOK_LAUNCH(KK_TILES, 1,
-                   launch_build_tiles(sch->offsets, E, 0, R, PAIR_DGRAD_TILE_ROWS, w.tiles,
+                   launch_build_tiles(sch->offsets, E, 0, R, PAIR_TILE_ROWS, w.tiles,
                                       w.tiles_cap, status, stream));
         MOK_LAUNCH(KK_GEMM_DGRAD, 1, launch_gemm_dgrad_pair_tc(dg, E, w.rpad_cap, stream));
     } else {
@@ -800,16 +806,24 @@ mok_status mok_shared_expert_forward(const mok_config *c, const void *x, const v
     carve_shared(c, ws, &w);
     // one expert owning every token, in token order: x itself is the ring (slot t = t)
     const Ring ring{c->T, c->minibatch, 0};
+    // gate/up on SM pairs over tiles of up to 256 rows, then the down GEMM over tiles of up
+    // to 128 (the list rebuilt in place)
+    const bool up_pairs = gemm_pairs(c, false, true);
     MOK_LAUNCH(KK_TILES, 2,
                first_error(launch_single_expert_offsets(w.offsets, c->T, stream),
-                           launch_build_tiles(w.offsets, 1, 0, c->T, gemm_tc_tile_rows(false),
+                           launch_build_tiles(w.offsets, 1, 0, c->T,
+                                              up_pairs ? PAIR_TILE_ROWS : gemm_tc_tile_rows(false),
                                               w.tiles, w.tiles_cap, status, stream)));
     GemmUpArgs ua{w.tiles, w.tiles_cap, x, nullptr, w13_s, nullptr, w.h, nullptr,
                   saved_preact_s, c->H, c->I, 1, false, ring, status};
     ua.preact_f32 = f32_storage(c);
     MOK_LAUNCH(KK_SHARED_UP, 1,
-               gemm_pairs(c, false, c->T >= PAIR_ROWS) ? launch_gemm_up_pair_tc(ua, c->T, stream)
-                                                       : launch_gemm_up_tc(ua, c->T, stream));
+               up_pairs ? launch_gemm_up_pair_tc(ua, c->T, stream)
+                        : launch_gemm_up_tc(ua, c->T, stream));
+    if (up_pairs)
+        MOK_LAUNCH(KK_TILES, 1,
+                   launch_build_tiles(w.offsets, 1, 0, c->T, gemm_tc_tile_rows(false), w.tiles,
+                                      w.tiles_cap, status, stream));
     GemmDownArgs da{w.tiles, w.tiles_cap, w.h, nullptr, w2_s, nullptr, nullptr, y,
                     c->H, c->I, 1, false, ring, status, true};
     da.out_f32 = f32_storage(c);
@@ -951,7 +965,7 @@ mok_status shared_backward_impl(const mok_config *c, const void *x, const void *
                                                        w.poff, 2 * I, w.sf_dA, stream));
         if (gemm_pairs(c, mx, false)) {  // dx adds into the routed part
             MOK_LAUNCH(KK_TILES, 1,
-                       launch_build_tiles(w.offsets, 1, 0, T, PAIR_DGRAD_TILE_ROWS, w.tiles,
+                       launch_build_tiles(w.offsets, 1, 0, T, PAIR_TILE_ROWS, w.tiles,
                                           w.tiles_cap, status, stream));
             MOK_LAUNCH(KK_SHARED_BWD, 1, launch_gemm_dgrad_pair_tc(dg, 1, w.tpad, stream));
         } else {

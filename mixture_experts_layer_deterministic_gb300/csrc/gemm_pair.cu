@@ -24,7 +24,8 @@
 //              of both CTAs
 //   warps 2-9  epilogue (both ranks): TMEM -> the policy's epilogue; each warp then arrives
 //              on rank 0's accumulator-free barrier
-// Two accumulator sets of 256 columns alternate between consecutive units. The clusters
+// Two accumulator sets of 256 columns alternate between consecutive units (a set holds
+// one accumulator of N <= 256 columns, or two of N <= 128 at columns 0 and 128). The clusters
 // take the units in a static stride; consecutive units share operand tiles, so the clusters
 // running at one time share them in L2.
 //
@@ -32,6 +33,11 @@
 //   WgradPair  A, B MN-major over an expert's padded rows -> dW (output rows on M)
 //   DgradPair  A = W13^T (MN-major), B = dA (K-major) in token tiles of <= 256 rows
 //              -> reverse-dispatch scatter to the dx slots (features on M)
+//   UpPair     A = 64 gate + 64 up rows of W13 per CTA (K-major), B = x ring rows in tiles
+//              of <= 256 -> SwiGLU, with gate and up values of a feature handed between
+//              two epilogue warps through shared memory
+//   DownPair   A = two 128-row blocks of W2 per CTA (K-major, two MMAs per K step), B = h
+//              ring rows in tiles of <= 128 -> push scatter to the slots
 //
 // Every wait is bounded (2 s); a CTA that gives up records MOK_ERR_TIMEOUT and leaves its
 // loops, and both CTAs meet at a cluster barrier before TMEM is freed.
@@ -50,6 +56,7 @@ struct PairSmem {
     uint64_t empty[PAIR_MAX_STAGES];  // each CTA: the MMAs that read the stage are done
     uint64_t tmem_full[2];            // each CTA: accumulator set b holds a finished unit
     uint64_t tmem_empty[2];           // rank 0: both CTAs' epilogues have drained set b
+    uint64_t xbar[4];                 // exchange between the two warps of a lane pair
     uint32_t tmem_base;
     int abort;
     int32_t col[EPI_WARPS][PAIR_TILE];  // per epilogue warp: one index per column of a unit
@@ -57,7 +64,7 @@ struct PairSmem {
 
 template <class P>
 __host__ __device__ constexpr int pair_smem() {
-    return P::STAGES * P::STAGE_BYTES + 1024 + (int)sizeof(PairSmem);
+    return P::STAGES * P::STAGE_BYTES + 1024 + (int)sizeof(PairSmem) + P::XCH_BYTES;
 }
 
 // One unit as one CTA of the pair loads and multiplies it: the policy's coordinates and
@@ -68,6 +75,18 @@ struct PairGeom {
     int nbox;
     int n_mma;            // N of each pair MMA (multiple of 16; of 128 for MN-major B)
     int k_steps;          // 16-element K steps; 0 leaves the accumulators unwritten
+};
+
+// What an epilogue warp gets besides its accumulator: a scratch of one index per column,
+// the CTA's exchange buffers and barriers (policies whose SwiGLU pairs lanes of two warps),
+// this warp's exchange phase, and the status / abort words of its bounded waits.
+struct PairEpi {
+    int32_t *col;
+    float *xch;
+    uint64_t *xbar;
+    uint32_t *xph;
+    int *status;
+    volatile int *abort;
 };
 
 // 32 accumulator columns from TMEM address c (this warp's lane quadrant), one round trip
@@ -94,6 +113,7 @@ MOK_DEV void tmem_ld32(uint32_t c, float (&v)[32]) {
 struct WgradPair {
     static constexpr bool A_MN = true, B_MN = true, TWO = false;
     static constexpr int A_BYTES = 2 * PAIR_BOX, STAGE_BYTES = 4 * PAIR_BOX, STAGES = 6;
+    static constexpr int XCH_BYTES = 0;
     const int32_t *counts, *poff;
     void *out;     // [E][N][M], fp32 if out_f32, else bf16
     bool out_f32;
@@ -134,7 +154,7 @@ struct WgradPair {
             tc::tma_load_2d_pair(st + A_BYTES + j * PAIR_BOX, tmB, fb, g.bx + 64 * j,
                                  g.by + k0);
     }
-    MOK_DEV void epilogue(int64_t u, uint32_t rank, uint32_t c, int32_t *, int q, int hw,
+    MOK_DEV bool epilogue(int64_t u, uint32_t rank, uint32_t c, const PairEpi &, int q, int hw,
                           int lane) const {
         int e, mb, nb;
         get(u, &e, &mb, &nb);
@@ -154,6 +174,7 @@ struct WgradPair {
                     st_val(out, o + (int64_t)j * M, any ? v[j] : 0.f, out_f32);
             }
         }
+        return true;
     }
 };
 
@@ -186,6 +207,7 @@ MOK_DEV void scatter32(void *outp, bool out_f32, bool accumulate, const int32_t 
 struct DgradPair {
     static constexpr bool A_MN = true, B_MN = false, TWO = false;
     static constexpr int A_BYTES = 2 * PAIR_BOX, STAGE_BYTES = 4 * PAIR_BOX, STAGES = 6;
+    static constexpr int XCH_BYTES = 0;
     TileUnits tu;
     int H, I;
     const int32_t *offsets, *poff, *perm;
@@ -219,8 +241,9 @@ struct DgradPair {
         tc::tma_load_2d_pair(st + PAIR_BOX, tmA, fb, g.ax + 64, g.ay + k0);
         tc::tma_load_2d_pair(st + A_BYTES, tmB, fb, k0, g.by);
     }
-    MOK_DEV void epilogue(int64_t u, uint32_t rank, uint32_t c, int32_t *fcol, int q, int hw,
+    MOK_DEV bool epilogue(int64_t u, uint32_t rank, uint32_t c, const PairEpi &pe, int q, int hw,
                           int lane) const {
+        int32_t *fcol = pe.col;
         int e, mb;
         int64_t r0, r1;
         tu.get(u, &e, &r0, &r1, &mb);
@@ -235,17 +258,30 @@ struct DgradPair {
             if (f < H) scatter32(dx_slots, out_f32, accumulate, fcol, n0, nr, H, f, v);
         }
         __syncwarp();
+        return true;
     }
 };
 
-// forward gate/up with SwiGLU (BF16): a[r][j] = sum_c W13[e][j][c] xring[r][c],
-// h[r][i] = silu(a[r][i]) a[r][I+i]; a unit is (tile of <= 128 rows, 256-feature block pb),
-// rank r taking features [pb*256 + 128r, +128) with their gate rows and up rows as A rows
-// 0-127 and 128-255: two MMAs per K step (gate, up), both halves of a feature on one lane
+// both warps of a lane pair arrive (all 64 threads), then wait for the other (bounded)
+MOK_DEV bool xsync(const PairEpi &pe, int pair) {
+    tc::mbar_arrive(&pe.xbar[pair]);
+    const bool ok = tc::wait_bounded(&pe.xbar[pair], *pe.xph, pe.status, pe.abort,
+                                     tc::WAIT_LIMIT_NS);
+    *pe.xph ^= 1u;
+    return ok;
+}
+
+// forward gate/up with SwiGLU (BF16) on token tiles of <= 256 rows: a unit is (tile,
+// 128-feature block fb), rank r taking features [fb*128 + 64r, +64) with their gate rows as
+// A rows 0-63 and their up rows as A rows 64-127: one MMA per K step, N up to 256. A
+// feature's gate value then sits on TMEM lane l of quadrant q < 2 and its up value on lane
+// l of quadrant q + 2, in two warps: per 32-column chunk each of the two hands the other
+// half of its columns through shared memory, and each computes SwiGLU for 16 columns.
 struct UpPair {
-    static constexpr bool A_MN = false, B_MN = false, TWO = true;
-    static constexpr int A_BYTES = 4 * PAIR_BOX, STAGE_BYTES = 5 * PAIR_BOX, STAGES = 5;
-    TileUnits tu;  // n_mblocks = I / 256
+    static constexpr bool A_MN = false, B_MN = false, TWO = false;
+    static constexpr int A_BYTES = 2 * PAIR_BOX, STAGE_BYTES = 4 * PAIR_BOX, STAGES = 6;
+    static constexpr int XCH_BYTES = 4 * 2 * 16 * 32 * 4;  // per lane pair: 2 x 16 x 32 fp32
+    TileUnits tu;   // n_mblocks = I / 128
     int H, I;
     Ring ring;
     void *hring;    // [rows][I] bf16
@@ -255,14 +291,14 @@ struct UpPair {
 
     MOK_DEV int64_t n_units() const { return tu.count(); }
     MOK_DEV PairGeom geom(int64_t u, uint32_t rank) const {
-        int e, pb;
+        int e, fb;
         int64_t r0, r1;
-        tu.get(u, &e, &r0, &r1, &pb);
+        tu.get(u, &e, &r0, &r1, &fb);
         PairGeom g;
         g.n_mma = (int)((r1 - r0 + 15) & ~15);
         g.ax = 0;
-        g.ay = 2 * pb + (int)rank;  // 128-feature block of the CTA
-        g.ay2 = e;
+        g.ay = e * 2 * I + fb * 128 + (int)rank * 64;  // gate rows of the CTA's features
+        g.ay2 = g.ay + I;                              // their up rows
         g.bx = 0;
         // a tile never straddles a lap of the ring: its rows are consecutive ring rows
         g.by = (int32_t)RingMap{ring.R, ring.MB, ring.n_slots}(r0) + (int)rank * (g.n_mma / 2);
@@ -270,46 +306,64 @@ struct UpPair {
         g.k_steps = H / 16;
         return g;
     }
-    MOK_DEV uint32_t tx(const PairGeom &) const { return A_BYTES + PAIR_BOX; }
-    // A: the CTA's gate block and up block (one 5D box); B: 64 K-major rows of the x ring,
-    // of which the MMA reads n_mma / 2
+    MOK_DEV uint32_t tx(const PairGeom &) const { return A_BYTES + 2 * PAIR_BOX; }
+    // A: two 64-row K-major boxes of W13 (gate, up); B: one 128-row K-major box of the x
+    // ring, of which the MMA reads n_mma / 2 rows
     MOK_DEV void load(uint8_t *st, uint32_t fb, const PairGeom &g, int k0,
                       const CUtensorMap *tmA, const CUtensorMap *tmB) const {
-        tc::tma_load_5d_pair(st, tmA, fb, k0, 0, g.ay, 0, g.ay2);
+        tc::tma_load_2d_pair(st, tmA, fb, k0, g.ay);
+        tc::tma_load_2d_pair(st + PAIR_BOX, tmA, fb, k0, g.ay2);
         tc::tma_load_2d_pair(st + A_BYTES, tmB, fb, k0, g.by);
     }
-    MOK_DEV void epilogue(int64_t u, uint32_t rank, uint32_t c, int32_t *, int q, int hw,
+    MOK_DEV bool epilogue(int64_t u, uint32_t rank, uint32_t c, const PairEpi &pe, int q, int hw,
                           int lane) const {
-        int e, pb;
+        int e, fb;
         int64_t r0, r1;
-        tu.get(u, &e, &r0, &r1, &pb);
+        tu.get(u, &e, &r0, &r1, &fb);
         const int nr = (int)(r1 - r0);
         const int n_mma = (nr + 15) & ~15;
         const int64_t hrow0 = RingMap{ring.R, ring.MB, ring.n_slots}(r0);
-        const int i = pb * 256 + (int)rank * 128 + q * 32 + lane;  // gate feature; up: I + i
-        if (pb * 256 + (int)rank * 128 >= I) return;  // past I when I % 256 == 128
-        for (int n0 = 16 * hw; n0 < n_mma; n0 += 32) {
-            float d0[16], d1[16];
-            tc::tmem_ld16(c + n0, d0);
-            tc::tmem_ld16(c + 128 + n0, d1);
-            tc::tmem_ld_wait();
+        const int i = fb * 128 + (int)rank * 64 + (q & 1) * 32 + lane;  // this lane's feature
+        const int pair = (q & 1) + 2 * hw;  // the two warps of a lane pair share hw
+        const bool gate_side = q < 2;
+        float *xg = pe.xch + pair * 1024;   // written by the gate side: its columns 16-31
+        float *xu = xg + 512;               // written by the up side: its columns 0-15
+        for (int n0 = 32 * hw; n0 < n_mma; n0 += 64) {
+            float v[32];
+            tmem_ld32(c + n0, v);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const int n = n0 + j;
+                if (gate_side)
+                    xg[j * 32 + lane] = v[16 + j];
+                else
+                    xu[j * 32 + lane] = v[j];
+            }
+            if (!xsync(pe, pair)) return false;
+            // the gate side finishes columns n0..n0+15, the up side n0+16..n0+31
+            float g[16], up[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                g[j] = gate_side ? v[j] : xg[j * 32 + lane];
+                up[j] = gate_side ? xu[j * 32 + lane] : v[16 + j];
+            }
+            if (!xsync(pe, pair)) return false;  // the buffers are free again
+            const int nb = gate_side ? n0 : n0 + 16;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int n = nb + j;
                 if (n < nr) {
                     const int64_t r = r0 + n;
                     if (preact != nullptr) {
                         if (preact_f32)
-                            static_cast<float2 *>(preact)[r * I + i] = make_float2(d0[j], d1[j]);
+                            static_cast<float2 *>(preact)[r * I + i] = make_float2(g[j], up[j]);
                         else
-                            static_cast<uint32_t *>(preact)[r * I + i] =
-                                pack_bf16x2(d0[j], d1[j]);
+                            static_cast<uint32_t *>(preact)[r * I + i] = pack_bf16x2(g[j], up[j]);
                     }
-                    ((uint16_t *)hring)[(hrow0 + n) * I + i] =
-                        f32_to_bf16(silu_f(d0[j]) * d1[j]);
+                    ((uint16_t *)hring)[(hrow0 + n) * I + i] = f32_to_bf16(silu_f(g[j]) * up[j]);
                 }
             }
         }
+        return true;
     }
 };
 
@@ -320,6 +374,7 @@ struct UpPair {
 struct DownPair {
     static constexpr bool A_MN = false, B_MN = false, TWO = true;
     static constexpr int A_BYTES = 4 * PAIR_BOX, STAGE_BYTES = 5 * PAIR_BOX, STAGES = 5;
+    static constexpr int XCH_BYTES = 0;
     TileUnits tu;  // n_mblocks = ceil(H / 512)
     int H, I;
     Ring ring;
@@ -355,8 +410,9 @@ struct DownPair {
         tc::tma_load_2d_pair(st + 2 * PAIR_BOX, tmA, fb, k0, g.ay2);
         tc::tma_load_2d_pair(st + A_BYTES, tmB, fb, k0, g.by);
     }
-    MOK_DEV void epilogue(int64_t u, uint32_t rank, uint32_t c, int32_t *fcol, int q, int hw,
+    MOK_DEV bool epilogue(int64_t u, uint32_t rank, uint32_t c, const PairEpi &pe, int q, int hw,
                           int lane) const {
+        int32_t *fcol = pe.col;
         int e, pb;
         int64_t r0, r1;
         tu.get(u, &e, &r0, &r1, &pb);
@@ -376,6 +432,7 @@ struct DownPair {
             if (f < H) scatter32(slots, out_f32, accumulate, fcol, n0, nr, H, f, v);
         }
         __syncwarp();
+        return true;
     }
 };
 
@@ -414,6 +471,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::mbar_init(&sm->tmem_full[b], 1);
             tc::mbar_init(&sm->tmem_empty[b], 2 * EPI_WARPS);
         }
+        for (int j = 0; j < 4; ++j) tc::mbar_init(&sm->xbar[j], 64);
         sm->abort = 0;
         tc::fence_mbar_init();
         tc::prefetch_tmap(&tmA);
@@ -530,7 +588,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int hw = (warp - 2) >> 2;    // which alternate 32-column chunks it takes
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const uint32_t empty0 = tc::cluster_addr(&sm->tmem_empty[0], 0);
-        int32_t *col = sm->col[warp - 2];
+        uint32_t xph = 0;
+        const PairEpi pe{sm->col[warp - 2], (float *)((uint8_t *)sm + sizeof(PairSmem)), sm->xbar,
+                         &xph, p.status, abort};
         int64_t a = 0;
         for (int64_t u = cid; u < n_units; u += ncl, ++a) {
             const int ab = (int)(a & 1);
@@ -538,8 +598,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 break;
             tc::tc_fence_after();
             // this quadrant's lanes of the unit's accumulator set
-            p.epilogue(u, rank, tmem + lane_base + (uint32_t)ab * PAIR_SET_COLS, col, q, hw,
-                       lane);
+            if (!p.epilogue(u, rank, tmem + lane_base + (uint32_t)ab * PAIR_SET_COLS, pe, q, hw,
+                            lane))
+                break;
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster(empty0 + (uint32_t)ab * 8u);
@@ -652,18 +713,18 @@ cudaError_t launch_wgrad_pair_tc(const int32_t *counts, const int32_t *poff, con
     return launch_pair(ma, mb, p, (int64_t)E * nmb * nnb, s);
 }
 
-// BF16 forward gate/up over tiles of <= 128 rows
+// BF16 forward gate/up over tiles of <= PAIR_TILE_ROWS rows
 cudaError_t launch_gemm_up_pair_tc(const GemmUpArgs &a, int64_t ring_rows, cudaStream_t s) {
     if (a.mxfp8) return cudaErrorInvalidValue;
     cudaError_t e = init_host();
     if (e != cudaSuccess) return e;
-    CUtensorMap ma, mb;  // A: W13 gate/up block pairs; B: the x ring, 64-row boxes
-    if ((e = make_map_w13_pairs(&ma, a.w13, a.E, a.I, a.H, false)) != cudaSuccess) return e;
-    if ((e = make_map_bf16(&mb, a.xring, ring_rows, a.H, 64)) != cudaSuccess) return e;
-    const int npb = (a.I + 255) / 256;
-    UpPair p{TileUnits{a.tiles, a.tiles_cap, npb}, a.H, a.I, a.ring, a.hring, a.preact,
-             a.preact_f32, a.status};
-    return launch_pair(ma, mb, p, a.tiles_cap * npb, s);
+    CUtensorMap ma, mb;  // A: W13 as [E*2I][H], 64-row boxes; B: the x ring, 128-row boxes
+    if ((e = make_map_bf16(&ma, a.w13, (int64_t)a.E * 2 * a.I, a.H, 64)) != cudaSuccess)
+        return e;
+    if ((e = make_map_bf16(&mb, a.xring, ring_rows, a.H, KBOX_ROWS)) != cudaSuccess) return e;
+    UpPair p{TileUnits{a.tiles, a.tiles_cap, a.I / 128}, a.H, a.I, a.ring, a.hring, a.preact,
+              a.preact_f32, a.status};
+    return launch_pair(ma, mb, p, a.tiles_cap * (a.I / 128), s);
 }
 
 // BF16 forward down with the push scatter over tiles of <= 128 rows
@@ -680,7 +741,7 @@ cudaError_t launch_gemm_down_pair_tc(const GemmDownArgs &a, int64_t ring_rows, c
     return launch_pair(ma, mb, p, a.tiles_cap * npb, s);
 }
 
-// BF16 dgrad over a tile list of <= 256-row tiles (PAIR_DGRAD_TILE_ROWS)
+// BF16 dgrad over tiles of <= PAIR_TILE_ROWS rows
 cudaError_t launch_gemm_dgrad_pair_tc(const GemmDgradArgs &a, int E, int64_t rpad_cap,
                                       cudaStream_t s) {
     if (a.mxfp8) return cudaErrorInvalidValue;

@@ -272,14 +272,12 @@ struct GemmDgradArgs {
 cudaError_t launch_gemm_g_tc(const GemmGArgs &a, int E, int64_t rpad_cap, cudaStream_t s);
 cudaError_t launch_gemm_dgrad_tc(const GemmDgradArgs &a, int E, int64_t rpad_cap,
                                  cudaStream_t s);
-// BF16 forward gate/up and down on pairs of SMs sharing their operand tiles (tcgen05
-// cta_group::2), bit for bit equal to launch_gemm_up_tc / launch_gemm_down_tc, over the
-// same tiles of <= gemm_tc_tile_rows(false) rows
+// BF16 expert GEMMs on pairs of SMs sharing their operand tiles (tcgen05 cta_group::2),
+// bit for bit equal to the one-SM launchers: gate/up and dgrad over tiles of <=
+// PAIR_TILE_ROWS rows, down over tiles of <= gemm_tc_tile_rows(false) rows
+constexpr int PAIR_TILE_ROWS = 256;
 cudaError_t launch_gemm_up_pair_tc(const GemmUpArgs &a, int64_t ring_rows, cudaStream_t s);
 cudaError_t launch_gemm_down_pair_tc(const GemmDownArgs &a, int64_t ring_rows, cudaStream_t s);
-// BF16 dgrad on pairs of SMs sharing their operand tiles (tcgen05 cta_group::2), bit for
-// bit equal to launch_gemm_dgrad_tc; a.tiles holds tiles of <= PAIR_DGRAD_TILE_ROWS rows
-constexpr int PAIR_DGRAD_TILE_ROWS = 256;
 cudaError_t launch_gemm_dgrad_pair_tc(const GemmDgradArgs &a, int E, int64_t rpad_cap,
                                       cudaStream_t s);
 // out [E][N][M] = per expert e, sum over its padded rows p of A[p][m] * B[p][n]

@@ -12,13 +12,14 @@
 // M rows against all N columns. Per 64-element K block a SM loads 128 A rows and N/2 B rows
 // for 128 x N outputs, where the one-SM engine loads 256 A rows and N B rows (N <= 128) for
 // 256 x N: at N = 256 the operand feed per FLOP falls by a third, the weight tiles' by half.
+// (A policy with two MMAs per K step loads 256 A rows for 256 x N, N <= 128.)
 // Each output element is the same fixed-order fp32 dot product as in the one-SM engine (K
 // in 16-element steps from the first), so the results are the same bit for bit.
 //
 // Per CTA, 320 threads:
-//   warp 0     TMA producer (both ranks): its own A half (two 64-wide MN-major boxes) and B
-//              half into a 6-stage ring; the copies of both ranks complete on rank 0's full
-//              barrier of the stage, whose expected bytes rank 0 sets
+//   warp 0     TMA producer (both ranks): its own halves of the unit's operands (boxes per
+//              policy) into a ring of 5-6 stages; the copies of both ranks complete on rank
+//              0's full barrier of the stage, whose expected bytes rank 0 sets
 //   warp 1     TMEM owner (both ranks: the pair allocates together); on rank 0 the MMA
 //              issuer, whose commits arrive on the stage-free and accumulator-full barriers
 //              of both CTAs
@@ -105,8 +106,9 @@ MOK_DEV void tmem_ld32(uint32_t c, float (&v)[32]) {
 // Policy interface: STAGES x STAGE_BYTES of operand ring, the A region (A_BYTES) first in
 // each stage; A_MN / B_MN operand majors; TWO: two MMAs per K step, on A rows 0-127 and
 // 128-255 of the A region into accumulator columns 0 and 128 of a set (N <= 128), else one
-// on A rows 0-127 into columns 0 (N <= 256); tx(g): bytes one CTA loads per stage;
-// load(..): its copies of one stage; epilogue(..): TMEM -> outputs.
+// on A rows 0-127 into columns 0 (N <= 256); XCH_BYTES: shared memory for the epilogue's
+// lane exchange; tx(g): bytes one CTA loads per stage; load(..): its copies of one stage;
+// epilogue(..): TMEM -> outputs, false when a bounded wait gave up.
 
 // weight gradient: out[e][n][m] = sum over the expert's padded rows p of A[p][m] B[p][n];
 // a unit is (expert, 256-column block nb, 256-row block mb)

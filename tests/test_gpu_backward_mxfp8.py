@@ -30,10 +30,10 @@ def test_transposed_weight_quantization_is_bit_exact():
     np.testing.assert_array_equal(s.cpu().numpy(), so)
 
 
-def gpu_backward_mx(dims, x, logits, w13, w2, dy, MB, reps=1):
+def gpu_backward_mx(dims, x, logits, w13, w2, dy, MB, reps=1, flags=0):
     import torch
     T, H, I, E, K = dims
-    L = MoELayer(T, H, I, E, K, MB, 0, B.MOK_MXFP8, backward=True)
+    L = MoELayer(T, H, I, E, K, MB, 0, B.MOK_MXFP8, backward=True, flags=flags)
     xd, dyd, w13d, w2d = to_dev(x), to_dev(dy), to_dev(w13), to_dev(w2)
     q13, s13 = quantize_mxfp8(w13d)
     q2, s2 = quantize_mxfp8(w2d)
@@ -104,6 +104,17 @@ def test_ragged_and_empty_experts(dims, skew):
     if skew:
         assert len(np.unique(g["idx"])) < dims[3]  # some experts get no rows
     check_all(outs, g, L, pre, x, w13, w2, dy)
+
+
+@pytest.mark.parametrize("dims", [(600, 256, 256, 16, 4), (2048, 256, 128, 4, 2)])
+def test_weight_gradients_on_sm_pairs(dims):
+    """The MXFP8 backward's weight gradients (bf16 operands) on SM pairs equal those on one
+    SM bit for bit; the second shape (1024 rows per expert) takes the pairs by default."""
+    x, lg, w13, w2, dy = small_case(*dims, seed=dims[0] + 3)
+    a = gpu_backward_mx(dims, x, lg, w13, w2, dy, 100, flags=B.MOK_FLAG_SM_PAIR_GEMMS)[0]
+    b = gpu_backward_mx(dims, x, lg, w13, w2, dy, 100, flags=B.MOK_FLAG_ONE_SM_GEMMS)[0]
+    for k in a[0]:
+        assert same_bits(a[0][k], b[0][k]), k
 
 
 def test_full_size_sampled():

@@ -135,3 +135,35 @@ def check_expert(g, st, x, w13, w2, dy, mx, e, mxw=None, tag=""):
     _, d13o, d2o, _, _, s13o, s2o = run()
     check_tol("bwd dW13 e2e" + tag, g13, d13o[0], s13o[0], tol, max_slack_rms=0.6)
     check_tol("bwd dW2 e2e" + tag, g2, d2o[0], s2o[0], tol, max_slack_rms=0.6)
+
+
+def check_expert_features(g, st, x, w13, w2, dy, e, feats, tag=""):
+    """dW13[e] rows (gate and up) and dW2[e] columns of the features `feats` (BF16). A
+    feature's weight gradients depend only on its own gate, up and W2 weights: the oracle
+    runs the expert restricted to those features, a SwiGLU FFN of len(feats) features, so a
+    hot expert's thousands of rows stay cheap. From the GPU's own A, dA and w*h, then end to
+    end."""
+    K, I = g["K"], w2.shape[2]
+    idx, w = g["idx"], g["w"]
+    feats = np.asarray(feats, np.int64)
+    cols = np.concatenate([feats, I + feats])          # gate rows, then up rows
+    r0, r1 = int(st["offsets"][e]), int(st["offsets"][e + 1])
+    f = st["perm"][r0:r1]
+    t_e, k_e = f // K, f % K
+    g13 = host(g["dw13"][e])[cols]
+    g2 = host(g["dw2"][e])[:, feats]
+    if len(f) == 0:
+        assert np.all(g13 == 0) and np.all(g2 == 0)
+        return
+    run = lambda **kw: oracle.backward(  # noqa: E731
+        oracle.bf16_to_f64(x[t_e]), np.zeros((len(f), 1), np.int32), w[t_e, k_e][:, None],
+        w13[[e]][:, cols], w2[[e]][:, :, feats], oracle.bf16_to_f64(dy[t_e]),
+        mode=oracle.BF16, store=oracle.STORE_BF16, with_slack=True, **kw)
+    gr = _rows_of(st, np.arange(r0, r1))
+    _, d13, d2, _, _, s13, s2 = run(given={"a_in": gr["a"][:, cols], "da_in": gr["da"][:, cols],
+                                           "sh_in": gr["sh"][:, feats]})
+    check_exact("bwd dW13 | gpu dA" + tag, g13, d13[0], s13[0], max_flagged=0.35)
+    check_exact("bwd dW2 | gpu w*h" + tag, g2, d2[0], s2[0], max_flagged=0.35)
+    _, d13o, d2o, _, _, s13o, s2o = run()
+    check_tol("bwd dW13 e2e" + tag, g13, d13o[0], s13o[0], TOL_BF16, max_slack_rms=0.6)
+    check_tol("bwd dW2 e2e" + tag, g2, d2o[0], s2o[0], TOL_BF16, max_slack_rms=0.6)

@@ -914,3 +914,31 @@ def test_router_gradient_slack_covers_the_saved_a_decisions():
         assert np.all(dld <= sdl * (1 + 1e-9) + 1e-12 * np.abs(dl).max())
         moved += int((d > 1e-12 * np.abs(dtk)).sum())
     assert moved > 0
+
+
+def test_backward_weight_gradients_restrict_to_features():
+    """A feature's dW13 rows (gate, up) and dW2 column depend only on its own weights: the
+    oracle's expert restricted to a feature subset (its gate and up rows of W13, its W2
+    columns) gives the full expert's rows and columns bit for bit, slack included. The
+    full-size GPU check of hot experts' weight gradients rests on this."""
+    r = np.random.default_rng(1)
+    n, H, I = 300, 256, 128
+    x = oracle.bf16_to_f64(f32_to_bf16_bits(r.standard_normal((n, H)).astype(np.float32)))
+    dy = oracle.bf16_to_f64(f32_to_bf16_bits(r.standard_normal((n, H)).astype(np.float32)))
+    w13 = f32_to_bf16_bits((r.standard_normal((1, 2 * I, H)) / 16).astype(np.float32))
+    w2 = f32_to_bf16_bits((r.standard_normal((1, H, I)) / 16).astype(np.float32))
+    w = r.random((n, 1))
+    one = np.zeros((n, 1), np.int32)
+    run = lambda a, b: oracle.backward(x, one, w, a, b, dy, mode=oracle.BF16,  # noqa: E731
+                                       store=oracle.STORE_BF16, with_slack=True)
+    full = run(w13, w2)
+    feats = np.sort(r.choice(I, 16, replace=False))
+    cols = np.concatenate([feats, I + feats])
+    sub = run(w13[:, cols], w2[:, :, feats])
+    assert np.array_equal(full[1][0][cols], sub[1][0])           # dW13 rows
+    assert np.array_equal(full[2][0][:, feats], sub[2][0])       # dW2 columns
+    assert np.array_equal(full[5][0][cols], sub[5][0])           # their slack
+    assert np.array_equal(full[6][0][:, feats], sub[6][0])
+    # and not trivially: another subset's rows differ
+    other = np.setdiff1d(np.arange(I), feats)[:16]
+    assert not np.array_equal(full[1][0][other], sub[1][0])

@@ -356,6 +356,11 @@ void oracle_mxfp8_qdq_slack(int64_t n, const double *v, const double *err, doubl
 /* A value v that a kernel computes to within err (its fp32 arithmetic) and that earlier
  * decisions may move by up to up, rounded to bf16: returns the rounding and sets *slack to
  * the distance within which a correct result lies from it. */
+double oracle_dot_rel_rows(int64_t n)
+{
+    return n > 2048 ? ORACLE_DOT_REL * sqrt((double)n / 2048.0) : ORACLE_DOT_REL;
+}
+
 static double round_bf16_with_slack(double v, double err, double up, double *slack)
 {
     *slack = up + oracle_bf16_slack(v, err + up);
@@ -791,9 +796,11 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
             double *U2 = (double *)calloc((size_t)n2, sizeof(double));
             memset(DW13, 0, sizeof(double) * (size_t)n13);
             memset(DW2, 0, sizeof(double) * (size_t)n2);
+            int64_t ne = 0; /* the expert's rows: the length of its weight-gradient sums */
             for (int64_t f = 0; f < R; ++f) {
                 if (idx[f] != e)
                     continue;
+                ++ne;
                 const int64_t t = f / K;
                 const double *xt = x + t * (int64_t)H;
                 const double *dyt = dy + t * (int64_t)H;
@@ -816,17 +823,18 @@ void oracle_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, cons
             }
             double *S13 = sdw13 ? sdw13 + (int64_t)e * n13 : NULL;
             double *S2 = sdw2 ? sdw2 + (int64_t)e * n2 : NULL;
+            const double rel = oracle_dot_rel_rows(ne);
             for (int64_t o = 0; o < n13; ++o) {
                 double sl = U13[o];
                 if (sto) /* dW = bf16 of the sum over the expert's rows */
-                    DW13[o] = round_bf16_with_slack(DW13[o], ORACLE_DOT_REL * M13[o], U13[o], &sl);
+                    DW13[o] = round_bf16_with_slack(DW13[o], rel * M13[o], U13[o], &sl);
                 if (S13)
                     S13[o] = sl;
             }
             for (int64_t o = 0; o < n2; ++o) {
                 double sl = U2[o];
                 if (sto)
-                    DW2[o] = round_bf16_with_slack(DW2[o], ORACLE_DOT_REL * M2[o], U2[o], &sl);
+                    DW2[o] = round_bf16_with_slack(DW2[o], rel * M2[o], U2[o], &sl);
                 if (S2)
                     S2[o] = sl;
             }

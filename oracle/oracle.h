@@ -85,6 +85,16 @@ double oracle_round_bf16(double v);
 #define ORACLE_SLACK_REL 9.5367431640625e-07 /* 2^-20 */
 #define ORACLE_DOT_REL 1.9073486328125e-06   /* 2^-19 */
 #define ORACLE_SUM_ULP 5.9604644775390625e-08 /* 2^-24: fp32 unit roundoff */
+
+/* The weight gradients are dot products over an expert's routed rows, whose number n runs
+ * from 0 to T, and a dot product's fp32 error grows with its length. Measured on GB300
+ * (dW13 of the experts of one Zipf-routed workload, 64 x 4096 outputs each, against the
+ * exact sums of the GPU's own bf16 operands), the largest |fp32 result - exact| / sum|terms|
+ * was 2^-21.3 at n = 318, 2^-20.0 at 1897, 2^-19.2 at 3975, 2^-19.1 at 8829, 2^-18.6 at
+ * 16218 and 2^-18.0 at 34469 and 65535: growth of about sqrt(n), as for the accumulation
+ * of random-sign terms. The oracle takes ORACLE_DOT_REL * max(1, sqrt(n / 2048)) for a
+ * weight gradient over n rows, at least 1.6x above every value seen. */
+double oracle_dot_rel_rows(int64_t n);
 double oracle_bf16_slack(double v, double err);
 
 /* MXFP8 quantize-dequantize of n values (n a multiple of 32) in 32-element blocks, each

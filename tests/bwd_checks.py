@@ -162,8 +162,12 @@ def check_expert_features(g, st, x, w13, w2, dy, e, feats, tag=""):
     gr = _rows_of(st, np.arange(r0, r1))
     _, d13, d2, _, _, s13, s2 = run(given={"a_in": gr["a"][:, cols], "da_in": gr["da"][:, cols],
                                            "sh_in": gr["sh"][:, feats]})
-    check_exact("bwd dW13 | gpu dA" + tag, g13, d13[0], s13[0], max_flagged=0.35)
-    check_exact("bwd dW2 | gpu w*h" + tag, g2, d2[0], s2[0], max_flagged=0.35)
+    # the oracle's error window of a sum over n rows grows as sqrt(n / 2048) beyond 2048 rows
+    # (oracle_dot_rel_rows), and with it the share of roundings it cannot decide: at 65535
+    # rows the measured fp32 error reaches about a quarter of a bf16 step
+    cap = 0.35 if len(f) <= 2048 else min(0.75, 0.35 * np.sqrt(len(f) / 2048))
+    check_exact("bwd dW13 | gpu dA" + tag, g13, d13[0], s13[0], max_flagged=cap)
+    check_exact("bwd dW2 | gpu w*h" + tag, g2, d2[0], s2[0], max_flagged=cap)
     _, d13o, d2o, _, _, s13o, s2o = run()
     check_tol("bwd dW13 e2e" + tag, g13, d13o[0], s13o[0], TOL_BF16, max_slack_rms=0.6)
     check_tol("bwd dW2 e2e" + tag, g2, d2o[0], s2o[0], TOL_BF16, max_slack_rms=0.6)

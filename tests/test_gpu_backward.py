@@ -187,26 +187,28 @@ def test_full_size_bwd():
               experts=experts, tag=" full")
 
 
-def test_full_size_imbalanced_bwd():
-    """The Zipf-routed 64-expert workload's backward (8192 tokens, 1280 rows per expert on
-    average, the hottest experts taking every token, some none): its dx and weight
-    gradients run on SM pairs by default. Token-local outputs on 64 sampled tokens; the
-    weight gradients of the hottest expert, a mid-sized one and an empty one on 32 sampled
-    features each (a feature's dW13 rows and dW2 column are the oracle's expert restricted
-    to that feature)."""
-    cfg = CONFIGS["ring_bf16_e64"].with_(passes="bwd", ring_capacity=0)
+@pytest.mark.parametrize("name", ["ring_bf16_e64", "imbalanced_bf16"])
+def test_full_size_imbalanced_bwd(name):
+    """The backward of the Zipf-routed workloads (8192 tokens over 64 experts; 65536 over
+    512): 1280 rows per expert on average, the hottest experts taking every token, some
+    none; their dx and weight gradients run on SM pairs by default. Token-local outputs on
+    64 sampled tokens; the weight gradients of the hottest expert, a mid-sized one and an
+    empty one on 32 sampled features each (a feature's dW13 rows and dW2 column are the
+    oracle's expert restricted to that feature)."""
+    cfg = CONFIGS[name].with_(passes="bwd", ring_capacity=0)
     d = inputs(cfg)
     dims = (cfg.T, cfg.H, cfg.I, cfg.E, cfg.K)
     outs, g, L, wsi = gpu_backward(dims, d["x"], d["logits"], d["w13"], d["w2"], d["dy"],
                                    cfg.minibatch)
     counts = np.bincount(g["idx"].reshape(-1), minlength=cfg.E)
-    assert counts.max() == cfg.T and counts.min() == 0, counts  # the skew this test wants
+    assert counts.max() >= cfg.T // 2 and counts.min() == 0, counts  # the skew this test wants
     ws, which, pre = wsi
     st = gpu_state(L, ws, which, pre)
     gg = dict(g, **outs[0])
     check_tokens(gg, st, d["x"], d["w13"], d["w2"], d["dy"], False,
                  sample_tokens(cfg.T, 64, seed=cfg.seed), tag=" zipf")
-    mid = int(np.argsort(counts)[cfg.E // 2])
+    nz = np.flatnonzero(counts > 0)
+    mid = int(nz[np.argsort(counts[nz], kind="stable")[len(nz) // 2]])
     r = np.random.default_rng(8)
     for e in (int(np.argmax(counts)), mid, int(np.argmin(counts))):
         feats = np.sort(r.choice(cfg.I, 32, replace=False))

@@ -942,3 +942,30 @@ def test_backward_weight_gradients_restrict_to_features():
     # and not trivially: another subset's rows differ
     other = np.setdiff1d(np.arange(I), feats)[:16]
     assert not np.array_equal(full[1][0][other], sub[1][0])
+
+
+def test_weight_gradient_window_grows_with_the_expert_rows():
+    """A weight gradient over n rows may round either way when its exact value lies within
+    2^-19 max(1, sqrt(n / 2048)) sum|terms| (+ 2^-20 of the value) of a rounding midpoint:
+    the tensor cores' fp32 error grows with the length of the sum (measured on GB300 up to
+    65535 rows). One dW13 element is built to lie 0.0029296875 above the midpoint
+    1.00390625 of the bf16 values 1 and 1.0078125, with sum|terms| = 1199.0068 from 1200
+    nonzero rows and the rest zero: over 2048 rows the window is 0.00229 and the rounding is
+    certain (slack 0); over 8192 rows (the same nonzero rows) it is 0.00457 and the element
+    is flagged with the slack of one bf16 step."""
+    H, I = 8, 2
+    target = 1.0 + 0.0068359375
+    out = {}
+    for n in (2048, 8192):
+        da = np.zeros((n, 2 * I))
+        da[:1198:2, 0], da[1:1198:2, 0] = 1.0, -1.0        # sum 0, sum|.| 1198
+        da[1198, 0], da[1199, 0] = 1.0, 0.0068359375       # both exact in bf16
+        x = np.ones((n, H))
+        _, d13, _, _, _, s13, _ = oracle.backward(
+            x, np.zeros((n, 1), np.int32), np.ones((n, 1)), np.zeros((1, 2 * I, H)),
+            np.zeros((1, H, I)), np.zeros((n, H)), mode=oracle.BF16, store=oracle.STORE_BF16,
+            with_slack=True, given={"da_in": da, "sh_in": np.zeros((n, I))})
+        assert np.all(d13[0, 0] == oracle.round_bf16(target)), d13[0, 0]  # 1.0078125
+        out[n] = s13[0, 0]
+    assert np.all(out[2048] == 0.0), out[2048]
+    assert np.all(out[8192] == 2.0 ** -7), out[8192]

@@ -53,6 +53,8 @@ def lib():
         L.oracle_bf16_slack.restype = ctypes.c_double
         L.oracle_round_bf16.argtypes = [ctypes.c_double]
         L.oracle_round_bf16.restype = ctypes.c_double
+        L.oracle_dot_rel_rows.argtypes = [i64]
+        L.oracle_dot_rel_rows.restype = ctypes.c_double
         L.oracle_router_grad.argtypes = [i64, i32, i32, p, p, p, p]
         L.oracle_router_grad_slack.argtypes = [i64, i32, i32, p, p, p, p]
         _lib = L
@@ -212,6 +214,12 @@ def mxfp8_qdq_slack(v, err):
 
 def round_bf16(v: float) -> float:
     return float(lib().oracle_round_bf16(float(v)))
+
+
+def dot_rel_rows(n: int) -> float:
+    """The oracle's fp32 error bound, relative to sum|terms|, of a weight gradient summed
+    over n rows (oracle_dot_rel_rows)."""
+    return float(lib().oracle_dot_rel_rows(int(n)))
 
 
 def _weights(w):

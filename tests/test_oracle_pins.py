@@ -955,17 +955,24 @@ def test_weight_gradient_window_grows_with_the_expert_rows():
     is flagged with the slack of one bf16 step."""
     H, I = 8, 2
     target = 1.0 + 0.0068359375
+    col = np.zeros(8192)
+    col[:1198:2], col[1:1198:2] = 1.0, -1.0                # sum 0, sum|.| 1198
+    col[1198], col[1199] = 1.0, 0.0068359375               # both exact in bf16
     out = {}
     for n in (2048, 8192):
+        # dW13[0][c] = sum_r dA[r][0] x[r][c] with x = 1; dW2[c][0] = sum_r dy[r][c] (w*h)[r][0]
+        # with dy = 1: both equal the sum of `col` over the first n rows
         da = np.zeros((n, 2 * I))
-        da[:1198:2, 0], da[1:1198:2, 0] = 1.0, -1.0        # sum 0, sum|.| 1198
-        da[1198, 0], da[1199, 0] = 1.0, 0.0068359375       # both exact in bf16
-        x = np.ones((n, H))
-        _, d13, _, _, _, s13, _ = oracle.backward(
-            x, np.zeros((n, 1), np.int32), np.ones((n, 1)), np.zeros((1, 2 * I, H)),
-            np.zeros((1, H, I)), np.zeros((n, H)), mode=oracle.BF16, store=oracle.STORE_BF16,
-            with_slack=True, given={"da_in": da, "sh_in": np.zeros((n, I))})
+        sh = np.zeros((n, I))
+        da[:, 0] = sh[:, 0] = col[:n]
+        _, d13, d2, _, _, s13, s2 = oracle.backward(
+            np.ones((n, H)), np.zeros((n, 1), np.int32), np.ones((n, 1)),
+            np.zeros((1, 2 * I, H)), np.zeros((1, H, I)), np.ones((n, H)), mode=oracle.BF16,
+            store=oracle.STORE_BF16, with_slack=True, given={"da_in": da, "sh_in": sh})
         assert np.all(d13[0, 0] == oracle.round_bf16(target)), d13[0, 0]  # 1.0078125
-        out[n] = s13[0, 0]
-    assert np.all(out[2048] == 0.0), out[2048]
-    assert np.all(out[8192] == 2.0 ** -7), out[8192]
+        assert np.all(d2[0][:, 0] == oracle.round_bf16(target)), d2[0][:, 0]
+        out[n] = (s13[0, 0], s2[0][:, 0])
+    for s in out[2048]:
+        assert np.all(s == 0.0), s
+    for s in out[8192]:
+        assert np.all(s == 2.0 ** -7), s

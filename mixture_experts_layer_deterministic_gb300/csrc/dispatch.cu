@@ -68,7 +68,8 @@ MOK_DEV uint32_t quant_block32_regs(const uint16_t *__restrict__ src, uint32_t (
     const uint32_t *w = reinterpret_cast<const uint32_t *>(v);
     float amax = 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+    for (int j = 0; j < 16; ++j)
+        amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
     const uint32_t sb = mx_scale_byte(amax);
     const float inv = mx_inv_scale(sb);
 #pragma unroll
@@ -88,7 +89,8 @@ MOK_DEV void quant_block32(const uint16_t *__restrict__ src, uint8_t *__restrict
     const uint32_t *w = reinterpret_cast<const uint32_t *>(v);
     float amax = 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+    for (int j = 0; j < 16; ++j)
+        amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
     const uint32_t sb = mx_scale_byte(amax);
     const float inv = mx_inv_scale(sb);
     uint32_t out[8];
